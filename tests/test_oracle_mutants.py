@@ -1,0 +1,52 @@
+"""Each planted oracle mistake is caught by at least one pin.
+
+The mutants are the tinyllm page's pitfall list where it applies to a two-pass
+oracle (s03 logical block index as block id, s04 KV-head offset dropped, s05
+round-robin GQA, s06 a window of w + 1, s07 query at n instead of n - 1, s08 V
+read from the K pool, s13 empty context accepted, s14 max_blocks trusted, s15
+block ids trusted) and further plausible slips in the scatter, gather, score,
+split-KV reduction and merge arithmetic.
+"""
+import pytest
+
+import oracle
+from tests import oracle_pins as P
+
+KILLERS = {
+    3: ["hand_example", "brute_force", "block_permutation"],
+    4: ["brute_force"],
+    5: ["brute_force"],
+    6: ["brute_force"],
+    7: ["hand_example", "brute_force"],
+    8: ["hand_example", "closed_forms"],
+    13: ["validation"],
+    14: ["validation"],
+    15: ["validation"],
+    20: ["hand_example_via_cache", "scatter_gather_roundtrip"],
+    21: ["hand_example_via_cache", "scatter_gather_roundtrip"],
+    22: ["scatter_gather_roundtrip"],
+    30: ["brute_force"],
+    31: ["brute_force"],
+    32: ["hand_example", "closed_forms"],
+    40: ["splitkv_masked_partition"],
+    41: ["splitkv_all_masked"],
+    42: ["splitkv_matches_full"],
+    50: ["merge_edge_cases"],
+    51: ["merge_edge_cases"],
+    52: ["merge_identity"],
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(KILLERS))
+def test_mutant_is_killed(mutant):
+    oracle.set_mutant(mutant)
+    try:
+        caught = []
+        for name in KILLERS[mutant]:
+            try:
+                P.ALL_PINS[name]()
+            except AssertionError:
+                caught.append(name)
+        assert caught, f"mutant {mutant} survived {KILLERS[mutant]}"
+    finally:
+        oracle.set_mutant(0)
