@@ -1,0 +1,390 @@
+"""Benchmark of the batched paged-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch resident in HBM:
+slot mapping -> scatter of the step's new K/V rows into the paged pool -> varlen paged
+attention (validation + plan, then the attention kernel).  The default workload is the
+64-sequence decode batch with the Llama-3-8B attention shape (H 32, Hkv 8, D 128, bf16,
+contexts U{512..4096}); its K/V (~600 MB per step) is larger than L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2|3|4|5] [--impl reference]
+
+Prints one JSON line.  `value` is whole-job KV GB/s (algorithmic K/V bytes the attention
+reads per step, summed over ranks, divided by the slowest rank's time).  With --gpus N > 1
+(under torchrun) every rank runs an independent replica of the batch ("replicas only": the
+path needs no exchange between GPUs).  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV GB/s (% HBM peak); mixed-batch prefill TFLOP/s; tokens/s"
+KERNEL_SOURCES = {"k_mma16": "paged_kv_cache_31_gb300/csrc/k_decode_mma.cu"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall-time budget of the CPU oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------------
+# ranks
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(local_ms: float, units_per_rank: float, world: int, group=None):
+    """Slowest rank's time and the whole-job throughput: units of all ranks / that time.
+    Collective only when world > 1."""
+    ms = local_ms
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([local_ms], dtype=torch.float64)
+        if dist.get_backend(group) == "nccl":
+            t = t.cuda()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+        ms = float(t.item())
+    return ms, units_per_rank * world / (ms * 1e-3)
+
+
+# ------------------------------------------------------------------------------------------
+# workload accounting (algorithmic units, independent of the kernels)
+
+
+def kv_bytes(w) -> int:
+    """K and V bytes the attention must read: every visible (position, kv head) row once."""
+    esz = 2 if w.dtype.__repr__().endswith("bfloat16") else 4
+    row = w.num_kv_heads * w.head_dim * esz * 2
+    total = 0
+    qsl = w.query_start_loc.cpu().tolist()
+    pos = w.positions.cpu().tolist()
+    for s, n in enumerate(w.seq_lens_list):
+        lo, hi = None, 0
+        for t in range(qsl[s], qsl[s + 1]):
+            e = pos[t] + 1 if w.causal else n
+            b = max(0, e - w.sliding_window) if w.sliding_window > 0 else 0
+            lo = b if lo is None else min(lo, b)
+            hi = max(hi, e)
+        if lo is not None:
+            total += (hi - lo) * row
+    return total
+
+
+def attn_flops(w) -> int:
+    """4 * D * H per visible (query token, key) pair: QK^T and PV multiply-adds."""
+    vis = 0
+    qsl = w.query_start_loc.cpu().tolist()
+    pos = w.positions.cpu().tolist()
+    for s, n in enumerate(w.seq_lens_list):
+        for t in range(qsl[s], qsl[s + 1]):
+            e = pos[t] + 1 if w.causal else n
+            b = max(0, e - w.sliding_window) if w.sliding_window > 0 else 0
+            vis += e - b
+    return 4 * w.head_dim * w.num_heads * vis
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), float(parts[3]),
+                             parts[4:8]))
+            except ValueError:
+                continue
+        busy = [r for r in rows if r[3] > 0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i, v in enumerate(r[4]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in busy) if busy else None,
+                "sm_max_mhz": max(r[1] for r in busy) if busy else None,
+                "power_w_max": max(r[2] for r in busy) if busy else None,
+                "samples": len(busy), "reasons": reasons}
+
+
+# ------------------------------------------------------------------------------------------
+# measured peaks and ncu traffic
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), "measured"
+    return 6800.0, "fallback"
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none or the kernel source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}/{workload}")
+    if not e:
+        return None
+    with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return e.get("bytes_per_launch") if e.get("source_sha") == sha else None
+
+
+# ------------------------------------------------------------------------------------------
+# the CPU oracle (reference arm and cpu_baseline)
+
+
+def time_oracle(w, budget_s: float):
+    """Run the oracle on the whole batch repeatedly for about budget_s seconds of wall time
+    (at least once).  Returns (seconds per batch, batches run, threads)."""
+    import oracle
+
+    oracle.build()
+    q, kb, vb = w.q.cpu(), w.k_blocks.cpu(), w.v_blocks.cpu()
+    meta = [w.query_start_loc.cpu(), w.seq_lens.cpu(), w.positions.cpu(), w.block_tables.cpu()]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        st, _, _ = oracle.varlen_attention(q, kb, vb, *meta, w.scale, causal=w.causal,
+                                           sliding_window=w.sliding_window)
+        assert st == oracle.OK
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return el / n, n, oracle.num_threads()
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    per, n, cores = time_oracle(w, max(args.cpu_seconds, 1.0))
+    kvb = kv_bytes(w)
+    value = kvb / per / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": n, "warmup": 0, "ms_per_step": per * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "seed": args.seed},
+        "tokens_per_s": w.num_tokens / per,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} passes of the whole {w.name} batch"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# the GPU arm
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    import torch
+
+    from paged_kv_cache_31_gb300 import workloads
+
+    if args.impl == "reference":
+        if rank == 0:
+            w = workloads.named(args.config, seed=args.seed, device="cpu")
+            run_reference(args, w, rank)
+        return
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    group = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    from paged_kv_cache_31_gb300 import binding as pa
+
+    w = workloads.named(args.config, seed=args.seed, device=dev)
+    kvb = kv_bytes(w)
+    flops = attn_flops(w)
+    T = w.num_tokens
+    ws = pa.workspace_for(w.q, w.k_blocks, w.query_start_loc, w.block_tables)
+    kb, vb = w.k_blocks, w.v_blocks
+    out = torch.empty_like(w.q)
+    slots = torch.empty(T, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pa.pa_slot_mapping(w.query_start_loc, w.positions, w.block_tables, w.block_size,
+                           w.num_blocks, out=slots)
+        pa.pa_reshape_and_cache(w.k_new, w.v_new, kb, vb, slots)
+        pa.pa_varlen_forward(w.q, kb, vb, out, w.query_start_loc, w.seq_lens, w.positions,
+                             w.block_tables, w.scale, causal=w.causal,
+                             sliding_window=w.sliding_window, workspace=ws)
+
+    launches_per_step = 5  # slot map, slot check, scatter, validate+plan, attention
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert pa.pa_device_status() == pa.PA_OK
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
+    with sampler:
+        time.sleep(0.3)
+        # ---- whole step, inputs resident in HBM
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        step_ms = e0.elapsed_time(e1) / args.steps
+
+        # ---- the attention call alone (validate+plan and the attention kernel)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            pa.pa_varlen_forward(w.q, kb, vb, out, w.query_start_loc, w.seq_lens, w.positions,
+                                 w.block_tables, w.scale, causal=w.causal,
+                                 sliding_window=w.sliding_window, workspace=ws)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        attn_ms = a0.elapsed_time(a1) / args.steps
+
+        # ---- end to end through the public API with host buffers
+        host = {k: getattr(w, k).cpu().pin_memory()
+                for k in ("q", "k_new", "v_new", "query_start_loc", "seq_lens", "positions",
+                          "block_tables")}
+        dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        hout = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = hout.numel() * hout.element_size()
+        e2e_steps = max(1, args.steps // 4)
+
+        def e2e_step():
+            for k, v in host.items():
+                dbuf[k].copy_(v, non_blocking=True)
+            pa.pa_slot_mapping(dbuf["query_start_loc"], dbuf["positions"], dbuf["block_tables"],
+                               w.block_size, w.num_blocks, out=slots)
+            pa.pa_reshape_and_cache(dbuf["k_new"], dbuf["v_new"], kb, vb, slots)
+            pa.pa_varlen_forward(dbuf["q"], kb, vb, out, dbuf["query_start_loc"],
+                                 dbuf["seq_lens"], dbuf["positions"], dbuf["block_tables"],
+                                 w.scale, causal=w.causal, sliding_window=w.sliding_window,
+                                 workspace=ws)
+            hout.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+        barrier()
+    assert pa.pa_device_status() == pa.PA_OK, "device status set during the timed region"
+
+    step_ms, value = aggregate(step_ms, kvb / 1e9, world, group)
+    e2e_ms, e2e_value = aggregate(e2e_ms, kvb / 1e9, world, group)
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    achieved = kvb / (attn_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_tokens": T,
+                   "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "block_size": w.block_size,
+                   "sliding_window": w.sliding_window, "kv_bytes_per_step": kvb,
+                   "attn_flops_per_step": flops, "seed": args.seed,
+                   "l2": f"inputs larger than L2 ({kvb / 1e6:.0f} MB of K/V read per step)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "tokens_per_s": T * world / (step_ms * 1e-3),
+        "attn_tflops": flops / (attn_ms * 1e-3) / 1e12,
+        "clocks": sampler.summary(),
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic("k_mma16", w.name),
+                     "kernel": "pa_varlen_forward (validate+plan, k_mma16)",
+                     "peak_kind": f"{peak_kind} hbm_gbs", "ms_per_launch": attn_ms},
+    }
+    if not args.no_cpu_baseline:
+        per, n, cores = time_oracle(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": kvb / per / 1e9, "unit": "GB/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{n} passes of the whole {w.name} batch "
+                                          f"({per:.2f} s each)"}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * pa.h -- batched paged attention over a block-pooled KV cache, for GB300 (sm_103a).
+ *
+ * C ABI of libpa.so.  Every pointer argument named *_blocks, q, k, v, out, lse, the
+ * int32 metadata arrays and any workspace is a DEVICE pointer that the caller owns;
+ * the library allocates no device memory.  Every call is asynchronous on `stream`
+ * (0 = the legacy default stream) and returns after enqueueing its kernels.
+ *
+ * Layouts (row-major, as the TensorSharp "ManagedPagedAttention.cs" class summary
+ * states them):
+ *   q, out               [num_tokens, num_heads, head_dim]
+ *   k, v (new tokens)    [num_tokens, num_kv_heads, head_dim]
+ *   k_blocks, v_blocks   [num_blocks, block_size, num_kv_heads, head_dim]
+ *   block_tables         int32 [num_seqs, max_blocks_per_seq]: position j of sequence s
+ *                        lives in row j mod block_size of block block_tables[s][j / block_size]
+ *                        (tinyllm "Paged attention for decode in C", section 2.1)
+ *   query_start_loc      int32 [num_seqs + 1], query_start_loc[0] = 0,
+ *                        query_start_loc[num_seqs] = num_tokens
+ *   seq_lens             int32 [num_seqs]: cached positions of the sequence, new tokens included
+ *   positions            int32 [num_tokens]: absolute position of each token in its sequence
+ *   lse                  fp32 [num_heads, num_tokens], natural log (vllm.cpp cpu_mla_prefill.cpp)
+ *
+ * Errors.  Argument and shape errors are returned immediately and nothing is enqueued.
+ * Errors in the device-resident metadata (a block id outside the pool, a table too short,
+ * an empty context, a position outside its context, a slot outside the pool) are found on
+ * the device by a validation kernel that runs before any output is written: the call then
+ * writes NO output, and the error is recorded in a per-device status word that
+ * pa_device_status() returns.  The recorded error is sticky: until pa_device_status() reads
+ * and clears it, every later call on that device also skips its writes.  A bounded wait
+ * that runs out inside a kernel records PA_ETIMEOUT the same way.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes: the error classes of the tinyllm decode interface (section 4:
+ * TL_EINVAL, TL_ESHAPE; section 2.6: TL_EUNSUPPORTED) plus the CUDA and timeout cases. */
+typedef enum {
+  PA_OK = 0,
+  PA_EINVAL = 1,       /* NULL pointer, bad metadata, sizes out of range */
+  PA_ESHAPE = 2,       /* num_heads % num_kv_heads != 0, non-positive dims */
+  PA_EUNSUPPORTED = 3, /* dtype or shape this build does not implement */
+  PA_ECUDA = 4,        /* a CUDA runtime call failed */
+  PA_ETIMEOUT = 5      /* a bounded wait inside a kernel ran out */
+} pa_status;
+
+/* Element types (vllm.cpp cpu_mla_prefill.cpp LoadF/StoreF: f32 and bf16). */
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* pa_status_string(pa_status status);
+
+/* Synchronises `stream`, then returns and clears this device's sticky status word
+ * (PA_OK if no kernel recorded an error).  Returns PA_ECUDA if the synchronisation
+ * itself fails. */
+pa_status pa_device_status(cudaStream_t stream);
+
+/*
+ * pa_slot_mapping -- the physical slot of every new token.
+ * slot_mapping[t] = block_tables[s][p / block_size] * block_size + p % block_size for
+ * token t of sequence s at position p = positions[t] (TensorSharp class summary,
+ * "slot = blockId * blockSize + offsetInBlock"; tinyllm section 2.1).
+ * A token whose position lies outside its table row, or whose block id lies outside
+ * [0, num_blocks), gets slot -1 and records PA_EINVAL.
+ */
+pa_status pa_slot_mapping(const int32_t* query_start_loc, const int32_t* positions,
+                          const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                          int32_t max_blocks_per_seq, int32_t block_size, int64_t num_blocks,
+                          int32_t* slot_mapping, cudaStream_t stream);
+
+/*
+ * pa_reshape_and_cache -- scatter the new tokens' K and V rows into the pool
+ * (TensorSharp WriteKvToPagedPool): the num_kv_heads * head_dim elements of token t go to
+ * block slot_mapping[t] / block_size, row slot_mapping[t] % block_size, of each pool.
+ * A pure copy: bit-exact.  Every slot is checked on the device before any row is written;
+ * one slot outside [0, num_blocks * block_size) writes nothing and records PA_EINVAL.
+ * Duplicate slots are undefined.
+ */
+pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                               const int32_t* slot_mapping, int64_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int64_t num_blocks, pa_dtype kv_dtype, cudaStream_t stream);
+
+/*
+ * pa_varlen_forward_workspace_size -- bytes of device workspace pa_varlen_forward needs
+ * for these sizes (the per-call plan of work items and split-KV partial states).
+ */
+size_t pa_varlen_forward_workspace_size(int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t max_blocks_per_seq, int32_t block_size);
+
+/*
+ * pa_varlen_forward -- batched varlen paged attention (TensorSharp Forward /
+ * ComputeSingleQueryAttention; tinyllm section 2.2).  One call serves any mix of prefill
+ * chunks and decode tokens.  For token t of sequence s at position p and head h, with
+ * kv head g = h / (num_heads / num_kv_heads):
+ *     end   = causal ? p + 1 : seq_lens[s]
+ *     start = sliding_window > 0 ? max(0, end - sliding_window) : 0
+ *     out[t, h] = softmax_j(scale * q[t, h] . K_j) V_j   over positions j in [start, end)
+ * where K_j, V_j are pool rows of kv head g found through the block table.  out has
+ * q_dtype.  k_blocks/v_blocks have kv_dtype.
+ * Validation (tinyllm section 2.6), for every sequence with at least one query token:
+ * seq_lens[s] >= 1, ceil(seq_lens[s] / block_size) <= max_blocks_per_seq, those table
+ * entries in [0, num_blocks), positions in [0, seq_lens[s]); query_start_loc starts at 0,
+ * never decreases and ends at num_tokens.  Failures record PA_EINVAL and leave out
+ * untouched.  workspace must hold pa_varlen_forward_workspace_size(...) bytes, 256-byte
+ * aligned; it is scratch owned by the caller and must not be shared by calls that overlap
+ * on the device.
+ */
+pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_blocks, void* out,
+                            const int32_t* query_start_loc, const int32_t* seq_lens,
+                            const int32_t* positions, const int32_t* block_tables,
+                            int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int64_t num_blocks, int32_t max_blocks_per_seq, pa_dtype q_dtype,
+                            pa_dtype kv_dtype, float scale, int32_t causal,
+                            int32_t sliding_window, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/*
+ * pa_decode_splitkv_partials -- phase 1 of split-KV decode ("paged_attention_v2_pytorch.py",
+ * partition loop).  One query per sequence, q [num_seqs, num_heads, head_dim], at position
+ * seq_lens[s] - 1 (causal by construction).  Partition p covers positions
+ * [p * partition_size, min((p + 1) * partition_size, seq_lens[s])), intersected with the
+ * window [max(0, seq_lens[s] - sliding_window), seq_lens[s]) when sliding_window > 0.
+ * For every (s, h, p < max_num_partitions):
+ *     max_logits[s, h, p] = max_j scale * q . K_j            (-inf if no position)
+ *     exp_sums[s, h, p]   = sum_j exp(scale * q . K_j - max)  (0 if no position)
+ *     tmp_out[s, h, p, :] = sum_j exp(...) V_j / exp_sum      (zeros if no position)
+ * tmp_out holds the NORMALISED partition output (the reading under which the page's
+ * reduction is a log-sum-exp merge).  max_logits / exp_sums are fp32 [S, H, P]; tmp_out fp32
+ * [S, H, P, D].  Validation: seq_lens[s] >= 1, the table covers ceil(seq_len / block_size)
+ * blocks with ids in [0, num_blocks), ceil(seq_len / partition_size) <= max_num_partitions.
+ * partition_size must be a positive multiple of block_size.
+ */
+pa_status pa_decode_splitkv_partials(const void* q, const void* k_blocks, const void* v_blocks,
+                                     float* max_logits, float* exp_sums, float* tmp_out,
+                                     const int32_t* seq_lens, const int32_t* block_tables,
+                                     int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                     int32_t max_blocks_per_seq, int32_t partition_size,
+                                     int32_t max_num_partitions, pa_dtype q_dtype,
+                                     pa_dtype kv_dtype, float scale, int32_t sliding_window,
+                                     cudaStream_t stream);
+
+/*
+ * pa_decode_splitkv_reduce -- phase 2 ("Phase 2: Cross-partition reduction").  For each
+ * (s, h) over partitions p < ceil(seq_lens[s] / partition_size):
+ *     lse_p = max_logits + log(exp_sums), or -inf when max_logits is +/-inf or exp_sums <= 0
+ *     M = max_p lse_p;  w_p = exp(lse_p - M);  out = sum_p w_p tmp_out_p * (1 / sum_p w_p)
+ * and when every lse_p is -inf, out = tmp_out of partition 0 (the both-minus-infinity rule of
+ * vllm.cpp MergeAttnStatesKernel, extended to P partitions).  Partitions combine in
+ * increasing p.  out is [num_seqs, num_heads, head_dim] in out_dtype.
+ */
+pa_status pa_decode_splitkv_reduce(void* out, const float* max_logits, const float* exp_sums,
+                                   const float* tmp_out, const int32_t* seq_lens,
+                                   int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                   int32_t partition_size, int32_t max_num_partitions,
+                                   pa_dtype out_dtype, cudaStream_t stream);
+
+/* pa_decode_splitkv -- pa_decode_splitkv_partials followed by pa_decode_splitkv_reduce on
+ * the same stream; the partial buffers are caller-owned scratch. */
+pa_status pa_decode_splitkv(const void* q, const void* k_blocks, const void* v_blocks, void* out,
+                            float* max_logits, float* exp_sums, float* tmp_out,
+                            const int32_t* seq_lens, const int32_t* block_tables,
+                            int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                            int32_t max_blocks_per_seq, int32_t partition_size,
+                            int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype,
+                            float scale, int32_t sliding_window, cudaStream_t stream);
+
+/*
+ * pa_merge_attn_states -- merge two attention states of the same queries (vllm.cpp
+ * cpu_mla_prefill.cpp, MergeAttnStatesKernel).  out/prefix_out/suffix_out [T, H, D] in dtype;
+ * lse arrays fp32 [H, T]; out_lse may be NULL.  Tokens t >= prefill_tokens_with_context
+ * (when that is >= 0) copy the suffix and its lse.  Otherwise an infinite lse of either sign
+ * counts as -inf; if both are -inf the prefix output is emitted with lse -inf; else
+ *     p_scale = p_se / (p_se + s_se), s_scale = s_se / (p_se + s_se),
+ *     p_se = exp(p_lse - max), s_se = exp(s_lse - max),
+ *     out = prefix * p_scale + suffix * s_scale,  out_lse = log(p_se + s_se) + max.
+ */
+pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
+                               const float* prefix_lse, const void* suffix_out,
+                               const float* suffix_lse, int64_t num_tokens, int32_t num_heads,
+                               int32_t head_dim, int64_t prefill_tokens_with_context,
+                               pa_dtype dtype, cudaStream_t stream);
+
+/*
+ * pa_gather_kv -- copy sequences' cached rows into dense buffers (vllm.cpp
+ * GatherMlaCacheKernel).  Output rows [cu_seq_lens[s], cu_seq_lens[s + 1]) receive the pool
+ * rows (all kv heads) at positions (r - cu_seq_lens[s]) + seq_starts[s] of sequence s;
+ * seq_starts may be NULL (all 0).  k_out/v_out are [cu_seq_lens[num_seqs], num_kv_heads,
+ * head_dim]; v_blocks and v_out may both be NULL.  A position past the table row or a block
+ * id outside the pool records PA_EINVAL and writes nothing.  Bit-exact copy.
+ */
+pa_status pa_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, void* v_out,
+                       const int32_t* cu_seq_lens, const int32_t* seq_starts,
+                       const int32_t* block_tables, int32_t num_seqs, int64_t num_out_rows,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int64_t num_blocks, int32_t max_blocks_per_seq, pa_dtype kv_dtype,
+                       cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

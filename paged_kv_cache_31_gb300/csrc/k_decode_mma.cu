@@ -1,0 +1,456 @@
+// k_decode_mma.cu -- paged attention for tiles of up to 16 query rows of one (sequence,
+// kv head): decode tokens (one CTA serves the whole GQA group of a kv head) and the split-KV
+// partitions of PagedAttention V2.
+//
+// Data path.  The pool is [num_blocks, 16, num_kv_heads, D] bf16.  One (block, kv head) K or
+// V tile is 16 rows of D elements, rows 2 * num_kv_heads * D bytes apart.  Each warp of the
+// CTA owns a private ring of NS stages; its lane 0 streams whole blocks into the ring with
+// 3-D TMA tile loads (box 64 x 1 x 16, 128-byte swizzle, one 2 KB box per 64-dim half, K and
+// V on one mbarrier).  Warps take the visible blocks round-robin, so every byte is read once
+// per kv head and the reads stay 16-byte vectorised and coalesced.
+//
+// Math.  The tile's query rows are (token, head) pairs, token-major; q stays in registers as
+// bf16 A fragments.  Per block: S = Q K^T on the m16n8k16 tensor-core MMA (fp32 accumulate),
+// mask to each row's visible range [start, end), scale into the log2 domain, block max via
+// quad shuffles, the online-softmax update m' = max(m, .), alpha = 2^(m - m'),
+// l = alpha l + sum p, O = alpha O + P V (tinyllm section 2.2, applied per 16-key block).
+// P is rounded to bf16 for the PV MMA and l sums those same rounded weights.  At the end the
+// warps' (m, l, O) states are merged in fixed warp order and o = O * (1 / l).
+//
+// Why warp MMA here: these tiles are HBM-bound (one pass over K and V per kv head), so the
+// tensor core only has to take the ~2 G D FMA per key off the FP32 pipe; with G = 8 the FMA
+// path would need about half the chip's FP32 rate at full HBM bandwidth.
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kBlk = 16;  // positions per pool block on this path
+
+template <int D>
+struct Geom {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kHalfBytes = kBlk * 128;            // 16 rows x 64 bf16
+  static constexpr int kTileBytes = kHalves * kHalfBytes;  // one K (or V) block tile
+  static constexpr int kStageBytes = 2 * kTileBytes;       // K + V
+  static constexpr int kNT = D / 8;                        // n-tiles of the output
+  static constexpr int kKS = D / 16;                       // k-steps of QK^T
+};
+
+template <int D, int NW, int NS>
+constexpr size_t smem_bytes() {
+  // ring | full barriers | merge m, l | fail flag ; the O merge area aliases the ring
+  return 1024 + (size_t)NW * NS * Geom<D>::kStageBytes + NW * NS * 8 + NW * 16 * 4 * 2 + 16;
+}
+
+// Byte offset of 16-byte chunk `chunk` (along D) of row `row` inside a tile written by TMA
+// with the 128-byte swizzle: halves of 64 dims are separate 2 KB boxes; inside a half the
+// chunk index is XORed with row mod 8.
+__device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
+  const int half = chunk >> 3, c = chunk & 7;
+  return (uint32_t)(half * (kBlk * 128) + row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+template <int D, int NW, int NS, bool SPLIT>
+__global__ void __launch_bounds__(NW * 32, 2)
+    k_mma16(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+            const Mma16Params p) {
+  using G_ = Geom<D>;
+  extern __shared__ uint8_t smem_raw[];
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NW * NS * G_::kStageBytes);
+  float* mrg_m = reinterpret_cast<float*>(full + NW * NS);
+  float* mrg_l = mrg_m + NW * 16;
+  int* fail = reinterpret_cast<int*>(mrg_l + NW * 16);
+  float* mrg_o = reinterpret_cast<float*>(ring);  // [NW][16][D + 4], used after the ring drains
+  constexpr int kOStride = D + 4;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < NW * NS) mbar_init(&full[threadIdx.x], 1);
+  if (threadIdx.x == 0) {
+    // failed validation or an earlier sticky error: the whole CTA writes nothing
+    *fail = status_set(p.status) ? 1 : 0;
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+  }
+  fence_mbar_init();
+  __syncthreads();
+  if (*reinterpret_cast<volatile int*>(fail)) return;
+
+  const VarlenMeta& m = p.m;
+  const int kvh = blockIdx.y;
+  const int G = m.group;
+  const int H = m.num_heads;
+  uint32_t ring_pos = 0;  // blocks this warp has pushed through its ring so far
+
+  int n_items;
+  const int2* items = nullptr;
+  if constexpr (SPLIT) {
+    n_items = m.num_seqs * p.max_parts;
+  } else {
+    n_items = p.plan[0];
+    const int64_t tok_words = (m.num_tokens + 1) & ~int64_t(1);
+    items = reinterpret_cast<const int2*>(p.plan + kPlanHeaderWords + tok_words);
+  }
+
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    // ---------------------------------------------------------------- item geometry
+    int s, row0, rows_total, part = 0, qs, n;
+    if constexpr (SPLIT) {
+      s = item / p.max_parts;
+      part = item % p.max_parts;
+      qs = s;
+      row0 = 0;
+      rows_total = G;
+    } else {
+      const int2 it = items[item];
+      s = it.x;
+      row0 = it.y * 16;
+      qs = m.query_start_loc[s];
+      rows_total = (m.query_start_loc[s + 1] - qs) * G;
+    }
+    n = m.seq_lens[s];
+
+    // this lane's two rows: r0 = lane / 4 and r1 = r0 + 8
+    int st[2], en[2], tok[2], head[2];
+    bool valid[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int R = row0 + (lane >> 2) + 8 * i;
+      valid[i] = R < rows_total;
+      const int tl = valid[i] ? R / G : 0;
+      tok[i] = qs + tl;
+      head[i] = kvh * G + (valid[i] ? R % G : 0);
+      int e, b;
+      if constexpr (SPLIT) {
+        e = n;  // the decode query sits at n - 1: causal by construction
+        b = m.window > 0 ? max(0, e - m.window) : 0;
+        b = max(b, part * p.partition_size);
+        e = min(e, (part + 1) * p.partition_size);
+      } else {
+        const int pos = m.positions[tok[i]];
+        e = m.causal ? pos + 1 : n;
+        b = m.window > 0 ? max(0, e - m.window) : 0;
+      }
+      st[i] = valid[i] ? b : 0;
+      en[i] = valid[i] ? max(e, b) : 0;
+    }
+    // union of the rows' visible ranges -> the blocks to stream
+    int lo = INT_MAX, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if (valid[i] && en[i] > st[i]) {
+        lo = min(lo, st[i]);
+        hi = max(hi, en[i]);
+      }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      lo = min(lo, __shfl_xor_sync(kFull, lo, o));
+      hi = max(hi, __shfl_xor_sync(kFull, hi, o));
+    }
+    const int blk_lo = lo < hi ? lo / kBlk : 0;
+    const int nblk = lo < hi ? (hi + kBlk - 1) / kBlk - blk_lo : 0;
+    const int my_count = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+    const int32_t* table_row = m.block_tables + (int64_t)s * m.max_blocks;
+
+    // ---------------------------------------------------------------- q fragments
+    uint32_t qa[G_::kKS][4];
+    {
+      const uint32_t* q0 =
+          reinterpret_cast<const uint32_t*>(p.q + ((int64_t)tok[0] * H + head[0]) * D);
+      const uint32_t* q1 =
+          reinterpret_cast<const uint32_t*>(p.q + ((int64_t)tok[1] * H + head[1]) * D);
+      const int c = (lane & 3);
+#pragma unroll
+      for (int kk = 0; kk < G_::kKS; ++kk) {
+        qa[kk][0] = valid[0] ? q0[kk * 8 + c] : 0u;
+        qa[kk][1] = valid[1] ? q1[kk * 8 + c] : 0u;
+        qa[kk][2] = valid[0] ? q0[kk * 8 + 4 + c] : 0u;
+        qa[kk][3] = valid[1] ? q1[kk * 8 + 4 + c] : 0u;
+      }
+    }
+
+    // ---------------------------------------------------------------- streaming
+    float mrow[2] = {-INFINITY, -INFINITY};
+    float lrow[2] = {0.f, 0.f};
+    float o[G_::kNT][4];
+#pragma unroll
+    for (int j = 0; j < G_::kNT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+    int tbl_win = -1, tbl_val = 0;
+    auto block_id = [&](int x) -> int {  // whole warp; x = this warp's block index
+      const int win = x >> 5;
+      if (win != tbl_win) {
+        tbl_win = win;
+        const int lb = warp + (win * 32 + lane) * NW;
+        tbl_val = lb < nblk ? table_row[blk_lo + lb] : 0;
+      }
+      return __shfl_sync(kFull, tbl_val, x & 31);
+    };
+    auto issue = [&](int x) {  // whole warp
+      const int id = block_id(x);
+      if (lane == 0) {
+        const uint32_t slot = (ring_pos + x) % NS;
+        uint64_t* bar = &full[warp * NS + slot];
+        uint8_t* dst = ring + (size_t)(warp * NS + slot) * G_::kStageBytes;
+        mbar_arrive_expect_tx(bar, G_::kStageBytes);
+#pragma unroll
+        for (int h = 0; h < G_::kHalves; ++h) {
+          tma_load_3d(dst + h * G_::kHalfBytes, &tk, h * 64, kvh, id * kBlk, bar);
+          tma_load_3d(dst + G_::kTileBytes + h * G_::kHalfBytes, &tv, h * 64, kvh, id * kBlk, bar);
+        }
+      }
+    };
+
+    const int pro = my_count < NS ? my_count : NS;
+    for (int x = 0; x < pro; ++x) issue(x);
+    int issued = pro;
+    bool timed_out = false;
+
+    for (int x = 0; x < my_count; ++x) {
+      const uint32_t cnt = ring_pos + x;
+      const uint32_t slot = cnt % NS;
+      if (!mbar_wait(&full[warp * NS + slot], (cnt / NS) & 1u, p.wait_limit_ns)) {
+        timed_out = true;
+        break;
+      }
+      uint8_t* kt = ring + (size_t)(warp * NS + slot) * G_::kStageBytes;
+      uint8_t* vt = kt + G_::kTileBytes;
+      const int lb = blk_lo + warp + x * NW;
+      const int key_base = lb * kBlk;
+
+      // rows of the sequence's last block past seq_len were never written: zero their V so
+      // that 0-weight * garbage cannot turn into NaN
+      if (key_base + kBlk > n) {
+        const int first = n - key_base;  // 1..15
+        for (int i = lane; i < (kBlk - first) * G_::kHalves * 8; i += 32) {
+          const int r = first + i / (G_::kHalves * 8);
+          const int rest = i % (G_::kHalves * 8);
+          *reinterpret_cast<uint4*>(vt + (rest >> 3) * G_::kHalfBytes + r * 128 + (rest & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+
+      // S = Q K^T for 16 keys: two n-tiles of 8 keys
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int key = rr + ((mi >> 1) << 3);
+        const uint32_t kbase = smem_u32(kt);
+#pragma unroll
+        for (int kk = 0; kk < G_::kKS; ++kk) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kbase + tile_off(key, kk * 2 + (mi & 1)), b0, b1, b2, b3);
+          mma_bf16_16816(sc[0], qa[kk], b0, b1);
+          mma_bf16_16816(sc[1], qa[kk], b2, b3);
+        }
+      }
+
+      // mask, scale to log2 units, online softmax update
+      const int kcol = key_base + (lane & 3) * 2;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int key = kcol + nt * 8 + (c & 1);
+          const int r = c >> 1;
+          const bool vis = key >= st[r] && key < en[r];
+          sc[nt][c] = vis ? sc[nt][c] * p.scale_log2 : -INFINITY;
+        }
+      float alpha[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float mx = fmaxf(fmaxf(sc[0][2 * r], sc[0][2 * r + 1]), fmaxf(sc[1][2 * r], sc[1][2 * r + 1]));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        const float mn = fmaxf(mrow[r], mx);
+        const float base = mn == -INFINITY ? 0.f : mn;
+        alpha[r] = exp2f(mrow[r] - base);
+        mrow[r] = mn;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          sc[nt][2 * r] = exp2f(sc[nt][2 * r] - base);
+          sc[nt][2 * r + 1] = exp2f(sc[nt][2 * r + 1] - base);
+        }
+      }
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
+      pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
+      pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
+      pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+      {
+        // l sums the bf16-rounded weights that the PV product uses
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(pa);
+        const float2 w0 = __bfloat1622float2(pb[0]), w1 = __bfloat1622float2(pb[1]);
+        const float2 w2 = __bfloat1622float2(pb[2]), w3 = __bfloat1622float2(pb[3]);
+        lrow[0] = lrow[0] * alpha[0] + ((w0.x + w0.y) + (w2.x + w2.y));
+        lrow[1] = lrow[1] * alpha[1] + ((w1.x + w1.y) + (w3.x + w3.y));
+      }
+#pragma unroll
+      for (int j = 0; j < G_::kNT; ++j) {
+        o[j][0] *= alpha[0];
+        o[j][1] *= alpha[0];
+        o[j][2] *= alpha[1];
+        o[j][3] *= alpha[1];
+      }
+      // O += P V: V is the k-major B operand, read with transposing ldmatrix
+      {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int key = rr + ((mi & 1) << 3);
+        const uint32_t vbase = smem_u32(vt);
+#pragma unroll
+        for (int dd = 0; dd < D / 16; ++dd) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_trans(vbase + tile_off(key, dd * 2 + (mi >> 1)), b0, b1, b2, b3);
+          mma_bf16_16816(o[2 * dd], pa, b0, b1);
+          mma_bf16_16816(o[2 * dd + 1], pa, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (issued < my_count) {
+        issue(issued);
+        ++issued;
+      }
+    }
+
+    if (timed_out) {
+      if (lane == 0) {
+        record_error(p.status, PA_ETIMEOUT);
+        atomicExch(fail, 1);
+      }
+      // wait (bounded) for this warp's copies still in flight before the CTA leaves
+      for (int x = 0; x < issued; ++x) {
+        const uint32_t cnt = ring_pos + x;
+        mbar_wait(&full[warp * NS + cnt % NS], (cnt / NS) & 1u, 100000000ull);
+      }
+    }
+    ring_pos += issued;
+
+    // ---------------------------------------------------------------- merge the warps
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      lrow[r] += __shfl_xor_sync(kFull, lrow[r], 1);
+      lrow[r] += __shfl_xor_sync(kFull, lrow[r], 2);
+    }
+    __syncthreads();  // every warp is done with its ring: the O area may alias it now
+    if (*reinterpret_cast<volatile int*>(fail)) return;
+    {
+      const int r0 = lane >> 2;
+      if ((lane & 3) == 0) {
+        mrg_m[warp * 16 + r0] = mrow[0];
+        mrg_m[warp * 16 + r0 + 8] = mrow[1];
+        mrg_l[warp * 16 + r0] = lrow[0];
+        mrg_l[warp * 16 + r0 + 8] = lrow[1];
+      }
+      float* ob = mrg_o + (size_t)warp * 16 * kOStride;
+#pragma unroll
+      for (int j = 0; j < G_::kNT; ++j) {
+        const int col = j * 8 + (lane & 3) * 2;
+        *reinterpret_cast<float2*>(ob + r0 * kOStride + col) = make_float2(o[j][0], o[j][1]);
+        *reinterpret_cast<float2*>(ob + (r0 + 8) * kOStride + col) = make_float2(o[j][2], o[j][3]);
+      }
+    }
+    __syncthreads();
+    {
+      constexpr int kSegs = NW * 32 / 16;  // threads per row
+      constexpr int kSeg = D / kSegs;      // dims per thread
+      static_assert(kSeg % 8 == 0, "epilogue writes 16-byte chunks");
+      const int row = threadIdx.x / kSegs, seg = threadIdx.x % kSegs;
+      const int R = row0 + row;
+      if (R < rows_total) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * 16 + row]);
+        float wsc[NW];
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          wsc[w] = M == -INFINITY ? 0.f : exp2f(mrg_m[w * 16 + row] - M);
+          L += wsc[w] * mrg_l[w * 16 + row];
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const int t = qs + R / G;
+        const int h = kvh * G + R % G;
+        float vals[kSeg];
+#pragma unroll
+        for (int d = 0; d < kSeg; ++d) {
+          float acc = 0.f;
+#pragma unroll
+          for (int w = 0; w < NW; ++w)
+            acc += wsc[w] * mrg_o[((size_t)w * 16 + row) * kOStride + seg * kSeg + d];
+          vals[d] = acc * inv;
+        }
+        if constexpr (SPLIT) {
+          const int64_t idx = ((int64_t)s * H + h) * p.max_parts + part;
+          float* dst = p.tmp_out + idx * D + seg * kSeg;
+#pragma unroll
+          for (int d = 0; d < kSeg; d += 4)
+            *reinterpret_cast<float4*>(dst + d) =
+                make_float4(vals[d], vals[d + 1], vals[d + 2], vals[d + 3]);
+          if (seg == 0) {
+            p.max_logits[idx] = M == -INFINITY ? -INFINITY : M * kLn2;
+            p.exp_sums[idx] = L;
+          }
+        } else {
+          __nv_bfloat16* dst =
+              reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * H + h) * D + seg * kSeg;
+#pragma unroll
+          for (int d = 0; d < kSeg; d += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(vals[d], vals[d + 1]);
+            v.y = pack_bf16x2(vals[d + 2], vals[d + 3]);
+            v.z = pack_bf16x2(vals[d + 4], vals[d + 5]);
+            v.w = pack_bf16x2(vals[d + 6], vals[d + 7]);
+            *reinterpret_cast<uint4*>(dst + d) = v;
+          }
+        }
+      }
+    }
+    __syncthreads();  // the merge area is the ring of the next item
+  }
+}
+
+constexpr int kNW = 4;
+constexpr int kNS = 3;
+
+template <int D, bool SPLIT>
+cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p, int grid_x,
+                   cudaStream_t stream) {
+  auto kern = k_mma16<D, kNW, kNS, SPLIT>;
+  constexpr size_t smem = smem_bytes<D, kNW, kNS>();
+  static_assert((size_t)kNW * 16 * (D + 4) * 4 <= (size_t)kNW * kNS * Geom<D>::kStageBytes,
+                "merge area must fit in the ring");
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(grid_x, p.m.num_kv_heads);
+  kern<<<grid, kNW * 32, smem, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mma16_varlen(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p,
+                                int head_dim, int items_cap, cudaStream_t stream) {
+  const int grid_x = items_cap < 1 ? 1 : (items_cap > 65535 ? 65535 : items_cap);
+  if (head_dim == 128) return launch<128, false>(tk, tv, p, grid_x, stream);
+  if (head_dim == 64) return launch<64, false>(tk, tv, p, grid_x, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_mma16_split(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p,
+                               int head_dim, cudaStream_t stream) {
+  const int64_t items = (int64_t)p.m.num_seqs * p.max_parts;
+  const int grid_x = items > 65535 ? 65535 : (int)items;
+  if (grid_x <= 0) return cudaSuccess;
+  if (head_dim == 128) return launch<128, true>(tk, tv, p, grid_x, stream);
+  if (head_dim == 64) return launch<64, true>(tk, tv, p, grid_x, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -1,0 +1,352 @@
+// k_meta.cu -- metadata kernels: validation and work planning, slot mapping, the K/V
+// scatter into the paged pool and the gather back out of it.
+//
+// Every kernel first looks at the device status word: when an earlier kernel (or an earlier
+// call) recorded an error, it writes nothing.  Validation always runs as its own launch
+// before the kernel that writes, so a bad table is found before the first byte of output.
+#include <algorithm>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Exclusive prefix sum of one int per thread across the block; *total receives the sum.
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int before = warp ? s_warp[warp - 1] : 0;
+  *total = s_warp[nwarps - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+// Validation and planning of one pa_varlen_forward call (tinyllm section 2.6 checks), in a
+// single CTA so that the work list can be built with one block-wide scan:
+//  A. query_start_loc starts at 0, never decreases, ends at num_tokens;
+//  B. for each sequence with query tokens: seq_len >= 1, ceil(seq_len / b) <= max_blocks,
+//     those table entries inside the pool, query positions inside [0, seq_len); and the
+//     token -> sequence map;
+//  C. the list of (sequence, 16-row tile) items: a sequence's q_len * G query rows (token
+//     major, head minor within the kv group) are cut into tiles of 16.
+__global__ void __launch_bounds__(1024) k_plan_varlen(VarlenMeta m, int32_t* plan, int* status) {
+  __shared__ int s_err;
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  if (tid == 0) s_err = status_set(status) ? -1 : 0;
+  __syncthreads();
+  if (s_err == 0) {
+    for (int s = tid; s < m.num_seqs; s += blockDim.x) {
+      const int a = m.query_start_loc[s], b = m.query_start_loc[s + 1];
+      if ((s == 0 && a != 0) || b < a) atomicCAS(&s_err, 0, PA_EINVAL);
+    }
+    if (tid == 0 && (int64_t)m.query_start_loc[m.num_seqs] != m.num_tokens)
+      atomicCAS(&s_err, 0, PA_EINVAL);
+  }
+  __syncthreads();
+  if (s_err == 0) {
+    for (int s = warp; s < m.num_seqs; s += nwarps) {
+      const int a = m.query_start_loc[s], b = m.query_start_loc[s + 1];
+      if (a == b) continue;
+      const int n = m.seq_lens[s];
+      if (n < 1) {
+        if (lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
+        continue;
+      }
+      const int64_t need = ((int64_t)n + m.block_size - 1) / m.block_size;
+      if (need > m.max_blocks) {
+        if (lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
+        continue;
+      }
+      const int32_t* row = m.block_tables + (int64_t)s * m.max_blocks;
+      bool bad = false;
+      for (int64_t i = lane; i < need; i += 32) {
+        const int32_t id = row[i];
+        bad |= (id < 0 || (int64_t)id >= m.num_blocks);
+      }
+      for (int t = a + lane; t < b; t += 32) {
+        const int32_t pos = m.positions[t];
+        bad |= (pos < 0 || pos >= n);
+        plan[kPlanHeaderWords + t] = s;
+      }
+      if (__any_sync(kFull, bad) && lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
+    }
+  }
+  __syncthreads();
+  if (s_err != 0) {
+    if (tid == 0) {
+      if (s_err > 0) record_error(status, s_err);
+      plan[0] = 0;
+    }
+    return;
+  }
+  const int64_t tok_words = (m.num_tokens + 1) & ~int64_t(1);  // keep the int2 list 8-byte aligned
+  int2* items = reinterpret_cast<int2*>(plan + kPlanHeaderWords + tok_words);
+  int carry = 0;
+  for (int base = 0; base < m.num_seqs; base += blockDim.x) {
+    const int s = base + tid;
+    int cnt = 0;
+    if (s < m.num_seqs) {
+      const int64_t rows = (int64_t)(m.query_start_loc[s + 1] - m.query_start_loc[s]) * m.group;
+      cnt = (int)((rows + 15) / 16);
+    }
+    int total;
+    const int excl = block_exclusive_scan(cnt, s_warp, &total);
+    for (int i = 0; i < cnt; ++i) items[carry + excl + i] = make_int2(s, i);
+    carry += total;
+  }
+  if (tid == 0) plan[0] = carry;
+}
+
+// Split-KV decode validation: one CTA per sequence.
+__global__ void k_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
+                                  int32_t max_blocks, int32_t block_size, int64_t num_blocks,
+                                  int32_t partition_size, int32_t max_parts, int check_tables,
+                                  int* status) {
+  const int s = blockIdx.x;
+  const int n = seq_lens[s];
+  if (n < 1) {
+    if (threadIdx.x == 0) record_error(status, PA_EINVAL);
+    return;
+  }
+  if (partition_size > 0 && ((int64_t)n + partition_size - 1) / partition_size > max_parts) {
+    if (threadIdx.x == 0) record_error(status, PA_EINVAL);
+    return;
+  }
+  if (!check_tables) return;
+  const int64_t need = ((int64_t)n + block_size - 1) / block_size;
+  if (need > max_blocks) {
+    if (threadIdx.x == 0) record_error(status, PA_EINVAL);
+    return;
+  }
+  const int32_t* row = block_tables + (int64_t)s * max_blocks;
+  bool bad = false;
+  for (int64_t i = threadIdx.x; i < need; i += blockDim.x) {
+    const int32_t id = row[i];
+    bad |= (id < 0 || (int64_t)id >= num_blocks);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) record_error(status, PA_EINVAL);
+}
+
+// Slot mapping: one CTA per sequence.
+__global__ void k_slot_mapping(const int32_t* qsl, const int32_t* positions,
+                               const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                               int32_t max_blocks, int32_t block_size, int64_t num_blocks,
+                               int32_t* slots, int* status) {
+  if (status_set(status)) return;
+  const int s = blockIdx.x;
+  const int a = qsl[s], b = qsl[s + 1];
+  if (a < 0 || b < a || (int64_t)b > num_tokens) {
+    if (threadIdx.x == 0) record_error(status, PA_EINVAL);
+    return;
+  }
+  const int32_t* row = block_tables + (int64_t)s * max_blocks;
+  for (int t = a + threadIdx.x; t < b; t += blockDim.x) {
+    const int32_t pos = positions[t];
+    int32_t slot = -1;
+    if (pos >= 0 && pos / block_size < max_blocks) {
+      const int32_t id = row[pos / block_size];
+      if (id >= 0 && (int64_t)id < num_blocks) slot = id * block_size + pos % block_size;
+    }
+    if (slot < 0) record_error(status, PA_EINVAL);
+    slots[t] = slot;
+  }
+}
+
+__global__ void k_validate_slots(const int32_t* slots, int64_t num_tokens, int64_t num_slots,
+                                 int* status) {
+  bool bad = false;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < num_tokens;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t s = slots[t];
+    bad |= (s < 0 || (int64_t)s >= num_slots);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) record_error(status, PA_EINVAL);
+}
+
+// Scatter: one warp per token copies its K row and its V row (num_kv_heads * head_dim
+// elements each, contiguous on both sides) with VEC-wide accesses.
+template <typename VEC>
+__global__ void k_reshape_and_cache(const VEC* __restrict__ k, const VEC* __restrict__ v,
+                                    VEC* __restrict__ k_blocks, VEC* __restrict__ v_blocks,
+                                    const int32_t* __restrict__ slots, int64_t num_tokens,
+                                    int64_t row_vecs, const int* status) {
+  if (status_set(status)) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= num_tokens) return;
+  const int64_t dst = (int64_t)slots[t] * row_vecs;  // pool row index == slot
+  const int64_t src = t * row_vecs;
+  for (int64_t i = lane; i < row_vecs; i += 32) {
+    const VEC a = k[src + i];
+    const VEC b = v[src + i];
+    k_blocks[dst + i] = a;
+    v_blocks[dst + i] = b;
+  }
+}
+
+// Gather validation: one CTA per sequence.
+__global__ void k_validate_gather(const int32_t* cu, const int32_t* starts, const int32_t* tables,
+                                  int64_t num_rows, int32_t block_size, int64_t num_blocks,
+                                  int32_t max_blocks, int* status) {
+  const int s = blockIdx.x;
+  const int a = cu[s], b = cu[s + 1];
+  const int64_t start = starts ? starts[s] : 0;
+  if (a < 0 || b < a || (int64_t)b > num_rows || start < 0) {
+    if (threadIdx.x == 0) record_error(status, PA_EINVAL);
+    return;
+  }
+  const int32_t* row = tables + (int64_t)s * max_blocks;
+  bool bad = false;
+  for (int r = a + threadIdx.x; r < b; r += blockDim.x) {
+    const int64_t pos = (r - a) + start;
+    if (pos / block_size >= max_blocks) {
+      bad = true;
+      continue;
+    }
+    const int32_t id = row[pos / block_size];
+    bad |= (id < 0 || (int64_t)id >= num_blocks);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) record_error(status, PA_EINVAL);
+}
+
+// Gather: CTA (s, y) copies rows a + y * warps + warp, stepping by gridDim.y * warps.
+template <typename VEC>
+__global__ void k_gather_kv(const VEC* __restrict__ k_blocks, const VEC* __restrict__ v_blocks,
+                            VEC* __restrict__ k_out, VEC* __restrict__ v_out,
+                            const int32_t* __restrict__ cu, const int32_t* __restrict__ starts,
+                            const int32_t* __restrict__ tables, int32_t block_size,
+                            int32_t max_blocks, int64_t row_vecs, const int* status) {
+  if (status_set(status)) return;
+  const int s = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int a = cu[s], b = cu[s + 1];
+  const int64_t start = starts ? starts[s] : 0;
+  const int32_t* row = tables + (int64_t)s * max_blocks;
+  for (int r = a + blockIdx.y * nwarps + warp; r < b; r += gridDim.y * nwarps) {
+    const int64_t pos = (r - a) + start;
+    const int64_t slot = (int64_t)row[pos / block_size] * block_size + pos % block_size;
+    const int64_t src = slot * row_vecs, dst = (int64_t)r * row_vecs;
+    for (int64_t i = lane; i < row_vecs; i += 32) {
+      k_out[dst + i] = k_blocks[src + i];
+      if (v_out) v_out[dst + i] = v_blocks[src + i];
+    }
+  }
+}
+
+template <typename VEC>
+cudaError_t scatter_as(const void* k, const void* v, void* kb, void* vb, const int32_t* slots,
+                       int64_t T, int64_t row_bytes, const int* status, cudaStream_t stream) {
+  const int warps = 8;
+  const int64_t grid = (T + warps - 1) / warps;
+  k_reshape_and_cache<VEC><<<(unsigned)grid, warps * 32, 0, stream>>>(
+      (const VEC*)k, (const VEC*)v, (VEC*)kb, (VEC*)vb, slots, T,
+      row_bytes / (int64_t)sizeof(VEC), status);
+  return cudaGetLastError();
+}
+
+template <typename VEC>
+cudaError_t gather_as(const void* kb, const void* vb, void* ko, void* vo, const int32_t* cu,
+                      const int32_t* starts, const int32_t* tables, int32_t S, int64_t row_bytes,
+                      int32_t bs, int32_t max_blocks, const int* status, cudaStream_t stream) {
+  dim3 grid(S, 16);
+  k_gather_kv<VEC><<<grid, 256, 0, stream>>>((const VEC*)kb, (const VEC*)vb, (VEC*)ko, (VEC*)vo,
+                                             cu, starts, tables, bs, max_blocks,
+                                             row_bytes / (int64_t)sizeof(VEC), status);
+  return cudaGetLastError();
+}
+
+bool aligned(const void* p, size_t a) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, int* status, int /*items_cap*/,
+                               cudaStream_t stream) {
+  k_plan_varlen<<<1, 1024, 0, stream>>>(m, plan, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
+                                   int32_t num_seqs, int32_t max_blocks, int32_t block_size,
+                                   int64_t num_blocks, int32_t partition_size, int32_t max_parts,
+                                   int check_tables, int* status, cudaStream_t stream) {
+  if (num_seqs <= 0) return cudaSuccess;
+  k_validate_decode<<<num_seqs, 256, 0, stream>>>(seq_lens, block_tables, max_blocks, block_size,
+                                                  num_blocks, partition_size, max_parts,
+                                                  check_tables, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slot_mapping(const int32_t* qsl, const int32_t* positions,
+                                const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                                int32_t max_blocks, int32_t block_size, int64_t num_blocks,
+                                int32_t* slots, int* status, cudaStream_t stream) {
+  if (num_seqs <= 0) return cudaSuccess;
+  k_slot_mapping<<<num_seqs, 256, 0, stream>>>(qsl, positions, block_tables, num_seqs, num_tokens,
+                                               max_blocks, block_size, num_blocks, slots, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                                     const int32_t* slots, int64_t num_tokens, int64_t row_bytes,
+                                     int32_t block_size, int64_t num_blocks, int* status,
+                                     cudaStream_t stream) {
+  if (num_tokens <= 0) return cudaSuccess;
+  const int64_t vgrid = std::min<int64_t>((num_tokens + 255) / 256, 1024);
+  k_validate_slots<<<(unsigned)vgrid, 256, 0, stream>>>(slots, num_tokens,
+                                                        num_blocks * block_size, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (row_bytes % 16 == 0 && aligned(k, 16) && aligned(v, 16) && aligned(k_blocks, 16) &&
+      aligned(v_blocks, 16))
+    return scatter_as<uint4>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, status, stream);
+  if (row_bytes % 4 == 0 && aligned(k, 4) && aligned(v, 4) && aligned(k_blocks, 4) &&
+      aligned(v_blocks, 4))
+    return scatter_as<uint32_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, status,
+                                stream);
+  return scatter_as<uint16_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, status,
+                              stream);
+}
+
+cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, void* v_out,
+                             const int32_t* cu, const int32_t* starts, const int32_t* tables,
+                             int32_t num_seqs, int64_t num_rows, int64_t row_bytes,
+                             int32_t block_size, int64_t num_blocks, int32_t max_blocks,
+                             int* status, cudaStream_t stream) {
+  if (num_seqs <= 0) return cudaSuccess;
+  k_validate_gather<<<num_seqs, 256, 0, stream>>>(cu, starts, tables, num_rows, block_size,
+                                                  num_blocks, max_blocks, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (row_bytes % 16 == 0 && aligned(k_blocks, 16) && aligned(v_blocks, 16) && aligned(k_out, 16) &&
+      aligned(v_out, 16))
+    return gather_as<uint4>(k_blocks, v_blocks, k_out, v_out, cu, starts, tables, num_seqs,
+                            row_bytes, block_size, max_blocks, status, stream);
+  if (row_bytes % 4 == 0 && aligned(k_blocks, 4) && aligned(v_blocks, 4) && aligned(k_out, 4) &&
+      aligned(v_out, 4))
+    return gather_as<uint32_t>(k_blocks, v_blocks, k_out, v_out, cu, starts, tables, num_seqs,
+                               row_bytes, block_size, max_blocks, status, stream);
+  return gather_as<uint16_t>(k_blocks, v_blocks, k_out, v_out, cu, starts, tables, num_seqs,
+                             row_bytes, block_size, max_blocks, status, stream);
+}
+
+}  // namespace pa

@@ -1,0 +1,142 @@
+// k_simt.cu -- the general paged-attention kernel: any mix of fp32 / bf16 for q and the
+// pool, any head size up to 256 and any block size.  One warp serves one (token, head)
+// (or one (sequence, head, partition) in split-KV mode) and walks the visible positions in
+// increasing order through the block table with the per-position online softmax of the
+// TensorSharp ComputeSingleQueryAttention routine: the dot product is spread over the
+// lanes and reduced with shuffles, the running max / denominator / numerator are rescaled
+// when a larger score arrives, and the output is numerator * (1 / denominator).
+//
+// It serves the shapes the tensor-core kernels do not cover (fp32 caches, head sizes other
+// than 64 / 128, block sizes other than 16, GQA groups above 16 in split-KV decode).
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <typename TQ, typename TKV, int DPL>
+__global__ void __launch_bounds__(128) k_simt(const SimtParams p) {
+  if (status_set(p.status)) return;  // no barriers in this kernel: per-warp exit is safe
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  const VarlenMeta& m = p.m;
+  const int H = m.num_heads, D = m.head_dim;
+  int64_t t;
+  int s, h, part = 0, start, end;
+  if (p.split) {
+    const int64_t total = (int64_t)m.num_seqs * H * p.max_parts;
+    if (gw >= total) return;
+    part = (int)(gw % p.max_parts);
+    h = (int)((gw / p.max_parts) % H);
+    s = (int)(gw / ((int64_t)p.max_parts * H));
+    t = s;
+    const int n = m.seq_lens[s];
+    end = n;
+    start = m.window > 0 ? max(0, n - m.window) : 0;
+    start = max(start, part * p.partition_size);
+    end = min(end, (part + 1) * p.partition_size);
+  } else {
+    const int64_t total = m.num_tokens * H;
+    if (gw >= total) return;
+    t = gw / H;
+    h = (int)(gw % H);
+    s = p.plan[kPlanHeaderWords + t];
+    const int pos = m.positions[t];
+    end = m.causal ? pos + 1 : m.seq_lens[s];
+    start = m.window > 0 ? max(0, end - m.window) : 0;
+  }
+  const int g = h / m.group;
+  const TQ* q = reinterpret_cast<const TQ*>(p.q) + (t * H + h) * (int64_t)D;
+  const TKV* kb = reinterpret_cast<const TKV*>(p.k_blocks);
+  const TKV* vb = reinterpret_cast<const TKV*>(p.v_blocks);
+  const int32_t* row = m.block_tables + (int64_t)s * m.max_blocks;
+
+  float qr[DPL], acc[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) {
+    const int d = lane + 32 * i;
+    qr[i] = d < D ? to_f32(q[d]) : 0.f;
+    acc[i] = 0.f;
+  }
+  float mx = -INFINITY, den = 0.f;
+  for (int j = start; j < end; ++j) {
+    const int64_t blk = row[j / m.block_size];
+    const int64_t base = ((blk * m.block_size + j % m.block_size) * m.num_kv_heads + g) * D;
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      const int d = lane + 32 * i;
+      if (d < D) dot += qr[i] * to_f32(kb[base + d]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
+    const float sc = dot * p.scale;
+    if (sc > mx) {
+      const float r = expf(mx - sc);
+      den *= r;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) acc[i] *= r;
+      mx = sc;
+    }
+    const float e = expf(sc - mx);
+    den += e;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      const int d = lane + 32 * i;
+      if (d < D) acc[i] += e * to_f32(vb[base + d]);
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  if (p.split) {
+    const int64_t idx = ((int64_t)s * H + h) * p.max_parts + part;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      const int d = lane + 32 * i;
+      if (d < D) p.tmp_out[idx * D + d] = acc[i] * inv;
+    }
+    if (lane == 0) {
+      p.max_logits[idx] = mx;
+      p.exp_sums[idx] = den;
+    }
+  } else {
+    TQ* out = reinterpret_cast<TQ*>(p.out) + (t * H + h) * (int64_t)D;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      const int d = lane + 32 * i;
+      if (d < D) out[d] = from_f32<TQ>(acc[i] * inv);
+    }
+  }
+}
+
+template <typename TQ, typename TKV>
+cudaError_t launch_dtypes(const SimtParams& p, cudaStream_t stream) {
+  const int64_t warps = p.split ? (int64_t)p.m.num_seqs * p.m.num_heads * p.max_parts
+                                : p.m.num_tokens * p.m.num_heads;
+  if (warps <= 0) return cudaSuccess;
+  const int64_t grid = (warps + 3) / 4;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int D = p.m.head_dim;
+  if (D <= 32)
+    k_simt<TQ, TKV, 1><<<(unsigned)grid, 128, 0, stream>>>(p);
+  else if (D <= 64)
+    k_simt<TQ, TKV, 2><<<(unsigned)grid, 128, 0, stream>>>(p);
+  else if (D <= 128)
+    k_simt<TQ, TKV, 4><<<(unsigned)grid, 128, 0, stream>>>(p);
+  else if (D <= 256)
+    k_simt<TQ, TKV, 8><<<(unsigned)grid, 128, 0, stream>>>(p);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream) {
+  if (p.q_bf16 && p.kv_bf16) return launch_dtypes<__nv_bfloat16, __nv_bfloat16>(p, stream);
+  if (p.q_bf16) return launch_dtypes<__nv_bfloat16, float>(p, stream);
+  if (p.kv_bf16) return launch_dtypes<float, __nv_bfloat16>(p, stream);
+  return launch_dtypes<float, float>(p, stream);
+}
+
+}  // namespace pa

@@ -1,0 +1,450 @@
+// pa_api.cu -- the C ABI of libpa (include/pa.h): argument checks, tensor-map encoding,
+// path selection and kernel launches.  No device memory is allocated here.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "pa_internal.cuh"
+
+// Sticky per-device status word (one copy per device context): the first error a kernel
+// records stays until pa_device_status() reads and clears it.
+__device__ int g_pa_status = 0;
+
+namespace pa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  int* status = nullptr;
+  int sms = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Status-word address and SM count of the current device, looked up once per device with
+// that device current.
+const DeviceState* device_state() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.status) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_status) != cudaSuccess) return nullptr;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return nullptr;
+    d.sms = sms;
+    d.status = static_cast<int*>(p);
+  }
+  return &d;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// TMA descriptor of a bf16 pool [num_blocks, 16, Hkv, D] seen as the 3-D tensor
+// (D, Hkv, num_blocks * 16) with a 64 x 1 x 16 box and the 128-byte swizzle.
+bool pool_map(CUtensorMap* map, const void* base, int64_t num_blocks, int block_size, int hkv,
+              int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)(num_blocks * block_size)};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hkv * d * 2};
+  cuuint32_t box[3] = {64, 1, 16};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool dtype_ok(pa_dtype t) { return t == PA_F32 || t == PA_BF16; }
+int esize(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+
+pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ECUDA; }
+
+int64_t items_cap(int64_t num_tokens, int32_t group, int32_t num_seqs) {
+  return (num_tokens * group + 15) / 16 + num_seqs + 1;
+}
+
+// Fast path of the attention kernels: bf16 q and pool, head size 64 or 128, 16-position
+// blocks, TMA-compatible pool addresses.
+bool mma_path(pa_dtype q_dtype, pa_dtype kv_dtype, int32_t head_dim, int32_t block_size,
+              const void* q, const void* kb, const void* vb, const void* out) {
+  return q_dtype == PA_BF16 && kv_dtype == PA_BF16 && (head_dim == 64 || head_dim == 128) &&
+         block_size == 16 && aligned(kb, 16) && aligned(vb, 16) && aligned(q, 4) &&
+         (out == nullptr || aligned(out, 16));
+}
+
+}  // namespace
+
+int num_sms() {
+  const DeviceState* d = device_state();
+  return d ? d->sms : 0;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_EINVAL: return "PA_EINVAL";
+    case PA_ESHAPE: return "PA_ESHAPE";
+    case PA_EUNSUPPORTED: return "PA_EUNSUPPORTED";
+    case PA_ECUDA: return "PA_ECUDA";
+    case PA_ETIMEOUT: return "PA_ETIMEOUT";
+  }
+  return "PA_UNKNOWN";
+}
+
+pa_status pa_device_status(cudaStream_t stream) {
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  int v = 0;
+  if (cudaMemcpyAsync(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return PA_ECUDA;
+  if (cudaMemsetAsync(d->status, 0, sizeof(int), stream) != cudaSuccess) return PA_ECUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ECUDA;
+  return static_cast<pa_status>(v);
+}
+
+pa_status pa_slot_mapping(const int32_t* query_start_loc, const int32_t* positions,
+                          const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                          int32_t max_blocks_per_seq, int32_t block_size, int64_t num_blocks,
+                          int32_t* slot_mapping, cudaStream_t stream) {
+  if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 0 || num_blocks < 0) return PA_EINVAL;
+  if (block_size <= 0) return PA_ESHAPE;
+  if (num_seqs == 0) return PA_OK;
+  if (!query_start_loc || !positions || !block_tables || !slot_mapping) return PA_EINVAL;
+  if (num_blocks * block_size > INT32_MAX) return PA_EUNSUPPORTED;  // slots are int32
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  return from_cuda(launch_slot_mapping(query_start_loc, positions, block_tables, num_seqs,
+                                       num_tokens, max_blocks_per_seq, block_size, num_blocks,
+                                       slot_mapping, d->status, stream));
+}
+
+pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                               const int32_t* slot_mapping, int64_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int64_t num_blocks, pa_dtype kv_dtype, cudaStream_t stream) {
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return PA_ESHAPE;
+  if (!dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (num_tokens < 0 || num_blocks < 0) return PA_EINVAL;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_blocks || !v_blocks || !slot_mapping) return PA_EINVAL;
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * esize(kv_dtype);
+  return from_cuda(launch_reshape_and_cache(k, v, k_blocks, v_blocks, slot_mapping, num_tokens,
+                                            row_bytes, block_size, num_blocks, d->status, stream));
+}
+
+size_t pa_varlen_forward_workspace_size(int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t max_blocks_per_seq, int32_t block_size) {
+  (void)head_dim;
+  (void)max_blocks_per_seq;
+  (void)block_size;
+  if (num_seqs < 0 || num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+      num_heads % num_kv_heads != 0)
+    return 0;
+  const int64_t group = num_heads / num_kv_heads;
+  const int64_t words = kPlanHeaderWords + ((num_tokens + 1) & ~int64_t(1)) +
+                        2 * items_cap(num_tokens, (int32_t)group, num_seqs);
+  return (size_t)((words * 4 + 255) / 256 * 256);
+}
+
+pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_blocks, void* out,
+                            const int32_t* query_start_loc, const int32_t* seq_lens,
+                            const int32_t* positions, const int32_t* block_tables,
+                            int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int64_t num_blocks, int32_t max_blocks_per_seq, pa_dtype q_dtype,
+                            pa_dtype kv_dtype, float scale, int32_t causal,
+                            int32_t sliding_window, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_heads % num_kv_heads != 0)
+    return PA_ESHAPE;
+  if (!dtype_ok(q_dtype) || !dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (head_dim > 256) return PA_EUNSUPPORTED;
+  if (num_seqs < 0 || num_tokens < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return PA_EINVAL;
+  if (num_tokens > INT32_MAX / 2) return PA_EUNSUPPORTED;
+  if (num_seqs == 0 && num_tokens == 0) return PA_OK;
+  if (!q || !k_blocks || !v_blocks || !out || !query_start_loc || !seq_lens || !positions ||
+      !block_tables || !workspace)
+    return PA_EINVAL;
+  const size_t need = pa_varlen_forward_workspace_size(num_seqs, num_tokens, num_heads,
+                                                       num_kv_heads, head_dim, max_blocks_per_seq,
+                                                       block_size);
+  if (workspace_bytes < need || !aligned(workspace, 256)) return PA_EINVAL;
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+
+  VarlenMeta m;
+  m.query_start_loc = query_start_loc;
+  m.seq_lens = seq_lens;
+  m.positions = positions;
+  m.block_tables = block_tables;
+  m.num_seqs = num_seqs;
+  m.num_tokens = num_tokens;
+  m.num_heads = num_heads;
+  m.num_kv_heads = num_kv_heads;
+  m.group = num_heads / num_kv_heads;
+  m.head_dim = head_dim;
+  m.block_size = block_size;
+  m.num_blocks = num_blocks;
+  m.max_blocks = max_blocks_per_seq;
+  m.causal = causal ? 1 : 0;
+  m.window = sliding_window > 0 ? sliding_window : 0;
+  int32_t* plan = static_cast<int32_t*>(workspace);
+  const int64_t cap = items_cap(num_tokens, m.group, num_seqs);
+
+  cudaError_t e = launch_plan_varlen(m, plan, d->status, (int)cap, stream);
+  if (e != cudaSuccess) return PA_ECUDA;
+
+  if (mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out)) {
+    CUtensorMap tk, tv;
+    if (!pool_map(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) ||
+        !pool_map(&tv, v_blocks, num_blocks, block_size, num_kv_heads, head_dim))
+      return PA_ECUDA;
+    Mma16Params p;
+    std::memset(&p, 0, sizeof p);
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.out = out;
+    p.m = m;
+    p.plan = plan;
+    p.status = d->status;
+    p.scale_log2 = scale * kLog2e;
+    p.wait_limit_ns = kWaitLimitNs;
+    return from_cuda(launch_mma16_varlen(tk, tv, p, head_dim, (int)std::min<int64_t>(cap, 65535),
+                                         stream));
+  }
+  SimtParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k_blocks = k_blocks;
+  p.v_blocks = v_blocks;
+  p.out = out;
+  p.m = m;
+  p.plan = plan;
+  p.status = d->status;
+  p.scale = scale;
+  p.q_bf16 = q_dtype == PA_BF16;
+  p.kv_bf16 = kv_dtype == PA_BF16;
+  return from_cuda(launch_simt(p, stream));
+}
+
+static pa_status splitkv_partials(const void* q, const void* k_blocks, const void* v_blocks,
+                                  float* max_logits, float* exp_sums, float* tmp_out,
+                                  const int32_t* seq_lens, const int32_t* block_tables,
+                                  int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                  int32_t max_blocks_per_seq, int32_t partition_size,
+                                  int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype,
+                                  float scale, int32_t sliding_window, cudaStream_t stream) {
+  if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_heads % num_kv_heads != 0 || partition_size <= 0 || max_num_partitions <= 0)
+    return PA_ESHAPE;
+  if (!dtype_ok(q_dtype) || !dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (head_dim > 256 || partition_size % block_size != 0) return PA_EUNSUPPORTED;
+  if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return PA_EINVAL;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_blocks || !v_blocks || !max_logits || !exp_sums || !tmp_out || !seq_lens ||
+      !block_tables)
+    return PA_EINVAL;
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  cudaError_t e = launch_validate_decode(seq_lens, block_tables, num_seqs, max_blocks_per_seq,
+                                         block_size, num_blocks, partition_size,
+                                         max_num_partitions, 1, d->status, stream);
+  if (e != cudaSuccess) return PA_ECUDA;
+  VarlenMeta m;
+  std::memset(&m, 0, sizeof m);
+  m.seq_lens = seq_lens;
+  m.block_tables = block_tables;
+  m.num_seqs = num_seqs;
+  m.num_tokens = num_seqs;
+  m.num_heads = num_heads;
+  m.num_kv_heads = num_kv_heads;
+  m.group = num_heads / num_kv_heads;
+  m.head_dim = head_dim;
+  m.block_size = block_size;
+  m.num_blocks = num_blocks;
+  m.max_blocks = max_blocks_per_seq;
+  m.causal = 1;
+  m.window = sliding_window > 0 ? sliding_window : 0;
+  if (mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, nullptr) &&
+      m.group <= 16 && aligned(tmp_out, 16)) {
+    CUtensorMap tk, tv;
+    if (!pool_map(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) ||
+        !pool_map(&tv, v_blocks, num_blocks, block_size, num_kv_heads, head_dim))
+      return PA_ECUDA;
+    Mma16Params p;
+    std::memset(&p, 0, sizeof p);
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.m = m;
+    p.status = d->status;
+    p.scale_log2 = scale * kLog2e;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.tmp_out = tmp_out;
+    p.partition_size = partition_size;
+    p.max_parts = max_num_partitions;
+    p.wait_limit_ns = kWaitLimitNs;
+    return from_cuda(launch_mma16_split(tk, tv, p, head_dim, stream));
+  }
+  SimtParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q;
+  p.k_blocks = k_blocks;
+  p.v_blocks = v_blocks;
+  p.m = m;
+  p.status = d->status;
+  p.scale = scale;
+  p.q_bf16 = q_dtype == PA_BF16;
+  p.kv_bf16 = kv_dtype == PA_BF16;
+  p.max_logits = max_logits;
+  p.exp_sums = exp_sums;
+  p.tmp_out = tmp_out;
+  p.partition_size = partition_size;
+  p.max_parts = max_num_partitions;
+  p.split = 1;
+  return from_cuda(launch_simt(p, stream));
+}
+
+static pa_status splitkv_reduce(void* out, const float* max_logits, const float* exp_sums,
+                                const float* tmp_out, const int32_t* seq_lens, int32_t num_seqs,
+                                int32_t num_heads, int32_t head_dim, int32_t partition_size,
+                                int32_t max_num_partitions, pa_dtype out_dtype, bool validate,
+                                cudaStream_t stream) {
+  if (num_heads <= 0 || head_dim <= 0 || partition_size <= 0 || max_num_partitions <= 0)
+    return PA_ESHAPE;
+  if (!dtype_ok(out_dtype)) return PA_EUNSUPPORTED;
+  if (head_dim % 4 != 0 || !aligned(tmp_out, 16) || max_num_partitions > 16384)
+    return PA_EUNSUPPORTED;
+  if (num_seqs < 0) return PA_EINVAL;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !max_logits || !exp_sums || !tmp_out || !seq_lens) return PA_EINVAL;
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  if (validate) {
+    cudaError_t e = launch_validate_decode(seq_lens, nullptr, num_seqs, 0, 1, 0, partition_size,
+                                           max_num_partitions, 0, d->status, stream);
+    if (e != cudaSuccess) return PA_ECUDA;
+  }
+  return from_cuda(launch_splitkv_reduce(out, out_dtype == PA_BF16, max_logits, exp_sums, tmp_out,
+                                         seq_lens, num_seqs, num_heads, head_dim, partition_size,
+                                         max_num_partitions, d->status, stream));
+}
+
+pa_status pa_decode_splitkv_partials(const void* q, const void* k_blocks, const void* v_blocks,
+                                     float* max_logits, float* exp_sums, float* tmp_out,
+                                     const int32_t* seq_lens, const int32_t* block_tables,
+                                     int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                     int32_t max_blocks_per_seq, int32_t partition_size,
+                                     int32_t max_num_partitions, pa_dtype q_dtype,
+                                     pa_dtype kv_dtype, float scale, int32_t sliding_window,
+                                     cudaStream_t stream) {
+  return splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
+                          block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, partition_size, max_num_partitions,
+                          q_dtype, kv_dtype, scale, sliding_window, stream);
+}
+
+pa_status pa_decode_splitkv_reduce(void* out, const float* max_logits, const float* exp_sums,
+                                   const float* tmp_out, const int32_t* seq_lens,
+                                   int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                   int32_t partition_size, int32_t max_num_partitions,
+                                   pa_dtype out_dtype, cudaStream_t stream) {
+  return splitkv_reduce(out, max_logits, exp_sums, tmp_out, seq_lens, num_seqs, num_heads,
+                        head_dim, partition_size, max_num_partitions, out_dtype, true, stream);
+}
+
+pa_status pa_decode_splitkv(const void* q, const void* k_blocks, const void* v_blocks, void* out,
+                            float* max_logits, float* exp_sums, float* tmp_out,
+                            const int32_t* seq_lens, const int32_t* block_tables,
+                            int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                            int32_t max_blocks_per_seq, int32_t partition_size,
+                            int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype,
+                            float scale, int32_t sliding_window, cudaStream_t stream) {
+  if (!out) return PA_EINVAL;
+  if (head_dim % 4 != 0 || !aligned(tmp_out, 16) || max_num_partitions > 16384)
+    return PA_EUNSUPPORTED;
+  pa_status st = splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
+                                  block_tables, num_seqs, num_heads, num_kv_heads, head_dim,
+                                  block_size, num_blocks, max_blocks_per_seq, partition_size,
+                                  max_num_partitions, q_dtype, kv_dtype, scale, sliding_window,
+                                  stream);
+  if (st != PA_OK) return st;
+  return splitkv_reduce(out, max_logits, exp_sums, tmp_out, seq_lens, num_seqs, num_heads,
+                        head_dim, partition_size, max_num_partitions, q_dtype, false, stream);
+}
+
+pa_status pa_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
+                               const float* prefix_lse, const void* suffix_out,
+                               const float* suffix_lse, int64_t num_tokens, int32_t num_heads,
+                               int32_t head_dim, int64_t prefill_tokens_with_context,
+                               pa_dtype dtype, cudaStream_t stream) {
+  if (num_heads <= 0 || head_dim <= 0) return PA_ESHAPE;
+  if (!dtype_ok(dtype)) return PA_EUNSUPPORTED;
+  if (num_tokens < 0) return PA_EINVAL;
+  if (num_tokens == 0) return PA_OK;
+  if (!out || !prefix_out || !prefix_lse || !suffix_out || !suffix_lse) return PA_EINVAL;
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  const int64_t prefix_tokens =
+      prefill_tokens_with_context < 0 ? num_tokens : prefill_tokens_with_context;
+  return from_cuda(launch_merge_attn_states(out, out_lse, prefix_out, prefix_lse, suffix_out,
+                                            suffix_lse, num_tokens, num_heads, head_dim,
+                                            prefix_tokens, dtype == PA_BF16, d->status, stream));
+}
+
+pa_status pa_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, void* v_out,
+                       const int32_t* cu_seq_lens, const int32_t* seq_starts,
+                       const int32_t* block_tables, int32_t num_seqs, int64_t num_out_rows,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int64_t num_blocks, int32_t max_blocks_per_seq, pa_dtype kv_dtype,
+                       cudaStream_t stream) {
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return PA_ESHAPE;
+  if (!dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (num_seqs < 0 || num_out_rows < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
+    return PA_EINVAL;
+  if (num_seqs == 0) return PA_OK;
+  if (!k_blocks || !k_out || !cu_seq_lens || !block_tables) return PA_EINVAL;
+  if ((v_blocks == nullptr) != (v_out == nullptr)) return PA_EINVAL;
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * esize(kv_dtype);
+  return from_cuda(launch_gather_kv(k_blocks, v_blocks, k_out, v_out, cu_seq_lens, seq_starts,
+                                    block_tables, num_seqs, num_out_rows, row_bytes, block_size,
+                                    num_blocks, max_blocks_per_seq, d->status, stream));
+}
+
+}  // extern "C"

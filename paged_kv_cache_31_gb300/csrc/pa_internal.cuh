@@ -1,0 +1,267 @@
+// pa_internal.cuh -- shared device helpers and launch interfaces of libpa (sm_103a only).
+//
+// Nothing here is part of the public ABI (include/pa.h).  The helpers wrap the PTX the
+// kernels use directly: mbarrier phases with bounded waits, 3-D TMA tile loads, ldmatrix,
+// the bf16 m16n8k16 warp MMA, and the device status word.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the driver is reached through cudaGetDriverEntryPoint)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "libpa is written for sm_103a (Blackwell) only"
+#endif
+
+namespace pa {
+
+// ------------------------------------------------------------------------------------------
+// device status word
+
+__device__ __forceinline__ void record_error(int* status, int code) {
+  atomicCAS(status, 0, code);  // the first error wins; later ones keep it
+}
+
+__device__ __forceinline__ bool status_set(const int* status) {
+  return *reinterpret_cast<const volatile int*>(status) != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------------------------------
+// shared memory, mbarriers, TMA
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, for at most `limit_ns` of wall time.
+// Returns false when the limit ran out (the caller records PA_ETIMEOUT and unwinds).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// 3-D tiled TMA load global -> shared, completing `bytes` on `bar`.  c0 is the innermost
+// coordinate; callers keep c0 * sizeof(element) a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int32_t c0,
+                                            int32_t c1, int32_t c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------------------------------------
+// warp-level tensor-core helpers (bf16 m16n8k16, fp32 accumulate)
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32"
+      " {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------------------------------
+// element access for the generic kernels
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not landed by then never will
+
+// ------------------------------------------------------------------------------------------
+// per-call plan kept in the caller's workspace (int32 words)
+//   [0] number of 16-row tile items for the tensor-core kernel
+//   [1..15] reserved
+//   [16, 16 + T) token -> sequence
+//   then int2 items (seq, tile)
+constexpr int kPlanHeaderWords = 16;
+
+struct VarlenMeta {
+  const int32_t* query_start_loc;
+  const int32_t* seq_lens;
+  const int32_t* positions;
+  const int32_t* block_tables;
+  int32_t num_seqs;
+  int64_t num_tokens;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t group;  // num_heads / num_kv_heads
+  int32_t head_dim;
+  int32_t block_size;
+  int64_t num_blocks;
+  int32_t max_blocks;
+  int32_t causal;
+  int32_t window;
+};
+
+struct Mma16Params {
+  const __nv_bfloat16* q;
+  void* out;  // bf16 [T, H, D] (varlen) / [S, H, D]
+  VarlenMeta m;
+  const int32_t* plan;  // varlen: workspace plan; split: nullptr
+  int* status;
+  float scale_log2;  // scale * log2(e)
+  // split-KV partial outputs (mode split)
+  float* max_logits;
+  float* exp_sums;
+  float* tmp_out;
+  int32_t partition_size;
+  int32_t max_parts;
+  uint64_t wait_limit_ns;
+};
+
+struct SimtParams {
+  const void* q;
+  const void* k_blocks;
+  const void* v_blocks;
+  void* out;
+  VarlenMeta m;
+  const int32_t* plan;  // token -> seq at plan + kPlanHeaderWords
+  int* status;
+  float scale;
+  int32_t q_bf16, kv_bf16;
+  // split-KV mode (out unused): one warp per (s, h, p)
+  float* max_logits;
+  float* exp_sums;
+  float* tmp_out;
+  int32_t partition_size;
+  int32_t max_parts;
+  int32_t split;
+};
+
+// ---- launchers (defined next to their kernels) --------------------------------------------
+cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, int* status, int items_cap,
+                               cudaStream_t stream);
+cudaError_t launch_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
+                                   int32_t num_seqs, int32_t max_blocks, int32_t block_size,
+                                   int64_t num_blocks, int32_t partition_size, int32_t max_parts,
+                                   int check_tables, int* status, cudaStream_t stream);
+cudaError_t launch_slot_mapping(const int32_t* qsl, const int32_t* positions,
+                                const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                                int32_t max_blocks, int32_t block_size, int64_t num_blocks,
+                                int32_t* slots, int* status, cudaStream_t stream);
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                                     const int32_t* slots, int64_t num_tokens, int64_t row_bytes,
+                                     int32_t block_size, int64_t num_blocks, int* status,
+                                     cudaStream_t stream);
+cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, void* v_out,
+                             const int32_t* cu, const int32_t* starts, const int32_t* tables,
+                             int32_t num_seqs, int64_t num_rows, int64_t row_bytes,
+                             int32_t block_size, int64_t num_blocks, int32_t max_blocks,
+                             int* status, cudaStream_t stream);
+cudaError_t launch_mma16_varlen(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p,
+                                int head_dim, int items_cap, cudaStream_t stream);
+cudaError_t launch_mma16_split(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p,
+                               int head_dim, cudaStream_t stream);
+cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream);
+cudaError_t launch_splitkv_reduce(void* out, int out_bf16, const float* max_logits,
+                                  const float* exp_sums, const float* tmp_out,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                                  int32_t head_dim, int32_t partition_size, int32_t max_parts,
+                                  int* status, cudaStream_t stream);
+cudaError_t launch_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
+                                     const float* prefix_lse, const void* suffix_out,
+                                     const float* suffix_lse, int64_t num_tokens,
+                                     int32_t num_heads, int32_t head_dim, int64_t prefix_tokens,
+                                     int bf16, int* status, cudaStream_t stream);
+
+int num_sms();  // SM count of the current device (cached)
+
+}  // namespace pa

@@ -1,0 +1,78 @@
+"""The C-ABI library builds, loads on a machine without a GPU, and exports every call that
+include/pa.h declares.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "pa.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_31_gb300 import _build
+
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for want in ("pa_reshape_and_cache", "pa_varlen_forward", "pa_decode_splitkv",
+                 "pa_decode_splitkv_partials", "pa_decode_splitkv_reduce",
+                 "pa_merge_attn_states", "pa_gather_kv", "pa_slot_mapping", "pa_device_status"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_the_header(lib):
+    from paged_kv_cache_31_gb300 import binding
+
+    assert sorted(binding.EXPORTED) == _declared()
+    assert binding.version() >= 100
+    assert binding.status_string(binding.PA_EINVAL) == "PA_EINVAL"
+
+
+def test_host_side_argument_errors_need_no_gpu(lib):
+    """Shape and argument errors are returned before anything touches the device."""
+    from paged_kv_cache_31_gb300 import binding as b
+
+    L = b._lib
+    # heads not a multiple of kv heads
+    st = L.pa_varlen_forward(None, None, None, None, None, None, None, None, 1, 1, 6, 4, 128, 16,
+                             8, 1, b.PA_BF16, b.PA_BF16, 1.0, 1, 0, None, 0, None)
+    assert st == b.PA_ESHAPE
+    # unsupported dtype
+    st = L.pa_varlen_forward(None, None, None, None, None, None, None, None, 1, 1, 8, 4, 128, 16,
+                             8, 1, 7, b.PA_BF16, 1.0, 1, 0, None, 0, None)
+    assert st == b.PA_EUNSUPPORTED
+    # missing pointers
+    st = L.pa_varlen_forward(None, None, None, None, None, None, None, None, 1, 1, 8, 4, 128, 16,
+                             8, 1, b.PA_BF16, b.PA_BF16, 1.0, 1, 0, None, 0, None)
+    assert st == b.PA_EINVAL
+    st = L.pa_reshape_and_cache(None, None, None, None, None, 4, 0, 128, 16, 8, b.PA_BF16, None)
+    assert st == b.PA_ESHAPE
+    st = L.pa_merge_attn_states(None, None, None, None, None, None, 4, 8, 128, -1, b.PA_F32, None)
+    assert st == b.PA_EINVAL
+    st = L.pa_decode_splitkv_partials(None, None, None, None, None, None, None, None, 2, 8, 2, 128,
+                                      16, 64, 8, 500, 4, b.PA_BF16, b.PA_BF16, 1.0, 0, None)
+    assert st == b.PA_EUNSUPPORTED  # partition not a multiple of the block size
+    # empty batches are a no-op
+    assert L.pa_varlen_forward(None, None, None, None, None, None, None, None, 0, 0, 8, 4, 128, 16,
+                               8, 1, b.PA_BF16, b.PA_BF16, 1.0, 1, 0, None, 0, None) == b.PA_OK
+    # workspace size grows with the batch and is 256-byte granular
+    a = b.pa_varlen_forward_workspace_size(4, 27, 4, 2, 64, 4, 16)
+    c = b.pa_varlen_forward_workspace_size(256, 4344, 32, 8, 128, 512, 16)
+    assert a % 256 == 0 and c % 256 == 0 and c > a > 0
