@@ -14,8 +14,9 @@
 // mask to each row's visible range [start, end), scale into the log2 domain, block max via
 // quad shuffles, the online-softmax update m' = max(m, .), alpha = 2^(m - m'),
 // l = alpha l + sum p, O = alpha O + P V (tinyllm section 2.2, applied per 16-key block).
-// P is rounded to bf16 for the PV MMA and l sums those same rounded weights.  At the end the
-// warps' (m, l, O) states are merged in fixed warp order and o = O * (1 / l).
+// P enters the PV MMA as a bf16 hi/lo pair (two MMAs), so the weights keep ~17 bits; l sums
+// the fp32 weights.  At the end the warps' (m, l, O) states are merged in fixed warp order
+// and o = O * (1 / l).
 //
 // Why warp MMA here: these tiles are HBM-bound (one pass over K and V per kv head), so the
 // tensor core only has to take the ~2 G D FMA per key off the FP32 pipe; with G = 8 the FMA
@@ -279,19 +280,19 @@ __global__ void __launch_bounds__(NW * 32, 2)
           sc[nt][2 * r + 1] = exp2f(sc[nt][2 * r + 1] - base);
         }
       }
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
-      pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
-      pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
-      pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
-      {
-        // l sums the bf16-rounded weights that the PV product uses
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(pa);
-        const float2 w0 = __bfloat1622float2(pb[0]), w1 = __bfloat1622float2(pb[1]);
-        const float2 w2 = __bfloat1622float2(pb[2]), w3 = __bfloat1622float2(pb[3]);
-        lrow[0] = lrow[0] * alpha[0] + ((w0.x + w0.y) + (w2.x + w2.y));
-        lrow[1] = lrow[1] * alpha[1] + ((w1.x + w1.y) + (w3.x + w3.y));
+      // P as two bf16 A fragments, hi = bf16(p) and lo = bf16(p - hi): the PV product of
+      // both keeps the weights to ~2^-17 relative, where bf16 P alone can be off by 2^-9 of
+      // |v| when a row sees few keys.
+      uint32_t ph[4], pl[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = sc[i >> 1][(i & 1) * 2], b = sc[i >> 1][(i & 1) * 2 + 1];
+        ph[i] = pack_bf16x2(a, b);
+        const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ph[i]));
+        pl[i] = pack_bf16x2(a - hv.x, b - hv.y);
       }
+      lrow[0] = lrow[0] * alpha[0] + ((sc[0][0] + sc[0][1]) + (sc[1][0] + sc[1][1]));
+      lrow[1] = lrow[1] * alpha[1] + ((sc[0][2] + sc[0][3]) + (sc[1][2] + sc[1][3]));
 #pragma unroll
       for (int j = 0; j < G_::kNT; ++j) {
         o[j][0] *= alpha[0];
@@ -308,8 +309,10 @@ __global__ void __launch_bounds__(NW * 32, 2)
         for (int dd = 0; dd < D / 16; ++dd) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4_trans(vbase + tile_off(key, dd * 2 + (mi >> 1)), b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * dd], pa, b0, b1);
-          mma_bf16_16816(o[2 * dd + 1], pa, b2, b3);
+          mma_bf16_16816(o[2 * dd], ph, b0, b1);
+          mma_bf16_16816(o[2 * dd + 1], ph, b2, b3);
+          mma_bf16_16816(o[2 * dd], pl, b0, b1);
+          mma_bf16_16816(o[2 * dd + 1], pl, b2, b3);
         }
       }
       __syncwarp();

@@ -17,6 +17,10 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kReduceWarps = 8;
 
+// Words of the partition-weight array in the reduce kernel's shared memory, rounded up to
+// a multiple of 4 so that the float4 partial sums after it stay 16-byte aligned.
+__host__ __device__ constexpr int weights_words(int max_parts) { return (max_parts + 3) & ~3; }
+
 __device__ __forceinline__ float part_lse(float m, float l) {
   return (isinf(m) || !(l > 0.f)) ? -INFINITY : m + logf(l);
 }
@@ -28,15 +32,15 @@ __global__ void __launch_bounds__(kReduceWarps * 32)
                      const float* __restrict__ exp_sums, const float* __restrict__ tmp_out,
                      const int32_t* __restrict__ seq_lens, int32_t num_heads, int32_t head_dim,
                      int32_t partition_size, int32_t max_parts, const int* status) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   __shared__ float s_red[kReduceWarps];
   __shared__ int s_skip;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) s_skip = status_set(status);
   __syncthreads();
   if (s_skip) return;
-  float* w = sm;                 // [max_parts]
-  float* part = sm + max_parts;  // [kReduceWarps][D]
+  float* w = sm;                                 // [max_parts]
+  float* part = sm + weights_words(max_parts);  // [kReduceWarps][D], 16-byte aligned
   const int s = blockIdx.x / num_heads, h = blockIdx.x % num_heads;
   const int D = head_dim;
   const int np = (seq_lens[s] + partition_size - 1) / partition_size;
@@ -147,7 +151,8 @@ cudaError_t launch_splitkv_reduce(void* out, int out_bf16, const float* max_logi
                                   int* status, cudaStream_t stream) {
   const int64_t ctas = (int64_t)num_seqs * num_heads;
   if (ctas <= 0) return cudaSuccess;
-  const size_t smem = ((size_t)max_parts + (size_t)kReduceWarps * head_dim) * sizeof(float);
+  const size_t smem =
+      ((size_t)weights_words(max_parts) + (size_t)kReduceWarps * head_dim) * sizeof(float);
   if (out_bf16) {
     auto k = k_splitkv_reduce<__nv_bfloat16>;
     if (smem > 48 * 1024) {
