@@ -129,6 +129,35 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
                             cudaStream_t stream);
 
 /*
+ * pa_varlen_forward_noalloc -- pa_varlen_forward for callers that cannot allocate device
+ * memory.  The pages have no counterpart: it exists for the library's users, not for the
+ * method.  Some callers cannot hand this library a workspace: a host framework that gives an
+ * op only its input and output buffers and owns all other device memory, a runtime whose
+ * allocator is out of reach of the calling code, or a serving step that must not risk the
+ * device synchronisation of cudaMalloc / cudaFree.  This call computes exactly what
+ * pa_varlen_forward computes (same arguments, minus the workspace) and keeps its per-call
+ * plan in a 4 MiB array inside the library, one copy per device, held until the process
+ * exits.  It allocates nothing and calls no allocating routine.
+ *   - The first call on a device looks up that device's copy of the array (with the
+ *     device current); make that first call before capturing the stream into a graph.
+ *   - A batch whose pa_varlen_forward_workspace_size(...) exceeds 4 MiB returns PA_EINVAL
+ *     at once and enqueues nothing.
+ *   - All calls on a device share the array: calls that may overlap on the GPU (different
+ *     streams without ordering between them) race and must not be issued.  Calls on one
+ *     stream are ordered and safe.  Each call writes every word of the array it later reads,
+ *     so nothing has to start at zero.
+ */
+pa_status pa_varlen_forward_noalloc(const void* q, const void* k_blocks, const void* v_blocks,
+                                    void* out, const int32_t* query_start_loc,
+                                    const int32_t* seq_lens, const int32_t* positions,
+                                    const int32_t* block_tables, int32_t num_seqs,
+                                    int64_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                    int32_t max_blocks_per_seq, pa_dtype q_dtype,
+                                    pa_dtype kv_dtype, float scale, int32_t causal,
+                                    int32_t sliding_window, cudaStream_t stream);
+
+/*
  * pa_decode_splitkv_partials -- phase 1 of split-KV decode ("paged_attention_v2_pytorch.py",
  * partition loop).  One query per sequence, q [num_seqs, num_heads, head_dim], at position
  * seq_lens[s] - 1 (causal by construction).  Partition p covers positions

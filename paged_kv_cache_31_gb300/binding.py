@@ -39,6 +39,9 @@ _SIGS = {
     "pa_varlen_forward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
                            _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32, _i32, _vp,
                            _sz, _vp], ctypes.c_int),
+    "pa_varlen_forward_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
+                                   _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32,
+                                   _i32, _vp], ctypes.c_int),
     "pa_decode_splitkv_partials": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                     _i32, _i64, _i32, _i32, _i32, ctypes.c_int, ctypes.c_int, _f32,
                                     _i32, _vp], ctypes.c_int),
@@ -174,6 +177,31 @@ def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, pos
                                   float(scale), int(bool(causal)), int(sliding_window),
                                   _p(workspace), workspace.numel(), _stream(stream)),
            "pa_varlen_forward")
+    return out
+
+
+def pa_varlen_forward_noalloc(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
+                              block_tables, scale, causal=True, sliding_window=0, stream=None):
+    """pa_varlen_forward for callers that cannot allocate: the plan lives in a fixed 4 MiB
+    array inside the library (one per device), so no workspace is passed or allocated.
+    Calls that may overlap on the GPU share that array and must not be issued."""
+    _dev(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions, block_tables)
+    _i32t(query_start_loc, seq_lens, positions, block_tables)
+    if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q and out must be [T, H, D] of one dtype")
+    if k_blocks.shape != v_blocks.shape or k_blocks.dtype != v_blocks.dtype:
+        raise ValueError("k_blocks and v_blocks must match")
+    T, H, D = q.shape
+    NB, bs, Hkv, D2 = k_blocks.shape
+    if D2 != D:
+        raise ValueError("head size differs between q and the pool")
+    _check(_lib.pa_varlen_forward_noalloc(_p(q), _p(k_blocks), _p(v_blocks), _p(out),
+                                          _p(query_start_loc), _p(seq_lens), _p(positions),
+                                          _p(block_tables), query_start_loc.numel() - 1, T, H,
+                                          Hkv, D, bs, NB, block_tables.shape[1], _DT[q.dtype],
+                                          _DT[k_blocks.dtype], float(scale), int(bool(causal)),
+                                          int(sliding_window), _stream(stream)),
+           "pa_varlen_forward_noalloc")
     return out
 
 
