@@ -94,8 +94,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
     n_items = m.num_seqs * p.max_parts;
   } else {
     n_items = p.plan[0];
-    const int64_t tok_words = (m.num_tokens + 1) & ~int64_t(1);
-    items = reinterpret_cast<const int2*>(p.plan + kPlanHeaderWords + tok_words);
+    items = reinterpret_cast<const int2*>(p.plan + p.items_off);
   }
 
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {

@@ -5,6 +5,7 @@
 // call) recorded an error, it writes nothing.  Validation always runs as its own launch
 // before the kernel that writes, so a bad table is found before the first byte of output.
 #include <algorithm>
+#include <climits>
 
 #include "pa_internal.cuh"
 
@@ -48,7 +49,8 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
 //     token -> sequence map;
 //  C. the list of (sequence, 16-row tile) items: a sequence's q_len * G query rows (token
 //     major, head minor within the kv group) are cut into tiles of 16.
-__global__ void __launch_bounds__(1024) k_plan_varlen(VarlenMeta m, int32_t* plan, int* status) {
+__global__ void __launch_bounds__(1024)
+    k_plan_varlen(VarlenMeta m, int32_t* plan, const PlanLayout L, int* status) {
   __shared__ int s_err;
   __shared__ int s_warp[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(1024) k_plan_varlen(VarlenMeta m, int32_t* pla
       for (int t = a + lane; t < b; t += 32) {
         const int32_t pos = m.positions[t];
         bad |= (pos < 0 || pos >= n);
-        plan[kPlanHeaderWords + t] = s;
+        plan[L.tok_off + t] = s;
       }
       if (__any_sync(kFull, bad) && lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
     }
@@ -96,25 +98,53 @@ __global__ void __launch_bounds__(1024) k_plan_varlen(VarlenMeta m, int32_t* pla
     if (tid == 0) {
       if (s_err > 0) record_error(status, s_err);
       plan[0] = 0;
+      plan[1] = 0;
     }
     return;
   }
-  const int64_t tok_words = (m.num_tokens + 1) & ~int64_t(1);  // keep the int2 list 8-byte aligned
-  int2* items = reinterpret_cast<int2*>(plan + kPlanHeaderWords + tok_words);
-  int carry = 0;
+  int2* mma_items = reinterpret_cast<int2*>(plan + L.mma_off);
+  int4* tc_items = reinterpret_cast<int4*>(plan + L.tc_off);
+  const int tok_per_tile = 128 / m.group;  // used only when use_tc (group divides 128)
+  int carry_m = 0, carry_t = 0;
   for (int base = 0; base < m.num_seqs; base += blockDim.x) {
     const int s = base + tid;
-    int cnt = 0;
+    int cm = 0, ct = 0;
     if (s < m.num_seqs) {
       const int64_t rows = (int64_t)(m.query_start_loc[s + 1] - m.query_start_loc[s]) * m.group;
-      cnt = (int)((rows + 15) / 16);
+      if (L.use_tc && rows > L.tc_min_rows)
+        ct = (int)((rows + 127) / 128);
+      else
+        cm = (int)((rows + 15) / 16);
     }
-    int total;
-    const int excl = block_exclusive_scan(cnt, s_warp, &total);
-    for (int i = 0; i < cnt; ++i) items[carry + excl + i] = make_int2(s, i);
-    carry += total;
+    int tot_m, tot_t;
+    const int em = block_exclusive_scan(cm, s_warp, &tot_m);
+    const int et = block_exclusive_scan(ct, s_warp, &tot_t);
+    for (int i = 0; i < cm; ++i) mma_items[carry_m + em + i] = make_int2(s, i);
+    if (ct > 0) {
+      // 128-row tiles, the last one (most keys under a causal mask) first; each carries the
+      // union [lo, hi) of its tokens' visible ranges
+      const int qs = m.query_start_loc[s], qe = m.query_start_loc[s + 1];
+      const int n = m.seq_lens[s];
+      for (int i = 0; i < ct; ++i) {
+        const int qt = ct - 1 - i;
+        const int ta = qs + qt * tok_per_tile, tb = min(qe, ta + tok_per_tile);
+        int lo = INT_MAX, hi = 0;
+        for (int t = ta; t < tb; ++t) {
+          const int e = m.causal ? m.positions[t] + 1 : n;
+          const int b = m.window > 0 ? max(0, e - m.window) : 0;
+          lo = min(lo, b);
+          hi = max(hi, e);
+        }
+        tc_items[carry_t + et + i] = make_int4(s, qt, lo, hi);
+      }
+    }
+    carry_m += tot_m;
+    carry_t += tot_t;
   }
-  if (tid == 0) plan[0] = carry;
+  if (tid == 0) {
+    plan[0] = carry_m;
+    plan[1] = carry_t;
+  }
 }
 
 // Split-KV decode validation: one CTA per sequence.
@@ -279,9 +309,9 @@ bool aligned(const void* p, size_t a) { return p == nullptr || (reinterpret_cast
 
 }  // namespace
 
-cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, int* status, int /*items_cap*/,
-                               cudaStream_t stream) {
-  k_plan_varlen<<<1, 1024, 0, stream>>>(m, plan, status);
+cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, const PlanLayout& L,
+                               int* status, cudaStream_t stream) {
+  k_plan_varlen<<<1, 1024, 0, stream>>>(m, plan, L, status);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,538 @@
+// k_prefill_tc.cu -- paged attention for prefill chunks on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in tensor memory), sm_103a.
+//
+// Work item: (sequence, kv head, 128-row query tile).  The 128 rows are (token, head) pairs of
+// one kv head's GQA group, token-major, so one K/V tile serves all G query heads.  Key tiles
+// are 128 positions = 8 pool blocks, each block fetched by TMA from wherever the block table
+// puts it (two 64-dim boxes of 16 rows per block, 128-byte swizzle); a block past the
+// visible range is fetched at a negative row coordinate, which TMA fills with zeros.
+//
+// One CTA per SM, persistent over items, 6 warps:
+//   warp 0      TMA producer: Q once per item, then K_j and V_j through a 2-stage ring;
+//   warp 1      TMEM owner and MMA issuer (one thread):
+//                 S_j = Q K_j^T      (M 128, N 128, K 128: 8 MMAs, K-major operands)
+//                 O  += P_j V_j      (P as a bf16 hi/lo pair: 16 MMAs, V MN-major)
+//               S is double-buffered in TMEM (columns 0 / 128), O lives in columns 256..383;
+//   warps 2..5  softmax, one query row per thread (TMEM lane = row): mask, row max, exp2,
+//               row sum, P to shared memory, lazy O rescale, and the epilogue
+//               o = O * (1 / l) -> bf16.
+// The online softmax follows the per-tile update of the tinyllm decode page (section 2.2)
+// with one change that leaves the result unchanged: the reference max m is only moved (and
+// O, l rescaled by 2^(m_old - m_new)) when a tile's max exceeds it by more than 8 (log2
+// units), so the weights stay <= 2^8 and most tiles need no O rescale.
+//
+// Every mbarrier wait is bounded; a wait that runs out records PA_ETIMEOUT, raises an abort
+// flag that makes the other roles unwind, and the CTA still frees its tensor memory.
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kBM = 128;          // query rows per tile
+constexpr int kBN = 128;          // keys per tile (8 blocks of 16)
+constexpr int kD = 128;           // head size on this path
+constexpr int kHalf = 16384;      // one 64-dim half of a 128-row bf16 tile
+constexpr int kTile = 2 * kHalf;  // 128 x 128 bf16
+constexpr int kStages = 2;
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;
+constexpr int kOffV = kOffK + kStages * kTile;
+constexpr int kOffPh = kOffV + kStages * kTile;
+constexpr int kOffPl = kOffPh + kTile;
+constexpr int kOffBar = kOffPl + kTile;
+constexpr int kNumBars = 18;
+constexpr int kOffTmem = kOffBar + kNumBars * 8;
+constexpr int kOffFlag = kOffTmem + 16;
+constexpr int kSmemBytes = kOffFlag + 16 + 1024;  // + slack to align the base to 1024
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;
+
+// barrier indices
+enum {
+  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 4, B_VFULL = 6, B_VEMPTY = 8, B_SFULL = 10,
+  B_SFREE = 12, B_PFULL = 14, B_ODONE = 15, B_OFREE = 16, B_FIN = 17
+};
+
+// ---- tcgen05 / TMEM wrappers -----------------------------------------------------------------
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+// Wait for this thread's outstanding TMEM loads; the register operands tie the loaded values
+// to the wait so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+        "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+        "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]),
+        "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]),
+        "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+      :
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (canonical layouts of 8-row, 1024-byte
+// atoms).  K-major: rows of 128 B, 8-row groups `sbo` apart.  MN-major: 64-element MN blocks
+// `lbo` apart, 8-row K groups `sbo` apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 operands and an fp32 accumulator.
+constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 1);
+
+// ---- shared state -----------------------------------------------------------------------------
+
+struct Ctx {
+  uint8_t* sm;
+  uint64_t* bar;
+  volatile int* abort;
+  int* status;
+  uint64_t limit;
+};
+
+// Bounded wait that also gives up when another role aborted.
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
+  uint64_t* b = c.bar + idx;
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*c.abort) return false;
+      if (globaltimer_ns() - t0 > c.limit) {
+        record_error(c.status, PA_ETIMEOUT);
+        *c.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+struct Item {
+  int s, kvh, qt, t0, n_tok, n, kv0, ntiles, nblk_vis;
+};
+
+__device__ __forceinline__ Item load_item(const TcParams& p, int idx) {
+  const VarlenMeta& m = p.m;
+  const int4 it = reinterpret_cast<const int4*>(p.plan + p.tc_off)[idx / m.num_kv_heads];
+  Item r;
+  r.s = it.x;
+  r.qt = it.y;
+  r.kvh = idx % m.num_kv_heads;
+  const int tpt = kBM / m.group;
+  const int qs = m.query_start_loc[r.s], qe = m.query_start_loc[r.s + 1];
+  r.t0 = qs + r.qt * tpt;
+  r.n_tok = min(tpt, qe - r.t0);
+  r.n = m.seq_lens[r.s];
+  const int lo = it.z, hi = it.w;
+  r.kv0 = (lo / 16) * 16;
+  r.ntiles = (hi - r.kv0 + kBN - 1) / kBN;
+  r.nblk_vis = (hi + 15) / 16;  // logical blocks [kv0 / 16, nblk_vis) hold visible keys
+  return r;
+}
+
+// ---- roles ------------------------------------------------------------------------------------
+
+__device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
+                         const CUtensorMap* tk, const CUtensorMap* tv, int n_items) {
+  const int lane = threadIdx.x & 31;
+  const VarlenMeta& m = p.m;
+  uint32_t kv = 0, it_cnt = 0;
+  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it_cnt) {
+    const Item I = load_item(p, idx);
+    const int32_t* row = m.block_tables + (int64_t)I.s * m.max_blocks;
+    const int blk0 = I.kv0 / 16;
+    // Q: (D, H, T) tensor, box 64 x G x 128/G
+    bool qok = true;
+    if (lane == 0) {
+      qok = wait_bar(c, B_QEMPTY, (it_cnt & 1u) ^ 1u);
+      if (qok) {
+        mbar_arrive_expect_tx(c.bar + B_QFULL, kTile);
+        tma_load_3d(c.sm + kOffQ, tq, 0, I.kvh * m.group, I.t0, c.bar + B_QFULL);
+        tma_load_3d(c.sm + kOffQ + kHalf, tq, 64, I.kvh * m.group, I.t0, c.bar + B_QFULL);
+      }
+    }
+    if (!__shfl_sync(kFull, (int)qok, 0)) return;
+    int next_id = (lane < 8 && blk0 + lane < I.nblk_vis) ? row[blk0 + lane] : -1;
+    for (int j = 0; j < I.ntiles; ++j, ++kv) {
+      const int id = next_id;
+      if (j + 1 < I.ntiles) {  // prefetch the next tile's block ids
+        const int lb = blk0 + 8 * (j + 1) + lane;
+        next_id = (lane < 8 && lb < I.nblk_vis) ? row[lb] : -1;
+      }
+      int ids[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) ids[b] = __shfl_sync(kFull, id, b);
+      bool ok = true;
+      if (lane == 0) {
+        const uint32_t st = kv % kStages, ph = (kv / kStages) & 1u;
+        ok = wait_bar(c, B_KEMPTY + st, ph ^ 1u);
+        if (ok) {
+          mbar_arrive_expect_tx(c.bar + B_KFULL + st, kTile);
+          uint8_t* dst = c.sm + kOffK + st * kTile;
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const int r = ids[b] >= 0 ? ids[b] * 16 : -16;
+            tma_load_3d(dst + b * 2048, tk, 0, I.kvh, r, c.bar + B_KFULL + st);
+            tma_load_3d(dst + kHalf + b * 2048, tk, 64, I.kvh, r, c.bar + B_KFULL + st);
+          }
+          ok = wait_bar(c, B_VEMPTY + st, ph ^ 1u);
+        }
+        if (ok) {
+          mbar_arrive_expect_tx(c.bar + B_VFULL + st, kTile);
+          uint8_t* dst = c.sm + kOffV + st * kTile;
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const int r = ids[b] >= 0 ? ids[b] * 16 : -16;
+            tma_load_3d(dst + b * 2048, tv, 0, I.kvh, r, c.bar + B_VFULL + st);
+            tma_load_3d(dst + kHalf + b * 2048, tv, 64, I.kvh, r, c.bar + B_VFULL + st);
+          }
+        }
+      }
+      if (!__shfl_sync(kFull, (int)ok, 0)) return;
+    }
+  }
+}
+
+__device__ void mma_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
+  const uint32_t sm = smem_u32(c.sm);
+  uint32_t kv = 0, sc = 0, pv = 0, it_cnt = 0;
+  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it_cnt) {
+    const Item I = load_item(p, idx);
+    if (!wait_bar(c, B_QFULL, it_cnt & 1u)) return;
+    auto issue_pv = [&](int jj) -> bool {
+      if (jj == 0 && !wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u)) return false;
+      if (!wait_bar(c, B_PFULL, pv & 1u)) return false;
+      const uint32_t kvj = kv + jj, st = kvj % kStages;
+      if (!wait_bar(c, B_VFULL + st, (kvj / kStages) & 1u)) return false;
+      tc_fence_after();
+      const uint32_t vb = sm + kOffV + st * kTile;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma(tmem + kColO, sdesc(sm + kOffPh + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
+               sdesc(vb + kk * 2048, kHalf, 1024), kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma(tmem + kColO, sdesc(sm + kOffPl + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
+               sdesc(vb + kk * 2048, kHalf, 1024), kIdescPV, 1u);
+      tc_commit(c.bar + B_ODONE);
+      tc_commit(c.bar + B_VEMPTY + st);
+      ++pv;
+      return true;
+    };
+    for (int j = 0; j < I.ntiles; ++j) {
+      const uint32_t kvj = kv + j, st = kvj % kStages;
+      const uint32_t s = sc + j, b = s & 1u;
+      if (!wait_bar(c, B_KFULL + st, (kvj / kStages) & 1u)) return;
+      if (!wait_bar(c, B_SFREE + b, ((s >> 1) & 1u) ^ 1u)) return;
+      tc_fence_after();
+      const uint32_t kb = sm + kOffK + st * kTile;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma(tmem + b * 128, sdesc(sm + kOffQ + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
+               sdesc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), kIdescQK,
+               kk > 0 ? 1u : 0u);
+      tc_commit(c.bar + B_SFULL + b);
+      tc_commit(c.bar + B_KEMPTY + st);
+      if (j == I.ntiles - 1) tc_commit(c.bar + B_QEMPTY);
+      if (j >= 1 && !issue_pv(j - 1)) return;
+    }
+    if (!issue_pv(I.ntiles - 1)) return;
+    kv += I.ntiles;
+    sc += I.ntiles;
+  }
+}
+
+__device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
+  const VarlenMeta& m = p.m;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = 32 * (warp & 3) + lane;  // this thread's query row == TMEM lane
+  const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
+  const int tid128 = threadIdx.x - 64;  // 0..127 across the four softmax warps
+  uint8_t* ph_row = c.sm + kOffPh + r * 128;
+  uint8_t* pl_row = c.sm + kOffPl + r * 128;
+  uint32_t kv = 0, sc = 0, pv = 0;
+  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
+    const Item I = load_item(p, idx);
+    const int tl = r / m.group;
+    const bool valid = tl < I.n_tok;
+    const int t = I.t0 + (valid ? tl : 0);
+    const int h = I.kvh * m.group + r % m.group;
+    int start = 0, end = 0;
+    if (valid) {
+      const int pos = m.positions[t];
+      end = m.causal ? pos + 1 : I.n;
+      start = m.window > 0 ? max(0, end - m.window) : 0;
+    }
+    // the sequence's last block is partly unwritten past n: which tile / block holds it
+    const int last_blk = (I.n - 1) / 16;
+    const int fix_rel = last_blk * 16 - I.kv0;  // offset of that block inside the item's keys
+    const bool need_fix = (I.n % 16) != 0 && last_blk < I.nblk_vis && fix_rel >= 0;
+    const int fix_tile = need_fix ? fix_rel / kBN : -1;
+
+    float m_ref = -INFINITY, l = 0.f;
+    for (int j = 0; j < I.ntiles; ++j) {
+      const uint32_t s = sc + j, b = s & 1u;
+      if (!__all_sync(kFull, wait_bar(c, B_SFULL + b, (s >> 1) & 1u))) return;
+      tc_fence_after();
+      float x[128];
+      {
+        uint32_t v[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_addr + b * 128 + q * 32, v[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_wait_ld(v[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[q * 32 + i] = __uint_as_float(v[q][i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar + B_SFREE + b);
+
+      const int key0 = I.kv0 + j * kBN;
+      if (!valid) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) x[i] = -INFINITY;
+      } else if (key0 >= start && key0 + kBN <= end) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) x[i] *= p.scale_log2;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          x[i] = (key0 + i >= start && key0 + i < end) ? x[i] * p.scale_log2 : -INFINITY;
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mt = fmaxf(mt, x[i]);
+      const float m_new = fmaxf(m_ref, mt);
+      const bool resc = m_new > m_ref + 8.f;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = exp2f(m_ref - m_new);  // 0 when nothing was visible before
+        m_ref = m_new;
+        l *= alpha;
+      }
+      const float base = m_ref == -INFINITY ? 0.f : m_ref;
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        x[i] = exp2f(x[i] - base);
+        rs += x[i];
+      }
+      l += rs;
+
+      // P_{j-1} V_{j-1} done: the P buffer is free and O is stable
+      if (j >= 1 && !__all_sync(kFull, wait_bar(c, B_ODONE, (pv + j - 1) & 1u))) return;
+      if (j >= 1 && __any_sync(kFull, resc)) {
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_addr + kColO + q * 32, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tmem + lane_addr + kColO + q * 32, o);
+        }
+        tmem_wait_st();
+      }
+      if (j == fix_tile) {
+        // zero the V rows of the sequence's last block at positions >= n (never written)
+        const uint32_t kvj = kv + j, st = kvj % kStages;
+        if (!__all_sync(kFull, wait_bar(c, B_VFULL + st, (kvj / kStages) & 1u))) return;
+        const int blk = (fix_rel % kBN) / 16, first = I.n % 16;
+        uint8_t* vt = c.sm + kOffV + st * kTile;
+        const int chunks = (16 - first) * 2 * 8;  // rows x halves x 16-byte chunks
+        for (int i = tid128; i < chunks; i += 128) {
+          const int rr = first + i / 16, half = (i / 8) & 1, ch = i & 7;
+          *reinterpret_cast<uint4*>(vt + half * kHalf + (blk * 16 + rr) * 128 + ch * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      // P as bf16 hi / lo rows, K-major 128-byte swizzle (keys 0..63 in the first atom)
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = x[q * 8 + 2 * e], bb = x[q * 8 + 2 * e + 1];
+          hi[e] = pack_bf16x2(a, bb);
+          const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[e]));
+          lo[e] = pack_bf16x2(a - hv.x, bb - hv.y);
+        }
+        const uint32_t off = (q >> 3) * kHalf + (((q & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(ph_row + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(pl_row + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar + B_PFULL);
+    }
+
+    // epilogue: o = O / l
+    if (!__all_sync(kFull, wait_bar(c, B_ODONE, (pv + I.ntiles - 1) & 1u))) return;
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * m.num_heads + h) * kD;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t o[32];
+      tmem_ld32(tmem + lane_addr + kColO + q * 32, o);
+      tmem_wait_ld(o);
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
+          *reinterpret_cast<uint4*>(dst + q * 32 + i) = w;
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar + B_OFREE);
+    kv += I.ntiles;
+    sc += I.ntiles;
+    pv += I.ntiles;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_prefill(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
+  int* flags = reinterpret_cast<int*>(sm + kOffFlag);  // [0] skip everything, [1] abort
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+    flags[0] = status_set(p.status) ? 1 : 0;
+    flags[1] = 0;
+    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 1, 4, 1};
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, counts[i]);
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+  }
+  fence_mbar_init();
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  Ctx c{sm, bar, reinterpret_cast<volatile int*>(flags + 1), p.status, p.wait_limit_ns};
+  const int n_items = flags[0] ? 0 : p.plan[1] * p.m.num_kv_heads;
+
+  if (warp == 0) {
+    producer(c, p, &tq, &tk, &tv, n_items);
+  } else if (warp == 1) {
+    if ((threadIdx.x & 31) == 0) {
+      mma_issuer(c, p, tmem, n_items);
+      // every MMA issued above has completed before the tensor memory is released
+      tc_commit(bar + B_FIN);
+      uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar + B_FIN, 0) && globaltimer_ns() - t0 < 1000000000ull) {
+      }
+    }
+    __syncwarp();
+  } else {
+    softmax_role(c, p, tmem, n_items);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const TcParams& p, int grid, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  cudaError_t e =
+      cudaFuncSetAttribute(k_tc_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  k_tc_prefill<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -74,15 +75,37 @@ bool pool_map(CUtensorMap* map, const void* base, int64_t num_blocks, int block_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// TMA descriptor of q [T, H, D] bf16 seen as the 3-D tensor (D, H, T): a 64 x G x 128/G box
+// is the 64-dim half of a 128-row query tile whose rows are the G heads of one kv head for
+// 128/G consecutive tokens.
+bool query_map(CUtensorMap* map, const void* q, int64_t num_tokens, int h, int d, int group) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)h, (cuuint64_t)num_tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)h * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tcgen05 prefill kernel can be switched off with PA_DISABLE_TC=1 (the prefill-class
+// sequences then run on the 16-row warp-MMA kernel), for A/B comparisons.
+bool tc_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("PA_DISABLE_TC");
+    return !(v && v[0] == '1');
+  }();
+  return on;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool dtype_ok(pa_dtype t) { return t == PA_F32 || t == PA_BF16; }
 int esize(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
 
 pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ECUDA; }
-
-int64_t items_cap(int64_t num_tokens, int32_t group, int32_t num_seqs) {
-  return (num_tokens * group + 15) / 16 + num_seqs + 1;
-}
 
 // Fast path of the attention kernels: bf16 q and pool, head size 64 or 128, 16-position
 // blocks, TMA-compatible pool addresses.
@@ -172,10 +195,8 @@ size_t pa_varlen_forward_workspace_size(int32_t num_seqs, int64_t num_tokens, in
   if (num_seqs < 0 || num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
       num_heads % num_kv_heads != 0)
     return 0;
-  const int64_t group = num_heads / num_kv_heads;
-  const int64_t words = kPlanHeaderWords + ((num_tokens + 1) & ~int64_t(1)) +
-                        2 * items_cap(num_tokens, (int32_t)group, num_seqs);
-  return (size_t)((words * 4 + 255) / 256 * 256);
+  const PlanLayout L = plan_layout(num_seqs, num_tokens, num_heads / num_kv_heads);
+  return (size_t)((L.words * 4 + 255) / 256 * 256);
 }
 
 pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_blocks, void* out,
@@ -222,27 +243,49 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
   m.causal = causal ? 1 : 0;
   m.window = sliding_window > 0 ? sliding_window : 0;
   int32_t* plan = static_cast<int32_t*>(workspace);
-  const int64_t cap = items_cap(num_tokens, m.group, num_seqs);
+  PlanLayout L = plan_layout(num_seqs, num_tokens, m.group);
+  const bool fast = mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
+  // prefill-class sequences (more than 64 query rows per kv head) go to the tcgen05 kernel:
+  // head size 128 and a GQA group that divides the 128-row tile
+  L.use_tc = fast && head_dim == 128 && m.group <= 128 && (128 % m.group) == 0 &&
+             aligned(q, 16) && tc_enabled();
 
-  cudaError_t e = launch_plan_varlen(m, plan, d->status, (int)cap, stream);
+  cudaError_t e = launch_plan_varlen(m, plan, L, d->status, stream);
   if (e != cudaSuccess) return PA_ECUDA;
 
-  if (mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out)) {
+  if (fast) {
     CUtensorMap tk, tv;
     if (!pool_map(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) ||
         !pool_map(&tv, v_blocks, num_blocks, block_size, num_kv_heads, head_dim))
       return PA_ECUDA;
+    if (L.use_tc) {
+      CUtensorMap tq;
+      if (!query_map(&tq, q, num_tokens, num_heads, head_dim, m.group)) return PA_ECUDA;
+      TcParams tp;
+      std::memset(&tp, 0, sizeof tp);
+      tp.out = out;
+      tp.m = m;
+      tp.plan = plan;
+      tp.tc_off = L.tc_off;
+      tp.status = d->status;
+      tp.scale_log2 = scale * kLog2e;
+      tp.wait_limit_ns = kWaitLimitNs;
+      const int64_t work = L.tc_cap * num_kv_heads;
+      e = launch_tc_prefill(tq, tk, tv, tp, (int)std::min<int64_t>(work, d->sms), stream);
+      if (e != cudaSuccess) return PA_ECUDA;
+    }
     Mma16Params p;
     std::memset(&p, 0, sizeof p);
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.out = out;
     p.m = m;
     p.plan = plan;
+    p.items_off = L.mma_off;
     p.status = d->status;
     p.scale_log2 = scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
-    return from_cuda(launch_mma16_varlen(tk, tv, p, head_dim, (int)std::min<int64_t>(cap, 65535),
-                                         stream));
+    return from_cuda(launch_mma16_varlen(tk, tv, p, head_dim,
+                                         (int)std::min<int64_t>(L.mma_cap, 65535), stream));
   }
   SimtParams p;
   std::memset(&p, 0, sizeof p);

@@ -167,11 +167,35 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not lan
 
 // ------------------------------------------------------------------------------------------
 // per-call plan kept in the caller's workspace (int32 words)
-//   [0] number of 16-row tile items for the tensor-core kernel
-//   [1..15] reserved
-//   [16, 16 + T) token -> sequence
-//   then int2 items (seq, tile)
+//   [0] number of 16-row tile items (decode-class sequences, warp-MMA kernel)
+//   [1] number of 128-row tile items (prefill-class sequences, tcgen05 kernel)
+//   [2..15] reserved
+//   [tok_off, tok_off + T)        token -> sequence
+//   [mma_off, + 2 * mma_cap)      int2 items (seq, 16-row tile)
+//   [tc_off, + 4 * tc_cap)        int4 items (seq, 128-row tile, kv lo, kv hi)
 constexpr int kPlanHeaderWords = 16;
+
+struct PlanLayout {
+  int64_t tok_off, mma_off, tc_off;
+  int64_t mma_cap, tc_cap;
+  int64_t words;
+  int32_t use_tc;       // prefill-class sequences go to the tcgen05 kernel
+  int32_t tc_min_rows;  // a sequence is prefill-class when q_len * G exceeds this
+};
+
+// Layout of the plan for a batch of num_tokens tokens over num_seqs sequences.
+inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t group) {
+  PlanLayout L;
+  L.tok_off = kPlanHeaderWords;
+  L.mma_cap = (num_tokens * group + 15) / 16 + num_seqs + 1;
+  L.tc_cap = (num_tokens * group + 127) / 128 + num_seqs + 1;
+  L.mma_off = (L.tok_off + num_tokens + 3) & ~int64_t(3);
+  L.tc_off = (L.mma_off + 2 * L.mma_cap + 3) & ~int64_t(3);
+  L.words = L.tc_off + 4 * L.tc_cap;
+  L.use_tc = 0;
+  L.tc_min_rows = 64;
+  return L;
+}
 
 struct VarlenMeta {
   const int32_t* query_start_loc;
@@ -196,6 +220,7 @@ struct Mma16Params {
   void* out;  // bf16 [T, H, D] (varlen) / [S, H, D]
   VarlenMeta m;
   const int32_t* plan;  // varlen: workspace plan; split: nullptr
+  int64_t items_off;    // varlen: word offset of the int2 item list in the plan
   int* status;
   float scale_log2;  // scale * log2(e)
   // split-KV partial outputs (mode split)
@@ -226,9 +251,21 @@ struct SimtParams {
   int32_t split;
 };
 
+struct TcParams {
+  void* out;  // bf16 [T, H, D]
+  VarlenMeta m;
+  const int32_t* plan;
+  int64_t tc_off;  // word offset of the int4 item list
+  int* status;
+  float scale_log2;
+  uint64_t wait_limit_ns;
+};
+
 // ---- launchers (defined next to their kernels) --------------------------------------------
-cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, int* status, int items_cap,
-                               cudaStream_t stream);
+cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, const PlanLayout& L,
+                               int* status, cudaStream_t stream);
+cudaError_t launch_tc_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const TcParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
                                    int32_t num_seqs, int32_t max_blocks, int32_t block_size,
                                    int64_t num_blocks, int32_t partition_size, int32_t max_parts,

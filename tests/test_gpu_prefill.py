@@ -1,0 +1,96 @@
+"""GPU parity of prefill chunks, the sequences with more than 64 query rows per kv head that
+run on the tcgen05 / tensor-memory kernel: every GQA group that divides the 128-row tile,
+ragged chunk lengths, prior contexts that leave the first key tile partial, sliding windows,
+non-causal chunks, NaN in never-written slots, and batches mixing them with decode tokens."""
+import pytest
+import torch
+
+from paged_kv_cache_31_gb300 import workloads
+from tests.gpu_helpers import assert_attn_close, oracle_attention
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_31_gb300 import binding
+
+    assert binding.pa_device_status() == binding.PA_OK
+    return binding
+
+
+def _run(pa, w):
+    out = torch.full_like(w.q, float("nan"))
+    pa.pa_varlen_forward(w.q, w.k_blocks, w.v_blocks, out, w.query_start_loc, w.seq_lens,
+                         w.positions, w.block_tables, w.scale, causal=w.causal,
+                         sliding_window=w.sliding_window)
+    assert pa.pa_device_status() == pa.PA_OK
+    return out
+
+
+@pytest.mark.parametrize("H,Hkv", [(8, 8), (16, 8), (32, 8), (64, 8), (32, 2), (64, 2)])
+def test_prefill_gqa_groups(pa, H, Hkv):
+    # chunks after prior contexts of 0, 5, 16, 200 and 1000 positions, lengths not multiples
+    # of the tile, plus two decode tokens
+    prior = [0, 5, 16, 200, 1000, 3000, 40]
+    chunk = [70, 130, 33, 256, 97, 1, 1]
+    w = workloads.build("pre", seq_lens=[p + c for p, c in zip(prior, chunk)], q_lens=chunk,
+                        num_heads=H, num_kv_heads=Hkv, head_dim=128, seed=H + Hkv, device=DEV)
+    out = _run(pa, w)
+    assert_attn_close(out, oracle_attention(w, w.k_blocks.cpu(), w.v_blocks.cpu()),
+                      f"H {H} Hkv {Hkv}")
+
+
+@pytest.mark.parametrize("window,causal", [(64, True), (300, True), (1, True), (0, False),
+                                           (150, False)])
+def test_prefill_windows_and_noncausal(pa, window, causal):
+    prior = [0, 100, 700, 33]
+    chunk = [200, 150, 300, 129]
+    w = workloads.build("prewin", seq_lens=[p + c for p, c in zip(prior, chunk)], q_lens=chunk,
+                        num_heads=32, num_kv_heads=8, head_dim=128, seed=window + 3,
+                        sliding_window=window, causal=causal, device=DEV)
+    out = _run(pa, w)
+    assert_attn_close(out, oracle_attention(w, w.k_blocks.cpu(), w.v_blocks.cpu()),
+                      f"window {window} causal {causal}")
+
+
+def test_prefill_nan_in_unwritten_slots(pa):
+    prior = [3, 250, 40]
+    chunk = [90, 100, 300]
+    w = workloads.build("prenan", seq_lens=[p + c for p, c in zip(prior, chunk)], q_lens=chunk,
+                        num_heads=32, num_kv_heads=8, head_dim=128, seed=77, device=DEV,
+                        extra_table_cols=2)
+    kb, vb = w.k_blocks.clone(), w.v_blocks.clone()
+    used = set()
+    for s, n in enumerate(w.seq_lens_list):
+        for i in range((n + 15) // 16):
+            used.add(int(w.block_tables[s, i]))
+        last = int(w.block_tables[s, (n - 1) // 16])
+        if n % 16:
+            kb[last, n % 16:] = float("nan")
+            vb[last, n % 16:] = float("inf")
+    for b in range(w.num_blocks):  # blocks no table uses
+        if b not in used:
+            kb[b] = float("nan")
+            vb[b] = float("nan")
+    w.k_blocks, w.v_blocks = kb, vb
+    out = _run(pa, w)
+    assert torch.isfinite(out.float()).all()
+    assert_attn_close(out, oracle_attention(w, kb.cpu(), vb.cpu()), "nan tails")
+
+
+def test_prefill_many_chunks_and_decodes(pa):
+    g = torch.Generator().manual_seed(5)
+    prior = [int(x) for x in torch.randint(0, 1500, (12,), generator=g)]
+    chunk = [int(x) for x in torch.randint(17, 400, (12,), generator=g)]
+    dec = [int(x) for x in torch.randint(1, 3000, (20,), generator=g)]
+    w = workloads.build("premix", seq_lens=dec + [p + c for p, c in zip(prior, chunk)],
+                        q_lens=[1] * 20 + chunk, num_heads=32, num_kv_heads=8, head_dim=128,
+                        seed=6, sliding_window=1024, device=DEV)
+    out = _run(pa, w)
+    assert_attn_close(out, oracle_attention(w, w.k_blocks.cpu(), w.v_blocks.cpu()), "mixed")
+    again = _run(pa, w)
+    assert torch.equal(out, again), "prefill path not deterministic"
