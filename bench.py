@@ -1,17 +1,22 @@
 """Benchmark of the batched paged-attention hot path on GB300.
 
 One step = one pass of the whole path over one batch resident in HBM:
-slot mapping -> scatter of the step's new K/V rows into the paged pool -> varlen paged
-attention (validation + plan, then the attention kernel).  The default workload is the
-64-sequence decode batch with the Llama-3-8B attention shape (H 32, Hkv 8, D 128, bf16,
-contexts U{512..4096}); its K/V (~600 MB per step) is larger than L2, so no flush is needed.
+slot mapping -> scatter of the step's new K/V rows into the paged pool -> attention
+(varlen: validation + plan, the tcgen05 prefill kernel for prefill chunks and the warp-MMA
+kernel for decode tokens; split-KV: validation, partials, log-sum-exp reduction).  The
+default workload is the 64-sequence decode batch with the Llama-3-8B attention shape
+(H 32, Hkv 8, D 128, bf16, contexts U{512..4096}); its K/V (~600 MB per step) is larger
+than L2, so no flush is needed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2|3|4|5] [--impl reference]
 
-Prints one JSON line.  `value` is whole-job KV GB/s (algorithmic K/V bytes the attention
-reads per step, summed over ranks, divided by the slowest rank's time).  With --gpus N > 1
-(under torchrun) every rank runs an independent replica of the batch ("replicas only": the
-path needs no exchange between GPUs).  --impl reference times the CPU oracle instead.
+Prints one JSON line.  `value` is whole-job K/V GB/s (algorithmic K/V bytes the attention
+reads per step, summed over ranks, divided by the slowest rank's time).  The line also
+carries secondary per-class measurements of the other workloads (prefill-chunk TFLOP/s of
+the mixed batch against the bf16 tensor peak, its decode GB/s, split-KV and shared-prefix
+GB/s) unless --no-secondary.  With --gpus N > 1 (under torchrun) every rank runs an
+independent replica ("replicas only": the path needs no exchange between GPUs).
+--impl reference times the CPU oracle instead.
 """
 from __future__ import annotations
 
@@ -28,7 +33,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode KV GB/s (% HBM peak); mixed-batch prefill TFLOP/s; tokens/s"
-KERNEL_SOURCES = {"k_mma16": "paged_kv_cache_31_gb300/csrc/k_decode_mma.cu"}
+KERNEL_SOURCES = {"k_mma16": "paged_kv_cache_31_gb300/csrc/k_decode_mma.cu",
+                  "k_tc_prefill": "paged_kv_cache_31_gb300/csrc/k_prefill_tc.cu"}
 
 
 def parse():
@@ -42,6 +48,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-time budget of the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--secondary-steps", type=int, default=30)
     return ap.parse_args()
 
 
@@ -74,36 +82,44 @@ def aggregate(local_ms: float, units_per_rank: float, world: int, group=None):
 # workload accounting (algorithmic units, independent of the kernels)
 
 
-def kv_bytes(w) -> int:
-    """K and V bytes the attention must read: every visible (position, kv head) row once."""
-    esz = 2 if w.dtype.__repr__().endswith("bfloat16") else 4
-    row = w.num_kv_heads * w.head_dim * esz * 2
-    total = 0
+def _ranges(w):
     qsl = w.query_start_loc.cpu().tolist()
     pos = w.positions.cpu().tolist()
     for s, n in enumerate(w.seq_lens_list):
-        lo, hi = None, 0
         for t in range(qsl[s], qsl[s + 1]):
             e = pos[t] + 1 if w.causal else n
             b = max(0, e - w.sliding_window) if w.sliding_window > 0 else 0
-            lo = b if lo is None else min(lo, b)
-            hi = max(hi, e)
-        if lo is not None:
-            total += (hi - lo) * row
-    return total
+            yield s, b, e
+
+
+def kv_bytes(w) -> int:
+    """K and V bytes the attention must read: every visible (position, kv head) row once per
+    sequence (the union of its tokens' visible ranges)."""
+    esz = 2 if str(w.dtype).endswith("bfloat16") else 4
+    row = w.num_kv_heads * w.head_dim * esz * 2
+    span = {}
+    for s, b, e in _ranges(w):
+        lo, hi = span.get(s, (b, e))
+        span[s] = (min(lo, b), max(hi, e))
+    return sum((hi - lo) * row for lo, hi in span.values())
 
 
 def attn_flops(w) -> int:
     """4 * D * H per visible (query token, key) pair: QK^T and PV multiply-adds."""
-    vis = 0
-    qsl = w.query_start_loc.cpu().tolist()
-    pos = w.positions.cpu().tolist()
-    for s, n in enumerate(w.seq_lens_list):
-        for t in range(qsl[s], qsl[s + 1]):
-            e = pos[t] + 1 if w.causal else n
-            b = max(0, e - w.sliding_window) if w.sliding_window > 0 else 0
-            vis += e - b
-    return 4 * w.head_dim * w.num_heads * vis
+    return 4 * w.head_dim * w.num_heads * sum(e - b for _, b, e in _ranges(w))
+
+
+def launches(w, varlen: bool) -> int:
+    """Kernels of the library launched by one step: slot mapping, slot check and scatter,
+    then validate+plan, the tcgen05 kernel when a sequence can exceed 64 query rows per kv
+    head (the library's own rule) and the warp-MMA kernel; or, split-KV, validation,
+    partials and reduction."""
+    if not varlen:
+        return 3 + 3
+    T, S, G = w.num_tokens, w.num_seqs, w.group
+    tc = str(w.dtype).endswith("bfloat16") and w.head_dim == 128 and 128 % G == 0 and \
+        (T - S + 1) * G > 64
+    return 3 + 2 + (1 if tc else 0)
 
 
 # ------------------------------------------------------------------------------------------
@@ -115,9 +131,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index):
         self.index = index
         self.proc = None
+        self.out = ""
 
     def __enter__(self):
         try:
@@ -169,8 +186,10 @@ def measured_peaks():
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return d.get("hbm_gbs"), "measured"
-    return 6800.0, "fallback"
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "kind": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "kind": "fallback"}
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -213,9 +232,7 @@ def time_oracle(w, budget_s: float):
     return el / n, n, oracle.num_threads()
 
 
-def run_reference(args, w, rank):
-    if rank != 0:
-        return
+def run_reference(args, w):
     per, n, cores = time_oracle(w, max(args.cpu_seconds, 1.0))
     kvb = kv_bytes(w)
     value = kvb / per / 1e9
@@ -236,6 +253,134 @@ def run_reference(args, w, rank):
 # the GPU arm
 
 
+class Runner:
+    """Device buffers of one workload and the library calls of its step."""
+
+    def __init__(self, pa, w):
+        import torch
+
+        self.pa, self.w = pa, w
+        self.varlen = not w.partition_size
+        self.out = torch.empty_like(w.q)
+        self.slots = torch.empty(w.num_tokens, dtype=torch.int32, device=w.q.device)
+        self.ws = pa.workspace_for(w.q, w.k_blocks, w.query_start_loc, w.block_tables)
+        if not self.varlen:
+            S, H, D, P = w.num_seqs, w.num_heads, w.head_dim, w.max_partitions()
+            self.ml = torch.empty((S, H, P), device=w.q.device)
+            self.es = torch.empty((S, H, P), device=w.q.device)
+            self.to = torch.empty((S, H, P, D), device=w.q.device)
+
+    def cache(self, m=None):
+        w, pa = self.w, self.pa
+        m = m or {}
+        pa.pa_slot_mapping(m.get("query_start_loc", w.query_start_loc),
+                           m.get("positions", w.positions), m.get("block_tables", w.block_tables),
+                           w.block_size, w.num_blocks, out=self.slots)
+        pa.pa_reshape_and_cache(m.get("k_new", w.k_new), m.get("v_new", w.v_new), w.k_blocks,
+                                w.v_blocks, self.slots)
+
+    def attention(self, m=None):
+        w, pa = self.w, self.pa
+        m = m or {}
+        q = m.get("q", w.q)
+        if self.varlen:
+            pa.pa_varlen_forward(q, w.k_blocks, w.v_blocks, self.out,
+                                 m.get("query_start_loc", w.query_start_loc),
+                                 m.get("seq_lens", w.seq_lens), m.get("positions", w.positions),
+                                 m.get("block_tables", w.block_tables), w.scale, causal=w.causal,
+                                 sliding_window=w.sliding_window, workspace=self.ws)
+        else:
+            pa.pa_decode_splitkv(q, w.k_blocks, w.v_blocks, self.out, self.ml, self.es, self.to,
+                                 m.get("seq_lens", w.seq_lens),
+                                 m.get("block_tables", w.block_tables), w.scale,
+                                 w.partition_size, w.sliding_window)
+
+    def step(self, m=None):
+        self.cache(m)
+        self.attention(m)
+
+
+def time_calls(fn, n, stream):
+    import torch
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def secondary(pa, dev, args, peaks, stream):
+    """Per-class measurements of the mixed batch (prefill chunks alone: TFLOP/s of the
+    tcgen05 path; decode tokens alone: K/V GB/s), the long-context split-KV batch and the
+    shared-prefix fork batch."""
+    import torch
+
+    from paged_kv_cache_31_gb300 import workloads
+
+    res = {}
+    n = args.secondary_steps
+    w3 = workloads.named(3, seed=args.seed, device=dev)
+    r3 = Runner(pa, w3)
+    for _ in range(3):
+        r3.step()
+    full_ms = time_calls(r3.step, n, stream)
+    dec = [s for s, q in enumerate(w3.q_lens_list) if q == 1]
+    pre = [s for s, q in enumerate(w3.q_lens_list) if q > 1]
+    wp, wd = workloads.subset(w3, pre, "prefill-chunks"), workloads.subset(w3, dec, "decode")
+    rp, rd = Runner(pa, wp), Runner(pa, wd)
+    for _ in range(3):
+        rp.attention()
+        rd.attention()
+    p_ms = time_calls(rp.attention, n, stream)
+    d_ms = time_calls(rd.attention, n, stream)
+    fl, kvd = attn_flops(wp), kv_bytes(wd)
+    res["mixed"] = {
+        "workload": w3.name, "tokens_per_s": w3.num_tokens / (full_ms * 1e-3),
+        "ms_per_step": full_ms,
+        "prefill": {"tokens": wp.num_tokens, "flops": fl, "ms": p_ms,
+                    "tflops": fl / (p_ms * 1e-3) / 1e12,
+                    "frac_of_bf16_peak": fl / (p_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                    "bound": "tensor", "peak_tflops": peaks["bf16_tflops"],
+                    "traffic": ncu_traffic("k_tc_prefill", wp.name)},
+        "decode": {"tokens": wd.num_tokens, "kv_bytes": kvd, "ms": d_ms,
+                   "gbs": kvd / (d_ms * 1e-3) / 1e9,
+                   "frac_of_hbm": kvd / (d_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+    }
+    assert pa.pa_device_status() == pa.PA_OK
+    del w3, r3, wp, wd, rp, rd
+    torch.cuda.empty_cache()
+
+    w4 = workloads.named(4, seed=args.seed, device=dev)
+    r4 = Runner(pa, w4)
+    for _ in range(3):
+        r4.attention()
+    ms4 = time_calls(r4.attention, max(5, n // 3), stream)
+    kv4 = kv_bytes(w4)
+    res["splitkv"] = {"workload": w4.name, "kv_bytes": kv4, "ms": ms4,
+                      "gbs": kv4 / (ms4 * 1e-3) / 1e9,
+                      "frac_of_hbm": kv4 / (ms4 * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    assert pa.pa_device_status() == pa.PA_OK
+    del w4, r4
+    torch.cuda.empty_cache()
+
+    w5 = workloads.named(5, seed=args.seed, device=dev)
+    r5 = Runner(pa, w5)
+    for _ in range(3):
+        r5.attention()
+    ms5 = time_calls(r5.attention, n, stream)
+    kv5 = kv_bytes(w5)
+    res["shared_prefix"] = {"workload": w5.name, "logical_kv_bytes": kv5, "ms": ms5,
+                            "logical_gbs": kv5 / (ms5 * 1e-3) / 1e9,
+                            "tokens_per_s": w5.num_tokens / (ms5 * 1e-3)}
+    assert pa.pa_device_status() == pa.PA_OK
+    del w5, r5
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -245,8 +390,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            w = workloads.named(args.config, seed=args.seed, device="cpu")
-            run_reference(args, w, rank)
+            run_reference(args, workloads.named(args.config, seed=args.seed, device="cpu"))
         return
 
     torch.cuda.set_device(local)
@@ -258,32 +402,20 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     from paged_kv_cache_31_gb300 import binding as pa
 
+    peaks = measured_peaks()
     w = workloads.named(args.config, seed=args.seed, device=dev)
     kvb = kv_bytes(w)
     flops = attn_flops(w)
     T = w.num_tokens
-    ws = pa.workspace_for(w.q, w.k_blocks, w.query_start_loc, w.block_tables)
-    kb, vb = w.k_blocks, w.v_blocks
-    out = torch.empty_like(w.q)
-    slots = torch.empty(T, dtype=torch.int32, device=dev)
+    run = Runner(pa, w)
     stream = torch.cuda.current_stream()
-
-    def step():
-        pa.pa_slot_mapping(w.query_start_loc, w.positions, w.block_tables, w.block_size,
-                           w.num_blocks, out=slots)
-        pa.pa_reshape_and_cache(w.k_new, w.v_new, kb, vb, slots)
-        pa.pa_varlen_forward(w.q, kb, vb, out, w.query_start_loc, w.seq_lens, w.positions,
-                             w.block_tables, w.scale, causal=w.causal,
-                             sliding_window=w.sliding_window, workspace=ws)
-
-    launches_per_step = 5  # slot map, slot check, scatter, validate+plan, attention
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
     for _ in range(max(3, args.warmup)):
-        step()
+        run.step()
     torch.cuda.synchronize()
     assert pa.pa_device_status() == pa.PA_OK
 
@@ -295,30 +427,14 @@ def main():
         # ---- whole step, inputs resident in HBM
         barrier()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
+        step_ms = time_calls(run.step, args.steps, stream)
         barrier()
-        step_ms = e0.elapsed_time(e1) / args.steps
-
-        # ---- the attention call alone (validate+plan and the attention kernel)
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(args.steps):
-            pa.pa_varlen_forward(w.q, kb, vb, out, w.query_start_loc, w.seq_lens, w.positions,
-                                 w.block_tables, w.scale, causal=w.causal,
-                                 sliding_window=w.sliding_window, workspace=ws)
-        a1.record(stream)
-        torch.cuda.synchronize()
-        attn_ms = a0.elapsed_time(a1) / args.steps
+        # ---- the attention call alone (the dominant kernels)
+        attn_ms = time_calls(run.attention, args.steps, stream)
 
         # ---- end to end through the public API with host buffers
-        host = {k: getattr(w, k).cpu().pin_memory()
-                for k in ("q", "k_new", "v_new", "query_start_loc", "seq_lens", "positions",
-                          "block_tables")}
+        names = ["q", "k_new", "v_new", "query_start_loc", "seq_lens", "positions", "block_tables"]
+        host = {k: getattr(w, k).cpu().pin_memory() for k in names}
         dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
         hout = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -328,14 +444,8 @@ def main():
         def e2e_step():
             for k, v in host.items():
                 dbuf[k].copy_(v, non_blocking=True)
-            pa.pa_slot_mapping(dbuf["query_start_loc"], dbuf["positions"], dbuf["block_tables"],
-                               w.block_size, w.num_blocks, out=slots)
-            pa.pa_reshape_and_cache(dbuf["k_new"], dbuf["v_new"], kb, vb, slots)
-            pa.pa_varlen_forward(dbuf["q"], kb, vb, out, dbuf["query_start_loc"],
-                                 dbuf["seq_lens"], dbuf["positions"], dbuf["block_tables"],
-                                 w.scale, causal=w.causal, sliding_window=w.sliding_window,
-                                 workspace=ws)
-            hout.copy_(out, non_blocking=True)
+            run.step(dbuf)
+            hout.copy_(run.out, non_blocking=True)
 
         for _ in range(3):
             e2e_step()
@@ -348,13 +458,14 @@ def main():
         e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
         barrier()
     assert pa.pa_device_status() == pa.PA_OK, "device status set during the timed region"
+    clocks = sampler.summary()
 
     step_ms, value = aggregate(step_ms, kvb / 1e9, world, group)
     e2e_ms, e2e_value = aggregate(e2e_ms, kvb / 1e9, world, group)
     if rank != 0:
         return
-    peak, peak_kind = measured_peaks()
     achieved = kvb / (attn_ms * 1e-3) / 1e9
+    kernel = "k_mma16" if run.varlen else "k_mma16"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
@@ -367,16 +478,18 @@ def main():
                    "l2": f"inputs larger than L2 ({kvb / 1e6:.0f} MB of K/V read per step)",
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": T * world / (step_ms * 1e-3),
-        "attn_tflops": flops / (attn_ms * 1e-3) / 1e12,
-        "clocks": sampler.summary(),
+        "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic("k_mma16", w.name),
-                     "kernel": "pa_varlen_forward (validate+plan, k_mma16)",
-                     "peak_kind": f"{peak_kind} hbm_gbs", "ms_per_launch": attn_ms},
+        "gpu_launches": launches(w, run.varlen) * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic(kernel, w.name),
+                     "kernel": "attention call (validate+plan, attention kernels)",
+                     "peak_kind": f"{peaks['kind']} hbm_gbs (copy)", "ms_per_launch": attn_ms},
     }
+    if not args.no_secondary:
+        line["secondary"] = secondary(pa, dev, args, peaks, stream)
     if not args.no_cpu_baseline:
         per, n, cores = time_oracle(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": kvb / per / 1e9, "unit": "GB/s", "cores": cores,

@@ -7,15 +7,15 @@
 // puts it (two 64-dim boxes of 16 rows per block, 128-byte swizzle); a block past the
 // visible range is fetched at a negative row coordinate, which TMA fills with zeros.
 //
-// One CTA per SM, persistent over items, 6 warps:
+// One CTA per SM, persistent over items, 10 warps:
 //   warp 0      TMA producer: Q once per item, then K_j and V_j through a 2-stage ring;
 //   warp 1      TMEM owner and MMA issuer (one thread):
 //                 S_j = Q K_j^T      (M 128, N 128, K 128: 8 MMAs, K-major operands)
 //                 O  += P_j V_j      (P as a bf16 hi/lo pair: 16 MMAs, V MN-major)
 //               S is double-buffered in TMEM (columns 0 / 128), O lives in columns 256..383;
-//   warps 2..5  softmax, one query row per thread (TMEM lane = row): mask, row max, exp2,
-//               row sum, P to shared memory, lazy O rescale, and the epilogue
-//               o = O * (1 / l) -> bf16.
+//   warps 2..9  softmax: two threads per query row (TMEM lane = row), one per 64-column
+//               half; mask, row max (combined through shared memory), exp2, row sum, P to
+//               shared memory, lazy O rescale, and the epilogue o = O * (1 / l) -> bf16.
 // The online softmax follows the per-tile update of the tinyllm decode page (section 2.2)
 // with one change that leaves the result unchanged: the reference max m is only moved (and
 // O, l rescaled by 2^(m_old - m_new)) when a tile's max exceeds it by more than 8 (log2
@@ -44,8 +44,11 @@ constexpr int kOffBar = kOffPl + kTile;
 constexpr int kNumBars = 18;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffFlag = kOffTmem + 16;
-constexpr int kSmemBytes = kOffFlag + 16 + 1024;  // + slack to align the base to 1024
-constexpr int kThreads = 192;
+constexpr int kOffXchg = kOffFlag + 16;               // row max / sum exchange, 2 x 128 fp32
+constexpr int kSmemBytes = kOffXchg + 2 * 128 * 4 + 1024;  // + slack to align the base
+static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
+constexpr int kSoftWarps = 8;                           // two column halves x four lane quarters
+constexpr int kThreads = 64 + kSoftWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 
@@ -139,6 +142,13 @@ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
 }
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 1);
+
+// 2^x with the SFU's approximate base-2 exponential (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // ---- shared state -----------------------------------------------------------------------------
 
@@ -303,14 +313,23 @@ __device__ void mma_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n
   }
 }
 
+// Named barrier of the two softmax warps that share 32 query rows (one per column half).
+__device__ __forceinline__ void pair_sync(int quad) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+}
+
 __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
   const VarlenMeta& m = p.m;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = 32 * (warp & 3) + lane;  // this thread's query row == TMEM lane
-  const uint32_t lane_addr = (uint32_t)(32 * (warp & 3)) << 16;
-  const int tid128 = threadIdx.x - 64;  // 0..127 across the four softmax warps
-  uint8_t* ph_row = c.sm + kOffPh + r * 128;
-  uint8_t* pl_row = c.sm + kOffPl + r * 128;
+  const int hf = (warp - 2) >> 2;  // column half of S / P / O this warp handles
+  const int quad = warp & 3;       // TMEM lane quarter this warp may access
+  const int r = 32 * quad + lane;  // this thread's query row == TMEM lane
+  const int col0 = hf * 64;
+  const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
+  const int tid256 = threadIdx.x - 64;  // 0..255 across the softmax warps
+  float* xchg = reinterpret_cast<float*>(c.sm + kOffXchg);  // [half][row]
+  uint8_t* ph_row = c.sm + kOffPh + hf * kHalf + r * 128;   // one 64-key swizzle atom
+  uint8_t* pl_row = c.sm + kOffPl + hf * kHalf + r * 128;
   uint32_t kv = 0, sc = 0, pv = 0;
   for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
     const Item I = load_item(p, idx);
@@ -335,15 +354,15 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       const uint32_t s = sc + j, b = s & 1u;
       if (!__all_sync(kFull, wait_bar(c, B_SFULL + b, (s >> 1) & 1u))) return;
       tc_fence_after();
-      float x[128];
+      float x[64];
       {
-        uint32_t v[4][32];
+        uint32_t v[2][32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_addr + b * 128 + q * 32, v[q]);
+        for (int q = 0; q < 2; ++q) tmem_ld32(tmem + lane_addr + b * 128 + col0 + q * 32, v[q]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_wait_ld(v[q]);
+        for (int q = 0; q < 2; ++q) tmem_wait_ld(v[q]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[q * 32 + i] = __uint_as_float(v[q][i]);
       }
@@ -351,50 +370,57 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar + B_SFREE + b);
 
-      const int key0 = I.kv0 + j * kBN;
-      if (!valid) {
+      // mask the raw scores (scale > 0 on this path, so the max commutes with it); an
+      // invalid row has start == end == 0 and masks everything
+      const int key0 = I.kv0 + j * kBN + col0;
+      if (!(key0 >= start && key0 + 64 <= end)) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) x[i] = -INFINITY;
-      } else if (key0 >= start && key0 + kBN <= end) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) x[i] *= p.scale_log2;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          x[i] = (key0 + i >= start && key0 + i < end) ? x[i] * p.scale_log2 : -INFINITY;
+        for (int i = 0; i < 64; ++i)
+          x[i] = (key0 + i >= start && key0 + i < end) ? x[i] : -INFINITY;
       }
-      float mt = x[0];
+      float mx[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mt = fmaxf(mt, x[i]);
+      for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+      for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+      const float mine = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // the row max over both column halves
+      xchg[hf * 128 + r] = mine;
+      pair_sync(quad);
+      const float mt = fmaxf(mine, xchg[(hf ^ 1) * 128 + r]) * p.scale_log2;
+      pair_sync(quad);  // both read before either writes again
       const float m_new = fmaxf(m_ref, mt);
       const bool resc = m_new > m_ref + 8.f;
       float alpha = 1.f;
       if (resc) {
-        alpha = exp2f(m_ref - m_new);  // 0 when nothing was visible before
+        alpha = fast_exp2(m_ref - m_new);  // 0 when nothing was visible before
         m_ref = m_new;
         l *= alpha;
       }
-      const float base = m_ref == -INFINITY ? 0.f : m_ref;
-      float rs = 0.f;
+      const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
+      float rs[8];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        x[i] = exp2f(x[i] - base);
-        rs += x[i];
+      for (int k = 0; k < 8; ++k) rs[k] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        x[i] = fast_exp2(fmaf(x[i], p.scale_log2, nbase));
+        rs[i & 7] += x[i];
       }
-      l += rs;
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
 
       // P_{j-1} V_{j-1} done: the P buffer is free and O is stable
       if (j >= 1 && !__all_sync(kFull, wait_bar(c, B_ODONE, (pv + j - 1) & 1u))) return;
       if (j >= 1 && __any_sync(kFull, resc)) {
         tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_addr + kColO + q * 32, o);
+          tmem_ld32(tmem + lane_addr + kColO + col0 + q * 32, o);
           tmem_wait_ld(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tmem + lane_addr + kColO + q * 32, o);
+          tmem_st32(tmem + lane_addr + kColO + col0 + q * 32, o);
         }
         tmem_wait_st();
       }
@@ -405,15 +431,15 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
         const int blk = (fix_rel % kBN) / 16, first = I.n % 16;
         uint8_t* vt = c.sm + kOffV + st * kTile;
         const int chunks = (16 - first) * 2 * 8;  // rows x halves x 16-byte chunks
-        for (int i = tid128; i < chunks; i += 128) {
+        for (int i = tid256; i < chunks; i += 256) {
           const int rr = first + i / 16, half = (i / 8) & 1, ch = i & 7;
           *reinterpret_cast<uint4*>(vt + half * kHalf + (blk * 16 + rr) * 128 + ch * 16) =
               make_uint4(0, 0, 0, 0);
         }
       }
-      // P as bf16 hi / lo rows, K-major 128-byte swizzle (keys 0..63 in the first atom)
+      // this half of P as bf16 hi / lo rows (K-major, 128-byte swizzle)
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < 8; ++q) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -422,7 +448,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
           const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[e]));
           lo[e] = pack_bf16x2(a - hv.x, bb - hv.y);
         }
-        const uint32_t off = (q >> 3) * kHalf + (((q & 7) ^ (r & 7)) << 4);
+        const uint32_t off = (uint32_t)((q ^ (r & 7)) << 4);
         *reinterpret_cast<uint4*>(ph_row + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(pl_row + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
@@ -432,15 +458,22 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       if (lane == 0) mbar_arrive(c.bar + B_PFULL);
     }
 
-    // epilogue: o = O / l
+    // epilogue: o = O / l, with l summed over both column halves
+    {
+      xchg[hf * 128 + r] = l;
+      pair_sync(quad);
+      l += xchg[(hf ^ 1) * 128 + r];
+      pair_sync(quad);  // both read before either writes again
+    }
     if (!__all_sync(kFull, wait_bar(c, B_ODONE, (pv + I.ntiles - 1) & 1u))) return;
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * m.num_heads + h) * kD;
+    __nv_bfloat16* dst =
+        reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * m.num_heads + h) * kD + col0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 2; ++q) {
       uint32_t o[32];
-      tmem_ld32(tmem + lane_addr + kColO + q * 32, o);
+      tmem_ld32(tmem + lane_addr + kColO + col0 + q * 32, o);
       tmem_wait_ld(o);
       if (valid) {
 #pragma unroll
@@ -477,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     flags[0] = status_set(p.status) ? 1 : 0;
     flags[1] = 0;
-    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 1, 4, 1};
+    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 8, 8, 8, 1, 8, 1};
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, counts[i]);
     prefetch_tmap(&tq);
     prefetch_tmap(&tk);

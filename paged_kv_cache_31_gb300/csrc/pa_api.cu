@@ -247,8 +247,11 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
   const bool fast = mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
   // prefill-class sequences (more than 64 query rows per kv head) go to the tcgen05 kernel:
   // head size 128 and a GQA group that divides the 128-row tile
+  // No sequence can have more than num_tokens - num_seqs + 1 query tokens: when even that
+  // many rows fit the warp-MMA path, the tcgen05 kernel is not launched at all.
+  const int64_t max_rows = (num_tokens - (num_seqs > 0 ? num_seqs : 1) + 1) * m.group;
   L.use_tc = fast && head_dim == 128 && m.group <= 128 && (128 % m.group) == 0 &&
-             aligned(q, 16) && tc_enabled();
+             aligned(q, 16) && max_rows > L.tc_min_rows && scale > 0.f && tc_enabled();
 
   cudaError_t e = launch_plan_varlen(m, plan, L, d->status, stream);
   if (e != cudaSuccess) return PA_ECUDA;

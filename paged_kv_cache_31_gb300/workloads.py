@@ -21,7 +21,7 @@ from typing import List, Optional
 
 import torch
 
-__all__ = ["Workload", "build", "named", "NAMES"]
+__all__ = ["Workload", "build", "named", "subset", "NAMES"]
 
 
 @dataclasses.dataclass
@@ -155,6 +155,29 @@ def build(name: str, seq_lens: List[int], q_lens: List[int], num_heads: int, num
         block_tables=tables.to(device), q=q, k_new=k_new, v_new=v_new,
         k_blocks=k_blocks, v_blocks=v_blocks, partition_size=partition_size,
         masked_partition=masked_partition, shared_prefix_blocks=shared_prefix_blocks, seed=seed)
+
+
+def subset(w: Workload, seqs: List[int], name: Optional[str] = None) -> Workload:
+    """The sequences `seqs` of w as a batch of their own, over the same pool (its query rows,
+    new K/V rows and metadata, re-indexed)."""
+    qsl = w.query_start_loc.cpu().tolist()
+    rows = [t for s in seqs for t in range(qsl[s], qsl[s + 1])]
+    dev = w.q.device
+    idx = torch.tensor(rows, dtype=torch.long, device=dev)
+    sel = torch.tensor(seqs, dtype=torch.long, device=dev)
+    new_qsl = [0]
+    for s in seqs:
+        new_qsl.append(new_qsl[-1] + qsl[s + 1] - qsl[s])
+    fields = {f.name: getattr(w, f.name) for f in dataclasses.fields(w)}
+    fields.update(
+        name=name or f"{w.name}-subset", seq_lens_list=[w.seq_lens_list[s] for s in seqs],
+        q_lens_list=[w.q_lens_list[s] for s in seqs],
+        query_start_loc=torch.tensor(new_qsl, dtype=torch.int32, device=dev),
+        seq_lens=w.seq_lens[sel].contiguous(), positions=w.positions[idx].contiguous(),
+        block_tables=w.block_tables[sel].contiguous(), q=w.q[idx].contiguous(),
+        k_new=w.k_new[idx].contiguous(), v_new=w.v_new[idx].contiguous(),
+        masked_partition=[w.masked_partition[s] for s in seqs] if w.masked_partition else None)
+    return Workload(**fields)
 
 
 def _uniform(gen, lo, hi, n):
