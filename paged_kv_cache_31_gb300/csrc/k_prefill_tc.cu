@@ -8,14 +8,15 @@
 // visible range is fetched at a negative row coordinate, which TMA fills with zeros.
 //
 // One CTA per SM, persistent over items, 10 warps:
-//   warp 0      TMA producer: Q once per item, then K_j and V_j through a 2-stage ring;
+//   warp 0      TMA producer: Q once per item (two buffers, so the next item's Q loads while
+//               this one finishes), then K_j and V_j through a 2-stage ring;
 //   warp 1      TMEM owner and MMA issuer (one thread):
 //                 S_j = Q K_j^T      (M 128, N 128, K 128: 8 MMAs, K-major operands)
-//                 O  += P_j V_j      (P as a bf16 hi/lo pair: 16 MMAs, V MN-major)
-//               S is double-buffered in TMEM (columns 0 / 128), O lives in columns 256..383;
+//                 O  += P_j V_j      (P as a bf16 hi/lo pair read from TMEM: 16 MMAs, V MN-major)
+//               TMEM columns: S double-buffered at 0 / 128, O at 256, P hi / lo at 384 / 448;
 //   warps 2..9  softmax: two threads per query row (TMEM lane = row), one per 64-column
 //               half; mask, row max (combined through shared memory), exp2, row sum, P to
-//               shared memory, lazy O rescale, and the epilogue o = O * (1 / l) -> bf16.
+//               tensor memory, lazy O rescale, and the epilogue o = O * (1 / l) -> bf16.
 // The online softmax follows the per-tile update of the tinyllm decode page (section 2.2)
 // with one change that leaves the result unchanged: the reference max m is only moved (and
 // O, l rescaled by 2^(m_old - m_new)) when a tile's max exceeds it by more than 8 (log2
@@ -35,27 +36,27 @@ constexpr int kD = 128;           // head size on this path
 constexpr int kHalf = 16384;      // one 64-dim half of a 128-row bf16 tile
 constexpr int kTile = 2 * kHalf;  // 128 x 128 bf16
 constexpr int kStages = 2;
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;
+constexpr int kOffQ = 0;                          // two Q buffers (consecutive items)
+constexpr int kOffK = kOffQ + 2 * kTile;
 constexpr int kOffV = kOffK + kStages * kTile;
-constexpr int kOffPh = kOffV + kStages * kTile;
-constexpr int kOffPl = kOffPh + kTile;
-constexpr int kOffBar = kOffPl + kTile;
-constexpr int kNumBars = 18;
+constexpr int kOffBar = kOffV + kStages * kTile;
+constexpr int kNumBars = 20;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffFlag = kOffTmem + 16;
 constexpr int kOffXchg = kOffFlag + 16;               // row max / sum exchange, 2 x 128 fp32
 constexpr int kSmemBytes = kOffXchg + 2 * 128 * 4 + 1024;  // + slack to align the base
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
-constexpr int kSoftWarps = 8;                           // two column halves x four lane quarters
+constexpr int kSoftWarps = 8;                         // two column halves x four lane quarters
 constexpr int kThreads = 64 + kSoftWarps * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = 256;    // O: columns 256..383 (S buffers at 0 and 128)
+constexpr uint32_t kColPh = 384;   // P hi: 128 bf16 per row packed in 64 columns
+constexpr uint32_t kColPl = 448;   // P lo
 
 // barrier indices
 enum {
-  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 4, B_VFULL = 6, B_VEMPTY = 8, B_SFULL = 10,
-  B_SFREE = 12, B_PFULL = 14, B_ODONE = 15, B_OFREE = 16, B_FIN = 17
+  B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 6, B_VFULL = 8, B_VEMPTY = 10, B_SFULL = 12,
+  B_SFREE = 14, B_PFULL = 16, B_ODONE = 17, B_OFREE = 18, B_FIN = 19
 };
 
 // ---- tcgen05 / TMEM wrappers -----------------------------------------------------------------
@@ -78,6 +79,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Same with the A operand in tensor memory (row r in lane r, two bf16 per 32-bit column).
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -215,11 +225,13 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
     // Q: (D, H, T) tensor, box 64 x G x 128/G
     bool qok = true;
     if (lane == 0) {
-      qok = wait_bar(c, B_QEMPTY, (it_cnt & 1u) ^ 1u);
+      const uint32_t qb = it_cnt & 1u;
+      qok = wait_bar(c, B_QEMPTY + qb, ((it_cnt >> 1) & 1u) ^ 1u);
       if (qok) {
-        mbar_arrive_expect_tx(c.bar + B_QFULL, kTile);
-        tma_load_3d(c.sm + kOffQ, tq, 0, I.kvh * m.group, I.t0, c.bar + B_QFULL);
-        tma_load_3d(c.sm + kOffQ + kHalf, tq, 64, I.kvh * m.group, I.t0, c.bar + B_QFULL);
+        mbar_arrive_expect_tx(c.bar + B_QFULL + qb, kTile);
+        uint8_t* dst = c.sm + kOffQ + qb * kTile;
+        tma_load_3d(dst, tq, 0, I.kvh * m.group, I.t0, c.bar + B_QFULL + qb);
+        tma_load_3d(dst + kHalf, tq, 64, I.kvh * m.group, I.t0, c.bar + B_QFULL + qb);
       }
     }
     if (!__shfl_sync(kFull, (int)qok, 0)) return;
@@ -269,7 +281,9 @@ __device__ void mma_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n
   uint32_t kv = 0, sc = 0, pv = 0, it_cnt = 0;
   for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it_cnt) {
     const Item I = load_item(p, idx);
-    if (!wait_bar(c, B_QFULL, it_cnt & 1u)) return;
+    const uint32_t qb = it_cnt & 1u;
+    if (!wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u)) return;
+    const uint32_t qbase = sm + kOffQ + qb * kTile;
     auto issue_pv = [&](int jj) -> bool {
       if (jj == 0 && !wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u)) return false;
       if (!wait_bar(c, B_PFULL, pv & 1u)) return false;
@@ -279,12 +293,12 @@ __device__ void mma_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n
       const uint32_t vb = sm + kOffV + st * kTile;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc_mma(tmem + kColO, sdesc(sm + kOffPh + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-               sdesc(vb + kk * 2048, kHalf, 1024), kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+        tc_mma_ta(tmem + kColO, tmem + kColPh + kk * 8, sdesc(vb + kk * 2048, kHalf, 1024),
+                  kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc_mma(tmem + kColO, sdesc(sm + kOffPl + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-               sdesc(vb + kk * 2048, kHalf, 1024), kIdescPV, 1u);
+        tc_mma_ta(tmem + kColO, tmem + kColPl + kk * 8, sdesc(vb + kk * 2048, kHalf, 1024),
+                  kIdescPV, 1u);
       tc_commit(c.bar + B_ODONE);
       tc_commit(c.bar + B_VEMPTY + st);
       ++pv;
@@ -299,12 +313,12 @@ __device__ void mma_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n
       const uint32_t kb = sm + kOffK + st * kTile;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc_mma(tmem + b * 128, sdesc(sm + kOffQ + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
+        tc_mma(tmem + b * 128, sdesc(qbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
                sdesc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), kIdescQK,
                kk > 0 ? 1u : 0u);
       tc_commit(c.bar + B_SFULL + b);
       tc_commit(c.bar + B_KEMPTY + st);
-      if (j == I.ntiles - 1) tc_commit(c.bar + B_QEMPTY);
+      if (j == I.ntiles - 1) tc_commit(c.bar + B_QEMPTY + qb);
       if (j >= 1 && !issue_pv(j - 1)) return;
     }
     if (!issue_pv(I.ntiles - 1)) return;
@@ -328,8 +342,6 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
   const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
   const int tid256 = threadIdx.x - 64;  // 0..255 across the softmax warps
   float* xchg = reinterpret_cast<float*>(c.sm + kOffXchg);  // [half][row]
-  uint8_t* ph_row = c.sm + kOffPh + hf * kHalf + r * 128;   // one 64-key swizzle atom
-  uint8_t* pl_row = c.sm + kOffPl + hf * kHalf + r * 128;
   uint32_t kv = 0, sc = 0, pv = 0;
   for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
     const Item I = load_item(p, idx);
@@ -436,23 +448,22 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
           *reinterpret_cast<uint4*>(vt + half * kHalf + (blk * 16 + rr) * 128 + ch * 16) =
               make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();  // the MMA reads V through the async proxy
       }
-      // this half of P as bf16 hi / lo rows (K-major, 128-byte swizzle)
+      // this half of P as bf16 hi / lo pairs into tensor memory (columns 32 * half ...)
+      {
+        uint32_t hi[32], lo[32];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = x[q * 8 + 2 * e], bb = x[q * 8 + 2 * e + 1];
+        for (int e = 0; e < 32; ++e) {
+          const float a = x[2 * e], bb = x[2 * e + 1];
           hi[e] = pack_bf16x2(a, bb);
           const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[e]));
           lo[e] = pack_bf16x2(a - hv.x, bb - hv.y);
         }
-        const uint32_t off = (uint32_t)((q ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(ph_row + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(pl_row + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        tmem_st32(tmem + lane_addr + kColPh + hf * 32, hi);
+        tmem_st32(tmem + lane_addr + kColPl + hf * 32, lo);
+        tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar + B_PFULL);
@@ -510,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     flags[0] = status_set(p.status) ? 1 : 0;
     flags[1] = 0;
-    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 8, 8, 8, 1, 8, 1};
+    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 8, 8, 8, 1, 8, 1};
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, counts[i]);
     prefetch_tmap(&tq);
     prefetch_tmap(&tk);
