@@ -47,8 +47,9 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
 //  B. for each sequence with query tokens: seq_len >= 1, ceil(seq_len / b) <= max_blocks,
 //     those table entries inside the pool, query positions inside [0, seq_len); and the
 //     token -> sequence map;
-//  C. the list of (sequence, 16-row tile) items: a sequence's q_len * G query rows (token
-//     major, head minor within the kv group) are cut into tiles of 16.
+//  C. the work lists: a sequence's q_len * G query rows (token major, head minor within the
+//     kv group) are cut into 16-row tiles for the warp-MMA kernel, or, for prefill-class
+//     sequences, into 256-row items for the tcgen05 kernel.
 __global__ void __launch_bounds__(1024)
     k_plan_varlen(VarlenMeta m, int32_t* plan, const PlanLayout L, int* status) {
   __shared__ int s_err;
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(1024)
   }
   int2* mma_items = reinterpret_cast<int2*>(plan + L.mma_off);
   int4* tc_items = reinterpret_cast<int4*>(plan + L.tc_off);
-  const int tok_per_tile = 128 / m.group;  // used only when use_tc (group divides 128)
+  const int tok_per_item = 256 / m.group;  // used only when use_tc (group divides 128)
   int carry_m = 0, carry_t = 0;
   for (int base = 0; base < m.num_seqs; base += blockDim.x) {
     const int s = base + tid;
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(1024)
     if (s < m.num_seqs) {
       const int64_t rows = (int64_t)(m.query_start_loc[s + 1] - m.query_start_loc[s]) * m.group;
       if (L.use_tc && rows > L.tc_min_rows)
-        ct = (int)((rows + 127) / 128);
+        ct = (int)((rows + 255) / 256);
       else
         cm = (int)((rows + 15) / 16);
     }
@@ -121,13 +122,13 @@ __global__ void __launch_bounds__(1024)
     const int et = block_exclusive_scan(ct, s_warp, &tot_t);
     for (int i = 0; i < cm; ++i) mma_items[carry_m + em + i] = make_int2(s, i);
     if (ct > 0) {
-      // 128-row tiles, the last one (most keys under a causal mask) first; each carries the
-      // union [lo, hi) of its tokens' visible ranges
+      // 256-row items (two 128-row tiles), the last one (most keys under a causal mask)
+      // first; each carries the union [lo, hi) of its tokens' visible ranges
       const int qs = m.query_start_loc[s], qe = m.query_start_loc[s + 1];
       const int n = m.seq_lens[s];
       for (int i = 0; i < ct; ++i) {
         const int qt = ct - 1 - i;
-        const int ta = qs + qt * tok_per_tile, tb = min(qe, ta + tok_per_tile);
+        const int ta = qs + qt * tok_per_item, tb = min(qe, ta + tok_per_item);
         int lo = INT_MAX, hi = 0;
         for (int t = ta; t < tb; ++t) {
           const int e = m.causal ? m.positions[t] + 1 : n;

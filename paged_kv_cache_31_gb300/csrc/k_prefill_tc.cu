@@ -7,10 +7,15 @@
 // puts it (two 64-dim boxes of 16 rows per block, 128-byte swizzle); a block past the
 // visible range is fetched at a negative row coordinate, which TMA fills with zeros.
 //
-// One CTA per SM, persistent over items, 10 warps:
-//   warp 0      TMA producer: Q once per item (two buffers, so the next item's Q loads while
-//               this one finishes), then K_j and V_j through a 2-stage ring;
-//   warp 1      TMEM owner and MMA issuer (one thread):
+// Work items are 256-row pairs of such tiles, run by a cluster of two CTAs on two SMs: each
+// CTA computes one tile, and each fetches half of every K / V tile (alternate blocks) with TMA
+// multicast into both CTAs' shared memory, so a CTA issues 16 boxes per key tile instead of 32;
+// a stage is refilled only after both CTAs' MMAs released it.
+//
+// One CTA per SM, persistent over items, 12 warps:
+//   warp 0      TMA producer of Q (two buffers, so the next item's Q loads while this one
+//               finishes) and K_j through a 2-stage ring; warp 10 produces V_j the same way;
+//   warp 1      TMEM owner and QK^T issuer (one thread); warp 11 issues PV (one thread):
 //                 S_j = Q K_j^T      (M 128, N 128, K 128: 8 MMAs, K-major operands)
 //                 O  += P_j V_j      (P as a bf16 hi/lo pair read from TMEM: 16 MMAs, V MN-major)
 //               TMEM columns: S double-buffered at 0 / 128, O at 256, P hi / lo at 384 / 448;
@@ -47,7 +52,7 @@ constexpr int kOffXchg = kOffFlag + 16;               // row max / sum exchange,
 constexpr int kSmemBytes = kOffXchg + 2 * 128 * 4 + 1024;  // + slack to align the base
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 constexpr int kSoftWarps = 8;                         // two column halves x four lane quarters
-constexpr int kThreads = 64 + kSoftWarps * 32;
+constexpr int kThreads = 64 + kSoftWarps * 32 + 64;  // + the V producer and PV issuer warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;    // O: columns 256..383 (S buffers at 0 and 128)
 constexpr uint32_t kColPh = 384;   // P hi: 128 bf16 per row packed in 64 columns
@@ -153,6 +158,50 @@ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 1);
 
+// ---- thread-block cluster (pairs of CTAs on two SMs) ------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+// 3-D TMA tile load delivered to the same shared-memory offset (and barrier) of every CTA in
+// `mask`.
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int32_t c0,
+                                               int32_t c1, int32_t c2, uint64_t* bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+// Arrive on the barrier at this offset in every CTA of `mask` once this thread's MMAs are done.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
 // 2^x with the SFU's approximate base-2 exponential (flush-to-zero; 2^-inf = 0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -168,6 +217,9 @@ struct Ctx {
   volatile int* abort;
   int* status;
   uint64_t limit;
+  uint32_t rank;       // this CTA's place in its pair
+  int cluster;         // pair index
+  int nclusters;       // number of pairs
 };
 
 // Bounded wait that also gives up when another role aborted.
@@ -192,7 +244,8 @@ struct Item {
   int s, kvh, qt, t0, n_tok, n, kv0, ntiles, nblk_vis;
 };
 
-__device__ __forceinline__ Item load_item(const TcParams& p, int idx) {
+// Item idx = (256-row pair, kv head); this CTA of the pair takes the 128-row tile `rank`.
+__device__ __forceinline__ Item load_item(const TcParams& p, int idx, uint32_t rank) {
   const VarlenMeta& m = p.m;
   const int4 it = reinterpret_cast<const int4*>(p.plan + p.tc_off)[idx / m.num_kv_heads];
   Item r;
@@ -201,8 +254,8 @@ __device__ __forceinline__ Item load_item(const TcParams& p, int idx) {
   r.kvh = idx % m.num_kv_heads;
   const int tpt = kBM / m.group;
   const int qs = m.query_start_loc[r.s], qe = m.query_start_loc[r.s + 1];
-  r.t0 = qs + r.qt * tpt;
-  r.n_tok = min(tpt, qe - r.t0);
+  r.t0 = qs + (2 * r.qt + (int)rank) * tpt;
+  r.n_tok = max(0, min(tpt, qe - r.t0));
   r.n = m.seq_lens[r.s];
   const int lo = it.z, hi = it.w;
   r.kv0 = (lo / 16) * 16;
@@ -213,28 +266,35 @@ __device__ __forceinline__ Item load_item(const TcParams& p, int idx) {
 
 // ---- roles ------------------------------------------------------------------------------------
 
+// TMA producers.  The K warp also loads Q; the V warp runs its own copy of the loop, so a K
+// tile is fetched as soon as its stage is free (gated only by the QK^T MMAs) and never waits
+// behind a V stage that the slower PV MMAs still hold.
 __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
-                         const CUtensorMap* tk, const CUtensorMap* tv, int n_items) {
+                         const CUtensorMap* tkv, bool is_v, int n_items) {
   const int lane = threadIdx.x & 31;
   const VarlenMeta& m = p.m;
+  const int full = is_v ? B_VFULL : B_KFULL, empty = is_v ? B_VEMPTY : B_KEMPTY;
+  const int off = is_v ? kOffV : kOffK;
   uint32_t kv = 0, it_cnt = 0;
-  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it_cnt) {
-    const Item I = load_item(p, idx);
+  for (int idx = c.cluster; idx < n_items; idx += c.nclusters, ++it_cnt) {
+    const Item I = load_item(p, idx, c.rank);
     const int32_t* row = m.block_tables + (int64_t)I.s * m.max_blocks;
     const int blk0 = I.kv0 / 16;
-    // Q: (D, H, T) tensor, box 64 x G x 128/G
-    bool qok = true;
-    if (lane == 0) {
-      const uint32_t qb = it_cnt & 1u;
-      qok = wait_bar(c, B_QEMPTY + qb, ((it_cnt >> 1) & 1u) ^ 1u);
-      if (qok) {
-        mbar_arrive_expect_tx(c.bar + B_QFULL + qb, kTile);
-        uint8_t* dst = c.sm + kOffQ + qb * kTile;
-        tma_load_3d(dst, tq, 0, I.kvh * m.group, I.t0, c.bar + B_QFULL + qb);
-        tma_load_3d(dst + kHalf, tq, 64, I.kvh * m.group, I.t0, c.bar + B_QFULL + qb);
+    if (!is_v) {
+      // Q: (D, H, T) tensor, box 64 x G x 128/G
+      bool qok = true;
+      if (lane == 0) {
+        const uint32_t qb = it_cnt & 1u;
+        qok = wait_bar(c, B_QEMPTY + qb, ((it_cnt >> 1) & 1u) ^ 1u);
+        if (qok) {
+          mbar_arrive_expect_tx(c.bar + B_QFULL + qb, kTile);
+          uint8_t* dst = c.sm + kOffQ + qb * kTile;
+          tma_load_3d(dst, tq, 0, I.kvh * m.group, I.t0, c.bar + B_QFULL + qb);
+          tma_load_3d(dst + kHalf, tq, 64, I.kvh * m.group, I.t0, c.bar + B_QFULL + qb);
+        }
       }
+      if (!__shfl_sync(kFull, (int)qok, 0)) return;
     }
-    if (!__shfl_sync(kFull, (int)qok, 0)) return;
     int next_id = (lane < 8 && blk0 + lane < I.nblk_vis) ? row[blk0 + lane] : -1;
     for (int j = 0; j < I.ntiles; ++j, ++kv) {
       const int id = next_id;
@@ -248,26 +308,15 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
       bool ok = true;
       if (lane == 0) {
         const uint32_t st = kv % kStages, ph = (kv / kStages) & 1u;
-        ok = wait_bar(c, B_KEMPTY + st, ph ^ 1u);
+        ok = wait_bar(c, empty + st, ph ^ 1u);
         if (ok) {
-          mbar_arrive_expect_tx(c.bar + B_KFULL + st, kTile);
-          uint8_t* dst = c.sm + kOffK + st * kTile;
+          mbar_arrive_expect_tx(c.bar + full + st, kTile);
+          uint8_t* dst = c.sm + off + st * kTile;
 #pragma unroll
-          for (int b = 0; b < 8; ++b) {
+          for (int b = c.rank; b < 8; b += 2) {  // this CTA fetches every other block for both
             const int r = ids[b] >= 0 ? ids[b] * 16 : -16;
-            tma_load_3d(dst + b * 2048, tk, 0, I.kvh, r, c.bar + B_KFULL + st);
-            tma_load_3d(dst + kHalf + b * 2048, tk, 64, I.kvh, r, c.bar + B_KFULL + st);
-          }
-          ok = wait_bar(c, B_VEMPTY + st, ph ^ 1u);
-        }
-        if (ok) {
-          mbar_arrive_expect_tx(c.bar + B_VFULL + st, kTile);
-          uint8_t* dst = c.sm + kOffV + st * kTile;
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            const int r = ids[b] >= 0 ? ids[b] * 16 : -16;
-            tma_load_3d(dst + b * 2048, tv, 0, I.kvh, r, c.bar + B_VFULL + st);
-            tma_load_3d(dst + kHalf + b * 2048, tv, 64, I.kvh, r, c.bar + B_VFULL + st);
+            tma_load_3d_mc(dst + b * 2048, tkv, 0, I.kvh, r, c.bar + full + st, 0x3);
+            tma_load_3d_mc(dst + kHalf + b * 2048, tkv, 64, I.kvh, r, c.bar + full + st, 0x3);
           }
         }
       }
@@ -276,34 +325,17 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
   }
 }
 
-__device__ void mma_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
+// MMA issue runs on two threads (warps 1 and 11) so that one thread's instruction issue
+// never delays the other chain: the QK^T issuer releases K and Q stages, the PV issuer
+// releases V stages and O.  They share no TMEM columns (S at 0 / 128, O at 256, P at 384).
+__device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
   const uint32_t sm = smem_u32(c.sm);
-  uint32_t kv = 0, sc = 0, pv = 0, it_cnt = 0;
-  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++it_cnt) {
-    const Item I = load_item(p, idx);
+  uint32_t kv = 0, sc = 0, it_cnt = 0;
+  for (int idx = c.cluster; idx < n_items; idx += c.nclusters, ++it_cnt) {
+    const Item I = load_item(p, idx, c.rank);
     const uint32_t qb = it_cnt & 1u;
     if (!wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u)) return;
     const uint32_t qbase = sm + kOffQ + qb * kTile;
-    auto issue_pv = [&](int jj) -> bool {
-      if (jj == 0 && !wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u)) return false;
-      if (!wait_bar(c, B_PFULL, pv & 1u)) return false;
-      const uint32_t kvj = kv + jj, st = kvj % kStages;
-      if (!wait_bar(c, B_VFULL + st, (kvj / kStages) & 1u)) return false;
-      tc_fence_after();
-      const uint32_t vb = sm + kOffV + st * kTile;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        tc_mma_ta(tmem + kColO, tmem + kColPh + kk * 8, sdesc(vb + kk * 2048, kHalf, 1024),
-                  kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        tc_mma_ta(tmem + kColO, tmem + kColPl + kk * 8, sdesc(vb + kk * 2048, kHalf, 1024),
-                  kIdescPV, 1u);
-      tc_commit(c.bar + B_ODONE);
-      tc_commit(c.bar + B_VEMPTY + st);
-      ++pv;
-      return true;
-    };
     for (int j = 0; j < I.ntiles; ++j) {
       const uint32_t kvj = kv + j, st = kvj % kStages;
       const uint32_t s = sc + j, b = s & 1u;
@@ -317,13 +349,39 @@ __device__ void mma_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n
                sdesc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), kIdescQK,
                kk > 0 ? 1u : 0u);
       tc_commit(c.bar + B_SFULL + b);
-      tc_commit(c.bar + B_KEMPTY + st);
+      tc_commit_mc(c.bar + B_KEMPTY + st, 0x3);  // both CTAs must be done before a refill
       if (j == I.ntiles - 1) tc_commit(c.bar + B_QEMPTY + qb);
-      if (j >= 1 && !issue_pv(j - 1)) return;
     }
-    if (!issue_pv(I.ntiles - 1)) return;
     kv += I.ntiles;
     sc += I.ntiles;
+  }
+}
+
+__device__ void pv_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
+  const uint32_t sm = smem_u32(c.sm);
+  uint32_t kv = 0, pv = 0, it_cnt = 0;
+  for (int idx = c.cluster; idx < n_items; idx += c.nclusters, ++it_cnt) {
+    const Item I = load_item(p, idx, c.rank);
+    for (int j = 0; j < I.ntiles; ++j) {
+      if (j == 0 && !wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u)) return;
+      if (!wait_bar(c, B_PFULL, pv & 1u)) return;
+      const uint32_t kvj = kv + j, st = kvj % kStages;
+      if (!wait_bar(c, B_VFULL + st, (kvj / kStages) & 1u)) return;
+      tc_fence_after();
+      const uint32_t vb = sm + kOffV + st * kTile;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma_ta(tmem + kColO, tmem + kColPh + kk * 8, sdesc(vb + kk * 2048, kHalf, 1024),
+                  kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma_ta(tmem + kColO, tmem + kColPl + kk * 8, sdesc(vb + kk * 2048, kHalf, 1024),
+                  kIdescPV, 1u);
+      tc_commit(c.bar + B_ODONE);
+      tc_commit_mc(c.bar + B_VEMPTY + st, 0x3);
+      ++pv;
+    }
+    kv += I.ntiles;
   }
 }
 
@@ -343,8 +401,8 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
   const int tid256 = threadIdx.x - 64;  // 0..255 across the softmax warps
   float* xchg = reinterpret_cast<float*>(c.sm + kOffXchg);  // [half][row]
   uint32_t kv = 0, sc = 0, pv = 0;
-  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
-    const Item I = load_item(p, idx);
+  for (int idx = c.cluster; idx < n_items; idx += c.nclusters) {
+    const Item I = load_item(p, idx, c.rank);
     const int tl = r / m.group;
     const bool valid = tl < I.n_tok;
     const int t = I.t0 + (valid ? tl : 0);
@@ -521,7 +579,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     flags[0] = status_set(p.status) ? 1 : 0;
     flags[1] = 0;
-    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 8, 8, 8, 1, 8, 1};
+    // k_empty / v_empty: one arrival from each CTA of the pair; s_free / p_full / o_free: one
+    // per softmax warp
+    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 2, 2, 1, 1, 2, 2, 1, 1, 8, 8, 8, 1, 8, 2};
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, counts[i]);
     prefetch_tmap(&tq);
     prefetch_tmap(&tk);
@@ -536,18 +596,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // the partner's barriers are initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  Ctx c{sm, bar, reinterpret_cast<volatile int*>(flags + 1), p.status, p.wait_limit_ns};
+  Ctx c{sm, bar, reinterpret_cast<volatile int*>(flags + 1), p.status, p.wait_limit_ns,
+        cluster_rank(), (int)cluster_id_x(), (int)num_clusters_x()};
   const int n_items = flags[0] ? 0 : p.plan[1] * p.m.num_kv_heads;
 
   if (warp == 0) {
-    producer(c, p, &tq, &tk, &tv, n_items);
-  } else if (warp == 1) {
+    producer(c, p, &tq, &tk, false, n_items);
+  } else if (warp == 2 + kSoftWarps) {
+    producer(c, p, &tq, &tv, true, n_items);
+  } else if (warp == 1 || warp == 3 + kSoftWarps) {
     if ((threadIdx.x & 31) == 0) {
-      mma_issuer(c, p, tmem, n_items);
-      // every MMA issued above has completed before the tensor memory is released
+      if (warp == 1)
+        s_issuer(c, p, tmem, n_items);
+      else
+        pv_issuer(c, p, tmem, n_items);
+      // every MMA issued by either thread has completed before the tensor memory is released
       tc_commit(bar + B_FIN);
       uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(bar + B_FIN, 0) && globaltimer_ns() - t0 < 1000000000ull) {
@@ -558,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     softmax_role(c, p, tmem, n_items);
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its partner may still write to its shared memory
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -571,12 +637,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_tc_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const TcParams& p, int grid, cudaStream_t stream) {
-  if (grid <= 0) return cudaSuccess;
+  if (grid < 2) grid = 2;
   cudaError_t e =
       cudaFuncSetAttribute(k_tc_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  k_tc_prefill<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  // pairs of CTAs (a cluster of two SMs) share every K / V tile through TMA multicast
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(grid & ~1), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_tc_prefill, tq, tk, tv, p);
 }
 
 }  // namespace pa
