@@ -21,6 +21,8 @@
 // Why warp MMA here: these tiles are HBM-bound (one pass over K and V per kv head), so the
 // tensor core only has to take the ~2 G D FMA per key off the FP32 pipe; with G = 8 the FMA
 // path would need about half the chip's FP32 rate at full HBM bandwidth.
+#include <algorithm>
+
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -41,7 +43,7 @@ struct Geom {
 
 template <int D, int NW, int NS>
 constexpr size_t smem_bytes() {
-  // ring | full barriers | merge m, l | fail flag ; the O merge area aliases the ring
+  // ring | full barriers | merge m, l | fail flag, work unit ; the O merge area aliases the ring
   return 1024 + (size_t)NW * NS * Geom<D>::kStageBytes + NW * NS * 8 + NW * 16 * 4 * 2 + 16;
 }
 
@@ -83,21 +85,36 @@ __global__ void __launch_bounds__(NW * 32, 2)
   if (*reinterpret_cast<volatile int*>(fail)) return;
 
   const VarlenMeta& m = p.m;
-  const int kvh = blockIdx.y;
   const int G = m.group;
   const int H = m.num_heads;
   uint32_t ring_pos = 0;  // blocks this warp has pushed through its ring so far
 
-  int n_items;
+  // Split-KV: grid (partition x sequence, kv head), strided.  Varlen: a persistent 1-D grid
+  // whose CTAs take (item, kv head) units from the plan's work counter, longest items first.
+  int n_units;
   const int2* items = nullptr;
+  int* unit_slot = fail + 1;
   if constexpr (SPLIT) {
-    n_items = m.num_seqs * p.max_parts;
+    n_units = m.num_seqs * p.max_parts;
   } else {
-    n_items = p.plan[0];
+    n_units = p.plan[0] * m.num_kv_heads;
     items = reinterpret_cast<const int2*>(p.plan + p.items_off);
   }
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+  for (int it_no = 0;; ++it_no) {
+    int item, kvh;
+    if constexpr (SPLIT) {
+      item = blockIdx.x + it_no * gridDim.x;
+      if (item >= n_units) break;
+      kvh = blockIdx.y;
+    } else {
+      if (threadIdx.x == 0) *unit_slot = atomicAdd(const_cast<int32_t*>(p.plan) + 2, 1);
+      __syncthreads();
+      const int unit = *reinterpret_cast<volatile int*>(unit_slot);
+      if (unit >= n_units) break;
+      item = unit / m.num_kv_heads;
+      kvh = unit % m.num_kv_heads;
+    }
     // ---------------------------------------------------------------- item geometry
     int s, row0, rows_total, part = 0, qs, n;
     if constexpr (SPLIT) {
@@ -430,7 +447,7 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Para
                 "merge area must fit in the ring");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(grid_x, p.m.num_kv_heads);
+  dim3 grid(grid_x, SPLIT ? p.m.num_kv_heads : 1);
   kern<<<grid, kNW * 32, smem, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }
@@ -439,7 +456,10 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Para
 
 cudaError_t launch_mma16_varlen(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p,
                                 int head_dim, int items_cap, cudaStream_t stream) {
-  const int grid_x = items_cap < 1 ? 1 : (items_cap > 65535 ? 65535 : items_cap);
+  // persistent: two resident CTAs per SM, never more than there can be units
+  const int64_t units = (int64_t)items_cap * p.m.num_kv_heads;
+  const int64_t resident = 2 * (int64_t)num_sms();
+  const int grid_x = (int)std::max<int64_t>(1, std::min(units, resident));
   if (head_dim == 128) return launch<128, false>(tk, tv, p, grid_x, stream);
   if (head_dim == 64) return launch<64, false>(tk, tv, p, grid_x, stream);
   return cudaErrorInvalidValue;

@@ -41,6 +41,16 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
   return before + x - v;
 }
 
+// Work buckets for ordering: a cost c > 0 maps to 16 sub-buckets per power of two
+// (descending: the largest costs get the smallest bucket index).
+constexpr int kCostBuckets = 512;
+__device__ __forceinline__ int cost_bucket(int c) {
+  if (c <= 0) return kCostBuckets - 1;
+  const int lg = 31 - __clz(c);
+  const int sub = lg >= 4 ? (c >> (lg - 4)) & 15 : (c << (4 - lg)) & 15;
+  return kCostBuckets - 1 - (lg * 16 + sub);
+}
+
 // Validation and planning of one pa_varlen_forward call (tinyllm section 2.6 checks), in a
 // single CTA so that the work list can be built with one block-wide scan:
 //  A. query_start_loc starts at 0, never decreases, ends at num_tokens;
@@ -54,6 +64,7 @@ __global__ void __launch_bounds__(1024)
     k_plan_varlen(VarlenMeta m, int32_t* plan, const PlanLayout L, int* status) {
   __shared__ int s_err;
   __shared__ int s_warp[32];
+  __shared__ int s_hist[kCostBuckets];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   if (tid == 0) s_err = status_set(status) ? -1 : 0;
   __syncthreads();
@@ -69,7 +80,10 @@ __global__ void __launch_bounds__(1024)
   if (s_err == 0) {
     for (int s = warp; s < m.num_seqs; s += nwarps) {
       const int a = m.query_start_loc[s], b = m.query_start_loc[s + 1];
-      if (a == b) continue;
+      if (a == b) {
+        if (lane == 0) plan[L.cost_off + s] = 0;
+        continue;
+      }
       const int n = m.seq_lens[s];
       if (n < 1) {
         if (lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
@@ -86,11 +100,21 @@ __global__ void __launch_bounds__(1024)
         const int32_t id = row[i];
         bad |= (id < 0 || (int64_t)id >= m.num_blocks);
       }
+      int lo = INT_MAX, hi = 0;
       for (int t = a + lane; t < b; t += 32) {
         const int32_t pos = m.positions[t];
         bad |= (pos < 0 || pos >= n);
         plan[L.tok_off + t] = s;
+        const int e = m.causal ? pos + 1 : n;
+        lo = min(lo, m.window > 0 ? max(0, e - m.window) : 0);
+        hi = max(hi, e);
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(kFull, lo, o));
+        hi = max(hi, __shfl_xor_sync(kFull, hi, o));
+      }
+      if (lane == 0) plan[L.cost_off + s] = max(0, hi - lo);
       if (__any_sync(kFull, bad) && lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
     }
   }
@@ -106,7 +130,9 @@ __global__ void __launch_bounds__(1024)
   int2* mma_items = reinterpret_cast<int2*>(plan + L.mma_off);
   int4* tc_items = reinterpret_cast<int4*>(plan + L.tc_off);
   const int tok_per_item = 256 / m.group;  // used only when use_tc (group divides 128)
-  int carry_m = 0, carry_t = 0;
+  for (int i = tid; i < kCostBuckets; i += blockDim.x) s_hist[i] = 0;
+  __syncthreads();
+  int carry_t = 0;
   for (int base = 0; base < m.num_seqs; base += blockDim.x) {
     const int s = base + tid;
     int cm = 0, ct = 0;
@@ -117,10 +143,9 @@ __global__ void __launch_bounds__(1024)
       else
         cm = (int)((rows + 15) / 16);
     }
-    int tot_m, tot_t;
-    const int em = block_exclusive_scan(cm, s_warp, &tot_m);
+    if (cm > 0) atomicAdd(&s_hist[cost_bucket(plan[L.cost_off + s])], cm);
+    int tot_t;
     const int et = block_exclusive_scan(ct, s_warp, &tot_t);
-    for (int i = 0; i < cm; ++i) mma_items[carry_m + em + i] = make_int2(s, i);
     if (ct > 0) {
       // 256-row items (two 128-row tiles), the last one (most keys under a causal mask)
       // first; each carries the union [lo, hi) of its tokens' visible ranges
@@ -139,12 +164,31 @@ __global__ void __launch_bounds__(1024)
         tc_items[carry_t + et + i] = make_int4(s, qt, lo, hi);
       }
     }
-    carry_m += tot_m;
     carry_t += tot_t;
+  }
+  __syncthreads();
+  // 16-row tiles, the sequences with the most visible keys first (a counting sort over
+  // logarithmic cost buckets), so the persistent kernel's last units are the short ones
+  int carry_m = 0;
+  for (int b0 = 0; b0 < kCostBuckets; b0 += blockDim.x) {
+    const int v = b0 + tid < kCostBuckets ? s_hist[b0 + tid] : 0;
+    int tot;
+    const int e = block_exclusive_scan(v, s_warp, &tot);
+    if (b0 + tid < kCostBuckets) s_hist[b0 + tid] = carry_m + e;  // bucket start
+    carry_m += tot;
+  }
+  __syncthreads();
+  for (int s = tid; s < m.num_seqs; s += blockDim.x) {
+    const int64_t rows = (int64_t)(m.query_start_loc[s + 1] - m.query_start_loc[s]) * m.group;
+    if (rows == 0 || (L.use_tc && rows > L.tc_min_rows)) continue;
+    const int cm = (int)((rows + 15) / 16);
+    const int at = atomicAdd(&s_hist[cost_bucket(plan[L.cost_off + s])], cm);
+    for (int i = 0; i < cm; ++i) mma_items[at + i] = make_int2(s, i);
   }
   if (tid == 0) {
     plan[0] = carry_m;
     plan[1] = carry_t;
+    plan[2] = 0;  // work counter of the warp-MMA kernel
   }
 }
 

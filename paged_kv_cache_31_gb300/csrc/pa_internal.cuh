@@ -168,15 +168,17 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not lan
 // ------------------------------------------------------------------------------------------
 // per-call plan kept in the caller's workspace (int32 words)
 //   [0] number of 16-row tile items (decode-class sequences, warp-MMA kernel)
-//   [1] number of 128-row tile items (prefill-class sequences, tcgen05 kernel)
-//   [2..15] reserved
+//   [1] number of 256-row items (prefill-class sequences, tcgen05 kernel)
+//   [2] work counter of the warp-MMA kernel (zeroed by the plan)
+//   [3..15] reserved
 //   [tok_off, tok_off + T)        token -> sequence
-//   [mma_off, + 2 * mma_cap)      int2 items (seq, 16-row tile)
-//   [tc_off, + 4 * tc_cap)        int4 items (seq, 128-row tile, kv lo, kv hi)
+//   [cost_off, cost_off + S)      per sequence: keys its query rows can see (work estimate)
+//   [mma_off, + 2 * mma_cap)      int2 items (seq, 16-row tile), longest first
+//   [tc_off, + 4 * tc_cap)        int4 items (seq, 256-row item, kv lo, kv hi)
 constexpr int kPlanHeaderWords = 16;
 
 struct PlanLayout {
-  int64_t tok_off, mma_off, tc_off;
+  int64_t tok_off, cost_off, mma_off, tc_off;
   int64_t mma_cap, tc_cap;
   int64_t words;
   int32_t use_tc;       // prefill-class sequences go to the tcgen05 kernel
@@ -188,8 +190,9 @@ inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t grou
   PlanLayout L;
   L.tok_off = kPlanHeaderWords;
   L.mma_cap = (num_tokens * group + 15) / 16 + num_seqs + 1;
-  L.tc_cap = (num_tokens * group + 127) / 128 + num_seqs + 1;
-  L.mma_off = (L.tok_off + num_tokens + 3) & ~int64_t(3);
+  L.tc_cap = (num_tokens * group + 255) / 256 + num_seqs + 1;
+  L.cost_off = L.tok_off + num_tokens;
+  L.mma_off = (L.cost_off + num_seqs + 3) & ~int64_t(3);
   L.tc_off = (L.mma_off + 2 * L.mma_cap + 3) & ~int64_t(3);
   L.words = L.tc_off + 4 * L.tc_cap;
   L.use_tc = 0;
