@@ -59,12 +59,14 @@ __device__ __forceinline__ int cost_bucket(int c) {
 //     token -> sequence map;
 //  C. the work lists: a sequence's q_len * G query rows (token major, head minor within the
 //     kv group) are cut into 16-row tiles for the warp-MMA kernel, or, for prefill-class
-//     sequences, into 256-row items for the tcgen05 kernel.
+//     sequences, into 256-row items for the tcgen05 kernel; both lists are ordered by the
+//     number of keys their rows see, longest first, so the kernels' last units are short.
 __global__ void __launch_bounds__(1024)
     k_plan_varlen(VarlenMeta m, int32_t* plan, const PlanLayout L, int* status) {
   __shared__ int s_err;
   __shared__ int s_warp[32];
-  __shared__ int s_hist[kCostBuckets];
+  __shared__ int s_hist[kCostBuckets];    // 16-row tiles per cost bucket
+  __shared__ int s_hist_t[kCostBuckets];  // 256-row items per cost bucket
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   if (tid == 0) s_err = status_set(status) ? -1 : 0;
   __syncthreads();
@@ -129,9 +131,15 @@ __global__ void __launch_bounds__(1024)
   }
   int2* mma_items = reinterpret_cast<int2*>(plan + L.mma_off);
   int4* tc_items = reinterpret_cast<int4*>(plan + L.tc_off);
+  int4* tc_tmp = reinterpret_cast<int4*>(plan + L.tc_tmp_off);
   const int tok_per_item = 256 / m.group;  // used only when use_tc (group divides 128)
-  for (int i = tid; i < kCostBuckets; i += blockDim.x) s_hist[i] = 0;
+  for (int i = tid; i < kCostBuckets; i += blockDim.x) {
+    s_hist[i] = 0;
+    s_hist_t[i] = 0;
+  }
   __syncthreads();
+  // C1: 256-row items of prefill-class sequences, in sequence order, the last one (most keys
+  // under a causal mask) first; the histogram of the 16-row tiles' costs
   int carry_t = 0;
   for (int base = 0; base < m.num_seqs; base += blockDim.x) {
     const int s = base + tid;
@@ -146,27 +154,52 @@ __global__ void __launch_bounds__(1024)
     if (cm > 0) atomicAdd(&s_hist[cost_bucket(plan[L.cost_off + s])], cm);
     int tot_t;
     const int et = block_exclusive_scan(ct, s_warp, &tot_t);
-    if (ct > 0) {
-      // 256-row items (two 128-row tiles), the last one (most keys under a causal mask)
-      // first; each carries the union [lo, hi) of its tokens' visible ranges
-      const int qs = m.query_start_loc[s], qe = m.query_start_loc[s + 1];
-      const int n = m.seq_lens[s];
-      for (int i = 0; i < ct; ++i) {
-        const int qt = ct - 1 - i;
-        const int ta = qs + qt * tok_per_item, tb = min(qe, ta + tok_per_item);
-        int lo = INT_MAX, hi = 0;
-        for (int t = ta; t < tb; ++t) {
-          const int e = m.causal ? m.positions[t] + 1 : n;
-          const int b = m.window > 0 ? max(0, e - m.window) : 0;
-          lo = min(lo, b);
-          hi = max(hi, e);
-        }
-        tc_items[carry_t + et + i] = make_int4(s, qt, lo, hi);
-      }
-    }
+    for (int i = 0; i < ct; ++i) tc_tmp[carry_t + et + i] = make_int4(s, ct - 1 - i, 0, 0);
     carry_t += tot_t;
   }
   __syncthreads();
+  // C2: each item's key range [lo, hi), the union of its tokens' visible ranges (a warp per
+  // item), and the histogram of the items' costs (carry_t is the same in every thread)
+  if (carry_t > 0) {
+    for (int k = warp; k < carry_t; k += nwarps) {
+      const int4 it = tc_tmp[k];
+      const int qs = m.query_start_loc[it.x], qe = m.query_start_loc[it.x + 1];
+      const int n = m.seq_lens[it.x];
+      const int ta = qs + it.y * tok_per_item, tb = min(qe, ta + tok_per_item);
+      int lo = INT_MAX, hi = 0;
+      for (int t = ta + lane; t < tb; t += 32) {
+        const int e = m.causal ? m.positions[t] + 1 : n;
+        lo = min(lo, m.window > 0 ? max(0, e - m.window) : 0);
+        hi = max(hi, e);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(kFull, lo, o));
+        hi = max(hi, __shfl_xor_sync(kFull, hi, o));
+      }
+      if (lane == 0) {
+        tc_tmp[k] = make_int4(it.x, it.y, lo, hi);
+        atomicAdd(&s_hist_t[cost_bucket(hi - lo)], 1);
+      }
+    }
+    __syncthreads();
+    // C3: the items ordered by cost, longest first (a counting sort over the cost buckets)
+    {
+      int carry = 0;
+      for (int b0 = 0; b0 < kCostBuckets; b0 += blockDim.x) {
+        const int v = b0 + tid < kCostBuckets ? s_hist_t[b0 + tid] : 0;
+        int tot;
+        const int e = block_exclusive_scan(v, s_warp, &tot);
+        if (b0 + tid < kCostBuckets) s_hist_t[b0 + tid] = carry + e;  // bucket start
+        carry += tot;
+      }
+    }
+    __syncthreads();
+    for (int k = tid; k < carry_t; k += blockDim.x) {
+      const int4 it = tc_tmp[k];
+      tc_items[atomicAdd(&s_hist_t[cost_bucket(it.w - it.z)], 1)] = it;
+    }
+  }
   // 16-row tiles, the sequences with the most visible keys first (a counting sort over
   // logarithmic cost buckets), so the persistent kernel's last units are the short ones
   int carry_m = 0;

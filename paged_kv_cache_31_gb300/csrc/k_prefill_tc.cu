@@ -15,13 +15,17 @@
 // One CTA per SM, persistent over items, 12 warps:
 //   warp 0      TMA producer of Q (two buffers, so the next item's Q loads while this one
 //               finishes) and K_j through a 2-stage ring; warp 10 produces V_j the same way;
-//   warp 1      TMEM owner and QK^T issuer (one thread); warp 11 issues PV (one thread):
+//   warp 1      TMEM owner and QK^T issuer (one thread); warp 11 issues PV (one lane; the
+//               warp first zeroes the never-written V rows past a sequence's end):
 //                 S_j = Q K_j^T      (M 128, N 128, K 128: 8 MMAs, K-major operands)
 //                 O  += P_j V_j      (P as a bf16 hi/lo pair read from TMEM: 16 MMAs, V MN-major)
-//               TMEM columns: S double-buffered at 0 / 128, O at 256, P hi / lo at 384 / 448;
+//               TMEM columns: three S buffers at 0 / 128 / 384, O at 256.  P_j is written over
+//               the S_j it came from, so S_{j+3} may only be issued once P_j V_j is done;
 //   warps 2..9  softmax: two threads per query row (TMEM lane = row), one per 64-column
 //               half; mask, row max (combined through shared memory), exp2, row sum, P to
 //               tensor memory, lazy O rescale, and the epilogue o = O * (1 / l) -> bf16.
+//               A softmax thread waits for the previous P V only when it must rescale O,
+//               so the exponentials of tile j run while the tensor core works on tile j - 1.
 // The online softmax follows the per-tile update of the tinyllm decode page (section 2.2)
 // with one change that leaves the result unchanged: the reference max m is only moved (and
 // O, l rescaled by 2^(m_old - m_new)) when a tile's max exceeds it by more than 8 (log2
@@ -45,8 +49,8 @@ constexpr int kOffQ = 0;                          // two Q buffers (consecutive 
 constexpr int kOffK = kOffQ + 2 * kTile;
 constexpr int kOffV = kOffK + kStages * kTile;
 constexpr int kOffBar = kOffV + kStages * kTile;
-constexpr int kNumBars = 20;
-constexpr int kOffTmem = kOffBar + kNumBars * 8;
+constexpr int kNumBarsMax = 24;
+constexpr int kOffTmem = kOffBar + kNumBarsMax * 8;
 constexpr int kOffFlag = kOffTmem + 16;
 constexpr int kOffXchg = kOffFlag + 16;               // row max / sum exchange, 2 x 128 fp32
 constexpr int kSmemBytes = kOffXchg + 2 * 128 * 4 + 1024;  // + slack to align the base
@@ -54,15 +58,21 @@ static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 constexpr int kSoftWarps = 8;                         // two column halves x four lane quarters
 constexpr int kThreads = 64 + kSoftWarps * 32 + 64;  // + the V producer and PV issuer warps
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;    // O: columns 256..383 (S buffers at 0 and 128)
-constexpr uint32_t kColPh = 384;   // P hi: 128 bf16 per row packed in 64 columns
-constexpr uint32_t kColPl = 448;   // P lo
+constexpr uint32_t kColO = 256;    // O: columns 256..383
+constexpr int kSBufs = 3;          // S / P buffers at columns 0, 128 and 384
+__device__ __forceinline__ uint32_t col_s(uint32_t b) { return b == 2 ? 384u : b * 128u; }
+// Inside an S buffer, P_j of key half h (keys 64h .. 64h+63) is stored by the thread that read
+// those scores: hi at columns 64h .. 64h+31, lo at 64h+32 .. 64h+63 (two bf16 per column).
+__device__ __forceinline__ uint32_t col_p(int kstep, int lo) {
+  return (uint32_t)((kstep >> 2) * 64 + lo * 32 + (kstep & 3) * 8);
+}
 
-// barrier indices
+// barrier indices (the per-buffer ones are consecutive)
 enum {
   B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 6, B_VFULL = 8, B_VEMPTY = 10, B_SFULL = 12,
-  B_SFREE = 14, B_PFULL = 16, B_ODONE = 17, B_OFREE = 18, B_FIN = 19
+  B_PFULL = 15, B_PVDONE = 18, B_OFREE = 21, B_FIN = 22
 };
+constexpr int kNumBars = 23;
 
 // ---- tcgen05 / TMEM wrappers -----------------------------------------------------------------
 
@@ -209,6 +219,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (Blackwell's two-wide FP32 instructions: one issue for two lanes of
+// work).  A pair lives in one 64-bit register, .x in the low half.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // ---- shared state -----------------------------------------------------------------------------
 
 struct Ctx {
@@ -222,13 +258,27 @@ struct Ctx {
   int nclusters;       // number of pairs
 };
 
+// try_wait that lets the thread sleep until the phase completes or `ns` passed, so that
+// waiting roles take few issue slots from the softmax warps on the same scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait that also gives up when another role aborted.
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
   uint64_t* b = c.bar + idx;
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(b, parity)) return true;
+    if (mbar_try_wait_sleep(b, parity, 20000u)) return true;
     if ((i & 31u) == 0) {
       if (*c.abort) return false;
       if (globaltimer_ns() - t0 > c.limit) {
@@ -238,6 +288,12 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity)
       }
     }
   }
+}
+
+// The k-th item of this pair.  Items are ordered longest first; the pairs take them in snake
+// order (round k runs over the pairs backwards when k is odd), which evens out their totals.
+__device__ __forceinline__ int item_of(const Ctx& c, int k) {
+  return k * c.nclusters + ((k & 1) ? c.nclusters - 1 - c.cluster : c.cluster);
 }
 
 struct Item {
@@ -276,7 +332,7 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
   const int full = is_v ? B_VFULL : B_KFULL, empty = is_v ? B_VEMPTY : B_KEMPTY;
   const int off = is_v ? kOffV : kOffK;
   uint32_t kv = 0, it_cnt = 0;
-  for (int idx = c.cluster; idx < n_items; idx += c.nclusters, ++it_cnt) {
+  for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
     const int32_t* row = m.block_tables + (int64_t)I.s * m.max_blocks;
     const int blk0 = I.kv0 / 16;
@@ -327,25 +383,31 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
 
 // MMA issue runs on two threads (warps 1 and 11) so that one thread's instruction issue
 // never delays the other chain: the QK^T issuer releases K and Q stages, the PV issuer
-// releases V stages and O.  They share no TMEM columns (S at 0 / 128, O at 256, P at 384).
+// releases V stages, S / P buffers and O.
+//
+// Tile counters run over all items of the CTA; tile s uses S / P buffer s % 3, and each
+// per-buffer barrier completes once per use, so its phase parity is (s / 3) & 1.
+__device__ __forceinline__ uint32_t buf_of(uint32_t s) { return s % kSBufs; }
+__device__ __forceinline__ uint32_t use_par(uint32_t s) { return (s / kSBufs) & 1u; }
+
 __device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
   const uint32_t sm = smem_u32(c.sm);
-  uint32_t kv = 0, sc = 0, it_cnt = 0;
-  for (int idx = c.cluster; idx < n_items; idx += c.nclusters, ++it_cnt) {
+  uint32_t kv = 0, it_cnt = 0;
+  for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
     const uint32_t qb = it_cnt & 1u;
     if (!wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u)) return;
     const uint32_t qbase = sm + kOffQ + qb * kTile;
     for (int j = 0; j < I.ntiles; ++j) {
-      const uint32_t kvj = kv + j, st = kvj % kStages;
-      const uint32_t s = sc + j, b = s & 1u;
-      if (!wait_bar(c, B_KFULL + st, (kvj / kStages) & 1u)) return;
-      if (!wait_bar(c, B_SFREE + b, ((s >> 1) & 1u) ^ 1u)) return;
+      const uint32_t s = kv + j, st = s % kStages, b = buf_of(s);
+      if (!wait_bar(c, B_KFULL + st, (s / kStages) & 1u)) return;
+      // the buffer's previous tile (s - 3): its P was consumed by its P V
+      if (!wait_bar(c, B_PVDONE + b, use_par(s) ^ 1u)) return;
       tc_fence_after();
       const uint32_t kb = sm + kOffK + st * kTile;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc_mma(tmem + b * 128, sdesc(qbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
+        tc_mma(tmem + col_s(b), sdesc(qbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
                sdesc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), kIdescQK,
                kk > 0 ? 1u : 0u);
       tc_commit(c.bar + B_SFULL + b);
@@ -353,33 +415,54 @@ __device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_i
       if (j == I.ntiles - 1) tc_commit(c.bar + B_QEMPTY + qb);
     }
     kv += I.ntiles;
-    sc += I.ntiles;
   }
 }
 
+// The whole warp runs the PV loop (lane 0 issues): the V rows of a sequence's last block at
+// positions >= n were never written and may hold anything, so before the MMAs read that block
+// the warp zeroes them in this CTA's copy of the stage.  This role consumes the V stages in
+// order, so its V-full wait always names the right phase.
 __device__ void pv_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
-  const uint32_t sm = smem_u32(c.sm);
-  uint32_t kv = 0, pv = 0, it_cnt = 0;
-  for (int idx = c.cluster; idx < n_items; idx += c.nclusters, ++it_cnt) {
+  const int lane = threadIdx.x & 31;
+  uint32_t kv = 0, it_cnt = 0;
+  for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
+    const int last_blk = (I.n - 1) / 16;
+    const int fix_rel = last_blk * 16 - I.kv0;  // offset of that block inside the item's keys
+    const bool need_fix = (I.n % 16) != 0 && last_blk < I.nblk_vis && fix_rel >= 0;
+    const int fix_tile = need_fix ? fix_rel / kBN : -1;
     for (int j = 0; j < I.ntiles; ++j) {
-      if (j == 0 && !wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u)) return;
-      if (!wait_bar(c, B_PFULL, pv & 1u)) return;
-      const uint32_t kvj = kv + j, st = kvj % kStages;
-      if (!wait_bar(c, B_VFULL + st, (kvj / kStages) & 1u)) return;
-      tc_fence_after();
-      const uint32_t vb = sm + kOffV + st * kTile;
+      const uint32_t s = kv + j, st = s % kStages, b = buf_of(s);
+      if (j == 0 && !__all_sync(kFull, wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u))) return;
+      if (!__all_sync(kFull, wait_bar(c, B_PFULL + b, use_par(s)))) return;
+      if (!__all_sync(kFull, wait_bar(c, B_VFULL + st, (s / kStages) & 1u))) return;
+      uint8_t* vt = c.sm + kOffV + st * kTile;
+      if (j == fix_tile) {
+        const int blk = (fix_rel % kBN) / 16, first = I.n % 16;
+        const int chunks = (16 - first) * 2 * 8;  // rows x halves x 16-byte chunks
+        for (int i = lane; i < chunks; i += 32) {
+          const int rr = first + i / 16, half = (i / 8) & 1, ch = i & 7;
+          *reinterpret_cast<uint4*>(vt + half * kHalf + (blk * 16 + rr) * 128 + ch * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();  // the MMA reads V through the async proxy
+        __syncwarp();
+      }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t vb = smem_u32(vt), pb = tmem + col_s(b);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        tc_mma_ta(tmem + kColO, tmem + kColPh + kk * 8, sdesc(vb + kk * 2048, kHalf, 1024),
-                  kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_ta(tmem + kColO, pb + col_p(kk, 0), sdesc(vb + kk * 2048, kHalf, 1024),
+                    kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        tc_mma_ta(tmem + kColO, tmem + kColPl + kk * 8, sdesc(vb + kk * 2048, kHalf, 1024),
-                  kIdescPV, 1u);
-      tc_commit(c.bar + B_ODONE);
-      tc_commit_mc(c.bar + B_VEMPTY + st, 0x3);
-      ++pv;
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_ta(tmem + kColO, pb + col_p(kk, 1), sdesc(vb + kk * 2048, kHalf, 1024),
+                    kIdescPV, 1u);
+        tc_commit(c.bar + B_PVDONE + b);
+        tc_commit_mc(c.bar + B_VEMPTY + st, 0x3);
+      }
+      __syncwarp();
     }
     kv += I.ntiles;
   }
@@ -398,10 +481,9 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
   const int r = 32 * quad + lane;  // this thread's query row == TMEM lane
   const int col0 = hf * 64;
   const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
-  const int tid256 = threadIdx.x - 64;  // 0..255 across the softmax warps
   float* xchg = reinterpret_cast<float*>(c.sm + kOffXchg);  // [half][row]
-  uint32_t kv = 0, sc = 0, pv = 0;
-  for (int idx = c.cluster; idx < n_items; idx += c.nclusters) {
+  uint32_t kv = 0;
+  for (int k = 0, idx; (idx = item_of(c, k)) < n_items; ++k) {
     const Item I = load_item(p, idx, c.rank);
     const int tl = r / m.group;
     const bool valid = tl < I.n_tok;
@@ -413,22 +495,17 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       end = m.causal ? pos + 1 : I.n;
       start = m.window > 0 ? max(0, end - m.window) : 0;
     }
-    // the sequence's last block is partly unwritten past n: which tile / block holds it
-    const int last_blk = (I.n - 1) / 16;
-    const int fix_rel = last_blk * 16 - I.kv0;  // offset of that block inside the item's keys
-    const bool need_fix = (I.n % 16) != 0 && last_blk < I.nblk_vis && fix_rel >= 0;
-    const int fix_tile = need_fix ? fix_rel / kBN : -1;
-
     float m_ref = -INFINITY, l = 0.f;
     for (int j = 0; j < I.ntiles; ++j) {
-      const uint32_t s = sc + j, b = s & 1u;
-      if (!__all_sync(kFull, wait_bar(c, B_SFULL + b, (s >> 1) & 1u))) return;
+      const uint32_t s = kv + j, b = buf_of(s);
+      const uint32_t sbase = tmem + lane_addr + col_s(b) + col0;  // this thread's S / P columns
+      if (!__all_sync(kFull, wait_bar(c, B_SFULL + b, use_par(s)))) return;
       tc_fence_after();
       float x[64];
       {
         uint32_t v[2][32];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) tmem_ld32(tmem + lane_addr + b * 128 + col0 + q * 32, v[q]);
+        for (int q = 0; q < 2; ++q) tmem_ld32(sbase + q * 32, v[q]);
 #pragma unroll
         for (int q = 0; q < 2; ++q) tmem_wait_ld(v[q]);
 #pragma unroll
@@ -436,9 +513,6 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[q * 32 + i] = __uint_as_float(v[q][i]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar + B_SFREE + b);
 
       // mask the raw scores (scale > 0 on this path, so the max commutes with it); an
       // invalid row has start == end == 0 and masks everything
@@ -468,20 +542,39 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
         m_ref = m_new;
         l *= alpha;
       }
+      // p = 2^(x * scale_log2 - m_ref) two at a time, the row sum, and p split into a bf16
+      // pair hi + lo (hi = RNE(p), lo = RNE(p - hi)) for the two P V MMAs
       const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
-      float rs[8];
+      const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2), nb2 = f2_pack(nbase, nbase);
+      uint32_t hi[32], lo[32];
+      {
+        uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) rs[k] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        x[i] = fast_exp2(fmaf(x[i], p.scale_log2, nbase));
-        rs[i & 7] += x[i];
+        for (int e = 0; e < 32; ++e) {
+          float a, bb;
+          f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sl2, nb2), a, bb);
+          a = fast_exp2(a);
+          bb = fast_exp2(bb);
+          const uint64_t pp = f2_pack(a, bb);
+          rs2[e & 3] = f2_add(rs2[e & 3], pp);
+          hi[e] = pack_bf16x2(a, bb);
+          const uint64_t hv =
+              f2_pack(__uint_as_float(hi[e] << 16), __uint_as_float(hi[e] & 0xffff0000u));
+          float la, lb;
+          f2_unpack(f2_sub(pp, hv), la, lb);
+          lo[e] = pack_bf16x2(la, lb);
+        }
+        float r0, r1, r2, r3, r4, r5, r6, r7;
+        f2_unpack(rs2[0], r0, r1);
+        f2_unpack(rs2[1], r2, r3);
+        f2_unpack(rs2[2], r4, r5);
+        f2_unpack(rs2[3], r6, r7);
+        l += ((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7));
       }
-      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
 
-      // P_{j-1} V_{j-1} done: the P buffer is free and O is stable
-      if (j >= 1 && !__all_sync(kFull, wait_bar(c, B_ODONE, (pv + j - 1) & 1u))) return;
+      // O rescale: only after P_{j-1} V_{j-1} is done (O stable); most tiles skip both
       if (j >= 1 && __any_sync(kFull, resc)) {
+        if (!__all_sync(kFull, wait_bar(c, B_PVDONE + buf_of(s - 1), use_par(s - 1)))) return;
         tc_fence_after();
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -494,37 +587,13 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
         }
         tmem_wait_st();
       }
-      if (j == fix_tile) {
-        // zero the V rows of the sequence's last block at positions >= n (never written)
-        const uint32_t kvj = kv + j, st = kvj % kStages;
-        if (!__all_sync(kFull, wait_bar(c, B_VFULL + st, (kvj / kStages) & 1u))) return;
-        const int blk = (fix_rel % kBN) / 16, first = I.n % 16;
-        uint8_t* vt = c.sm + kOffV + st * kTile;
-        const int chunks = (16 - first) * 2 * 8;  // rows x halves x 16-byte chunks
-        for (int i = tid256; i < chunks; i += 256) {
-          const int rr = first + i / 16, half = (i / 8) & 1, ch = i & 7;
-          *reinterpret_cast<uint4*>(vt + half * kHalf + (blk * 16 + rr) * 128 + ch * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();  // the MMA reads V through the async proxy
-      }
-      // this half of P as bf16 hi / lo pairs into tensor memory (columns 32 * half ...)
-      {
-        uint32_t hi[32], lo[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float a = x[2 * e], bb = x[2 * e + 1];
-          hi[e] = pack_bf16x2(a, bb);
-          const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[e]));
-          lo[e] = pack_bf16x2(a - hv.x, bb - hv.y);
-        }
-        tmem_st32(tmem + lane_addr + kColPh + hf * 32, hi);
-        tmem_st32(tmem + lane_addr + kColPl + hf * 32, lo);
-        tmem_wait_st();
-      }
+      // this half of P over the scores it came from
+      tmem_st32(sbase, hi);
+      tmem_st32(sbase + 32, lo);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar + B_PFULL);
+      if (lane == 0) mbar_arrive(c.bar + B_PFULL + b);
     }
 
     // epilogue: o = O / l, with l summed over both column halves
@@ -534,7 +603,8 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       l += xchg[(hf ^ 1) * 128 + r];
       pair_sync(quad);  // both read before either writes again
     }
-    if (!__all_sync(kFull, wait_bar(c, B_ODONE, (pv + I.ntiles - 1) & 1u))) return;
+    const uint32_t last = kv + I.ntiles - 1;
+    if (!__all_sync(kFull, wait_bar(c, B_PVDONE + buf_of(last), use_par(last)))) return;
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16* dst =
@@ -560,8 +630,6 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar + B_OFREE);
     kv += I.ntiles;
-    sc += I.ntiles;
-    pv += I.ntiles;
   }
 }
 
@@ -579,9 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     flags[0] = status_set(p.status) ? 1 : 0;
     flags[1] = 0;
-    // k_empty / v_empty: one arrival from each CTA of the pair; s_free / p_full / o_free: one
-    // per softmax warp
-    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 2, 2, 1, 1, 2, 2, 1, 1, 8, 8, 8, 1, 8, 2};
+    // k_empty / v_empty: one arrival from each CTA of the pair; p_full / o_free: one per
+    // softmax warp; fin: one per MMA-issuing thread
+    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 2, 2, 1, 1, 2, 2,
+                                       1, 1, 1, 8, 8, 8, 1, 1, 1, 8, 2};
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, counts[i]);
     prefetch_tmap(&tq);
     prefetch_tmap(&tk);
@@ -608,11 +677,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 2 + kSoftWarps) {
     producer(c, p, &tq, &tv, true, n_items);
   } else if (warp == 1 || warp == 3 + kSoftWarps) {
+    if (warp == 1) {
+      if ((threadIdx.x & 31) == 0) s_issuer(c, p, tmem, n_items);
+    } else {
+      pv_issuer(c, p, tmem, n_items);
+    }
+    __syncwarp();
     if ((threadIdx.x & 31) == 0) {
-      if (warp == 1)
-        s_issuer(c, p, tmem, n_items);
-      else
-        pv_issuer(c, p, tmem, n_items);
       // every MMA issued by either thread has completed before the tensor memory is released
       tc_commit(bar + B_FIN);
       uint64_t t0 = globaltimer_ns();

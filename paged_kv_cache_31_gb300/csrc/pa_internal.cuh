@@ -174,11 +174,12 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not lan
 //   [tok_off, tok_off + T)        token -> sequence
 //   [cost_off, cost_off + S)      per sequence: keys its query rows can see (work estimate)
 //   [mma_off, + 2 * mma_cap)      int2 items (seq, 16-row tile), longest first
-//   [tc_off, + 4 * tc_cap)        int4 items (seq, 256-row item, kv lo, kv hi)
+//   [tc_off, + 4 * tc_cap)        int4 items (seq, 256-row item, kv lo, kv hi), longest first
+//   [tc_tmp_off, + 4 * tc_cap)    the same items in sequence order (planning scratch)
 constexpr int kPlanHeaderWords = 16;
 
 struct PlanLayout {
-  int64_t tok_off, cost_off, mma_off, tc_off;
+  int64_t tok_off, cost_off, mma_off, tc_off, tc_tmp_off;
   int64_t mma_cap, tc_cap;
   int64_t words;
   int32_t use_tc;       // prefill-class sequences go to the tcgen05 kernel
@@ -194,7 +195,8 @@ inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t grou
   L.cost_off = L.tok_off + num_tokens;
   L.mma_off = (L.cost_off + num_seqs + 3) & ~int64_t(3);
   L.tc_off = (L.mma_off + 2 * L.mma_cap + 3) & ~int64_t(3);
-  L.words = L.tc_off + 4 * L.tc_cap;
+  L.tc_tmp_off = L.tc_off + 4 * L.tc_cap;
+  L.words = L.tc_tmp_off + 4 * L.tc_cap;
   L.use_tc = 0;
   L.tc_min_rows = 64;
   return L;
