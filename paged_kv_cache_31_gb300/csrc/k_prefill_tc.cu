@@ -15,8 +15,9 @@
 // One CTA per SM, persistent over items, 12 warps:
 //   warp 0      TMA producer of Q (two buffers, so the next item's Q loads while this one
 //               finishes) and K_j through a 2-stage ring; warp 10 produces V_j the same way;
-//   warp 1      TMEM owner and QK^T issuer (one thread); warp 11 issues PV (one lane; the
-//               warp first zeroes the never-written V rows past a sequence's end):
+//   warp 1      TMEM owner and QK^T issuer; warp 11 issues PV (it also zeroes the
+//               never-written V rows past a sequence's end).  Lane 0 issues, in warp-uniform
+//               code:
 //                 S_j = Q K_j^T      (M 128, N 128, K 128: 8 MMAs, K-major operands)
 //                 O  += P_j V_j      (P as a bf16 hi/lo pair read from TMEM: 16 MMAs, V MN-major)
 //               TMEM columns: three S buffers at 0 / 128 / 384, O at 256.  P_j is written over
@@ -82,26 +83,34 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+// The MMA issuers run as whole warps in uniform control flow (so the compiler keeps the
+// descriptors in uniform registers; a lone thread in a divergent branch issues at about half
+// the tensor core's rate), and only lane 0 executes the tcgen05 instructions: the wrappers
+// below are predicated on %laneid inside the asm.  Every MMA and commit of a role therefore
+// comes from the same thread, as tcgen05.commit requires.
+__device__ __forceinline__ void tc_commit_l0(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n\t.reg .u32 l;\n\t.reg .pred e;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_u32(bar))
       : "memory");
 }
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma_l0(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .u32 l;\n\t.reg .pred e, p;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Same with the A operand in tensor memory (row r in lane r, two bf16 per 32-bit column).
-__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma_ta_l0(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .u32 l;\n\t.reg .pred e, p;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -204,10 +213,11 @@ __device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map
       : "memory");
 }
 // Arrive on the barrier at this offset in every CTA of `mask` once this thread's MMAs are done.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+__device__ __forceinline__ void tc_commit_mc_l0(uint64_t* bar, uint16_t mask) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "{\n\t.reg .u32 l;\n\t.reg .pred e;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
       "h"(mask)
       : "memory");
 }
@@ -396,23 +406,24 @@ __device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_i
   for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
     const uint32_t qb = it_cnt & 1u;
-    if (!wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u)) return;
+    if (!__all_sync(kFull, wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u))) return;
     const uint32_t qbase = sm + kOffQ + qb * kTile;
     for (int j = 0; j < I.ntiles; ++j) {
       const uint32_t s = kv + j, st = s % kStages, b = buf_of(s);
-      if (!wait_bar(c, B_KFULL + st, (s / kStages) & 1u)) return;
+      if (!__all_sync(kFull, wait_bar(c, B_KFULL + st, (s / kStages) & 1u))) return;
       // the buffer's previous tile (s - 3): its P was consumed by its P V
-      if (!wait_bar(c, B_PVDONE + b, use_par(s) ^ 1u)) return;
+      if (!__all_sync(kFull, wait_bar(c, B_PVDONE + b, use_par(s) ^ 1u))) return;
       tc_fence_after();
       const uint32_t kb = sm + kOffK + st * kTile;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc_mma(tmem + col_s(b), sdesc(qbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-               sdesc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), kIdescQK,
-               kk > 0 ? 1u : 0u);
-      tc_commit(c.bar + B_SFULL + b);
-      tc_commit_mc(c.bar + B_KEMPTY + st, 0x3);  // both CTAs must be done before a refill
-      if (j == I.ntiles - 1) tc_commit(c.bar + B_QEMPTY + qb);
+        tc_mma_l0(tmem + col_s(b), sdesc(qbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
+                  sdesc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), kIdescQK,
+                  kk > 0 ? 1u : 0u);
+      tc_commit_l0(c.bar + B_SFULL + b);
+      tc_commit_mc_l0(c.bar + B_KEMPTY + st, 0x3);  // both CTAs must be done before a refill
+      if (j == I.ntiles - 1) tc_commit_l0(c.bar + B_QEMPTY + qb);
+      __syncwarp();
     }
     kv += I.ntiles;
   }
@@ -448,20 +459,18 @@ __device__ void pv_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_
         fence_proxy_async_smem();  // the MMA reads V through the async proxy
         __syncwarp();
       }
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t vb = smem_u32(vt), pb = tmem + col_s(b);
+      tc_fence_after();
+      const uint32_t vb = smem_u32(vt), pb = tmem + col_s(b);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_ta(tmem + kColO, pb + col_p(kk, 0), sdesc(vb + kk * 2048, kHalf, 1024),
-                    kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma_ta_l0(tmem + kColO, pb + col_p(kk, 0), sdesc(vb + kk * 2048, kHalf, 1024),
+                     kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_ta(tmem + kColO, pb + col_p(kk, 1), sdesc(vb + kk * 2048, kHalf, 1024),
-                    kIdescPV, 1u);
-        tc_commit(c.bar + B_PVDONE + b);
-        tc_commit_mc(c.bar + B_VEMPTY + st, 0x3);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma_ta_l0(tmem + kColO, pb + col_p(kk, 1), sdesc(vb + kk * 2048, kHalf, 1024),
+                     kIdescPV, 1u);
+      tc_commit_l0(c.bar + B_PVDONE + b);
+      tc_commit_mc_l0(c.bar + B_VEMPTY + st, 0x3);
       __syncwarp();
     }
     kv += I.ntiles;
@@ -677,15 +686,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 2 + kSoftWarps) {
     producer(c, p, &tq, &tv, true, n_items);
   } else if (warp == 1 || warp == 3 + kSoftWarps) {
-    if (warp == 1) {
-      if ((threadIdx.x & 31) == 0) s_issuer(c, p, tmem, n_items);
-    } else {
+    if (warp == 1)
+      s_issuer(c, p, tmem, n_items);
+    else
       pv_issuer(c, p, tmem, n_items);
-    }
     __syncwarp();
+    // every MMA issued by either warp has completed before the tensor memory is released
+    tc_commit_l0(bar + B_FIN);
     if ((threadIdx.x & 31) == 0) {
-      // every MMA issued by either thread has completed before the tensor memory is released
-      tc_commit(bar + B_FIN);
       uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(bar + B_FIN, 0) && globaltimer_ns() - t0 < 1000000000ull) {
       }
