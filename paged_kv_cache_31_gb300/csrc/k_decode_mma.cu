@@ -75,12 +75,15 @@ __global__ void __launch_bounds__(NW * 32, 2)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x < NW * NS) mbar_init(&full[threadIdx.x], 1);
   if (threadIdx.x == 0) {
-    // failed validation or an earlier sticky error: the whole CTA writes nothing
-    *fail = status_set(p.status) ? 1 : 0;
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
   }
   fence_mbar_init();
+  // varlen launches overlap the kernels before them (programmatic dependent launch): the
+  // plan, the status word and the inputs are read only after those have finished
+  pdl_wait();
+  // failed validation or an earlier sticky error: the whole CTA writes nothing
+  if (threadIdx.x == 0) *fail = status_set(p.status) ? 1 : 0;
   __syncthreads();
   if (*reinterpret_cast<volatile int*>(fail)) return;
 
@@ -447,9 +450,17 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Para
                 "merge area must fit in the ring");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(grid_x, SPLIT ? p.m.num_kv_heads : 1);
-  kern<<<grid, kNW * 32, smem, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_x, SPLIT ? p.m.num_kv_heads : 1);
+  cfg.blockDim = dim3(kNW * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = SPLIT ? 0 : 1;  // varlen: overlaps the plan (or prefill) kernel
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace

@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(1024)
   __shared__ int s_hist[kCostBuckets];    // 16-row tiles per cost bucket
   __shared__ int s_hist_t[kCostBuckets];  // 256-row items per cost bucket
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  pdl_launch_dependents();  // the attention kernels' prologues may overlap this kernel
   if (tid == 0) s_err = status_set(status) ? -1 : 0;
   __syncthreads();
   if (s_err == 0) {
@@ -98,18 +99,36 @@ __global__ void __launch_bounds__(1024)
       }
       const int32_t* row = m.block_tables + (int64_t)s * m.max_blocks;
       bool bad = false;
-      for (int64_t i = lane; i < need; i += 32) {
-        const int32_t id = row[i];
-        bad |= (id < 0 || (int64_t)id >= m.num_blocks);
+      // eight loads in flight per lane: these loops are bound by load latency, not bandwidth
+      for (int64_t base = 0; base < need; base += 256) {
+        int32_t id[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int64_t i = base + lane + 32 * u;
+          id[u] = i < need ? row[i] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) bad |= (id[u] < 0 || (int64_t)id[u] >= m.num_blocks);
       }
       int lo = INT_MAX, hi = 0;
-      for (int t = a + lane; t < b; t += 32) {
-        const int32_t pos = m.positions[t];
-        bad |= (pos < 0 || pos >= n);
-        plan[L.tok_off + t] = s;
-        const int e = m.causal ? pos + 1 : n;
-        lo = min(lo, m.window > 0 ? max(0, e - m.window) : 0);
-        hi = max(hi, e);
+      for (int t0 = a; t0 < b; t0 += 256) {
+        int32_t pos[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int t = t0 + lane + 32 * u;
+          pos[u] = t < b ? m.positions[t] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int t = t0 + lane + 32 * u;
+          if (t < b) {
+            bad |= (pos[u] < 0 || pos[u] >= n);
+            plan[L.tok_off + t] = s;
+            const int e = m.causal ? pos[u] + 1 : n;
+            lo = min(lo, m.window > 0 ? max(0, e - m.window) : 0);
+            hi = max(hi, e);
+          }
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {

@@ -14,7 +14,8 @@
 //
 // One CTA per SM, persistent over items, 12 warps:
 //   warp 0      TMA producer of Q (two buffers, so the next item's Q loads while this one
-//               finishes) and K_j through a 2-stage ring; warp 10 produces V_j the same way;
+//               finishes) and K_j through a 2-stage ring; warp 10 produces V_j through a
+//               3-stage ring;
 //   warp 1      TMEM owner and QK^T issuer; warp 11 issues PV (it also zeroes the
 //               never-written V rows past a sequence's end).  Lane 0 issues, in warp-uniform
 //               code:
@@ -45,12 +46,13 @@ constexpr int kBN = 128;          // keys per tile (8 blocks of 16)
 constexpr int kD = 128;           // head size on this path
 constexpr int kHalf = 16384;      // one 64-dim half of a 128-row bf16 tile
 constexpr int kTile = 2 * kHalf;  // 128 x 128 bf16
-constexpr int kStages = 2;
+constexpr int kStagesK = 2;  // K ring (a K tile is released as soon as its S MMAs finish)
+constexpr int kStagesV = 3;  // V ring (held until P V, so it needs one more stage in flight)
 constexpr int kOffQ = 0;                          // two Q buffers (consecutive items)
 constexpr int kOffK = kOffQ + 2 * kTile;
-constexpr int kOffV = kOffK + kStages * kTile;
-constexpr int kOffBar = kOffV + kStages * kTile;
-constexpr int kNumBarsMax = 24;
+constexpr int kOffV = kOffK + kStagesK * kTile;
+constexpr int kOffBar = kOffV + kStagesV * kTile;
+constexpr int kNumBarsMax = 26;
 constexpr int kOffTmem = kOffBar + kNumBarsMax * 8;
 constexpr int kOffFlag = kOffTmem + 16;
 constexpr int kOffXchg = kOffFlag + 16;               // row max / sum exchange, 2 x 128 fp32
@@ -70,10 +72,10 @@ __device__ __forceinline__ uint32_t col_p(int kstep, int lo) {
 
 // barrier indices (the per-buffer ones are consecutive)
 enum {
-  B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 6, B_VFULL = 8, B_VEMPTY = 10, B_SFULL = 12,
-  B_PFULL = 15, B_PVDONE = 18, B_OFREE = 21, B_FIN = 22
+  B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 6, B_VFULL = 8, B_VEMPTY = 11, B_SFULL = 14,
+  B_PFULL = 17, B_PVDONE = 20, B_OFREE = 23, B_FIN = 24
 };
-constexpr int kNumBars = 23;
+constexpr int kNumBars = 25;
 
 // ---- tcgen05 / TMEM wrappers -----------------------------------------------------------------
 
@@ -341,6 +343,7 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
   const VarlenMeta& m = p.m;
   const int full = is_v ? B_VFULL : B_KFULL, empty = is_v ? B_VEMPTY : B_KEMPTY;
   const int off = is_v ? kOffV : kOffK;
+  const uint32_t nst = is_v ? kStagesV : kStagesK;
   uint32_t kv = 0, it_cnt = 0;
   for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
@@ -373,7 +376,7 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
       for (int b = 0; b < 8; ++b) ids[b] = __shfl_sync(kFull, id, b);
       bool ok = true;
       if (lane == 0) {
-        const uint32_t st = kv % kStages, ph = (kv / kStages) & 1u;
+        const uint32_t st = kv % nst, ph = (kv / nst) & 1u;
         ok = wait_bar(c, empty + st, ph ^ 1u);
         if (ok) {
           mbar_arrive_expect_tx(c.bar + full + st, kTile);
@@ -409,8 +412,8 @@ __device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_i
     if (!__all_sync(kFull, wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u))) return;
     const uint32_t qbase = sm + kOffQ + qb * kTile;
     for (int j = 0; j < I.ntiles; ++j) {
-      const uint32_t s = kv + j, st = s % kStages, b = buf_of(s);
-      if (!__all_sync(kFull, wait_bar(c, B_KFULL + st, (s / kStages) & 1u))) return;
+      const uint32_t s = kv + j, st = s % kStagesK, b = buf_of(s);
+      if (!__all_sync(kFull, wait_bar(c, B_KFULL + st, (s / kStagesK) & 1u))) return;
       // the buffer's previous tile (s - 3): its P was consumed by its P V
       if (!__all_sync(kFull, wait_bar(c, B_PVDONE + b, use_par(s) ^ 1u))) return;
       tc_fence_after();
@@ -443,10 +446,10 @@ __device__ void pv_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_
     const bool need_fix = (I.n % 16) != 0 && last_blk < I.nblk_vis && fix_rel >= 0;
     const int fix_tile = need_fix ? fix_rel / kBN : -1;
     for (int j = 0; j < I.ntiles; ++j) {
-      const uint32_t s = kv + j, st = s % kStages, b = buf_of(s);
+      const uint32_t s = kv + j, st = s % kStagesV, b = buf_of(s);
       if (j == 0 && !__all_sync(kFull, wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u))) return;
       if (!__all_sync(kFull, wait_bar(c, B_PFULL + b, use_par(s)))) return;
-      if (!__all_sync(kFull, wait_bar(c, B_VFULL + st, (s / kStages) & 1u))) return;
+      if (!__all_sync(kFull, wait_bar(c, B_VFULL + st, (s / kStagesV) & 1u))) return;
       uint8_t* vt = c.sm + kOffV + st * kTile;
       if (j == fix_tile) {
         const int blk = (fix_rel % kBN) / 16, first = I.n % 16;
@@ -492,16 +495,21 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
   const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
   float* xchg = reinterpret_cast<float*>(c.sm + kOffXchg);  // [half][row]
   uint32_t kv = 0;
-  for (int k = 0, idx; (idx = item_of(c, k)) < n_items; ++k) {
-    const Item I = load_item(p, idx, c.rank);
+  // an item's metadata (plan entry, sequence bounds, this row's position) is a chain of
+  // dependent loads: the next item's is fetched while the current one's last P V runs
+  Item In{};
+  int pos_n = 0;
+  if (item_of(c, 0) < n_items) In = load_item(p, item_of(c, 0), c.rank);
+  if (r / m.group < In.n_tok) pos_n = m.positions[In.t0 + r / m.group];
+  for (int k = 0; item_of(c, k) < n_items; ++k) {
+    const Item I = In;
     const int tl = r / m.group;
     const bool valid = tl < I.n_tok;
     const int t = I.t0 + (valid ? tl : 0);
     const int h = I.kvh * m.group + r % m.group;
     int start = 0, end = 0;
     if (valid) {
-      const int pos = m.positions[t];
-      end = m.causal ? pos + 1 : I.n;
+      end = m.causal ? pos_n + 1 : I.n;
       start = m.window > 0 ? max(0, end - m.window) : 0;
     }
     float m_ref = -INFINITY, l = 0.f;
@@ -527,9 +535,10 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       // invalid row has start == end == 0 and masks everything
       const int key0 = I.kv0 + j * kBN + col0;
       if (!(key0 >= start && key0 + 64 <= end)) {
+        // visible columns of this thread: [a, b) within its 64
+        const int a = start - key0, bnd = end - key0;
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          x[i] = (key0 + i >= start && key0 + i < end) ? x[i] : -INFINITY;
+        for (int i = 0; i < 64; ++i) x[i] = (i >= a && i < bnd) ? x[i] : -INFINITY;
       }
       float mx[8];
 #pragma unroll
@@ -605,6 +614,10 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       if (lane == 0) mbar_arrive(c.bar + B_PFULL + b);
     }
 
+    if (item_of(c, k + 1) < n_items) {
+      In = load_item(p, item_of(c, k + 1), c.rank);
+      if (tl < In.n_tok) pos_n = m.positions[In.t0 + tl];
+    }
     // epilogue: o = O / l, with l summed over both column halves
     {
       xchg[hf * 128 + r] = l;
@@ -618,11 +631,14 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     const float inv = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16* dst =
         reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * m.num_heads + h) * kD + col0;
+    uint32_t oo[2][32];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tmem_ld32(tmem + lane_addr + kColO + col0 + q * 32, oo[q]);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tmem_wait_ld(oo[q]);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t o[32];
-      tmem_ld32(tmem + lane_addr + kColO + col0 + q * 32, o);
-      tmem_wait_ld(o);
+      const uint32_t (&o)[32] = oo[q];
       if (valid) {
 #pragma unroll
         for (int i = 0; i < 32; i += 8) {
@@ -654,11 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
-    flags[0] = status_set(p.status) ? 1 : 0;
     flags[1] = 0;
     // k_empty / v_empty: one arrival from each CTA of the pair; p_full / o_free: one per
     // softmax warp; fin: one per MMA-issuing thread
-    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 2, 2, 1, 1, 2, 2,
+    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 2, 2, 1, 1, 1, 2, 2, 2,
                                        1, 1, 1, 8, 8, 8, 1, 1, 1, 8, 2};
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, counts[i]);
     prefetch_tmap(&tq);
@@ -676,6 +691,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   cluster_sync();  // the partner's barriers are initialised before any multicast reaches them
   tc_fence_after();
+  // everything above overlaps the planning kernel (programmatic dependent launch); the plan
+  // and the status word are read only after it has finished
+  pdl_wait();
+  if (threadIdx.x == 0) flags[0] = status_set(p.status) ? 1 : 0;
+  __syncthreads();
+  pdl_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   Ctx c{sm, bar, reinterpret_cast<volatile int*>(flags + 1), p.status, p.wait_limit_ns,
         cluster_rank(), (int)cluster_id_x(), (int)num_clusters_x()};
@@ -726,13 +747,15 @@ cudaError_t launch_tc_prefill(const CUtensorMap& tq, const CUtensorMap& tk, cons
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the plan kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_tc_prefill, tq, tk, tv, p);
 }
 

@@ -88,6 +88,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization
+// may start while the kernel before it on the stream still runs; pdl_wait() returns once that
+// kernel has finished and its writes are visible (at once when there is no such dependency).
+// pdl_launch_dependents() lets the next such kernel be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 3-D tiled TMA load global -> shared, completing `bytes` on `bar`.  c0 is the innermost
 // coordinate; callers keep c0 * sizeof(element) a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int32_t c0,
