@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--secondary-steps", type=int, default=30)
+    ap.add_argument("--case", default="bench", choices=["bench", "prefill-chunks"],
+                    help="prefill-chunks: time only the attention call on the mixed batch's "
+                         "prefill chunks (own pool; a small case for profiling)")
     return ap.parse_args()
 
 
@@ -300,16 +303,36 @@ class Runner:
         self.attention(m)
 
 
-def time_calls(fn, n, stream):
+def time_calls(fn, n, stream, flush=None):
+    """Mean ms per call of fn over n calls, timed with CUDA events on `stream`.  With `flush`
+    (a buffer larger than L2) every call is timed on its own after overwriting the buffer,
+    so no call finds the previous one's inputs in L2."""
     import torch
 
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:
+        flush.add_(1)
+        a.record(stream)
         fn()
-    e1.record(stream)
+        b.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / n
+    return sum(a.elapsed_time(b) for a, b in ev) / n
+
+
+def l2_flush_buffer(dev):
+    """256 MB, about twice the GB300's L2."""
+    import torch
+
+    return torch.zeros(64 << 20, dtype=torch.float32, device=dev)
 
 
 def secondary(pa, dev, args, peaks, stream):
@@ -334,8 +357,10 @@ def secondary(pa, dev, args, peaks, stream):
     for _ in range(3):
         rp.attention()
         rd.attention()
-    p_ms = time_calls(rp.attention, n, stream)
+    flush = l2_flush_buffer(dev)
+    p_ms = time_calls(rp.attention, n, stream, flush=flush)  # its K/V would fit in L2
     d_ms = time_calls(rd.attention, n, stream)
+    del flush
     fl, kvd = attn_flops(wp), kv_bytes(wd)
     res["mixed"] = {
         "workload": w3.name, "tokens_per_s": w3.num_tokens / (full_ms * 1e-3),
@@ -343,6 +368,7 @@ def secondary(pa, dev, args, peaks, stream):
         "prefill": {"tokens": wp.num_tokens, "flops": fl, "ms": p_ms,
                     "tflops": fl / (p_ms * 1e-3) / 1e12,
                     "frac_of_bf16_peak": fl / (p_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                    "l2": "flushed between calls",
                     "bound": "tensor", "peak_tflops": peaks["bf16_tflops"],
                     "traffic": ncu_traffic("k_tc_prefill", wp.name)},
         "decode": {"tokens": wd.num_tokens, "kv_bytes": kvd, "ms": d_ms,
@@ -403,6 +429,20 @@ def main():
     from paged_kv_cache_31_gb300 import binding as pa
 
     peaks = measured_peaks()
+    if args.case == "prefill-chunks":
+        wp = workloads.prefill_chunks(seed=args.seed, device=dev)
+        rp = Runner(pa, wp)
+        for _ in range(max(3, args.warmup)):
+            rp.attention()
+        ms = time_calls(rp.attention, args.steps, torch.cuda.current_stream(),
+                        flush=l2_flush_buffer(dev))
+        assert pa.pa_device_status() == pa.PA_OK
+        fl = attn_flops(wp)
+        print(json.dumps({"case": wp.name, "flops": fl, "ms": ms, "l2": "flushed between calls",
+                          "tflops": fl / (ms * 1e-3) / 1e12,
+                          "frac_of_bf16_peak": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}),
+              flush=True)
+        return
     w = workloads.named(args.config, seed=args.seed, device=dev)
     kvb = kv_bytes(w)
     flops = attn_flops(w)

@@ -44,6 +44,7 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
 // Work buckets for ordering: a cost c > 0 maps to 16 sub-buckets per power of two
 // (descending: the largest costs get the smallest bucket index).
 constexpr int kCostBuckets = 512;
+constexpr int kPlanCacheSeqs = 8192;  // sequences whose q_len / cost the plan keeps in smem
 __device__ __forceinline__ int cost_bucket(int c) {
   if (c <= 0) return kCostBuckets - 1;
   const int lg = 31 - __clz(c);
@@ -53,80 +54,71 @@ __device__ __forceinline__ int cost_bucket(int c) {
 
 // Validation and planning of one pa_varlen_forward call (tinyllm section 2.6 checks), in a
 // single CTA so that the work list can be built with one block-wide scan:
-//  A. query_start_loc starts at 0, never decreases, ends at num_tokens;
-//  B. for each sequence with query tokens: seq_len >= 1, ceil(seq_len / b) <= max_blocks,
-//     those table entries inside the pool, query positions inside [0, seq_len); and the
-//     token -> sequence map;
-//  C. the work lists: a sequence's q_len * G query rows (token major, head minor within the
+//  A. per sequence (a warp each): query_start_loc[s] <= query_start_loc[s + 1] <= num_tokens,
+//     query_start_loc[0] == 0 and query_start_loc[num_seqs] == num_tokens; for a sequence with
+//     query tokens: seq_len >= 1, ceil(seq_len / b) <= max_blocks, those table entries inside
+//     the pool, query positions inside [0, seq_len); the token -> sequence map and the keys the
+//     sequence's rows can see (its work estimate);
+//  B. the work lists: a sequence's q_len * G query rows (token major, head minor within the
 //     kv group) are cut into 16-row tiles for the warp-MMA kernel, or, for prefill-class
 //     sequences, into 256-row items for the tcgen05 kernel; both lists are ordered by the
 //     number of keys their rows see, longest first, so the kernels' last units are short.
+// The kernel is bound by the latency of its loads, not by bandwidth: phase A issues each
+// sequence's loads together, and keeps q_len and the work estimate in shared memory (up to
+// kPlanCacheSeqs sequences; larger batches read them back from global memory).
 __global__ void __launch_bounds__(1024)
     k_plan_varlen(VarlenMeta m, int32_t* plan, const PlanLayout L, int* status) {
   __shared__ int s_err;
   __shared__ int s_warp[32];
   __shared__ int s_hist[kCostBuckets];    // 16-row tiles per cost bucket
   __shared__ int s_hist_t[kCostBuckets];  // 256-row items per cost bucket
+  extern __shared__ int s_seq[];          // [2][num_seqs]: q_len, visible keys (when cached)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   pdl_launch_dependents();  // the attention kernels' prologues may overlap this kernel
+  const bool cached = m.num_seqs <= kPlanCacheSeqs;
+  int* s_qlen = s_seq;
+  int* s_cost = s_seq + (cached ? m.num_seqs : 0);
   if (tid == 0) s_err = status_set(status) ? -1 : 0;
-  __syncthreads();
-  if (s_err == 0) {
-    for (int s = tid; s < m.num_seqs; s += blockDim.x) {
-      const int a = m.query_start_loc[s], b = m.query_start_loc[s + 1];
-      if ((s == 0 && a != 0) || b < a) atomicCAS(&s_err, 0, PA_EINVAL);
-    }
-    if (tid == 0 && (int64_t)m.query_start_loc[m.num_seqs] != m.num_tokens)
-      atomicCAS(&s_err, 0, PA_EINVAL);
+  for (int i = tid; i < kCostBuckets; i += blockDim.x) {
+    s_hist[i] = 0;
+    s_hist_t[i] = 0;
   }
   __syncthreads();
   if (s_err == 0) {
+    if (m.num_seqs == 0 && tid == 0 && (int64_t)m.query_start_loc[0] != m.num_tokens)
+      atomicCAS(&s_err, 0, PA_EINVAL);
     for (int s = warp; s < m.num_seqs; s += nwarps) {
       const int a = m.query_start_loc[s], b = m.query_start_loc[s + 1];
-      if (a == b) {
-        if (lane == 0) plan[L.cost_off + s] = 0;
-        continue;
-      }
       const int n = m.seq_lens[s];
-      if (n < 1) {
-        if (lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
-        continue;
-      }
-      const int64_t need = ((int64_t)n + m.block_size - 1) / m.block_size;
-      if (need > m.max_blocks) {
-        if (lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
-        continue;
-      }
-      const int32_t* row = m.block_tables + (int64_t)s * m.max_blocks;
-      bool bad = false;
-      // eight loads in flight per lane: these loops are bound by load latency, not bandwidth
-      for (int64_t base = 0; base < need; base += 256) {
-        int32_t id[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int64_t i = base + lane + 32 * u;
-          id[u] = i < need ? row[i] : 0;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) bad |= (id[u] < 0 || (int64_t)id[u] >= m.num_blocks);
-      }
+      bool bad = a < 0 || b < a || (int64_t)b > m.num_tokens || (s == 0 && a != 0) ||
+                 (s == m.num_seqs - 1 && (int64_t)b != m.num_tokens);
       int lo = INT_MAX, hi = 0;
-      for (int t0 = a; t0 < b; t0 += 256) {
-        int32_t pos[8];
+      const int64_t need = n >= 1 ? ((int64_t)n + m.block_size - 1) / m.block_size : 0;
+      if (!bad && a < b) {
+        bad = n < 1 || need > m.max_blocks;
+        if (!bad) {
+          const int32_t* row = m.block_tables + (int64_t)s * m.max_blocks;
+          // eight loads in flight per lane, table entries and positions together
+          for (int64_t base = 0; base < need || base < b - a; base += 256) {
+            int32_t id[8], pos[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int t = t0 + lane + 32 * u;
-          pos[u] = t < b ? m.positions[t] : 0;
-        }
+            for (int u = 0; u < 8; ++u) {
+              const int64_t i = base + lane + 32 * u;
+              id[u] = i < need ? row[i] : 0;
+              pos[u] = i < b - a ? m.positions[a + i] : 0;
+            }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int t = t0 + lane + 32 * u;
-          if (t < b) {
-            bad |= (pos[u] < 0 || pos[u] >= n);
-            plan[L.tok_off + t] = s;
-            const int e = m.causal ? pos[u] + 1 : n;
-            lo = min(lo, m.window > 0 ? max(0, e - m.window) : 0);
-            hi = max(hi, e);
+            for (int u = 0; u < 8; ++u) {
+              const int64_t i = base + lane + 32 * u;
+              bad |= (id[u] < 0 || (int64_t)id[u] >= m.num_blocks);
+              if (i < b - a) {
+                bad |= (pos[u] < 0 || pos[u] >= n);
+                plan[L.tok_off + a + i] = s;
+                const int e = m.causal ? pos[u] + 1 : n;
+                lo = min(lo, m.window > 0 ? max(0, e - m.window) : 0);
+                hi = max(hi, e);
+              }
+            }
           }
         }
       }
@@ -135,7 +127,14 @@ __global__ void __launch_bounds__(1024)
         lo = min(lo, __shfl_xor_sync(kFull, lo, o));
         hi = max(hi, __shfl_xor_sync(kFull, hi, o));
       }
-      if (lane == 0) plan[L.cost_off + s] = max(0, hi - lo);
+      if (lane == 0) {
+        const int cost = max(0, hi - lo);
+        plan[L.cost_off + s] = cost;
+        if (cached) {
+          s_qlen[s] = b - a;
+          s_cost[s] = cost;
+        }
+      }
       if (__any_sync(kFull, bad) && lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
     }
   }
@@ -148,36 +147,36 @@ __global__ void __launch_bounds__(1024)
     }
     return;
   }
+  // per-sequence q_len and visible keys, from shared memory when cached
+  auto qlen_of = [&](int s) -> int {
+    return cached ? s_qlen[s] : m.query_start_loc[s + 1] - m.query_start_loc[s];
+  };
+  auto cost_of = [&](int s) -> int { return cached ? s_cost[s] : plan[L.cost_off + s]; };
   int2* mma_items = reinterpret_cast<int2*>(plan + L.mma_off);
   int4* tc_items = reinterpret_cast<int4*>(plan + L.tc_off);
   int4* tc_tmp = reinterpret_cast<int4*>(plan + L.tc_tmp_off);
   const int tok_per_item = 256 / m.group;  // used only when use_tc (group divides 128)
-  for (int i = tid; i < kCostBuckets; i += blockDim.x) {
-    s_hist[i] = 0;
-    s_hist_t[i] = 0;
-  }
-  __syncthreads();
-  // C1: 256-row items of prefill-class sequences, in sequence order, the last one (most keys
+  // B1: 256-row items of prefill-class sequences, in sequence order, the last one (most keys
   // under a causal mask) first; the histogram of the 16-row tiles' costs
   int carry_t = 0;
   for (int base = 0; base < m.num_seqs; base += blockDim.x) {
     const int s = base + tid;
     int cm = 0, ct = 0;
     if (s < m.num_seqs) {
-      const int64_t rows = (int64_t)(m.query_start_loc[s + 1] - m.query_start_loc[s]) * m.group;
+      const int64_t rows = (int64_t)qlen_of(s) * m.group;
       if (L.use_tc && rows > L.tc_min_rows)
         ct = (int)((rows + 255) / 256);
       else
         cm = (int)((rows + 15) / 16);
     }
-    if (cm > 0) atomicAdd(&s_hist[cost_bucket(plan[L.cost_off + s])], cm);
+    if (cm > 0) atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
     int tot_t;
     const int et = block_exclusive_scan(ct, s_warp, &tot_t);
     for (int i = 0; i < ct; ++i) tc_tmp[carry_t + et + i] = make_int4(s, ct - 1 - i, 0, 0);
     carry_t += tot_t;
   }
   __syncthreads();
-  // C2: each item's key range [lo, hi), the union of its tokens' visible ranges (a warp per
+  // B2: each item's key range [lo, hi), the union of its tokens' visible ranges (a warp per
   // item), and the histogram of the items' costs (carry_t is the same in every thread)
   if (carry_t > 0) {
     for (int k = warp; k < carry_t; k += nwarps) {
@@ -202,7 +201,7 @@ __global__ void __launch_bounds__(1024)
       }
     }
     __syncthreads();
-    // C3: the items ordered by cost, longest first (a counting sort over the cost buckets)
+    // B3: the items ordered by cost, longest first (a counting sort over the cost buckets)
     {
       int carry = 0;
       for (int b0 = 0; b0 < kCostBuckets; b0 += blockDim.x) {
@@ -231,10 +230,10 @@ __global__ void __launch_bounds__(1024)
   }
   __syncthreads();
   for (int s = tid; s < m.num_seqs; s += blockDim.x) {
-    const int64_t rows = (int64_t)(m.query_start_loc[s + 1] - m.query_start_loc[s]) * m.group;
+    const int64_t rows = (int64_t)qlen_of(s) * m.group;
     if (rows == 0 || (L.use_tc && rows > L.tc_min_rows)) continue;
     const int cm = (int)((rows + 15) / 16);
-    const int at = atomicAdd(&s_hist[cost_bucket(plan[L.cost_off + s])], cm);
+    const int at = atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
     for (int i = 0; i < cm; ++i) mma_items[at + i] = make_int2(s, i);
   }
   if (tid == 0) {
@@ -408,7 +407,11 @@ bool aligned(const void* p, size_t a) { return p == nullptr || (reinterpret_cast
 
 cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, const PlanLayout& L,
                                int* status, cudaStream_t stream) {
-  k_plan_varlen<<<1, 1024, 0, stream>>>(m, plan, L, status);
+  const size_t dyn = m.num_seqs <= kPlanCacheSeqs ? 2 * sizeof(int) * (size_t)m.num_seqs : 0;
+  cudaError_t e = cudaFuncSetAttribute(k_plan_varlen, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(2 * sizeof(int) * kPlanCacheSeqs));
+  if (e != cudaSuccess) return e;
+  k_plan_varlen<<<1, 1024, dyn, stream>>>(m, plan, L, status);
   return cudaGetLastError();
 }
 

@@ -194,6 +194,18 @@ NAMES = {
 }
 
 
+def prefill_chunks(seed: int = 0, device="cpu") -> Workload:
+    """The prefill chunks of workload 3 on their own: 8 chunks of 512 tokens after the same
+    prior contexts U{0..2048}, with a pool holding only their blocks (a small case of the
+    tcgen05 prefill kernel for profiling)."""
+    g = torch.Generator(device="cpu").manual_seed(1000 + seed * 7 + 3)
+    _uniform(g, 1024, 8192, 248)  # the decode contexts of workload 3, drawn first there
+    prior = _uniform(g, 0, 2048, 8)
+    return build("prefill-chunks", seq_lens=[c + 512 for c in prior], q_lens=[512] * 8,
+                 num_heads=32, num_kv_heads=8, head_dim=128, sliding_window=4096, seed=seed,
+                 device=device)
+
+
 def named(cfg: int, seed: int = 0, device="cpu", small: bool = False) -> Workload:
     """The five benchmark workloads.
 
