@@ -46,6 +46,7 @@ constexpr int kBN = 128;          // keys per tile (8 blocks of 16)
 constexpr int kD = 128;           // head size on this path
 constexpr int kHalf = 16384;      // one 64-dim half of a 128-row bf16 tile
 constexpr int kTile = 2 * kHalf;  // 128 x 128 bf16
+constexpr int kSBufs = 3;    // S / P buffers in tensor memory (columns 0, 128 and 384)
 constexpr int kStagesK = 2;  // K ring (a K tile is released as soon as its S MMAs finish)
 constexpr int kStagesV = 3;  // V ring (held until P V, so it needs one more stage in flight)
 constexpr int kOffQ = 0;                          // two Q buffers (consecutive items)
@@ -62,7 +63,6 @@ constexpr int kSoftWarps = 8;                         // two column halves x fou
 constexpr int kThreads = 64 + kSoftWarps * 32 + 64;  // + the V producer and PV issuer warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;    // O: columns 256..383
-constexpr int kSBufs = 3;          // S / P buffers at columns 0, 128 and 384
 __device__ __forceinline__ uint32_t col_s(uint32_t b) { return b == 2 ? 384u : b * 128u; }
 // Inside an S buffer, P_j of key half h (keys 64h .. 64h+63) is stored by the thread that read
 // those scores: hi at columns 64h .. 64h+31, lo at 64h+32 .. 64h+63 (two bf16 per column).
@@ -70,12 +70,22 @@ __device__ __forceinline__ uint32_t col_p(int kstep, int lo) {
   return (uint32_t)((kstep >> 2) * 64 + lo * 32 + (kstep & 3) * 8);
 }
 
-// barrier indices (the per-buffer ones are consecutive)
-enum {
-  B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 6, B_VFULL = 8, B_VEMPTY = 11, B_SFULL = 14,
-  B_PFULL = 17, B_PVDONE = 20, B_OFREE = 23, B_FIN = 24
+// barrier indices (the per-stage / per-buffer ones are consecutive)
+enum : int {
+  B_QFULL = 0,
+  B_QEMPTY = B_QFULL + 2,
+  B_KFULL = B_QEMPTY + 2,
+  B_KEMPTY = B_KFULL + kStagesK,
+  B_VFULL = B_KEMPTY + kStagesK,
+  B_VEMPTY = B_VFULL + kStagesV,
+  B_SFULL = B_VEMPTY + kStagesV,
+  B_PFULL = B_SFULL + kSBufs,
+  B_PVDONE = B_PFULL + kSBufs,
+  B_OFREE = B_PVDONE + kSBufs,
+  B_FIN = B_OFREE + 1,
+  kNumBars = B_FIN + 1
 };
-constexpr int kNumBars = 25;
+static_assert(kNumBars <= kNumBarsMax, "barrier area");
 
 // ---- tcgen05 / TMEM wrappers -----------------------------------------------------------------
 
@@ -672,10 +682,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     flags[1] = 0;
     // k_empty / v_empty: one arrival from each CTA of the pair; p_full / o_free: one per
-    // softmax warp; fin: one per MMA-issuing thread
-    const uint32_t counts[kNumBars] = {1, 1, 1, 1, 1, 1, 2, 2, 1, 1, 1, 2, 2, 2,
-                                       1, 1, 1, 8, 8, 8, 1, 1, 1, 8, 2};
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, counts[i]);
+    // softmax warp; fin: one per MMA-issuing warp; the rest: one
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t n = 1;
+      if ((i >= B_KEMPTY && i < B_KEMPTY + kStagesK) || (i >= B_VEMPTY && i < B_VEMPTY + kStagesV))
+        n = 2;
+      if ((i >= B_PFULL && i < B_PFULL + kSBufs) || i == B_OFREE) n = kSoftWarps;
+      if (i == B_FIN) n = 2;
+      mbar_init(bar + i, n);
+    }
     prefetch_tmap(&tq);
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
