@@ -57,6 +57,9 @@ def lib():
             L.oracle_varlen_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32,
                                                   i32, i32, i32, i64, i32, i32, i32, i32, f32, i32,
                                                   i32]
+            L.oracle_varlen_attention_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64,
+                                                     i32, i32, i32, i32, i64, i32, i32, i32, i32,
+                                                     f32, i32, i32, vp]
             L.oracle_splitkv_partials.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                   i32, i64, i32, i32, i32, i32, i32, f32, i32]
             L.oracle_splitkv_reduce.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
@@ -66,8 +69,9 @@ def lib():
             L.oracle_f32_to_bf16.argtypes = [f32]
             L.oracle_f32_to_bf16.restype = ctypes.c_uint16
             for name in ("oracle_slot_mapping", "oracle_reshape_and_cache", "oracle_gather_kv",
-                         "oracle_varlen_attention", "oracle_splitkv_partials",
-                         "oracle_splitkv_reduce", "oracle_merge_attn_states"):
+                         "oracle_varlen_attention", "oracle_varlen_attention_ex",
+                         "oracle_splitkv_partials", "oracle_splitkv_reduce",
+                         "oracle_merge_attn_states"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -135,8 +139,9 @@ def gather_kv(k_blocks, v_blocks, cu_seq_lens, block_tables, seq_starts=None):
 
 def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions, block_tables,
                      scale, causal=True, sliding_window=0, out_dtype=torch.float32,
-                     want_lse=False, num_kv_heads=None, out=None):
-    """Two-pass attention of every (token, head).  Returns (status, out [T,H,D], lse [H,T])."""
+                     want_lse=False, num_kv_heads=None, out=None, sinks=None):
+    """Two-pass attention of every (token, head).  Returns (status, out [T,H,D], lse [H,T]).
+    sinks: optional [H] fp32 sink logits (a virtual zero-valued position per head)."""
     q, kb, vb = _cpu(q), _cpu(k_blocks), _cpu(v_blocks)
     qsl, sl, pos, bt = _cpu(query_start_loc), _cpu(seq_lens), _cpu(positions), _cpu(block_tables)
     T, H, D = q.shape
@@ -146,10 +151,12 @@ def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions
     if out is None:
         out = torch.zeros((T, H, D), dtype=out_dtype)
     lse = torch.full((H, T), float("nan"), dtype=torch.float32) if want_lse else None
-    st = lib().oracle_varlen_attention(_p(q), _p(kb), _p(vb), _p(out), _p(lse), _p(qsl), _p(sl),
-                                       _p(pos), _p(bt), qsl.numel() - 1, T, H, Hkv, D, bs, NB,
-                                       bt.shape[1], _DT[q.dtype], _DT[kb.dtype], _DT[out.dtype],
-                                       float(scale), int(bool(causal)), int(sliding_window))
+    sk = None if sinks is None else _cpu(sinks).to(torch.float32).contiguous()
+    st = lib().oracle_varlen_attention_ex(_p(q), _p(kb), _p(vb), _p(out), _p(lse), _p(qsl),
+                                          _p(sl), _p(pos), _p(bt), qsl.numel() - 1, T, H, Hkv, D,
+                                          bs, NB, bt.shape[1], _DT[q.dtype], _DT[kb.dtype],
+                                          _DT[out.dtype], float(scale), int(bool(causal)),
+                                          int(sliding_window), _p(sk))
     return st, out, lse
 
 

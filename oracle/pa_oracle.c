@@ -221,12 +221,17 @@ static float attend_two_pass(const void* q, int64_t q_off, int q_dtype, const vo
                              int64_t start, int64_t end, int32_t block_size,
                              int32_t num_kv_heads, int32_t head_dim, int32_t kv_head,
                              float scale, float* logits, float* acc, void* out,
-                             int64_t out_off, int out_dtype, float* m_out, float* l_out) {
+                             int64_t out_off, int out_dtype, float* m_out, float* l_out,
+                             float sink) {
   const int64_t n = end > start ? end - start : 0;
+  /* An attention sink ([MPA] ForwardWithSinks) is one more, virtual, position whose score is
+   * the sink logit and whose value is zero: it enters the max and the exp-sum, never the
+   * weighted sum.  sink = -inf means none (and then changes nothing). */
+  const int has_sink = sink > -INFINITY;
 
   /* PASS 1: raw dot (ascending d), then the scale, and the row max
    * ([MPA] "Compute Q . K" then score *= scale; [MLA] PASS 1). */
-  float m = -INFINITY;
+  float m = has_sink ? sink : -INFINITY;
   for (int64_t i = 0; i < n; ++i) {
     int64_t j = start + i;
     int64_t k_off = pool_row_offset(table_row, j, block_size, num_kv_heads, head_dim, kv_head);
@@ -238,8 +243,10 @@ static float attend_two_pass(const void* q, int64_t q_off, int q_dtype, const vo
     if (s > m) m = s;
   }
 
-  /* PASS 2: the exp-sum, then the weighted sum; no running rescale ([MLA] PASS 2). */
+  /* PASS 2: the exp-sum (the sink's term first, as [MPA] seeds its denominator with it), then
+   * the weighted sum; no running rescale ([MLA] PASS 2). */
   float l = 0.0f;
+  if (has_sink && !MUTANT(60)) l = MUTANT(61) ? 1.0f : expf(sink - m); /* s60 / s61 */
   for (int64_t i = 0; i < n; ++i) {
     float p = expf(MUTANT(31) ? m - logits[i] : logits[i] - m);
     logits[i] = p;
@@ -310,14 +317,15 @@ static int validate_varlen(const void* q, const void* k_blocks, const void* v_bl
  * max(0, end - w) : 0  ([MPA] contextEndExclusive / contextStart), then softmax
  * attention over positions [start, end).  out is [T, H, D] in out_dtype; lse
  * (may be NULL) is [H, T] in natural log ([MLA] LSE layout). */
-int oracle_varlen_attention(const void* q, const void* k_blocks, const void* v_blocks,
-                            void* out, float* lse, const int32_t* query_start_loc,
-                            const int32_t* seq_lens, const int32_t* positions,
-                            const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
-                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                            int32_t block_size, int64_t num_blocks, int32_t max_blocks,
-                            int32_t q_dtype, int32_t kv_dtype, int32_t out_dtype, float scale,
-                            int32_t causal, int32_t sliding_window) {
+/* sinks: [num_heads] sink logits on the score scale ([MPA] ForwardWithSinks), or NULL. */
+int oracle_varlen_attention_ex(const void* q, const void* k_blocks, const void* v_blocks,
+                               void* out, float* lse, const int32_t* query_start_loc,
+                               const int32_t* seq_lens, const int32_t* positions,
+                               const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t num_blocks, int32_t max_blocks,
+                               int32_t q_dtype, int32_t kv_dtype, int32_t out_dtype, float scale,
+                               int32_t causal, int32_t sliding_window, const float* sinks) {
   int st = validate_varlen(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                            block_tables, num_seqs, num_tokens, num_heads, num_kv_heads,
                            head_dim, block_size, num_blocks, max_blocks, q_dtype, kv_dtype);
@@ -353,7 +361,8 @@ int oracle_varlen_attention(const void* q, const void* k_blocks, const void* v_b
       float l_lse = attend_two_pass(q, (t * num_heads + h) * (int64_t)head_dim, q_dtype, k_blocks,
                                     v_blocks, kv_dtype, row, start, end, block_size, num_kv_heads,
                                     head_dim, g, scale, logits, acc, out,
-                                    (t * num_heads + h) * (int64_t)head_dim, out_dtype, NULL, NULL);
+                                    (t * num_heads + h) * (int64_t)head_dim, out_dtype, NULL, NULL,
+                                    sinks ? sinks[h] : -INFINITY);
       if (lse) lse[(int64_t)h * num_tokens + t] = l_lse;
     }
     free(logits);
@@ -361,6 +370,21 @@ int oracle_varlen_attention(const void* q, const void* k_blocks, const void* v_b
   }
   free(tok_seq);
   return ORC_OK;
+}
+
+int oracle_varlen_attention(const void* q, const void* k_blocks, const void* v_blocks,
+                            void* out, float* lse, const int32_t* query_start_loc,
+                            const int32_t* seq_lens, const int32_t* positions,
+                            const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int64_t num_blocks, int32_t max_blocks,
+                            int32_t q_dtype, int32_t kv_dtype, int32_t out_dtype, float scale,
+                            int32_t causal, int32_t sliding_window) {
+  return oracle_varlen_attention_ex(q, k_blocks, v_blocks, out, lse, query_start_loc, seq_lens,
+                                    positions, block_tables, num_seqs, num_tokens, num_heads,
+                                    num_kv_heads, head_dim, block_size, num_blocks, max_blocks,
+                                    q_dtype, kv_dtype, out_dtype, scale, causal, sliding_window,
+                                    NULL);
 }
 
 /* ---- split-KV decode, phase 1 ([V2] partition loop) ------------------------
@@ -421,7 +445,7 @@ int oracle_splitkv_partials(const void* q, const void* k_blocks, const void* v_b
       attend_two_pass(q, ((int64_t)s * num_heads + h) * head_dim, q_dtype, k_blocks, v_blocks,
                       kv_dtype, block_tables + (int64_t)s * max_blocks, lo, hi, block_size,
                       num_kv_heads, head_dim, h / group, scale, logits, acc, tmp_out,
-                      idx * head_dim, ORC_F32, &m, &l);
+                      idx * head_dim, ORC_F32, &m, &l, -INFINITY);
       max_logits[idx] = m;
       exp_sums[idx] = l;
     }

@@ -8,7 +8,8 @@ value, identity or special case that does not come from the oracle itself:
   values, from which the paged pool is built (tinyllm section 4,
   matches_naive_over_the_gathered_cache: GQA 6:2, D = 32, lengths 1 / 37 / 70,
   windows 0 and 20);
-* closed forms (one visible key, a zero query, constant values);
+* closed forms (one visible key, a zero query, constant values), with and without
+  attention sinks (TensorSharp ForwardWithSinks);
 * invariances (permuted physical block ids, a sequence alone vs in a batch,
   shared prefix blocks vs private copies, thread count);
 * the log-sum-exp identities behind split-KV and merge_attn_states, and the
@@ -211,6 +212,89 @@ def pin_closed_forms():
     st, out, _ = oracle.varlen_attention(w.q, w.k_blocks, vc, scale=w.scale, **meta)
     assert st == oracle.OK
     np.testing.assert_allclose(out.numpy(), 0.625, rtol=1e-6, atol=0)
+
+
+# --------------------------------------------------------------------------------------------
+# attention sinks (TensorSharp ForwardWithSinks): a virtual position per head whose score is
+# the sink logit and whose value is zero
+
+
+def _sink_case(seed=41):
+    w = workloads.build("sinks", seq_lens=[3, 40, 70], q_lens=[1, 3, 2], num_heads=4,
+                        num_kv_heads=2, head_dim=16, dtype=torch.float32, seed=seed)
+    meta = dict(query_start_loc=w.query_start_loc, seq_lens=w.seq_lens, positions=w.positions,
+                block_tables=w.block_tables)
+    return w, meta, torch.tensor([-1.5, 0.7, 2.0, -0.3], dtype=torch.float32)
+
+
+def pin_sinks_closed_forms():
+    w, meta, sinks = _sink_case()
+    G = w.group
+    # (a) -inf sinks are no sinks: the same bits for o and lse
+    st, o0, l0 = oracle.varlen_attention(w.q, w.k_blocks, w.v_blocks, scale=w.scale,
+                                         want_lse=True, **meta)
+    st1, o1, l1 = oracle.varlen_attention(w.q, w.k_blocks, w.v_blocks, scale=w.scale,
+                                          want_lse=True, sinks=torch.full((4,), -math.inf),
+                                          **meta)
+    assert st == oracle.OK and st1 == oracle.OK
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    # (b) a zero query: every visible score is 0, so each of the n visible values gets weight
+    # 1 / (n + e^sink) and lse = log(n + e^sink)
+    qz = torch.zeros_like(w.q)
+    st, out, lse = oracle.varlen_attention(qz, w.k_blocks, w.v_blocks, scale=w.scale,
+                                           want_lse=True, sinks=sinks, **meta)
+    assert st == oracle.OK
+    for t in range(w.num_tokens):
+        s = int(np.searchsorted(w.query_start_loc.numpy(), t, side="right") - 1)
+        p = int(w.positions[t])
+        rows = [w.v_blocks[int(w.block_tables[s, j // 16]), j % 16].double() for j in range(p + 1)]
+        total = torch.stack(rows).sum(0)  # [Hkv, D]
+        n = p + 1
+        for h in range(w.num_heads):
+            den = n + math.exp(float(sinks[h]))
+            np.testing.assert_allclose(out[t, h].numpy(), (total[h // G] / den).numpy(),
+                                       rtol=1e-5, atol=1e-6)
+            assert abs(float(lse[h, t]) - math.log(den)) < 1e-5, (t, h)
+
+
+def pin_sinks_brute_force(seed=43):
+    """Float64 softmax over [visible scores..., sink] with values [visible v..., 0]."""
+    H, Hkv, D, b = 6, 2, 32, 16
+    lens, qlens = [1, 37, 70], [1, 5, 70]
+    gen = torch.Generator().manual_seed(seed)
+    dk = [torch.randn((n, Hkv, D), generator=gen) for n in lens]
+    dv = [torch.randn((n, Hkv, D), generator=gen) for n in lens]
+    kb, vb, table = _paged_from_dense(dk, dv, b, seed + 1)
+    T = sum(qlens)
+    q = torch.randn((T, H, D), generator=gen)
+    sinks = torch.randn((H,), generator=gen) * 2.0
+    qsl = np.cumsum([0] + qlens).tolist()
+    pos = [p for n, ql in zip(lens, qlens) for p in range(n - ql, n)]
+    scale = 1.0 / math.sqrt(D)
+    for window in (0, 20):
+        st, out, lse = oracle.varlen_attention(q, kb, vb, _t(qsl), _t(lens), _t(pos), table,
+                                               scale=scale, sliding_window=window,
+                                               want_lse=True, sinks=sinks)
+        assert st == oracle.OK
+        for s, n in enumerate(lens):
+            a, z = qsl[s], qsl[s + 1]
+            kk = np.repeat(dk[s].numpy().astype(np.float64), H // Hkv, axis=1)
+            vv = np.repeat(dv[s].numpy().astype(np.float64), H // Hkv, axis=1)
+            j = np.arange(n)[None, :]
+            end = np.asarray(pos[a:z])[:, None] + 1
+            vis = j < end
+            if window > 0:
+                vis &= j >= end - window
+            for h in range(H):
+                sc = (q[a:z, h, :].numpy().astype(np.float64) @ kk[:, h, :].T) * scale
+                sc = np.where(vis, sc, -np.inf)
+                sc = np.concatenate([sc, np.full((z - a, 1), float(sinks[h]))], axis=1)
+                mx = sc.max(axis=1, keepdims=True)
+                e = np.exp(sc - mx)
+                want = (e[:, :n] @ vv[:, h, :]) / e.sum(axis=1, keepdims=True)
+                np.testing.assert_allclose(out[a:z, h].numpy(), want, rtol=1e-5, atol=2e-5)
+                want_lse = (mx[:, 0] + np.log(e.sum(axis=1)))
+                np.testing.assert_allclose(lse[h, a:z].numpy(), want_lse, rtol=1e-5, atol=2e-5)
 
 
 # --------------------------------------------------------------------------------------------
@@ -544,6 +628,8 @@ def pin_bf16_codec():
 
 
 ALL_PINS = {
+    "sinks_closed_forms": pin_sinks_closed_forms,
+    "sinks_brute_force": pin_sinks_brute_force,
     "hand_example": pin_hand_example,
     "hand_example_via_cache": pin_hand_example_via_cache,
     "brute_force": pin_brute_force_all,

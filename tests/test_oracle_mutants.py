@@ -5,7 +5,8 @@ oracle (s03 logical block index as block id, s04 KV-head offset dropped, s05
 round-robin GQA, s06 a window of w + 1, s07 query at n instead of n - 1, s08 V
 read from the K pool, s13 empty context accepted, s14 max_blocks trusted, s15
 block ids trusted) and further plausible slips in the scatter, gather, score,
-split-KV reduction and merge arithmetic.
+split-KV reduction and merge arithmetic, and in the attention-sink term (s60 the sink
+left out of the exp-sum, s61 its term taken as 1 instead of e^(sink - m)).
 """
 import pytest
 
@@ -34,6 +35,8 @@ KILLERS = {
     50: ["merge_edge_cases"],
     51: ["merge_edge_cases"],
     52: ["merge_identity"],
+    60: ["sinks_closed_forms", "sinks_brute_force"],
+    61: ["sinks_closed_forms", "sinks_brute_force"],
 }
 
 
