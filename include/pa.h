@@ -129,6 +129,33 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
                             cudaStream_t stream);
 
 /*
+ * pa_varlen_forward_ex -- pa_varlen_forward with two optional extras (either may be NULL;
+ * with both NULL the call is pa_varlen_forward):
+ *   sinks  [num_heads] fp32, device.  Per-head attention sink logits on the score scale
+ *          (TensorSharp ForwardWithSinks): a virtual position with score sinks[h] and value
+ *          zero, so with the visible scores s_j
+ *              out[t, h] = sum_j e^(s_j - m) V_j / (e^(sinks[h] - m) + sum_j e^(s_j - m)),
+ *          m = max(sinks[h], max_j s_j).  -inf means no sink for that head.  Finite values
+ *          and -inf are defined; NaN and +inf are not.
+ *   lse    [num_heads, num_tokens] fp32, device, written (the vllm.cpp MLA-prefill layout):
+ *              lse[h, t] = log(e^sinks[h] + sum_j e^(s_j))   (natural log, sink term when given)
+ *          and -inf when the sum is empty (no visible position and no sink).  It is what
+ *          pa_merge_attn_states takes to combine two partial attentions of the same queries.
+ * Both are read or written only for tokens of sequences with query tokens, and lse is left
+ * untouched on a validation failure, like out.
+ */
+pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* v_blocks,
+                               void* out, const int32_t* query_start_loc,
+                               const int32_t* seq_lens, const int32_t* positions,
+                               const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t num_blocks,
+                               int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
+                               float scale, int32_t causal, int32_t sliding_window,
+                               const float* sinks, float* lse, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * pa_varlen_forward_noalloc -- pa_varlen_forward for callers that cannot allocate device
  * memory.  The pages have no counterpart: it exists for the library's users, not for the
  * method.  Some callers cannot hand this library a workspace: a host framework that gives an

@@ -39,6 +39,9 @@ _SIGS = {
     "pa_varlen_forward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
                            _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32, _i32, _vp,
                            _sz, _vp], ctypes.c_int),
+    "pa_varlen_forward_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
+                              _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32,
+                              _i32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     "pa_varlen_forward_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
                                    _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32,
                                    _i32, _vp], ctypes.c_int),
@@ -157,8 +160,11 @@ def workspace_for(q, k_blocks, query_start_loc, block_tables):
 
 def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                       block_tables, scale, causal=True, sliding_window=0, workspace=None,
-                      stream=None):
-    _dev(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions, block_tables, workspace)
+                      stream=None, sinks=None, lse=None):
+    """pa_varlen_forward, or pa_varlen_forward_ex when sinks ([H] fp32 sink logits) or lse
+    (a [H, T] fp32 output) is given."""
+    _dev(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions, block_tables, workspace,
+         sinks, lse)
     _i32t(query_start_loc, seq_lens, positions, block_tables)
     if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("q and out must be [T, H, D] of one dtype")
@@ -170,13 +176,30 @@ def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, pos
         raise ValueError("head size differs between q and the pool")
     if workspace is None:
         workspace = workspace_for(q, k_blocks, query_start_loc, block_tables)
-    _check(_lib.pa_varlen_forward(_p(q), _p(k_blocks), _p(v_blocks), _p(out), _p(query_start_loc),
-                                  _p(seq_lens), _p(positions), _p(block_tables),
-                                  query_start_loc.numel() - 1, T, H, Hkv, D, bs, NB,
-                                  block_tables.shape[1], _DT[q.dtype], _DT[k_blocks.dtype],
-                                  float(scale), int(bool(causal)), int(sliding_window),
-                                  _p(workspace), workspace.numel(), _stream(stream)),
-           "pa_varlen_forward")
+    if sinks is None and lse is None:
+        _check(_lib.pa_varlen_forward(_p(q), _p(k_blocks), _p(v_blocks), _p(out),
+                                      _p(query_start_loc), _p(seq_lens), _p(positions),
+                                      _p(block_tables), query_start_loc.numel() - 1, T, H, Hkv, D,
+                                      bs, NB, block_tables.shape[1], _DT[q.dtype],
+                                      _DT[k_blocks.dtype], float(scale), int(bool(causal)),
+                                      int(sliding_window), _p(workspace), workspace.numel(),
+                                      _stream(stream)),
+               "pa_varlen_forward")
+        return out
+    if sinks is not None and (sinks.dtype != torch.float32 or sinks.shape != (H,)
+                              or not sinks.is_contiguous()):
+        raise ValueError("sinks must be a contiguous fp32 [num_heads] tensor")
+    if lse is not None and (lse.dtype != torch.float32 or lse.shape != (H, T)
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [num_heads, num_tokens] tensor")
+    _check(_lib.pa_varlen_forward_ex(_p(q), _p(k_blocks), _p(v_blocks), _p(out),
+                                     _p(query_start_loc), _p(seq_lens), _p(positions),
+                                     _p(block_tables), query_start_loc.numel() - 1, T, H, Hkv, D,
+                                     bs, NB, block_tables.shape[1], _DT[q.dtype],
+                                     _DT[k_blocks.dtype], float(scale), int(bool(causal)),
+                                     int(sliding_window), _p(sinks), _p(lse), _p(workspace),
+                                     workspace.numel(), _stream(stream)),
+           "pa_varlen_forward_ex")
     return out
 
 

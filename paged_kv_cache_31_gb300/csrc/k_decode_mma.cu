@@ -396,9 +396,24 @@ __global__ void __launch_bounds__(NW * 32, 2)
           wsc[w] = M == -INFINITY ? 0.f : exp2f(mrg_m[w * 16 + row] - M);
           L += wsc[w] * mrg_l[w * 16 + row];
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
         const int t = qs + R / G;
         const int h = kvh * G + R % G;
+        if constexpr (!SPLIT) {
+          // an attention sink (TensorSharp ForwardWithSinks) is one more state to merge: max
+          // = the sink logit, exp-sum = 1, weighted sum = 0
+          const float sk = p.m.sinks ? p.m.sinks[h] * kLog2e : -INFINITY;
+          if (sk > -INFINITY) {
+            const float M2 = fmaxf(M, sk);
+            const float a = M == -INFINITY ? 0.f : exp2f(M - M2);
+#pragma unroll
+            for (int w = 0; w < NW; ++w) wsc[w] *= a;
+            L = L * a + exp2f(sk - M2);
+            M = M2;
+          }
+          if (p.m.lse && seg == 0)
+            p.m.lse[(int64_t)h * p.m.num_tokens + t] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
         float vals[kSeg];
 #pragma unroll
         for (int d = 0; d < kSeg; ++d) {

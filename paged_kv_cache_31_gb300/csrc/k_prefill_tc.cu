@@ -638,7 +638,21 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     const uint32_t last = kv + I.ntiles - 1;
     if (!__all_sync(kFull, wait_bar(c, B_PVDONE + buf_of(last), use_par(last)))) return;
     tc_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    // an attention sink (TensorSharp ForwardWithSinks) is one more state to merge: max = the
+    // sink logit, exp-sum = 1, weighted sum = 0
+    float o_scale = 1.f;
+    {
+      const float sk = m.sinks ? m.sinks[h] * kLog2e : -INFINITY;
+      if (sk > -INFINITY) {
+        const float m2 = fmaxf(m_ref, sk);
+        o_scale = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - m2);
+        l = l * o_scale + fast_exp2(sk - m2);
+        m_ref = m2;
+      }
+    }
+    if (m.lse && hf == 0 && valid)
+      m.lse[(int64_t)h * m.num_tokens + t] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    const float inv = l > 0.f ? o_scale / l : 0.f;
     __nv_bfloat16* dst =
         reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * m.num_heads + h) * kD + col0;
     uint32_t oo[2][32];

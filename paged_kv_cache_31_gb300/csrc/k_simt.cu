@@ -87,7 +87,20 @@ __global__ void __launch_bounds__(128) k_simt(const SimtParams p) {
       if (d < D) acc[i] += e * to_f32(vb[base + d]);
     }
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
+  float inv = den > 0.f ? 1.f / den : 0.f;
+  if (!p.split) {
+    // an attention sink (TensorSharp ForwardWithSinks): one more state with max = the sink
+    // logit, exp-sum 1 and weighted sum 0
+    const float sk = m.sinks ? m.sinks[h] : -INFINITY;
+    if (sk > -INFINITY) {
+      const float m2 = fmaxf(mx, sk);
+      const float a = mx == -INFINITY ? 0.f : expf(mx - m2);
+      den = den * a + expf(sk - m2);
+      mx = m2;
+      inv = a / den;
+    }
+    if (m.lse && lane == 0) m.lse[(int64_t)h * m.num_tokens + t] = den > 0.f ? mx + logf(den) : -INFINITY;
+  }
   if (p.split) {
     const int64_t idx = ((int64_t)s * H + h) * p.max_parts + part;
 #pragma unroll

@@ -208,6 +208,23 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
                             pa_dtype kv_dtype, float scale, int32_t causal,
                             int32_t sliding_window, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
+  return pa_varlen_forward_ex(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
+                              block_tables, num_seqs, num_tokens, num_heads, num_kv_heads,
+                              head_dim, block_size, num_blocks, max_blocks_per_seq, q_dtype,
+                              kv_dtype, scale, causal, sliding_window, nullptr, nullptr,
+                              workspace, workspace_bytes, stream);
+}
+
+pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* v_blocks,
+                               void* out, const int32_t* query_start_loc,
+                               const int32_t* seq_lens, const int32_t* positions,
+                               const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t num_blocks,
+                               int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
+                               float scale, int32_t causal, int32_t sliding_window,
+                               const float* sinks, float* lse, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0)
     return PA_ESHAPE;
@@ -226,7 +243,7 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
   const DeviceState* d = device_state();
   if (!d) return PA_ECUDA;
 
-  VarlenMeta m;
+  VarlenMeta m{};
   m.query_start_loc = query_start_loc;
   m.seq_lens = seq_lens;
   m.positions = positions;
@@ -242,6 +259,8 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
   m.max_blocks = max_blocks_per_seq;
   m.causal = causal ? 1 : 0;
   m.window = sliding_window > 0 ? sliding_window : 0;
+  m.sinks = sinks;
+  m.lse = lse;
   int32_t* plan = static_cast<int32_t*>(workspace);
   PlanLayout L = plan_layout(num_seqs, num_tokens, m.group);
   const bool fast = mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
@@ -329,7 +348,7 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
                                          block_size, num_blocks, partition_size,
                                          max_num_partitions, 1, d->status, stream);
   if (e != cudaSuccess) return PA_ECUDA;
-  VarlenMeta m;
+  VarlenMeta m{};
   std::memset(&m, 0, sizeof m);
   m.seq_lens = seq_lens;
   m.block_tables = block_tables;

@@ -227,6 +227,8 @@ struct VarlenMeta {
   int32_t max_blocks;
   int32_t causal;
   int32_t window;
+  const float* sinks;  // [num_heads] sink logits on the score scale, or null (varlen only)
+  float* lse;          // [num_heads, num_tokens] natural-log lse out, or null (varlen only)
 };
 
 struct Mma16Params {
