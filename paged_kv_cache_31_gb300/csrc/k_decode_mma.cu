@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
   // failed validation or an earlier sticky error: the whole CTA writes nothing
   if (threadIdx.x == 0) *fail = status_set(p.status) ? 1 : 0;
   __syncthreads();
+  if constexpr (!SPLIT) pdl_launch_dependents();  // the prefill kernel's prologue may start
   if (*reinterpret_cast<volatile int*>(fail)) return;
 
   const VarlenMeta& m = p.m;
