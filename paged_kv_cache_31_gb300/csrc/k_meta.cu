@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(1024)
   __shared__ int s_hist_t[kCostBuckets];  // 256-row items per cost bucket
   extern __shared__ int s_seq[];          // [2][num_seqs]: q_len, visible keys (when cached)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  pdl_wait();               // launched early: the batch's metadata may still be in flight
   pdl_launch_dependents();  // the attention kernels' prologues may overlap this kernel
   const bool cached = m.num_seqs <= kPlanCacheSeqs;
   int* s_qlen = s_seq;
@@ -278,6 +279,8 @@ __global__ void k_slot_mapping(const int32_t* qsl, const int32_t* positions,
                                const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
                                int32_t max_blocks, int32_t block_size, int64_t num_blocks,
                                int32_t* slots, int* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (status_set(status)) return;
   const int s = blockIdx.x;
   const int a = qsl[s], b = qsl[s + 1];
@@ -300,6 +303,8 @@ __global__ void k_slot_mapping(const int32_t* qsl, const int32_t* positions,
 
 __global__ void k_validate_slots(const int32_t* slots, int64_t num_tokens, int64_t num_slots,
                                  int* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   bool bad = false;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < num_tokens;
        t += (int64_t)gridDim.x * blockDim.x) {
@@ -316,6 +321,8 @@ __global__ void k_reshape_and_cache(const VEC* __restrict__ k, const VEC* __rest
                                     VEC* __restrict__ k_blocks, VEC* __restrict__ v_blocks,
                                     const int32_t* __restrict__ slots, int64_t num_tokens,
                                     int64_t row_vecs, const int* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (status_set(status)) return;
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -327,6 +334,41 @@ __global__ void k_reshape_and_cache(const VEC* __restrict__ k, const VEC* __rest
     const VEC b = v[src + i];
     k_blocks[dst + i] = a;
     v_blocks[dst + i] = b;
+  }
+}
+
+// Small batches (the decode step): the slot check and the scatter in one CTA, every slot
+// checked before the first row is written.  One warp per token, as above.
+constexpr int kSmallScatter = 128;
+template <typename VEC>
+__global__ void __launch_bounds__(1024)
+    k_scatter_small(const VEC* __restrict__ k, const VEC* __restrict__ v,
+                    VEC* __restrict__ k_blocks, VEC* __restrict__ v_blocks,
+                    const int32_t* __restrict__ slots, int num_tokens, int64_t num_slots,
+                    int64_t row_vecs, int* status) {
+  __shared__ int32_t s_slot[kSmallScatter];
+  pdl_wait();
+  pdl_launch_dependents();
+  if (status_set(status)) return;  // uniform across the CTA
+  bool bad = false;
+  for (int t = threadIdx.x; t < num_tokens; t += blockDim.x) {
+    const int32_t sl = slots[t];
+    s_slot[t] = sl;
+    bad |= (sl < 0 || (int64_t)sl >= num_slots);
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) record_error(status, PA_EINVAL);
+    return;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int t = warp; t < num_tokens; t += nwarps) {
+    const int64_t dst = (int64_t)s_slot[t] * row_vecs, src = (int64_t)t * row_vecs;
+    for (int64_t i = lane; i < row_vecs; i += 32) {
+      const VEC a = k[src + i];
+      const VEC b = v[src + i];
+      k_blocks[dst + i] = a;
+      v_blocks[dst + i] = b;
+    }
   }
 }
 
@@ -381,13 +423,22 @@ __global__ void k_gather_kv(const VEC* __restrict__ k_blocks, const VEC* __restr
 
 template <typename VEC>
 cudaError_t scatter_as(const void* k, const void* v, void* kb, void* vb, const int32_t* slots,
-                       int64_t T, int64_t row_bytes, const int* status, cudaStream_t stream) {
+                       int64_t T, int64_t row_bytes, int64_t num_slots, int* status,
+                       cudaStream_t stream) {
+  const int64_t row_vecs = row_bytes / (int64_t)sizeof(VEC);
+  if (T <= kSmallScatter)
+    return launch_pdl(k_scatter_small<VEC>, dim3(1), dim3(1024), 0, stream, (const VEC*)k,
+                      (const VEC*)v, (VEC*)kb, (VEC*)vb, slots, (int)T, num_slots, row_vecs,
+                      status);
+  const int64_t vgrid = std::min<int64_t>((T + 255) / 256, 1024);
+  cudaError_t e = launch_pdl(k_validate_slots, dim3((unsigned)vgrid), dim3(256), 0, stream, slots,
+                             T, num_slots, status);
+  if (e != cudaSuccess) return e;
   const int warps = 8;
   const int64_t grid = (T + warps - 1) / warps;
-  k_reshape_and_cache<VEC><<<(unsigned)grid, warps * 32, 0, stream>>>(
-      (const VEC*)k, (const VEC*)v, (VEC*)kb, (VEC*)vb, slots, T,
-      row_bytes / (int64_t)sizeof(VEC), status);
-  return cudaGetLastError();
+  return launch_pdl(k_reshape_and_cache<VEC>, dim3((unsigned)grid), dim3(warps * 32), 0, stream,
+                    (const VEC*)k, (const VEC*)v, (VEC*)kb, (VEC*)vb, slots, T, row_vecs,
+                    (const int*)status);
 }
 
 template <typename VEC>
@@ -411,8 +462,7 @@ cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, const PlanLay
   cudaError_t e = cudaFuncSetAttribute(k_plan_varlen, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)(2 * sizeof(int) * kPlanCacheSeqs));
   if (e != cudaSuccess) return e;
-  k_plan_varlen<<<1, 1024, dyn, stream>>>(m, plan, L, status);
-  return cudaGetLastError();
+  return launch_pdl(k_plan_varlen, dim3(1), dim3(1024), dyn, stream, m, plan, L, status);
 }
 
 cudaError_t launch_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
@@ -431,9 +481,9 @@ cudaError_t launch_slot_mapping(const int32_t* qsl, const int32_t* positions,
                                 int32_t max_blocks, int32_t block_size, int64_t num_blocks,
                                 int32_t* slots, int* status, cudaStream_t stream) {
   if (num_seqs <= 0) return cudaSuccess;
-  k_slot_mapping<<<num_seqs, 256, 0, stream>>>(qsl, positions, block_tables, num_seqs, num_tokens,
-                                               max_blocks, block_size, num_blocks, slots, status);
-  return cudaGetLastError();
+  return launch_pdl(k_slot_mapping, dim3(num_seqs), dim3(256), 0, stream, qsl, positions,
+                    block_tables, num_seqs, num_tokens, max_blocks, block_size, num_blocks, slots,
+                    status);
 }
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_blocks, void* v_blocks,
@@ -441,20 +491,17 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_block
                                      int32_t block_size, int64_t num_blocks, int* status,
                                      cudaStream_t stream) {
   if (num_tokens <= 0) return cudaSuccess;
-  const int64_t vgrid = std::min<int64_t>((num_tokens + 255) / 256, 1024);
-  k_validate_slots<<<(unsigned)vgrid, 256, 0, stream>>>(slots, num_tokens,
-                                                        num_blocks * block_size, status);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  const int64_t num_slots = num_blocks * block_size;
   if (row_bytes % 16 == 0 && aligned(k, 16) && aligned(v, 16) && aligned(k_blocks, 16) &&
       aligned(v_blocks, 16))
-    return scatter_as<uint4>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, status, stream);
+    return scatter_as<uint4>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, num_slots,
+                             status, stream);
   if (row_bytes % 4 == 0 && aligned(k, 4) && aligned(v, 4) && aligned(k_blocks, 4) &&
       aligned(v_blocks, 4))
-    return scatter_as<uint32_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, status,
-                                stream);
-  return scatter_as<uint16_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, status,
-                              stream);
+    return scatter_as<uint32_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes,
+                                num_slots, status, stream);
+  return scatter_as<uint16_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, num_slots,
+                              status, stream);
 }
 
 cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, void* v_out,

@@ -97,6 +97,25 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Launch `kern` with programmatic stream serialization: it may be scheduled while the kernel
+// before it on the stream still runs, so it must call pdl_wait() before it touches anything an
+// earlier kernel (of this library or the caller) may write.
+template <typename... Exp, typename... Act>
+inline cudaError_t launch_pdl(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Act&&>(args)...);
+}
+
 // 3-D tiled TMA load global -> shared, completing `bytes` on `bar`.  c0 is the innermost
 // coordinate; callers keep c0 * sizeof(element) a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int32_t c0,
