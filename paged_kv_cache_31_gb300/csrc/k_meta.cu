@@ -337,38 +337,38 @@ __global__ void k_reshape_and_cache(const VEC* __restrict__ k, const VEC* __rest
   }
 }
 
-// Small batches (the decode step): the slot check and the scatter in one CTA, every slot
-// checked before the first row is written.  One warp per token, as above.
-constexpr int kSmallScatter = 128;
+// Batches of up to kCheckedScatter tokens (the decode step): the slot check and the scatter in
+// one kernel.  Every CTA checks all slots before it writes (the same data, so either every CTA
+// writes or none does, with no grid-wide barrier) and then copies its own eight tokens, one
+// warp per token as above.
+constexpr int kCheckedScatter = 2048;
 template <typename VEC>
-__global__ void __launch_bounds__(1024)
-    k_scatter_small(const VEC* __restrict__ k, const VEC* __restrict__ v,
-                    VEC* __restrict__ k_blocks, VEC* __restrict__ v_blocks,
-                    const int32_t* __restrict__ slots, int num_tokens, int64_t num_slots,
-                    int64_t row_vecs, int* status) {
-  __shared__ int32_t s_slot[kSmallScatter];
+__global__ void __launch_bounds__(256)
+    k_scatter_checked(const VEC* __restrict__ k, const VEC* __restrict__ v,
+                      VEC* __restrict__ k_blocks, VEC* __restrict__ v_blocks,
+                      const int32_t* __restrict__ slots, int num_tokens, int64_t num_slots,
+                      int64_t row_vecs, int* status) {
   pdl_wait();
   pdl_launch_dependents();
   if (status_set(status)) return;  // uniform across the CTA
   bool bad = false;
   for (int t = threadIdx.x; t < num_tokens; t += blockDim.x) {
     const int32_t sl = slots[t];
-    s_slot[t] = sl;
     bad |= (sl < 0 || (int64_t)sl >= num_slots);
   }
   if (__syncthreads_or(bad)) {
-    if (threadIdx.x == 0) record_error(status, PA_EINVAL);
+    if (blockIdx.x == 0 && threadIdx.x == 0) record_error(status, PA_EINVAL);
     return;
   }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  for (int t = warp; t < num_tokens; t += nwarps) {
-    const int64_t dst = (int64_t)s_slot[t] * row_vecs, src = (int64_t)t * row_vecs;
-    for (int64_t i = lane; i < row_vecs; i += 32) {
-      const VEC a = k[src + i];
-      const VEC b = v[src + i];
-      k_blocks[dst + i] = a;
-      v_blocks[dst + i] = b;
-    }
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= num_tokens) return;
+  const int64_t dst = (int64_t)slots[t] * row_vecs, src = (int64_t)t * row_vecs;
+  for (int64_t i = lane; i < row_vecs; i += 32) {
+    const VEC a = k[src + i];
+    const VEC b = v[src + i];
+    k_blocks[dst + i] = a;
+    v_blocks[dst + i] = b;
   }
 }
 
@@ -426,10 +426,10 @@ cudaError_t scatter_as(const void* k, const void* v, void* kb, void* vb, const i
                        int64_t T, int64_t row_bytes, int64_t num_slots, int* status,
                        cudaStream_t stream) {
   const int64_t row_vecs = row_bytes / (int64_t)sizeof(VEC);
-  if (T <= kSmallScatter)
-    return launch_pdl(k_scatter_small<VEC>, dim3(1), dim3(1024), 0, stream, (const VEC*)k,
-                      (const VEC*)v, (VEC*)kb, (VEC*)vb, slots, (int)T, num_slots, row_vecs,
-                      status);
+  if (T <= kCheckedScatter)
+    return launch_pdl(k_scatter_checked<VEC>, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, stream,
+                      (const VEC*)k, (const VEC*)v, (VEC*)kb, (VEC*)vb, slots, (int)T, num_slots,
+                      row_vecs, status);
   const int64_t vgrid = std::min<int64_t>((T + 255) / 256, 1024);
   cudaError_t e = launch_pdl(k_validate_slots, dim3((unsigned)vgrid), dim3(256), 0, stream, slots,
                              T, num_slots, status);
