@@ -26,7 +26,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, EINVAL, ESHAPE, EUNSUPPORTED = 0, 1, 2, 3
-_DT = {torch.float32: 0, torch.bfloat16: 1}
+_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2}
 
 
 def build(force: bool = False) -> str:
@@ -53,23 +53,30 @@ def lib():
             L.oracle_set_num_threads.argtypes = [ctypes.c_int]
             L.oracle_slot_mapping.argtypes = [vp, vp, vp, i32, i32, i32, i64, vp]
             L.oracle_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i32]
+            L.oracle_reshape_and_cache_ex.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64,
+                                                      i32, i32, f32, f32]
             L.oracle_gather_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, i32, i32]
             L.oracle_varlen_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32,
                                                   i32, i32, i32, i64, i32, i32, i32, i32, f32, i32,
                                                   i32]
             L.oracle_varlen_attention_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64,
                                                      i32, i32, i32, i32, i64, i32, i32, i32, i32,
-                                                     f32, i32, i32, vp]
+                                                     f32, i32, i32, vp, f32, f32]
             L.oracle_splitkv_partials.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                   i32, i64, i32, i32, i32, i32, i32, f32, i32]
             L.oracle_splitkv_reduce.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
             L.oracle_merge_attn_states.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i32]
+            L.oracle_fp8_to_f32.argtypes = [ctypes.c_uint8]
+            L.oracle_fp8_to_f32.restype = f32
+            L.oracle_f32_to_fp8.argtypes = [f32]
+            L.oracle_f32_to_fp8.restype = ctypes.c_uint8
             L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
             L.oracle_bf16_to_f32.restype = f32
             L.oracle_f32_to_bf16.argtypes = [f32]
             L.oracle_f32_to_bf16.restype = ctypes.c_uint16
             for name in ("oracle_slot_mapping", "oracle_reshape_and_cache", "oracle_gather_kv",
                          "oracle_varlen_attention", "oracle_varlen_attention_ex",
+                         "oracle_reshape_and_cache_ex",
                          "oracle_splitkv_partials", "oracle_splitkv_reduce",
                          "oracle_merge_attn_states"):
                 getattr(L, name).restype = ctypes.c_int
@@ -116,6 +123,26 @@ def slot_mapping(query_start_loc, positions, block_tables, block_size, num_block
     return st, out
 
 
+def fp8_to_f32(code: int) -> float:
+    return lib().oracle_fp8_to_f32(code)
+
+
+def f32_to_fp8(x: float) -> int:
+    return lib().oracle_f32_to_fp8(x)
+
+
+def reshape_and_cache_ex(k, v, k_blocks, v_blocks, slot_mapping_, block_size, k_scale=1.0,
+                         v_scale=1.0):
+    """Scatter with conversion: the pool (possibly fp8) receives k / k_scale, v / v_scale."""
+    k, v, sm = _cpu(k), _cpu(v), _cpu(slot_mapping_)
+    assert k_blocks.is_contiguous() and v_blocks.is_contiguous()
+    T, Hkv, D = k.shape
+    return lib().oracle_reshape_and_cache_ex(_p(k), _p(v), _p(k_blocks), _p(v_blocks), _p(sm),
+                                             T, Hkv, D, block_size, k_blocks.shape[0],
+                                             _DT[k.dtype], _DT[k_blocks.dtype], float(k_scale),
+                                             float(v_scale))
+
+
 def reshape_and_cache(k, v, k_blocks, v_blocks, slot_mapping_, block_size):
     """Scatter in place into (CPU) k_blocks / v_blocks."""
     k, v, sm = _cpu(k), _cpu(v), _cpu(slot_mapping_)
@@ -139,9 +166,11 @@ def gather_kv(k_blocks, v_blocks, cu_seq_lens, block_tables, seq_starts=None):
 
 def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions, block_tables,
                      scale, causal=True, sliding_window=0, out_dtype=torch.float32,
-                     want_lse=False, num_kv_heads=None, out=None, sinks=None):
+                     want_lse=False, num_kv_heads=None, out=None, sinks=None, k_scale=1.0,
+                     v_scale=1.0):
     """Two-pass attention of every (token, head).  Returns (status, out [T,H,D], lse [H,T]).
-    sinks: optional [H] fp32 sink logits (a virtual zero-valued position per head)."""
+    sinks: optional [H] fp32 sink logits (a virtual zero-valued position per head);
+    k_scale / v_scale: dequantisation scales of the pool (K = k_scale * pool)."""
     q, kb, vb = _cpu(q), _cpu(k_blocks), _cpu(v_blocks)
     qsl, sl, pos, bt = _cpu(query_start_loc), _cpu(seq_lens), _cpu(positions), _cpu(block_tables)
     T, H, D = q.shape
@@ -156,7 +185,8 @@ def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions
                                           _p(sl), _p(pos), _p(bt), qsl.numel() - 1, T, H, Hkv, D,
                                           bs, NB, bt.shape[1], _DT[q.dtype], _DT[kb.dtype],
                                           _DT[out.dtype], float(scale), int(bool(causal)),
-                                          int(sliding_window), _p(sk))
+                                          int(sliding_window), _p(sk), float(k_scale),
+                                          float(v_scale))
     return st, out, lse
 
 

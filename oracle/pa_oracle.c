@@ -40,8 +40,9 @@
 /* Status codes of the tinyllm interface ([TL] section 4: TL_EINVAL, TL_ESHAPE;
  * section 2.6: TL_EUNSUPPORTED). */
 enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_ESHAPE = 2, ORC_EUNSUPPORTED = 3 };
-/* Element types the pages use for q / K / V / out ([MLA] LoadF/StoreF). */
-enum { ORC_F32 = 0, ORC_BF16 = 1 };
+/* Element types the pages use for q / K / V / out ([MLA] LoadF/StoreF), and fp8 (e4m3) K/V
+ * pools ([V2] kv_cache_dtype "fp8" with k_scale / v_scale; [TL] "Going further": fp8 KV). */
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8 = 2 };
 
 static int g_mutant = 0;
 #define MUTANT(n) (g_mutant == (n))
@@ -85,20 +86,62 @@ static uint16_t float_to_bf16_bits(float f) {
   return (uint16_t)(u >> 16);
 }
 
+/* fp8 e4m3 ("fn": no infinities): sign, 4 exponent bits with bias 7, 3 mantissa bits.
+ * Exponent 0 holds the subnormals m * 2^-9; S.1111.111 is NaN; the largest finite value is
+ * 1.75 * 2^8 = 448.  Widening is exact. */
+static float fp8_bits_to_float(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  float v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexpf((float)m, -9);
+  else
+    v = ldexpf(1.0f + (float)m / 8.0f, e - (MUTANT(70) ? 8 : 7)); /* s70: wrong bias */
+  return sign ? -v : v;
+}
+
+/* binary32 -> e4m3: saturate to +-448, then round to nearest, ties to even, over the
+ * representable values (subnormals included); NaN stays NaN. */
+static uint8_t float_to_fp8_bits(float f) {
+  if (isnan(f)) return 0x7f;
+  const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+  float a = fabsf(f);
+  if (a > 448.0f) a = 448.0f;
+  /* candidates: the 127 non-negative finite codes are monotone in value */
+  int lo = 0, hi = 126;
+  while (lo < hi) { /* the largest code whose value is <= a */
+    int mid = (lo + hi + 1) / 2;
+    if (fp8_bits_to_float((uint8_t)mid) <= a) lo = mid; else hi = mid - 1;
+  }
+  int code = lo;
+  if (code < 126) {
+    float below = fp8_bits_to_float((uint8_t)code), above = fp8_bits_to_float((uint8_t)(code + 1));
+    float d0 = a - below, d1 = above - a;
+    if (MUTANT(71)) d1 = INFINITY; /* s71: truncation instead of rounding */
+    if (d1 < d0 || (d1 == d0 && (code & 1))) code += 1;
+  }
+  return (uint8_t)(sign | code);
+}
+
 static float load_elem(const void* base, int dt, int64_t i) {
   if (dt == ORC_BF16) return bf16_bits_to_float(((const uint16_t*)base)[i]);
+  if (dt == ORC_FP8) return fp8_bits_to_float(((const uint8_t*)base)[i]);
   return ((const float*)base)[i];
 }
 
 static void store_elem(void* base, int dt, int64_t i, float v) {
   if (dt == ORC_BF16)
     ((uint16_t*)base)[i] = float_to_bf16_bits(v);
+  else if (dt == ORC_FP8)
+    ((uint8_t*)base)[i] = float_to_fp8_bits(v);
   else
     ((float*)base)[i] = v;
 }
 
-static int elem_bytes(int dt) { return dt == ORC_BF16 ? 2 : 4; }
+static int elem_bytes(int dt) { return dt == ORC_FP8 ? 1 : dt == ORC_BF16 ? 2 : 4; }
+/* q / out / new K-V rows: fp32 or bf16; pools: those or fp8 */
 static int dtype_ok(int dt) { return dt == ORC_F32 || dt == ORC_BF16; }
+static int pool_dtype_ok(int dt) { return dtype_ok(dt) || dt == ORC_FP8; }
 
 /* ---- where position j of a sequence lives ([TL] 2.1; [MPA] kvBaseOffset) ---
  * Logical block j / b of the sequence is physical block table[j / b]; the row
@@ -149,7 +192,7 @@ int oracle_reshape_and_cache(const void* k, const void* v, void* k_blocks, void*
                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                              int64_t num_blocks, int32_t kv_dtype) {
   if (!k || !v || !k_blocks || !v_blocks || !slot_mapping) return ORC_EINVAL;
-  if (!dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
+  if (!pool_dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
   if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return ORC_ESHAPE;
   for (int64_t t = 0; t < num_tokens; ++t) {
     int64_t slot = slot_mapping[t];
@@ -169,6 +212,32 @@ int oracle_reshape_and_cache(const void* k, const void* v, void* k_blocks, void*
   return ORC_OK;
 }
 
+/* ---- scatter with conversion: new rows of src_dtype into a pool of kv_dtype, the pool
+ * holding x / k_scale (x / v_scale) rounded to its type; for an fp8 pool that is the e4m3
+ * code of the quotient (saturated, round to nearest even).  Every slot is checked first. */
+int oracle_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                                const int32_t* slot_mapping, int64_t num_tokens,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                int64_t num_blocks, int32_t src_dtype, int32_t kv_dtype,
+                                float k_scale, float v_scale) {
+  if (!k || !v || !k_blocks || !v_blocks || !slot_mapping) return ORC_EINVAL;
+  if (!dtype_ok(src_dtype) || !pool_dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return ORC_ESHAPE;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= num_blocks * block_size) return ORC_EINVAL;
+  }
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    for (int64_t i = 0; i < row; ++i) {
+      store_elem(k_blocks, kv_dtype, slot * row + i, load_elem(k, src_dtype, t * row + i) / k_scale);
+      store_elem(v_blocks, kv_dtype, slot * row + i, load_elem(v, src_dtype, t * row + i) / v_scale);
+    }
+  }
+  return ORC_OK;
+}
+
 /* ---- gather of a sequence's rows into a dense buffer ([MLA] GatherMlaCache) --
  * Output rows [cu[s], cu[s+1]) of k_out/v_out ([rows, Hkv, D]) receive the pool
  * rows at positions (r - cu[s]) + seq_starts[s] of sequence s (seq_starts may be
@@ -181,7 +250,7 @@ int oracle_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, vo
                      int32_t max_blocks, int32_t kv_dtype) {
   if (!k_blocks || !k_out || !cu_seq_lens || !block_tables) return ORC_EINVAL;
   if ((v_blocks == NULL) != (v_out == NULL)) return ORC_EINVAL;
-  if (!dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
+  if (!pool_dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
   if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return ORC_ESHAPE;
   for (int32_t s = 0; s < num_seqs; ++s) {
     if (cu_seq_lens[s + 1] < cu_seq_lens[s]) return ORC_EINVAL;
@@ -222,7 +291,7 @@ static float attend_two_pass(const void* q, int64_t q_off, int q_dtype, const vo
                              int32_t num_kv_heads, int32_t head_dim, int32_t kv_head,
                              float scale, float* logits, float* acc, void* out,
                              int64_t out_off, int out_dtype, float* m_out, float* l_out,
-                             float sink) {
+                             float sink, float k_scale, float v_scale) {
   const int64_t n = end > start ? end - start : 0;
   /* An attention sink ([MPA] ForwardWithSinks) is one more, virtual, position whose score is
    * the sink logit and whose value is zero: it enters the max and the exp-sum, never the
@@ -237,7 +306,9 @@ static float attend_two_pass(const void* q, int64_t q_off, int q_dtype, const vo
     int64_t k_off = pool_row_offset(table_row, j, block_size, num_kv_heads, head_dim, kv_head);
     float dot = 0.0f;
     for (int32_t d = 0; d < head_dim; ++d)
-      dot += load_elem(q, q_dtype, q_off + d) * load_elem(k_blocks, kv_dtype, k_off + d);
+      dot += load_elem(q, q_dtype, q_off + d) *
+             (MUTANT(72) ? load_elem(k_blocks, kv_dtype, k_off + d)
+                         : load_elem(k_blocks, kv_dtype, k_off + d) * k_scale);
     float s = MUTANT(30) ? dot : dot * scale;
     logits[i] = s;
     if (s > m) m = s;
@@ -258,7 +329,9 @@ static float attend_two_pass(const void* q, int64_t q_off, int q_dtype, const vo
     int64_t v_off = pool_row_offset(table_row, j, block_size, num_kv_heads, head_dim, kv_head);
     const void* vsrc = MUTANT(8) ? k_blocks : v_blocks; /* s08: V read from the K pool */
     float p = logits[i];
-    for (int32_t d = 0; d < head_dim; ++d) acc[d] += p * load_elem(vsrc, kv_dtype, v_off + d);
+    for (int32_t d = 0; d < head_dim; ++d)
+      acc[d] += p * (MUTANT(73) ? load_elem(vsrc, kv_dtype, v_off + d)
+                                : load_elem(vsrc, kv_dtype, v_off + d) * v_scale);
   }
 
   /* o = acc * (1/l); an empty range writes zeros ([MPA] "Empty context: write
@@ -288,7 +361,7 @@ static int validate_varlen(const void* q, const void* k_blocks, const void* v_bl
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
     return ORC_ESHAPE;
   if (num_heads % num_kv_heads != 0) return ORC_ESHAPE;
-  if (!dtype_ok(q_dtype) || !dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
+  if (!dtype_ok(q_dtype) || !pool_dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
   if (!q || !k_blocks || !v_blocks || !out || !qsl || !seq_lens || !positions || !block_tables)
     return ORC_EINVAL;
   if (num_seqs < 0 || num_tokens < 0 || max_blocks < 0 || num_blocks < 0) return ORC_EINVAL;
@@ -317,7 +390,9 @@ static int validate_varlen(const void* q, const void* k_blocks, const void* v_bl
  * max(0, end - w) : 0  ([MPA] contextEndExclusive / contextStart), then softmax
  * attention over positions [start, end).  out is [T, H, D] in out_dtype; lse
  * (may be NULL) is [H, T] in natural log ([MLA] LSE layout). */
-/* sinks: [num_heads] sink logits on the score scale ([MPA] ForwardWithSinks), or NULL. */
+/* sinks: [num_heads] sink logits on the score scale ([MPA] ForwardWithSinks), or NULL.
+ * k_scale / v_scale: the pool holds K / k_scale and V / v_scale ([V2]: "k_flat.float()
+ * .mul_(k_scale)"), so attention uses K = k_scale * pool and V = v_scale * pool. */
 int oracle_varlen_attention_ex(const void* q, const void* k_blocks, const void* v_blocks,
                                void* out, float* lse, const int32_t* query_start_loc,
                                const int32_t* seq_lens, const int32_t* positions,
@@ -325,7 +400,8 @@ int oracle_varlen_attention_ex(const void* q, const void* k_blocks, const void* 
                                int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                                int32_t block_size, int64_t num_blocks, int32_t max_blocks,
                                int32_t q_dtype, int32_t kv_dtype, int32_t out_dtype, float scale,
-                               int32_t causal, int32_t sliding_window, const float* sinks) {
+                               int32_t causal, int32_t sliding_window, const float* sinks,
+                               float k_scale, float v_scale) {
   int st = validate_varlen(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                            block_tables, num_seqs, num_tokens, num_heads, num_kv_heads,
                            head_dim, block_size, num_blocks, max_blocks, q_dtype, kv_dtype);
@@ -362,7 +438,7 @@ int oracle_varlen_attention_ex(const void* q, const void* k_blocks, const void* 
                                     v_blocks, kv_dtype, row, start, end, block_size, num_kv_heads,
                                     head_dim, g, scale, logits, acc, out,
                                     (t * num_heads + h) * (int64_t)head_dim, out_dtype, NULL, NULL,
-                                    sinks ? sinks[h] : -INFINITY);
+                                    sinks ? sinks[h] : -INFINITY, k_scale, v_scale);
       if (lse) lse[(int64_t)h * num_tokens + t] = l_lse;
     }
     free(logits);
@@ -384,7 +460,7 @@ int oracle_varlen_attention(const void* q, const void* k_blocks, const void* v_b
                                     positions, block_tables, num_seqs, num_tokens, num_heads,
                                     num_kv_heads, head_dim, block_size, num_blocks, max_blocks,
                                     q_dtype, kv_dtype, out_dtype, scale, causal, sliding_window,
-                                    NULL);
+                                    NULL, 1.0f, 1.0f);
 }
 
 /* ---- split-KV decode, phase 1 ([V2] partition loop) ------------------------
@@ -445,7 +521,7 @@ int oracle_splitkv_partials(const void* q, const void* k_blocks, const void* v_b
       attend_two_pass(q, ((int64_t)s * num_heads + h) * head_dim, q_dtype, k_blocks, v_blocks,
                       kv_dtype, block_tables + (int64_t)s * max_blocks, lo, hi, block_size,
                       num_kv_heads, head_dim, h / group, scale, logits, acc, tmp_out,
-                      idx * head_dim, ORC_F32, &m, &l, -INFINITY);
+                      idx * head_dim, ORC_F32, &m, &l, -INFINITY, 1.0f, 1.0f);
       max_logits[idx] = m;
       exp_sums[idx] = l;
     }
@@ -580,5 +656,8 @@ int oracle_merge_attn_states(void* out, float* out_lse, const void* prefix_out,
 }
 
 /* Codec entry points, so the tests can pin the rounding against known values. */
+float oracle_fp8_to_f32(uint8_t b) { return fp8_bits_to_float(b); }
+uint8_t oracle_f32_to_fp8(float f) { return float_to_fp8_bits(f); }
+
 float oracle_bf16_to_f32(uint16_t b) { return bf16_bits_to_float(b); }
 uint16_t oracle_f32_to_bf16(float f) { return float_to_bf16_bits(f); }

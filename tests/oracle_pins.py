@@ -16,7 +16,8 @@ value, identity or special case that does not come from the oracle itself:
   merge's infinite-lse special cases (vllm.cpp cpu_mla_prefill.cpp,
   MergeAttnStatesKernel);
 * the validation contract (tinyllm section 2.6 / bad_tables_and_shapes);
-* bfloat16 rounding against torch's own conversion.
+* bfloat16 rounding against torch's own conversion, and the fp8 (e4m3) codes of every value
+  against torch's float8_e4m3fn (with the pools' dequantisation scales).
 
 The mutant test (test_oracle_mutants.py) plants known mistakes in the oracle
 and checks that each is caught by at least one of these pins.
@@ -295,6 +296,100 @@ def pin_sinks_brute_force(seed=43):
                 np.testing.assert_allclose(out[a:z, h].numpy(), want, rtol=1e-5, atol=2e-5)
                 want_lse = (mx[:, 0] + np.log(e.sum(axis=1)))
                 np.testing.assert_allclose(lse[h, a:z].numpy(), want_lse, rtol=1e-5, atol=2e-5)
+
+
+# --------------------------------------------------------------------------------------------
+# fp8 (e4m3) K/V pools with dequantisation scales (the V2 page's kv_cache_dtype "fp8",
+# k_scale / v_scale: attention uses K = k_scale * pool, V = v_scale * pool)
+
+
+def pin_fp8_codec():
+    # decoding: every code, against torch's float8_e4m3fn
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).float()
+    got = torch.tensor([oracle.fp8_to_f32(int(c)) for c in codes])
+    assert bool(((ref == got) | (ref.isnan() & got.isnan())).all())
+    # encoding: saturate to +-448, then round to nearest even -- torch's cast after a clamp
+    # (values: every midpoint between neighbouring codes, their neighbours, and a sweep)
+    fin = ref[(codes < 127)]  # non-negative finite codes, increasing
+    mids = (fin[:-1] + fin[1:]) / 2
+    g = torch.Generator().manual_seed(71)
+    sweep = torch.randn(4000, generator=g) * torch.exp(torch.randn(4000, generator=g) * 3)
+    xs = torch.cat([mids, torch.nextafter(mids, torch.zeros_like(mids)),
+                    torch.nextafter(mids, torch.full_like(mids, 1e4)), sweep, -sweep,
+                    torch.tensor([0.0, -0.0, 448.0, 449.0, 1e6, -1e6, 2.0 ** -10])])
+    want = torch.clamp(xs, -448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    got = torch.tensor([oracle.f32_to_fp8(float(x)) for x in xs], dtype=torch.uint8)
+    assert torch.equal(got, want)
+
+
+def pin_fp8_scatter():
+    # the pool receives the e4m3 code of x / scale, exactly as torch quantises it
+    g = torch.Generator().manual_seed(72)
+    T, Hkv, D, b, NB = 20, 2, 32, 16, 4
+    k = (torch.randn((T, Hkv, D), generator=g) * 3).to(torch.bfloat16)
+    v = (torch.randn((T, Hkv, D), generator=g) * 100).to(torch.bfloat16)
+    kb = torch.zeros((NB, b, Hkv, D), dtype=torch.float8_e4m3fn)
+    vb = torch.zeros_like(kb)
+    slots = torch.randperm(NB * b, generator=g)[:T].to(torch.int32)
+    ks, vs = 0.0625, 0.37
+    st = oracle.reshape_and_cache_ex(k, v, kb, vb, slots, b, k_scale=ks, v_scale=vs)
+    assert st == oracle.OK
+    q = lambda x, sc: torch.clamp(x.float() / sc, -448, 448).to(torch.float8_e4m3fn)
+    for t in range(T):
+        sl = int(slots[t])
+        assert torch.equal(kb[sl // b, sl % b].view(torch.uint8), q(k[t], ks).view(torch.uint8))
+        assert torch.equal(vb[sl // b, sl % b].view(torch.uint8), q(v[t], vs).view(torch.uint8))
+
+
+def _fp8_case(seed=73):
+    H, Hkv, D, b = 6, 2, 32, 16
+    lens, qlens = [1, 37, 70], [1, 5, 70]
+    gen = torch.Generator().manual_seed(seed)
+    dk = [torch.randn((n, Hkv, D), generator=gen) for n in lens]
+    dv = [torch.randn((n, Hkv, D), generator=gen) for n in lens]
+    kb, vb, table = _paged_from_dense(dk, dv, b, seed + 1)
+    kb8, vb8 = (kb * 4).to(torch.float8_e4m3fn), (vb * 4).to(torch.float8_e4m3fn)
+    T = sum(qlens)
+    q = torch.randn((T, H, D), generator=gen)
+    qsl = np.cumsum([0] + qlens).tolist()
+    pos = [p for n, ql in zip(lens, qlens) for p in range(n - ql, n)]
+    return H, Hkv, D, lens, qsl, pos, q, kb8, vb8, table
+
+
+def pin_fp8_attention_brute_force():
+    H, Hkv, D, lens, qsl, pos, q, kb8, vb8, table = _fp8_case()
+    ks, vs = 0.25, 0.37
+    scale = 1.0 / math.sqrt(D)
+    for window in (0, 20):
+        st, out, _ = oracle.varlen_attention(q, kb8, vb8, _t(qsl), _t(lens), _t(pos), table,
+                                             scale=scale, sliding_window=window, k_scale=ks,
+                                             v_scale=vs)
+        assert st == oracle.OK
+        for s, n in enumerate(lens):
+            rows = [table[s, j // 16] for j in range(n)]
+            dk = torch.stack([kb8[int(rows[j]), j % 16].float() for j in range(n)]) * ks
+            dv = torch.stack([vb8[int(rows[j]), j % 16].float() for j in range(n)]) * vs
+            a, z = qsl[s], qsl[s + 1]
+            want = _dense_attention_f64(q[a:z].numpy(), dk.numpy(), dv.numpy(), pos[a:z], n,
+                                        scale, True, window)
+            np.testing.assert_allclose(out[a:z].numpy(), want, rtol=1e-5, atol=2e-5)
+
+
+def pin_dequant_scales():
+    # k_scale multiplies every score exactly as the softmax scale does; v_scale multiplies the
+    # output (a bf16 pool here: the scales are general dequantisation factors)
+    w = workloads.build("scales", seq_lens=[5, 40, 70], q_lens=[1, 3, 2], num_heads=4,
+                        num_kv_heads=2, head_dim=16, dtype=torch.float32, seed=74)
+    meta = dict(query_start_loc=w.query_start_loc, seq_lens=w.seq_lens, positions=w.positions,
+                block_tables=w.block_tables)
+    st, o1, l1 = oracle.varlen_attention(w.q, w.k_blocks, w.v_blocks, scale=w.scale * 2.5,
+                                         want_lse=True, **meta)
+    st2, o2, l2 = oracle.varlen_attention(w.q, w.k_blocks, w.v_blocks, scale=w.scale,
+                                          want_lse=True, k_scale=2.5, v_scale=3.0, **meta)
+    assert st == oracle.OK and st2 == oracle.OK
+    np.testing.assert_allclose(o2.numpy(), 3.0 * o1.numpy(), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(l2.numpy(), l1.numpy(), rtol=1e-5, atol=1e-6)
 
 
 # --------------------------------------------------------------------------------------------
@@ -628,6 +723,10 @@ def pin_bf16_codec():
 
 
 ALL_PINS = {
+    "fp8_codec": pin_fp8_codec,
+    "fp8_scatter": pin_fp8_scatter,
+    "fp8_attention_brute_force": pin_fp8_attention_brute_force,
+    "dequant_scales": pin_dequant_scales,
     "sinks_closed_forms": pin_sinks_closed_forms,
     "sinks_brute_force": pin_sinks_brute_force,
     "hand_example": pin_hand_example,

@@ -6,7 +6,9 @@ round-robin GQA, s06 a window of w + 1, s07 query at n instead of n - 1, s08 V
 read from the K pool, s13 empty context accepted, s14 max_blocks trusted, s15
 block ids trusted) and further plausible slips in the scatter, gather, score,
 split-KV reduction and merge arithmetic, and in the attention-sink term (s60 the sink
-left out of the exp-sum, s61 its term taken as 1 instead of e^(sink - m)).
+left out of the exp-sum, s61 its term taken as 1 instead of e^(sink - m)) and the fp8 pools
+(s70 a wrong exponent bias, s71 truncation instead of rounding, s72 / s73 a dequantisation
+scale ignored).
 """
 import pytest
 
@@ -37,6 +39,10 @@ KILLERS = {
     52: ["merge_identity"],
     60: ["sinks_closed_forms", "sinks_brute_force"],
     61: ["sinks_closed_forms", "sinks_brute_force"],
+    70: ["fp8_codec", "fp8_attention_brute_force"],
+    71: ["fp8_codec", "fp8_scatter"],
+    72: ["fp8_attention_brute_force", "dequant_scales"],
+    73: ["fp8_attention_brute_force", "dequant_scales"],
 }
 
 
