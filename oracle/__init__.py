@@ -64,6 +64,9 @@ def lib():
                                                      f32, i32, i32, vp, f32, f32]
             L.oracle_splitkv_partials.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                   i32, i64, i32, i32, i32, i32, i32, f32, i32]
+            L.oracle_splitkv_partials_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                     i32, i32, i64, i32, i32, i32, i32, i32, f32,
+                                                     i32, f32, f32]
             L.oracle_splitkv_reduce.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
             L.oracle_merge_attn_states.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i32]
             L.oracle_fp8_to_f32.argtypes = [ctypes.c_uint8]
@@ -77,7 +80,8 @@ def lib():
             for name in ("oracle_slot_mapping", "oracle_reshape_and_cache", "oracle_gather_kv",
                          "oracle_varlen_attention", "oracle_varlen_attention_ex",
                          "oracle_reshape_and_cache_ex",
-                         "oracle_splitkv_partials", "oracle_splitkv_reduce",
+                         "oracle_splitkv_partials", "oracle_splitkv_partials_ex",
+                         "oracle_splitkv_reduce",
                          "oracle_merge_attn_states"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -191,18 +195,20 @@ def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions
 
 
 def splitkv_partials(q, k_blocks, v_blocks, seq_lens, block_tables, scale, partition_size,
-                     max_parts, sliding_window=0):
-    """Phase 1 of split-KV decode: (status, max_logits, exp_sums, tmp_out)."""
+                     max_parts, sliding_window=0, k_scale=1.0, v_scale=1.0):
+    """Phase 1 of split-KV decode: (status, max_logits, exp_sums, tmp_out).  k_scale / v_scale:
+    dequantisation scales of the pool (K = k_scale * pool)."""
     q, kb, vb, sl, bt = _cpu(q), _cpu(k_blocks), _cpu(v_blocks), _cpu(seq_lens), _cpu(block_tables)
     S, H, D = q.shape
     NB, bs, Hkv, _ = kb.shape
     ml = torch.full((S, H, max_parts), float("nan"), dtype=torch.float32)
     es = torch.full((S, H, max_parts), float("nan"), dtype=torch.float32)
     to = torch.full((S, H, max_parts, D), float("nan"), dtype=torch.float32)
-    st = lib().oracle_splitkv_partials(_p(q), _p(kb), _p(vb), _p(ml), _p(es), _p(to), _p(sl),
-                                       _p(bt), S, H, Hkv, D, bs, NB, bt.shape[1], partition_size,
-                                       max_parts, _DT[q.dtype], _DT[kb.dtype], float(scale),
-                                       int(sliding_window))
+    st = lib().oracle_splitkv_partials_ex(_p(q), _p(kb), _p(vb), _p(ml), _p(es), _p(to), _p(sl),
+                                          _p(bt), S, H, Hkv, D, bs, NB, bt.shape[1],
+                                          partition_size, max_parts, _DT[q.dtype], _DT[kb.dtype],
+                                          float(scale), int(sliding_window), float(k_scale),
+                                          float(v_scale))
     return st, ml, es, to
 
 

@@ -471,19 +471,21 @@ int oracle_varlen_attention(const void* q, const void* k_blocks, const void* v_b
  * max scaled score, its exp-sum and its NORMALISED output sum_j e^{s_j-m} v_j / l
  * (the reading taken of the page's reduction, which only makes sense when
  * tmp_output holds normalised partition outputs).  Partitions with no visible
- * position, including those at or past ceil(seq_len / P), get (-inf, 0, zeros). */
-int oracle_splitkv_partials(const void* q, const void* k_blocks, const void* v_blocks,
-                            float* max_logits, float* exp_sums, float* tmp_out,
-                            const int32_t* seq_lens, const int32_t* block_tables,
-                            int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
-                            int32_t head_dim, int32_t block_size, int64_t num_blocks,
-                            int32_t max_blocks, int32_t partition_size, int32_t max_parts,
-                            int32_t q_dtype, int32_t kv_dtype, float scale,
-                            int32_t sliding_window) {
+ * position, including those at or past ceil(seq_len / P), get (-inf, 0, zeros).
+ * k_scale / v_scale: the pools hold K / k_scale and V / v_scale, possibly as fp8
+ * ([V2]: kv_cache_dtype, "Apply scales" before the partition loop). */
+int oracle_splitkv_partials_ex(const void* q, const void* k_blocks, const void* v_blocks,
+                               float* max_logits, float* exp_sums, float* tmp_out,
+                               const int32_t* seq_lens, const int32_t* block_tables,
+                               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                               int32_t max_blocks, int32_t partition_size, int32_t max_parts,
+                               int32_t q_dtype, int32_t kv_dtype, float scale,
+                               int32_t sliding_window, float k_scale, float v_scale) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0 || partition_size <= 0 || max_parts <= 0)
     return ORC_ESHAPE;
-  if (!dtype_ok(q_dtype) || !dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
+  if (!dtype_ok(q_dtype) || !pool_dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
   if (!q || !k_blocks || !v_blocks || !max_logits || !exp_sums || !tmp_out || !seq_lens ||
       !block_tables)
     return ORC_EINVAL;
@@ -521,7 +523,7 @@ int oracle_splitkv_partials(const void* q, const void* k_blocks, const void* v_b
       attend_two_pass(q, ((int64_t)s * num_heads + h) * head_dim, q_dtype, k_blocks, v_blocks,
                       kv_dtype, block_tables + (int64_t)s * max_blocks, lo, hi, block_size,
                       num_kv_heads, head_dim, h / group, scale, logits, acc, tmp_out,
-                      idx * head_dim, ORC_F32, &m, &l, -INFINITY, 1.0f, 1.0f);
+                      idx * head_dim, ORC_F32, &m, &l, -INFINITY, k_scale, v_scale);
       max_logits[idx] = m;
       exp_sums[idx] = l;
     }
@@ -529,6 +531,21 @@ int oracle_splitkv_partials(const void* q, const void* k_blocks, const void* v_b
     free(acc);
   }
   return ORC_OK;
+}
+
+int oracle_splitkv_partials(const void* q, const void* k_blocks, const void* v_blocks,
+                            float* max_logits, float* exp_sums, float* tmp_out,
+                            const int32_t* seq_lens, const int32_t* block_tables,
+                            int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                            int32_t max_blocks, int32_t partition_size, int32_t max_parts,
+                            int32_t q_dtype, int32_t kv_dtype, float scale,
+                            int32_t sliding_window) {
+  return oracle_splitkv_partials_ex(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out,
+                                    seq_lens, block_tables, num_seqs, num_heads, num_kv_heads,
+                                    head_dim, block_size, num_blocks, max_blocks, partition_size,
+                                    max_parts, q_dtype, kv_dtype, scale, sliding_window, 1.0f,
+                                    1.0f);
 }
 
 /* ---- log-sum-exp of one partition ----------------------------------------

@@ -490,6 +490,25 @@ def pin_splitkv_matches_full():
                 assert torch.all(to[s, :, p] == 0)
 
 
+def pin_splitkv_fp8_scaled():
+    # split-KV partials over an fp8 pool with scales (the V2 page: kv_cache_dtype "fp8",
+    # k_scale, v_scale) equal, bit for bit, the partials over the fp32 pool holding
+    # k_scale * value(code) and v_scale * value(code) (torch's e4m3 decoding, one fp32 product)
+    w = _split_case(window=700, seed=35)
+    g = torch.Generator().manual_seed(36)
+    kb8 = (torch.randn(w.k_blocks.shape, generator=g) * 8).to(torch.float8_e4m3fn)
+    vb8 = (torch.randn(w.v_blocks.shape, generator=g) * 8).to(torch.float8_e4m3fn)
+    ks, vs = 0.15, 0.11
+    P, MP = 512, w.max_partitions()
+    a = oracle.splitkv_partials(w.q, kb8, vb8, w.seq_lens, w.block_tables, w.scale, P, MP, 700,
+                                k_scale=ks, v_scale=vs)
+    b = oracle.splitkv_partials(w.q, kb8.float() * ks, vb8.float() * vs, w.seq_lens,
+                                w.block_tables, w.scale, P, MP, 700)
+    assert a[0] == oracle.OK and b[0] == oracle.OK
+    for x, y in zip(a[1:], b[1:]):
+        assert torch.equal(x, y)
+
+
 def pin_splitkv_single_partition_passthrough():
     w = _split_case()
     st, ml, es, to = oracle.splitkv_partials(w.q, w.k_blocks, w.v_blocks, w.seq_lens,
@@ -737,6 +756,7 @@ ALL_PINS = {
     "batch_and_shared_prefix": pin_batch_invariance_and_shared_prefix,
     "threads": pin_thread_invariance,
     "splitkv_matches_full": pin_splitkv_matches_full,
+    "splitkv_fp8_scaled": pin_splitkv_fp8_scaled,
     "splitkv_single_partition": pin_splitkv_single_partition_passthrough,
     "splitkv_masked_partition": pin_splitkv_masked_partition,
     "splitkv_all_masked": pin_splitkv_all_masked,

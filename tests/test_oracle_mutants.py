@@ -41,8 +41,8 @@ KILLERS = {
     61: ["sinks_closed_forms", "sinks_brute_force"],
     70: ["fp8_codec", "fp8_attention_brute_force"],
     71: ["fp8_codec", "fp8_scatter"],
-    72: ["fp8_attention_brute_force", "dequant_scales"],
-    73: ["fp8_attention_brute_force", "dequant_scales"],
+    72: ["fp8_attention_brute_force", "dequant_scales", "splitkv_fp8_scaled"],
+    73: ["fp8_attention_brute_force", "dequant_scales", "splitkv_fp8_scaled"],
 }
 
 
