@@ -95,10 +95,11 @@ def _ranges(w):
             yield s, b, e
 
 
-def kv_bytes(w) -> int:
+def kv_bytes(w, elem_bytes=None) -> int:
     """K and V bytes the attention must read: every visible (position, kv head) row once per
-    sequence (the union of its tokens' visible ranges)."""
-    esz = 2 if str(w.dtype).endswith("bfloat16") else 4
+    sequence (the union of its tokens' visible ranges).  elem_bytes: the pool's element size
+    when it differs from w.dtype's (1 for fp8 pools)."""
+    esz = elem_bytes or (2 if str(w.dtype).endswith("bfloat16") else 4)
     row = w.num_kv_heads * w.head_dim * esz * 2
     span = {}
     for s, b, e in _ranges(w):
@@ -305,8 +306,9 @@ class Runner:
 
 def time_calls(fn, n, stream, flush=None):
     """Mean ms per call of fn over n calls, timed with CUDA events on `stream`.  With `flush`
-    (a buffer larger than L2) every call is timed on its own after overwriting the buffer,
-    so no call finds the previous one's inputs in L2."""
+    (two buffers larger than L2) every call is timed on its own after overwriting the first
+    buffer and then reading the second: no call finds the previous one's inputs in L2, and
+    the flush's dirty lines are written back before the timed call, not inside it."""
     import torch
 
     if flush is None:
@@ -319,8 +321,10 @@ def time_calls(fn, n, stream, flush=None):
         return e0.elapsed_time(e1) / n
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n)]
+    wbuf, rbuf = flush
     for a, b in ev:
-        flush.add_(1)
+        wbuf.add_(1)
+        rbuf.amax()
         a.record(stream)
         fn()
         b.record(stream)
@@ -329,10 +333,11 @@ def time_calls(fn, n, stream, flush=None):
 
 
 def l2_flush_buffer(dev):
-    """256 MB, about twice the GB300's L2."""
+    """Two buffers of 256 MB, each about twice the GB300's L2: one to overwrite, one to read."""
     import torch
 
-    return torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    return (torch.zeros(64 << 20, dtype=torch.float32, device=dev),
+            torch.zeros(64 << 20, dtype=torch.float32, device=dev))
 
 
 def secondary(pa, dev, args, peaks, stream):
@@ -377,6 +382,29 @@ def secondary(pa, dev, args, peaks, stream):
     }
     assert pa.pa_device_status() == pa.PA_OK
     del w3, r3, wp, wd, rp, rd
+    torch.cuda.empty_cache()
+
+    # the decode batch over fp8 (e4m3) pools with dequantisation scales: half the K/V bytes
+    w2 = workloads.named(2, seed=args.seed, device=dev)
+    kb8, vb8 = workloads.fp8_pools(w2)
+    out2 = torch.empty_like(w2.q)
+    ws2 = pa.workspace_for(w2.q, kb8, w2.query_start_loc, w2.block_tables)
+
+    def fp8_call():
+        pa.pa_varlen_forward(w2.q, kb8, vb8, out2, w2.query_start_loc, w2.seq_lens,
+                             w2.positions, w2.block_tables, w2.scale, workspace=ws2,
+                             k_scale=0.125, v_scale=0.125)
+
+    for _ in range(3):
+        fp8_call()
+    ms8 = time_calls(fp8_call, n, stream)
+    kv8 = kv_bytes(w2, elem_bytes=1)
+    res["fp8_decode"] = {"workload": w2.name + "-fp8", "kv_bytes": kv8, "ms": ms8,
+                         "gbs": kv8 / (ms8 * 1e-3) / 1e9,
+                         "frac_of_hbm": kv8 / (ms8 * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                         "l2": "inputs (pools of ~300 MB) larger than L2"}
+    assert pa.pa_device_status() == pa.PA_OK
+    del w2, kb8, vb8, out2, ws2
     torch.cuda.empty_cache()
 
     w4 = workloads.named(4, seed=args.seed, device=dev)

@@ -52,8 +52,13 @@ typedef enum {
   PA_ETIMEOUT = 5      /* a bounded wait inside a kernel ran out */
 } pa_status;
 
-/* Element types (vllm.cpp cpu_mla_prefill.cpp LoadF/StoreF: f32 and bf16). */
-typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+/* Element types (vllm.cpp cpu_mla_prefill.cpp LoadF/StoreF: f32 and bf16), and fp8 e4m3
+ * for K/V pools only ("paged_attention_v2_pytorch.py": kv_cache_dtype "fp8" with k_scale /
+ * v_scale; tinyllm "Going further": fp8 KV caches, half the bytes per token).  PA_FP8_E4M3
+ * is the OCP e4m3 "fn" format: 1 sign, 4 exponent (bias 7) and 3 mantissa bits, no
+ * infinities, S.1111.111 NaN, largest finite value 448.  q, out and new K/V rows are f32 or
+ * bf16. */
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int pa_version(void);
@@ -83,7 +88,9 @@ pa_status pa_slot_mapping(const int32_t* query_start_loc, const int32_t* positio
  * pa_reshape_and_cache -- scatter the new tokens' K and V rows into the pool
  * (TensorSharp WriteKvToPagedPool): the num_kv_heads * head_dim elements of token t go to
  * block slot_mapping[t] / block_size, row slot_mapping[t] % block_size, of each pool.
- * A pure copy: bit-exact.  Every slot is checked on the device before any row is written;
+ * A pure copy: bit-exact (for PA_FP8_E4M3 the new rows are e4m3 codes already; to quantise
+ * f32 / bf16 rows into an fp8 pool use pa_reshape_and_cache_ex).  Every slot is checked on
+ * the device before any row is written;
  * one slot outside [0, num_blocks * block_size) writes nothing and records PA_EINVAL.
  * Duplicate slots are undefined.
  */
@@ -91,6 +98,21 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_blocks, voi
                                const int32_t* slot_mapping, int64_t num_tokens,
                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                int64_t num_blocks, pa_dtype kv_dtype, cudaStream_t stream);
+
+/*
+ * pa_reshape_and_cache_ex -- the scatter of pa_reshape_and_cache with a conversion: new rows
+ * of src_dtype (f32 or bf16) go into pools of kv_dtype (f32, bf16 or fp8 e4m3), element x of
+ * K stored as x / k_scale and of V as x / v_scale, the quotient taken in fp32 (IEEE division)
+ * and rounded to kv_dtype to nearest, ties to even; an fp8 store saturates to +-448
+ * ("paged_attention_v2_pytorch.py": the pool holds K / k_scale, so that K = k_scale * pool).
+ * k_scale and v_scale must be finite and positive (PA_EINVAL otherwise).  Slots are checked as
+ * in pa_reshape_and_cache.  Same pool layout [num_blocks, block_size, num_kv_heads, head_dim].
+ */
+pa_status pa_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                                  const int32_t* slot_mapping, int64_t num_tokens,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int64_t num_blocks, pa_dtype src_dtype, pa_dtype kv_dtype,
+                                  float k_scale, float v_scale, cudaStream_t stream);
 
 /*
  * pa_varlen_forward_workspace_size -- bytes of device workspace pa_varlen_forward needs
@@ -109,7 +131,8 @@ size_t pa_varlen_forward_workspace_size(int32_t num_seqs, int64_t num_tokens, in
  *     start = sliding_window > 0 ? max(0, end - sliding_window) : 0
  *     out[t, h] = softmax_j(scale * q[t, h] . K_j) V_j   over positions j in [start, end)
  * where K_j, V_j are pool rows of kv head g found through the block table.  out has
- * q_dtype.  k_blocks/v_blocks have kv_dtype.
+ * q_dtype.  k_blocks/v_blocks have kv_dtype (PA_FP8_E4M3: the codes' values, i.e. scales 1;
+ * see pa_varlen_forward_ex for scaled pools).
  * Validation (tinyllm section 2.6), for every sequence with at least one query token:
  * seq_lens[s] >= 1, ceil(seq_lens[s] / block_size) <= max_blocks_per_seq, those table
  * entries in [0, num_blocks), positions in [0, seq_lens[s]); query_start_loc starts at 0,
@@ -129,8 +152,8 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
                             cudaStream_t stream);
 
 /*
- * pa_varlen_forward_ex -- pa_varlen_forward with two optional extras (either may be NULL;
- * with both NULL the call is pa_varlen_forward):
+ * pa_varlen_forward_ex -- pa_varlen_forward with optional extras (with sinks and lse NULL and
+ * both scales 1 the call is pa_varlen_forward):
  *   sinks  [num_heads] fp32, device.  Per-head attention sink logits on the score scale
  *          (TensorSharp ForwardWithSinks): a virtual position with score sinks[h] and value
  *          zero, so with the visible scores s_j
@@ -141,8 +164,17 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
  *              lse[h, t] = log(e^sinks[h] + sum_j e^(s_j))   (natural log, sink term when given)
  *          and -inf when the sum is empty (no visible position and no sink).  It is what
  *          pa_merge_attn_states takes to combine two partial attentions of the same queries.
- * Both are read or written only for tokens of sequences with query tokens, and lse is left
- * untouched on a validation failure, like out.
+ *   k_scale, v_scale  dequantisation scales of the pools ("paged_attention_v2_pytorch.py":
+ *          K = k_scale * k_blocks, V = v_scale * v_blocks before the attention), finite and
+ *          > 0 (PA_EINVAL otherwise).  The scores above are scale * q . K_j with the scaled K.
+ *          kv_dtype PA_FP8_E4M3 (pools written by pa_reshape_and_cache_ex) is accepted here:
+ *          the pool's codes widen exactly to f16; on the tensor-core path q (bf16) enters the
+ *          products as f16, so q entries must lie within f16's range (|q| <= 65504; entries
+ *          below 2^-14 keep f16's subnormal precision), and the softmax weights enter the PV
+ *          product as f16 (2^-11 relative).  fp8 pools take the warp-MMA kernel for head size
+ *          128 with 16-position blocks and the generic kernel otherwise.
+ * sinks and lse are read or written only for tokens of sequences with query tokens, and lse
+ * is left untouched on a validation failure, like out.
  */
 pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* v_blocks,
                                void* out, const int32_t* query_start_loc,
@@ -152,8 +184,8 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
                                int32_t block_size, int64_t num_blocks,
                                int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
                                float scale, int32_t causal, int32_t sliding_window,
-                               const float* sinks, float* lse, void* workspace,
-                               size_t workspace_bytes, cudaStream_t stream);
+                               const float* sinks, float* lse, float k_scale, float v_scale,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * pa_varlen_forward_noalloc -- pa_varlen_forward for callers that cannot allocate device
@@ -209,6 +241,22 @@ pa_status pa_decode_splitkv_partials(const void* q, const void* k_blocks, const 
                                      int32_t max_num_partitions, pa_dtype q_dtype,
                                      pa_dtype kv_dtype, float scale, int32_t sliding_window,
                                      cudaStream_t stream);
+
+/*
+ * pa_decode_splitkv_partials_ex -- pa_decode_splitkv_partials over scaled pools
+ * ("paged_attention_v2_pytorch.py": kv_cache_dtype, k_scale, v_scale; K = k_scale * k_blocks
+ * and V = v_scale * v_blocks, both finite and > 0, else PA_EINVAL).  kv_dtype may be
+ * PA_FP8_E4M3 (bf16 q and head size 128 take the warp-MMA kernel, with the f16 operand
+ * rounding described at pa_varlen_forward_ex).  pa_decode_splitkv_partials is this call with
+ * both scales 1; the reduce step needs no scales.
+ */
+pa_status pa_decode_splitkv_partials_ex(
+    const void* q, const void* k_blocks, const void* v_blocks, float* max_logits,
+    float* exp_sums, float* tmp_out, const int32_t* seq_lens, const int32_t* block_tables,
+    int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int32_t partition_size,
+    int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
+    int32_t sliding_window, float k_scale, float v_scale, cudaStream_t stream);
 
 /*
  * pa_decode_splitkv_reduce -- phase 2 ("Phase 2: Cross-partition reduction").  For each

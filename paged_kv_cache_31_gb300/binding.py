@@ -23,8 +23,8 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 PA_OK, PA_EINVAL, PA_ESHAPE, PA_EUNSUPPORTED, PA_ECUDA, PA_ETIMEOUT = range(6)
-PA_F32, PA_BF16 = 0, 1
-_DT = {torch.float32: PA_F32, torch.bfloat16: PA_BF16}
+PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
+_DT = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float8_e4m3fn: PA_FP8_E4M3}
 
 _vp, _i32, _i64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                               ctypes.c_size_t)
@@ -35,19 +35,24 @@ _SIGS = {
     "pa_slot_mapping": ([_vp, _vp, _vp, _i32, _i64, _i32, _i32, _i64, _vp, _vp], ctypes.c_int),
     "pa_reshape_and_cache": ([_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64, ctypes.c_int,
                               _vp], ctypes.c_int),
+    "pa_reshape_and_cache_ex": ([_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64,
+                                 ctypes.c_int, ctypes.c_int, _f32, _f32, _vp], ctypes.c_int),
     "pa_varlen_forward_workspace_size": ([_i32, _i64, _i32, _i32, _i32, _i32, _i32], _sz),
     "pa_varlen_forward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
                            _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32, _i32, _vp,
                            _sz, _vp], ctypes.c_int),
     "pa_varlen_forward_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
                               _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32,
-                              _i32, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
+                              _i32, _vp, _vp, _f32, _f32, _vp, _sz, _vp], ctypes.c_int),
     "pa_varlen_forward_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
                                    _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32,
                                    _i32, _vp], ctypes.c_int),
     "pa_decode_splitkv_partials": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                     _i32, _i64, _i32, _i32, _i32, ctypes.c_int, ctypes.c_int, _f32,
                                     _i32, _vp], ctypes.c_int),
+    "pa_decode_splitkv_partials_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                       _i32, _i32, _i64, _i32, _i32, _i32, ctypes.c_int,
+                                       ctypes.c_int, _f32, _i32, _f32, _f32, _vp], ctypes.c_int),
     "pa_decode_splitkv_reduce": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                   ctypes.c_int, _vp], ctypes.c_int),
     "pa_decode_splitkv": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -128,20 +133,32 @@ def pa_slot_mapping(query_start_loc, positions, block_tables, block_size, num_bl
     return out
 
 
-def pa_reshape_and_cache(k, v, k_blocks, v_blocks, slot_mapping, stream=None):
+def pa_reshape_and_cache(k, v, k_blocks, v_blocks, slot_mapping, stream=None, k_scale=None,
+                         v_scale=None):
+    """pa_reshape_and_cache (rows and pools of one dtype, a copy), or pa_reshape_and_cache_ex
+    when the pools' dtype differs from the rows' or a scale is given (pool = rows / scale,
+    rounded to the pool's dtype, e.g. torch.float8_e4m3fn)."""
     _dev(k, v, k_blocks, v_blocks, slot_mapping)
     _i32t(slot_mapping)
     if k.shape != v.shape or k.dim() != 3 or k_blocks.shape != v_blocks.shape:
         raise ValueError("k, v must be [T, Hkv, D]; pools [NB, b, Hkv, D]")
-    if k.dtype != k_blocks.dtype or v.dtype != v_blocks.dtype or k.dtype != v.dtype:
-        raise ValueError("new rows and pools must share one dtype")
+    if k.dtype != v.dtype or k_blocks.dtype != v_blocks.dtype:
+        raise ValueError("k and v (and the two pools) must share one dtype")
     T, Hkv, D = k.shape
     NB, bs, Hkv2, D2 = k_blocks.shape
     if (Hkv, D) != (Hkv2, D2):
         raise ValueError("kv heads / head size differ between rows and pool")
-    _check(_lib.pa_reshape_and_cache(_p(k), _p(v), _p(k_blocks), _p(v_blocks), _p(slot_mapping), T,
-                                     Hkv, D, bs, NB, _DT[k.dtype], _stream(stream)),
-           "pa_reshape_and_cache")
+    if k.dtype == k_blocks.dtype and k_scale is None and v_scale is None:
+        _check(_lib.pa_reshape_and_cache(_p(k), _p(v), _p(k_blocks), _p(v_blocks),
+                                         _p(slot_mapping), T, Hkv, D, bs, NB, _DT[k.dtype],
+                                         _stream(stream)), "pa_reshape_and_cache")
+        return
+    _check(_lib.pa_reshape_and_cache_ex(_p(k), _p(v), _p(k_blocks), _p(v_blocks),
+                                        _p(slot_mapping), T, Hkv, D, bs, NB, _DT[k.dtype],
+                                        _DT[k_blocks.dtype],
+                                        1.0 if k_scale is None else float(k_scale),
+                                        1.0 if v_scale is None else float(v_scale),
+                                        _stream(stream)), "pa_reshape_and_cache_ex")
 
 
 def pa_varlen_forward_workspace_size(num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
@@ -160,9 +177,9 @@ def workspace_for(q, k_blocks, query_start_loc, block_tables):
 
 def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                       block_tables, scale, causal=True, sliding_window=0, workspace=None,
-                      stream=None, sinks=None, lse=None):
-    """pa_varlen_forward, or pa_varlen_forward_ex when sinks ([H] fp32 sink logits) or lse
-    (a [H, T] fp32 output) is given."""
+                      stream=None, sinks=None, lse=None, k_scale=1.0, v_scale=1.0):
+    """pa_varlen_forward, or pa_varlen_forward_ex when sinks ([H] fp32 sink logits), lse
+    (a [H, T] fp32 output) or a dequantisation scale other than 1 is given."""
     _dev(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions, block_tables, workspace,
          sinks, lse)
     _i32t(query_start_loc, seq_lens, positions, block_tables)
@@ -176,7 +193,7 @@ def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, pos
         raise ValueError("head size differs between q and the pool")
     if workspace is None:
         workspace = workspace_for(q, k_blocks, query_start_loc, block_tables)
-    if sinks is None and lse is None:
+    if sinks is None and lse is None and k_scale == 1.0 and v_scale == 1.0:
         _check(_lib.pa_varlen_forward(_p(q), _p(k_blocks), _p(v_blocks), _p(out),
                                       _p(query_start_loc), _p(seq_lens), _p(positions),
                                       _p(block_tables), query_start_loc.numel() - 1, T, H, Hkv, D,
@@ -197,8 +214,9 @@ def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, pos
                                      _p(block_tables), query_start_loc.numel() - 1, T, H, Hkv, D,
                                      bs, NB, block_tables.shape[1], _DT[q.dtype],
                                      _DT[k_blocks.dtype], float(scale), int(bool(causal)),
-                                     int(sliding_window), _p(sinks), _p(lse), _p(workspace),
-                                     workspace.numel(), _stream(stream)),
+                                     int(sliding_window), _p(sinks), _p(lse), float(k_scale),
+                                     float(v_scale), _p(workspace), workspace.numel(),
+                                     _stream(stream)),
            "pa_varlen_forward_ex")
     return out
 
@@ -240,10 +258,20 @@ def _split_shapes(q, k_blocks, max_logits, tmp_out):
 
 def pa_decode_splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
                                block_tables, scale, partition_size=512, sliding_window=0,
-                               stream=None):
+                               stream=None, k_scale=1.0, v_scale=1.0):
+    """pa_decode_splitkv_partials, or pa_decode_splitkv_partials_ex when a dequantisation scale
+    other than 1 is given."""
     _dev(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens, block_tables)
     _i32t(seq_lens, block_tables)
     S, H, D, NB, bs, Hkv, P = _split_shapes(q, k_blocks, max_logits, tmp_out)
+    if k_scale != 1.0 or v_scale != 1.0:
+        _check(_lib.pa_decode_splitkv_partials_ex(
+            _p(q), _p(k_blocks), _p(v_blocks), _p(max_logits), _p(exp_sums), _p(tmp_out),
+            _p(seq_lens), _p(block_tables), S, H, Hkv, D, bs, NB, block_tables.shape[1],
+            partition_size, P, _DT[q.dtype], _DT[k_blocks.dtype], float(scale),
+            int(sliding_window), float(k_scale), float(v_scale), _stream(stream)),
+            "pa_decode_splitkv_partials_ex")
+        return
     _check(_lib.pa_decode_splitkv_partials(_p(q), _p(k_blocks), _p(v_blocks), _p(max_logits),
                                            _p(exp_sums), _p(tmp_out), _p(seq_lens),
                                            _p(block_tables), S, H, Hkv, D, bs, NB,

@@ -21,6 +21,23 @@
 // Why warp MMA here: these tiles are HBM-bound (one pass over K and V per kv head), so the
 // tensor core only has to take the ~2 G D FMA per key off the FP32 pipe; with G = 8 the FMA
 // path would need about half the chip's FP32 rate at full HBM bandwidth.
+//
+// fp8 (e4m3) pools, head size 128 ("paged_attention_v2_pytorch.py": kv_cache_dtype "fp8",
+// K = k_scale * pool, V = v_scale * pool).  A tile is 16 rows of 128 one-byte codes, one TMA
+// box of 2 KB with the 128-byte swizzle, so a stage is half the bf16 one and the ring is
+// twice as deep.  The codes stay in shared memory as they arrived; each lane loads the
+// bytes of its own MMA fragments with 16-byte loads and widens them in registers to f16
+// (exact for e4m3), and the products run on the f16 m16n8k16 MMA.  To make every lane's bytes
+// contiguous, both contractions are read in a permuted order, which leaves the sums alone:
+//   S = Q K^T: in k-step kk, fragment column 2c + j (c = lane % 4) is dimension 32c + 4kk + j
+//     and column 2c + 8 + j is dimension 32c + 4kk + 2 + j, so the lane reads bytes
+//     [32c, 32c + 32) of its key row and q is loaded in the same order;
+//   O = P V: output n-tile nt, fragment column n is dimension 16n + nt, so the lane reads
+//     bytes [16g, 16g + 16) (g = lane / 4) of its four key rows, pairs the bytes of rows 2c,
+//     2c + 1 (and 2c + 8, 2c + 9) with byte permutes and widens each pair; the accumulator
+//     columns are put back in order when the warps' states are merged.
+// k_scale is folded into the score scale and v_scale into the final normalisation.  P enters
+// the PV product as one f16 fragment (11 significant bits) instead of the bf16 hi/lo pair.
 #include <algorithm>
 
 #include "pa_internal.cuh"
@@ -31,20 +48,35 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBlk = 16;  // positions per pool block on this path
 
-template <int D>
+template <int D, bool FP8>
 struct Geom {
-  static constexpr int kHalves = D / 64;
-  static constexpr int kHalfBytes = kBlk * 128;            // 16 rows x 64 bf16
+  static_assert(!FP8 || D == 128, "fp8 tiles are one 128-byte-wide box");
+  static constexpr int kHalves = FP8 ? 1 : D / 64;         // TMA boxes per tile
+  static constexpr int kHalfBytes = kBlk * 128;            // 16 rows x 128 bytes
   static constexpr int kTileBytes = kHalves * kHalfBytes;  // one K (or V) block tile
   static constexpr int kStageBytes = 2 * kTileBytes;       // K + V
   static constexpr int kNT = D / 8;                        // n-tiles of the output
   static constexpr int kKS = D / 16;                       // k-steps of QK^T
 };
 
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool FP8>
 constexpr size_t smem_bytes() {
   // ring | full barriers | merge m, l | fail flag, work unit ; the O merge area aliases the ring
-  return 1024 + (size_t)NW * NS * Geom<D>::kStageBytes + NW * NS * 8 + NW * 16 * 4 * 2 + 16;
+  return 1024 + (size_t)NW * NS * Geom<D, FP8>::kStageBytes + NW * NS * 8 + NW * 16 * 4 * 2 + 16;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// bf16x2 -> f16x2 (exact inside f16's normal range)
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  return pack_f16x2(f.x, f.y);
 }
 
 // Byte offset of 16-byte chunk `chunk` (along D) of row `row` inside a tile written by TMA
@@ -55,11 +87,11 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
   return (uint32_t)(half * (kBlk * 128) + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
-template <int D, int NW, int NS, bool SPLIT>
+template <int D, int NW, int NS, bool SPLIT, bool FP8>
 __global__ void __launch_bounds__(NW * 32, 2)
     k_mma16(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
             const Mma16Params p) {
-  using G_ = Geom<D>;
+  using G_ = Geom<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -188,6 +220,14 @@ __global__ void __launch_bounds__(NW * 32, 2)
       const int c = (lane & 3);
 #pragma unroll
       for (int kk = 0; kk < G_::kKS; ++kk) {
+        if constexpr (FP8) {  // f16, dimensions in the permuted order (header comment)
+          const int w = 16 * c + 2 * kk;
+          qa[kk][0] = valid[0] ? bf2_to_h2(q0[w]) : 0u;
+          qa[kk][1] = valid[1] ? bf2_to_h2(q1[w]) : 0u;
+          qa[kk][2] = valid[0] ? bf2_to_h2(q0[w + 1]) : 0u;
+          qa[kk][3] = valid[1] ? bf2_to_h2(q1[w + 1]) : 0u;
+          continue;
+        }
         qa[kk][0] = valid[0] ? q0[kk * 8 + c] : 0u;
         qa[kk][1] = valid[1] ? q1[kk * 8 + c] : 0u;
         qa[kk][2] = valid[0] ? q0[kk * 8 + 4 + c] : 0u;
@@ -220,7 +260,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
         uint8_t* dst = ring + (size_t)(warp * NS + slot) * G_::kStageBytes;
         mbar_arrive_expect_tx(bar, G_::kStageBytes);
 #pragma unroll
-        for (int h = 0; h < G_::kHalves; ++h) {
+        for (int h = 0; h < G_::kHalves; ++h) {  // fp8: one 128-byte box per tile, x = 0
           tma_load_3d(dst + h * G_::kHalfBytes, &tk, h * 64, kvh, id * kBlk, bar);
           tma_load_3d(dst + G_::kTileBytes + h * G_::kHalfBytes, &tv, h * 64, kvh, id * kBlk, bar);
         }
@@ -245,8 +285,8 @@ __global__ void __launch_bounds__(NW * 32, 2)
       const int key_base = lb * kBlk;
 
       // rows of the sequence's last block past seq_len were never written: zero their V so
-      // that 0-weight * garbage cannot turn into NaN
-      if (key_base + kBlk > n) {
+      // that 0-weight * garbage cannot turn into NaN (fp8: in registers, below)
+      if (!FP8 && key_base + kBlk > n) {
         const int first = n - key_base;  // 1..15
         for (int i = lane; i < (kBlk - first) * G_::kHalves * 8; i += 32) {
           const int r = first + i / (G_::kHalves * 8);
@@ -260,7 +300,34 @@ __global__ void __launch_bounds__(NW * 32, 2)
 
       // S = Q K^T for 16 keys: two n-tiles of 8 keys
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
+      if constexpr (FP8) {
+        // key rows lane / 4 and lane / 4 + 8, bytes [32c, 32c + 32): chunks 2c and 2c + 1
+        const uint32_t kbase = smem_u32(kt);
+        const int c = lane & 3;
+        uint4 kw[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int key = (lane >> 2) + nt * 8;
+          kw[nt][0] = lds128(kbase + key * 128 + (((2 * c) ^ (key & 7)) << 4));
+          kw[nt][1] = lds128(kbase + key * 128 + (((2 * c + 1) ^ (key & 7)) << 4));
+        }
+        // two accumulators per n-tile (even / odd k-steps): four dependent chains of four
+        float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < G_::kKS; ++kk)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const uint4& q4 = kw[nt][kk >> 2];
+            const uint32_t w = (kk & 3) == 0 ? q4.x : (kk & 3) == 1 ? q4.y : (kk & 3) == 2 ? q4.z : q4.w;
+            uint32_t b0, b1;
+            e4m3x4_to_f16(w, b0, b1);
+            mma_f16_16816((kk & 1) ? sc2[nt] : sc[nt], qa[kk], b0, b1);
+          }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int c2 = 0; c2 < 4; ++c2) sc[nt][c2] += sc2[nt][c2];
+      } else {
         const int mi = lane >> 3, rr = lane & 7;
         const int key = rr + ((mi >> 1) << 3);
         const uint32_t kbase = smem_u32(kt);
@@ -285,6 +352,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
           sc[nt][c] = vis ? sc[nt][c] * p.scale_log2 : -INFINITY;
         }
       float alpha[2];
+      bool grew = false;  // a row's running max rose: its O needs the rescale (else alpha = 1)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         float mx = fmaxf(fmaxf(sc[0][2 * r], sc[0][2 * r + 1]), fmaxf(sc[1][2 * r], sc[1][2 * r + 1]));
@@ -293,6 +361,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
         const float mn = fmaxf(mrow[r], mx);
         const float base = mn == -INFINITY ? 0.f : mn;
         alpha[r] = exp2f(mrow[r] - base);
+        grew |= mn > mrow[r];
         mrow[r] = mn;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -302,26 +371,64 @@ __global__ void __launch_bounds__(NW * 32, 2)
       }
       // P as two bf16 A fragments, hi = bf16(p) and lo = bf16(p - hi): the PV product of
       // both keeps the weights to ~2^-17 relative, where bf16 P alone can be off by 2^-9 of
-      // |v| when a row sees few keys.
+      // |v| when a row sees few keys.  fp8 pools: one f16 fragment.
       uint32_t ph[4], pl[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float a = sc[i >> 1][(i & 1) * 2], b = sc[i >> 1][(i & 1) * 2 + 1];
+        if constexpr (FP8) {
+          ph[i] = pack_f16x2(a, b);
+          pl[i] = 0u;
+          continue;
+        }
         ph[i] = pack_bf16x2(a, b);
         const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ph[i]));
         pl[i] = pack_bf16x2(a - hv.x, b - hv.y);
       }
       lrow[0] = lrow[0] * alpha[0] + ((sc[0][0] + sc[0][1]) + (sc[1][0] + sc[1][1]));
       lrow[1] = lrow[1] * alpha[1] + ((sc[0][2] + sc[0][3]) + (sc[1][2] + sc[1][3]));
+      if (__any_sync(kFull, grew)) {  // skipped, the factors are exactly 1
 #pragma unroll
-      for (int j = 0; j < G_::kNT; ++j) {
-        o[j][0] *= alpha[0];
-        o[j][1] *= alpha[0];
-        o[j][2] *= alpha[1];
-        o[j][3] *= alpha[1];
+        for (int j = 0; j < G_::kNT; ++j) {
+          o[j][0] *= alpha[0];
+          o[j][1] *= alpha[0];
+          o[j][2] *= alpha[1];
+          o[j][3] *= alpha[1];
+        }
       }
       // O += P V: V is the k-major B operand, read with transposing ldmatrix
-      {
+      if constexpr (FP8) {
+        // key rows 2c, 2c + 1, 2c + 8, 2c + 9, bytes [16g, 16g + 16) of each
+        const uint32_t vbase = smem_u32(vt);
+        const int c = lane & 3, g = lane >> 2;
+        const int lim = n - key_base;  // rows at or past it were never written
+        uint4 vr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 2 * c + (i & 1) + (i >> 1) * 8;
+          vr[i] = lds128(vbase + r * 128 + ((g ^ (r & 7)) << 4));
+          if (r >= lim) vr[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        const uint32_t ra[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w};
+        const uint32_t rb[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
+        const uint32_t rc[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w};
+        const uint32_t rd[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          // byte j of word i is dimension 16g + 4i + j: pair rows (2c, 2c + 1) and
+          // (2c + 8, 2c + 9) byte by byte, lower key in the lower byte
+          const uint32_t lo01 = __byte_perm(ra[i], rb[i], 0x5140);
+          const uint32_t hi01 = __byte_perm(ra[i], rb[i], 0x7362);
+          const uint32_t lo89 = __byte_perm(rc[i], rd[i], 0x5140);
+          const uint32_t hi89 = __byte_perm(rc[i], rd[i], 0x7362);
+          const uint32_t pr01[4] = {lo01 & 0xffffu, lo01 >> 16, hi01 & 0xffffu, hi01 >> 16};
+          const uint32_t pr89[4] = {lo89 & 0xffffu, lo89 >> 16, hi89 & 0xffffu, hi89 >> 16};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            mma_f16_16816(o[4 * i + j], ph, e4m3x2_to_f16x2((uint16_t)pr01[j]),
+                          e4m3x2_to_f16x2((uint16_t)pr89[j]));
+        }
+      } else {
         const int mi = lane >> 3, rr = lane & 7;
         const int key = rr + ((mi & 1) << 3);
         const uint32_t vbase = smem_u32(vt);
@@ -372,11 +479,27 @@ __global__ void __launch_bounds__(NW * 32, 2)
         mrg_l[warp * 16 + r0 + 8] = lrow[1];
       }
       float* ob = mrg_o + (size_t)warp * 16 * kOStride;
+      if constexpr (FP8) {
+        // accumulator column n of n-tile nt is dimension 16n + nt (n = 2c + j)
+        const int c = lane & 3;
 #pragma unroll
-      for (int j = 0; j < G_::kNT; ++j) {
-        const int col = j * 8 + (lane & 3) * 2;
-        *reinterpret_cast<float2*>(ob + r0 * kOStride + col) = make_float2(o[j][0], o[j][1]);
-        *reinterpret_cast<float2*>(ob + (r0 + 8) * kOStride + col) = make_float2(o[j][2], o[j][3]);
+        for (int j = 0; j < G_::kNT; j += 2) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 16 * (2 * c + e) + j;
+            *reinterpret_cast<float2*>(ob + r0 * kOStride + col) = make_float2(o[j][e], o[j + 1][e]);
+            *reinterpret_cast<float2*>(ob + (r0 + 8) * kOStride + col) =
+                make_float2(o[j][2 + e], o[j + 1][2 + e]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < G_::kNT; ++j) {
+          const int col = j * 8 + (lane & 3) * 2;
+          *reinterpret_cast<float2*>(ob + r0 * kOStride + col) = make_float2(o[j][0], o[j][1]);
+          *reinterpret_cast<float2*>(ob + (r0 + 8) * kOStride + col) =
+              make_float2(o[j][2], o[j][3]);
+        }
       }
     }
     __syncthreads();
@@ -414,7 +537,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
           if (p.m.lse && seg == 0)
             p.m.lse[(int64_t)h * p.m.num_tokens + t] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float inv = L > 0.f ? p.m.v_scale / L : 0.f;
         float vals[kSeg];
 #pragma unroll
         for (int d = 0; d < kSeg; ++d) {
@@ -455,15 +578,18 @@ __global__ void __launch_bounds__(NW * 32, 2)
 }
 
 constexpr int kNW = 4;
-constexpr int kNS = 3;
+constexpr int kNS = 3;    // bf16: 8 KB stages (D = 128)
+constexpr int kNS8 = 6;   // fp8: 4 KB stages, twice as many: the same bytes in flight
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool FP8 = false>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p, int grid_x,
                    cudaStream_t stream) {
-  auto kern = k_mma16<D, kNW, kNS, SPLIT>;
-  constexpr size_t smem = smem_bytes<D, kNW, kNS>();
-  static_assert((size_t)kNW * 16 * (D + 4) * 4 <= (size_t)kNW * kNS * Geom<D>::kStageBytes,
+  constexpr int NS = FP8 ? kNS8 : kNS;
+  auto kern = k_mma16<D, kNW, NS, SPLIT, FP8>;
+  constexpr size_t smem = smem_bytes<D, kNW, NS, FP8>();
+  static_assert((size_t)kNW * 16 * (D + 4) * 4 <= (size_t)kNW * NS * Geom<D, FP8>::kStageBytes,
                 "merge area must fit in the ring");
+  static_assert(2 * (smem + 1024) <= 228 * 1024, "two CTAs per SM");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -490,6 +616,22 @@ cudaError_t launch_mma16_varlen(const CUtensorMap& tk, const CUtensorMap& tv, co
   if (head_dim == 128) return launch<128, false>(tk, tv, p, grid_x, stream);
   if (head_dim == 64) return launch<64, false>(tk, tv, p, grid_x, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_mma16_varlen_fp8(const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const Mma16Params& p, int items_cap, cudaStream_t stream) {
+  const int64_t units = (int64_t)items_cap * p.m.num_kv_heads;
+  const int64_t resident = 2 * (int64_t)num_sms();
+  const int grid_x = (int)std::max<int64_t>(1, std::min(units, resident));
+  return launch<128, false, true>(tk, tv, p, grid_x, stream);
+}
+
+cudaError_t launch_mma16_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const Mma16Params& p, cudaStream_t stream) {
+  const int64_t items = (int64_t)p.m.num_seqs * p.max_parts;
+  const int grid_x = items > 65535 ? 65535 : (int)items;
+  if (grid_x <= 0) return cudaSuccess;
+  return launch<128, true, true>(tk, tv, p, grid_x, stream);
 }
 
 cudaError_t launch_mma16_split(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p,

@@ -372,6 +372,69 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Scatter with conversion ("paged_attention_v2_pytorch.py": the pool holds K / k_scale and
+// V / v_scale in kv_cache_dtype).  One warp per token; every element is divided by its scale
+// in fp32 (IEEE division, as written) and rounded to the pool's type to nearest even, fp8
+// saturating to +-448.  CHECKED: every CTA first checks all slots (batches up to
+// kCheckedScatter tokens), otherwise k_validate_slots ran before.
+template <typename TS, int DST, bool CHECKED>
+__global__ void __launch_bounds__(256)
+    k_scatter_convert(const TS* __restrict__ k, const TS* __restrict__ v, void* __restrict__ kb,
+                      void* __restrict__ vb, const int32_t* __restrict__ slots, int64_t num_tokens,
+                      int64_t num_slots, int64_t row_elems, float k_scale, float v_scale,
+                      int* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (status_set(status)) return;  // uniform across the CTA
+  if constexpr (CHECKED) {
+    bool bad = false;
+    for (int64_t t = threadIdx.x; t < num_tokens; t += blockDim.x) {
+      const int32_t sl = slots[t];
+      bad |= (sl < 0 || (int64_t)sl >= num_slots);
+    }
+    if (__syncthreads_or(bad)) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) record_error(status, PA_EINVAL);
+      return;
+    }
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= num_tokens) return;
+  const int64_t dst = (int64_t)slots[t] * row_elems, src = t * row_elems;
+  for (int64_t i = lane; i < row_elems; i += 32) {
+    const float a = __fdiv_rn(to_f32(k[src + i]), k_scale);
+    const float b = __fdiv_rn(to_f32(v[src + i]), v_scale);
+    if constexpr (DST == PA_FP8_E4M3) {
+      static_cast<uint8_t*>(kb)[dst + i] = (uint8_t)(f32x2_to_e4m3x2(a, 0.f) & 0xffu);
+      static_cast<uint8_t*>(vb)[dst + i] = (uint8_t)(f32x2_to_e4m3x2(b, 0.f) & 0xffu);
+    } else if constexpr (DST == PA_BF16) {
+      static_cast<__nv_bfloat16*>(kb)[dst + i] = __float2bfloat16_rn(a);
+      static_cast<__nv_bfloat16*>(vb)[dst + i] = __float2bfloat16_rn(b);
+    } else {
+      static_cast<float*>(kb)[dst + i] = a;
+      static_cast<float*>(vb)[dst + i] = b;
+    }
+  }
+}
+
+template <typename TS, int DST>
+cudaError_t convert_as(const void* k, const void* v, void* kb, void* vb, const int32_t* slots,
+                       int64_t T, int64_t row_elems, int64_t num_slots, float k_scale,
+                       float v_scale, int* status, cudaStream_t stream) {
+  const dim3 grid((unsigned)((T + 7) / 8)), block(256);
+  if (T <= kCheckedScatter)
+    return launch_pdl(k_scatter_convert<TS, DST, true>, grid, block, 0, stream, (const TS*)k,
+                      (const TS*)v, kb, vb, slots, T, num_slots, row_elems, k_scale, v_scale,
+                      status);
+  const int64_t vgrid = std::min<int64_t>((T + 255) / 256, 1024);
+  cudaError_t e = launch_pdl(k_validate_slots, dim3((unsigned)vgrid), dim3(256), 0, stream, slots,
+                             T, num_slots, status);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_scatter_convert<TS, DST, false>, grid, block, 0, stream, (const TS*)k,
+                    (const TS*)v, kb, vb, slots, T, num_slots, row_elems, k_scale, v_scale,
+                    status);
+}
+
 // Gather validation: one CTA per sequence.
 __global__ void k_validate_gather(const int32_t* cu, const int32_t* starts, const int32_t* tables,
                                   int64_t num_rows, int32_t block_size, int64_t num_blocks,
@@ -500,8 +563,40 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_block
       aligned(v_blocks, 4))
     return scatter_as<uint32_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes,
                                 num_slots, status, stream);
-  return scatter_as<uint16_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, num_slots,
-                              status, stream);
+  if (row_bytes % 2 == 0 && aligned(k, 2) && aligned(v, 2) && aligned(k_blocks, 2) &&
+      aligned(v_blocks, 2))
+    return scatter_as<uint16_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes,
+                                num_slots, status, stream);
+  return scatter_as<uint8_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, num_slots,
+                             status, stream);
+}
+
+cudaError_t launch_reshape_and_cache_convert(const void* k, const void* v, void* k_blocks,
+                                             void* v_blocks, const int32_t* slots,
+                                             int64_t num_tokens, int64_t row_elems,
+                                             int32_t block_size, int64_t num_blocks, int src_bf16,
+                                             int dst, float k_scale, float v_scale, int* status,
+                                             cudaStream_t stream) {
+  if (num_tokens <= 0) return cudaSuccess;
+  const int64_t ns = num_blocks * block_size;
+  if (src_bf16) {
+    if (dst == PA_FP8_E4M3)
+      return convert_as<__nv_bfloat16, PA_FP8_E4M3>(k, v, k_blocks, v_blocks, slots, num_tokens,
+                                                    row_elems, ns, k_scale, v_scale, status, stream);
+    if (dst == PA_BF16)
+      return convert_as<__nv_bfloat16, PA_BF16>(k, v, k_blocks, v_blocks, slots, num_tokens,
+                                                row_elems, ns, k_scale, v_scale, status, stream);
+    return convert_as<__nv_bfloat16, PA_F32>(k, v, k_blocks, v_blocks, slots, num_tokens,
+                                             row_elems, ns, k_scale, v_scale, status, stream);
+  }
+  if (dst == PA_FP8_E4M3)
+    return convert_as<float, PA_FP8_E4M3>(k, v, k_blocks, v_blocks, slots, num_tokens, row_elems,
+                                          ns, k_scale, v_scale, status, stream);
+  if (dst == PA_BF16)
+    return convert_as<float, PA_BF16>(k, v, k_blocks, v_blocks, slots, num_tokens, row_elems, ns,
+                                      k_scale, v_scale, status, stream);
+  return convert_as<float, PA_F32>(k, v, k_blocks, v_blocks, slots, num_tokens, row_elems, ns,
+                                   k_scale, v_scale, status, stream);
 }
 
 cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, void* v_out,
@@ -522,8 +617,12 @@ cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k
       aligned(v_out, 4))
     return gather_as<uint32_t>(k_blocks, v_blocks, k_out, v_out, cu, starts, tables, num_seqs,
                                row_bytes, block_size, max_blocks, status, stream);
-  return gather_as<uint16_t>(k_blocks, v_blocks, k_out, v_out, cu, starts, tables, num_seqs,
-                             row_bytes, block_size, max_blocks, status, stream);
+  if (row_bytes % 2 == 0 && aligned(k_blocks, 2) && aligned(v_blocks, 2) && aligned(k_out, 2) &&
+      aligned(v_out, 2))
+    return gather_as<uint16_t>(k_blocks, v_blocks, k_out, v_out, cu, starts, tables, num_seqs,
+                               row_bytes, block_size, max_blocks, status, stream);
+  return gather_as<uint8_t>(k_blocks, v_blocks, k_out, v_out, cu, starts, tables, num_seqs,
+                            row_bytes, block_size, max_blocks, status, stream);
 }
 
 }  // namespace pa

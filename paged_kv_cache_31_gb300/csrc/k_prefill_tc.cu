@@ -652,7 +652,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     }
     if (m.lse && hf == 0 && valid)
       m.lse[(int64_t)h * m.num_tokens + t] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-    const float inv = l > 0.f ? o_scale / l : 0.f;
+    const float inv = l > 0.f ? o_scale * m.v_scale / l : 0.f;
     __nv_bfloat16* dst =
         reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * m.num_heads + h) * kD + col0;
     uint32_t oo[2][32];

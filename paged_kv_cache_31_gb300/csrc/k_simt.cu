@@ -7,7 +7,9 @@
 // when a larger score arrives, and the output is numerator * (1 / denominator).
 //
 // It serves the shapes the tensor-core kernels do not cover (fp32 caches, head sizes other
-// than 64 / 128, block sizes other than 16, GQA groups above 16 in split-KV decode).
+// than 64 / 128, block sizes other than 16, GQA groups above 16 in split-KV decode, fp8
+// pools with fp32 q or head sizes other than 128).  fp8 pools: p.scale carries k_scale and
+// the output is multiplied by v_scale ("paged_attention_v2_pytorch.py", "Apply scales").
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(128) k_simt(const SimtParams p) {
       if (d < D) acc[i] += e * to_f32(vb[base + d]);
     }
   }
-  float inv = den > 0.f ? 1.f / den : 0.f;
+  float inv = den > 0.f ? m.v_scale / den : 0.f;
   if (!p.split) {
     // an attention sink (TensorSharp ForwardWithSinks): one more state with max = the sink
     // logit, exp-sum 1 and weighted sum 0
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(128) k_simt(const SimtParams p) {
       const float a = mx == -INFINITY ? 0.f : expf(mx - m2);
       den = den * a + expf(sk - m2);
       mx = m2;
-      inv = a / den;
+      inv = a * m.v_scale / den;
     }
     if (m.lse && lane == 0) m.lse[(int64_t)h * m.num_tokens + t] = den > 0.f ? mx + logf(den) : -INFINITY;
   }
@@ -146,6 +148,9 @@ cudaError_t launch_dtypes(const SimtParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream) {
+  if (p.kv_fp8)
+    return p.q_bf16 ? launch_dtypes<__nv_bfloat16, e4m3_t>(p, stream)
+                    : launch_dtypes<float, e4m3_t>(p, stream);
   if (p.q_bf16 && p.kv_bf16) return launch_dtypes<__nv_bfloat16, __nv_bfloat16>(p, stream);
   if (p.q_bf16) return launch_dtypes<__nv_bfloat16, float>(p, stream);
   if (p.kv_bf16) return launch_dtypes<float, __nv_bfloat16>(p, stream);

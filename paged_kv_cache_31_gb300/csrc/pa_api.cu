@@ -75,6 +75,23 @@ bool pool_map(CUtensorMap* map, const void* base, int64_t num_blocks, int block_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// TMA descriptor of an fp8 pool [num_blocks, 16, Hkv, 128] (one byte per element) seen as
+// the 3-D byte tensor (128, Hkv, num_blocks * 16): one 128 x 1 x 16 box is a whole K (or V)
+// block tile of one kv head, 2 KB, with the 128-byte swizzle.
+bool pool_map_fp8(CUtensorMap* map, const void* base, int64_t num_blocks, int block_size,
+                  int hkv, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)(num_blocks * block_size)};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)hkv * d};
+  cuuint32_t box[3] = {128, 1, 16};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // TMA descriptor of q [T, H, D] bf16 seen as the 3-D tensor (D, H, T): a 64 x G x 128/G box
 // is the 64-dim half of a 128-row query tile whose rows are the G heads of one kv head for
 // 128/G consecutive tokens.
@@ -102,8 +119,11 @@ bool tc_enabled() {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-bool dtype_ok(pa_dtype t) { return t == PA_F32 || t == PA_BF16; }
-int esize(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+bool dtype_ok(pa_dtype t) { return t == PA_F32 || t == PA_BF16; }  // q, out, new rows
+bool pool_dtype_ok(pa_dtype t) { return dtype_ok(t) || t == PA_FP8_E4M3; }
+int esize(pa_dtype t) { return t == PA_FP8_E4M3 ? 1 : t == PA_BF16 ? 2 : 4; }
+// dequantisation scales: finite and positive
+bool scale_ok(float s) { return s > 0.f && s <= 3.402823466e38f; }
 
 pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ECUDA; }
 
@@ -113,6 +133,14 @@ bool mma_path(pa_dtype q_dtype, pa_dtype kv_dtype, int32_t head_dim, int32_t blo
               const void* q, const void* kb, const void* vb, const void* out) {
   return q_dtype == PA_BF16 && kv_dtype == PA_BF16 && (head_dim == 64 || head_dim == 128) &&
          block_size == 16 && aligned(kb, 16) && aligned(vb, 16) && aligned(q, 4) &&
+         (out == nullptr || aligned(out, 16));
+}
+
+// The same kernel over fp8 pools: bf16 q, head size 128.
+bool mma_path_fp8(pa_dtype q_dtype, pa_dtype kv_dtype, int32_t head_dim, int32_t block_size,
+                  const void* q, const void* kb, const void* vb, const void* out) {
+  return q_dtype == PA_BF16 && kv_dtype == PA_FP8_E4M3 && head_dim == 128 && block_size == 16 &&
+         aligned(kb, 16) && aligned(vb, 16) && aligned(q, 4) &&
          (out == nullptr || aligned(out, 16));
 }
 
@@ -175,7 +203,7 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_blocks, voi
                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                int64_t num_blocks, pa_dtype kv_dtype, cudaStream_t stream) {
   if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return PA_ESHAPE;
-  if (!dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (!pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
   if (num_tokens < 0 || num_blocks < 0) return PA_EINVAL;
   if (num_tokens == 0) return PA_OK;
   if (!k || !v || !k_blocks || !v_blocks || !slot_mapping) return PA_EINVAL;
@@ -184,6 +212,25 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_blocks, voi
   const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * esize(kv_dtype);
   return from_cuda(launch_reshape_and_cache(k, v, k_blocks, v_blocks, slot_mapping, num_tokens,
                                             row_bytes, block_size, num_blocks, d->status, stream));
+}
+
+pa_status pa_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                                  const int32_t* slot_mapping, int64_t num_tokens,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int64_t num_blocks, pa_dtype src_dtype, pa_dtype kv_dtype,
+                                  float k_scale, float v_scale, cudaStream_t stream) {
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return PA_ESHAPE;
+  if (!dtype_ok(src_dtype) || !pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (num_tokens < 0 || num_blocks < 0) return PA_EINVAL;
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_EINVAL;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_blocks || !v_blocks || !slot_mapping) return PA_EINVAL;
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  return from_cuda(launch_reshape_and_cache_convert(
+      k, v, k_blocks, v_blocks, slot_mapping, num_tokens, (int64_t)num_kv_heads * head_dim,
+      block_size, num_blocks, src_dtype == PA_BF16, kv_dtype, k_scale, v_scale, d->status,
+      stream));
 }
 
 size_t pa_varlen_forward_workspace_size(int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
@@ -211,8 +258,8 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
   return pa_varlen_forward_ex(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                               block_tables, num_seqs, num_tokens, num_heads, num_kv_heads,
                               head_dim, block_size, num_blocks, max_blocks_per_seq, q_dtype,
-                              kv_dtype, scale, causal, sliding_window, nullptr, nullptr,
-                              workspace, workspace_bytes, stream);
+                              kv_dtype, scale, causal, sliding_window, nullptr, nullptr, 1.f,
+                              1.f, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* v_blocks,
@@ -223,12 +270,13 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
                                int32_t block_size, int64_t num_blocks,
                                int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
                                float scale, int32_t causal, int32_t sliding_window,
-                               const float* sinks, float* lse, void* workspace,
-                               size_t workspace_bytes, cudaStream_t stream) {
+                               const float* sinks, float* lse, float k_scale, float v_scale,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0)
     return PA_ESHAPE;
-  if (!dtype_ok(q_dtype) || !dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (!dtype_ok(q_dtype) || !pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_EINVAL;
   if (head_dim > 256) return PA_EUNSUPPORTED;
   if (num_seqs < 0 || num_tokens < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return PA_EINVAL;
   if (num_tokens > INT32_MAX / 2) return PA_EUNSUPPORTED;
@@ -261,6 +309,8 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
   m.window = sliding_window > 0 ? sliding_window : 0;
   m.sinks = sinks;
   m.lse = lse;
+  m.v_scale = v_scale;
+  scale *= k_scale;  // K = k_scale * pool: the scores take it with the softmax scale
   int32_t* plan = static_cast<int32_t*>(workspace);
   PlanLayout L = plan_layout(num_seqs, num_tokens, m.group);
   const bool fast = mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
@@ -275,6 +325,25 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
   cudaError_t e = launch_plan_varlen(m, plan, L, d->status, stream);
   if (e != cudaSuccess) return PA_ECUDA;
 
+  if (mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out)) {
+    // fp8 pools: every sequence on the warp-MMA kernel (the plan had use_tc off)
+    CUtensorMap tk, tv;
+    if (!pool_map_fp8(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) ||
+        !pool_map_fp8(&tv, v_blocks, num_blocks, block_size, num_kv_heads, head_dim))
+      return PA_ECUDA;
+    Mma16Params p;
+    std::memset(&p, 0, sizeof p);
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.out = out;
+    p.m = m;
+    p.plan = plan;
+    p.items_off = L.mma_off;
+    p.status = d->status;
+    p.scale_log2 = scale * kLog2e;
+    p.wait_limit_ns = kWaitLimitNs;
+    return from_cuda(
+        launch_mma16_varlen_fp8(tk, tv, p, (int)std::min<int64_t>(L.mma_cap, 65535), stream));
+  }
   if (fast) {
     CUtensorMap tk, tv;
     if (!pool_map(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) ||
@@ -323,6 +392,7 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
   p.scale = scale;
   p.q_bf16 = q_dtype == PA_BF16;
   p.kv_bf16 = kv_dtype == PA_BF16;
+  p.kv_fp8 = kv_dtype == PA_FP8_E4M3;
   return from_cuda(launch_simt(p, stream));
 }
 
@@ -333,11 +403,14 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
                                   int32_t head_dim, int32_t block_size, int64_t num_blocks,
                                   int32_t max_blocks_per_seq, int32_t partition_size,
                                   int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype,
-                                  float scale, int32_t sliding_window, cudaStream_t stream) {
+                                  float scale, int32_t sliding_window, float k_scale,
+                                  float v_scale, cudaStream_t stream) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0 || partition_size <= 0 || max_num_partitions <= 0)
     return PA_ESHAPE;
-  if (!dtype_ok(q_dtype) || !dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (!dtype_ok(q_dtype) || !pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_EINVAL;
+  scale *= k_scale;
   if (head_dim > 256 || partition_size % block_size != 0) return PA_EUNSUPPORTED;
   if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return PA_EINVAL;
   if (num_seqs == 0) return PA_OK;
@@ -365,12 +438,18 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
   m.max_blocks = max_blocks_per_seq;
   m.causal = 1;
   m.window = sliding_window > 0 ? sliding_window : 0;
-  if (mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, nullptr) &&
+  m.v_scale = v_scale;
+  const bool fp8 =
+      mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, nullptr);
+  if ((fp8 || mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, nullptr)) &&
       m.group <= 16 && aligned(tmp_out, 16)) {
     CUtensorMap tk, tv;
-    if (!pool_map(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) ||
-        !pool_map(&tv, v_blocks, num_blocks, block_size, num_kv_heads, head_dim))
-      return PA_ECUDA;
+    const bool ok =
+        fp8 ? pool_map_fp8(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) &&
+                  pool_map_fp8(&tv, v_blocks, num_blocks, block_size, num_kv_heads, head_dim)
+            : pool_map(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) &&
+                  pool_map(&tv, v_blocks, num_blocks, block_size, num_kv_heads, head_dim);
+    if (!ok) return PA_ECUDA;
     Mma16Params p;
     std::memset(&p, 0, sizeof p);
     p.q = static_cast<const __nv_bfloat16*>(q);
@@ -383,7 +462,8 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
     p.partition_size = partition_size;
     p.max_parts = max_num_partitions;
     p.wait_limit_ns = kWaitLimitNs;
-    return from_cuda(launch_mma16_split(tk, tv, p, head_dim, stream));
+    return from_cuda(fp8 ? launch_mma16_split_fp8(tk, tv, p, stream)
+                         : launch_mma16_split(tk, tv, p, head_dim, stream));
   }
   SimtParams p;
   std::memset(&p, 0, sizeof p);
@@ -395,6 +475,7 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
   p.scale = scale;
   p.q_bf16 = q_dtype == PA_BF16;
   p.kv_bf16 = kv_dtype == PA_BF16;
+  p.kv_fp8 = kv_dtype == PA_FP8_E4M3;
   p.max_logits = max_logits;
   p.exp_sums = exp_sums;
   p.tmp_out = tmp_out;
@@ -441,7 +522,20 @@ pa_status pa_decode_splitkv_partials(const void* q, const void* k_blocks, const 
   return splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
                           block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                           num_blocks, max_blocks_per_seq, partition_size, max_num_partitions,
-                          q_dtype, kv_dtype, scale, sliding_window, stream);
+                          q_dtype, kv_dtype, scale, sliding_window, 1.f, 1.f, stream);
+}
+
+pa_status pa_decode_splitkv_partials_ex(
+    const void* q, const void* k_blocks, const void* v_blocks, float* max_logits,
+    float* exp_sums, float* tmp_out, const int32_t* seq_lens, const int32_t* block_tables,
+    int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int32_t partition_size,
+    int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
+    int32_t sliding_window, float k_scale, float v_scale, cudaStream_t stream) {
+  return splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
+                          block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, partition_size, max_num_partitions,
+                          q_dtype, kv_dtype, scale, sliding_window, k_scale, v_scale, stream);
 }
 
 pa_status pa_decode_splitkv_reduce(void* out, const float* max_logits, const float* exp_sums,
@@ -468,7 +562,7 @@ pa_status pa_decode_splitkv(const void* q, const void* k_blocks, const void* v_b
                                   block_tables, num_seqs, num_heads, num_kv_heads, head_dim,
                                   block_size, num_blocks, max_blocks_per_seq, partition_size,
                                   max_num_partitions, q_dtype, kv_dtype, scale, sliding_window,
-                                  stream);
+                                  1.f, 1.f, stream);
   if (st != PA_OK) return st;
   return splitkv_reduce(out, max_logits, exp_sums, tmp_out, seq_lens, num_seqs, num_heads,
                         head_dim, partition_size, max_num_partitions, q_dtype, false, stream);
@@ -500,7 +594,7 @@ pa_status pa_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, 
                        int64_t num_blocks, int32_t max_blocks_per_seq, pa_dtype kv_dtype,
                        cudaStream_t stream) {
   if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return PA_ESHAPE;
-  if (!dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (!pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
   if (num_seqs < 0 || num_out_rows < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
     return PA_EINVAL;
   if (num_seqs == 0) return PA_OK;

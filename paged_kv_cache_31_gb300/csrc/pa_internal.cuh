@@ -7,6 +7,7 @@
 
 #include <cuda.h>  // CUtensorMap (type only; the driver is reached through cudaGetDriverEntryPoint)
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -164,6 +165,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// The same MMA with f16 operands (the fp8 pools' path: e4m3 widens to f16 exactly).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32"
+      " {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two e4m3 codes (the low byte is the element at the lower address) -> f16x2, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+  return r;
+}
+// Four codes of a 32-bit word -> two f16x2 words, in element order.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3x2_to_f16x2((uint16_t)(w & 0xffffu));
+  hi = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+}
+// Two floats -> two e4m3 codes (saturating to +-448, round to nearest even), a at the lower
+// address.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
 // ------------------------------------------------------------------------------------------
 // element access for the generic kernels
 
@@ -176,6 +211,16 @@ __device__ __forceinline__ float to_f32<float>(float x) {
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
   return __bfloat162float(x);
+}
+
+// An e4m3 pool element (the code; its value widens exactly through f16).
+struct e4m3_t {
+  uint8_t bits;
+};
+template <>
+__device__ __forceinline__ float to_f32<e4m3_t>(e4m3_t x) {
+  const uint32_t h = e4m3x2_to_f16x2((uint16_t)x.bits);
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
 }
 
 template <typename T>
@@ -248,6 +293,7 @@ struct VarlenMeta {
   int32_t window;
   const float* sinks;  // [num_heads] sink logits on the score scale, or null (varlen only)
   float* lse;          // [num_heads, num_tokens] natural-log lse out, or null (varlen only)
+  float v_scale;       // V = v_scale * pool: applied to the normalised output (1 = none)
 };
 
 struct Mma16Params {
@@ -275,8 +321,8 @@ struct SimtParams {
   VarlenMeta m;
   const int32_t* plan;  // token -> seq at plan + kPlanHeaderWords
   int* status;
-  float scale;
-  int32_t q_bf16, kv_bf16;
+  float scale;  // includes k_scale
+  int32_t q_bf16, kv_bf16, kv_fp8;
   // split-KV mode (out unused): one warp per (s, h, p)
   float* max_logits;
   float* exp_sums;
@@ -313,6 +359,15 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_block
                                      const int32_t* slots, int64_t num_tokens, int64_t row_bytes,
                                      int32_t block_size, int64_t num_blocks, int* status,
                                      cudaStream_t stream);
+// Scatter with conversion: element x of K (V) is stored as x / k_scale (x / v_scale), the
+// quotient rounded to the pool's type.  src_bf16: new rows are bf16 (else f32); dst: the
+// pool's pa_dtype.  row_elems = num_kv_heads * head_dim.
+cudaError_t launch_reshape_and_cache_convert(const void* k, const void* v, void* k_blocks,
+                                             void* v_blocks, const int32_t* slots,
+                                             int64_t num_tokens, int64_t row_elems,
+                                             int32_t block_size, int64_t num_blocks, int src_bf16,
+                                             int dst, float k_scale, float v_scale, int* status,
+                                             cudaStream_t stream);
 cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, void* v_out,
                              const int32_t* cu, const int32_t* starts, const int32_t* tables,
                              int32_t num_seqs, int64_t num_rows, int64_t row_bytes,
@@ -320,6 +375,11 @@ cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k
                              int* status, cudaStream_t stream);
 cudaError_t launch_mma16_varlen(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p,
                                 int head_dim, int items_cap, cudaStream_t stream);
+// The same kernel over e4m3 pools (head size 128; tk / tv are byte maps, box 128 x 1 x 16).
+cudaError_t launch_mma16_varlen_fp8(const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const Mma16Params& p, int items_cap, cudaStream_t stream);
+cudaError_t launch_mma16_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const Mma16Params& p, cudaStream_t stream);
 cudaError_t launch_mma16_split(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p,
                                int head_dim, cudaStream_t stream);
 cudaError_t launch_simt(const SimtParams& p, cudaStream_t stream);

@@ -21,7 +21,7 @@ from typing import List, Optional
 
 import torch
 
-__all__ = ["Workload", "build", "named", "subset", "NAMES"]
+__all__ = ["Workload", "build", "named", "subset", "fp8_pools", "NAMES"]
 
 
 @dataclasses.dataclass
@@ -155,6 +155,20 @@ def build(name: str, seq_lens: List[int], q_lens: List[int], num_heads: int, num
         block_tables=tables.to(device), q=q, k_new=k_new, v_new=v_new,
         k_blocks=k_blocks, v_blocks=v_blocks, partition_size=partition_size,
         masked_partition=masked_partition, shared_prefix_blocks=shared_prefix_blocks, seed=seed)
+
+
+def fp8_pools(w: Workload, spread: float = 8.0, seed: Optional[int] = None):
+    """e4m3 K and V pools of w's shape: i.i.d. N(0, spread^2) values drawn in fp32 (seeded) and
+    cast with torch's float8_e4m3fn conversion, so the codes span the format's normal range and
+    some subnormals.  With k_scale = v_scale = 1 / spread the dequantised pools are about
+    N(0, 1), like the bf16 pools.  Only draws inputs: the attention over them is what is
+    tested."""
+    dev = w.k_blocks.device
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 7 if seed is None else seed)
+    shape = tuple(w.k_blocks.shape)
+    kb = (torch.randn(shape, generator=gen, device=dev) * spread).to(torch.float8_e4m3fn)
+    vb = (torch.randn(shape, generator=gen, device=dev) * spread).to(torch.float8_e4m3fn)
+    return kb, vb
 
 
 def subset(w: Workload, seqs: List[int], name: Optional[str] = None) -> Workload:
