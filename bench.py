@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode KV GB/s (% HBM peak); mixed-batch prefill TFLOP/s; tokens/s"
 KERNEL_SOURCES = {"k_mma16": "paged_kv_cache_31_gb300/csrc/k_decode_mma.cu",
+                  "k_mma16_fp8": "paged_kv_cache_31_gb300/csrc/k_decode_mma.cu",
                   "k_tc_prefill": "paged_kv_cache_31_gb300/csrc/k_prefill_tc.cu"}
 
 
@@ -50,9 +51,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--secondary-steps", type=int, default=30)
-    ap.add_argument("--case", default="bench", choices=["bench", "prefill-chunks"],
+    ap.add_argument("--case", default="bench", choices=["bench", "prefill-chunks", "decode-fp8"],
                     help="prefill-chunks: time only the attention call on the mixed batch's "
-                         "prefill chunks (own pool; a small case for profiling)")
+                         "prefill chunks (own pool; a small case for profiling); decode-fp8: "
+                         "time only the attention call on the decode batch over fp8 pools")
     return ap.parse_args()
 
 
@@ -340,6 +342,35 @@ def l2_flush_buffer(dev):
             torch.zeros(64 << 20, dtype=torch.float32, device=dev))
 
 
+def fp8_decode(pa, dev, args, peaks, stream, n):
+    """The decode batch over fp8 (e4m3) pools with dequantisation scales: half the K/V bytes
+    of the bf16 batch, 303 MB of codes (larger than L2, so no flush)."""
+    import torch
+
+    from paged_kv_cache_31_gb300 import workloads
+
+    w2 = workloads.named(2, seed=args.seed, device=dev)
+    kb8, vb8 = workloads.fp8_pools(w2)
+    out2 = torch.empty_like(w2.q)
+    ws2 = pa.workspace_for(w2.q, kb8, w2.query_start_loc, w2.block_tables)
+
+    def call():
+        pa.pa_varlen_forward(w2.q, kb8, vb8, out2, w2.query_start_loc, w2.seq_lens,
+                             w2.positions, w2.block_tables, w2.scale, workspace=ws2,
+                             k_scale=0.125, v_scale=0.125)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    ms = time_calls(call, n, stream)
+    assert pa.pa_device_status() == pa.PA_OK
+    kv = kv_bytes(w2, elem_bytes=1)
+    name = w2.name + "-fp8"
+    return {"workload": name, "kv_bytes": kv, "ms": ms, "gbs": kv / (ms * 1e-3) / 1e9,
+            "frac_of_hbm": kv / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "l2": "inputs (pools of ~300 MB) larger than L2",
+            "traffic": ncu_traffic("k_mma16_fp8", name)}
+
+
 def secondary(pa, dev, args, peaks, stream):
     """Per-class measurements of the mixed batch (prefill chunks alone: TFLOP/s of the
     tcgen05 path; decode tokens alone: K/V GB/s), the long-context split-KV batch and the
@@ -384,27 +415,7 @@ def secondary(pa, dev, args, peaks, stream):
     del w3, r3, wp, wd, rp, rd
     torch.cuda.empty_cache()
 
-    # the decode batch over fp8 (e4m3) pools with dequantisation scales: half the K/V bytes
-    w2 = workloads.named(2, seed=args.seed, device=dev)
-    kb8, vb8 = workloads.fp8_pools(w2)
-    out2 = torch.empty_like(w2.q)
-    ws2 = pa.workspace_for(w2.q, kb8, w2.query_start_loc, w2.block_tables)
-
-    def fp8_call():
-        pa.pa_varlen_forward(w2.q, kb8, vb8, out2, w2.query_start_loc, w2.seq_lens,
-                             w2.positions, w2.block_tables, w2.scale, workspace=ws2,
-                             k_scale=0.125, v_scale=0.125)
-
-    for _ in range(3):
-        fp8_call()
-    ms8 = time_calls(fp8_call, n, stream)
-    kv8 = kv_bytes(w2, elem_bytes=1)
-    res["fp8_decode"] = {"workload": w2.name + "-fp8", "kv_bytes": kv8, "ms": ms8,
-                         "gbs": kv8 / (ms8 * 1e-3) / 1e9,
-                         "frac_of_hbm": kv8 / (ms8 * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                         "l2": "inputs (pools of ~300 MB) larger than L2"}
-    assert pa.pa_device_status() == pa.PA_OK
-    del w2, kb8, vb8, out2, ws2
+    res["fp8_decode"] = fp8_decode(pa, dev, args, peaks, stream, n)
     torch.cuda.empty_cache()
 
     w4 = workloads.named(4, seed=args.seed, device=dev)
@@ -457,6 +468,11 @@ def main():
     from paged_kv_cache_31_gb300 import binding as pa
 
     peaks = measured_peaks()
+    if args.case == "decode-fp8":
+        print(json.dumps(dict(case="decode-fp8", **fp8_decode(pa, dev, args, peaks,
+                                                               torch.cuda.current_stream(),
+                                                               args.steps))), flush=True)
+        return
     if args.case == "prefill-chunks":
         wp = workloads.prefill_chunks(seed=args.seed, device=dev)
         rp = Runner(pa, wp)
