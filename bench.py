@@ -262,10 +262,10 @@ def run_reference(args, w):
 class Runner:
     """Device buffers of one workload and the library calls of its step."""
 
-    def __init__(self, pa, w):
+    def __init__(self, pa, w, bitwise=False):
         import torch
 
-        self.pa, self.w = pa, w
+        self.pa, self.w, self.bitwise = pa, w, bitwise
         self.varlen = not w.partition_size
         self.out = torch.empty_like(w.q)
         self.slots = torch.empty(w.num_tokens, dtype=torch.int32, device=w.q.device)
@@ -294,7 +294,8 @@ class Runner:
                                  m.get("query_start_loc", w.query_start_loc),
                                  m.get("seq_lens", w.seq_lens), m.get("positions", w.positions),
                                  m.get("block_tables", w.block_tables), w.scale, causal=w.causal,
-                                 sliding_window=w.sliding_window, workspace=self.ws)
+                                 sliding_window=w.sliding_window, workspace=self.ws,
+                                 bitwise=self.bitwise)
         else:
             pa.pa_decode_splitkv(q, w.k_blocks, w.v_blocks, self.out, self.ml, self.es, self.to,
                                  m.get("seq_lens", w.seq_lens),
@@ -395,6 +396,11 @@ def secondary(pa, dev, args, peaks, stream):
         rd.attention()
     flush = l2_flush_buffer(dev)
     p_ms = time_calls(rp.attention, n, stream, flush=flush)  # its K/V would fit in L2
+    # the same chunks with PA_FLAG_BITWISE (warp-MMA kernel: decode and prefill agree bitwise)
+    rb = Runner(pa, wp, bitwise=True)
+    for _ in range(3):
+        rb.attention()
+    b_ms = time_calls(rb.attention, n, stream, flush=flush)
     d_ms = time_calls(rd.attention, n, stream)
     del flush
     fl, kvd = attn_flops(wp), kv_bytes(wd)
@@ -406,13 +412,15 @@ def secondary(pa, dev, args, peaks, stream):
                     "frac_of_bf16_peak": fl / (p_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                     "l2": "flushed between calls",
                     "bound": "tensor", "peak_tflops": peaks["bf16_tflops"],
-                    "traffic": ncu_traffic("k_tc_prefill", wp.name)},
+                    "traffic": ncu_traffic("k_tc_prefill", wp.name),
+                    "bitwise_flag": {"ms": b_ms, "tflops": fl / (b_ms * 1e-3) / 1e12,
+                                     "kernel": "warp-MMA (PA_FLAG_BITWISE)"}},
         "decode": {"tokens": wd.num_tokens, "kv_bytes": kvd, "ms": d_ms,
                    "gbs": kvd / (d_ms * 1e-3) / 1e9,
                    "frac_of_hbm": kvd / (d_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
     }
     assert pa.pa_device_status() == pa.PA_OK
-    del w3, r3, wp, wd, rp, rd
+    del w3, r3, wp, wd, rp, rd, rb
     torch.cuda.empty_cache()
 
     res["fp8_decode"] = fp8_decode(pa, dev, args, peaks, stream, n)

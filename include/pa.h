@@ -60,6 +60,9 @@ typedef enum {
  * bf16. */
 typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
+/* Flags of pa_varlen_forward_ex. */
+enum { PA_FLAG_BITWISE = 1u };
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int pa_version(void);
 
@@ -173,6 +176,17 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
  *          below 2^-14 keep f16's subnormal precision), and the softmax weights enter the PV
  *          product as f16 (2^-11 relative).  fp8 pools take the warp-MMA kernel for head size
  *          128 with 16-position blocks and the generic kernel otherwise.
+ *   flags  0, or PA_FLAG_BITWISE: every sequence runs on the 16-row warp-MMA kernel (bf16 or
+ *          fp8 pools, head size 64 / 128, 16-position blocks), including prefill-class
+ *          sequences that would otherwise take the tensor-core prefill kernel.  That kernel
+ *          folds each query row over the same 16-position blocks, in the same order and
+ *          grouping, whatever the other rows of the batch are, so a token's out row and lse
+ *          have the same bits computed as a decode token (q_len 1) or inside a prefill chunk,
+ *          alone or in any batch (tinyllm 2.4: decode equals FlashAttention bit for bit, so
+ *          prefill with one kernel and decode with the other agree).  Without the flag this
+ *          holds for every sequence of at most 64 query rows per kv head; longer ones take
+ *          the tcgen05 kernel, whose 128-key tiles group the sums differently (results within
+ *          the tolerance, not bitwise).  Other bits: PA_EINVAL.
  * sinks and lse are read or written only for tokens of sequences with query tokens, and lse
  * is left untouched on a validation failure, like out.
  */
@@ -185,7 +199,8 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
                                int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
                                float scale, int32_t causal, int32_t sliding_window,
                                const float* sinks, float* lse, float k_scale, float v_scale,
-                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                               uint32_t flags, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
 
 /*
  * pa_varlen_forward_noalloc -- pa_varlen_forward for callers that cannot allocate device

@@ -24,6 +24,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 PA_OK, PA_EINVAL, PA_ESHAPE, PA_EUNSUPPORTED, PA_ECUDA, PA_ETIMEOUT = range(6)
 PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
+PA_FLAG_BITWISE = 1
 _DT = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float8_e4m3fn: PA_FP8_E4M3}
 
 _vp, _i32, _i64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
@@ -43,7 +44,8 @@ _SIGS = {
                            _sz, _vp], ctypes.c_int),
     "pa_varlen_forward_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
                               _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32,
-                              _i32, _vp, _vp, _f32, _f32, _vp, _sz, _vp], ctypes.c_int),
+                              _i32, _vp, _vp, _f32, _f32, ctypes.c_uint32, _vp, _sz, _vp],
+                             ctypes.c_int),
     "pa_varlen_forward_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
                                    _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32,
                                    _i32, _vp], ctypes.c_int),
@@ -177,9 +179,11 @@ def workspace_for(q, k_blocks, query_start_loc, block_tables):
 
 def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                       block_tables, scale, causal=True, sliding_window=0, workspace=None,
-                      stream=None, sinks=None, lse=None, k_scale=1.0, v_scale=1.0):
+                      stream=None, sinks=None, lse=None, k_scale=1.0, v_scale=1.0,
+                      bitwise=False):
     """pa_varlen_forward, or pa_varlen_forward_ex when sinks ([H] fp32 sink logits), lse
-    (a [H, T] fp32 output) or a dequantisation scale other than 1 is given."""
+    (a [H, T] fp32 output), a dequantisation scale other than 1 or bitwise=True
+    (PA_FLAG_BITWISE: decode and prefill rows give the same bits) is given."""
     _dev(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions, block_tables, workspace,
          sinks, lse)
     _i32t(query_start_loc, seq_lens, positions, block_tables)
@@ -193,7 +197,7 @@ def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, pos
         raise ValueError("head size differs between q and the pool")
     if workspace is None:
         workspace = workspace_for(q, k_blocks, query_start_loc, block_tables)
-    if sinks is None and lse is None and k_scale == 1.0 and v_scale == 1.0:
+    if sinks is None and lse is None and k_scale == 1.0 and v_scale == 1.0 and not bitwise:
         _check(_lib.pa_varlen_forward(_p(q), _p(k_blocks), _p(v_blocks), _p(out),
                                       _p(query_start_loc), _p(seq_lens), _p(positions),
                                       _p(block_tables), query_start_loc.numel() - 1, T, H, Hkv, D,
@@ -215,8 +219,8 @@ def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, pos
                                      bs, NB, block_tables.shape[1], _DT[q.dtype],
                                      _DT[k_blocks.dtype], float(scale), int(bool(causal)),
                                      int(sliding_window), _p(sinks), _p(lse), float(k_scale),
-                                     float(v_scale), _p(workspace), workspace.numel(),
-                                     _stream(stream)),
+                                     float(v_scale), PA_FLAG_BITWISE if bitwise else 0,
+                                     _p(workspace), workspace.numel(), _stream(stream)),
            "pa_varlen_forward_ex")
     return out
 

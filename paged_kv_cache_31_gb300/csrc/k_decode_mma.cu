@@ -207,7 +207,12 @@ __global__ void __launch_bounds__(NW * 32, 2)
     }
     const int blk_lo = lo < hi ? lo / kBlk : 0;
     const int nblk = lo < hi ? (hi + kBlk - 1) / kBlk - blk_lo : 0;
-    const int my_count = nblk > warp ? (nblk - warp + NW - 1) / NW : 0;
+    // warp w takes the blocks whose absolute index is w mod NW, so a row's arithmetic (which
+    // blocks each warp folds, in which order, and the fixed-order merge of the warps) does
+    // not depend on the other rows of its tile: a token gets the same bits as a decode token,
+    // inside a prefill chunk, alone or in any batch.  Blocks a row cannot see add exact zeros.
+    const int first = ((warp - blk_lo) % NW + NW) % NW;  // this warp's first block, relative
+    const int my_count = nblk > first ? (nblk - first + NW - 1) / NW : 0;
     const int32_t* table_row = m.block_tables + (int64_t)s * m.max_blocks;
 
     // ---------------------------------------------------------------- q fragments
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
       const int win = x >> 5;
       if (win != tbl_win) {
         tbl_win = win;
-        const int lb = warp + (win * 32 + lane) * NW;
+        const int lb = first + (win * 32 + lane) * NW;
         tbl_val = lb < nblk ? table_row[blk_lo + lb] : 0;
       }
       return __shfl_sync(kFull, tbl_val, x & 31);
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
       }
       uint8_t* kt = ring + (size_t)(warp * NS + slot) * G_::kStageBytes;
       uint8_t* vt = kt + G_::kTileBytes;
-      const int lb = blk_lo + warp + x * NW;
+      const int lb = blk_lo + first + x * NW;
       const int key_base = lb * kBlk;
 
       // rows of the sequence's last block past seq_len were never written: zero their V so

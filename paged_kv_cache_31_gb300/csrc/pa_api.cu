@@ -259,7 +259,7 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
                               block_tables, num_seqs, num_tokens, num_heads, num_kv_heads,
                               head_dim, block_size, num_blocks, max_blocks_per_seq, q_dtype,
                               kv_dtype, scale, causal, sliding_window, nullptr, nullptr, 1.f,
-                              1.f, workspace, workspace_bytes, stream);
+                              1.f, 0u, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* v_blocks,
@@ -271,12 +271,14 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
                                int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
                                float scale, int32_t causal, int32_t sliding_window,
                                const float* sinks, float* lse, float k_scale, float v_scale,
-                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                               uint32_t flags, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0)
     return PA_ESHAPE;
   if (!dtype_ok(q_dtype) || !pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
   if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_EINVAL;
+  if (flags & ~(uint32_t)PA_FLAG_BITWISE) return PA_EINVAL;
   if (head_dim > 256) return PA_EUNSUPPORTED;
   if (num_seqs < 0 || num_tokens < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return PA_EINVAL;
   if (num_tokens > INT32_MAX / 2) return PA_EUNSUPPORTED;
@@ -320,7 +322,8 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
   // many rows fit the warp-MMA path, the tcgen05 kernel is not launched at all.
   const int64_t max_rows = (num_tokens - (num_seqs > 0 ? num_seqs : 1) + 1) * m.group;
   L.use_tc = fast && head_dim == 128 && m.group <= 128 && (128 % m.group) == 0 &&
-             aligned(q, 16) && max_rows > L.tc_min_rows && scale > 0.f && tc_enabled();
+             aligned(q, 16) && max_rows > L.tc_min_rows && scale > 0.f && tc_enabled() &&
+             !(flags & PA_FLAG_BITWISE);
 
   cudaError_t e = launch_plan_varlen(m, plan, L, d->status, stream);
   if (e != cudaSuccess) return PA_ECUDA;
