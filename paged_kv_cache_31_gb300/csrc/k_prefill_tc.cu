@@ -7,20 +7,26 @@
 // puts it (two 64-dim boxes of 16 rows per block, 128-byte swizzle); a block past the
 // visible range is fetched at a negative row coordinate, which TMA fills with zeros.
 //
-// Work items are 256-row pairs of such tiles, run by a cluster of two CTAs on two SMs: each
-// CTA computes one tile, and each fetches half of every K / V tile (alternate blocks) with TMA
-// multicast into both CTAs' shared memory, so a CTA issues 16 boxes per key tile instead of 32;
-// a stage is refilled only after both CTAs' MMAs released it.
+// Work items are 256-row pairs of such tiles, run by a cluster of two CTAs on two SMs with the
+// pair's 2-SM MMAs (tcgen05 cta_group::2, M = 256): CTA r holds query rows 128r .. 128r + 127,
+// its own S, P and O in its tensor memory, and only its part of every K / V tile: keys
+// 64r .. 64r + 63 of K (all 128 dims) and dims 64r .. 64r + 63 of V (all 128 keys), 16 KB each.
+// The MMA splits A by rows and B by columns across the pair, so each SM's shared memory is
+// filled with half of every K / V tile -- the fill rate of shared memory, not the tensor core,
+// is what bounds this kernel.  CTA 0 (the leader) issues every MMA; its barriers also count
+// the peer's arrivals (the peer's idle issuer warps forward "my part of this stage has landed"
+// with remote mbarrier arrives), and the MMA completions are multicast to both CTAs.
 //
 // One CTA per SM, persistent over items, 12 warps:
 //   warp 0      TMA producer of Q (two buffers, so the next item's Q loads while this one
-//               finishes) and K_j through a 2-stage ring; warp 10 produces V_j through a
-//               3-stage ring;
-//   warp 1      TMEM owner and QK^T issuer; warp 11 issues PV (it also zeroes the
-//               never-written V rows past a sequence's end).  Lane 0 issues, in warp-uniform
-//               code:
-//                 S_j = Q K_j^T      (M 128, N 128, K 128: 8 MMAs, K-major operands)
+//               finishes) and of this CTA's part of K_j through a 4-stage ring; warp 10
+//               produces its part of V_j through a 5-stage ring;
+//   warp 1      TMEM owner and QK^T issuer; warp 11 issues PV and zeroes the never-written
+//               V rows past a sequence's end in this CTA's part.  In the leader lane 0 issues,
+//               in warp-uniform code:
+//                 S_j = Q K_j^T      (M 256, N 128, K 128: 8 MMAs, K-major operands)
 //                 O  += P_j V_j      (P as a bf16 hi/lo pair read from TMEM: 16 MMAs, V MN-major)
+//               In the peer the two warps forward the Q / K and V arrivals to the leader.
 //               TMEM columns: three S buffers at 0 / 128 / 384, O at 256.  P_j is written over
 //               the S_j it came from, so S_{j+3} may only be issued once P_j V_j is done;
 //   warps 2..9  softmax: two threads per query row (TMEM lane = row), one per 64-column
@@ -44,16 +50,18 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per tile (8 blocks of 16)
 constexpr int kD = 128;           // head size on this path
-constexpr int kHalf = 16384;      // one 64-dim half of a 128-row bf16 tile
-constexpr int kTile = 2 * kHalf;  // 128 x 128 bf16
+constexpr int kHalf = 16384;      // one 64-dim half of a 128-row bf16 Q tile
+constexpr int kTile = 2 * kHalf;  // 128 x 128 bf16 (this CTA's Q rows)
+constexpr int kKVHalf = 8192;     // K part: one 64-dim half of this CTA's 64 keys
+constexpr int kPart = 16384;      // this CTA's part of a K (or V) tile
 constexpr int kSBufs = 3;    // S / P buffers in tensor memory (columns 0, 128 and 384)
-constexpr int kStagesK = 2;  // K ring (a K tile is released as soon as its S MMAs finish)
-constexpr int kStagesV = 3;  // V ring (held until P V, so it needs one more stage in flight)
+constexpr int kStagesK = 4;  // K ring (a K tile is released as soon as its S MMAs finish)
+constexpr int kStagesV = 5;  // V ring (held until P V, so it needs more stages in flight)
 constexpr int kOffQ = 0;                          // two Q buffers (consecutive items)
 constexpr int kOffK = kOffQ + 2 * kTile;
-constexpr int kOffV = kOffK + kStagesK * kTile;
-constexpr int kOffBar = kOffV + kStagesV * kTile;
-constexpr int kNumBarsMax = 26;
+constexpr int kOffV = kOffK + kStagesK * kPart;
+constexpr int kOffBar = kOffV + kStagesV * kPart;
+constexpr int kNumBarsMax = 40;
 constexpr int kOffTmem = kOffBar + kNumBarsMax * 8;
 constexpr int kOffFlag = kOffTmem + 16;
 constexpr int kOffXchg = kOffFlag + 16;               // row max / sum exchange, 2 x 128 fp32
@@ -99,20 +107,16 @@ __device__ __forceinline__ void tc_fence_after() {
 // descriptors in uniform registers; a lone thread in a divergent branch issues at about half
 // the tensor core's rate), and only lane 0 executes the tcgen05 instructions: the wrappers
 // below are predicated on %laneid inside the asm.  Every MMA and commit of a role therefore
-// comes from the same thread, as tcgen05.commit requires.
-__device__ __forceinline__ void tc_commit_l0(uint64_t* bar) {
-  asm volatile(
-      "{\n\t.reg .u32 l;\n\t.reg .pred e;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
+// comes from the same thread, as tcgen05.commit requires.  All tcgen05 operations of this
+// kernel are cta_group::2 (the pair): one MMA computes 256 rows, 128 in each CTA's tensor
+// memory, with A taken from each CTA's own rows and B split by columns between the two CTAs'
+// shared memory at the same offset.
 __device__ __forceinline__ void tc_mma_l0(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .u32 l;\n\t.reg .pred e, p;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -122,7 +126,7 @@ __device__ __forceinline__ void tc_mma_ta_l0(uint32_t d_tmem, uint32_t a_tmem, u
   asm volatile(
       "{\n\t.reg .u32 l;\n\t.reg .pred e, p;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -186,8 +190,8 @@ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0);
-constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 1);
+constexpr uint32_t kIdescQK = idesc_bf16(256, 128, 0);  // M spans the pair
+constexpr uint32_t kIdescPV = idesc_bf16(256, 128, 1);
 
 // ---- thread-block cluster (pairs of CTAs on two SMs) ------------------------------------------
 
@@ -212,25 +216,22 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
 }
-// 3-D TMA tile load delivered to the same shared-memory offset (and barrier) of every CTA in
-// `mask`.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int32_t c0,
-                                               int32_t c1, int32_t c2, uint64_t* bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
 // Arrive on the barrier at this offset in every CTA of `mask` once this thread's MMAs are done.
 __device__ __forceinline__ void tc_commit_mc_l0(uint64_t* bar, uint16_t mask) {
   asm volatile(
       "{\n\t.reg .u32 l;\n\t.reg .pred e;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
       "h"(mask)
+      : "memory");
+}
+// Arrive on the barrier at this offset in the leader CTA of the pair (default semantics: a
+// cluster-scope release would fence every arrival; the data it announces is either written
+// by the asynchronous proxy (TMA) or ordered by the tcgen05 fences around the arrive).
+__device__ __forceinline__ void arrive_leader(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, 0;\n\t"
+      "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
 
@@ -275,7 +276,7 @@ struct Ctx {
   volatile int* abort;
   int* status;
   uint64_t limit;
-  uint32_t rank;       // this CTA's place in its pair
+  uint32_t rank;       // this CTA's place in its pair (0: the leader, which issues the MMAs)
   int cluster;         // pair index
   int nclusters;       // number of pairs
 };
@@ -293,11 +294,22 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 // Bounded wait that also gives up when another role aborted.
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
   uint64_t* b = c.bar + idx;
-  if (mbar_try_wait(b, parity)) return true;
+  if (mbar_try_wait_cl(b, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_sleep(b, parity, 20000u)) return true;
@@ -344,9 +356,11 @@ __device__ __forceinline__ Item load_item(const TcParams& p, int idx, uint32_t r
 
 // ---- roles ------------------------------------------------------------------------------------
 
-// TMA producers.  The K warp also loads Q; the V warp runs its own copy of the loop, so a K
-// tile is fetched as soon as its stage is free (gated only by the QK^T MMAs) and never waits
-// behind a V stage that the slower PV MMAs still hold.
+// TMA producers of this CTA's parts.  The K warp also loads Q; the V warp runs its own copy of
+// the loop, so a K tile is fetched as soon as its stage is free (gated only by the QK^T MMAs)
+// and never waits behind a V stage that the slower PV MMAs still hold.  K part: blocks
+// 4r .. 4r + 3 of the tile (keys 64r ..), both 64-dim halves, [half][64 keys][64 dims]; V part:
+// all 8 blocks, dims 64r .. 64r + 63, [128 keys][64 dims].
 __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
                          const CUtensorMap* tkv, bool is_v, int n_items) {
   const int lane = threadIdx.x & 31;
@@ -389,13 +403,22 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
         const uint32_t st = kv % nst, ph = (kv / nst) & 1u;
         ok = wait_bar(c, empty + st, ph ^ 1u);
         if (ok) {
-          mbar_arrive_expect_tx(c.bar + full + st, kTile);
-          uint8_t* dst = c.sm + off + st * kTile;
+          mbar_arrive_expect_tx(c.bar + full + st, kPart);
+          uint8_t* dst = c.sm + off + st * kPart;
+          if (!is_v) {
 #pragma unroll
-          for (int b = c.rank; b < 8; b += 2) {  // this CTA fetches every other block for both
-            const int r = ids[b] >= 0 ? ids[b] * 16 : -16;
-            tma_load_3d_mc(dst + b * 2048, tkv, 0, I.kvh, r, c.bar + full + st, 0x3);
-            tma_load_3d_mc(dst + kHalf + b * 2048, tkv, 64, I.kvh, r, c.bar + full + st, 0x3);
+            for (int bb = 0; bb < 4; ++bb) {
+              const int b = 4 * (int)c.rank + bb;
+              const int r = ids[b] >= 0 ? ids[b] * 16 : -16;
+              tma_load_3d(dst + bb * 2048, tkv, 0, I.kvh, r, c.bar + full + st);
+              tma_load_3d(dst + kKVHalf + bb * 2048, tkv, 64, I.kvh, r, c.bar + full + st);
+            }
+          } else {
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+              const int r = ids[b] >= 0 ? ids[b] * 16 : -16;
+              tma_load_3d(dst + b * 2048, tkv, 64 * (int)c.rank, I.kvh, r, c.bar + full + st);
+            }
           }
         }
       }
@@ -404,9 +427,11 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
   }
 }
 
-// MMA issue runs on two threads (warps 1 and 11) so that one thread's instruction issue
-// never delays the other chain: the QK^T issuer releases K and Q stages, the PV issuer
-// releases V stages, S / P buffers and O.
+// MMA issue runs on two threads of the leader (warps 1 and 11) so that one thread's
+// instruction issue never delays the other chain: the QK^T issuer releases K and Q stages, the
+// PV issuer releases V stages, S / P buffers and O.  In the peer the same warps forward the
+// arrival of its Q / K parts and (after zeroing unwritten rows) V parts to the leader's full
+// barriers, which count two arrivals: the leader's own producer and the peer's forward.
 //
 // Tile counters run over all items of the CTA; tile s uses S / P buffer s % 3, and each
 // per-buffer barrier completes once per use, so its phase parity is (s / 3) & 1.
@@ -419,23 +444,29 @@ __device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_i
   for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
     const uint32_t qb = it_cnt & 1u;
+    const bool leader = c.rank == 0;
     if (!__all_sync(kFull, wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u))) return;
+    if (!leader && (threadIdx.x & 31) == 0) arrive_leader(c.bar + B_QFULL + qb);
     const uint32_t qbase = sm + kOffQ + qb * kTile;
     for (int j = 0; j < I.ntiles; ++j) {
       const uint32_t s = kv + j, st = s % kStagesK, b = buf_of(s);
       if (!__all_sync(kFull, wait_bar(c, B_KFULL + st, (s / kStagesK) & 1u))) return;
+      if (!leader) {
+        if ((threadIdx.x & 31) == 0) arrive_leader(c.bar + B_KFULL + st);
+        continue;
+      }
       // the buffer's previous tile (s - 3): its P was consumed by its P V
       if (!__all_sync(kFull, wait_bar(c, B_PVDONE + b, use_par(s) ^ 1u))) return;
       tc_fence_after();
-      const uint32_t kb = sm + kOffK + st * kTile;
+      const uint32_t kb = sm + kOffK + st * kPart;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         tc_mma_l0(tmem + col_s(b), sdesc(qbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-                  sdesc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), kIdescQK,
+                  sdesc(kb + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024), kIdescQK,
                   kk > 0 ? 1u : 0u);
-      tc_commit_l0(c.bar + B_SFULL + b);
-      tc_commit_mc_l0(c.bar + B_KEMPTY + st, 0x3);  // both CTAs must be done before a refill
-      if (j == I.ntiles - 1) tc_commit_l0(c.bar + B_QEMPTY + qb);
+      tc_commit_mc_l0(c.bar + B_SFULL + b, 0x3);
+      tc_commit_mc_l0(c.bar + B_KEMPTY + st, 0x3);
+      if (j == I.ntiles - 1) tc_commit_mc_l0(c.bar + B_QEMPTY + qb, 0x3);
       __syncwarp();
     }
     kv += I.ntiles;
@@ -444,8 +475,9 @@ __device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_i
 
 // The whole warp runs the PV loop (lane 0 issues): the V rows of a sequence's last block at
 // positions >= n were never written and may hold anything, so before the MMAs read that block
-// the warp zeroes them in this CTA's copy of the stage.  This role consumes the V stages in
-// order, so its V-full wait always names the right phase.
+// each CTA's warp zeroes them in its own part of the stage (the peer then forwards the stage
+// to the leader).  This role consumes the V stages in order, so its V-full wait always names
+// the right phase.
 __device__ void pv_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
   const int lane = threadIdx.x & 31;
   uint32_t kv = 0, it_cnt = 0;
@@ -455,34 +487,41 @@ __device__ void pv_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_
     const int fix_rel = last_blk * 16 - I.kv0;  // offset of that block inside the item's keys
     const bool need_fix = (I.n % 16) != 0 && last_blk < I.nblk_vis && fix_rel >= 0;
     const int fix_tile = need_fix ? fix_rel / kBN : -1;
+    const bool leader = c.rank == 0;
     for (int j = 0; j < I.ntiles; ++j) {
       const uint32_t s = kv + j, st = s % kStagesV, b = buf_of(s);
-      if (j == 0 && !__all_sync(kFull, wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u))) return;
-      if (!__all_sync(kFull, wait_bar(c, B_PFULL + b, use_par(s)))) return;
+      if (leader) {
+        if (j == 0 && !__all_sync(kFull, wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u))) return;
+        if (!__all_sync(kFull, wait_bar(c, B_PFULL + b, use_par(s)))) return;
+      }
       if (!__all_sync(kFull, wait_bar(c, B_VFULL + st, (s / kStagesV) & 1u))) return;
-      uint8_t* vt = c.sm + kOffV + st * kTile;
+      uint8_t* vt = c.sm + kOffV + st * kPart;
       if (j == fix_tile) {
         const int blk = (fix_rel % kBN) / 16, first = I.n % 16;
-        const int chunks = (16 - first) * 2 * 8;  // rows x halves x 16-byte chunks
+        const int chunks = (16 - first) * 8;  // rows x 16-byte chunks of this CTA's 64 dims
         for (int i = lane; i < chunks; i += 32) {
-          const int rr = first + i / 16, half = (i / 8) & 1, ch = i & 7;
-          *reinterpret_cast<uint4*>(vt + half * kHalf + (blk * 16 + rr) * 128 + ch * 16) =
-              make_uint4(0, 0, 0, 0);
+          const int rr = first + i / 8, ch = i & 7;
+          *reinterpret_cast<uint4*>(vt + (blk * 16 + rr) * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
         }
-        fence_proxy_async_smem();  // the MMA reads V through the async proxy
+        // the MMA (issued by the leader) reads V through the async proxy
+        asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
         __syncwarp();
+      }
+      if (!leader) {
+        if (lane == 0) arrive_leader(c.bar + B_VFULL + st);
+        continue;
       }
       tc_fence_after();
       const uint32_t vb = smem_u32(vt), pb = tmem + col_s(b);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc_mma_ta_l0(tmem + kColO, pb + col_p(kk, 0), sdesc(vb + kk * 2048, kHalf, 1024),
+        tc_mma_ta_l0(tmem + kColO, pb + col_p(kk, 0), sdesc(vb + kk * 2048, 1024, 1024),
                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc_mma_ta_l0(tmem + kColO, pb + col_p(kk, 1), sdesc(vb + kk * 2048, kHalf, 1024),
+        tc_mma_ta_l0(tmem + kColO, pb + col_p(kk, 1), sdesc(vb + kk * 2048, 1024, 1024),
                      kIdescPV, 1u);
-      tc_commit_l0(c.bar + B_PVDONE + b);
+      tc_commit_mc_l0(c.bar + B_PVDONE + b, 0x3);
       tc_commit_mc_l0(c.bar + B_VEMPTY + st, 0x3);
       __syncwarp();
     }
@@ -621,7 +660,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar + B_PFULL + b);
+      if (lane == 0) arrive_leader(c.bar + B_PFULL + b);  // the leader issues this P's MMAs
     }
 
     if (item_of(c, k + 1) < n_items) {
@@ -677,7 +716,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(c.bar + B_OFREE);
+    if (lane == 0) arrive_leader(c.bar + B_OFREE);
     kv += I.ntiles;
   }
 }
@@ -693,16 +732,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* flags = reinterpret_cast<int*>(sm + kOffFlag);  // [0] skip everything, [1] abort
   const int warp = threadIdx.x >> 5;
 
+  const bool leader = cluster_rank() == 0;
   if (threadIdx.x == 0) {
     flags[1] = 0;
-    // k_empty / v_empty: one arrival from each CTA of the pair; p_full / o_free: one per
-    // softmax warp; fin: one per MMA-issuing warp; the rest: one
+    // leader: q/k/v full count its producer and the peer's forward, p_full / o_free one
+    // arrival per softmax warp of both CTAs, fin one per MMA-issuing warp; the empty / done
+    // barriers of both CTAs get one multicast commit per phase; the rest one arrival
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t n = 1;
-      if ((i >= B_KEMPTY && i < B_KEMPTY + kStagesK) || (i >= B_VEMPTY && i < B_VEMPTY + kStagesV))
-        n = 2;
-      if ((i >= B_PFULL && i < B_PFULL + kSBufs) || i == B_OFREE) n = kSoftWarps;
-      if (i == B_FIN) n = 2;
+      if (leader) {
+        if ((i >= B_QFULL && i < B_QFULL + 2) || (i >= B_KFULL && i < B_KFULL + kStagesK) ||
+            (i >= B_VFULL && i < B_VFULL + kStagesV))
+          n = 2;
+        if ((i >= B_PFULL && i < B_PFULL + kSBufs) || i == B_OFREE) n = 2 * kSoftWarps;
+        if (i == B_FIN) n = 2;
+      }
       mbar_init(bar + i, n);
     }
     prefetch_tmap(&tq);
@@ -710,15 +754,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tv);
   }
   fence_mbar_init();
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+  if (warp == 1) {  // one warp of each CTA of the pair allocates, collectively
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  cluster_sync();  // the partner's barriers are initialised before any multicast reaches them
+  cluster_sync();  // the partner's barriers are initialised before any commit or arrive reaches them
   tc_fence_after();
   // everything above overlaps the planning kernel (programmatic dependent launch); the plan
   // and the status word are read only after it has finished
@@ -741,11 +785,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       pv_issuer(c, p, tmem, n_items);
     __syncwarp();
-    // every MMA issued by either warp has completed before the tensor memory is released
-    tc_commit_l0(bar + B_FIN);
-    if ((threadIdx.x & 31) == 0) {
-      uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(bar + B_FIN, 0) && globaltimer_ns() - t0 < 1000000000ull) {
+    // every MMA issued by either warp of the leader has completed before the tensor memory is
+    // released
+    if (leader) {
+      tc_commit_mc_l0(bar + B_FIN, 0x1);
+      if ((threadIdx.x & 31) == 0) {
+        uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar + B_FIN, 0) && globaltimer_ns() - t0 < 1000000000ull) {
+        }
       }
     }
     __syncwarp();
@@ -754,9 +801,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   cluster_sync();  // neither CTA leaves while its partner may still write to its shared memory
-  if (warp == 1) {
+  if (warp == 1) {  // collectively, like the allocation
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
   }
@@ -770,7 +817,7 @@ cudaError_t launch_tc_prefill(const CUtensorMap& tq, const CUtensorMap& tk, cons
   cudaError_t e =
       cudaFuncSetAttribute(k_tc_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  // pairs of CTAs (a cluster of two SMs) share every K / V tile through TMA multicast
+  // pairs of CTAs (a cluster of two SMs) run the 2-SM MMAs
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(grid & ~1), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
