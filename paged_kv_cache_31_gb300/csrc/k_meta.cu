@@ -41,6 +41,34 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
   return before + x - v;
 }
 
+// Exclusive prefix sum, in place, of the kCostBuckets ints at h, by one warp (16 per lane);
+// the total goes to *total.  Called by warp 0 between two __syncthreads.
+template <int N>
+__device__ void warp_scan_inplace(int* h, int* total) {
+  static_assert(N % 32 == 0, "buckets per lane");
+  constexpr int kPer = N / 32;
+  const int lane = threadIdx.x & 31;
+  int v[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    v[i] = h[lane * kPer + i];
+    sum += v[i];
+  }
+  int x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  int run = x - sum;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    h[lane * kPer + i] = run;
+    run += v[i];
+  }
+  if (lane == 31) *total = x;
+}
+
 // Work buckets for ordering: a cost c > 0 maps to 16 sub-buckets per power of two
 // (descending: the largest costs get the smallest bucket index).
 constexpr int kCostBuckets = 512;
@@ -63,34 +91,45 @@ __device__ __forceinline__ int cost_bucket(int c) {
 //     kv group) are cut into 16-row tiles for the warp-MMA kernel, or, for prefill-class
 //     sequences, into 256-row items for the tcgen05 kernel; both lists are ordered by the
 //     number of keys their rows see, longest first, so the kernels' last units are short.
-// The kernel is bound by the latency of its loads, not by bandwidth: phase A issues each
-// sequence's loads together, and keeps q_len and the work estimate in shared memory (up to
-// kPlanCacheSeqs sequences; larger batches read them back from global memory).
+// The kernel is bound by the latency of its loads, not by bandwidth: every sequence's query
+// start and length come into shared memory in one coalesced pass, phase A then issues each
+// sequence's table and position loads together, and the work estimates stay in shared memory
+// (up to kPlanCacheSeqs sequences; larger batches read everything from global memory).  The
+// bucket scans run in one warp, and the prefill-item pass only when the tcgen05 kernel runs.
 __global__ void __launch_bounds__(1024)
     k_plan_varlen(VarlenMeta m, int32_t* plan, const PlanLayout L, int* status) {
   __shared__ int s_err;
   __shared__ int s_warp[32];
   __shared__ int s_hist[kCostBuckets];    // 16-row tiles per cost bucket
   __shared__ int s_hist_t[kCostBuckets];  // 256-row items per cost bucket
-  extern __shared__ int s_seq[];          // [2][num_seqs]: q_len, visible keys (when cached)
+  __shared__ int s_tot;
+  // when cached: [num_seqs + 1] query starts, [num_seqs] seq_len, [num_seqs] visible keys
+  extern __shared__ int s_seq[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   pdl_wait();               // launched early: the batch's metadata may still be in flight
   pdl_launch_dependents();  // the attention kernels' prologues may overlap this kernel
   const bool cached = m.num_seqs <= kPlanCacheSeqs;
-  int* s_qlen = s_seq;
-  int* s_cost = s_seq + (cached ? m.num_seqs : 0);
+  int* s_qsl = s_seq;
+  int* s_n = s_qsl + (cached ? m.num_seqs + 1 : 0);
+  int* s_cost = s_n + (cached ? m.num_seqs : 0);
   if (tid == 0) s_err = status_set(status) ? -1 : 0;
   for (int i = tid; i < kCostBuckets; i += blockDim.x) {
     s_hist[i] = 0;
     s_hist_t[i] = 0;
   }
+  if (cached)
+    for (int i = tid; i <= m.num_seqs; i += blockDim.x) {
+      s_qsl[i] = m.query_start_loc[i];
+      if (i < m.num_seqs) s_n[i] = m.seq_lens[i];
+    }
   __syncthreads();
   if (s_err == 0) {
     if (m.num_seqs == 0 && tid == 0 && (int64_t)m.query_start_loc[0] != m.num_tokens)
       atomicCAS(&s_err, 0, PA_EINVAL);
     for (int s = warp; s < m.num_seqs; s += nwarps) {
-      const int a = m.query_start_loc[s], b = m.query_start_loc[s + 1];
-      const int n = m.seq_lens[s];
+      const int a = cached ? s_qsl[s] : m.query_start_loc[s];
+      const int b = cached ? s_qsl[s + 1] : m.query_start_loc[s + 1];
+      const int n = cached ? s_n[s] : m.seq_lens[s];
       bool bad = a < 0 || b < a || (int64_t)b > m.num_tokens || (s == 0 && a != 0) ||
                  (s == m.num_seqs - 1 && (int64_t)b != m.num_tokens);
       int lo = INT_MAX, hi = 0;
@@ -130,11 +169,10 @@ __global__ void __launch_bounds__(1024)
       }
       if (lane == 0) {
         const int cost = max(0, hi - lo);
-        plan[L.cost_off + s] = cost;
-        if (cached) {
-          s_qlen[s] = b - a;
+        if (cached)
           s_cost[s] = cost;
-        }
+        else
+          plan[L.cost_off + s] = cost;
       }
       if (__any_sync(kFull, bad) && lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
     }
@@ -150,7 +188,7 @@ __global__ void __launch_bounds__(1024)
   }
   // per-sequence q_len and visible keys, from shared memory when cached
   auto qlen_of = [&](int s) -> int {
-    return cached ? s_qlen[s] : m.query_start_loc[s + 1] - m.query_start_loc[s];
+    return cached ? s_qsl[s + 1] - s_qsl[s] : m.query_start_loc[s + 1] - m.query_start_loc[s];
   };
   auto cost_of = [&](int s) -> int { return cached ? s_cost[s] : plan[L.cost_off + s]; };
   int2* mma_items = reinterpret_cast<int2*>(plan + L.mma_off);
@@ -160,21 +198,28 @@ __global__ void __launch_bounds__(1024)
   // B1: 256-row items of prefill-class sequences, in sequence order, the last one (most keys
   // under a causal mask) first; the histogram of the 16-row tiles' costs
   int carry_t = 0;
-  for (int base = 0; base < m.num_seqs; base += blockDim.x) {
-    const int s = base + tid;
-    int cm = 0, ct = 0;
-    if (s < m.num_seqs) {
-      const int64_t rows = (int64_t)qlen_of(s) * m.group;
-      if (L.use_tc && rows > L.tc_min_rows)
-        ct = (int)((rows + 255) / 256);
-      else
-        cm = (int)((rows + 15) / 16);
+  if (L.use_tc) {
+    for (int base = 0; base < m.num_seqs; base += blockDim.x) {
+      const int s = base + tid;
+      int cm = 0, ct = 0;
+      if (s < m.num_seqs) {
+        const int64_t rows = (int64_t)qlen_of(s) * m.group;
+        if (rows > L.tc_min_rows)
+          ct = (int)((rows + 255) / 256);
+        else
+          cm = (int)((rows + 15) / 16);
+      }
+      if (cm > 0) atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
+      int tot_t;
+      const int et = block_exclusive_scan(ct, s_warp, &tot_t);
+      for (int i = 0; i < ct; ++i) tc_tmp[carry_t + et + i] = make_int4(s, ct - 1 - i, 0, 0);
+      carry_t += tot_t;
     }
-    if (cm > 0) atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
-    int tot_t;
-    const int et = block_exclusive_scan(ct, s_warp, &tot_t);
-    for (int i = 0; i < ct; ++i) tc_tmp[carry_t + et + i] = make_int4(s, ct - 1 - i, 0, 0);
-    carry_t += tot_t;
+  } else {
+    for (int s = tid; s < m.num_seqs; s += blockDim.x) {
+      const int cm = (int)(((int64_t)qlen_of(s) * m.group + 15) / 16);
+      if (cm > 0) atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
+    }
   }
   __syncthreads();
   // B2: each item's key range [lo, hi), the union of its tokens' visible ranges (a warp per
@@ -203,16 +248,7 @@ __global__ void __launch_bounds__(1024)
     }
     __syncthreads();
     // B3: the items ordered by cost, longest first (a counting sort over the cost buckets)
-    {
-      int carry = 0;
-      for (int b0 = 0; b0 < kCostBuckets; b0 += blockDim.x) {
-        const int v = b0 + tid < kCostBuckets ? s_hist_t[b0 + tid] : 0;
-        int tot;
-        const int e = block_exclusive_scan(v, s_warp, &tot);
-        if (b0 + tid < kCostBuckets) s_hist_t[b0 + tid] = carry + e;  // bucket start
-        carry += tot;
-      }
-    }
+    if (warp == 0) warp_scan_inplace<kCostBuckets>(s_hist_t, &s_tot);  // bucket starts
     __syncthreads();
     for (int k = tid; k < carry_t; k += blockDim.x) {
       const int4 it = tc_tmp[k];
@@ -221,15 +257,9 @@ __global__ void __launch_bounds__(1024)
   }
   // 16-row tiles, the sequences with the most visible keys first (a counting sort over
   // logarithmic cost buckets), so the persistent kernel's last units are the short ones
-  int carry_m = 0;
-  for (int b0 = 0; b0 < kCostBuckets; b0 += blockDim.x) {
-    const int v = b0 + tid < kCostBuckets ? s_hist[b0 + tid] : 0;
-    int tot;
-    const int e = block_exclusive_scan(v, s_warp, &tot);
-    if (b0 + tid < kCostBuckets) s_hist[b0 + tid] = carry_m + e;  // bucket start
-    carry_m += tot;
-  }
+  if (warp == 0) warp_scan_inplace<kCostBuckets>(s_hist, &s_tot);  // bucket starts
   __syncthreads();
+  const int carry_m = s_tot;
   for (int s = tid; s < m.num_seqs; s += blockDim.x) {
     const int64_t rows = (int64_t)qlen_of(s) * m.group;
     if (rows == 0 || (L.use_tc && rows > L.tc_min_rows)) continue;
@@ -521,9 +551,10 @@ bool aligned(const void* p, size_t a) { return p == nullptr || (reinterpret_cast
 
 cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, const PlanLayout& L,
                                int* status, cudaStream_t stream) {
-  const size_t dyn = m.num_seqs <= kPlanCacheSeqs ? 2 * sizeof(int) * (size_t)m.num_seqs : 0;
+  const size_t dyn =
+      m.num_seqs <= kPlanCacheSeqs ? sizeof(int) * (3 * (size_t)m.num_seqs + 1) : 0;
   cudaError_t e = cudaFuncSetAttribute(k_plan_varlen, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(2 * sizeof(int) * kPlanCacheSeqs));
+                                       (int)(sizeof(int) * (3 * kPlanCacheSeqs + 1)));
   if (e != cudaSuccess) return e;
   return launch_pdl(k_plan_varlen, dim3(1), dim3(1024), dyn, stream, m, plan, L, status);
 }

@@ -245,7 +245,8 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not lan
 //   [2] work counter of the warp-MMA kernel (zeroed by the plan)
 //   [3..15] reserved
 //   [tok_off, tok_off + T)        token -> sequence
-//   [cost_off, cost_off + S)      per sequence: keys its query rows can see (work estimate)
+//   [cost_off, cost_off + S)      per sequence: keys its query rows can see (work estimate;
+//                                 written only for batches too large to keep it in smem)
 //   [mma_off, + 2 * mma_cap)      int2 items (seq, 16-row tile), longest first
 //   [tc_off, + 4 * tc_cap)        int4 items (seq, 256-row item, kv lo, kv hi), longest first
 //   [tc_tmp_off, + 4 * tc_cap)    the same items in sequence order (planning scratch)
