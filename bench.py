@@ -116,16 +116,18 @@ def attn_flops(w) -> int:
 
 
 def launches(w, varlen: bool) -> int:
-    """Kernels of the library launched by one step: slot mapping, slot check and scatter,
-    then validate+plan, the tcgen05 kernel when a sequence can exceed 64 query rows per kv
-    head (the library's own rule) and the warp-MMA kernel; or, split-KV, validation,
-    partials and reduction."""
-    if not varlen:
-        return 3 + 3
+    """Kernels of the library launched by one step: slot mapping + scatter (one kernel for up
+    to 2048 tokens and 2047 sequences, else slot mapping, slot check and scatter), then
+    validate+plan, the tcgen05 kernel when a sequence can exceed 64 query rows per kv head
+    (the library's own rule) and the warp-MMA kernel; or, split-KV, validation, partials and
+    reduction."""
     T, S, G = w.num_tokens, w.num_seqs, w.group
+    cache = 1 if (T <= 2048 and S <= 2047) else 3
+    if not varlen:
+        return cache + 3
     tc = str(w.dtype).endswith("bfloat16") and w.head_dim == 128 and 128 % G == 0 and \
         (T - S + 1) * G > 64
-    return 3 + 2 + (1 if tc else 0)
+    return cache + 2 + (1 if tc else 0)
 
 
 # ------------------------------------------------------------------------------------------
@@ -277,13 +279,14 @@ class Runner:
             self.to = torch.empty((S, H, P, D), device=w.q.device)
 
     def cache(self, m=None):
+        """Slot mapping and scatter of the new tokens' K/V (one launch for decode batches)."""
         w, pa = self.w, self.pa
         m = m or {}
-        pa.pa_slot_mapping(m.get("query_start_loc", w.query_start_loc),
-                           m.get("positions", w.positions), m.get("block_tables", w.block_tables),
-                           w.block_size, w.num_blocks, out=self.slots)
-        pa.pa_reshape_and_cache(m.get("k_new", w.k_new), m.get("v_new", w.v_new), w.k_blocks,
-                                w.v_blocks, self.slots)
+        pa.pa_slot_mapping_and_cache(m.get("k_new", w.k_new), m.get("v_new", w.v_new),
+                                     w.k_blocks, w.v_blocks,
+                                     m.get("query_start_loc", w.query_start_loc),
+                                     m.get("positions", w.positions),
+                                     m.get("block_tables", w.block_tables), out=self.slots)
 
     def attention(self, m=None):
         w, pa = self.w, self.pa

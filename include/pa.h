@@ -103,6 +103,25 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_blocks, voi
                                int64_t num_blocks, pa_dtype kv_dtype, cudaStream_t stream);
 
 /*
+ * pa_slot_mapping_and_cache -- pa_slot_mapping followed by pa_reshape_and_cache on the same
+ * stream, as one launch when num_tokens <= 2048 and num_seqs <= 2047 (a decode step; larger
+ * batches take the two launches).  Writes slot_mapping [num_tokens] (-1 for an invalid token)
+ * and scatters the new K/V rows of every token into its slot.  Every token's slot is computed
+ * and checked before any row is written: a token that no sequence's range
+ * [query_start_loc[s], query_start_loc[s + 1]) holds, a malformed query_start_loc, a position
+ * outside its table row or a block id outside [0, num_blocks) writes no row and records
+ * PA_EINVAL.  Layouts and dtypes as in pa_slot_mapping and pa_reshape_and_cache (a copy, so
+ * bit-exact).  Duplicate slots are undefined.
+ */
+pa_status pa_slot_mapping_and_cache(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                                    const int32_t* query_start_loc, const int32_t* positions,
+                                    const int32_t* block_tables, int32_t num_seqs,
+                                    int64_t num_tokens, int32_t max_blocks_per_seq,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                    int64_t num_blocks, pa_dtype kv_dtype, int32_t* slot_mapping,
+                                    cudaStream_t stream);
+
+/*
  * pa_reshape_and_cache_ex -- the scatter of pa_reshape_and_cache with a conversion: new rows
  * of src_dtype (f32 or bf16) go into pools of kv_dtype (f32, bf16 or fp8 e4m3), element x of
  * K stored as x / k_scale and of V as x / v_scale, the quotient taken in fp32 (IEEE division)

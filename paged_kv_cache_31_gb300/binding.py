@@ -36,6 +36,8 @@ _SIGS = {
     "pa_slot_mapping": ([_vp, _vp, _vp, _i32, _i64, _i32, _i32, _i64, _vp, _vp], ctypes.c_int),
     "pa_reshape_and_cache": ([_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64, ctypes.c_int,
                               _vp], ctypes.c_int),
+    "pa_slot_mapping_and_cache": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
+                                   _i32, _i32, _i64, ctypes.c_int, _vp, _vp], ctypes.c_int),
     "pa_reshape_and_cache_ex": ([_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64,
                                  ctypes.c_int, ctypes.c_int, _f32, _f32, _vp], ctypes.c_int),
     "pa_varlen_forward_workspace_size": ([_i32, _i64, _i32, _i32, _i32, _i32, _i32], _sz),
@@ -132,6 +134,30 @@ def pa_slot_mapping(query_start_loc, positions, block_tables, block_size, num_bl
     _check(_lib.pa_slot_mapping(_p(query_start_loc), _p(positions), _p(block_tables),
                                 query_start_loc.numel() - 1, T, block_tables.shape[1], block_size,
                                 num_blocks, _p(out), _stream(stream)), "pa_slot_mapping")
+    return out
+
+
+def pa_slot_mapping_and_cache(k, v, k_blocks, v_blocks, query_start_loc, positions,
+                              block_tables, out=None, stream=None):
+    """pa_slot_mapping followed by pa_reshape_and_cache, one launch for decode-sized batches;
+    returns the slot mapping."""
+    _dev(k, v, k_blocks, v_blocks, query_start_loc, positions, block_tables, out)
+    _i32t(query_start_loc, positions, block_tables, out)
+    if k.shape != v.shape or k.dim() != 3 or k_blocks.shape != v_blocks.shape:
+        raise ValueError("k, v must be [T, Hkv, D]; pools [NB, b, Hkv, D]")
+    if k.dtype != k_blocks.dtype or v.dtype != v_blocks.dtype or k.dtype != v.dtype:
+        raise ValueError("new rows and pools must share one dtype")
+    T, Hkv, D = k.shape
+    NB, bs, Hkv2, D2 = k_blocks.shape
+    if (Hkv, D) != (Hkv2, D2) or positions.numel() != T:
+        raise ValueError("kv heads / head size / token count differ between rows and pool")
+    if out is None:
+        out = torch.empty(T, dtype=torch.int32, device=k.device)
+    _check(_lib.pa_slot_mapping_and_cache(_p(k), _p(v), _p(k_blocks), _p(v_blocks),
+                                          _p(query_start_loc), _p(positions), _p(block_tables),
+                                          query_start_loc.numel() - 1, T, block_tables.shape[1],
+                                          Hkv, D, bs, NB, _DT[k.dtype], _p(out),
+                                          _stream(stream)), "pa_slot_mapping_and_cache")
     return out
 
 

@@ -378,9 +378,12 @@ __global__ void __launch_bounds__(256)
                       VEC* __restrict__ k_blocks, VEC* __restrict__ v_blocks,
                       const int32_t* __restrict__ slots, int num_tokens, int64_t num_slots,
                       int64_t row_vecs, int* status) {
+  __shared__ int s_skip;
   pdl_wait();
   pdl_launch_dependents();
-  if (status_set(status)) return;  // uniform across the CTA
+  if (threadIdx.x == 0) s_skip = status_set(status) ? 1 : 0;  // one read for the whole CTA
+  __syncthreads();
+  if (s_skip) return;
   bool bad = false;
   for (int t = threadIdx.x; t < num_tokens; t += blockDim.x) {
     const int32_t sl = slots[t];
@@ -413,9 +416,12 @@ __global__ void __launch_bounds__(256)
                       void* __restrict__ vb, const int32_t* __restrict__ slots, int64_t num_tokens,
                       int64_t num_slots, int64_t row_elems, float k_scale, float v_scale,
                       int* status) {
+  __shared__ int s_skip;
   pdl_wait();
   pdl_launch_dependents();
-  if (status_set(status)) return;  // uniform across the CTA
+  if (threadIdx.x == 0) s_skip = status_set(status) ? 1 : 0;  // one read for the whole CTA
+  __syncthreads();
+  if (s_skip) return;
   if constexpr (CHECKED) {
     bool bad = false;
     for (int64_t t = threadIdx.x; t < num_tokens; t += blockDim.x) {
@@ -462,6 +468,89 @@ cudaError_t convert_as(const void* k, const void* v, void* kb, void* vb, const i
   if (e != cudaSuccess) return e;
   return launch_pdl(k_scatter_convert<TS, DST, false>, grid, block, 0, stream, (const TS*)k,
                     (const TS*)v, kb, vb, slots, T, num_slots, row_elems, k_scale, v_scale,
+                    status);
+}
+
+// Slot mapping and scatter in one launch, for batches of up to kCheckedScatter tokens and
+// kFusedSeqs sequences (a decode step): every CTA loads the query start locations into shared
+// memory, finds each token's sequence by binary search, computes every token's slot by the rule
+// of k_slot_mapping and checks it; only when all are valid does it copy its own eight tokens'
+// rows (one warp per token).  CTA 0 writes the slot mapping (-1 for an invalid token).  A token
+// that no sequence's range holds is invalid.
+constexpr int kFusedSeqs = 2047;
+template <typename VEC>
+__global__ void __launch_bounds__(256)
+    k_map_and_scatter(const VEC* __restrict__ k, const VEC* __restrict__ v,
+                      VEC* __restrict__ k_blocks, VEC* __restrict__ v_blocks,
+                      const int32_t* __restrict__ qsl, const int32_t* __restrict__ positions,
+                      const int32_t* __restrict__ tables, int num_seqs, int num_tokens,
+                      int32_t max_blocks, int32_t block_size, int64_t num_blocks,
+                      int64_t row_vecs, int32_t* __restrict__ slots, int* status) {
+  __shared__ int s_qsl[kFusedSeqs + 1];
+  __shared__ int s_slot[kCheckedScatter];
+  __shared__ int s_skip;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) s_skip = status_set(status) ? 1 : 0;  // one read for the whole CTA
+  __syncthreads();
+  if (s_skip) return;
+  for (int i = threadIdx.x; i <= num_seqs; i += blockDim.x) s_qsl[i] = qsl[i];
+  __syncthreads();
+  bool bad = false;
+  for (int i = threadIdx.x; i < num_seqs; i += blockDim.x) {
+    const int a = s_qsl[i], b = s_qsl[i + 1];
+    bad |= a < 0 || b < a || b > num_tokens;
+  }
+  for (int t = threadIdx.x; t < num_tokens; t += blockDim.x) {
+    int lo = 0, hi = num_seqs - 1, s = -1;  // the last sequence starting at or before t
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_qsl[mid] <= t) {
+        s = mid;
+        lo = mid + 1;
+      } else {
+        hi = mid - 1;
+      }
+    }
+    int32_t slot = -1;
+    if (s >= 0 && t < s_qsl[s + 1]) {
+      const int32_t pos = positions[t];
+      if (pos >= 0 && pos / block_size < max_blocks) {
+        const int32_t id = tables[(int64_t)s * max_blocks + pos / block_size];
+        if (id >= 0 && (int64_t)id < num_blocks) slot = id * block_size + pos % block_size;
+      }
+    }
+    s_slot[t] = slot;
+    bad |= slot < 0;
+  }
+  bad = __syncthreads_or(bad);
+  if (blockIdx.x == 0)
+    for (int t = threadIdx.x; t < num_tokens; t += blockDim.x) slots[t] = s_slot[t];
+  if (bad) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) record_error(status, PA_EINVAL);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= num_tokens) return;
+  const int64_t dst = (int64_t)s_slot[t] * row_vecs, src = (int64_t)t * row_vecs;
+  for (int64_t i = lane; i < row_vecs; i += 32) {
+    const VEC a = k[src + i];
+    const VEC b = v[src + i];
+    k_blocks[dst + i] = a;
+    v_blocks[dst + i] = b;
+  }
+}
+
+template <typename VEC>
+cudaError_t map_and_scatter_as(const void* k, const void* v, void* kb, void* vb,
+                               const int32_t* qsl, const int32_t* positions,
+                               const int32_t* tables, int32_t S, int64_t T, int32_t max_blocks,
+                               int32_t bs, int64_t nb, int64_t row_bytes, int32_t* slots,
+                               int* status, cudaStream_t stream) {
+  return launch_pdl(k_map_and_scatter<VEC>, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, stream,
+                    (const VEC*)k, (const VEC*)v, (VEC*)kb, (VEC*)vb, qsl, positions, tables,
+                    (int)S, (int)T, max_blocks, bs, nb, row_bytes / (int64_t)sizeof(VEC), slots,
                     status);
 }
 
@@ -600,6 +689,47 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_block
                                 num_slots, status, stream);
   return scatter_as<uint8_t>(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes, num_slots,
                              status, stream);
+}
+
+cudaError_t launch_slot_mapping_and_cache(const void* k, const void* v, void* k_blocks,
+                                          void* v_blocks, const int32_t* qsl,
+                                          const int32_t* positions, const int32_t* tables,
+                                          int32_t num_seqs, int64_t num_tokens,
+                                          int32_t max_blocks, int32_t block_size,
+                                          int64_t num_blocks, int64_t row_bytes, int32_t* slots,
+                                          int* status, cudaStream_t stream) {
+  if (num_tokens <= 0) return cudaSuccess;
+  if (num_tokens > kCheckedScatter || num_seqs > kFusedSeqs || num_seqs <= 0) {
+    // larger batches: the two launches of pa_slot_mapping and pa_reshape_and_cache; slots
+    // start at -1, so a token no sequence holds fails the scatter's check
+    cudaError_t e = cudaMemsetAsync(slots, 0xff, (size_t)num_tokens * sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    e = num_seqs > 0 ? launch_slot_mapping(qsl, positions, tables, num_seqs, num_tokens,
+                                           max_blocks, block_size, num_blocks, slots, status,
+                                           stream)
+                     : cudaSuccess;
+    if (e != cudaSuccess) return e;
+    return launch_reshape_and_cache(k, v, k_blocks, v_blocks, slots, num_tokens, row_bytes,
+                                    block_size, num_blocks, status, stream);
+  }
+  if (row_bytes % 16 == 0 && aligned(k, 16) && aligned(v, 16) && aligned(k_blocks, 16) &&
+      aligned(v_blocks, 16))
+    return map_and_scatter_as<uint4>(k, v, k_blocks, v_blocks, qsl, positions, tables, num_seqs,
+                                     num_tokens, max_blocks, block_size, num_blocks, row_bytes,
+                                     slots, status, stream);
+  if (row_bytes % 4 == 0 && aligned(k, 4) && aligned(v, 4) && aligned(k_blocks, 4) &&
+      aligned(v_blocks, 4))
+    return map_and_scatter_as<uint32_t>(k, v, k_blocks, v_blocks, qsl, positions, tables,
+                                        num_seqs, num_tokens, max_blocks, block_size, num_blocks,
+                                        row_bytes, slots, status, stream);
+  if (row_bytes % 2 == 0 && aligned(k, 2) && aligned(v, 2) && aligned(k_blocks, 2) &&
+      aligned(v_blocks, 2))
+    return map_and_scatter_as<uint16_t>(k, v, k_blocks, v_blocks, qsl, positions, tables,
+                                        num_seqs, num_tokens, max_blocks, block_size, num_blocks,
+                                        row_bytes, slots, status, stream);
+  return map_and_scatter_as<uint8_t>(k, v, k_blocks, v_blocks, qsl, positions, tables, num_seqs,
+                                     num_tokens, max_blocks, block_size, num_blocks, row_bytes,
+                                     slots, status, stream);
 }
 
 cudaError_t launch_reshape_and_cache_convert(const void* k, const void* v, void* k_blocks,

@@ -214,6 +214,30 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_blocks, voi
                                             row_bytes, block_size, num_blocks, d->status, stream));
 }
 
+pa_status pa_slot_mapping_and_cache(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                                    const int32_t* query_start_loc, const int32_t* positions,
+                                    const int32_t* block_tables, int32_t num_seqs,
+                                    int64_t num_tokens, int32_t max_blocks_per_seq,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                    int64_t num_blocks, pa_dtype kv_dtype, int32_t* slot_mapping,
+                                    cudaStream_t stream) {
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return PA_ESHAPE;
+  if (!pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 0 || num_blocks < 0)
+    return PA_EINVAL;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_blocks || !v_blocks || !query_start_loc || !positions || !block_tables ||
+      !slot_mapping)
+    return PA_EINVAL;
+  if (num_blocks * block_size > INT32_MAX) return PA_EUNSUPPORTED;  // slots are int32
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * esize(kv_dtype);
+  return from_cuda(launch_slot_mapping_and_cache(
+      k, v, k_blocks, v_blocks, query_start_loc, positions, block_tables, num_seqs, num_tokens,
+      max_blocks_per_seq, block_size, num_blocks, row_bytes, slot_mapping, d->status, stream));
+}
+
 pa_status pa_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, void* v_blocks,
                                   const int32_t* slot_mapping, int64_t num_tokens,
                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
