@@ -307,8 +307,21 @@ class Runner:
                                  w.partition_size, w.sliding_window)
 
     def step(self, m=None):
-        self.cache(m)
-        self.attention(m)
+        """One step: the new tokens' K/V into the cache, then attention (varlen: one library
+        call, whose scatter overlaps the attention's planning kernel)."""
+        if not self.varlen:
+            self.cache(m)
+            self.attention(m)
+            return
+        w, pa = self.w, self.pa
+        m = m or {}
+        pa.pa_cache_and_attend(m.get("k_new", w.k_new), m.get("v_new", w.v_new),
+                               m.get("q", w.q), w.k_blocks, w.v_blocks, m.get("out", self.out),
+                               m.get("query_start_loc", w.query_start_loc),
+                               m.get("seq_lens", w.seq_lens), m.get("positions", w.positions),
+                               m.get("block_tables", w.block_tables), w.scale, causal=w.causal,
+                               sliding_window=w.sliding_window, workspace=self.ws,
+                               slot_mapping=self.slots)
 
 
 def time_calls(fn, n, stream, flush=None):

@@ -222,6 +222,26 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
                                cudaStream_t stream);
 
 /*
+ * pa_cache_and_attend -- one decode / prefill step over the cache: pa_slot_mapping_and_cache
+ * of the new tokens' rows (k_new, v_new [num_tokens, num_kv_heads, head_dim] of kv_dtype;
+ * slot_mapping [num_tokens] written) followed by pa_varlen_forward of q over the updated pools,
+ * with the same arguments, results and errors as those two calls made one after the other.
+ * For batches of up to 2048 tokens and 2047 sequences the slot mapping and scatter run as one
+ * kernel launched right after the attention's planning kernel, overlapping it (neither reads
+ * what the other writes), instead of in front of it.
+ */
+pa_status pa_cache_and_attend(const void* k_new, const void* v_new, const void* q,
+                              void* k_blocks, void* v_blocks, void* out,
+                              const int32_t* query_start_loc, const int32_t* seq_lens,
+                              const int32_t* positions, const int32_t* block_tables,
+                              int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, int32_t max_blocks_per_seq, pa_dtype q_dtype,
+                              pa_dtype kv_dtype, float scale, int32_t causal,
+                              int32_t sliding_window, int32_t* slot_mapping, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * pa_varlen_forward_noalloc -- pa_varlen_forward for callers that cannot allocate device
  * memory.  The pages have no counterpart: it exists for the library's users, not for the
  * method.  Some callers cannot hand this library a workspace: a host framework that gives an

@@ -48,6 +48,9 @@ _SIGS = {
                               _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32,
                               _i32, _vp, _vp, _f32, _f32, ctypes.c_uint32, _vp, _sz, _vp],
                              ctypes.c_int),
+    "pa_cache_and_attend": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32,
+                             _i32, _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32,
+                             _i32, _i32, _vp, _vp, _sz, _vp], ctypes.c_int),
     "pa_varlen_forward_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
                                    _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32,
                                    _i32, _vp], ctypes.c_int),
@@ -249,6 +252,38 @@ def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, pos
                                      _p(workspace), workspace.numel(), _stream(stream)),
            "pa_varlen_forward_ex")
     return out
+
+
+def pa_cache_and_attend(k_new, v_new, q, k_blocks, v_blocks, out, query_start_loc, seq_lens,
+                        positions, block_tables, scale, causal=True, sliding_window=0,
+                        workspace=None, slot_mapping=None, stream=None):
+    """pa_slot_mapping_and_cache of the new rows, then pa_varlen_forward of q (one call; the
+    scatter overlaps the attention's planning kernel).  Returns the slot mapping."""
+    _dev(k_new, v_new, q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
+         block_tables, workspace, slot_mapping)
+    _i32t(query_start_loc, seq_lens, positions, block_tables, slot_mapping)
+    if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q and out must be [T, H, D] of one dtype")
+    if k_blocks.shape != v_blocks.shape or k_blocks.dtype != v_blocks.dtype:
+        raise ValueError("k_blocks and v_blocks must match")
+    if k_new.shape != v_new.shape or k_new.dtype != k_blocks.dtype or v_new.dtype != v_blocks.dtype:
+        raise ValueError("new rows must be [T, Hkv, D] of the pool dtype")
+    T, H, D = q.shape
+    NB, bs, Hkv, D2 = k_blocks.shape
+    if D2 != D or k_new.shape != (T, Hkv, D):
+        raise ValueError("shapes of q, the new rows and the pool differ")
+    if workspace is None:
+        workspace = workspace_for(q, k_blocks, query_start_loc, block_tables)
+    if slot_mapping is None:
+        slot_mapping = torch.empty(T, dtype=torch.int32, device=q.device)
+    _check(_lib.pa_cache_and_attend(_p(k_new), _p(v_new), _p(q), _p(k_blocks), _p(v_blocks),
+                                    _p(out), _p(query_start_loc), _p(seq_lens), _p(positions),
+                                    _p(block_tables), query_start_loc.numel() - 1, T, H, Hkv, D,
+                                    bs, NB, block_tables.shape[1], _DT[q.dtype],
+                                    _DT[k_blocks.dtype], float(scale), int(bool(causal)),
+                                    int(sliding_window), _p(slot_mapping), _p(workspace),
+                                    workspace.numel(), _stream(stream)), "pa_cache_and_attend")
+    return slot_mapping
 
 
 def pa_varlen_forward_noalloc(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,

@@ -477,19 +477,23 @@ cudaError_t convert_as(const void* k, const void* v, void* kb, void* vb, const i
 // of k_slot_mapping and checks it; only when all are valid does it copy its own eight tokens'
 // rows (one warp per token).  CTA 0 writes the slot mapping (-1 for an invalid token).  A token
 // that no sequence's range holds is invalid.
+//
+// AFTER_PLAN: launched right after the planning kernel of the same attention call (which has
+// already waited for the kernels before it), so it runs alongside the plan instead of before
+// it; it then waits for the plan before it ends, so the attention kernel behind it (which
+// waits for this grid) still finds both done.
 constexpr int kFusedSeqs = 2047;
-template <typename VEC>
-__global__ void __launch_bounds__(256)
-    k_map_and_scatter(const VEC* __restrict__ k, const VEC* __restrict__ v,
-                      VEC* __restrict__ k_blocks, VEC* __restrict__ v_blocks,
-                      const int32_t* __restrict__ qsl, const int32_t* __restrict__ positions,
-                      const int32_t* __restrict__ tables, int num_seqs, int num_tokens,
-                      int32_t max_blocks, int32_t block_size, int64_t num_blocks,
-                      int64_t row_vecs, int32_t* __restrict__ slots, int* status) {
+template <typename VEC, bool AFTER_PLAN>
+__device__ __forceinline__ void map_and_scatter_body(
+    const VEC* __restrict__ k, const VEC* __restrict__ v, VEC* __restrict__ k_blocks,
+    VEC* __restrict__ v_blocks, const int32_t* __restrict__ qsl,
+    const int32_t* __restrict__ positions, const int32_t* __restrict__ tables, int num_seqs,
+    int num_tokens, int32_t max_blocks, int32_t block_size, int64_t num_blocks,
+    int64_t row_vecs, int32_t* __restrict__ slots, int* status) {
   __shared__ int s_qsl[kFusedSeqs + 1];
   __shared__ int s_slot[kCheckedScatter];
   __shared__ int s_skip;
-  pdl_wait();
+  if (!AFTER_PLAN) pdl_wait();
   pdl_launch_dependents();
   if (threadIdx.x == 0) s_skip = status_set(status) ? 1 : 0;  // one read for the whole CTA
   __syncthreads();
@@ -542,13 +546,28 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <typename VEC>
+template <typename VEC, bool AFTER_PLAN>
+__global__ void __launch_bounds__(256)
+    k_map_and_scatter(const VEC* __restrict__ k, const VEC* __restrict__ v,
+                      VEC* __restrict__ k_blocks, VEC* __restrict__ v_blocks,
+                      const int32_t* __restrict__ qsl, const int32_t* __restrict__ positions,
+                      const int32_t* __restrict__ tables, int num_seqs, int num_tokens,
+                      int32_t max_blocks, int32_t block_size, int64_t num_blocks,
+                      int64_t row_vecs, int32_t* __restrict__ slots, int* status) {
+  map_and_scatter_body<VEC, AFTER_PLAN>(k, v, k_blocks, v_blocks, qsl, positions, tables,
+                                        num_seqs, num_tokens, max_blocks, block_size,
+                                        num_blocks, row_vecs, slots, status);
+  if (AFTER_PLAN) pdl_wait();  // this grid ends only after the plan has
+}
+
+template <typename VEC, bool AFTER_PLAN = false>
 cudaError_t map_and_scatter_as(const void* k, const void* v, void* kb, void* vb,
                                const int32_t* qsl, const int32_t* positions,
                                const int32_t* tables, int32_t S, int64_t T, int32_t max_blocks,
                                int32_t bs, int64_t nb, int64_t row_bytes, int32_t* slots,
                                int* status, cudaStream_t stream) {
-  return launch_pdl(k_map_and_scatter<VEC>, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, stream,
+  return launch_pdl(k_map_and_scatter<VEC, AFTER_PLAN>, dim3((unsigned)((T + 7) / 8)), dim3(256),
+                    0, stream,
                     (const VEC*)k, (const VEC*)v, (VEC*)kb, (VEC*)vb, qsl, positions, tables,
                     (int)S, (int)T, max_blocks, bs, nb, row_bytes / (int64_t)sizeof(VEC), slots,
                     status);
@@ -730,6 +749,38 @@ cudaError_t launch_slot_mapping_and_cache(const void* k, const void* v, void* k_
   return map_and_scatter_as<uint8_t>(k, v, k_blocks, v_blocks, qsl, positions, tables, num_seqs,
                                      num_tokens, max_blocks, block_size, num_blocks, row_bytes,
                                      slots, status, stream);
+}
+
+bool map_and_scatter_fits(int32_t num_seqs, int64_t num_tokens) {
+  return num_tokens > 0 && num_tokens <= kCheckedScatter && num_seqs > 0 &&
+         num_seqs <= kFusedSeqs;
+}
+
+cudaError_t launch_map_and_scatter_after_plan(const void* k, const void* v, void* k_blocks,
+                                              void* v_blocks, const int32_t* qsl,
+                                              const int32_t* positions, const int32_t* tables,
+                                              int32_t num_seqs, int64_t num_tokens,
+                                              int32_t max_blocks, int32_t block_size,
+                                              int64_t num_blocks, int64_t row_bytes,
+                                              int32_t* slots, int* status, cudaStream_t stream) {
+  if (row_bytes % 16 == 0 && aligned(k, 16) && aligned(v, 16) && aligned(k_blocks, 16) &&
+      aligned(v_blocks, 16))
+    return map_and_scatter_as<uint4, true>(k, v, k_blocks, v_blocks, qsl, positions, tables,
+                                           num_seqs, num_tokens, max_blocks, block_size,
+                                           num_blocks, row_bytes, slots, status, stream);
+  if (row_bytes % 4 == 0 && aligned(k, 4) && aligned(v, 4) && aligned(k_blocks, 4) &&
+      aligned(v_blocks, 4))
+    return map_and_scatter_as<uint32_t, true>(k, v, k_blocks, v_blocks, qsl, positions, tables,
+                                              num_seqs, num_tokens, max_blocks, block_size,
+                                              num_blocks, row_bytes, slots, status, stream);
+  if (row_bytes % 2 == 0 && aligned(k, 2) && aligned(v, 2) && aligned(k_blocks, 2) &&
+      aligned(v_blocks, 2))
+    return map_and_scatter_as<uint16_t, true>(k, v, k_blocks, v_blocks, qsl, positions, tables,
+                                              num_seqs, num_tokens, max_blocks, block_size,
+                                              num_blocks, row_bytes, slots, status, stream);
+  return map_and_scatter_as<uint8_t, true>(k, v, k_blocks, v_blocks, qsl, positions, tables,
+                                           num_seqs, num_tokens, max_blocks, block_size,
+                                           num_blocks, row_bytes, slots, status, stream);
 }
 
 cudaError_t launch_reshape_and_cache_convert(const void* k, const void* v, void* k_blocks,

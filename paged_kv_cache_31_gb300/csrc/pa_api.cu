@@ -286,17 +286,26 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
                               1.f, 0u, workspace, workspace_bytes, stream);
 }
 
-pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* v_blocks,
-                               void* out, const int32_t* query_start_loc,
-                               const int32_t* seq_lens, const int32_t* positions,
-                               const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
-                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                               int32_t block_size, int64_t num_blocks,
-                               int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
-                               float scale, int32_t causal, int32_t sliding_window,
-                               const float* sinks, float* lse, float k_scale, float v_scale,
-                               uint32_t flags, void* workspace, size_t workspace_bytes,
-                               cudaStream_t stream) {
+// The new tokens' rows of pa_cache_and_attend, scattered by the kernel launched right after
+// the plan.
+struct CacheArgs {
+  const void* k;
+  const void* v;
+  int32_t* slots;
+  int64_t row_bytes;
+};
+
+static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_blocks,
+                             void* out, const int32_t* query_start_loc, const int32_t* seq_lens,
+                             const int32_t* positions, const int32_t* block_tables,
+                             int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int64_t num_blocks, int32_t max_blocks_per_seq, pa_dtype q_dtype,
+                             pa_dtype kv_dtype, float scale, int32_t causal,
+                             int32_t sliding_window, const float* sinks, float* lse,
+                             float k_scale, float v_scale, uint32_t flags, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream,
+                             const CacheArgs* cache) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0)
     return PA_ESHAPE;
@@ -351,6 +360,14 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
 
   cudaError_t e = launch_plan_varlen(m, plan, L, d->status, stream);
   if (e != cudaSuccess) return PA_ECUDA;
+  if (cache) {  // the new tokens' slots and rows, alongside the plan
+    e = launch_map_and_scatter_after_plan(cache->k, cache->v, const_cast<void*>(k_blocks),
+                                          const_cast<void*>(v_blocks), query_start_loc,
+                                          positions, block_tables, num_seqs, num_tokens,
+                                          max_blocks_per_seq, block_size, num_blocks,
+                                          cache->row_bytes, cache->slots, d->status, stream);
+    if (e != cudaSuccess) return PA_ECUDA;
+  }
 
   if (mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out)) {
     // fp8 pools: every sequence on the warp-MMA kernel (the plan had use_tc off)
@@ -421,6 +438,61 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
   p.kv_bf16 = kv_dtype == PA_BF16;
   p.kv_fp8 = kv_dtype == PA_FP8_E4M3;
   return from_cuda(launch_simt(p, stream));
+}
+
+pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* v_blocks,
+                               void* out, const int32_t* query_start_loc,
+                               const int32_t* seq_lens, const int32_t* positions,
+                               const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t num_blocks,
+                               int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
+                               float scale, int32_t causal, int32_t sliding_window,
+                               const float* sinks, float* lse, float k_scale, float v_scale,
+                               uint32_t flags, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  return varlen_impl(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
+                     block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, max_blocks_per_seq, q_dtype, kv_dtype, scale, causal,
+                     sliding_window, sinks, lse, k_scale, v_scale, flags, workspace,
+                     workspace_bytes, stream, nullptr);
+}
+
+pa_status pa_cache_and_attend(const void* k_new, const void* v_new, const void* q,
+                              void* k_blocks, void* v_blocks, void* out,
+                              const int32_t* query_start_loc, const int32_t* seq_lens,
+                              const int32_t* positions, const int32_t* block_tables,
+                              int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, int32_t max_blocks_per_seq, pa_dtype q_dtype,
+                              pa_dtype kv_dtype, float scale, int32_t causal,
+                              int32_t sliding_window, int32_t* slot_mapping, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return PA_ESHAPE;
+  if (!pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (num_seqs < 0 || num_tokens < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
+    return PA_EINVAL;
+  if (num_tokens > 0 && (!k_new || !v_new || !slot_mapping)) return PA_EINVAL;
+  if (num_blocks * block_size > INT32_MAX) return PA_EUNSUPPORTED;  // slots are int32
+  if (!map_and_scatter_fits(num_seqs, num_tokens)) {  // larger batches: one call after the other
+    const pa_status st = pa_slot_mapping_and_cache(
+        k_new, v_new, k_blocks, v_blocks, query_start_loc, positions, block_tables, num_seqs,
+        num_tokens, max_blocks_per_seq, num_kv_heads, head_dim, block_size, num_blocks, kv_dtype,
+        slot_mapping, stream);
+    if (st != PA_OK) return st;
+    return pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
+                             block_tables, num_seqs, num_tokens, num_heads, num_kv_heads,
+                             head_dim, block_size, num_blocks, max_blocks_per_seq, q_dtype,
+                             kv_dtype, scale, causal, sliding_window, workspace,
+                             workspace_bytes, stream);
+  }
+  const CacheArgs cache{k_new, v_new, slot_mapping,
+                        (int64_t)num_kv_heads * head_dim * esize(kv_dtype)};
+  return varlen_impl(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
+                     block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, max_blocks_per_seq, q_dtype, kv_dtype, scale, causal,
+                     sliding_window, nullptr, nullptr, 1.f, 1.f, 0u, workspace, workspace_bytes,
+                     stream, &cache);
 }
 
 static pa_status splitkv_partials(const void* q, const void* k_blocks, const void* v_blocks,

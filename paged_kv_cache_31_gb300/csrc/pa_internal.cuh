@@ -368,6 +368,16 @@ cudaError_t launch_slot_mapping_and_cache(const void* k, const void* v, void* k_
                                           int32_t max_blocks, int32_t block_size,
                                           int64_t num_blocks, int64_t row_bytes, int32_t* slots,
                                           int* status, cudaStream_t stream);
+// The same, launched right after an attention call's plan kernel so that the two overlap
+// (decode-sized batches only: map_and_scatter_fits).
+bool map_and_scatter_fits(int32_t num_seqs, int64_t num_tokens);
+cudaError_t launch_map_and_scatter_after_plan(const void* k, const void* v, void* k_blocks,
+                                              void* v_blocks, const int32_t* qsl,
+                                              const int32_t* positions, const int32_t* tables,
+                                              int32_t num_seqs, int64_t num_tokens,
+                                              int32_t max_blocks, int32_t block_size,
+                                              int64_t num_blocks, int64_t row_bytes,
+                                              int32_t* slots, int* status, cudaStream_t stream);
 // Scatter with conversion: element x of K (V) is stored as x / k_scale (x / v_scale), the
 // quotient rounded to the pool's type.  src_bf16: new rows are bf16 (else f32); dst: the
 // pool's pa_dtype.  row_elems = num_kv_heads * head_dim.

@@ -126,3 +126,68 @@ def test_invalid_tokens_write_nothing(pa):
     w.query_start_loc[3] = w.num_tokens - 1
     _bad(pa, w, "uncovered token")
     assert pa.pa_device_status() == pa.PA_OK
+
+
+# ------------------------------------------------------------------- pa_cache_and_attend
+
+STEP_CASES = {
+    "decode-64": dict(cfg=2),
+    # prefill chunks (tcgen05 kernel) and decode tokens, windowed
+    "mixed": dict(seq_lens=[600, 1300, 90, 2000, 4000], q_lens=[512, 130, 1, 1, 1],
+                  num_heads=32, num_kv_heads=8, head_dim=128, sliding_window=1000),
+    # past the one-launch limits: the calls run one after the other
+    "big-3000": dict(seq_lens=[1500, 2000], q_lens=[1500, 1500], num_heads=8, num_kv_heads=8,
+                     head_dim=64),
+}
+
+
+def _step_build(name):
+    kw = dict(STEP_CASES[name])
+    if "cfg" in kw:
+        return workloads.named(kw["cfg"], seed=6, device=DEV)
+    return workloads.build(name, seed=sorted(STEP_CASES).index(name) + 21, device=DEV, **kw)
+
+
+def _two_calls(pa, w, kb, vb):
+    s = pa.pa_slot_mapping_and_cache(w.k_new, w.v_new, kb, vb, w.query_start_loc, w.positions,
+                                     w.block_tables)
+    out = torch.full_like(w.q, float("nan"))
+    pa.pa_varlen_forward(w.q, kb, vb, out, w.query_start_loc, w.seq_lens, w.positions,
+                         w.block_tables, w.scale, causal=w.causal,
+                         sliding_window=w.sliding_window)
+    return s, out
+
+
+@pytest.mark.parametrize("case", sorted(STEP_CASES))
+def test_cache_and_attend_equals_the_two_calls(pa, case):
+    w = _step_build(case)
+    kb1, vb1 = w.k_blocks.clone(), w.v_blocks.clone()
+    s1, out1 = _two_calls(pa, w, kb1, vb1)
+    assert pa.pa_device_status() == pa.PA_OK
+    out = torch.full_like(w.q, float("nan"))
+    s = pa.pa_cache_and_attend(w.k_new, w.v_new, w.q, w.k_blocks, w.v_blocks, out,
+                               w.query_start_loc, w.seq_lens, w.positions, w.block_tables,
+                               w.scale, causal=w.causal, sliding_window=w.sliding_window)
+    assert pa.pa_device_status() == pa.PA_OK
+    assert torch.equal(s, s1)
+    assert torch.equal(w.k_blocks, kb1) and torch.equal(w.v_blocks, vb1)
+    assert torch.equal(out, out1)
+
+
+def test_cache_and_attend_failures_leave_out_untouched(pa):
+    w = _step_build("decode-64")
+    w.block_tables[3, 0] = w.num_blocks + 1  # a bad block id: the scatter and the plan fail
+    out = torch.full_like(w.q, 7.0)
+    kb0, vb0 = w.k_blocks.clone(), w.v_blocks.clone()
+    pa.pa_cache_and_attend(w.k_new, w.v_new, w.q, w.k_blocks, w.v_blocks, out,
+                           w.query_start_loc, w.seq_lens, w.positions, w.block_tables, w.scale)
+    assert pa.pa_device_status() == pa.PA_EINVAL
+    assert bool((out == 7.0).all())
+    w = _step_build("decode-64")
+    w.seq_lens[5] = 0  # a context the plan rejects (the slots are fine: the rows are written)
+    out = torch.full_like(w.q, 7.0)
+    pa.pa_cache_and_attend(w.k_new, w.v_new, w.q, w.k_blocks, w.v_blocks, out,
+                           w.query_start_loc, w.seq_lens, w.positions, w.block_tables, w.scale)
+    assert pa.pa_device_status() == pa.PA_EINVAL
+    assert bool((out == 7.0).all())
+    assert pa.pa_device_status() == pa.PA_OK
