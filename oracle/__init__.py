@@ -21,7 +21,10 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "pa_oracle.c")
-_LIB = os.path.join(_HERE, "libpa_oracle.so")
+# PA_ORACLE_SANITIZE=1: an AddressSanitizer + UndefinedBehaviorSanitizer build (the process
+# must preload the ASan runtime; tests/test_oracle_sanitizers.py runs the pins that way)
+_SANITIZE = os.environ.get("PA_ORACLE_SANITIZE") == "1"
+_LIB = os.path.join(_HERE, "libpa_oracle_san.so" if _SANITIZE else "libpa_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -35,6 +38,9 @@ def build(force: bool = False) -> str:
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["gcc", "-std=c11", "-O2", "-fopenmp", "-fPIC", "-shared", "-Wall", "-Wextra",
                "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+        if _SANITIZE:
+            cmd[2:3] = ["-O1", "-g", "-fsanitize=address,undefined", "-fno-sanitize-recover=all",
+                        "-fno-omit-frame-pointer"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
