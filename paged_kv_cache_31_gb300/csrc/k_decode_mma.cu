@@ -61,8 +61,10 @@ struct Geom {
 
 template <int D, int NW, int NS, bool FP8>
 constexpr size_t smem_bytes() {
-  // ring | full barriers | merge m, l | fail flag, work unit ; the O merge area aliases the ring
-  return 1024 + (size_t)NW * NS * Geom<D, FP8>::kStageBytes + NW * NS * 8 + NW * 16 * 4 * 2 + 16;
+  // ring | full barriers, one that no copy signals | merge m, l | fail flag, work unit ; the O
+  // merge area aliases the ring
+  return 1024 + (size_t)NW * NS * Geom<D, FP8>::kStageBytes + (NW * NS + 1) * 8 +
+         NW * 16 * 4 * 2 + 16;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -98,14 +100,15 @@ __global__ void __launch_bounds__(NW * 32, 2)
                                              ~uintptr_t(1023));
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NW * NS * G_::kStageBytes);
-  float* mrg_m = reinterpret_cast<float*>(full + NW * NS);
+  uint64_t* never = full + NW * NS;  // no copy ever signals it (the debug_stall test hook)
+  float* mrg_m = reinterpret_cast<float*>(full + NW * NS + 1);
   float* mrg_l = mrg_m + NW * 16;
   int* fail = reinterpret_cast<int*>(mrg_l + NW * 16);
   float* mrg_o = reinterpret_cast<float*>(ring);  // [NW][16][D + 4], used after the ring drains
   constexpr int kOStride = D + 4;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x < NW * NS) mbar_init(&full[threadIdx.x], 1);
+  if (threadIdx.x <= NW * NS) mbar_init(&full[threadIdx.x], 1);  // the ring's and `never`
   if (threadIdx.x == 0) {
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
@@ -280,7 +283,10 @@ __global__ void __launch_bounds__(NW * 32, 2)
     for (int x = 0; x < my_count; ++x) {
       const uint32_t cnt = ring_pos + x;
       const uint32_t slot = cnt % NS;
-      if (!mbar_wait(&full[warp * NS + slot], (cnt / NS) & 1u, p.wait_limit_ns)) {
+      // debug_stall: the wait names a barrier nothing signals, so it runs out after
+      // wait_limit_ns and the kernel unwinds as from a copy that never landed
+      uint64_t* const wb = p.debug_stall ? never : &full[warp * NS + slot];
+      if (!mbar_wait(wb, p.debug_stall ? 0u : (cnt / NS) & 1u, p.wait_limit_ns)) {
         timed_out = true;
         break;
       }

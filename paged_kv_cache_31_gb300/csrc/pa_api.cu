@@ -118,6 +118,25 @@ bool tc_enabled() {
   return on;
 }
 
+// Test hook of the warp-MMA kernels (PA_DEBUG_STALL_NS=<ns>, read at every call): each of
+// their block waits then names a barrier that no copy signals, with a bound of <ns>, so it
+// runs out and the kernel records PA_ETIMEOUT and unwinds (waiting for its own copies still in
+// flight) exactly as from a copy that never landed.  Unset: real waits, bounded at 4 s.  The
+// tcgen05 kernel has no such hook.
+void mma_waits(Mma16Params& p) {
+  p.wait_limit_ns = kWaitLimitNs;
+  p.debug_stall = 0;
+  const char* v = std::getenv("PA_DEBUG_STALL_NS");
+  if (v && *v) {
+    char* end = nullptr;
+    const unsigned long long x = std::strtoull(v, &end, 10);
+    if (end && *end == 0 && x > 0 && x <= kWaitLimitNs) {
+      p.wait_limit_ns = x;
+      p.debug_stall = 1;
+    }
+  }
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool dtype_ok(pa_dtype t) { return t == PA_F32 || t == PA_BF16; }  // q, out, new rows
 bool pool_dtype_ok(pa_dtype t) { return dtype_ok(t) || t == PA_FP8_E4M3; }
@@ -384,7 +403,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
     p.items_off = L.mma_off;
     p.status = d->status;
     p.scale_log2 = scale * kLog2e;
-    p.wait_limit_ns = kWaitLimitNs;
+    mma_waits(p);
     return from_cuda(
         launch_mma16_varlen_fp8(tk, tv, p, (int)std::min<int64_t>(L.mma_cap, 65535), stream));
   }
@@ -405,7 +424,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
     p.items_off = L.mma_off;
     p.status = d->status;
     p.scale_log2 = scale * kLog2e;
-    p.wait_limit_ns = kWaitLimitNs;
+    mma_waits(p);
     e = launch_mma16_varlen(tk, tv, p, head_dim, (int)std::min<int64_t>(L.mma_cap, 65535),
                             stream);
     if (e != cudaSuccess || !L.use_tc) return from_cuda(e);
@@ -560,7 +579,7 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
     p.tmp_out = tmp_out;
     p.partition_size = partition_size;
     p.max_parts = max_num_partitions;
-    p.wait_limit_ns = kWaitLimitNs;
+    mma_waits(p);
     return from_cuda(fp8 ? launch_mma16_split_fp8(tk, tv, p, stream)
                          : launch_mma16_split(tk, tv, p, head_dim, stream));
   }

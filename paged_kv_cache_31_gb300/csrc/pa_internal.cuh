@@ -312,6 +312,7 @@ struct Mma16Params {
   int32_t partition_size;
   int32_t max_parts;
   uint64_t wait_limit_ns;
+  uint32_t debug_stall;  // tests only: every block wait runs out (see mma_debug_stall)
 };
 
 struct SimtParams {
