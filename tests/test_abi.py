@@ -76,3 +76,49 @@ def test_host_side_argument_errors_need_no_gpu(lib):
     a = b.pa_varlen_forward_workspace_size(4, 27, 4, 2, 64, 4, 16)
     c = b.pa_varlen_forward_workspace_size(256, 4344, 32, 8, 128, 512, 16)
     assert a % 256 == 0 and c % 256 == 0 and c > a > 0
+
+
+def test_host_side_errors_of_the_extended_calls(lib):
+    """The extended entry points' argument errors, also returned before any device work."""
+    from paged_kv_cache_31_gb300 import binding as b
+
+    L = b._lib
+    fake = ctypes.c_void_p(16)  # never dereferenced: every case below returns first
+    # pa_varlen_forward_ex: unknown flag bits, non-positive / non-finite scales
+    for ks, vs, flags in ((1.0, 1.0, 2), (0.0, 1.0, 0), (1.0, -1.0, 0), (float("inf"), 1.0, 0),
+                          (float("nan"), 1.0, 0)):
+        st = L.pa_varlen_forward_ex(None, None, None, None, None, None, None, None, 0, 0, 8, 4,
+                                    128, 16, 8, 1, b.PA_BF16, b.PA_BF16, 1.0, 1, 0, None, None,
+                                    ks, vs, flags, None, 0, None)
+        assert st == b.PA_EINVAL, (ks, vs, flags)
+    # fp8 is a pool type only
+    st = L.pa_varlen_forward_ex(None, None, None, None, None, None, None, None, 0, 0, 8, 4, 128,
+                                16, 8, 1, b.PA_FP8_E4M3, b.PA_FP8_E4M3, 1.0, 1, 0, None, None,
+                                1.0, 1.0, 0, None, 0, None)
+    assert st == b.PA_EUNSUPPORTED
+    # pa_reshape_and_cache_ex: fp8 new rows are not a source type; bad scales
+    st = L.pa_reshape_and_cache_ex(None, None, None, None, None, 0, 2, 128, 16, 8, b.PA_FP8_E4M3,
+                                   b.PA_FP8_E4M3, 1.0, 1.0, None)
+    assert st == b.PA_EUNSUPPORTED
+    st = L.pa_reshape_and_cache_ex(None, None, None, None, None, 0, 2, 128, 16, 8, b.PA_BF16,
+                                   b.PA_FP8_E4M3, 0.0, 1.0, None)
+    assert st == b.PA_EINVAL
+    # slots are int32: a pool of more than 2^31 - 1 slots is refused
+    big_nb = (1 << 31) // 16 + 1
+    st = L.pa_slot_mapping(fake, fake, fake, 1, 1, 1, 16, big_nb, fake, None)
+    assert st == b.PA_EUNSUPPORTED
+    st = L.pa_slot_mapping_and_cache(fake, fake, fake, fake, fake, fake, fake, 1, 1, 1, 2, 128,
+                                     16, big_nb, b.PA_BF16, fake, None)
+    assert st == b.PA_EUNSUPPORTED
+    st = L.pa_cache_and_attend(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1, 1, 8,
+                               2, 128, 16, big_nb, 1, b.PA_BF16, b.PA_BF16, 1.0, 1, 0, fake, fake,
+                               1 << 20, None)
+    assert st == b.PA_EUNSUPPORTED
+    # missing new rows
+    st = L.pa_cache_and_attend(None, None, fake, fake, fake, fake, fake, fake, fake, fake, 1, 1, 8,
+                               2, 128, 16, 8, 1, b.PA_BF16, b.PA_BF16, 1.0, 1, 0, None, fake,
+                               1 << 20, None)
+    assert st == b.PA_EINVAL
+    # empty steps are a no-op
+    assert L.pa_slot_mapping_and_cache(None, None, None, None, None, None, None, 0, 0, 0, 2, 128,
+                                       16, 8, b.PA_BF16, None, None) == b.PA_OK

@@ -78,6 +78,22 @@ def test_fused_equals_oracle_and_separate_calls(pa, case):
     assert torch.equal(s1, slots) and torch.equal(kb1, w.k_blocks) and torch.equal(vb1, w.v_blocks)
 
 
+@pytest.mark.parametrize("S,q", [(1024, 2), (683, 3), (2047, 1), (2048, 1)])
+def test_fused_at_its_limits(pa, S, q):
+    # 2048 tokens and 2047 sequences take the one-launch kernel; 2049 tokens (683 x 3) or 2048
+    # sequences take the two launches
+    lens = [q + (7 * i) % 60 for i in range(S)]
+    w = workloads.build("limits", seq_lens=lens, q_lens=[q] * S, num_heads=4, num_kv_heads=2,
+                        head_dim=32, seed=S + q, device=DEV)
+    kb0, vb0 = w.k_blocks.clone(), w.v_blocks.clone()
+    slots = pa.pa_slot_mapping_and_cache(w.k_new, w.v_new, w.k_blocks, w.v_blocks,
+                                         w.query_start_loc, w.positions, w.block_tables)
+    assert pa.pa_device_status() == pa.PA_OK
+    oslots, okb, ovb = _oracle(w, kb0, vb0)
+    assert torch.equal(slots.cpu(), oslots)
+    assert torch.equal(w.k_blocks.cpu(), okb) and torch.equal(w.v_blocks.cpu(), ovb)
+
+
 def test_fused_fp8_rows(pa):
     w = workloads.build("fp8", seq_lens=[9, 40], q_lens=[9, 3], num_heads=3, num_kv_heads=3,
                         head_dim=7, seed=8, device=DEV)

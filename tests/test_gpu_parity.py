@@ -92,6 +92,21 @@ def test_varlen_shapes(pa, kw):
     assert_attn_close(out, oracle_attention(w, okb, ovb), str(kw))
 
 
+@pytest.mark.parametrize("kw", [
+    dict(head_dim=256, num_heads=4, num_kv_heads=2),                     # largest head size
+    dict(head_dim=32, num_heads=8, num_kv_heads=2),                      # small head size
+    dict(head_dim=128, num_heads=8, num_kv_heads=2, block_size=8),       # small blocks
+    dict(head_dim=64, num_heads=4, num_kv_heads=2, block_size=64),       # large blocks
+    dict(head_dim=128, num_heads=64, num_kv_heads=1),                    # G = 64: 2 tokens per
+])                                                                       # tcgen05 query tile
+def test_varlen_extreme_shapes(pa, kw):
+    lens, qlens = [1, 64, 65, 300, 129], [1, 64, 40, 70, 1]
+    w = workloads.build("extreme", seq_lens=lens, q_lens=qlens, seed=7, device=DEV, **kw)
+    slots, kb, vb, out = _step(pa, w)
+    okb, ovb = _oracle_cache(w, slots)
+    assert_attn_close(out, oracle_attention(w, okb, ovb), str(kw))
+
+
 def test_varlen_fp32_query_bf16_pool(pa):
     w = workloads.build("mix", seq_lens=[40, 90], q_lens=[3, 1], num_heads=4, num_kv_heads=2,
                         head_dim=64, seed=9, device=DEV)
