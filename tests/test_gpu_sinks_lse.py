@@ -125,3 +125,27 @@ def test_huge_sink_drains_the_output(pa):
     out, lse = _gpu(pa, w, sinks)
     assert out.float().abs().max().item() < 1e-6
     assert torch.allclose(lse.cpu(), torch.full_like(lse.cpu(), 60.0), atol=1e-4)
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_scaled_wide_pools_match_oracle(pa, case):
+    # k_scale / v_scale on bf16 and f32 pools (every kernel folds k_scale into the softmax scale
+    # and v_scale into the output), with sinks and lse, against the oracle
+    kw = dict(CASES[case])
+    w = workloads.build(case, seed=sorted(CASES).index(case) + 71, device=DEV, **kw)
+    sinks = _sinks(w.num_heads, 9)
+    out = torch.full_like(w.q, float("nan"))
+    lse = torch.full((w.num_heads, w.num_tokens), float("nan"), device=DEV)
+    pa.pa_varlen_forward(w.q, w.k_blocks, w.v_blocks, out, w.query_start_loc, w.seq_lens,
+                         w.positions, w.block_tables, w.scale, causal=w.causal,
+                         sliding_window=w.sliding_window, sinks=sinks.to(DEV), lse=lse,
+                         k_scale=0.7, v_scale=1.9)
+    assert pa.pa_device_status() == pa.PA_OK
+    st, ref, ref_lse = oracle.varlen_attention(w.q.cpu(), w.k_blocks.cpu(), w.v_blocks.cpu(),
+                                               w.query_start_loc, w.seq_lens, w.positions,
+                                               w.block_tables, w.scale, causal=w.causal,
+                                               sliding_window=w.sliding_window, want_lse=True,
+                                               sinks=sinks, k_scale=0.7, v_scale=1.9)
+    assert st == oracle.OK
+    assert_attn_close(out, ref, f"{case} scaled out")
+    _assert_lse_close(lse, ref_lse, f"{case} scaled lse")
