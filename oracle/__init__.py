@@ -73,6 +73,14 @@ def lib():
             L.oracle_splitkv_partials_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                                      i32, i32, i64, i32, i32, i32, i32, i32, f32,
                                                      i32, f32, f32]
+            L.oracle_reshape_and_cache_per_head.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32,
+                                                            i32, i64, i32, i32, vp, vp]
+            L.oracle_varlen_attention_per_head.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                           i64, i32, i32, i32, i32, i64, i32, i32,
+                                                           i32, i32, f32, i32, i32, vp, vp, vp]
+            L.oracle_splitkv_partials_per_head.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                           i32, i32, i32, i32, i64, i32, i32, i32,
+                                                           i32, i32, f32, i32, vp, vp]
             L.oracle_splitkv_reduce.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
             L.oracle_merge_attn_states.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i32]
             L.oracle_fp8_to_f32.argtypes = [ctypes.c_uint8]
@@ -85,7 +93,8 @@ def lib():
             L.oracle_f32_to_bf16.restype = ctypes.c_uint16
             for name in ("oracle_slot_mapping", "oracle_reshape_and_cache", "oracle_gather_kv",
                          "oracle_varlen_attention", "oracle_varlen_attention_ex",
-                         "oracle_reshape_and_cache_ex",
+                         "oracle_reshape_and_cache_ex", "oracle_reshape_and_cache_per_head",
+                         "oracle_varlen_attention_per_head", "oracle_splitkv_partials_per_head",
                          "oracle_splitkv_partials", "oracle_splitkv_partials_ex",
                          "oracle_splitkv_reduce",
                          "oracle_merge_attn_states"):
@@ -153,6 +162,24 @@ def reshape_and_cache_ex(k, v, k_blocks, v_blocks, slot_mapping_, block_size, k_
                                              float(v_scale))
 
 
+def reshape_and_cache_per_head(k, v, k_blocks, v_blocks, slot_mapping_, block_size, k_scales,
+                               v_scales):
+    """Scatter with conversion and one scale per kv head: head g of a row is stored as
+    k / k_scales[g], v / v_scales[g] (None: 1 for every head)."""
+    k, v, sm = _cpu(k), _cpu(v), _cpu(slot_mapping_)
+    ksc, vsc = _scales(k_scales), _scales(v_scales)
+    assert k_blocks.is_contiguous() and v_blocks.is_contiguous()
+    T, Hkv, D = k.shape
+    return lib().oracle_reshape_and_cache_per_head(_p(k), _p(v), _p(k_blocks), _p(v_blocks),
+                                                   _p(sm), T, Hkv, D, block_size,
+                                                   k_blocks.shape[0], _DT[k.dtype],
+                                                   _DT[k_blocks.dtype], _p(ksc), _p(vsc))
+
+
+def _scales(x):
+    return None if x is None else _cpu(x).to(torch.float32).contiguous()
+
+
 def reshape_and_cache(k, v, k_blocks, v_blocks, slot_mapping_, block_size):
     """Scatter in place into (CPU) k_blocks / v_blocks."""
     k, v, sm = _cpu(k), _cpu(v), _cpu(slot_mapping_)
@@ -177,10 +204,11 @@ def gather_kv(k_blocks, v_blocks, cu_seq_lens, block_tables, seq_starts=None):
 def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions, block_tables,
                      scale, causal=True, sliding_window=0, out_dtype=torch.float32,
                      want_lse=False, num_kv_heads=None, out=None, sinks=None, k_scale=1.0,
-                     v_scale=1.0):
+                     v_scale=1.0, k_scales=None, v_scales=None):
     """Two-pass attention of every (token, head).  Returns (status, out [T,H,D], lse [H,T]).
     sinks: optional [H] fp32 sink logits (a virtual zero-valued position per head);
-    k_scale / v_scale: dequantisation scales of the pool (K = k_scale * pool)."""
+    k_scale / v_scale: dequantisation scales of the pool (K = k_scale * pool);
+    k_scales / v_scales: one scale per kv head instead (K = k_scales[g] * pool)."""
     q, kb, vb = _cpu(q), _cpu(k_blocks), _cpu(v_blocks)
     qsl, sl, pos, bt = _cpu(query_start_loc), _cpu(seq_lens), _cpu(positions), _cpu(block_tables)
     T, H, D = q.shape
@@ -191,30 +219,37 @@ def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions
         out = torch.zeros((T, H, D), dtype=out_dtype)
     lse = torch.full((H, T), float("nan"), dtype=torch.float32) if want_lse else None
     sk = None if sinks is None else _cpu(sinks).to(torch.float32).contiguous()
-    st = lib().oracle_varlen_attention_ex(_p(q), _p(kb), _p(vb), _p(out), _p(lse), _p(qsl),
-                                          _p(sl), _p(pos), _p(bt), qsl.numel() - 1, T, H, Hkv, D,
-                                          bs, NB, bt.shape[1], _DT[q.dtype], _DT[kb.dtype],
-                                          _DT[out.dtype], float(scale), int(bool(causal)),
-                                          int(sliding_window), _p(sk), float(k_scale),
-                                          float(v_scale))
+    args = (_p(q), _p(kb), _p(vb), _p(out), _p(lse), _p(qsl), _p(sl), _p(pos), _p(bt),
+            qsl.numel() - 1, T, H, Hkv, D, bs, NB, bt.shape[1], _DT[q.dtype], _DT[kb.dtype],
+            _DT[out.dtype], float(scale), int(bool(causal)), int(sliding_window), _p(sk))
+    if k_scales is not None or v_scales is not None:
+        ksc, vsc = _scales(k_scales), _scales(v_scales)
+        st = lib().oracle_varlen_attention_per_head(*args, _p(ksc), _p(vsc))
+    else:
+        st = lib().oracle_varlen_attention_ex(*args, float(k_scale), float(v_scale))
     return st, out, lse
 
 
 def splitkv_partials(q, k_blocks, v_blocks, seq_lens, block_tables, scale, partition_size,
-                     max_parts, sliding_window=0, k_scale=1.0, v_scale=1.0):
+                     max_parts, sliding_window=0, k_scale=1.0, v_scale=1.0, k_scales=None,
+                     v_scales=None):
     """Phase 1 of split-KV decode: (status, max_logits, exp_sums, tmp_out).  k_scale / v_scale:
-    dequantisation scales of the pool (K = k_scale * pool)."""
+    dequantisation scales of the pool (K = k_scale * pool); k_scales / v_scales: one per kv
+    head instead."""
     q, kb, vb, sl, bt = _cpu(q), _cpu(k_blocks), _cpu(v_blocks), _cpu(seq_lens), _cpu(block_tables)
     S, H, D = q.shape
     NB, bs, Hkv, _ = kb.shape
     ml = torch.full((S, H, max_parts), float("nan"), dtype=torch.float32)
     es = torch.full((S, H, max_parts), float("nan"), dtype=torch.float32)
     to = torch.full((S, H, max_parts, D), float("nan"), dtype=torch.float32)
-    st = lib().oracle_splitkv_partials_ex(_p(q), _p(kb), _p(vb), _p(ml), _p(es), _p(to), _p(sl),
-                                          _p(bt), S, H, Hkv, D, bs, NB, bt.shape[1],
-                                          partition_size, max_parts, _DT[q.dtype], _DT[kb.dtype],
-                                          float(scale), int(sliding_window), float(k_scale),
-                                          float(v_scale))
+    args = (_p(q), _p(kb), _p(vb), _p(ml), _p(es), _p(to), _p(sl), _p(bt), S, H, Hkv, D, bs, NB,
+            bt.shape[1], partition_size, max_parts, _DT[q.dtype], _DT[kb.dtype], float(scale),
+            int(sliding_window))
+    if k_scales is not None or v_scales is not None:
+        st = lib().oracle_splitkv_partials_per_head(*args, _p(_scales(k_scales)),
+                                                    _p(_scales(v_scales)))
+    else:
+        st = lib().oracle_splitkv_partials_ex(*args, float(k_scale), float(v_scale))
     return st, ml, es, to
 
 

@@ -29,6 +29,7 @@
  * Mutants: oracle_set_mutant(n) plants one known mistake (n > 0) so the tests can
  * show each pin fails on it.  0 (the default) is the correct oracle.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -41,7 +42,8 @@
  * section 2.6: TL_EUNSUPPORTED). */
 enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_ESHAPE = 2, ORC_EUNSUPPORTED = 3 };
 /* Element types the pages use for q / K / V / out ([MLA] LoadF/StoreF), and fp8 (e4m3) K/V
- * pools ([V2] kv_cache_dtype "fp8" with k_scale / v_scale; [TL] "Going further": fp8 KV). */
+ * pools ([V2] kv_cache_dtype "fp8" with k_scale / v_scale; [TL] "Going further": fp8 KV, with
+ * scales per head or per block -- the *_per_head functions take one scale per kv head). */
 enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8 = 2 };
 
 static int g_mutant = 0;
@@ -215,14 +217,29 @@ int oracle_reshape_and_cache(const void* k, const void* v, void* k_blocks, void*
 /* ---- scatter with conversion: new rows of src_dtype into a pool of kv_dtype, the pool
  * holding x / k_scale (x / v_scale) rounded to its type; for an fp8 pool that is the e4m3
  * code of the quotient (saturated, round to nearest even).  Every slot is checked first. */
-int oracle_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, void* v_blocks,
-                                const int32_t* slot_mapping, int64_t num_tokens,
-                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                int64_t num_blocks, int32_t src_dtype, int32_t kv_dtype,
-                                float k_scale, float v_scale) {
+/* Per kv head scales: k_scales / v_scales hold num_kv_heads factors (NULL: the scalar for
+ * every head); each must be finite and > 0. */
+static int head_scales_ok(const float* s, int32_t n) {
+  if (!s) return 1;
+  for (int32_t g = 0; g < n; ++g)
+    if (!(s[g] > 0.f && s[g] <= FLT_MAX)) return 0;
+  return 1;
+}
+static float head_scale(const float* s, int32_t g, int32_t num_kv_heads, float scalar) {
+  if (!s) return scalar;
+  return MUTANT(75) ? s[0] : s[g % num_kv_heads];
+}
+
+static int scatter_convert(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                           const int32_t* slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                           int32_t src_dtype, int32_t kv_dtype, const float* k_scales,
+                           const float* v_scales, float k_scale, float v_scale) {
   if (!k || !v || !k_blocks || !v_blocks || !slot_mapping) return ORC_EINVAL;
   if (!dtype_ok(src_dtype) || !pool_dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
   if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return ORC_ESHAPE;
+  if (!head_scales_ok(k_scales, num_kv_heads) || !head_scales_ok(v_scales, num_kv_heads))
+    return ORC_EINVAL;
   for (int64_t t = 0; t < num_tokens; ++t) {
     int64_t slot = slot_mapping[t];
     if (slot < 0 || slot >= num_blocks * block_size) return ORC_EINVAL;
@@ -231,11 +248,37 @@ int oracle_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, vo
   for (int64_t t = 0; t < num_tokens; ++t) {
     const int64_t slot = slot_mapping[t];
     for (int64_t i = 0; i < row; ++i) {
-      store_elem(k_blocks, kv_dtype, slot * row + i, load_elem(k, src_dtype, t * row + i) / k_scale);
-      store_elem(v_blocks, kv_dtype, slot * row + i, load_elem(v, src_dtype, t * row + i) / v_scale);
+      const int32_t g = (int32_t)(i / head_dim);
+      const float ks = head_scale(k_scales, g, num_kv_heads, k_scale);
+      const float vs = head_scale(v_scales, g, num_kv_heads, v_scale);
+      store_elem(k_blocks, kv_dtype, slot * row + i, load_elem(k, src_dtype, t * row + i) / ks);
+      store_elem(v_blocks, kv_dtype, slot * row + i, load_elem(v, src_dtype, t * row + i) / vs);
     }
   }
   return ORC_OK;
+}
+
+int oracle_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, void* v_blocks,
+                                const int32_t* slot_mapping, int64_t num_tokens,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                int64_t num_blocks, int32_t src_dtype, int32_t kv_dtype,
+                                float k_scale, float v_scale) {
+  return scatter_convert(k, v, k_blocks, v_blocks, slot_mapping, num_tokens, num_kv_heads,
+                         head_dim, block_size, num_blocks, src_dtype, kv_dtype, NULL, NULL,
+                         k_scale, v_scale);
+}
+
+/* The same with one scale per kv head: head g of a new row is stored as x / k_scales[g]
+ * (x / v_scales[g]).  A scale that is not finite and positive is EINVAL, before any write. */
+int oracle_reshape_and_cache_per_head(const void* k, const void* v, void* k_blocks,
+                                      void* v_blocks, const int32_t* slot_mapping,
+                                      int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int64_t num_blocks, int32_t src_dtype,
+                                      int32_t kv_dtype, const float* k_scales,
+                                      const float* v_scales) {
+  return scatter_convert(k, v, k_blocks, v_blocks, slot_mapping, num_tokens, num_kv_heads,
+                         head_dim, block_size, num_blocks, src_dtype, kv_dtype, k_scales,
+                         v_scales, 1.f, 1.f);
 }
 
 /* ---- gather of a sequence's rows into a dense buffer ([MLA] GatherMlaCache) --
@@ -393,15 +436,18 @@ static int validate_varlen(const void* q, const void* k_blocks, const void* v_bl
 /* sinks: [num_heads] sink logits on the score scale ([MPA] ForwardWithSinks), or NULL.
  * k_scale / v_scale: the pool holds K / k_scale and V / v_scale ([V2]: "k_flat.float()
  * .mul_(k_scale)"), so attention uses K = k_scale * pool and V = v_scale * pool. */
-int oracle_varlen_attention_ex(const void* q, const void* k_blocks, const void* v_blocks,
-                               void* out, float* lse, const int32_t* query_start_loc,
-                               const int32_t* seq_lens, const int32_t* positions,
-                               const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
-                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                               int32_t block_size, int64_t num_blocks, int32_t max_blocks,
-                               int32_t q_dtype, int32_t kv_dtype, int32_t out_dtype, float scale,
-                               int32_t causal, int32_t sliding_window, const float* sinks,
-                               float k_scale, float v_scale) {
+static int varlen_core(const void* q, const void* k_blocks, const void* v_blocks, void* out,
+                       float* lse, const int32_t* query_start_loc, const int32_t* seq_lens,
+                       const int32_t* positions, const int32_t* block_tables, int32_t num_seqs,
+                       int64_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                       int32_t max_blocks, int32_t q_dtype, int32_t kv_dtype, int32_t out_dtype,
+                       float scale, int32_t causal, int32_t sliding_window, const float* sinks,
+                       const float* k_scales, const float* v_scales, float k_scale,
+                       float v_scale) {
+  if (num_kv_heads > 0 &&
+      (!head_scales_ok(k_scales, num_kv_heads) || !head_scales_ok(v_scales, num_kv_heads)))
+    return ORC_EINVAL;
   int st = validate_varlen(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                            block_tables, num_seqs, num_tokens, num_heads, num_kv_heads,
                            head_dim, block_size, num_blocks, max_blocks, q_dtype, kv_dtype);
@@ -434,11 +480,14 @@ int oracle_varlen_attention_ex(const void* q, const void* k_blocks, const void* 
       int64_t win = MUTANT(6) ? (int64_t)sliding_window + 1 : sliding_window; /* s06 */
       int64_t start = sliding_window > 0 ? (end - win > 0 ? end - win : 0) : 0;
       const int32_t* row = block_tables + (int64_t)s * max_blocks;
+      const int32_t gs = MUTANT(74) ? h % num_kv_heads : g; /* s74: the query head's scale */
       float l_lse = attend_two_pass(q, (t * num_heads + h) * (int64_t)head_dim, q_dtype, k_blocks,
                                     v_blocks, kv_dtype, row, start, end, block_size, num_kv_heads,
                                     head_dim, g, scale, logits, acc, out,
                                     (t * num_heads + h) * (int64_t)head_dim, out_dtype, NULL, NULL,
-                                    sinks ? sinks[h] : -INFINITY, k_scale, v_scale);
+                                    sinks ? sinks[h] : -INFINITY,
+                                    head_scale(k_scales, gs, num_kv_heads, k_scale),
+                                    head_scale(v_scales, gs, num_kv_heads, v_scale));
       if (lse) lse[(int64_t)h * num_tokens + t] = l_lse;
     }
     free(logits);
@@ -446,6 +495,40 @@ int oracle_varlen_attention_ex(const void* q, const void* k_blocks, const void* 
   }
   free(tok_seq);
   return ORC_OK;
+}
+
+int oracle_varlen_attention_ex(const void* q, const void* k_blocks, const void* v_blocks,
+                               void* out, float* lse, const int32_t* query_start_loc,
+                               const int32_t* seq_lens, const int32_t* positions,
+                               const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
+                               int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t num_blocks, int32_t max_blocks,
+                               int32_t q_dtype, int32_t kv_dtype, int32_t out_dtype, float scale,
+                               int32_t causal, int32_t sliding_window, const float* sinks,
+                               float k_scale, float v_scale) {
+  return varlen_core(q, k_blocks, v_blocks, out, lse, query_start_loc, seq_lens, positions,
+                     block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, max_blocks, q_dtype, kv_dtype, out_dtype, scale,
+                     causal, sliding_window, sinks, NULL, NULL, k_scale, v_scale);
+}
+
+/* One dequantisation scale per kv head: query head h (kv head g = h / G) attends over
+ * K = k_scales[g] * pool and V = v_scales[g] * pool (NULL arrays: 1).  A scale that is not
+ * finite and positive is EINVAL. */
+int oracle_varlen_attention_per_head(const void* q, const void* k_blocks, const void* v_blocks,
+                                     void* out, float* lse, const int32_t* query_start_loc,
+                                     const int32_t* seq_lens, const int32_t* positions,
+                                     const int32_t* block_tables, int32_t num_seqs,
+                                     int64_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                     int32_t max_blocks, int32_t q_dtype, int32_t kv_dtype,
+                                     int32_t out_dtype, float scale, int32_t causal,
+                                     int32_t sliding_window, const float* sinks,
+                                     const float* k_scales, const float* v_scales) {
+  return varlen_core(q, k_blocks, v_blocks, out, lse, query_start_loc, seq_lens, positions,
+                     block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, max_blocks, q_dtype, kv_dtype, out_dtype, scale,
+                     causal, sliding_window, sinks, k_scales, v_scales, 1.f, 1.f);
 }
 
 int oracle_varlen_attention(const void* q, const void* k_blocks, const void* v_blocks,
@@ -474,20 +557,23 @@ int oracle_varlen_attention(const void* q, const void* k_blocks, const void* v_b
  * position, including those at or past ceil(seq_len / P), get (-inf, 0, zeros).
  * k_scale / v_scale: the pools hold K / k_scale and V / v_scale, possibly as fp8
  * ([V2]: kv_cache_dtype, "Apply scales" before the partition loop). */
-int oracle_splitkv_partials_ex(const void* q, const void* k_blocks, const void* v_blocks,
-                               float* max_logits, float* exp_sums, float* tmp_out,
-                               const int32_t* seq_lens, const int32_t* block_tables,
-                               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
-                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
-                               int32_t max_blocks, int32_t partition_size, int32_t max_parts,
-                               int32_t q_dtype, int32_t kv_dtype, float scale,
-                               int32_t sliding_window, float k_scale, float v_scale) {
+static int splitkv_core(const void* q, const void* k_blocks, const void* v_blocks,
+                        float* max_logits, float* exp_sums, float* tmp_out,
+                        const int32_t* seq_lens, const int32_t* block_tables, int32_t num_seqs,
+                        int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int64_t num_blocks, int32_t max_blocks,
+                        int32_t partition_size, int32_t max_parts, int32_t q_dtype,
+                        int32_t kv_dtype, float scale, int32_t sliding_window,
+                        const float* k_scales, const float* v_scales, float k_scale,
+                        float v_scale) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0 || partition_size <= 0 || max_parts <= 0)
     return ORC_ESHAPE;
   if (!dtype_ok(q_dtype) || !pool_dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
   if (!q || !k_blocks || !v_blocks || !max_logits || !exp_sums || !tmp_out || !seq_lens ||
       !block_tables)
+    return ORC_EINVAL;
+  if (!head_scales_ok(k_scales, num_kv_heads) || !head_scales_ok(v_scales, num_kv_heads))
     return ORC_EINVAL;
   int64_t max_ctx = 1;
   for (int32_t s = 0; s < num_seqs; ++s) {
@@ -523,7 +609,9 @@ int oracle_splitkv_partials_ex(const void* q, const void* k_blocks, const void* 
       attend_two_pass(q, ((int64_t)s * num_heads + h) * head_dim, q_dtype, k_blocks, v_blocks,
                       kv_dtype, block_tables + (int64_t)s * max_blocks, lo, hi, block_size,
                       num_kv_heads, head_dim, h / group, scale, logits, acc, tmp_out,
-                      idx * head_dim, ORC_F32, &m, &l, -INFINITY, k_scale, v_scale);
+                      idx * head_dim, ORC_F32, &m, &l, -INFINITY,
+                      head_scale(k_scales, h / group, num_kv_heads, k_scale),
+                      head_scale(v_scales, h / group, num_kv_heads, v_scale));
       max_logits[idx] = m;
       exp_sums[idx] = l;
     }
@@ -531,6 +619,37 @@ int oracle_splitkv_partials_ex(const void* q, const void* k_blocks, const void* 
     free(acc);
   }
   return ORC_OK;
+}
+
+int oracle_splitkv_partials_ex(const void* q, const void* k_blocks, const void* v_blocks,
+                               float* max_logits, float* exp_sums, float* tmp_out,
+                               const int32_t* seq_lens, const int32_t* block_tables,
+                               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                               int32_t max_blocks, int32_t partition_size, int32_t max_parts,
+                               int32_t q_dtype, int32_t kv_dtype, float scale,
+                               int32_t sliding_window, float k_scale, float v_scale) {
+  return splitkv_core(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
+                      block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, max_blocks, partition_size, max_parts, q_dtype, kv_dtype, scale,
+                      sliding_window, NULL, NULL, k_scale, v_scale);
+}
+
+/* Split-KV partials with one scale per kv head (NULL arrays: 1; not finite and positive:
+ * EINVAL). */
+int oracle_splitkv_partials_per_head(const void* q, const void* k_blocks, const void* v_blocks,
+                                     float* max_logits, float* exp_sums, float* tmp_out,
+                                     const int32_t* seq_lens, const int32_t* block_tables,
+                                     int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                     int32_t max_blocks, int32_t partition_size,
+                                     int32_t max_parts, int32_t q_dtype, int32_t kv_dtype,
+                                     float scale, int32_t sliding_window, const float* k_scales,
+                                     const float* v_scales) {
+  return splitkv_core(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
+                      block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, max_blocks, partition_size, max_parts, q_dtype, kv_dtype, scale,
+                      sliding_window, k_scales, v_scales, 1.f, 1.f);
 }
 
 int oracle_splitkv_partials(const void* q, const void* k_blocks, const void* v_blocks,

@@ -741,7 +741,80 @@ def pin_bf16_codec():
         assert got == float(ref), hex(bits)
 
 
+# --------------------------------------------------------------------------------------------
+# one dequantisation scale per kv head (tinyllm "Going further": fp8 KV caches with scales per
+# head or per block)
+
+
+def pin_per_head_scatter():
+    # head g of every new row holds x / k_scales[g]: torch's e4m3 code of the IEEE quotient
+    # (clamped to +-448) in an fp8 pool, the quotient itself in an fp32 pool
+    g = torch.Generator().manual_seed(75)
+    T, Hkv, D, b, NB = 20, 3, 16, 16, 4
+    k = (torch.randn((T, Hkv, D), generator=g) * 3).to(torch.bfloat16)
+    v = (torch.randn((T, Hkv, D), generator=g) * 50).to(torch.bfloat16)
+    ks = torch.tensor([0.0625, 0.5, 2.0])
+    vs = torch.tensor([0.37, 0.11, 1.3])
+    slots = torch.randperm(NB * b, generator=g)[:T].to(torch.int32)
+    for dt in (torch.float8_e4m3fn, torch.float32):
+        kb = torch.zeros((NB, b, Hkv, D), dtype=dt)
+        vb = torch.zeros_like(kb)
+        assert oracle.reshape_and_cache_per_head(k, v, kb, vb, slots, b, ks, vs) == oracle.OK
+        for t in range(T):
+            sl = int(slots[t])
+            wk, wv = k[t].float() / ks[:, None], v[t].float() / vs[:, None]
+            if dt == torch.float8_e4m3fn:
+                wk = torch.clamp(wk, -448, 448).to(dt).view(torch.uint8)
+                wv = torch.clamp(wv, -448, 448).to(dt).view(torch.uint8)
+                gk, gv = kb[sl // b, sl % b].view(torch.uint8), vb[sl // b, sl % b].view(torch.uint8)
+            else:
+                gk, gv = kb[sl // b, sl % b], vb[sl // b, sl % b]
+            assert torch.equal(gk, wk) and torch.equal(gv, wv)
+    # a scale that is not finite and positive: EINVAL, nothing written
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        ks2 = ks.clone()
+        ks2[1] = bad
+        kb = torch.zeros((NB, b, Hkv, D), dtype=torch.float32)
+        vb = torch.zeros_like(kb)
+        assert oracle.reshape_and_cache_per_head(k, v, kb, vb, slots, b, ks2, vs) == oracle.EINVAL
+        assert not kb.any() and not vb.any()
+
+
+def pin_per_head_attention():
+    # per kv head scales on an fp8 pool equal, bit for bit, the unscaled attention over the fp32
+    # pool holding k_scales[g] * value(code) (torch's e4m3 decoding, one fp32 product), with
+    # GQA 3 so that query head h reads kv head h // 3; the same for the split-KV partials
+    H, Hkv, D, lens, qsl, pos, q, kb8, vb8, table = _fp8_case(seed=76)
+    ks, vs = torch.tensor([0.25, 0.6]), torch.tensor([0.37, 1.7])
+    kbf = kb8.float() * ks.view(1, 1, Hkv, 1)
+    vbf = vb8.float() * vs.view(1, 1, Hkv, 1)
+    meta = dict(query_start_loc=_t(qsl), seq_lens=_t(lens), positions=_t(pos),
+                block_tables=table, scale=1.0 / math.sqrt(D), want_lse=True)
+    for window in (0, 20):
+        st, o1, l1 = oracle.varlen_attention(q, kb8, vb8, sliding_window=window, k_scales=ks,
+                                             v_scales=vs, **meta)
+        st2, o2, l2 = oracle.varlen_attention(q, kbf, vbf, sliding_window=window, **meta)
+        assert st == oracle.OK and st2 == oracle.OK
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # one decode query per sequence for the partials
+    qd = torch.stack([q[qsl[s + 1] - 1] for s in range(len(lens))])
+    a = oracle.splitkv_partials(qd, kb8, vb8, _t(lens), table, 1.0 / math.sqrt(D), 16, 8,
+                                k_scales=ks, v_scales=vs)
+    b = oracle.splitkv_partials(qd, kbf, vbf, _t(lens), table, 1.0 / math.sqrt(D), 16, 8)
+    assert a[0] == oracle.OK and b[0] == oracle.OK
+    for x, y in zip(a[1:], b[1:]):
+        assert torch.equal(x, y)
+    # an invalid scale is EINVAL
+    for bad in (0.0, float("nan")):
+        ks2 = ks.clone()
+        ks2[0] = bad
+        st, _, _ = oracle.varlen_attention(q, kb8, vb8, k_scales=ks2, v_scales=vs, **meta)
+        assert st == oracle.EINVAL
+
+
 ALL_PINS = {
+    "per_head_scatter": pin_per_head_scatter,
+    "per_head_attention": pin_per_head_attention,
     "fp8_codec": pin_fp8_codec,
     "fp8_scatter": pin_fp8_scatter,
     "fp8_attention_brute_force": pin_fp8_attention_brute_force,

@@ -8,7 +8,8 @@ block ids trusted) and further plausible slips in the scatter, gather, score,
 split-KV reduction and merge arithmetic, and in the attention-sink term (s60 the sink
 left out of the exp-sum, s61 its term taken as 1 instead of e^(sink - m)) and the fp8 pools
 (s70 a wrong exponent bias, s71 truncation instead of rounding, s72 / s73 a dequantisation
-scale ignored).
+scale ignored), and the per kv head scales (s74 the query head's index taken for the kv
+head's, s75 the first head's scale used for every head).
 """
 import pytest
 
@@ -43,6 +44,8 @@ KILLERS = {
     71: ["fp8_codec", "fp8_scatter"],
     72: ["fp8_attention_brute_force", "dequant_scales", "splitkv_fp8_scaled"],
     73: ["fp8_attention_brute_force", "dequant_scales", "splitkv_fp8_scaled"],
+    74: ["per_head_attention"],
+    75: ["per_head_scatter", "per_head_attention"],
 }
 
 
