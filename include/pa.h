@@ -137,6 +137,22 @@ pa_status pa_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, 
                                   float k_scale, float v_scale, cudaStream_t stream);
 
 /*
+ * pa_reshape_and_cache_per_head -- pa_reshape_and_cache_ex with one dequantisation scale per
+ * kv head (tinyllm "Going further": fp8 KV caches with scales per head): head g of a new row
+ * is stored as x / k_scales[g] (x / v_scales[g]).  k_scales, v_scales: DEVICE arrays of
+ * num_kv_heads floats owned by the caller, or NULL for 1 on every head.  A scale that is not
+ * finite and positive is recorded as PA_EINVAL in the device status (it is only read on the
+ * device) and nothing is written; other errors as pa_reshape_and_cache_ex.
+ */
+pa_status pa_reshape_and_cache_per_head(const void* k, const void* v, void* k_blocks,
+                                        void* v_blocks, const int32_t* slot_mapping,
+                                        int64_t num_tokens, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                        pa_dtype src_dtype, pa_dtype kv_dtype,
+                                        const float* k_scales, const float* v_scales,
+                                        cudaStream_t stream);
+
+/*
  * pa_varlen_forward_workspace_size -- bytes of device workspace pa_varlen_forward needs
  * for these sizes (the per-call plan of work items and split-KV partial states).
  */
@@ -220,6 +236,28 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
                                const float* sinks, float* lse, float k_scale, float v_scale,
                                uint32_t flags, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
+
+/*
+ * pa_varlen_forward_per_head -- pa_varlen_forward_ex with one dequantisation scale per kv
+ * head instead of one per pool: query head h (kv head g = h / (num_heads / num_kv_heads))
+ * attends over K = k_scales[g] * k_blocks and V = v_scales[g] * v_blocks (tinyllm "Going
+ * further": scales per head).  k_scales, v_scales: DEVICE arrays of num_kv_heads floats owned
+ * by the caller, or NULL for 1 on every head; a scale that is not finite and positive is
+ * recorded as PA_EINVAL in the device status and out / lse are left untouched.  All other
+ * arguments, kernels and errors as pa_varlen_forward_ex.
+ */
+pa_status pa_varlen_forward_per_head(const void* q, const void* k_blocks, const void* v_blocks,
+                                     void* out, const int32_t* query_start_loc,
+                                     const int32_t* seq_lens, const int32_t* positions,
+                                     const int32_t* block_tables, int32_t num_seqs,
+                                     int64_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                     int32_t max_blocks_per_seq, pa_dtype q_dtype,
+                                     pa_dtype kv_dtype, float scale, int32_t causal,
+                                     int32_t sliding_window, const float* sinks, float* lse,
+                                     const float* k_scales, const float* v_scales,
+                                     uint32_t flags, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream);
 
 /*
  * pa_cache_and_attend -- one decode / prefill step over the cache: pa_slot_mapping_and_cache
@@ -311,6 +349,19 @@ pa_status pa_decode_splitkv_partials_ex(
     int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int32_t partition_size,
     int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
     int32_t sliding_window, float k_scale, float v_scale, cudaStream_t stream);
+
+/*
+ * pa_decode_splitkv_partials_per_head -- pa_decode_splitkv_partials_ex with one scale per kv
+ * head: k_scales, v_scales are DEVICE arrays of num_kv_heads floats (NULL: 1), validated on
+ * the device as in pa_varlen_forward_per_head (PA_EINVAL recorded, partials untouched).
+ */
+pa_status pa_decode_splitkv_partials_per_head(
+    const void* q, const void* k_blocks, const void* v_blocks, float* max_logits,
+    float* exp_sums, float* tmp_out, const int32_t* seq_lens, const int32_t* block_tables,
+    int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int32_t partition_size,
+    int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
+    int32_t sliding_window, const float* k_scales, const float* v_scales, cudaStream_t stream);
 
 /*
  * pa_decode_splitkv_reduce -- phase 2 ("Phase 2: Cross-partition reduction").  For each

@@ -246,8 +246,8 @@ def splitkv_partials(q, k_blocks, v_blocks, seq_lens, block_tables, scale, parti
             bt.shape[1], partition_size, max_parts, _DT[q.dtype], _DT[kb.dtype], float(scale),
             int(sliding_window))
     if k_scales is not None or v_scales is not None:
-        st = lib().oracle_splitkv_partials_per_head(*args, _p(_scales(k_scales)),
-                                                    _p(_scales(v_scales)))
+        ksc, vsc = _scales(k_scales), _scales(v_scales)  # kept alive across the call
+        st = lib().oracle_splitkv_partials_per_head(*args, _p(ksc), _p(vsc))
     else:
         st = lib().oracle_splitkv_partials_ex(*args, float(k_scale), float(v_scale))
     return st, ml, es, to

@@ -170,6 +170,8 @@ __global__ void __launch_bounds__(NW * 32, 2)
       rows_total = (m.query_start_loc[s + 1] - qs) * G;
     }
     n = m.seq_lens[s];
+    // K = k_scales[kvh] * pool goes into the score scale (per kv head, when given)
+    const float sl2 = head_scale(m.k_scales, kvh, p.scale_log2);
 
     // this lane's two rows: r0 = lane / 4 and r1 = r0 + 8
     int st[2], en[2], tok[2], head[2];
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
           const int key = kcol + nt * 8 + (c & 1);
           const int r = c >> 1;
           const bool vis = key >= st[r] && key < en[r];
-          sc[nt][c] = vis ? sc[nt][c] * p.scale_log2 : -INFINITY;
+          sc[nt][c] = vis ? sc[nt][c] * sl2 : -INFINITY;
         }
       float alpha[2];
       bool grew = false;  // a row's running max rose: its O needs the rescale (else alpha = 1)
@@ -548,7 +550,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
           if (p.m.lse && seg == 0)
             p.m.lse[(int64_t)h * p.m.num_tokens + t] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
-        const float inv = L > 0.f ? p.m.v_scale / L : 0.f;
+        const float inv = L > 0.f ? head_scale(p.m.v_scales, kvh, p.m.v_scale) / L : 0.f;
         float vals[kSeg];
 #pragma unroll
         for (int d = 0; d < kSeg; ++d) {

@@ -415,7 +415,8 @@ __global__ void __launch_bounds__(256)
     k_scatter_convert(const TS* __restrict__ k, const TS* __restrict__ v, void* __restrict__ kb,
                       void* __restrict__ vb, const int32_t* __restrict__ slots, int64_t num_tokens,
                       int64_t num_slots, int64_t row_elems, float k_scale, float v_scale,
-                      int* status) {
+                      const float* __restrict__ k_scales, const float* __restrict__ v_scales,
+                      int32_t head_dim, int* status) {
   __shared__ int s_skip;
   pdl_wait();
   pdl_launch_dependents();
@@ -438,8 +439,10 @@ __global__ void __launch_bounds__(256)
   if (t >= num_tokens) return;
   const int64_t dst = (int64_t)slots[t] * row_elems, src = t * row_elems;
   for (int64_t i = lane; i < row_elems; i += 32) {
-    const float a = __fdiv_rn(to_f32(k[src + i]), k_scale);
-    const float b = __fdiv_rn(to_f32(v[src + i]), v_scale);
+    // one scale per kv head (head i / head_dim of the row) when the arrays are given
+    const int g = k_scales || v_scales ? (int)(i / head_dim) : 0;
+    const float a = __fdiv_rn(to_f32(k[src + i]), k_scales ? __ldg(k_scales + g) : k_scale);
+    const float b = __fdiv_rn(to_f32(v[src + i]), v_scales ? __ldg(v_scales + g) : v_scale);
     if constexpr (DST == PA_FP8_E4M3) {
       static_cast<uint8_t*>(kb)[dst + i] = (uint8_t)(f32x2_to_e4m3x2(a, 0.f) & 0xffu);
       static_cast<uint8_t*>(vb)[dst + i] = (uint8_t)(f32x2_to_e4m3x2(b, 0.f) & 0xffu);
@@ -456,20 +459,36 @@ __global__ void __launch_bounds__(256)
 template <typename TS, int DST>
 cudaError_t convert_as(const void* k, const void* v, void* kb, void* vb, const int32_t* slots,
                        int64_t T, int64_t row_elems, int64_t num_slots, float k_scale,
-                       float v_scale, int* status, cudaStream_t stream) {
+                       float v_scale, const float* ks, const float* vs, int32_t head_dim,
+                       int* status, cudaStream_t stream) {
   const dim3 grid((unsigned)((T + 7) / 8)), block(256);
   if (T <= kCheckedScatter)
     return launch_pdl(k_scatter_convert<TS, DST, true>, grid, block, 0, stream, (const TS*)k,
                       (const TS*)v, kb, vb, slots, T, num_slots, row_elems, k_scale, v_scale,
-                      status);
+                      ks, vs, head_dim, status);
   const int64_t vgrid = std::min<int64_t>((T + 255) / 256, 1024);
   cudaError_t e = launch_pdl(k_validate_slots, dim3((unsigned)vgrid), dim3(256), 0, stream, slots,
                              T, num_slots, status);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_scatter_convert<TS, DST, false>, grid, block, 0, stream, (const TS*)k,
-                    (const TS*)v, kb, vb, slots, T, num_slots, row_elems, k_scale, v_scale,
-                    status);
+                    (const TS*)v, kb, vb, slots, T, num_slots, row_elems, k_scale, v_scale, ks,
+                    vs, head_dim, status);
 }
+
+// Per kv head dequantisation scales must be finite and positive (tinyllm 2.6: reject before
+// any write); the kernels launched after this one see the recorded status and write nothing.
+__global__ void k_validate_scales(const float* k_scales, const float* v_scales,
+                                  int32_t num_kv_heads, int* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  bool bad = false;
+  for (int g = threadIdx.x; g < num_kv_heads; g += blockDim.x) {
+    const float a = k_scales ? k_scales[g] : 1.f, b = v_scales ? v_scales[g] : 1.f;
+    bad |= !(a > 0.f && a <= 3.402823466e38f) || !(b > 0.f && b <= 3.402823466e38f);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) record_error(status, PA_EINVAL);
+}
+
 
 // Slot mapping and scatter in one launch, for batches of up to kCheckedScatter tokens and
 // kFusedSeqs sequences (a decode step): every CTA loads the query start locations into shared
@@ -787,28 +806,25 @@ cudaError_t launch_reshape_and_cache_convert(const void* k, const void* v, void*
                                              void* v_blocks, const int32_t* slots,
                                              int64_t num_tokens, int64_t row_elems,
                                              int32_t block_size, int64_t num_blocks, int src_bf16,
-                                             int dst, float k_scale, float v_scale, int* status,
-                                             cudaStream_t stream) {
+                                             int dst, float k_scale, float v_scale,
+                                             const float* k_scales, const float* v_scales,
+                                             int32_t head_dim, int* status, cudaStream_t stream) {
   if (num_tokens <= 0) return cudaSuccess;
   const int64_t ns = num_blocks * block_size;
-  if (src_bf16) {
-    if (dst == PA_FP8_E4M3)
-      return convert_as<__nv_bfloat16, PA_FP8_E4M3>(k, v, k_blocks, v_blocks, slots, num_tokens,
-                                                    row_elems, ns, k_scale, v_scale, status, stream);
-    if (dst == PA_BF16)
-      return convert_as<__nv_bfloat16, PA_BF16>(k, v, k_blocks, v_blocks, slots, num_tokens,
-                                                row_elems, ns, k_scale, v_scale, status, stream);
-    return convert_as<__nv_bfloat16, PA_F32>(k, v, k_blocks, v_blocks, slots, num_tokens,
-                                             row_elems, ns, k_scale, v_scale, status, stream);
-  }
-  if (dst == PA_FP8_E4M3)
-    return convert_as<float, PA_FP8_E4M3>(k, v, k_blocks, v_blocks, slots, num_tokens, row_elems,
-                                          ns, k_scale, v_scale, status, stream);
-  if (dst == PA_BF16)
-    return convert_as<float, PA_BF16>(k, v, k_blocks, v_blocks, slots, num_tokens, row_elems, ns,
-                                      k_scale, v_scale, status, stream);
-  return convert_as<float, PA_F32>(k, v, k_blocks, v_blocks, slots, num_tokens, row_elems, ns,
-                                   k_scale, v_scale, status, stream);
+#define PA_CONVERT(TS, DST)                                                                  \
+  convert_as<TS, DST>(k, v, k_blocks, v_blocks, slots, num_tokens, row_elems, ns, k_scale,   \
+                      v_scale, k_scales, v_scales, head_dim, status, stream)
+  cudaError_t e;
+  if (src_bf16)
+    e = dst == PA_FP8_E4M3 ? PA_CONVERT(__nv_bfloat16, PA_FP8_E4M3)
+        : dst == PA_BF16   ? PA_CONVERT(__nv_bfloat16, PA_BF16)
+                           : PA_CONVERT(__nv_bfloat16, PA_F32);
+  else
+    e = dst == PA_FP8_E4M3 ? PA_CONVERT(float, PA_FP8_E4M3)
+        : dst == PA_BF16   ? PA_CONVERT(float, PA_BF16)
+                           : PA_CONVERT(float, PA_F32);
+#undef PA_CONVERT
+  return e;
 }
 
 cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, void* v_out,
@@ -835,6 +851,14 @@ cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k
                                row_bytes, block_size, max_blocks, status, stream);
   return gather_as<uint8_t>(k_blocks, v_blocks, k_out, v_out, cu, starts, tables, num_seqs,
                             row_bytes, block_size, max_blocks, status, stream);
+}
+
+
+cudaError_t launch_validate_scales(const float* k_scales, const float* v_scales,
+                                   int32_t num_kv_heads, int* status, cudaStream_t stream) {
+  if (!k_scales && !v_scales) return cudaSuccess;
+  return launch_pdl(k_validate_scales, dim3(1), dim3(256), 0, stream, k_scales, v_scales,
+                    num_kv_heads, status);
 }
 
 }  // namespace pa

@@ -562,6 +562,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       start = m.window > 0 ? max(0, end - m.window) : 0;
     }
     float m_ref = -INFINITY, l = 0.f;
+    const float sl = head_scale(m.k_scales, I.kvh, p.scale_log2);  // K = k_scales[g] * pool
     for (int j = 0; j < I.ntiles; ++j) {
       const uint32_t s = kv + j, b = buf_of(s);
       const uint32_t sbase = tmem + lane_addr + col_s(b) + col0;  // this thread's S / P columns
@@ -599,7 +600,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       // the row max over both column halves
       xchg[hf * 128 + r] = mine;
       pair_sync(quad);
-      const float mt = fmaxf(mine, xchg[(hf ^ 1) * 128 + r]) * p.scale_log2;
+      const float mt = fmaxf(mine, xchg[(hf ^ 1) * 128 + r]) * sl;
       pair_sync(quad);  // both read before either writes again
       const float m_new = fmaxf(m_ref, mt);
       const bool resc = m_new > m_ref + 8.f;
@@ -612,7 +613,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       // p = 2^(x * scale_log2 - m_ref) two at a time, the row sum, and p split into a bf16
       // pair hi + lo (hi = RNE(p), lo = RNE(p - hi)) for the two P V MMAs
       const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
-      const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2), nb2 = f2_pack(nbase, nbase);
+      const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(nbase, nbase);
       uint32_t hi[32], lo[32];
       {
         uint64_t rs2[4] = {0, 0, 0, 0};
@@ -691,7 +692,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     }
     if (m.lse && hf == 0 && valid)
       m.lse[(int64_t)h * m.num_tokens + t] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-    const float inv = l > 0.f ? o_scale * m.v_scale / l : 0.f;
+    const float inv = l > 0.f ? o_scale * head_scale(m.v_scales, I.kvh, m.v_scale) / l : 0.f;
     __nv_bfloat16* dst =
         reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * m.num_heads + h) * kD + col0;
     uint32_t oo[2][32];

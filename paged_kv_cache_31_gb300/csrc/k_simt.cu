@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(128) k_simt(const SimtParams p) {
     start = m.window > 0 ? max(0, end - m.window) : 0;
   }
   const int g = h / m.group;
+  const float psc = head_scale(m.k_scales, g, p.scale);   // K = k_scales[g] * pool
+  const float vsc = head_scale(m.v_scales, g, m.v_scale);  // V = v_scales[g] * pool
   const TQ* q = reinterpret_cast<const TQ*>(p.q) + (t * H + h) * (int64_t)D;
   const TKV* kb = reinterpret_cast<const TKV*>(p.k_blocks);
   const TKV* vb = reinterpret_cast<const TKV*>(p.v_blocks);
@@ -73,7 +75,7 @@ __global__ void __launch_bounds__(128) k_simt(const SimtParams p) {
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
-    const float sc = dot * p.scale;
+    const float sc = dot * psc;
     if (sc > mx) {
       const float r = expf(mx - sc);
       den *= r;
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(128) k_simt(const SimtParams p) {
       if (d < D) acc[i] += e * to_f32(vb[base + d]);
     }
   }
-  float inv = den > 0.f ? m.v_scale / den : 0.f;
+  float inv = den > 0.f ? vsc / den : 0.f;
   if (!p.split) {
     // an attention sink (TensorSharp ForwardWithSinks): one more state with max = the sink
     // logit, exp-sum 1 and weighted sum 0
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(128) k_simt(const SimtParams p) {
       const float a = mx == -INFINITY ? 0.f : expf(mx - m2);
       den = den * a + expf(sk - m2);
       mx = m2;
-      inv = a * m.v_scale / den;
+      inv = a * vsc / den;
     }
     if (m.lse && lane == 0) m.lse[(int64_t)h * m.num_tokens + t] = den > 0.f ? mx + logf(den) : -INFINITY;
   }

@@ -272,8 +272,30 @@ pa_status pa_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, 
   if (!d) return PA_ECUDA;
   return from_cuda(launch_reshape_and_cache_convert(
       k, v, k_blocks, v_blocks, slot_mapping, num_tokens, (int64_t)num_kv_heads * head_dim,
-      block_size, num_blocks, src_dtype == PA_BF16, kv_dtype, k_scale, v_scale, d->status,
-      stream));
+      block_size, num_blocks, src_dtype == PA_BF16, kv_dtype, k_scale, v_scale, nullptr, nullptr,
+      head_dim, d->status, stream));
+}
+
+pa_status pa_reshape_and_cache_per_head(const void* k, const void* v, void* k_blocks,
+                                        void* v_blocks, const int32_t* slot_mapping,
+                                        int64_t num_tokens, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                        pa_dtype src_dtype, pa_dtype kv_dtype,
+                                        const float* k_scales, const float* v_scales,
+                                        cudaStream_t stream) {
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return PA_ESHAPE;
+  if (!dtype_ok(src_dtype) || !pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (num_tokens < 0 || num_blocks < 0) return PA_EINVAL;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_blocks || !v_blocks || !slot_mapping) return PA_EINVAL;
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  if (launch_validate_scales(k_scales, v_scales, num_kv_heads, d->status, stream) != cudaSuccess)
+    return PA_ECUDA;
+  return from_cuda(launch_reshape_and_cache_convert(
+      k, v, k_blocks, v_blocks, slot_mapping, num_tokens, (int64_t)num_kv_heads * head_dim,
+      block_size, num_blocks, src_dtype == PA_BF16, kv_dtype, 1.f, 1.f, k_scales, v_scales,
+      head_dim, d->status, stream));
 }
 
 size_t pa_varlen_forward_workspace_size(int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
@@ -322,7 +344,8 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
                              int64_t num_blocks, int32_t max_blocks_per_seq, pa_dtype q_dtype,
                              pa_dtype kv_dtype, float scale, int32_t causal,
                              int32_t sliding_window, const float* sinks, float* lse,
-                             float k_scale, float v_scale, uint32_t flags, void* workspace,
+                             float k_scale, float v_scale, const float* k_scales,
+                             const float* v_scales, uint32_t flags, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream,
                              const CacheArgs* cache) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
@@ -364,8 +387,12 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
   m.sinks = sinks;
   m.lse = lse;
   m.v_scale = v_scale;
+  m.k_scales = k_scales;
+  m.v_scales = v_scales;
   scale *= k_scale;  // K = k_scale * pool: the scores take it with the softmax scale
   int32_t* plan = static_cast<int32_t*>(workspace);
+  if (launch_validate_scales(k_scales, v_scales, num_kv_heads, d->status, stream) != cudaSuccess)
+    return PA_ECUDA;
   PlanLayout L = plan_layout(num_seqs, num_tokens, m.group);
   const bool fast = mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
   // prefill-class sequences (more than 64 query rows per kv head) go to the tcgen05 kernel:
@@ -473,7 +500,26 @@ pa_status pa_varlen_forward_ex(const void* q, const void* k_blocks, const void* 
   return varlen_impl(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                      block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
                      block_size, num_blocks, max_blocks_per_seq, q_dtype, kv_dtype, scale, causal,
-                     sliding_window, sinks, lse, k_scale, v_scale, flags, workspace,
+                     sliding_window, sinks, lse, k_scale, v_scale, nullptr, nullptr, flags,
+                     workspace, workspace_bytes, stream, nullptr);
+}
+
+pa_status pa_varlen_forward_per_head(const void* q, const void* k_blocks, const void* v_blocks,
+                                     void* out, const int32_t* query_start_loc,
+                                     const int32_t* seq_lens, const int32_t* positions,
+                                     const int32_t* block_tables, int32_t num_seqs,
+                                     int64_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                     int32_t max_blocks_per_seq, pa_dtype q_dtype,
+                                     pa_dtype kv_dtype, float scale, int32_t causal,
+                                     int32_t sliding_window, const float* sinks, float* lse,
+                                     const float* k_scales, const float* v_scales,
+                                     uint32_t flags, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
+  return varlen_impl(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
+                     block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, max_blocks_per_seq, q_dtype, kv_dtype, scale, causal,
+                     sliding_window, sinks, lse, 1.f, 1.f, k_scales, v_scales, flags, workspace,
                      workspace_bytes, stream, nullptr);
 }
 
@@ -510,8 +556,8 @@ pa_status pa_cache_and_attend(const void* k_new, const void* v_new, const void* 
   return varlen_impl(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                      block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
                      block_size, num_blocks, max_blocks_per_seq, q_dtype, kv_dtype, scale, causal,
-                     sliding_window, nullptr, nullptr, 1.f, 1.f, 0u, workspace, workspace_bytes,
-                     stream, &cache);
+                     sliding_window, nullptr, nullptr, 1.f, 1.f, nullptr, nullptr, 0u, workspace,
+                     workspace_bytes, stream, &cache);
 }
 
 static pa_status splitkv_partials(const void* q, const void* k_blocks, const void* v_blocks,
@@ -522,7 +568,8 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
                                   int32_t max_blocks_per_seq, int32_t partition_size,
                                   int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype,
                                   float scale, int32_t sliding_window, float k_scale,
-                                  float v_scale, cudaStream_t stream) {
+                                  float v_scale, const float* k_scales, const float* v_scales,
+                                  cudaStream_t stream) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0 || partition_size <= 0 || max_num_partitions <= 0)
     return PA_ESHAPE;
@@ -537,6 +584,8 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
     return PA_EINVAL;
   const DeviceState* d = device_state();
   if (!d) return PA_ECUDA;
+  if (launch_validate_scales(k_scales, v_scales, num_kv_heads, d->status, stream) != cudaSuccess)
+    return PA_ECUDA;
   cudaError_t e = launch_validate_decode(seq_lens, block_tables, num_seqs, max_blocks_per_seq,
                                          block_size, num_blocks, partition_size,
                                          max_num_partitions, 1, d->status, stream);
@@ -557,6 +606,8 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
   m.causal = 1;
   m.window = sliding_window > 0 ? sliding_window : 0;
   m.v_scale = v_scale;
+  m.k_scales = k_scales;
+  m.v_scales = v_scales;
   const bool fp8 =
       mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, nullptr);
   if ((fp8 || mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, nullptr)) &&
@@ -640,7 +691,8 @@ pa_status pa_decode_splitkv_partials(const void* q, const void* k_blocks, const 
   return splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
                           block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                           num_blocks, max_blocks_per_seq, partition_size, max_num_partitions,
-                          q_dtype, kv_dtype, scale, sliding_window, 1.f, 1.f, stream);
+                          q_dtype, kv_dtype, scale, sliding_window, 1.f, 1.f, nullptr, nullptr,
+                          stream);
 }
 
 pa_status pa_decode_splitkv_partials_ex(
@@ -653,7 +705,22 @@ pa_status pa_decode_splitkv_partials_ex(
   return splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
                           block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                           num_blocks, max_blocks_per_seq, partition_size, max_num_partitions,
-                          q_dtype, kv_dtype, scale, sliding_window, k_scale, v_scale, stream);
+                          q_dtype, kv_dtype, scale, sliding_window, k_scale, v_scale, nullptr,
+                          nullptr, stream);
+}
+
+pa_status pa_decode_splitkv_partials_per_head(
+    const void* q, const void* k_blocks, const void* v_blocks, float* max_logits,
+    float* exp_sums, float* tmp_out, const int32_t* seq_lens, const int32_t* block_tables,
+    int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int32_t partition_size,
+    int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
+    int32_t sliding_window, const float* k_scales, const float* v_scales, cudaStream_t stream) {
+  return splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
+                          block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, partition_size, max_num_partitions,
+                          q_dtype, kv_dtype, scale, sliding_window, 1.f, 1.f, k_scales, v_scales,
+                          stream);
 }
 
 pa_status pa_decode_splitkv_reduce(void* out, const float* max_logits, const float* exp_sums,
@@ -680,7 +747,7 @@ pa_status pa_decode_splitkv(const void* q, const void* k_blocks, const void* v_b
                                   block_tables, num_seqs, num_heads, num_kv_heads, head_dim,
                                   block_size, num_blocks, max_blocks_per_seq, partition_size,
                                   max_num_partitions, q_dtype, kv_dtype, scale, sliding_window,
-                                  1.f, 1.f, stream);
+                                  1.f, 1.f, nullptr, nullptr, stream);
   if (st != PA_OK) return st;
   return splitkv_reduce(out, max_logits, exp_sums, tmp_out, seq_lens, num_seqs, num_heads,
                         head_dim, partition_size, max_num_partitions, q_dtype, false, stream);

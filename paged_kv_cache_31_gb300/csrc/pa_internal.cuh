@@ -295,7 +295,17 @@ struct VarlenMeta {
   const float* sinks;  // [num_heads] sink logits on the score scale, or null (varlen only)
   float* lse;          // [num_heads, num_tokens] natural-log lse out, or null (varlen only)
   float v_scale;       // V = v_scale * pool: applied to the normalised output (1 = none)
+  // one dequantisation scale per kv head (device, [num_kv_heads]), or null: K of kv head g is
+  // k_scales[g] * pool (taken with the score scale), V is v_scales[g] * pool
+  const float* k_scales;
+  const float* v_scales;
 };
+
+// The scale of kv head g from a per-head array, times the per-pool scalar; the scalar alone
+// when there is no array (no extra rounding step then).
+__device__ __forceinline__ float head_scale(const float* s, int g, float scalar) {
+  return s ? scalar * __ldg(s + g) : scalar;
+}
 
 struct Mma16Params {
   const __nv_bfloat16* q;
@@ -386,8 +396,12 @@ cudaError_t launch_reshape_and_cache_convert(const void* k, const void* v, void*
                                              void* v_blocks, const int32_t* slots,
                                              int64_t num_tokens, int64_t row_elems,
                                              int32_t block_size, int64_t num_blocks, int src_bf16,
-                                             int dst, float k_scale, float v_scale, int* status,
-                                             cudaStream_t stream);
+                                             int dst, float k_scale, float v_scale,
+                                             const float* k_scales, const float* v_scales,
+                                             int32_t head_dim, int* status, cudaStream_t stream);
+// Records PA_EINVAL when a per-head scale (either array may be null) is not finite and > 0.
+cudaError_t launch_validate_scales(const float* k_scales, const float* v_scales,
+                                   int32_t num_kv_heads, int* status, cudaStream_t stream);
 cudaError_t launch_gather_kv(const void* k_blocks, const void* v_blocks, void* k_out, void* v_out,
                              const int32_t* cu, const int32_t* starts, const int32_t* tables,
                              int32_t num_seqs, int64_t num_rows, int64_t row_bytes,

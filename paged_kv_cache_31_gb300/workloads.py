@@ -171,6 +171,19 @@ def fp8_pools(w: Workload, spread: float = 8.0, seed: Optional[int] = None):
     return kb, vb
 
 
+def fp8_pools_per_head(w: Workload, spreads, seed: Optional[int] = None):
+    """e4m3 K and V pools of w's shape whose kv head g is drawn i.i.d. N(0, spreads[g]^2) in
+    fp32 (seeded) and cast with torch's float8_e4m3fn conversion: with per-head scales
+    1 / spreads[g] every head dequantises to about N(0, 1).  Only draws inputs."""
+    dev = w.k_blocks.device
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 9 if seed is None else seed)
+    shape = tuple(w.k_blocks.shape)
+    sp = torch.tensor(list(spreads), dtype=torch.float32, device=dev).view(1, 1, -1, 1)
+    kb = (torch.randn(shape, generator=gen, device=dev) * sp).to(torch.float8_e4m3fn)
+    vb = (torch.randn(shape, generator=gen, device=dev) * sp).to(torch.float8_e4m3fn)
+    return kb, vb
+
+
 def subset(w: Workload, seqs: List[int], name: Optional[str] = None) -> Workload:
     """The sequences `seqs` of w as a batch of their own, over the same pool (its query rows,
     new K/V rows and metadata, re-indexed)."""

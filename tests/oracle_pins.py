@@ -798,8 +798,9 @@ def pin_per_head_attention():
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
     # one decode query per sequence for the partials
     qd = torch.stack([q[qsl[s + 1] - 1] for s in range(len(lens))])
+    # (float64 scales: the wrapper's fp32 copies must outlive the call)
     a = oracle.splitkv_partials(qd, kb8, vb8, _t(lens), table, 1.0 / math.sqrt(D), 16, 8,
-                                k_scales=ks, v_scales=vs)
+                                k_scales=ks.double(), v_scales=vs.double())
     b = oracle.splitkv_partials(qd, kbf, vbf, _t(lens), table, 1.0 / math.sqrt(D), 16, 8)
     assert a[0] == oracle.OK and b[0] == oracle.OK
     for x, y in zip(a[1:], b[1:]):

@@ -122,3 +122,43 @@ def test_host_side_errors_of_the_extended_calls(lib):
     # empty steps are a no-op
     assert L.pa_slot_mapping_and_cache(None, None, None, None, None, None, None, 0, 0, 0, 2, 128,
                                        16, 8, b.PA_BF16, None, None) == b.PA_OK
+
+
+def test_host_side_errors_of_the_per_head_calls(lib):
+    """The per kv head scale calls check shapes, dtypes and pointers on the host like the
+    per-pool ones (the scales themselves are device arrays, validated on the device)."""
+    from paged_kv_cache_31_gb300 import binding as b
+
+    L = b._lib
+    fake = ctypes.c_void_p(16)  # never dereferenced: every case below returns first
+    # scatter: fp8 is not a source type; a negative kv head count; missing rows
+    assert L.pa_reshape_and_cache_per_head(None, None, None, None, None, 1, 2, 128, 16, 8,
+                                           b.PA_FP8_E4M3, b.PA_FP8_E4M3, fake, fake,
+                                           None) == b.PA_EUNSUPPORTED
+    assert L.pa_reshape_and_cache_per_head(fake, fake, fake, fake, fake, 1, -2, 128, 16, 8,
+                                           b.PA_BF16, b.PA_FP8_E4M3, fake, fake,
+                                           None) == b.PA_ESHAPE
+    assert L.pa_reshape_and_cache_per_head(None, None, fake, fake, fake, 1, 2, 128, 16, 8,
+                                           b.PA_BF16, b.PA_FP8_E4M3, fake, fake,
+                                           None) == b.PA_EINVAL
+    assert L.pa_reshape_and_cache_per_head(None, None, None, None, None, 0, 2, 128, 16, 8,
+                                           b.PA_BF16, b.PA_FP8_E4M3, fake, fake,
+                                           None) == b.PA_OK  # nothing to write
+    # varlen: unknown flag bits; a GQA group that does not divide; fp8 queries
+    st = L.pa_varlen_forward_per_head(None, None, None, None, None, None, None, None, 0, 0, 8, 4,
+                                      128, 16, 8, 1, b.PA_BF16, b.PA_BF16, 1.0, 1, 0, None, None,
+                                      fake, fake, 2, None, 0, None)
+    assert st == b.PA_EINVAL
+    st = L.pa_varlen_forward_per_head(None, None, None, None, None, None, None, None, 0, 0, 8, 3,
+                                      128, 16, 8, 1, b.PA_BF16, b.PA_BF16, 1.0, 1, 0, None, None,
+                                      fake, fake, 0, None, 0, None)
+    assert st == b.PA_ESHAPE
+    st = L.pa_varlen_forward_per_head(None, None, None, None, None, None, None, None, 0, 0, 8, 4,
+                                      128, 16, 8, 1, b.PA_FP8_E4M3, b.PA_FP8_E4M3, 1.0, 1, 0,
+                                      None, None, fake, fake, 0, None, 0, None)
+    assert st == b.PA_EUNSUPPORTED
+    # split-KV partials: a partition size that is not a multiple of the block size
+    st = L.pa_decode_splitkv_partials_per_head(fake, fake, fake, fake, fake, fake, fake, fake, 1,
+                                               8, 4, 128, 16, 8, 1, 500, 4, b.PA_BF16,
+                                               b.PA_BF16, 1.0, 0, fake, fake, None)
+    assert st == b.PA_EUNSUPPORTED
