@@ -64,8 +64,11 @@ constexpr int kOffBar = kOffV + kStagesV * kPart;
 constexpr int kNumBarsMax = 40;
 constexpr int kOffTmem = kOffBar + kNumBarsMax * 8;
 constexpr int kOffFlag = kOffTmem + 16;
-constexpr int kOffXchg = kOffFlag + 16;               // row max / sum exchange, 2 x 128 fp32
-constexpr int kSmemBytes = kOffXchg + 2 * 128 * 4 + 1024;  // + slack to align the base
+// softmax pair exchange: [half][row] fp32 row max (or row sum), then [half][row] int failed-
+// wait flags of the item's end (a tile's failure travels in the row max slot as kBadMax)
+constexpr int kOffXchg = kOffFlag + 16;
+constexpr int kSmemBytes = kOffXchg + 2 * 2 * 128 * 4 + 1024;  // + slack to align the base
+constexpr uint32_t kBadMax = 0x7fc0dea1u;  // a NaN that no arithmetic produces (canonical 7fffffff)
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 constexpr int kSoftWarps = 8;                         // two column halves x four lane quarters
 constexpr int kThreads = 64 + kSoftWarps * 32 + 64;  // + the V producer and PV issuer warps
@@ -529,7 +532,10 @@ __device__ void pv_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_
   }
 }
 
-// Named barrier of the two softmax warps that share 32 query rows (one per column half).
+// Named barrier of the two softmax warps that share 32 query rows (one per column half).  A
+// softmax warp whose bounded wait fails does not leave at once: it carries the failure to
+// the pair's next exchange (the tile's row max, or the item's end), where both warps read
+// both flags and leave together, so neither is left waiting at this barrier.
 __device__ __forceinline__ void pair_sync(int quad) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
 }
@@ -543,6 +549,8 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
   const int col0 = hf * 64;
   const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
   float* xchg = reinterpret_cast<float*>(c.sm + kOffXchg);  // [half][row]
+  int* xbad_e = reinterpret_cast<int*>(xchg + 2 * 128);      // [half][row], item end
+  bool bad = false;  // a wait of this warp ran out or another role aborted (warp-uniform)
   uint32_t kv = 0;
   // an item's metadata (plan entry, sequence bounds, this row's position) is a chain of
   // dependent loads: the next item's is fetched while the current one's last P V runs
@@ -566,8 +574,10 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     for (int j = 0; j < I.ntiles; ++j) {
       const uint32_t s = kv + j, b = buf_of(s);
       const uint32_t sbase = tmem + lane_addr + col_s(b) + col0;  // this thread's S / P columns
-      if (!__all_sync(kFull, wait_bar(c, B_SFULL + b, use_par(s)))) return;
+      if (!bad) bad = !__all_sync(kFull, wait_bar(c, B_SFULL + b, use_par(s)));
       tc_fence_after();
+      // after a failed wait the values read here only travel to the exchange below, where
+      // the pair leaves (a read of allocated tensor memory is defined, whatever it holds)
       float x[64];
       {
         uint32_t v[2][32];
@@ -597,11 +607,14 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
       const float mine = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      // the row max over both column halves
-      xchg[hf * 128 + r] = mine;
+      // the row max over both column halves; a failed wait travels as kBadMax
+      xchg[hf * 128 + r] = bad ? __uint_as_float(kBadMax) : mine;
       pair_sync(quad);
-      const float mt = fmaxf(mine, xchg[(hf ^ 1) * 128 + r]) * sl;
+      const float other = xchg[(hf ^ 1) * 128 + r];
+      const float mt = fmaxf(mine, other) * sl;
+      const bool leave = __any_sync(kFull, bad || __float_as_uint(other) == kBadMax);
       pair_sync(quad);  // both read before either writes again
+      if (leave) return;
       const float m_new = fmaxf(m_ref, mt);
       const bool resc = m_new > m_ref + 8.f;
       float alpha = 1.f;
@@ -642,7 +655,9 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
 
       // O rescale: only after P_{j-1} V_{j-1} is done (O stable); most tiles skip both
       if (j >= 1 && __any_sync(kFull, resc)) {
-        if (!__all_sync(kFull, wait_bar(c, B_PVDONE + buf_of(s - 1), use_par(s - 1)))) return;
+        // a failure here is carried to the next exchange (what this warp writes to tensor
+        // memory until then is never read into the output)
+        if (!bad) bad = !__all_sync(kFull, wait_bar(c, B_PVDONE + buf_of(s - 1), use_par(s - 1)));
         tc_fence_after();
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -668,15 +683,18 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       In = load_item(p, item_of(c, k + 1), c.rank);
       if (tl < In.n_tok) pos_n = m.positions[In.t0 + tl];
     }
-    // epilogue: o = O / l, with l summed over both column halves
+    // epilogue: o = O / l, with l summed over both column halves; the pair's failure flags
+    // travel with the second barrier, so both warps leave before any output is written
+    const uint32_t last = kv + I.ntiles - 1;
     {
       xchg[hf * 128 + r] = l;
       pair_sync(quad);
       l += xchg[(hf ^ 1) * 128 + r];
-      pair_sync(quad);  // both read before either writes again
+      if (!bad) bad = !__all_sync(kFull, wait_bar(c, B_PVDONE + buf_of(last), use_par(last)));
+      xbad_e[hf * 128 + r] = bad ? 1 : 0;
+      pair_sync(quad);  // both read the sums before either writes again; the flags are read next
+      if (__any_sync(kFull, bad || xbad_e[(hf ^ 1) * 128 + r] != 0)) return;
     }
-    const uint32_t last = kv + I.ntiles - 1;
-    if (!__all_sync(kFull, wait_bar(c, B_PVDONE + buf_of(last), use_par(last)))) return;
     tc_fence_after();
     // an attention sink (TensorSharp ForwardWithSinks) is one more state to merge: max = the
     // sink logit, exp-sum = 1, weighted sum = 0
