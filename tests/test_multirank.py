@@ -2,6 +2,7 @@
 exchange (every rank runs an independent replica), so the only collective is the timing
 reduction: the whole-job time is the slowest rank's and the throughput counts every rank's
 units.  The reference arm runs on rank 0 only; the other ranks exit at once without work."""
+import json
 import os
 import socket
 import subprocess
@@ -71,3 +72,15 @@ def test_reference_arm_runs_on_rank_zero_only():
                        env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_line_echoes_steps_and_warmup():
+    # the oracle arm runs --warmup untimed and --steps timed steps, each over a bounded sample
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "1", "--reference-seconds", "2"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 3 and line["warmup"] == 1
+    assert line["value"] > 0 and line["unit"] == "GB/s"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
