@@ -126,6 +126,13 @@ __global__ void __launch_bounds__(1024)
   if (s_err == 0) {
     if (m.num_seqs == 0 && tid == 0 && (int64_t)m.query_start_loc[0] != m.num_tokens)
       atomicCAS(&s_err, 0, PA_EINVAL);
+    // per kv head dequantisation scales, when given, are finite and positive
+    if (m.k_scales || m.v_scales)
+      for (int g = tid; g < m.num_kv_heads; g += blockDim.x) {
+        const float ks = m.k_scales ? m.k_scales[g] : 1.f, vs = m.v_scales ? m.v_scales[g] : 1.f;
+        if (!(ks > 0.f && ks <= 3.402823466e38f) || !(vs > 0.f && vs <= 3.402823466e38f))
+          atomicCAS(&s_err, 0, PA_EINVAL);
+      }
     for (int s = warp; s < m.num_seqs; s += nwarps) {
       const int a = cached ? s_qsl[s] : m.query_start_loc[s];
       const int b = cached ? s_qsl[s + 1] : m.query_start_loc[s + 1];

@@ -390,9 +390,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
   m.k_scales = k_scales;
   m.v_scales = v_scales;
   scale *= k_scale;  // K = k_scale * pool: the scores take it with the softmax scale
-  int32_t* plan = static_cast<int32_t*>(workspace);
-  if (launch_validate_scales(k_scales, v_scales, num_kv_heads, d->status, stream) != cudaSuccess)
-    return PA_ECUDA;
+  int32_t* plan = static_cast<int32_t*>(workspace);  // (the plan also checks per-head scales)
   PlanLayout L = plan_layout(num_seqs, num_tokens, m.group);
   const bool fast = mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
   // prefill-class sequences (more than 64 query rows per kv head) go to the tcgen05 kernel:
