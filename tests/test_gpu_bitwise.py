@@ -97,6 +97,22 @@ def test_decode_equals_prefill_bitwise_fp8(pa):
     assert torch.equal(out_p, out_d) and torch.equal(lse_p, lse_d)
 
 
+def test_decode_equals_prefill_bitwise_fp8_per_head_scales(pa):
+    # one dequantisation scale per kv head: constant over a (sequence, kv head) unit, so the
+    # decode and prefill rows still see the same arithmetic
+    w = workloads.build("fp8-heads", seed=94, device=DEV, **CASES["gqa4"])
+    sp = [2.0 + 4.0 * g for g in range(w.num_kv_heads)]
+    kb8, vb8 = workloads.fp8_pools_per_head(w, sp)
+    ks = torch.tensor([1.0 / x for x in sp], device=DEV)
+    kw = dict(k_scales=ks, v_scales=ks * 0.7)
+    out_p, lse_p = _run(pa, w.q, kb8, vb8, w.query_start_loc, w.seq_lens, w.positions,
+                        w.block_tables, w, bitwise=True, **kw)
+    d = _as_decode(w)
+    out_d, lse_d = _run(pa, w.q, kb8, vb8, d["qsl"], d["seq_lens"], d["pos"], d["table"], w,
+                        bitwise=False, **kw)
+    assert torch.equal(out_p, out_d) and torch.equal(lse_p, lse_d)
+
+
 def test_short_chunks_agree_without_the_flag(pa):
     # sequences of at most 64 rows per kv head stay on the warp-MMA kernel by default
     w = workloads.build("short", seq_lens=[40, 700, 1025, 16], q_lens=[16, 9, 16, 1],
