@@ -35,8 +35,10 @@ def test_captured_step_replays_bitwise(pa, case):
     if case == "decode":  # the decode batch's shape, one spare table column for the next step
         g0 = torch.Generator().manual_seed(31)
         lens = torch.randint(512, 4097, (64,), generator=g0).tolist()
+        need = sum((n + 15) // 16 for n in lens)
         w = workloads.build("graph-decode", seq_lens=lens, q_lens=[1] * 64, num_heads=32,
                             num_kv_heads=8, head_dim=128, seed=31, device=DEV,
+                            num_blocks=need + 64,
                             extra_table_cols=1)
     else:
         w = workloads.build("graph-mixed", seq_lens=[600, 1300, 90, 2000], q_lens=[512, 130, 1, 1],
@@ -71,7 +73,19 @@ def test_captured_step_replays_bitwise(pa, case):
         assert torch.equal(kb_g, kb_e) and torch.equal(vb_g, vb_e)
     if case != "decode":
         return
-    # the next decode step: the metadata buffers the graph reads are updated in place
+    # the next decode step: the metadata buffers the graph reads are updated in place.  A
+    # sequence whose new token opens a block gets a block of its own in the spare table column
+    # (unused entries hold 0, a block another sequence owns: two new tokens would then share
+    # a slot, and the pool would depend on the order of their writes)
+    lens_now = w.seq_lens.tolist()
+    tables = w.block_tables.cpu()
+    used = {int(tables[s_, b_]) for s_, n in enumerate(lens_now) for b_ in range((n + 15) // 16)}
+    free = [i for i in range(w.num_blocks) if i not in used]
+    opening = [s_ for s_, n in enumerate(lens_now) if n % 16 == 0]
+    assert len(free) >= len(opening)
+    for s_, blk in zip(opening, free):
+        tables[s_, lens_now[s_] // 16] = blk
+    w.block_tables.copy_(tables)
     w.seq_lens.add_(1)
     w.positions.add_(1)
     kb_e2, vb_e2 = kb_e.clone(), vb_e.clone()
