@@ -713,6 +713,8 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     const float inv = l > 0.f ? o_scale * head_scale(m.v_scales, I.kvh, m.v_scale) / l : 0.f;
     __nv_bfloat16* dst =
         reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * m.num_heads + h) * kD + col0;
+    // rows start 256 bytes apart and halves at 0 / 128: 32-byte aligned when the output is
+    const bool st32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
     uint32_t oo[2][32];
 #pragma unroll
     for (int q = 0; q < 2; ++q) tmem_ld32(tmem + lane_addr + kColO + col0 + q * 32, oo[q]);
@@ -722,14 +724,23 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     for (int q = 0; q < 2; ++q) {
       const uint32_t (&o)[32] = oo[q];
       if (valid) {
+        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
-          *reinterpret_cast<uint4*>(dst + q * 32 + i) = w;
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        if (st32) {  // 32-byte stores: a whole sector each
+#pragma unroll
+          for (int i = 0; i < 16; i += 8)
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                             dst + q * 32 + 2 * i),
+                         "r"(w[i]), "r"(w[i + 1]), "r"(w[i + 2]), "r"(w[i + 3]), "r"(w[i + 4]),
+                         "r"(w[i + 5]), "r"(w[i + 6]), "r"(w[i + 7])
+                         : "memory");
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<uint4*>(dst + q * 32 + 2 * i) =
+                make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
         }
       }
     }
