@@ -94,3 +94,23 @@ def test_prefill_many_chunks_and_decodes(pa):
     assert_attn_close(out, oracle_attention(w, w.k_blocks.cpu(), w.v_blocks.cpu()), "mixed")
     again = _run(pa, w)
     assert torch.equal(out, again), "prefill path not deterministic"
+
+
+def test_prefill_output_only_16_byte_aligned(pa):
+    # the tcgen05 kernel writes 32-byte stores when the output is 32-byte aligned and 16-byte
+    # stores otherwise: an output that starts 16 bytes into its allocation must give the same
+    # bits as an aligned one
+    prior = [0, 300, 45]
+    chunk = [200, 129, 96]
+    w = workloads.build("pre16", seq_lens=[p + c for p, c in zip(prior, chunk)], q_lens=chunk,
+                        num_heads=32, num_kv_heads=8, head_dim=128, seed=16, device=DEV)
+    aligned = _run(pa, w)
+    assert aligned.data_ptr() % 32 == 0
+    buf = torch.full((w.q.numel() + 8,), float("nan"), dtype=w.q.dtype, device=DEV)
+    out = buf[8:].view_as(w.q)
+    assert out.data_ptr() % 32 == 16
+    pa.pa_varlen_forward(w.q, w.k_blocks, w.v_blocks, out, w.query_start_loc, w.seq_lens,
+                         w.positions, w.block_tables, w.scale, causal=w.causal)
+    assert pa.pa_device_status() == pa.PA_OK
+    assert torch.equal(out, aligned)
+    assert torch.isnan(buf[:8].float()).all()
