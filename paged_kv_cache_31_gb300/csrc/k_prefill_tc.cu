@@ -17,11 +17,12 @@
 // the peer's arrivals (the peer's idle issuer warps forward "my part of this stage has landed"
 // with remote mbarrier arrives), and the MMA completions are multicast to both CTAs.
 //
-// One CTA per SM, persistent over items, 12 warps:
+// One CTA per SM, persistent over items, 12 warps; warps 0..3 (one warpgroup) give up
+// registers to the two softmax warpgroups (setmaxnreg: 56 and 224 per thread):
 //   warp 0      TMA producer of Q (two buffers, so the next item's Q loads while this one
-//               finishes) and of this CTA's part of K_j through a 4-stage ring; warp 10
+//               finishes) and of this CTA's part of K_j through a 4-stage ring; warp 2
 //               produces its part of V_j through a 5-stage ring;
-//   warp 1      TMEM owner and QK^T issuer; warp 11 issues PV and zeroes the never-written
+//   warp 1      TMEM owner and QK^T issuer; warp 3 issues PV and zeroes the never-written
 //               V rows past a sequence's end in this CTA's part.  In the leader lane 0 issues,
 //               in warp-uniform code:
 //                 S_j = Q K_j^T      (M 256, N 128, K 128: 8 MMAs, K-major operands)
@@ -29,7 +30,7 @@
 //               In the peer the two warps forward the Q / K and V arrivals to the leader.
 //               TMEM columns: three S buffers at 0 / 128 / 384, O at 256.  P_j is written over
 //               the S_j it came from, so S_{j+3} may only be issued once P_j V_j is done;
-//   warps 2..9  softmax: two threads per query row (TMEM lane = row), one per 64-column
+//   warps 4..11 softmax: two threads per query row (TMEM lane = row), one per 64-column
 //               half; mask, row max (combined through shared memory), exp2, row sum, P to
 //               tensor memory, lazy O rescale, and the epilogue o = O * (1 / l) -> bf16.
 //               A softmax thread waits for the previous P V only when it must rescale O,
@@ -423,7 +424,7 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
   }
 }
 
-// MMA issue runs on two threads of the leader (warps 1 and 11) so that one thread's
+// MMA issue runs on two threads of the leader (warps 1 and 3) so that one thread's
 // instruction issue never delays the other chain: the QK^T issuer releases K and Q stages, the
 // PV issuer releases V stages, S / P buffers and O.  In the peer the same warps forward the
 // arrival of its Q / K parts and (after zeroing unwritten rows) V parts to the leader's full
@@ -536,7 +537,7 @@ __device__ __forceinline__ void pair_sync(int quad) {
 __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
   const VarlenMeta& m = p.m;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hf = (warp - 2) >> 2;  // column half of S / P / O this warp handles
+  const int hf = (warp - 4) >> 2;  // column half of S / P / O this warp handles
   const int quad = warp & 3;       // TMEM lane quarter this warp may access
   const int r = 32 * quad + lane;  // this thread's query row == TMEM lane
   const int col0 = hf * 64;
@@ -798,37 +799,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_rank(), (int)cluster_id_x(), (int)num_clusters_x()};
   const int n_items = flags[0] ? 0 : p.plan[1] * p.m.num_kv_heads;
 
-  if (warp == 0) {
-    producer(c, p, &tq, &tk, false, n_items);
-  } else if (warp == 2 + kSoftWarps) {
-    producer(c, p, &tq, &tv, true, n_items);
-  } else if (warp == 1 || warp == 3 + kSoftWarps) {
-    if (warp == 1)
-      s_issuer(c, p, tmem, n_items);
-    else
-      pv_issuer(c, p, tmem, n_items);
-    __syncwarp();
-    // every MMA issued by either warp of the leader has completed before the tensor memory is
-    // released
-    if (leader) {
-      tc_commit_mc_l0(bar + B_FIN, 0x1);
-      if ((threadIdx.x & 31) == 0) {
-        uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar + B_FIN, 0) && globaltimer_ns() - t0 < 1000000000ull) {
+  // warps 0..3 (one warpgroup) produce and issue and need few registers; the two softmax
+  // warpgroups take theirs: 4 x 56 + 8 x 224 = 12 x 168, the launch's registers per thread
+  // (each branch ends the kernel itself, so no code runs under both limits)
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    if (warp == 0) {
+      producer(c, p, &tq, &tk, false, n_items);
+    } else if (warp == 2) {
+      producer(c, p, &tq, &tv, true, n_items);
+    } else if (warp == 1 || warp == 3) {
+      if (warp == 1)
+        s_issuer(c, p, tmem, n_items);
+      else
+        pv_issuer(c, p, tmem, n_items);
+      __syncwarp();
+      // every MMA issued by either warp of the leader has completed before the tensor memory is
+      // released
+      if (leader) {
+        tc_commit_mc_l0(bar + B_FIN, 0x1);
+        if ((threadIdx.x & 31) == 0) {
+          uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar + B_FIN, 0) && globaltimer_ns() - t0 < 1000000000ull) {
+          }
         }
       }
+      __syncwarp();
     }
-    __syncwarp();
+    tc_fence_before();
+    cluster_sync();  // neither CTA leaves while its partner may still write to its shared memory
+    if (warp == 1) {  // collectively, like the allocation
+      tc_fence_after();
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(kTmemCols)
+                   : "memory");
+    }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
     softmax_role(c, p, tmem, n_items);
-  }
-  tc_fence_before();
-  cluster_sync();  // neither CTA leaves while its partner may still write to its shared memory
-  if (warp == 1) {  // collectively, like the allocation
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
-                 : "memory");
+    tc_fence_before();
+    cluster_sync();
   }
 }
 
