@@ -20,8 +20,8 @@
 // One CTA per SM, persistent over items, 12 warps; warps 0..3 (one warpgroup) give up
 // registers to the two softmax warpgroups (setmaxnreg: 56 and 224 per thread):
 //   warp 0      TMA producer of Q (two buffers, so the next item's Q loads while this one
-//               finishes) and of this CTA's part of K_j through a 4-stage ring; warp 2
-//               produces its part of V_j through a 5-stage ring;
+//               finishes) and of this CTA's part of K_j through a 3-stage ring; warp 2
+//               produces its part of V_j through a 6-stage ring;
 //   warp 1      TMEM owner and QK^T issuer; warp 3 issues PV and zeroes the never-written
 //               V rows past a sequence's end in this CTA's part.  In the leader lane 0 issues,
 //               in warp-uniform code:
@@ -56,8 +56,8 @@ constexpr int kTile = 2 * kHalf;  // 128 x 128 bf16 (this CTA's Q rows)
 constexpr int kKVHalf = 8192;     // K part: one 64-dim half of this CTA's 64 keys
 constexpr int kPart = 16384;      // this CTA's part of a K (or V) tile
 constexpr int kSBufs = 3;    // S / P buffers in tensor memory (columns 0, 128 and 384)
-constexpr int kStagesK = 4;  // K ring (a K tile is released as soon as its S MMAs finish)
-constexpr int kStagesV = 5;  // V ring (held until P V, so it needs more stages in flight)
+constexpr int kStagesK = 3;  // K ring (a K tile is released as soon as its S MMAs finish)
+constexpr int kStagesV = 6;  // V ring (held until P V, so it needs more stages in flight)
 constexpr int kOffQ = 0;                          // two Q buffers (consecutive items)
 constexpr int kOffK = kOffQ + 2 * kTile;
 constexpr int kOffV = kOffK + kStagesK * kPart;
