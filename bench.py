@@ -53,10 +53,17 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--secondary-steps", type=int, default=30)
-    ap.add_argument("--case", default="bench", choices=["bench", "prefill-chunks", "decode-fp8"],
-                    help="prefill-chunks: time only the attention call on the mixed batch's "
-                         "prefill chunks (own pool; a small case for profiling); decode-fp8: "
-                         "time only the attention call on the decode batch over fp8 pools")
+    ap.add_argument("--case", default="bench",
+                    choices=["bench", "prefill-chunks", "decode-fp8", "splitkv", "shared-prefix",
+                             "tiny"],
+                    help="a single timed case for profiling: prefill-chunks (the attention "
+                         "call on the mixed batch's prefill chunks, own pool), decode-fp8 (the "
+                         "decode batch over fp8 pools), splitkv (the long-context split-KV "
+                         "call), shared-prefix (the fork batch's attention call), tiny (the "
+                         "fp32 tiny mixed batch)")
+    ap.add_argument("--min-timed-ms", type=float, default=1000.0,
+                    help="the timed loop of --steps steps is repeated until the repeats "
+                         "together take at least this long (at least 5 repeats)")
     return ap.parse_args()
 
 
@@ -384,6 +391,25 @@ def time_calls(fn, n, stream, flush=None):
     return sum(a.elapsed_time(b) for a, b in ev) / n
 
 
+def time_repeats(fn, steps, stream, min_total_ms, min_reps=5, max_reps=2000):
+    """Repeat a timed loop of exactly `steps` calls (CUDA events on `stream`, synchronised
+    after each loop) until the loops together took min_total_ms, at least min_reps times.
+    Returns the per-call ms of every repeat."""
+    out, total = [], 0.0
+    while len(out) < max_reps and (len(out) < min_reps or total < min_total_ms):
+        ms = time_calls(fn, steps, stream)
+        out.append(ms)
+        total += ms * steps
+    return out
+
+
+def spread(xs):
+    """Median and range of repeat times (ms)."""
+    ys = sorted(xs)
+    return {"repeats": len(ys), "median_ms": statistics.median(ys), "min_ms": ys[0],
+            "max_ms": ys[-1]}
+
+
 def l2_flush_buffer(dev):
     """Two buffers of 256 MB, each about twice the GB300's L2: one to overwrite, one to read."""
     import torch
@@ -500,12 +526,30 @@ def secondary(pa, dev, args, peaks, stream):
         r5.attention()
     ms5 = time_calls(r5.attention, n, stream)
     kv5 = kv_bytes(w5)
+    # bytes the decode kernel actually read from DRAM (shared blocks once, the rest through
+    # L2), from the committed ncu capture of this call
+    uniq = ncu_traffic("k_mma16", w5.name)
     res["shared_prefix"] = {"workload": w5.name, "logical_kv_bytes": kv5, "ms": ms5,
                             "logical_gbs": kv5 / (ms5 * 1e-3) / 1e9,
+                            "dram_bytes": uniq,
+                            "dram_gbs": None if uniq is None else uniq / (ms5 * 1e-3) / 1e9,
                             "tokens_per_s": w5.num_tokens / (ms5 * 1e-3)}
     assert pa.pa_device_status() == pa.PA_OK
     del w5, r5
     torch.cuda.empty_cache()
+
+    # the tiny fp32 mixed batch: a latency figure (general kernel; far too small to load the
+    # GPU), per attention call and per whole step
+    w1 = workloads.named(1, seed=args.seed, device=dev)
+    r1 = Runner(pa, w1)
+    for _ in range(3):
+        r1.step()
+    ms1a = time_calls(r1.attention, n, stream)
+    ms1s = time_calls(r1.step, n, stream)
+    assert pa.pa_device_status() == pa.PA_OK
+    res["tiny_mixed"] = {"workload": w1.name, "tokens": w1.num_tokens, "us_per_call": ms1a * 1e3,
+                         "us_per_step": ms1s * 1e3, "dtype": "f32"}
+    del w1, r1
     return res
 
 
@@ -535,6 +579,18 @@ def main():
         print(json.dumps(dict(case="decode-fp8", **fp8_decode(pa, dev, args, peaks,
                                                                torch.cuda.current_stream(),
                                                                args.steps))), flush=True)
+        return
+    if args.case in ("splitkv", "shared-prefix", "tiny"):
+        w = workloads.named({"splitkv": 4, "shared-prefix": 5, "tiny": 1}[args.case],
+                            seed=args.seed, device=dev)
+        r = Runner(pa, w)
+        for _ in range(max(3, args.warmup)):
+            r.attention()
+        ms = time_calls(r.attention, args.steps, torch.cuda.current_stream())
+        assert pa.pa_device_status() == pa.PA_OK
+        kv = kv_bytes(w)
+        print(json.dumps({"case": w.name, "kv_bytes": kv, "ms": ms,
+                          "gbs": kv / (ms * 1e-3) / 1e9}), flush=True)
         return
     if args.case == "prefill-chunks":
         wp = workloads.prefill_chunks(seed=args.seed, device=dev)
@@ -571,13 +627,15 @@ def main():
     sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
     with sampler:
         time.sleep(0.3)
-        # ---- whole step, inputs resident in HBM
+        # ---- whole step, inputs resident in HBM: the loop of --steps steps, repeated
         barrier()
         torch.cuda.synchronize()
-        step_ms = time_calls(run.step, args.steps, stream)
+        step_reps = time_repeats(run.step, args.steps, stream, args.min_timed_ms)
+        step_ms = statistics.median(step_reps)
         barrier()
         # ---- the attention call alone (the dominant kernels)
-        attn_ms = time_calls(run.attention, args.steps, stream)
+        attn_reps = time_repeats(run.attention, args.steps, stream, args.min_timed_ms / 2)
+        attn_ms = statistics.median(attn_reps)
 
         # ---- end to end through the public API with host buffers: every step copies its
         # inputs (packed in one pinned buffer) to the device and its output back, on a copy
@@ -647,7 +705,9 @@ def main():
     if rank != 0:
         return
     achieved = kvb / (attn_ms * 1e-3) / 1e9
-    kernel = "k_mma16" if run.varlen else "k_mma16"
+    # the decode batch's attention kernel, and the split-KV partials kernel (the same
+    # warp-MMA kernel in its split mode); ncu traffic is recorded per (kernel, workload)
+    kernel = "k_mma16"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
@@ -660,6 +720,8 @@ def main():
                    "l2": f"inputs larger than L2 ({kvb / 1e6:.0f} MB of K/V read per step)",
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": T * world / (step_ms * 1e-3),
+        "timing": {"step": spread(step_reps), "attention_call": spread(attn_reps),
+                   "steps_per_repeat": args.steps},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -667,7 +729,9 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": ncu_traffic(kernel, w.name),
-                     "kernel": "attention call (validate+plan, attention kernels)",
+                     "kernel": kernel,
+                     "timed_as": "one library call: the validate+plan kernel (a few us, "
+                                 "overlapped by programmatic dependent launch) and " + kernel,
                      "peak_kind": f"{peaks['kind']} hbm_gbs (copy)", "ms_per_launch": attn_ms},
     }
     if not args.no_secondary:

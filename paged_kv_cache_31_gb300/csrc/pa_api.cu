@@ -14,11 +14,31 @@
 __device__ int g_pa_status = 0;
 
 namespace pa {
+
+// The driver context current on this thread (CUcontext), or nullptr when there is none or the
+// driver entry point cannot be had.
+void* current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
+  void* ctx = nullptr;  // the context the address below was looked up in
   int* status = nullptr;
   int sms = 0;
 };
@@ -26,14 +46,17 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
-// Status-word address and SM count of the current device, looked up once per device with
-// that device current.
+// Status-word address and SM count of the current device, looked up with that device
+// current, and again whenever the current context is not the one of the last lookup (after
+// cudaDeviceReset, or under another driver context, the module is loaded anew and its
+// __device__ variables may sit elsewhere).
 const DeviceState* device_state() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& d = g_dev[dev];
-  if (!d.status) {
+  if (!d.status || !ctx || d.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_pa_status) != cudaSuccess) return nullptr;
     int sms = 0;
@@ -41,6 +64,8 @@ const DeviceState* device_state() {
       return nullptr;
     d.sms = sms;
     d.status = static_cast<int*>(p);
+    // looked up again (the runtime may have just made the primary context current)
+    d.ctx = current_context();
   }
   return &d;
 }
@@ -169,6 +194,39 @@ int num_sms() {
   const DeviceState* d = device_state();
   return d ? d->sms : 0;
 }
+
+// The argument checks of the varlen attention calls, in their order, except for the
+// workspace: shapes (PA_ESHAPE), types (PA_EUNSUPPORTED), scales and flags (PA_EINVAL), head
+// size (PA_EUNSUPPORTED), negative counts (PA_EINVAL), token count (PA_EUNSUPPORTED), then
+// null pointers (PA_EINVAL).  *empty is set for a batch with no sequence and no token, which
+// is PA_OK with nothing to launch (pointers unchecked).
+pa_status varlen_check(const void* q, const void* k_blocks, const void* v_blocks,
+                       const void* out, const int32_t* query_start_loc, const int32_t* seq_lens,
+                       const int32_t* positions, const int32_t* block_tables, int32_t num_seqs,
+                       int64_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                       int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
+                       float k_scale, float v_scale, uint32_t flags, bool* empty) {
+  *empty = false;
+  if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_heads % num_kv_heads != 0)
+    return PA_ESHAPE;
+  if (!dtype_ok(q_dtype) || !pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_EINVAL;
+  if (flags & ~(uint32_t)PA_FLAG_BITWISE) return PA_EINVAL;
+  if (head_dim > 256) return PA_EUNSUPPORTED;
+  if (num_seqs < 0 || num_tokens < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return PA_EINVAL;
+  if (num_tokens > INT32_MAX / 2) return PA_EUNSUPPORTED;
+  if (num_seqs == 0 && num_tokens == 0) {
+    *empty = true;
+    return PA_OK;
+  }
+  if (!q || !k_blocks || !v_blocks || !out || !query_start_loc || !seq_lens || !positions ||
+      !block_tables)
+    return PA_EINVAL;
+  return PA_OK;
+}
+
 
 }  // namespace pa
 
@@ -348,19 +406,14 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
                              const float* v_scales, uint32_t flags, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream,
                              const CacheArgs* cache) {
-  if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-      num_heads % num_kv_heads != 0)
-    return PA_ESHAPE;
-  if (!dtype_ok(q_dtype) || !pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
-  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_EINVAL;
-  if (flags & ~(uint32_t)PA_FLAG_BITWISE) return PA_EINVAL;
-  if (head_dim > 256) return PA_EUNSUPPORTED;
-  if (num_seqs < 0 || num_tokens < 0 || num_blocks < 0 || max_blocks_per_seq < 0) return PA_EINVAL;
-  if (num_tokens > INT32_MAX / 2) return PA_EUNSUPPORTED;
-  if (num_seqs == 0 && num_tokens == 0) return PA_OK;
-  if (!q || !k_blocks || !v_blocks || !out || !query_start_loc || !seq_lens || !positions ||
-      !block_tables || !workspace)
-    return PA_EINVAL;
+  bool empty = false;
+  const pa_status chk = varlen_check(q, k_blocks, v_blocks, out, query_start_loc, seq_lens,
+                                     positions, block_tables, num_seqs, num_tokens, num_heads,
+                                     num_kv_heads, head_dim, block_size, num_blocks,
+                                     max_blocks_per_seq, q_dtype, kv_dtype, k_scale, v_scale,
+                                     flags, &empty);
+  if (chk != PA_OK || empty) return chk;
+  if (!workspace) return PA_EINVAL;
   const size_t need = pa_varlen_forward_workspace_size(num_seqs, num_tokens, num_heads,
                                                        num_kv_heads, head_dim, max_blocks_per_seq,
                                                        block_size);

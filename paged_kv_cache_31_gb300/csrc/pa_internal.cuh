@@ -429,5 +429,14 @@ cudaError_t launch_merge_attn_states(void* out, float* out_lse, const void* pref
                                      int bf16, int* status, cudaStream_t stream);
 
 int num_sms();  // SM count of the current device (cached)
+void* current_context();  // the calling thread's current driver context (CUcontext), or null
+// argument checks of the varlen attention calls (all but the workspace); see pa_api.cu
+pa_status varlen_check(const void* q, const void* k_blocks, const void* v_blocks,
+                       const void* out, const int32_t* query_start_loc, const int32_t* seq_lens,
+                       const int32_t* positions, const int32_t* block_tables, int32_t num_seqs,
+                       int64_t num_tokens, int32_t num_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                       int32_t max_blocks_per_seq, pa_dtype q_dtype, pa_dtype kv_dtype,
+                       float k_scale, float v_scale, uint32_t flags, bool* empty);
 
 }  // namespace pa

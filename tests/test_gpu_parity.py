@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from paged_kv_cache_31_gb300 import workloads
-from tests.gpu_helpers import assert_attn_close, oracle_attention, sub_batch
+from tests.gpu_helpers import assert_attn_close, oracle_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -138,7 +138,7 @@ def test_unwritten_tail_slots_are_never_read(pa):
 
 
 # ------------------------------------------------------------------------------------------
-# full-size workloads: every output of the decode batch, sampled sequences of the others
+# full-size workloads: every output of the decode, mixed and shared-prefix batches
 
 
 def test_decode_batch_full(pa):
@@ -149,26 +149,46 @@ def test_decode_batch_full(pa):
     assert_attn_close(out, oracle_attention(w, okb, ovb), w.name)
 
 
-def test_mixed_window_batch_full_sampled(pa):
+def test_mixed_window_batch_full(pa):
+    """All 4344 rows of the mixed batch (248 decode tokens and the 8 prefill chunks of 512
+    tokens, window 4096), as one call runs them: the decode tiles on the warp-MMA kernel and
+    the chunks on the tcgen05 kernel, both in their persistent longest-first orders."""
     w = workloads.named(3, device=DEV)
     slots, kb, vb, out = _step(pa, w)
     okb, ovb = _oracle_cache(w, slots)
     assert torch.equal(kb.cpu(), okb) and torch.equal(vb.cpu(), ovb)
-    g = torch.Generator().manual_seed(3)
-    dec = torch.randperm(248, generator=g)[:24].tolist()
-    seqs = sorted(dec) + [248, 255]  # two of the eight prefill chunks
-    ref = oracle_attention(w, okb, ovb, seqs=seqs)
-    rows = sub_batch(w, seqs)["rows"]
-    assert_attn_close(out.cpu()[rows], ref, w.name)
+    ref = oracle_attention(w, okb, ovb)
+    assert_attn_close(out, ref, w.name)
 
 
-def test_shared_prefix_full_sampled(pa):
+def test_shared_prefix_full(pa):
+    """All 256 fork sequences (128 shared physical blocks, private tails) against the oracle."""
     w = workloads.named(5, device=DEV)
     slots, kb, vb, out = _step(pa, w)
     okb, ovb = _oracle_cache(w, slots)
-    seqs = list(range(0, 256, 9))
-    ref = oracle_attention(w, okb, ovb, seqs=seqs)
-    assert_attn_close(out.cpu()[sub_batch(w, seqs)["rows"]], ref, w.name)
+    assert torch.equal(kb.cpu(), okb) and torch.equal(vb.cpu(), ovb)
+    assert_attn_close(out, oracle_attention(w, okb, ovb), w.name)
+
+
+def test_shared_prefix_each_sequence_alone_equals_batch(pa):
+    """The shared-prefix workload's own check: each of the 256 sequences, run alone through
+    pa_varlen_forward on the same pool (the 128 shared blocks included), gives its row of the
+    256-sequence batch bit for bit."""
+    w = workloads.named(5, device=DEV)
+    slots, kb, vb, batch = _step(pa, w)
+    qsl = w.query_start_loc.cpu().tolist()
+    assert (w.block_tables[:, :128] == w.block_tables[0, :128]).all(), "prefix not shared"
+    ws = pa.workspace_for(w.q, kb, w.query_start_loc, w.block_tables)
+    for s in range(w.num_seqs):
+        a, b = qsl[s], qsl[s + 1]
+        one = torch.full_like(w.q[a:b], 7.25)
+        pa.pa_varlen_forward(w.q[a:b], kb, vb, one,
+                             torch.tensor([0, b - a], dtype=torch.int32, device=DEV),
+                             w.seq_lens[s:s + 1], w.positions[a:b],
+                             w.block_tables[s:s + 1].contiguous(), w.scale, causal=w.causal,
+                             sliding_window=w.sliding_window, workspace=ws)
+        assert torch.equal(one, batch[a:b]), f"sequence {s} differs alone vs in the batch"
+    assert pa.pa_device_status() == pa.PA_OK
 
 
 # ------------------------------------------------------------------------------------------
