@@ -115,13 +115,22 @@ __global__ void __launch_bounds__(NW * 32, 2)
   }
   fence_mbar_init();
   // varlen launches overlap the kernels before them (programmatic dependent launch): the
-  // plan, the status word and the inputs are read only after those have finished
-  pdl_wait();
+  // plan, the status word and the inputs are read only after those have finished.  Behind
+  // the tcgen05 kernel this kernel cannot start before every CTA of that kernel has passed
+  // its own wait for the plan, so the plan (and all work before it) is complete already and
+  // the decode tiles run alongside the prefill items; the wait for the tcgen05 kernel itself
+  // comes before the recomputed items and before this kernel ends, so that whatever follows
+  // on the stream finds both kernels finished.
+  const bool after_tc = !SPLIT && p.after_tc != 0;
+  if (!after_tc) pdl_wait();
   // failed validation or an earlier sticky error: the whole CTA writes nothing
   if (threadIdx.x == 0) *fail = status_set(p.status) ? 1 : 0;
   __syncthreads();
-  if constexpr (!SPLIT) pdl_launch_dependents();  // the prefill kernel's prologue may start
-  if (*reinterpret_cast<volatile int*>(fail)) return;
+  if constexpr (!SPLIT) pdl_launch_dependents();  // the next kernel's prologue may start
+  if (*reinterpret_cast<volatile int*>(fail)) {
+    if (after_tc) pdl_wait();
+    return;
+  }
 
   const VarlenMeta& m = p.m;
   const int G = m.group;
@@ -129,10 +138,13 @@ __global__ void __launch_bounds__(NW * 32, 2)
   uint32_t ring_pos = 0;  // blocks this warp has pushed through its ring so far
 
   // Split-KV: grid (partition x sequence, kv head), strided.  Varlen: a persistent 1-D grid
-  // whose CTAs take (item, kv head) units from the plan's work counter, longest items first.
+  // whose CTAs take (item, kv head) units from the plan's work counter, longest items first;
+  // then (behind the tcgen05 kernel) the 16-row tiles of the 256-row items that kernel marked
+  // (V outside f16's range), from a second counter.
   int n_units;
   const int2* items = nullptr;
   int* unit_slot = fail + 1;
+  int phase = 0;
   if constexpr (SPLIT) {
     n_units = m.num_seqs * p.max_parts;
   } else {
@@ -147,10 +159,20 @@ __global__ void __launch_bounds__(NW * 32, 2)
       if (item >= n_units) break;
       kvh = blockIdx.y;
     } else {
-      if (threadIdx.x == 0) *unit_slot = atomicAdd(const_cast<int32_t*>(p.plan) + 2, 1);
+      if (threadIdx.x == 0) {
+        const int u = atomicAdd(const_cast<int32_t*>(p.plan) + (phase ? 4 : 2), 1);
+        *unit_slot = u < n_units ? u : -1;
+      }
       __syncthreads();
       const int unit = *reinterpret_cast<volatile int*>(unit_slot);
-      if (unit >= n_units) break;
+      if (unit < 0) {
+        if (phase == 1 || !after_tc) break;
+        __syncthreads();  // every thread has read the slot before it is written again
+        pdl_wait();       // the tcgen05 kernel has finished: its marks are final
+        phase = 1;
+        n_units = *reinterpret_cast<const volatile int32_t*>(p.plan + 3) * 16 * m.num_kv_heads;
+        continue;
+      }
       item = unit / m.num_kv_heads;
       kvh = unit % m.num_kv_heads;
     }
@@ -163,7 +185,14 @@ __global__ void __launch_bounds__(NW * 32, 2)
       row0 = 0;
       rows_total = G;
     } else {
-      const int2 it = items[item];
+      int2 it;
+      if (phase == 0) {
+        it = items[item];
+      } else {  // tile item % 16 of marked item item / 16: (sequence, 16-row tile index)
+        const int4 t4 =
+            reinterpret_cast<const int4*>(p.plan + p.tc_off)[p.plan[p.redo_list_off + item / 16]];
+        it = make_int2(t4.x, t4.y * 16 + item % 16);
+      }
       s = it.x;
       row0 = it.y * 16;
       qs = m.query_start_loc[s];
@@ -482,7 +511,10 @@ __global__ void __launch_bounds__(NW * 32, 2)
       lrow[r] += __shfl_xor_sync(kFull, lrow[r], 2);
     }
     __syncthreads();  // every warp is done with its ring: the O area may alias it now
-    if (*reinterpret_cast<volatile int*>(fail)) return;
+    if (*reinterpret_cast<volatile int*>(fail)) {
+      if (after_tc) pdl_wait();
+      return;
+    }
     {
       const int r0 = lane >> 2;
       if ((lane & 3) == 0) {

@@ -190,6 +190,8 @@ __global__ void __launch_bounds__(1024)
       if (s_err > 0) record_error(status, s_err);
       plan[0] = 0;
       plan[1] = 0;
+      plan[3] = 0;
+      plan[4] = 0;
     }
     return;
   }
@@ -274,10 +276,14 @@ __global__ void __launch_bounds__(1024)
     const int at = atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
     for (int i = 0; i < cm; ++i) mma_items[at + i] = make_int2(s, i);
   }
+  // no 256-row item is marked for recomputing yet (the tcgen05 kernel marks them)
+  for (int k = tid; k < carry_t; k += blockDim.x) plan[L.redo_off + k] = 0;
   if (tid == 0) {
     plan[0] = carry_m;
     plan[1] = carry_t;
     plan[2] = 0;  // work counter of the warp-MMA kernel
+    plan[3] = 0;  // items marked by the tcgen05 kernel
+    plan[4] = 0;  // work counter over their units
   }
 }
 

@@ -17,24 +17,33 @@
 // the peer's arrivals (the peer's idle issuer warps forward "my part of this stage has landed"
 // with remote mbarrier arrives), and the MMA completions are multicast to both CTAs.
 //
-// One CTA per SM, persistent over items, 12 warps; warps 0..3 (one warpgroup) give up
-// registers to the two softmax warpgroups (setmaxnreg: 56 and 224 per thread):
+// One CTA per SM, persistent over items, 16 warps; the producer / issuer and converter
+// warpgroups give up registers to the two softmax warpgroups (setmaxnreg: 56, 200, 200, 56):
 //   warp 0      TMA producer of Q (two buffers, so the next item's Q loads while this one
 //               finishes) and of this CTA's part of K_j through a 3-stage ring; warp 2
 //               produces its part of V_j through a 6-stage ring;
-//   warp 1      TMEM owner and QK^T issuer; warp 3 issues PV and zeroes the never-written
-//               V rows past a sequence's end in this CTA's part.  In the leader lane 0 issues,
+//   warp 1      TMEM owner and QK^T issuer; warp 3 issues PV.  In the leader lane 0 issues,
 //               in warp-uniform code:
-//                 S_j = Q K_j^T      (M 256, N 128, K 128: 8 MMAs, K-major operands)
-//                 O  += P_j V_j      (P as a bf16 hi/lo pair read from TMEM: 16 MMAs, V MN-major)
-//               In the peer the two warps forward the Q / K and V arrivals to the leader.
+//                 S_j = Q K_j^T      (M 256, N 128, K 128: 8 MMAs, bf16, K-major operands)
+//                 O  += P_j V_j      (f16 P read from TMEM, f16 V: 8 MMAs, V MN-major)
+//               In the peer warp 1 forwards the Q / K arrivals to the leader.
 //               TMEM columns: three S buffers at 0 / 128 / 384, O at 256.  P_j is written over
 //               the S_j it came from, so S_{j+3} may only be issued once P_j V_j is done;
 //   warps 4..11 softmax: two threads per query row (TMEM lane = row), one per 64-column
 //               half; mask, row max (combined through shared memory), exp2, row sum, P to
-//               tensor memory, lazy O rescale, and the epilogue o = O * (1 / l) -> bf16.
+//               tensor memory as f16, lazy O rescale, and the epilogue o = O * (1 / l) -> bf16.
 //               A softmax thread waits for the previous P V only when it must rescale O,
-//               so the exponentials of tile j run while the tensor core works on tile j - 1.
+//               so the exponentials of tile j run while the tensor core works on tile j - 1;
+//   warps 12..15 V converters, one per SM sub-partition: each widens a quarter of every V
+//               stage of its CTA (32 keys x 64 dims) from bf16 to f16 in place, zeroes the
+//               never-written rows past the sequence's end, and arrives on the leader's
+//               V-ready barrier, which the PV issuer waits for.
+// P enters the PV product as one f16 value (11 significant bits; the row sum l adds the fp32
+// weights), with V widened exactly to f16: a bf16 value converts without error when its
+// magnitude is below 65520 (below 2^-14 it becomes an f16 subnormal, off by at most 2^-25).
+// A stage holding a larger magnitude (or an inf / NaN) marks its 256-row item; the warp-MMA
+// kernel that runs after this one recomputes every marked item from the bf16 pool (bf16 hi /
+// lo weights), overwriting what this kernel wrote for it.
 // The online softmax follows the per-tile update of the tinyllm decode page (section 2.2)
 // with one change that leaves the result unchanged: the reference max m is only moved (and
 // O, l rescaled by 2^(m_old - m_new)) when a tile's max exceeds it by more than 8 (log2
@@ -71,15 +80,19 @@ constexpr int kOffXchg = kOffFlag + 16;
 constexpr int kSmemBytes = kOffXchg + 2 * 2 * 128 * 4 + 1024;  // + slack to align the base
 constexpr uint32_t kBadMax = 0x7fc0dea1u;  // a NaN that no arithmetic produces (canonical 7fffffff)
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
-constexpr int kSoftWarps = 8;                         // two column halves x four lane quarters
-constexpr int kThreads = 64 + kSoftWarps * 32 + 64;  // + the V producer and PV issuer warps
+constexpr int kSoftWarps = 8;   // two column halves x four lane quarters
+constexpr int kConvWarps = 4;   // V converters, a quarter of each V stage each
+constexpr int kThreads = 128 + kSoftWarps * 32 + kConvWarps * 32;
+constexpr int kFirstConvWarp = 4 + kSoftWarps;
+
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;    // O: columns 256..383
 __device__ __forceinline__ uint32_t col_s(uint32_t b) { return b == 2 ? 384u : b * 128u; }
 // Inside an S buffer, P_j of key half h (keys 64h .. 64h+63) is stored by the thread that read
-// those scores: hi at columns 64h .. 64h+31, lo at 64h+32 .. 64h+63 (two bf16 per column).
-__device__ __forceinline__ uint32_t col_p(int kstep, int lo) {
-  return (uint32_t)((kstep >> 2) * 64 + lo * 32 + (kstep & 3) * 8);
+// those scores, at columns 64h .. 64h+31 (two f16 per column); the MMA of key step k (keys
+// 16k .. 16k+15) reads 8 columns from col_p(k).
+__device__ __forceinline__ uint32_t col_p(int kstep) {
+  return (uint32_t)((kstep >> 2) * 64 + (kstep & 3) * 8);
 }
 
 // barrier indices (the per-stage / per-buffer ones are consecutive)
@@ -90,7 +103,8 @@ enum : int {
   B_KEMPTY = B_KFULL + kStagesK,
   B_VFULL = B_KEMPTY + kStagesK,
   B_VEMPTY = B_VFULL + kStagesV,
-  B_SFULL = B_VEMPTY + kStagesV,
+  B_VCONV = B_VEMPTY + kStagesV,  // leader: the stage's V is f16 in both CTAs
+  B_SFULL = B_VCONV + kStagesV,
   B_PFULL = B_SFULL + kSBufs,
   B_PVDONE = B_PFULL + kSBufs,
   B_OFREE = B_PVDONE + kSBufs,
@@ -189,13 +203,14 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 operands and an fp32 accumulator.
-constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16 with an fp32 accumulator; A and B both bf16 (bf16 = 1)
+// or both f16 (bf16 = 0).
+constexpr uint32_t idesc_f16kind(int M, int N, int b_mn_major, int bf16) {
+  return (1u << 4) | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10) |
+         ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t kIdescQK = idesc_bf16(256, 128, 0);  // M spans the pair
-constexpr uint32_t kIdescPV = idesc_bf16(256, 128, 1);
+constexpr uint32_t kIdescQK = idesc_f16kind(256, 128, 0, 1);  // bf16 Q, K; M spans the pair
+constexpr uint32_t kIdescPV = idesc_f16kind(256, 128, 1, 0);  // f16 P, V
 
 // ---- thread-block cluster (pairs of CTAs on two SMs) ------------------------------------------
 
@@ -238,6 +253,7 @@ __device__ __forceinline__ void arrive_leader(uint64_t* bar) {
       "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
+
 
 // 2^x with the SFU's approximate base-2 exponential (flush-to-zero; 2^-inf = 0).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -426,9 +442,9 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
 
 // MMA issue runs on two threads of the leader (warps 1 and 3) so that one thread's
 // instruction issue never delays the other chain: the QK^T issuer releases K and Q stages, the
-// PV issuer releases V stages, S / P buffers and O.  In the peer the same warps forward the
-// arrival of its Q / K parts and (after zeroing unwritten rows) V parts to the leader's full
-// barriers, which count two arrivals: the leader's own producer and the peer's forward.
+// PV issuer releases V stages, S / P buffers and O.  In the peer warp 1 forwards the arrival
+// of its Q / K parts to the leader's full barriers, which count two arrivals: the leader's own
+// producer and the peer's forward; the V parts reach the leader through the converters.
 //
 // Tile counters run over all items of the CTA; tile s uses S / P buffer s % 3, and each
 // per-buffer barrier completes once per use, so its phase parity is (s / 3) & 1.
@@ -470,57 +486,105 @@ __device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_i
   }
 }
 
-// The whole warp runs the PV loop (lane 0 issues): the V rows of a sequence's last block at
-// positions >= n were never written and may hold anything, so before the MMAs read that block
-// each CTA's warp zeroes them in its own part of the stage (the peer then forwards the stage
-// to the leader).  This role consumes the V stages in order, so its V-full wait always names
-// the right phase.
+// The leader's whole warp runs the PV loop (lane 0 issues): O += P_j V_j once P_j is in
+// tensor memory and both CTAs' parts of V_j are f16.  The peer's warp has nothing to do.
 __device__ void pv_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
-  const int lane = threadIdx.x & 31;
+  if (c.rank != 0) return;
   uint32_t kv = 0, it_cnt = 0;
   for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
-    const int last_blk = (I.n - 1) / 16;
-    const int fix_rel = last_blk * 16 - I.kv0;  // offset of that block inside the item's keys
-    const bool need_fix = (I.n % 16) != 0 && last_blk < I.nblk_vis && fix_rel >= 0;
-    const int fix_tile = need_fix ? fix_rel / kBN : -1;
-    const bool leader = c.rank == 0;
     for (int j = 0; j < I.ntiles; ++j) {
       const uint32_t s = kv + j, st = s % kStagesV, b = buf_of(s);
-      if (leader) {
-        if (j == 0 && !__all_sync(kFull, wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u))) return;
-        if (!__all_sync(kFull, wait_bar(c, B_PFULL + b, use_par(s)))) return;
-      }
-      if (!__all_sync(kFull, wait_bar(c, B_VFULL + st, (s / kStagesV) & 1u))) return;
-      uint8_t* vt = c.sm + kOffV + st * kPart;
-      if (j == fix_tile) {
-        const int blk = (fix_rel % kBN) / 16, first = I.n % 16;
-        const int chunks = (16 - first) * 8;  // rows x 16-byte chunks of this CTA's 64 dims
-        for (int i = lane; i < chunks; i += 32) {
-          const int rr = first + i / 8, ch = i & 7;
-          *reinterpret_cast<uint4*>(vt + (blk * 16 + rr) * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-        }
-        // the MMA (issued by the leader) reads V through the async proxy
-        asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-        __syncwarp();
-      }
-      if (!leader) {
-        if (lane == 0) arrive_leader(c.bar + B_VFULL + st);
-        continue;
-      }
+      if (j == 0 && !__all_sync(kFull, wait_bar(c, B_OFREE, (it_cnt & 1u) ^ 1u))) return;
+      if (!__all_sync(kFull, wait_bar(c, B_PFULL + b, use_par(s)))) return;
+      if (!__all_sync(kFull, wait_bar(c, B_VCONV + st, (s / kStagesV) & 1u))) return;
       tc_fence_after();
-      const uint32_t vb = smem_u32(vt), pb = tmem + col_s(b);
+      const uint32_t vb = smem_u32(c.sm + kOffV + st * kPart), pb = tmem + col_s(b);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc_mma_ta_l0(tmem + kColO, pb + col_p(kk, 0), sdesc(vb + kk * 2048, 1024, 1024),
-                     kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        tc_mma_ta_l0(tmem + kColO, pb + col_p(kk, 1), sdesc(vb + kk * 2048, 1024, 1024),
-                     kIdescPV, 1u);
+        tc_mma_ta_l0(tmem + kColO, pb + col_p(kk), sdesc(vb + kk * 2048, 1024, 1024), kIdescPV,
+                     (j > 0 || kk > 0) ? 1u : 0u);
       tc_commit_mc_l0(c.bar + B_PVDONE + b, 0x3);
       tc_commit_mc_l0(c.bar + B_VEMPTY + st, 0x3);
       __syncwarp();
+    }
+    kv += I.ntiles;
+  }
+}
+
+// bf16x2 -> f16x2, each half through fp32 (the widening to fp32 is exact; the narrowing
+// rounds to nearest even and is exact for magnitudes below 65520 down to f16's subnormal
+// step).  The high element goes to the high half.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;"
+      : "=r"(r)
+      : "f"(__uint_as_float(w & 0xffff0000u)), "f"(__uint_as_float(w << 16)));
+  return r;
+}
+// acc + h * 0 on f16 pairs: stays finite (+-0 added) until a half of h is infinite or NaN,
+// then NaN for good -- one instruction per word tells whether any widening overflowed.
+__device__ __forceinline__ uint32_t f16x2_poison(uint32_t acc, uint32_t h) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(h), "r"(0u), "r"(acc));
+  return r;
+}
+
+// V converter warp w (0..3) of either CTA: for every V stage of its CTA, once the TMA has
+// landed, the quarter holding keys 32w .. 32w + 31 (this CTA's 64 dims, 4 KB: rows of 128
+// bytes, the 128-byte swizzle only permutes 16-byte chunks inside a row) is widened from bf16
+// to f16 in place; rows at positions >= seq_len (never written: they may hold anything) become
+// zeros.  Then the leader's V-ready barrier of the stage gets this warp's arrival.  A quarter
+// with a value that f16 cannot hold (its magnitude rounds to infinity; an inf or NaN too)
+// marks the item for the recompute after this kernel.
+//
+// The arrival is a plain remote arrive, as for the other forwards: a cluster-scope release
+// on it stalls the warp on a memory barrier per stage, which measured 40% slower per call.
+// The stores are to this CTA's own shared memory, and fence.proxy.async (shared::cta) makes
+// them visible to the asynchronous proxy, through which the pair's MMAs read them.
+__device__ void v_converter(const Ctx& c, const TcParams& p, int n_items) {
+  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) - kFirstConvWarp;
+  uint32_t kv = 0, it_cnt = 0;
+  for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
+    const Item I = load_item(p, idx, c.rank);
+    uint32_t poison = 0;  // f16 pair; NaN once a widened value overflowed
+    for (int j = 0; j < I.ntiles; ++j) {
+      const uint32_t s = kv + j, st = s % kStagesV;
+      if (!__all_sync(kFull, wait_bar(c, B_VFULL + st, (s / kStagesV) & 1u))) return;
+      uint8_t* q = c.sm + kOffV + st * kPart + w * 4096;
+      const int pos0 = I.kv0 + j * kBN + 32 * w;  // position of the quarter's first row
+      // two groups of four 16-byte chunks per lane (chunk lane + 32 i holds row (lane + 32 i) / 8)
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          v[i] = *reinterpret_cast<const uint4*>(q + (lane + 32 * (4 * g + i)) * 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ch = lane + 32 * (4 * g + i);
+          if (pos0 + (ch >> 3) >= I.n) {
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+          } else {
+            v[i].x = bf16x2_to_f16x2(v[i].x);
+            v[i].y = bf16x2_to_f16x2(v[i].y);
+            v[i].z = bf16x2_to_f16x2(v[i].z);
+            v[i].w = bf16x2_to_f16x2(v[i].w);
+            poison = f16x2_poison(f16x2_poison(poison, v[i].x), v[i].y);
+            poison = f16x2_poison(f16x2_poison(poison, v[i].z), v[i].w);
+          }
+          *reinterpret_cast<uint4*>(q + ch * 16) = v[i];
+        }
+      }
+      // the MMA (issued by the leader) reads V through the asynchronous proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) arrive_leader(c.bar + B_VCONV + st);
+    }
+    const bool over = (poison & 0x7fffu) > 0x7c00u || ((poison >> 16) & 0x7fffu) > 0x7c00u;
+    if (__any_sync(kFull, over) && lane == 0) {
+      const int pi = idx / p.m.num_kv_heads;  // the plan's 256-row item (all its kv heads)
+      if (atomicCAS(p.redo_flags + pi, 0, 1) == 0) p.redo_list[atomicAdd(p.redo_count, 1)] = pi;
     }
     kv += I.ntiles;
   }
@@ -617,11 +681,11 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
         m_ref = m_new;
         l *= alpha;
       }
-      // p = 2^(x * scale_log2 - m_ref) two at a time, the row sum, and p split into a bf16
-      // pair hi + lo (hi = RNE(p), lo = RNE(p - hi)) for the two P V MMAs
+      // p = 2^(x * scale_log2 - m_ref) two at a time (p <= 2^8), the row sum of the fp32
+      // weights, and p rounded to f16 for the P V MMAs
       const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
       const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(nbase, nbase);
-      uint32_t hi[32], lo[32];
+      uint32_t ph[32];
       {
         uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -630,14 +694,8 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
           f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sl2, nb2), a, bb);
           a = fast_exp2(a);
           bb = fast_exp2(bb);
-          const uint64_t pp = f2_pack(a, bb);
-          rs2[e & 3] = f2_add(rs2[e & 3], pp);
-          hi[e] = pack_bf16x2(a, bb);
-          const uint64_t hv =
-              f2_pack(__uint_as_float(hi[e] << 16), __uint_as_float(hi[e] & 0xffff0000u));
-          float la, lb;
-          f2_unpack(f2_sub(pp, hv), la, lb);
-          lo[e] = pack_bf16x2(la, lb);
+          rs2[e & 3] = f2_add(rs2[e & 3], f2_pack(a, bb));
+          ph[e] = pack_f16x2(a, bb);
         }
         float r0, r1, r2, r3, r4, r5, r6, r7;
         f2_unpack(rs2[0], r0, r1);
@@ -665,8 +723,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
         tmem_wait_st();
       }
       // this half of P over the scores it came from
-      tmem_st32(sbase, hi);
-      tmem_st32(sbase + 32, lo);
+      tmem_st32(sbase, ph);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -759,15 +816,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = cluster_rank() == 0;
   if (threadIdx.x == 0) {
     flags[1] = 0;
-    // leader: q/k/v full count its producer and the peer's forward, p_full / o_free one
-    // arrival per softmax warp of both CTAs, fin one per MMA-issuing warp; the empty / done
-    // barriers of both CTAs get one multicast commit per phase; the rest one arrival
+    // leader: q/k full count its producer and the peer's forward, v-ready one arrival per
+    // converter warp of both CTAs, p_full / o_free one per softmax warp of both CTAs, fin one
+    // per MMA-issuing warp; the empty / done barriers of both CTAs get one multicast commit
+    // per phase; the rest (v full included: this CTA's own TMA) one arrival
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t n = 1;
       if (leader) {
-        if ((i >= B_QFULL && i < B_QFULL + 2) || (i >= B_KFULL && i < B_KFULL + kStagesK) ||
-            (i >= B_VFULL && i < B_VFULL + kStagesV))
-          n = 2;
+        if ((i >= B_QFULL && i < B_QFULL + 2) || (i >= B_KFULL && i < B_KFULL + kStagesK)) n = 2;
+        if (i >= B_VCONV && i < B_VCONV + kStagesV) n = 2 * kConvWarps;
         if ((i >= B_PFULL && i < B_PFULL + kSBufs) || i == B_OFREE) n = 2 * kSoftWarps;
         if (i == B_FIN) n = 2;
       }
@@ -799,10 +856,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_rank(), (int)cluster_id_x(), (int)num_clusters_x()};
   const int n_items = flags[0] ? 0 : p.plan[1] * p.m.num_kv_heads;
 
-  // warps 0..3 (one warpgroup) produce and issue and need few registers; the two softmax
-  // warpgroups take theirs: 4 x 56 + 8 x 224 = 12 x 168, the launch's registers per thread
-  // (each branch ends the kernel itself, so no code runs under both limits)
-  if (warp < 4) {
+  // warps 0..3 (one warpgroup) produce and issue, warps 12..15 convert V: both need few
+  // registers; the two softmax warpgroups take theirs: 8 x 56 + 8 x 200 = 16 x 128, the
+  // launch's registers per thread (each branch ends the kernel itself, so no code runs under
+  // two limits)
+  if (warp >= kFirstConvWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    v_converter(c, p, n_items);
+    tc_fence_before();
+    cluster_sync();
+  } else if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     if (warp == 0) {
       producer(c, p, &tq, &tk, false, n_items);
@@ -835,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : "memory");
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     softmax_role(c, p, tmem, n_items);
     tc_fence_before();
     cluster_sync();

@@ -490,9 +490,6 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
     if (!pool_map(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) ||
         !pool_map(&tv, v_blocks, num_blocks, block_size, num_kv_heads, head_dim))
       return PA_ECUDA;
-    // the warp-MMA kernel first: when the batch has no decode-class sequences its CTAs find
-    // no work at once, and the tcgen05 kernel's prologue overlaps that (programmatic
-    // dependent launch); with decode tokens the order does not change the total
     Mma16Params p;
     std::memset(&p, 0, sizeof p);
     p.q = static_cast<const __nv_bfloat16*>(q);
@@ -503,23 +500,34 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
     p.status = d->status;
     p.scale_log2 = scale * kLog2e;
     mma_waits(p);
-    e = launch_mma16_varlen(tk, tv, p, head_dim, (int)std::min<int64_t>(L.mma_cap, 65535),
-                            stream);
-    if (e != cudaSuccess || !L.use_tc) return from_cuda(e);
-    CUtensorMap tq;
-    if (!query_map(&tq, q, num_tokens, num_heads, head_dim, m.group)) return PA_ECUDA;
-    TcParams tp;
-    std::memset(&tp, 0, sizeof tp);
-    tp.out = out;
-    tp.m = m;
-    tp.plan = plan;
-    tp.tc_off = L.tc_off;
-    tp.status = d->status;
-    tp.scale_log2 = scale * kLog2e;
-    tp.wait_limit_ns = kWaitLimitNs;
-    const int64_t work = L.tc_cap * num_kv_heads;
-    return from_cuda(
-        launch_tc_prefill(tq, tk, tv, tp, (int)std::min<int64_t>(work, d->sms), stream));
+    if (L.use_tc) {
+      // the tcgen05 kernel first, then the warp-MMA kernel: its decode tiles start as soon as
+      // every tcgen05 CTA has found the plan complete (programmatic dependent launch), on the
+      // SMs the tcgen05 kernel leaves free; after that kernel it recomputes the items the
+      // tcgen05 kernel marked (V outside f16's range)
+      CUtensorMap tq;
+      if (!query_map(&tq, q, num_tokens, num_heads, head_dim, m.group)) return PA_ECUDA;
+      TcParams tp;
+      std::memset(&tp, 0, sizeof tp);
+      tp.out = out;
+      tp.m = m;
+      tp.plan = plan;
+      tp.tc_off = L.tc_off;
+      tp.status = d->status;
+      tp.scale_log2 = scale * kLog2e;
+      tp.wait_limit_ns = kWaitLimitNs;
+      tp.redo_flags = plan + L.redo_off;
+      tp.redo_list = plan + L.redo_list_off;
+      tp.redo_count = plan + 3;
+      const int64_t work = L.tc_cap * num_kv_heads;
+      e = launch_tc_prefill(tq, tk, tv, tp, (int)std::min<int64_t>(work, d->sms), stream);
+      if (e != cudaSuccess) return PA_ECUDA;
+      p.after_tc = 1;
+      p.tc_off = L.tc_off;
+      p.redo_list_off = L.redo_list_off;
+    }
+    return from_cuda(launch_mma16_varlen(tk, tv, p, head_dim,
+                                         (int)std::min<int64_t>(L.mma_cap, 65535), stream));
   }
   SimtParams p;
   std::memset(&p, 0, sizeof p);

@@ -243,17 +243,21 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not lan
 //   [0] number of 16-row tile items (decode-class sequences, warp-MMA kernel)
 //   [1] number of 256-row items (prefill-class sequences, tcgen05 kernel)
 //   [2] work counter of the warp-MMA kernel (zeroed by the plan)
-//   [3..15] reserved
+//   [3] number of 256-row items the tcgen05 kernel marked for recomputing (zeroed by the plan)
+//   [4] work counter of the warp-MMA kernel over those items (zeroed by the plan)
+//   [5..15] reserved
 //   [tok_off, tok_off + T)        token -> sequence
 //   [cost_off, cost_off + S)      per sequence: keys its query rows can see (work estimate;
 //                                 written only for batches too large to keep it in smem)
 //   [mma_off, + 2 * mma_cap)      int2 items (seq, 16-row tile), longest first
 //   [tc_off, + 4 * tc_cap)        int4 items (seq, 256-row item, kv lo, kv hi), longest first
 //   [tc_tmp_off, + 4 * tc_cap)    the same items in sequence order (planning scratch)
+//   [redo_off, + tc_cap)          per 256-row item: marked for recomputing (zeroed by the plan)
+//   [redo_list_off, + tc_cap)     the marked items, in the order they were marked
 constexpr int kPlanHeaderWords = 16;
 
 struct PlanLayout {
-  int64_t tok_off, cost_off, mma_off, tc_off, tc_tmp_off;
+  int64_t tok_off, cost_off, mma_off, tc_off, tc_tmp_off, redo_off, redo_list_off;
   int64_t mma_cap, tc_cap;
   int64_t words;
   int32_t use_tc;       // prefill-class sequences go to the tcgen05 kernel
@@ -270,7 +274,9 @@ inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t grou
   L.mma_off = (L.cost_off + num_seqs + 3) & ~int64_t(3);
   L.tc_off = (L.mma_off + 2 * L.mma_cap + 3) & ~int64_t(3);
   L.tc_tmp_off = L.tc_off + 4 * L.tc_cap;
-  L.words = L.tc_tmp_off + 4 * L.tc_cap;
+  L.redo_off = L.tc_tmp_off + 4 * L.tc_cap;
+  L.redo_list_off = L.redo_off + L.tc_cap;
+  L.words = L.redo_list_off + L.tc_cap;
   L.use_tc = 0;
   L.tc_min_rows = 64;
   return L;
@@ -323,6 +329,12 @@ struct Mma16Params {
   int32_t max_parts;
   uint64_t wait_limit_ns;
   uint32_t debug_stall;  // tests only: every block wait runs out (see mma_debug_stall)
+  // varlen, launched behind the tcgen05 kernel: the decode tiles do not wait for that kernel
+  // (the plan is complete once it has started), and the 256-row items it marked are
+  // recomputed after it has finished, 16 rows x one kv head per unit
+  int32_t after_tc;
+  int64_t tc_off;         // word offset of the int4 256-row items
+  int64_t redo_list_off;  // word offset of the list of marked items
 };
 
 struct SimtParams {
@@ -352,6 +364,11 @@ struct TcParams {
   int* status;
   float scale_log2;
   uint64_t wait_limit_ns;
+  // items whose V does not fit f16 (recomputed by the warp-MMA kernel afterwards): a flag per
+  // 256-row item, the list of marked items and its length (all in the plan)
+  int32_t* redo_flags;
+  int32_t* redo_list;
+  int32_t* redo_count;
 };
 
 // ---- launchers (defined next to their kernels) --------------------------------------------

@@ -114,3 +114,32 @@ def test_prefill_output_only_16_byte_aligned(pa):
     assert pa.pa_device_status() == pa.PA_OK
     assert torch.equal(out, aligned)
     assert torch.isnan(buf[:8].float()).all()
+
+
+@pytest.mark.parametrize("big", [5.99e4, -6.5e4, 1.0e6, -1.0e30])
+def test_prefill_v_beyond_f16_range(pa, big):
+    """The tcgen05 kernel multiplies f16 weights with V widened to f16.  A V magnitude that f16
+    holds (below 65520) is widened exactly; a larger one marks its 256-row item, which the
+    warp-MMA kernel recomputes from the bf16 pool after the tcgen05 kernel.  Either way the
+    output matches the oracle.  The large values sit at random visible positions, including
+    keys that the causal mask hides from some rows of the same item (where an f16 infinity
+    times a zero weight would be NaN), next to decode tokens that run alongside."""
+    prior = [0, 300, 45, 1000, 17]
+    chunk = [200, 129, 96, 1, 1]
+    H, Hkv = 32, 8
+    w = workloads.build("prebig", seq_lens=[p + c for p, c in zip(prior, chunk)], q_lens=chunk,
+                        num_heads=H, num_kv_heads=Hkv, head_dim=128, seed=21, device=DEV)
+    vb = w.v_blocks.clone()
+    g = torch.Generator().manual_seed(abs(int(big)) % 1000 + 3)
+    for s in range(3):  # the prefill chunks
+        n = w.seq_lens_list[s]
+        for _ in range(4):
+            pos = int(torch.randint(0, n, (1,), generator=g))
+            kvh = int(torch.randint(0, Hkv, (1,), generator=g))
+            d = int(torch.randint(0, 128, (1,), generator=g))
+            vb[int(w.block_tables[s, pos // 16]), pos % 16, kvh, d] = big
+    w.v_blocks = vb
+    out = _run(pa, w)
+    assert torch.isfinite(out.float()).all()
+    assert_attn_close(out, oracle_attention(w, w.k_blocks.cpu(), vb.cpu()), f"V with {big}")
+    assert torch.equal(_run(pa, w), out), "not deterministic"
