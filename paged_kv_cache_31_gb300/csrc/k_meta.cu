@@ -69,6 +69,27 @@ __device__ void warp_scan_inplace(int* h, int* total) {
   if (lane == 31) *total = x;
 }
 
+// The model of PlanLayout for K CTA pairs of the tcgen05 kernel (the warp-MMA kernel's decode
+// tiles run beside it on the other SMs), as a key for atomicMin: the estimated time (a
+// positive float: its bits order like its value) above, and ties broken towards the larger K
+// below.  tiles: 128-key tiles of all 256-row items (all kv heads); dec_bytes: K/V bytes the
+// decode tiles stream.  fp32 throughout (this GPU's fp64 rate is a small fraction of it).
+__device__ __forceinline__ unsigned long long split_key(const PlanLayout& L, int k, float tiles,
+                                                       float dec_bytes) {
+  const int free_sms = L.num_sms - 2 * k;
+  float t;
+  if (dec_bytes <= 0.f) {
+    t = L.margin * tiles * L.tile_ns / (float)k;  // no decode tiles: all pairs
+  } else if (free_sms <= 0) {
+    t = 3.0e38f;
+  } else {
+    const float pre = L.margin * tiles * L.tile_ns / (float)k;
+    const float dec = dec_bytes / L.hbm_bytes_per_ns * fmaxf(1.f, (float)L.decode_sat_sms / free_sms);
+    t = fmaxf(pre, dec);
+  }
+  return ((unsigned long long)__float_as_uint(t) << 32) | (0xffffffffu - (unsigned)k);
+}
+
 // Work buckets for ordering: a cost c > 0 maps to 16 sub-buckets per power of two
 // (descending: the largest costs get the smallest bucket index).
 constexpr int kCostBuckets = 512;
@@ -103,6 +124,9 @@ __global__ void __launch_bounds__(1024)
   __shared__ int s_hist[kCostBuckets];    // 16-row tiles per cost bucket
   __shared__ int s_hist_t[kCostBuckets];  // 256-row items per cost bucket
   __shared__ int s_tot;
+  __shared__ unsigned long long s_dec_units;  // decode tiles x visible keys
+  __shared__ unsigned int s_tc_tiles;         // 128-key tiles of the 256-row items
+  __shared__ unsigned long long s_split;      // best split key (split_key)
   // when cached: [num_seqs + 1] query starts, [num_seqs] seq_len, [num_seqs] visible keys
   extern __shared__ int s_seq[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -112,7 +136,12 @@ __global__ void __launch_bounds__(1024)
   int* s_qsl = s_seq;
   int* s_n = s_qsl + (cached ? m.num_seqs + 1 : 0);
   int* s_cost = s_n + (cached ? m.num_seqs : 0);
-  if (tid == 0) s_err = status_set(status) ? -1 : 0;
+  if (tid == 0) {
+    s_err = status_set(status) ? -1 : 0;
+    s_dec_units = 0;
+    s_tc_tiles = 0;
+    s_split = ~0ull;
+  }
   for (int i = tid; i < kCostBuckets; i += blockDim.x) {
     s_hist[i] = 0;
     s_hist_t[i] = 0;
@@ -208,6 +237,7 @@ __global__ void __launch_bounds__(1024)
   // under a causal mask) first; the histogram of the 16-row tiles' costs
   int carry_t = 0;
   if (L.use_tc) {
+    unsigned long long dec_units = 0;
     for (int base = 0; base < m.num_seqs; base += blockDim.x) {
       const int s = base + tid;
       int cm = 0, ct = 0;
@@ -218,12 +248,16 @@ __global__ void __launch_bounds__(1024)
         else
           cm = (int)((rows + 15) / 16);
       }
-      if (cm > 0) atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
+      if (cm > 0) {
+        atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
+        dec_units += (unsigned long long)cm * (unsigned long long)cost_of(s);
+      }
       int tot_t;
       const int et = block_exclusive_scan(ct, s_warp, &tot_t);
       for (int i = 0; i < ct; ++i) tc_tmp[carry_t + et + i] = make_int4(s, ct - 1 - i, 0, 0);
       carry_t += tot_t;
     }
+    if (dec_units) atomicAdd(&s_dec_units, dec_units);
   } else {
     for (int s = tid; s < m.num_seqs; s += blockDim.x) {
       const int cm = (int)(((int64_t)qlen_of(s) * m.group + 15) / 16);
@@ -253,6 +287,7 @@ __global__ void __launch_bounds__(1024)
       if (lane == 0) {
         tc_tmp[k] = make_int4(it.x, it.y, lo, hi);
         atomicAdd(&s_hist_t[cost_bucket(hi - lo)], 1);
+        if (hi > lo) atomicAdd(&s_tc_tiles, (unsigned)((hi - (lo / 16) * 16 + 127) / 128));
       }
     }
     __syncthreads();
@@ -278,12 +313,25 @@ __global__ void __launch_bounds__(1024)
   }
   // no 256-row item is marked for recomputing yet (the tcgen05 kernel marks them)
   for (int k = tid; k < carry_t; k += blockDim.x) plan[L.redo_off + k] = 0;
+  // the tcgen05 kernel's working pairs: every candidate K evaluated by its own thread
+  if (L.use_tc && L.force_pairs <= 0) {
+    const float tiles = (float)s_tc_tiles * m.num_kv_heads;
+    const float dec_bytes = (float)s_dec_units * m.num_kv_heads * 4.f * m.head_dim;
+    for (int k = tid + 1; k <= L.tc_pairs; k += blockDim.x)
+      atomicMin(&s_split, split_key(L, k, tiles, dec_bytes));
+  }
+  __syncthreads();
   if (tid == 0) {
     plan[0] = carry_m;
     plan[1] = carry_t;
     plan[2] = 0;  // work counter of the warp-MMA kernel
     plan[3] = 0;  // items marked by the tcgen05 kernel
     plan[4] = 0;  // work counter over their units
+    int pairs = 0;
+    if (L.use_tc)
+      pairs = L.force_pairs > 0 ? min(L.force_pairs, L.tc_pairs)
+                                : (int)(0xffffffffu - (unsigned)(s_split & 0xffffffffull));
+    plan[5] = max(0, min(pairs, L.tc_pairs));
   }
 }
 

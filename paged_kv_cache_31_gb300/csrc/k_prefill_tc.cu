@@ -282,11 +282,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 
 // ---- shared state -----------------------------------------------------------------------------
 
@@ -852,9 +847,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   pdl_launch_dependents();
   const uint32_t tmem = *tmem_slot;
+  // the plan's number of working pairs: the others take no item and leave, and the warp-MMA
+  // kernel launched behind this one runs its decode tiles on their SMs meanwhile
+  const int pairs = max(1, min((int)num_clusters_x(), p.plan[5]));
   Ctx c{sm, bar, reinterpret_cast<volatile int*>(flags + 1), p.status, p.wait_limit_ns,
-        cluster_rank(), (int)cluster_id_x(), (int)num_clusters_x()};
-  const int n_items = flags[0] ? 0 : p.plan[1] * p.m.num_kv_heads;
+        cluster_rank(), (int)cluster_id_x(), pairs};
+  const int n_items = (flags[0] || c.cluster >= pairs) ? 0 : p.plan[1] * p.m.num_kv_heads;
 
   // warps 0..3 (one warpgroup) produce and issue, warps 12..15 convert V: both need few
   // registers; the two softmax warpgroups take theirs: 8 x 56 + 8 x 200 = 16 x 128, the

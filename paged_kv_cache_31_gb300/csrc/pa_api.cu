@@ -455,6 +455,11 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
              aligned(q, 16) && max_rows > L.tc_min_rows && scale > 0.f && tc_enabled() &&
              !(flags & PA_FLAG_BITWISE);
 
+  // the tcgen05 kernel's launch: one CTA per SM, pairs, never more than there are items
+  const int64_t tc_work = L.tc_cap * num_kv_heads;
+  const int tc_grid = (int)std::max<int64_t>(2, std::min<int64_t>(tc_work, d->sms)) & ~1;
+  L.tc_pairs = tc_grid / 2;
+  L.num_sms = d->sms;
   cudaError_t e = launch_plan_varlen(m, plan, L, d->status, stream);
   if (e != cudaSuccess) return PA_ECUDA;
   if (cache) {  // the new tokens' slots and rows, alongside the plan
@@ -519,8 +524,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
       tp.redo_flags = plan + L.redo_off;
       tp.redo_list = plan + L.redo_list_off;
       tp.redo_count = plan + 3;
-      const int64_t work = L.tc_cap * num_kv_heads;
-      e = launch_tc_prefill(tq, tk, tv, tp, (int)std::min<int64_t>(work, d->sms), stream);
+      e = launch_tc_prefill(tq, tk, tv, tp, tc_grid, stream);
       if (e != cudaSuccess) return PA_ECUDA;
       p.after_tc = 1;
       p.tc_off = L.tc_off;

@@ -245,7 +245,9 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not lan
 //   [2] work counter of the warp-MMA kernel (zeroed by the plan)
 //   [3] number of 256-row items the tcgen05 kernel marked for recomputing (zeroed by the plan)
 //   [4] work counter of the warp-MMA kernel over those items (zeroed by the plan)
-//   [5..15] reserved
+//   [5] CTA pairs of the tcgen05 kernel that take 256-row items (the others leave at once,
+//       and their SMs run the warp-MMA kernel's decode tiles meanwhile)
+//   [6..15] reserved
 //   [tok_off, tok_off + T)        token -> sequence
 //   [cost_off, cost_off + S)      per sequence: keys its query rows can see (work estimate;
 //                                 written only for batches too large to keep it in smem)
@@ -262,6 +264,20 @@ struct PlanLayout {
   int64_t words;
   int32_t use_tc;       // prefill-class sequences go to the tcgen05 kernel
   int32_t tc_min_rows;  // a sequence is prefill-class when q_len * G exceeds this
+  // Split of the SMs between the tcgen05 kernel and the warp-MMA kernel that runs beside it
+  // (plan word [5]): the plan picks the number of CTA pairs K for the 256-row items that
+  // minimises max(margin * T_prefill(K), T_decode(num_sms - 2 K)), with
+  //   T_prefill(K) = (128-key tiles of all items) * tile_ns / K   (tiles spread over K pairs)
+  //   T_decode(m)  = decode K/V bytes / hbm_bytes_per_ns * max(1, decode_sat_sms / m)
+  // (decode tiles stream K/V at the HBM rate on decode_sat_sms SMs or more).  Ties go to the
+  // larger K: the prefill then ends first and its SMs join the decode tiles.
+  int32_t tc_pairs;        // CTA pairs the tcgen05 kernel is launched with
+  int32_t num_sms;
+  int32_t force_pairs;     // > 0: use this many pairs (measurements), else the model
+  int32_t decode_sat_sms;
+  float tile_ns;           // one 128-key tile of a 256-row item on one pair
+  float hbm_bytes_per_ns;  // decode tiles' K/V streaming rate on the whole GPU
+  float margin;            // the prefill estimate is taken this much longer
 };
 
 // Layout of the plan for a batch of num_tokens tokens over num_seqs sequences.
@@ -279,6 +295,13 @@ inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t grou
   L.words = L.redo_list_off + L.tc_cap;
   L.use_tc = 0;
   L.tc_min_rows = 64;
+  L.tc_pairs = 0;
+  L.num_sms = 0;
+  L.force_pairs = 0;
+  L.decode_sat_sms = 80;
+  L.tile_ns = 1300.f;
+  L.hbm_bytes_per_ns = 6700.f;
+  L.margin = 1.1f;
   return L;
 }
 

@@ -143,3 +143,25 @@ def test_prefill_v_beyond_f16_range(pa, big):
     assert torch.isfinite(out.float()).all()
     assert_attn_close(out, oracle_attention(w, w.k_blocks.cpu(), vb.cpu()), f"V with {big}")
     assert torch.equal(_run(pa, w), out), "not deterministic"
+
+
+def test_mixed_batch_equals_its_parts_bitwise(pa):
+    """In a mixed call the decode tiles run on the warp-MMA kernel beside the tcgen05 kernel,
+    which the plan gives only part of the SMs; a prefill-only call gives it all of them and a
+    decode-only call does not launch it.  Each item's arithmetic does not depend on where it
+    runs, so the mixed batch gives, bit for bit, what its prefill chunks and its decode tokens
+    give as two separate calls."""
+    from tests.gpu_helpers import sub_batch
+    w = workloads.named(3, device=DEV)
+    mixed = _run(pa, w)
+    for part in ([s for s, q in enumerate(w.q_lens_list) if q == 1],
+                 [s for s, q in enumerate(w.q_lens_list) if q > 1]):
+        sb = sub_batch(w, part)
+        rows = sb["rows"].to(DEV)
+        out = torch.full_like(w.q[rows], float("nan"))
+        pa.pa_varlen_forward(w.q[rows].contiguous(), w.k_blocks, w.v_blocks, out,
+                             sb["query_start_loc"].to(DEV), sb["seq_lens"].to(DEV),
+                             sb["positions"].to(DEV), sb["block_tables"].to(DEV), w.scale,
+                             causal=w.causal, sliding_window=w.sliding_window)
+        assert pa.pa_device_status() == pa.PA_OK
+        assert torch.equal(out, mixed[rows]), f"{len(part)} sequences differ from the mixed call"
