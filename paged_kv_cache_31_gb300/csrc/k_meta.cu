@@ -41,6 +41,20 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
   return before + x - v;
 }
 
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(kFull, v, o);
+    v = y < v ? y : v;
+  }
+  return v;
+}
+
 // Exclusive prefix sum, in place, of the kCostBuckets ints at h, by one warp (16 per lane);
 // the total goes to *total.  Called by warp 0 between two __syncthreads.
 template <int N>
@@ -93,7 +107,90 @@ __device__ __forceinline__ unsigned long long split_key(const PlanLayout& L, int
 // Work buckets for ordering: a cost c > 0 maps to 16 sub-buckets per power of two
 // (descending: the largest costs get the smallest bucket index).
 constexpr int kCostBuckets = 512;
-constexpr int kPlanCacheSeqs = 8192;  // sequences whose q_len / cost the plan keeps in smem
+constexpr int kPlanCacheSeqs = 4096;    // sequences whose metadata the planner keeps in smem
+constexpr int kPlanCacheTokens = 8192;  // tokens whose visible ranges it keeps there too
+constexpr int kPlanTokPer = kPlanCacheTokens / 1024;  // tokens per planner thread, at most
+constexpr int kPlanCacheItems = 2048;  // 256-row items the planner keeps in smem
+// 256-row items the planner keeps in shared memory for this layout (else in the plan)
+__host__ __device__ constexpr int plan_items_cached(const PlanLayout& L) {
+  return (L.use_tc && L.tc_cap <= kPlanCacheItems) ? (int)L.tc_cap : 0;
+}
+// dynamic shared memory of the planner for s cached sequences and t tokens: int4 [items]
+// 256-row items, then ints [s + 1] query starts, [s] seq_len, [s] visible keys, [s]
+// visible-range start, [s] visible-range end, and, when t <= kPlanCacheTokens, [t]
+// visible-range start and [t] end of each token
+__host__ __device__ constexpr size_t plan_smem_bytes(int s, int64_t t, int items) {
+  return 16 * (size_t)items + 4 * (5 * (size_t)s + 1 + (t <= kPlanCacheTokens ? 2 * (size_t)t : 0));
+}
+
+// Table check of one pa_varlen_forward call, in blocks 1 .. V of the planning launch, beside
+// the planner (block 0): the entries [0, ceil(seq_len / b)) of every sequence with query
+// tokens lie in [0, num_blocks) (tinyllm section 2.6).  Block c takes the sequences c,
+// c + V, c + 2V, ...; their tables are cut into chunks of 256 entries, which the warps take
+// two at a time (16 loads in flight per lane).  A bad entry records PA_EINVAL in the status
+// word; the attention kernels wait for the whole launch, so this happens before anything is
+// written.  Table lengths beyond max_blocks and the other per-sequence checks are the
+// planner's; only existing entries are read here, whatever query_start_loc holds.
+__device__ void check_tables(const VarlenMeta& m, int* status) {
+  __shared__ int v_off[1025];  // chunk offsets of this round's sequences
+  __shared__ int v_need[1024];
+  __shared__ int v_seq[1024];
+  __shared__ int v_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int V = gridDim.x - 1, c = blockIdx.x - 1;
+  const int K = c < m.num_seqs ? (m.num_seqs - c + V - 1) / V : 0;  // this block's sequences
+  bool bad = false;
+  for (int k0 = 0; k0 < K; k0 += blockDim.x) {
+    const int k = k0 + tid;
+    int nch = 0, need = 0, s = 0;
+    if (k < K) {
+      s = c + V * k;
+      const int a = m.query_start_loc[s], b = m.query_start_loc[s + 1], n = m.seq_lens[s];
+      if (a < b && n >= 1) {
+        const int64_t full = ((int64_t)n + m.block_size - 1) / m.block_size;
+        need = (int)(full < (int64_t)m.max_blocks ? full : (int64_t)m.max_blocks);
+        nch = (need + 255) / 256;
+      }
+    }
+    int total;
+    const int off = block_exclusive_scan(nch, v_warp, &total);
+    v_off[tid] = off;
+    v_need[tid] = need;
+    v_seq[tid] = s;
+    if (tid == 0) v_off[blockDim.x] = total;
+    __syncthreads();
+    const int cnt = min((int)blockDim.x, K - k0);  // sequences of this round
+    for (int j0 = warp; j0 < total; j0 += 2 * nwarps) {  // warp-uniform
+      int32_t id[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = j0 + h * nwarps;
+        int t = 0;
+        if (j < total) {  // the sequence owning chunk j: the last t with v_off[t] <= j
+          int lo2 = 0, hi2 = cnt;
+          while (hi2 - lo2 > 1) {
+            const int mid = (lo2 + hi2) >> 1;
+            if (v_off[mid] <= j) lo2 = mid; else hi2 = mid;
+          }
+          t = lo2;
+        }
+        const int base = (j - v_off[t]) * 256;
+        const int32_t* row = m.block_tables + (int64_t)v_seq[t] * m.max_blocks;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = base + lane + 32 * u;
+          id[h][u] = (j < total && i < v_need[t]) ? row[i] : 0;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) bad |= (id[h][u] < 0 || (int64_t)id[h][u] >= m.num_blocks);
+    }
+    __syncthreads();  // the next round reuses the arrays
+  }
+  if (__any_sync(kFull, bad) && lane == 0) record_error(status, PA_EINVAL);
+}
 __device__ __forceinline__ int cost_bucket(int c) {
   if (c <= 0) return kCostBuckets - 1;
   const int lg = 31 - __clz(c);
@@ -128,14 +225,34 @@ __global__ void __launch_bounds__(1024)
   __shared__ unsigned int s_tc_tiles;         // 128-key tiles of the 256-row items
   __shared__ unsigned long long s_split;      // best split key (split_key)
   // when cached: [num_seqs + 1] query starts, [num_seqs] seq_len, [num_seqs] visible keys
-  extern __shared__ int s_seq[];
+  extern __shared__ __align__(16) int s_dyn[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   pdl_wait();               // launched early: the batch's metadata may still be in flight
   pdl_launch_dependents();  // the attention kernels' prologues may overlap this kernel
+  if (blockIdx.x > 0) {     // blocks 1 .. V check the block tables
+    if (!status_set(status)) check_tables(m, status);
+    return;
+  }
   const bool cached = m.num_seqs <= kPlanCacheSeqs;
-  int* s_qsl = s_seq;
+  const bool tok_cached = cached && m.num_tokens <= kPlanCacheTokens;
+  const int item_cap = cached ? plan_items_cached(L) : 0;
+  int* s_qsl = s_dyn + 4 * item_cap;
   int* s_n = s_qsl + (cached ? m.num_seqs + 1 : 0);
   int* s_cost = s_n + (cached ? m.num_seqs : 0);
+  int* s_lo = s_cost + (cached ? m.num_seqs : 0);
+  int* s_hi = s_lo + (cached ? m.num_seqs : 0);
+  int* s_ts = s_hi + (cached ? m.num_seqs : 0);  // when tok_cached: per token visible start
+  int* s_te = s_ts + (tok_cached ? m.num_tokens : 0);  // ... and end
+  // each thread's run of tpt consecutive query positions is loaded now, together with the
+  // query starts and lengths below
+  const int tpt = (int)((m.num_tokens + blockDim.x - 1) / blockDim.x);  // <= kPlanTokPer
+  const int t_first = tid * tpt;
+  int32_t pos0[kPlanTokPer];
+  if (tok_cached) {
+#pragma unroll
+    for (int u = 0; u < kPlanTokPer; ++u)
+      pos0[u] = (u < tpt && t_first + u < m.num_tokens) ? m.positions[t_first + u] : 0;
+  }
   if (tid == 0) {
     s_err = status_set(status) ? -1 : 0;
     s_dec_units = 0;
@@ -162,55 +279,132 @@ __global__ void __launch_bounds__(1024)
         if (!(ks > 0.f && ks <= 3.402823466e38f) || !(vs > 0.f && vs <= 3.402823466e38f))
           atomicCAS(&s_err, 0, PA_EINVAL);
       }
-    for (int s = warp; s < m.num_seqs; s += nwarps) {
-      const int a = cached ? s_qsl[s] : m.query_start_loc[s];
-      const int b = cached ? s_qsl[s + 1] : m.query_start_loc[s + 1];
-      const int n = cached ? s_n[s] : m.seq_lens[s];
-      bool bad = a < 0 || b < a || (int64_t)b > m.num_tokens || (s == 0 && a != 0) ||
-                 (s == m.num_seqs - 1 && (int64_t)b != m.num_tokens);
-      int lo = INT_MAX, hi = 0;
-      const int64_t need = n >= 1 ? ((int64_t)n + m.block_size - 1) / m.block_size : 0;
-      if (!bad && a < b) {
-        bad = n < 1 || need > m.max_blocks;
-        if (!bad) {
-          const int32_t* row = m.block_tables + (int64_t)s * m.max_blocks;
-          // eight loads in flight per lane, table entries and positions together
-          for (int64_t base = 0; base < need || base < b - a; base += 256) {
-            int32_t id[8], pos[8];
+    if (tok_cached) {
+      // A1: per sequence (a thread each): the query-start order, a table long enough for
+      // seq_len, and an empty visible range to fill in (the entries themselves are checked
+      // by the other blocks of this launch)
+      for (int q = tid; q < m.num_seqs; q += blockDim.x) {
+        const int a = s_qsl[q], b = s_qsl[q + 1], n = s_n[q];
+        bool bad = a < 0 || b < a || (int64_t)b > m.num_tokens || (q == 0 && a != 0) ||
+                   (q == m.num_seqs - 1 && (int64_t)b != m.num_tokens);
+        if (!bad && a < b) {
+          const int64_t need = n >= 1 ? ((int64_t)n + m.block_size - 1) / m.block_size : 0;
+          bad = n < 1 || need > m.max_blocks;
+        }
+        s_lo[q] = INT_MAX;
+        s_hi[q] = 0;
+        if (bad) atomicCAS(&s_err, 0, PA_EINVAL);
+      }
+      __syncthreads();
+      if (s_err == 0 && m.num_seqs > 0) {
+        // A2: each thread's run of consecutive query tokens: their sequence (the last q with
+        // query_start_loc[q] <= t, found once and then advanced), the position check, the
+        // token -> sequence map, each token's visible range [start, end) and, per sequence,
+        // [min start, max end): folded in registers along the run, then (when the warp's
+        // lanes end on one sequence) across the warp, with few shared-memory atomics
+        bool bad = false;
+        int q = -1, run_st = INT_MAX, run_e = 0;
+        if (t_first < m.num_tokens) {
+          int lo2 = 0, hi2 = m.num_seqs;  // s_qsl[lo2] <= t < s_qsl[hi2]
+          while (hi2 - lo2 > 1) {
+            const int mid = (lo2 + hi2) >> 1;
+            if (s_qsl[mid] <= t_first) lo2 = mid; else hi2 = mid;
+          }
+          q = lo2;
+        }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int64_t i = base + lane + 32 * u;
-              id[u] = i < need ? row[i] : 0;
-              pos[u] = i < b - a ? m.positions[a + i] : 0;
+        for (int u = 0; u < kPlanTokPer; ++u) {
+          const int t = t_first + u;
+          if (u >= tpt || t >= m.num_tokens) break;
+          while (s_qsl[q + 1] <= t) {  // the run crosses into the next sequence
+            if (run_e > 0) {
+              atomicMin(&s_lo[q], run_st);
+              atomicMax(&s_hi[q], run_e);
             }
+            ++q;
+            run_st = INT_MAX;
+            run_e = 0;
+          }
+          const int n = s_n[q];
+          bad |= (pos0[u] < 0 || pos0[u] >= n);
+          plan[L.tok_off + t] = q;
+          const int e = m.causal ? pos0[u] + 1 : n;
+          const int st = m.window > 0 ? max(0, e - m.window) : 0;
+          s_ts[t] = st;
+          s_te[t] = e;
+          run_st = min(run_st, st);
+          run_e = max(run_e, e);
+        }
+        const int q_l0 = __shfl_sync(kFull, q, 0);
+        if (__all_sync(kFull, q == q_l0)) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int64_t i = base + lane + 32 * u;
-              bad |= (id[u] < 0 || (int64_t)id[u] >= m.num_blocks);
-              if (i < b - a) {
-                bad |= (pos[u] < 0 || pos[u] >= n);
-                plan[L.tok_off + a + i] = s;
-                const int e = m.causal ? pos[u] + 1 : n;
-                lo = min(lo, m.window > 0 ? max(0, e - m.window) : 0);
-                hi = max(hi, e);
+          for (int o = 16; o > 0; o >>= 1) {
+            run_st = min(run_st, __shfl_xor_sync(kFull, run_st, o));
+            run_e = max(run_e, __shfl_xor_sync(kFull, run_e, o));
+          }
+          if (lane == 0 && q >= 0 && run_e > 0) {
+            atomicMin(&s_lo[q], run_st);
+            atomicMax(&s_hi[q], run_e);
+          }
+        } else if (q >= 0 && run_e > 0) {
+          atomicMin(&s_lo[q], run_st);
+          atomicMax(&s_hi[q], run_e);
+        }
+        if (__any_sync(kFull, bad) && lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
+        __syncthreads();
+        for (int q = tid; q < m.num_seqs; q += blockDim.x) s_cost[q] = max(0, s_hi[q] - s_lo[q]);
+      }
+    } else {
+    for (int s = warp; s < m.num_seqs; s += nwarps) {
+        const int a = cached ? s_qsl[s] : m.query_start_loc[s];
+        const int b = cached ? s_qsl[s + 1] : m.query_start_loc[s + 1];
+        const int n = cached ? s_n[s] : m.seq_lens[s];
+        bool bad = a < 0 || b < a || (int64_t)b > m.num_tokens || (s == 0 && a != 0) ||
+                   (s == m.num_seqs - 1 && (int64_t)b != m.num_tokens);
+        int lo = INT_MAX, hi = 0;
+        const int64_t need = n >= 1 ? ((int64_t)n + m.block_size - 1) / m.block_size : 0;
+        if (!bad && a < b) {
+          bad = n < 1 || need > m.max_blocks;
+          if (!bad) {
+            const int32_t* row = m.block_tables + (int64_t)s * m.max_blocks;
+            // eight loads in flight per lane, table entries and positions together
+            for (int64_t base = 0; base < need || base < b - a; base += 256) {
+              int32_t id[8], pos[8];
+  #pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int64_t i = base + lane + 32 * u;
+                id[u] = i < need ? row[i] : 0;
+                pos[u] = i < b - a ? m.positions[a + i] : 0;
+              }
+  #pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int64_t i = base + lane + 32 * u;
+                bad |= (id[u] < 0 || (int64_t)id[u] >= m.num_blocks);
+                if (i < b - a) {
+                  bad |= (pos[u] < 0 || pos[u] >= n);
+                  plan[L.tok_off + a + i] = s;
+                  const int e = m.causal ? pos[u] + 1 : n;
+                  lo = min(lo, m.window > 0 ? max(0, e - m.window) : 0);
+                  hi = max(hi, e);
+                }
               }
             }
           }
         }
+  #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          lo = min(lo, __shfl_xor_sync(kFull, lo, o));
+          hi = max(hi, __shfl_xor_sync(kFull, hi, o));
+        }
+        if (lane == 0) {
+          const int cost = max(0, hi - lo);
+          if (cached)
+            s_cost[s] = cost;
+          else
+            plan[L.cost_off + s] = cost;
+        }
+        if (__any_sync(kFull, bad) && lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        lo = min(lo, __shfl_xor_sync(kFull, lo, o));
-        hi = max(hi, __shfl_xor_sync(kFull, hi, o));
-      }
-      if (lane == 0) {
-        const int cost = max(0, hi - lo);
-        if (cached)
-          s_cost[s] = cost;
-        else
-          plan[L.cost_off + s] = cost;
-      }
-      if (__any_sync(kFull, bad) && lane == 0) atomicCAS(&s_err, 0, PA_EINVAL);
     }
   }
   __syncthreads();
@@ -231,7 +425,8 @@ __global__ void __launch_bounds__(1024)
   auto cost_of = [&](int s) -> int { return cached ? s_cost[s] : plan[L.cost_off + s]; };
   int2* mma_items = reinterpret_cast<int2*>(plan + L.mma_off);
   int4* tc_items = reinterpret_cast<int4*>(plan + L.tc_off);
-  int4* tc_tmp = reinterpret_cast<int4*>(plan + L.tc_tmp_off);
+  // the items in sequence order: in shared memory when they fit, else in the plan
+  int4* tc_tmp = item_cap ? reinterpret_cast<int4*>(s_dyn) : reinterpret_cast<int4*>(plan + L.tc_tmp_off);
   const int tok_per_item = 256 / m.group;  // used only when use_tc (group divides 128)
   // B1: 256-row items of prefill-class sequences, in sequence order, the last one (most keys
   // under a causal mask) first; the histogram of the 16-row tiles' costs
@@ -257,7 +452,8 @@ __global__ void __launch_bounds__(1024)
       for (int i = 0; i < ct; ++i) tc_tmp[carry_t + et + i] = make_int4(s, ct - 1 - i, 0, 0);
       carry_t += tot_t;
     }
-    if (dec_units) atomicAdd(&s_dec_units, dec_units);
+    dec_units = warp_sum_u64(dec_units);  // one shared-memory atomic per warp
+    if (lane == 0 && dec_units) atomicAdd(&s_dec_units, dec_units);
   } else {
     for (int s = tid; s < m.num_seqs; s += blockDim.x) {
       const int cm = (int)(((int64_t)qlen_of(s) * m.group + 15) / 16);
@@ -270,13 +466,21 @@ __global__ void __launch_bounds__(1024)
   if (carry_t > 0) {
     for (int k = warp; k < carry_t; k += nwarps) {
       const int4 it = tc_tmp[k];
-      const int qs = m.query_start_loc[it.x], qe = m.query_start_loc[it.x + 1];
-      const int n = m.seq_lens[it.x];
+      const int qs = cached ? s_qsl[it.x] : m.query_start_loc[it.x];
+      const int qe = cached ? s_qsl[it.x + 1] : m.query_start_loc[it.x + 1];
+      const int n = cached ? s_n[it.x] : m.seq_lens[it.x];
       const int ta = qs + it.y * tok_per_item, tb = min(qe, ta + tok_per_item);
       int lo = INT_MAX, hi = 0;
       for (int t = ta + lane; t < tb; t += 32) {
-        const int e = m.causal ? m.positions[t] + 1 : n;
-        lo = min(lo, m.window > 0 ? max(0, e - m.window) : 0);
+        int e, st;
+        if (tok_cached) {
+          e = s_te[t];
+          st = s_ts[t];
+        } else {
+          e = m.causal ? m.positions[t] + 1 : n;
+          st = m.window > 0 ? max(0, e - m.window) : 0;
+        }
+        lo = min(lo, st);
         hi = max(hi, e);
       }
 #pragma unroll
@@ -317,8 +521,12 @@ __global__ void __launch_bounds__(1024)
   if (L.use_tc && L.force_pairs <= 0) {
     const float tiles = (float)s_tc_tiles * m.num_kv_heads;
     const float dec_bytes = (float)s_dec_units * m.num_kv_heads * 4.f * m.head_dim;
-    for (int k = tid + 1; k <= L.tc_pairs; k += blockDim.x)
-      atomicMin(&s_split, split_key(L, k, tiles, dec_bytes));
+    for (int k0 = warp * 32 + 1; k0 <= L.tc_pairs; k0 += blockDim.x) {
+      const int k = k0 + lane;
+      const unsigned long long key =
+          warp_min_u64(k <= L.tc_pairs ? split_key(L, k, tiles, dec_bytes) : ~0ull);
+      if (lane == 0) atomicMin(&s_split, key);  // one shared-memory atomic per warp
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -739,12 +947,19 @@ bool aligned(const void* p, size_t a) { return p == nullptr || (reinterpret_cast
 
 cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, const PlanLayout& L,
                                int* status, cudaStream_t stream) {
-  const size_t dyn =
-      m.num_seqs <= kPlanCacheSeqs ? sizeof(int) * (3 * (size_t)m.num_seqs + 1) : 0;
-  cudaError_t e = cudaFuncSetAttribute(k_plan_varlen, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(sizeof(int) * (3 * kPlanCacheSeqs + 1)));
+  // block 0 plans; when the batch's metadata fits the planner's shared memory, blocks 1 .. V
+  // check the block tables beside it (V = min(num_seqs, 32)); otherwise block 0 checks them
+  const bool cached = m.num_seqs <= kPlanCacheSeqs && m.num_tokens <= kPlanCacheTokens;
+  const size_t dyn = m.num_seqs <= kPlanCacheSeqs
+                         ? plan_smem_bytes(m.num_seqs, m.num_tokens, plan_items_cached(L))
+                         : 0;
+  const int validators = cached ? std::min(m.num_seqs, 32) : 0;
+  cudaError_t e = cudaFuncSetAttribute(
+      k_plan_varlen, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)plan_smem_bytes(kPlanCacheSeqs, kPlanCacheTokens, kPlanCacheItems));
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_plan_varlen, dim3(1), dim3(1024), dyn, stream, m, plan, L, status);
+  return launch_pdl(k_plan_varlen, dim3(1 + validators), dim3(1024), dyn, stream, m, plan, L,
+                    status);
 }
 
 cudaError_t launch_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
