@@ -50,7 +50,10 @@
 // units), so the weights stay <= 2^8 and most tiles need no O rescale.
 //
 // Every mbarrier wait is bounded; a wait that runs out records PA_ETIMEOUT, raises an abort
-// flag that makes the other roles unwind, and the CTA still frees its tensor memory.
+// flag that makes the other roles unwind, and the CTA still frees its tensor memory.  Before
+// a CTA leaves, its producers wait (bounded) for the TMA copies they issued last, the MMA
+// issuers for their last MMAs, and the pair meets at a cluster barrier, so no asynchronous
+// write lands in the shared memory or tensor memory of a CTA that has gone.
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -109,7 +112,8 @@ enum : int {
   B_PVDONE = B_PFULL + kSBufs,
   B_OFREE = B_PVDONE + kSBufs,
   B_FIN = B_OFREE + 1,
-  kNumBars = B_FIN + 1
+  B_NEVER = B_FIN + 1,  // nothing arrives on it (the debug_stall test hook)
+  kNumBars = B_NEVER + 1
 };
 static_assert(kNumBars <= kNumBarsMax, "barrier area");
 
@@ -376,14 +380,38 @@ __device__ __forceinline__ Item load_item(const TcParams& p, int idx, uint32_t r
 // and never waits behind a V stage that the slower PV MMAs still hold.  K part: blocks
 // 4r .. 4r + 3 of the tile (keys 64r ..), both 64-dim halves, [half][64 keys][64 dims]; V part:
 // all 8 blocks, dims 64r .. 64r + 63, [128 keys][64 dims].
+// Wait, bounded and whatever the abort flag says, until the copies behind the last `issued`
+// phases of a ring of `nst` full barriers have landed (all of them have, when their consumers
+// saw them; after an abort the newest may still be in flight).
+__device__ void drain_ring(const Ctx& c, int full, uint32_t nst, uint32_t issued) {
+  if ((threadIdx.x & 31) != 0) return;
+  for (uint32_t k = issued > nst ? issued - nst : 0; k < issued; ++k)
+    mbar_wait(c.bar + full + k % nst, (k / nst) & 1u, c.limit);
+}
+
+__device__ void producer_loop(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
+                              const CUtensorMap* tkv, bool is_v, int n_items, uint32_t& kv,
+                              uint32_t& q_issued);
+
 __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
                          const CUtensorMap* tkv, bool is_v, int n_items) {
+  uint32_t kv = 0, q_issued = 0;  // K (or V) stage loads and Q loads issued
+  producer_loop(c, p, tq, tkv, is_v, n_items, kv, q_issued);
+  // normally every issued copy has been consumed and these return at once
+  drain_ring(c, is_v ? B_VFULL : B_KFULL, is_v ? kStagesV : kStagesK, kv);
+  if (!is_v) drain_ring(c, B_QFULL, 2, q_issued);
+  __syncwarp();
+}
+
+__device__ void producer_loop(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
+                              const CUtensorMap* tkv, bool is_v, int n_items, uint32_t& kv,
+                              uint32_t& q_issued) {
   const int lane = threadIdx.x & 31;
   const VarlenMeta& m = p.m;
   const int full = is_v ? B_VFULL : B_KFULL, empty = is_v ? B_VEMPTY : B_KEMPTY;
   const int off = is_v ? kOffV : kOffK;
   const uint32_t nst = is_v ? kStagesV : kStagesK;
-  uint32_t kv = 0, it_cnt = 0;
+  uint32_t it_cnt = 0;
   for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
     const int32_t* row = m.block_tables + (int64_t)I.s * m.max_blocks;
@@ -402,6 +430,7 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
         }
       }
       if (!__shfl_sync(kFull, (int)qok, 0)) return;
+      ++q_issued;
     }
     int next_id = (lane < 8 && blk0 + lane < I.nblk_vis) ? row[blk0 + lane] : -1;
     for (int j = 0; j < I.ntiles; ++j, ++kv) {
@@ -430,6 +459,7 @@ __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
         else
           tma_load_3d(dst + lane * 2048, tkv, 64 * (int)c.rank, I.kvh, r, c.bar + full + st);
       }
+      // kv counts the loads issued: the loop's increment is skipped for this unissued one
       if (!__shfl_sync(kFull, (int)ok, 0)) return;
     }
   }
@@ -627,7 +657,11 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     for (int j = 0; j < I.ntiles; ++j) {
       const uint32_t s = kv + j, b = buf_of(s);
       const uint32_t sbase = tmem + lane_addr + col_s(b) + col0;  // this thread's S / P columns
-      if (!bad) bad = !__all_sync(kFull, wait_bar(c, B_SFULL + b, use_par(s)));
+      // debug_stall (tests only): the wait names a barrier nothing arrives on, so it runs out
+      // after the wait limit and the kernel unwinds as from an S that never completed
+      if (!bad)
+        bad = !__all_sync(kFull, p.debug_stall ? wait_bar(c, B_NEVER, 0u)
+                                               : wait_bar(c, B_SFULL + b, use_par(s)));
       tc_fence_after();
       // after a failed wait the values read here only travel to the exchange below, where
       // the pair leaves (a read of allocated tensor memory is defined, whatever it holds)

@@ -143,24 +143,25 @@ bool tc_enabled() {
   return on;
 }
 
-// Test hook of the warp-MMA kernels (PA_DEBUG_STALL_NS=<ns>, read at every call): each of
-// their block waits then names a barrier that no copy signals, with a bound of <ns>, so it
-// runs out and the kernel records PA_ETIMEOUT and unwinds (waiting for its own copies still in
-// flight) exactly as from a copy that never landed.  Unset: real waits, bounded at 4 s.  The
-// tcgen05 kernel has no such hook.
-void mma_waits(Mma16Params& p) {
-  p.wait_limit_ns = kWaitLimitNs;
-  p.debug_stall = 0;
+// Test hook of the attention kernels (PA_DEBUG_STALL_NS=<ns>, read at every call): every
+// wait then has a bound of <ns>, and the warp-MMA kernels' block waits and the tcgen05
+// kernel's softmax waits name a barrier that nothing signals, so they run out and the kernel
+// records PA_ETIMEOUT and unwinds (waiting for its own copies and MMAs still in flight)
+// exactly as from a copy or an MMA that never completed.  Unset: real waits, bounded at 4 s.
+void stall_hook(uint64_t& limit, uint32_t& stall) {
+  limit = kWaitLimitNs;
+  stall = 0;
   const char* v = std::getenv("PA_DEBUG_STALL_NS");
   if (v && *v) {
     char* end = nullptr;
     const unsigned long long x = std::strtoull(v, &end, 10);
     if (end && *end == 0 && x > 0 && x <= kWaitLimitNs) {
-      p.wait_limit_ns = x;
-      p.debug_stall = 1;
+      limit = x;
+      stall = 1;
     }
   }
 }
+void mma_waits(Mma16Params& p) { stall_hook(p.wait_limit_ns, p.debug_stall); }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool dtype_ok(pa_dtype t) { return t == PA_F32 || t == PA_BF16; }  // q, out, new rows
@@ -520,7 +521,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
       tp.tc_off = L.tc_off;
       tp.status = d->status;
       tp.scale_log2 = scale * kLog2e;
-      tp.wait_limit_ns = kWaitLimitNs;
+      stall_hook(tp.wait_limit_ns, tp.debug_stall);
       tp.redo_flags = plan + L.redo_off;
       tp.redo_list = plan + L.redo_list_off;
       tp.redo_count = plan + 3;

@@ -387,6 +387,7 @@ struct TcParams {
   int* status;
   float scale_log2;
   uint64_t wait_limit_ns;
+  uint32_t debug_stall;  // tests only: the softmax waits run out (PA_DEBUG_STALL_NS)
   // items whose V does not fit f16 (recomputed by the warp-MMA kernel afterwards): a flag per
   // 256-row item, the list of marked items and its length (all in the plan)
   int32_t* redo_flags;

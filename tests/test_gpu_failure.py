@@ -1,10 +1,12 @@
-"""Failure detection without a GPU fault.  Every wait inside the warp-MMA kernels is bounded:
+"""Failure detection without a GPU fault.  Every wait inside the attention kernels is bounded:
 when one runs out the kernel records PA_ETIMEOUT in the device status word (the tinyllm
-interface's error classes, extended with a timeout), waits for its own copies still in
-flight, writes nothing more and returns, so the context stays usable.  PA_DEBUG_STALL_NS=<ns>
-makes each of those waits name a barrier that nothing signals, bounded at <ns> (1 ms here), so
-it runs out; the test checks the status and that the next call on the device gives the same
-bits as before."""
+interface's error classes, extended with a timeout), waits for its own copies (and, in the
+tcgen05 kernel, MMAs) still in flight, writes nothing more and returns, so the context stays
+usable.  PA_DEBUG_STALL_NS=<ns> makes the warp-MMA kernels' block waits and the tcgen05
+kernel's softmax waits name a barrier that nothing signals, with every wait bounded at <ns>
+(1 ms here; 20 ms for the tcgen05 kernel, whose other roles then give up in turn), so they run
+out; the tests check the status, that the output is untouched, and that the next call on the
+device gives the same bits as before."""
 import contextlib
 import os
 
@@ -84,6 +86,32 @@ def test_waits_that_run_out_report_timeout_and_the_device_stays_usable(pa, case)
     out = call()
     assert pa.pa_device_status() == pa.PA_OK
     assert torch.equal(out, ref)
+
+
+def test_tcgen05_prefill_timeout_unwinds_and_the_device_stays_usable(pa):
+    """The tcgen05 kernel's unwinding: the softmax warps' waits run out, every other role of
+    both CTAs of each pair gives up at its next wait (the abort flag, or its own bounded
+    wait), the producers wait for the copies they issued, the MMA issuers for their MMAs, and
+    the pair meets before its tensor memory is freed.  No output row is written, and the next
+    call gives the same bits as a call before the stall."""
+    prior, chunk = [0, 300, 45, 700], [200, 129, 96, 257]
+    w = workloads.build("stall", seq_lens=[p + c for p, c in zip(prior, chunk)], q_lens=chunk,
+                        num_heads=32, num_kv_heads=8, head_dim=128, seed=14, device=DEV)
+
+    def call():
+        out = torch.full_like(w.q, 7.0)
+        pa.pa_varlen_forward(w.q, w.k_blocks, w.v_blocks, out, w.query_start_loc, w.seq_lens,
+                             w.positions, w.block_tables, w.scale)
+        return out
+    ref = call()
+    assert pa.pa_device_status() == pa.PA_OK
+    with _stalled_waits(20_000_000):
+        out = call()
+        assert pa.pa_device_status() == pa.PA_ETIMEOUT
+        assert bool((out == 7.0).all()), "a timed-out prefill call wrote output"
+    again = call()
+    assert pa.pa_device_status() == pa.PA_OK
+    assert torch.equal(again, ref)
 
 
 def test_a_recorded_error_stops_later_kernels_until_it_is_read(pa):
