@@ -55,12 +55,12 @@ def parse():
     ap.add_argument("--secondary-steps", type=int, default=30)
     ap.add_argument("--case", default="bench",
                     choices=["bench", "prefill-chunks", "decode-fp8", "splitkv", "shared-prefix",
-                             "tiny"],
+                             "tiny", "decode"],
                     help="a single timed case for profiling: prefill-chunks (the attention "
                          "call on the mixed batch's prefill chunks, own pool), decode-fp8 (the "
                          "decode batch over fp8 pools), splitkv (the long-context split-KV "
                          "call), shared-prefix (the fork batch's attention call), tiny (the "
-                         "fp32 tiny mixed batch)")
+                         "fp32 tiny mixed batch), decode (the decode batch's attention call)")
     ap.add_argument("--min-timed-ms", type=float, default=1000.0,
                     help="the timed loop of --steps steps is repeated until the repeats "
                          "together take at least this long (at least 5 repeats)")
@@ -515,7 +515,8 @@ def secondary(pa, dev, args, peaks, stream):
     kv4 = kv_bytes(w4)
     res["splitkv"] = {"workload": w4.name, "kv_bytes": kv4, "ms": ms4,
                       "gbs": kv4 / (ms4 * 1e-3) / 1e9,
-                      "frac_of_hbm": kv4 / (ms4 * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+                      "frac_of_hbm": kv4 / (ms4 * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                      "traffic_partials": ncu_traffic("k_mma16", w4.name)}
     assert pa.pa_device_status() == pa.PA_OK
     del w4, r4
     torch.cuda.empty_cache()
@@ -580,8 +581,8 @@ def main():
                                                                torch.cuda.current_stream(),
                                                                args.steps))), flush=True)
         return
-    if args.case in ("splitkv", "shared-prefix", "tiny"):
-        w = workloads.named({"splitkv": 4, "shared-prefix": 5, "tiny": 1}[args.case],
+    if args.case in ("splitkv", "shared-prefix", "tiny", "decode"):
+        w = workloads.named({"splitkv": 4, "shared-prefix": 5, "tiny": 1, "decode": 2}[args.case],
                             seed=args.seed, device=dev)
         r = Runner(pa, w)
         for _ in range(max(3, args.warmup)):
