@@ -54,13 +54,14 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--secondary-steps", type=int, default=30)
     ap.add_argument("--case", default="bench",
-                    choices=["bench", "prefill-chunks", "decode-fp8", "splitkv", "shared-prefix",
-                             "tiny", "decode"],
+                    choices=["bench", "prefill-chunks", "prefill-chunks-fp8", "decode-fp8",
+                             "splitkv", "shared-prefix", "tiny", "decode"],
                     help="a single timed case for profiling: prefill-chunks (the attention "
                          "call on the mixed batch's prefill chunks, own pool), decode-fp8 (the "
                          "decode batch over fp8 pools), splitkv (the long-context split-KV "
                          "call), shared-prefix (the fork batch's attention call), tiny (the "
-                         "fp32 tiny mixed batch), decode (the decode batch's attention call)")
+                         "fp32 tiny mixed batch), decode (the decode batch's attention call), "
+                         "prefill-chunks-fp8 (the prefill chunks over e4m3 pools)")
     ap.add_argument("--min-timed-ms", type=float, default=1000.0,
                     help="the timed loop of --steps steps is repeated until the repeats "
                          "together take at least this long (at least 5 repeats)")
@@ -453,6 +454,35 @@ def fp8_decode(pa, dev, args, peaks, stream, n):
                                 "frac_of_hbm": kv / (ms_h * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
 
 
+def fp8_prefill(pa, dev, args, peaks, stream, n):
+    """The mixed batch's prefill chunks over e4m3 pools with dequantisation scales (the
+    tcgen05 kernel widens the codes to f16 in shared memory), L2 flushed between calls."""
+    import torch
+
+    from paged_kv_cache_31_gb300 import workloads
+
+    wp = workloads.prefill_chunks(seed=args.seed, device=dev)
+    kb8, vb8 = workloads.fp8_pools(wp)
+    out = torch.empty_like(wp.q)
+    ws = pa.workspace_for(wp.q, kb8, wp.query_start_loc, wp.block_tables)
+
+    def call():
+        pa.pa_varlen_forward(wp.q, kb8, vb8, out, wp.query_start_loc, wp.seq_lens,
+                             wp.positions, wp.block_tables, wp.scale,
+                             sliding_window=wp.sliding_window, workspace=ws, k_scale=0.125,
+                             v_scale=0.125)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    ms = time_calls(call, n, stream, flush=l2_flush_buffer(dev))
+    assert pa.pa_device_status() == pa.PA_OK
+    fl = attn_flops(wp)
+    return {"workload": wp.name + "-fp8", "flops": fl, "ms": ms, "l2": "flushed between calls",
+            "tflops": fl / (ms * 1e-3) / 1e12,
+            "frac_of_bf16_peak": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "mma": "f16 x f16 (codes and q widened to f16), fp32 accumulation"}
+
+
 def secondary(pa, dev, args, peaks, stream):
     """Per-class measurements of the mixed batch (prefill chunks alone: TFLOP/s of the
     tcgen05 path; decode tokens alone: K/V GB/s), the long-context split-KV batch and the
@@ -505,6 +535,8 @@ def secondary(pa, dev, args, peaks, stream):
     torch.cuda.empty_cache()
 
     res["fp8_decode"] = fp8_decode(pa, dev, args, peaks, stream, n)
+    torch.cuda.empty_cache()
+    res["fp8_prefill"] = fp8_prefill(pa, dev, args, peaks, stream, n)
     torch.cuda.empty_cache()
 
     w4 = workloads.named(4, seed=args.seed, device=dev)
@@ -576,6 +608,11 @@ def main():
     from paged_kv_cache_31_gb300 import binding as pa
 
     peaks = measured_peaks()
+    if args.case == "prefill-chunks-fp8":
+        print(json.dumps(dict(case="prefill-chunks-fp8",
+                              **fp8_prefill(pa, dev, args, peaks, torch.cuda.current_stream(),
+                                            args.steps))), flush=True)
+        return
     if args.case == "decode-fp8":
         print(json.dumps(dict(case="decode-fp8", **fp8_decode(pa, dev, args, peaks,
                                                                torch.cuda.current_stream(),

@@ -74,7 +74,7 @@ constexpr int kOffQ = 0;                          // two Q buffers (consecutive 
 constexpr int kOffK = kOffQ + 2 * kTile;
 constexpr int kOffV = kOffK + kStagesK * kPart;
 constexpr int kOffBar = kOffV + kStagesV * kPart;
-constexpr int kNumBarsMax = 40;
+constexpr int kNumBarsMax = 48;
 constexpr int kOffTmem = kOffBar + kNumBarsMax * 8;
 constexpr int kOffFlag = kOffTmem + 16;
 // softmax pair exchange: [half][row] fp32 row max (or row sum), then [half][row] int failed-
@@ -107,7 +107,9 @@ enum : int {
   B_VFULL = B_KEMPTY + kStagesK,
   B_VEMPTY = B_VFULL + kStagesV,
   B_VCONV = B_VEMPTY + kStagesV,  // leader: the stage's V is f16 in both CTAs
-  B_SFULL = B_VCONV + kStagesV,
+  B_QCONV = B_VCONV + kStagesV,   // leader, fp8 pools: the Q buffer is f16 in both CTAs
+  B_KCONV = B_QCONV + 2,          // leader, fp8 pools: the stage's K is f16 in both CTAs
+  B_SFULL = B_KCONV + kStagesK,
   B_PFULL = B_SFULL + kSBufs,
   B_PVDONE = B_PFULL + kSBufs,
   B_OFREE = B_PVDONE + kSBufs,
@@ -215,6 +217,7 @@ constexpr uint32_t idesc_f16kind(int M, int N, int b_mn_major, int bf16) {
 }
 constexpr uint32_t kIdescQK = idesc_f16kind(256, 128, 0, 1);  // bf16 Q, K; M spans the pair
 constexpr uint32_t kIdescPV = idesc_f16kind(256, 128, 1, 0);  // f16 P, V
+constexpr uint32_t kIdescQK16 = idesc_f16kind(256, 128, 0, 0);  // fp8 pools: f16 Q, K
 
 // ---- thread-block cluster (pairs of CTAs on two SMs) ------------------------------------------
 
@@ -389,20 +392,23 @@ __device__ void drain_ring(const Ctx& c, int full, uint32_t nst, uint32_t issued
     mbar_wait(c.bar + full + k % nst, (k / nst) & 1u, c.limit);
 }
 
+template <bool FP8>
 __device__ void producer_loop(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
                               const CUtensorMap* tkv, bool is_v, int n_items, uint32_t& kv,
                               uint32_t& q_issued);
 
+template <bool FP8>
 __device__ void producer(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
                          const CUtensorMap* tkv, bool is_v, int n_items) {
   uint32_t kv = 0, q_issued = 0;  // K (or V) stage loads and Q loads issued
-  producer_loop(c, p, tq, tkv, is_v, n_items, kv, q_issued);
+  producer_loop<FP8>(c, p, tq, tkv, is_v, n_items, kv, q_issued);
   // normally every issued copy has been consumed and these return at once
   drain_ring(c, is_v ? B_VFULL : B_KFULL, is_v ? kStagesV : kStagesK, kv);
   if (!is_v) drain_ring(c, B_QFULL, 2, q_issued);
   __syncwarp();
 }
 
+template <bool FP8>
 __device__ void producer_loop(const Ctx& c, const TcParams& p, const CUtensorMap* tq,
                               const CUtensorMap* tkv, bool is_v, int n_items, uint32_t& kv,
                               uint32_t& q_issued) {
@@ -445,7 +451,7 @@ __device__ void producer_loop(const Ctx& c, const TcParams& p, const CUtensorMap
       bool ok = true;
       if (lane == 0) {
         ok = wait_bar(c, empty + st, ph ^ 1u);
-        if (ok) mbar_arrive_expect_tx(c.bar + full + st, kPart);
+        if (ok) mbar_arrive_expect_tx(c.bar + full + st, FP8 ? kPart / 2 : kPart);
       }
       // K: lane l loads dim half l / 4 of block 4 * rank + l % 4; V: lane l loads block l
       const int my_id = __shfl_sync(kFull, id, is_v ? (lane & 7) : 4 * (int)c.rank + (lane & 3));
@@ -453,11 +459,18 @@ __device__ void producer_loop(const Ctx& c, const TcParams& p, const CUtensorMap
       if (__shfl_sync(kFull, (int)ok, 0) && lane < 8) {
         uint8_t* dst = c.sm + off + st * kPart;
         const int r = my_id >= 0 ? my_id * 16 : -16;
-        if (!is_v)
+        if constexpr (FP8) {  // the codes go where the converters widen them in place
+          if (!is_v && lane < 4)  // block 4 * rank + lane, all 128 dims (128 x 1 x 16 bytes)
+            tma_load_3d(dst + kPart / 2 + lane * 2048, tkv, 0, I.kvh, r, c.bar + full + st);
+          else if (is_v)  // block lane, dims 64 * rank .. (64 x 1 x 16 bytes), into the back
+            tma_load_3d(dst + lane * 2048 + 1024, tkv, 64 * (int)c.rank, I.kvh, r,  // half of
+                        c.bar + full + st);                                        // its rows
+        } else if (!is_v) {
           tma_load_3d(dst + (lane >> 2) * kKVHalf + (lane & 3) * 2048, tkv, 64 * (lane >> 2),
                       I.kvh, r, c.bar + full + st);
-        else
+        } else {
           tma_load_3d(dst + lane * 2048, tkv, 64 * (int)c.rank, I.kvh, r, c.bar + full + st);
+        }
       }
       // kv counts the loads issued: the loop's increment is skipped for this unissued one
       if (!__shfl_sync(kFull, (int)ok, 0)) return;
@@ -476,19 +489,25 @@ __device__ void producer_loop(const Ctx& c, const TcParams& p, const CUtensorMap
 __device__ __forceinline__ uint32_t buf_of(uint32_t s) { return s % kSBufs; }
 __device__ __forceinline__ uint32_t use_par(uint32_t s) { return (s / kSBufs) & 1u; }
 
+template <bool FP8>
 __device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
   const uint32_t sm = smem_u32(c.sm);
+  const bool leader = c.rank == 0, fp8 = FP8;
+  // fp8 pools: the converters tell the leader when both CTAs' Q and K parts are f16, and the
+  // peer's warp has nothing to forward
+  if (fp8 && !leader) return;
+  const uint32_t idesc = fp8 ? kIdescQK16 : kIdescQK;
+  const int qready = fp8 ? B_QCONV : B_QFULL, kready = fp8 ? B_KCONV : B_KFULL;
   uint32_t kv = 0, it_cnt = 0;
   for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
     const uint32_t qb = it_cnt & 1u;
-    const bool leader = c.rank == 0;
-    if (!__all_sync(kFull, wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u))) return;
+    if (!__all_sync(kFull, wait_bar(c, qready + qb, (it_cnt >> 1) & 1u))) return;
     if (!leader && (threadIdx.x & 31) == 0) arrive_leader(c.bar + B_QFULL + qb);
     const uint32_t qbase = sm + kOffQ + qb * kTile;
     for (int j = 0; j < I.ntiles; ++j) {
       const uint32_t s = kv + j, st = s % kStagesK, b = buf_of(s);
-      if (!__all_sync(kFull, wait_bar(c, B_KFULL + st, (s / kStagesK) & 1u))) return;
+      if (!__all_sync(kFull, wait_bar(c, kready + st, (s / kStagesK) & 1u))) return;
       if (!leader) {
         if ((threadIdx.x & 31) == 0) arrive_leader(c.bar + B_KFULL + st);
         continue;
@@ -500,7 +519,7 @@ __device__ void s_issuer(const Ctx& c, const TcParams& p, uint32_t tmem, int n_i
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         tc_mma_l0(tmem + col_s(b), sdesc(qbase + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-                  sdesc(kb + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024), kIdescQK,
+                  sdesc(kb + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024), idesc,
                   kk > 0 ? 1u : 0u);
       tc_commit_mc_l0(c.bar + B_SFULL + b, 0x3);
       tc_commit_mc_l0(c.bar + B_KEMPTY + st, 0x3);
@@ -612,6 +631,111 @@ __device__ void v_converter(const Ctx& c, const TcParams& p, int n_items) {
       if (atomicCAS(p.redo_flags + pi, 0, 1) == 0) p.redo_list[atomicAdd(p.redo_count, 1)] = pi;
     }
     kv += I.ntiles;
+  }
+}
+
+
+// Two e4m3 codes per 16-bit half of w -> four f16 in two words (element order kept), exactly.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& a, uint32_t& b) {
+  a = e4m3x2_to_f16x2((uint16_t)(w & 0xffffu));
+  b = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+}
+
+// Converters over fp8 pools (e4m3 codes: K = k_scale * code, V = v_scale * code; the codes widen
+// to f16 exactly).  TMA writes a stage's codes into part of its 16 KB slot, and each converter
+// warp widens its own blocks into the f16 operand the MMAs read (rows of 128 bytes with the
+// 128-byte swizzle):
+//   K, warp w: block w of this CTA's four.  Its codes (16 rows x 128, swizzled like the
+//     operand) sit where its second dim half goes, [8 KB + 2 KB w, + 2 KB); the warp loads all
+//     of them, then writes dims 0..63 to [2 KB w, + 2 KB) and dims 64..127 over them.
+//   V, warp w: blocks 2w and 2w + 1.  Block b's codes (16 rows x this CTA's 64 dims, plain
+//     64-byte rows) sit in the back half of its own 2 KB output, [2 KB b + 1 KB, + 1 KB); the
+//     warp loads them, then writes the 16 f16 rows of 128 bytes over the whole 2 KB.  Rows at
+//     positions >= seq_len become zeros.
+// Every byte a warp overwrites is one it loaded itself, so __syncwarp() orders the loads
+// before the stores and the four warps need no barrier between them.  Q (bf16 from TMA) is
+// widened to f16 in place once per item, a quarter per warp: exact in f16's normal range,
+// which is how the warp-MMA fp8 path takes q as well.
+__device__ void fp8_converter(const Ctx& c, const TcParams& p, int n_items) {
+  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) - kFirstConvWarp;
+  uint32_t kv = 0, it_cnt = 0;
+  for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
+    const Item I = load_item(p, idx, c.rank);
+    {  // Q: this warp's quarter of the 128 x 128 bf16 tile, 16 chunks of 16 bytes per lane
+      const uint32_t qb = it_cnt & 1u;
+      if (!__all_sync(kFull, wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u))) return;
+      uint4* q = reinterpret_cast<uint4*>(c.sm + kOffQ + qb * kTile) + w * (kTile / 16 / 4);
+#pragma unroll 4
+      for (int i = 0; i < kTile / 16 / 4 / 32; ++i) {
+        uint4 v = q[lane + 32 * i];
+        v.x = bf16x2_to_f16x2(v.x);
+        v.y = bf16x2_to_f16x2(v.y);
+        v.z = bf16x2_to_f16x2(v.z);
+        v.w = bf16x2_to_f16x2(v.w);
+        q[lane + 32 * i] = v;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) arrive_leader(c.bar + B_QCONV + qb);
+    }
+    for (int j = 0; j < I.ntiles; ++j, ++kv) {
+      {  // K block w
+        const uint32_t st = kv % kStagesK;
+        if (!__all_sync(kFull, wait_bar(c, B_KFULL + st, (kv / kStagesK) & 1u))) return;
+        uint8_t* slot = c.sm + kOffK + st * kPart;
+        const uint4* stg = reinterpret_cast<const uint4*>(slot + kPart / 2 + w * 2048);
+        // four rounds of rows 4i .. 4i + 3: a round's stores overwrite only the staged codes
+        // of its own rows, which all lanes have loaded before the __syncwarp
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i) {
+          const uint4 src = stg[lane + 32 * i];
+          __syncwarp();
+          const int q = lane + 32 * i;                // staged chunk: row q / 8, chunk q % 8
+          const int r = q >> 3, L = (q & 7) ^ (r & 7);  // key row, dims 16 L .. 16 L + 15
+          const int h = L >> 2, c0 = 2 * (L & 3);     // dim half, first output chunk
+          uint4 lo, hi;
+          widen4(src.x, lo.x, lo.y);
+          widen4(src.y, lo.z, lo.w);
+          widen4(src.z, hi.x, hi.y);
+          widen4(src.w, hi.z, hi.w);
+          uint8_t* row = slot + h * kKVHalf + w * 2048 + r * 128;
+          *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) arrive_leader(c.bar + B_KCONV + st);
+      }
+      {  // V blocks 2w, 2w + 1
+        const uint32_t st = kv % kStagesV;
+        if (!__all_sync(kFull, wait_bar(c, B_VFULL + st, (kv / kStagesV) & 1u))) return;
+        uint8_t* slot = c.sm + kOffV + st * kPart;
+        const int pos0 = I.kv0 + j * kBN;  // position of the tile's first key
+        // per block, rows 0..7 first (their stores land in the block's front kilobyte, where
+        // no codes are staged), then rows 8..15, whose stores overwrite the block's staged
+        // codes: all loaded by then (__syncwarp)
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i) {
+          const int b = 2 * w + (i >> 1), q = lane + 32 * (i & 1);
+          const uint4 src = reinterpret_cast<const uint4*>(slot + b * 2048 + 1024)[q];
+          if (i & 1) __syncwarp();
+          const int r = q >> 2, L = q & 3;  // key row, dims 16 L .. 16 L + 15
+          uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+          if (pos0 + b * 16 + r < I.n) {  // rows past seq_len were never written
+            widen4(src.x, lo.x, lo.y);
+            widen4(src.y, lo.z, lo.w);
+            widen4(src.z, hi.x, hi.y);
+            widen4(src.w, hi.z, hi.w);
+          }
+          uint8_t* row = slot + b * 2048 + r * 128;
+          *reinterpret_cast<uint4*>(row + (((2 * L) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(row + (((2 * L + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) arrive_leader(c.bar + B_VCONV + st);
+      }
+    }
   }
 }
 
@@ -831,6 +955,7 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
   }
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_prefill(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const TcParams p) {
@@ -852,8 +977,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t n = 1;
       if (leader) {
-        if ((i >= B_QFULL && i < B_QFULL + 2) || (i >= B_KFULL && i < B_KFULL + kStagesK)) n = 2;
-        if (i >= B_VCONV && i < B_VCONV + kStagesV) n = 2 * kConvWarps;
+        // bf16 pools: q / k full count the leader's own TMA and the peer's forward; fp8 pools:
+        // the own TMA only (the converters then arrive on q / k / v conv, from both CTAs)
+        if ((i >= B_QFULL && i < B_QFULL + 2) || (i >= B_KFULL && i < B_KFULL + kStagesK))
+          n = FP8 ? 1 : 2;
+        if ((i >= B_VCONV && i < B_VCONV + kStagesV) || (i >= B_QCONV && i < B_QCONV + 2) ||
+            (i >= B_KCONV && i < B_KCONV + kStagesK))
+          n = 2 * kConvWarps;
         if ((i >= B_PFULL && i < B_PFULL + kSBufs) || i == B_OFREE) n = 2 * kSoftWarps;
         if (i == B_FIN) n = 2;
       }
@@ -888,24 +1018,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_rank(), (int)cluster_id_x(), pairs};
   const int n_items = (flags[0] || c.cluster >= pairs) ? 0 : p.plan[1] * p.m.num_kv_heads;
 
-  // warps 0..3 (one warpgroup) produce and issue, warps 12..15 convert V: both need few
-  // registers; the two softmax warpgroups take theirs: 8 x 56 + 8 x 200 = 16 x 128, the
-  // launch's registers per thread (each branch ends the kernel itself, so no code runs under
-  // two limits)
+  // warps 0..3 (one warpgroup) produce and issue, warps 12..15 convert: both need few
+  // registers; the two softmax warpgroups take theirs.  bf16 pools: 4 x 56 + 8 x 200 + 4 x 56,
+  // e4m3 pools (the converters also widen K and Q): 4 x 64 + 8 x 184 + 4 x 80; both 16 x 128,
+  // the launch's registers per thread (each branch ends the kernel itself, so no code runs
+  // under two limits)
+  static_assert(4 * 56 + 8 * 200 + 4 * 56 <= kThreads / 32 * 128, "register split, bf16");
+  static_assert(4 * 64 + 8 * 184 + 4 * 80 <= kThreads / 32 * 128, "register split, e4m3");
   if (warp >= kFirstConvWarp) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
-    v_converter(c, p, n_items);
+    if constexpr (FP8)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    else
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    if constexpr (FP8)
+      fp8_converter(c, p, n_items);
+    else
+      v_converter(c, p, n_items);
     tc_fence_before();
     cluster_sync();
   } else if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    if constexpr (FP8)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+    else
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     if (warp == 0) {
-      producer(c, p, &tq, &tk, false, n_items);
+      producer<FP8>(c, p, &tq, &tk, false, n_items);
     } else if (warp == 2) {
-      producer(c, p, &tq, &tv, true, n_items);
+      producer<FP8>(c, p, &tq, &tv, true, n_items);
     } else if (warp == 1 || warp == 3) {
       if (warp == 1)
-        s_issuer(c, p, tmem, n_items);
+        s_issuer<FP8>(c, p, tmem, n_items);
       else
         pv_issuer(c, p, tmem, n_items);
       __syncwarp();
@@ -930,7 +1072,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : "memory");
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
+    if constexpr (FP8)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
+    else
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     softmax_role(c, p, tmem, n_items);
     tc_fence_before();
     cluster_sync();
@@ -942,8 +1087,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_tc_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const TcParams& p, int grid, cudaStream_t stream) {
   if (grid < 2) grid = 2;
-  cudaError_t e =
-      cudaFuncSetAttribute(k_tc_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  auto kern = p.kv_fp8 ? k_tc_prefill<true> : k_tc_prefill<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // pairs of CTAs (a cluster of two SMs) run the 2-SM MMAs
   cudaLaunchConfig_t cfg = {};
@@ -960,7 +1105,7 @@ cudaError_t launch_tc_prefill(const CUtensorMap& tq, const CUtensorMap& tk, cons
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_tc_prefill, tq, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace pa

@@ -117,6 +117,23 @@ bool pool_map_fp8(CUtensorMap* map, const void* base, int64_t num_blocks, int bl
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same byte tensor with a 64 x 1 x 16 box and no swizzle: the 64 dims of one half of a
+// head size of 128 for one (block, kv head), 1 KB of plain 64-byte rows (the tcgen05 prefill
+// kernel's V part of a CTA).
+bool pool_map_fp8_half(CUtensorMap* map, const void* base, int64_t num_blocks, int block_size,
+                       int hkv, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)(num_blocks * block_size)};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)hkv * d};
+  cuuint32_t box[3] = {64, 1, 16};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // TMA descriptor of q [T, H, D] bf16 seen as the 3-D tensor (D, H, T): a 64 x G x 128/G box
 // is the 64-dim half of a 128-row query tile whose rows are the G heads of one kv head for
 // 128/G consecutive tokens.
@@ -447,12 +464,14 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
   int32_t* plan = static_cast<int32_t*>(workspace);  // (the plan also checks per-head scales)
   PlanLayout L = plan_layout(num_seqs, num_tokens, m.group);
   const bool fast = mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
+  const bool fast8 =
+      mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
   // prefill-class sequences (more than 64 query rows per kv head) go to the tcgen05 kernel:
-  // head size 128 and a GQA group that divides the 128-row tile
+  // head size 128 and a GQA group that divides the 128-row tile; bf16 or e4m3 pools
   // No sequence can have more than num_tokens - num_seqs + 1 query tokens: when even that
   // many rows fit the warp-MMA path, the tcgen05 kernel is not launched at all.
   const int64_t max_rows = (num_tokens - (num_seqs > 0 ? num_seqs : 1) + 1) * m.group;
-  L.use_tc = fast && head_dim == 128 && m.group <= 128 && (128 % m.group) == 0 &&
+  L.use_tc = (fast || fast8) && head_dim == 128 && m.group <= 128 && (128 % m.group) == 0 &&
              aligned(q, 16) && max_rows > L.tc_min_rows && scale > 0.f && tc_enabled() &&
              !(flags & PA_FLAG_BITWISE);
 
@@ -472,8 +491,9 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
     if (e != cudaSuccess) return PA_ECUDA;
   }
 
-  if (mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out)) {
-    // fp8 pools: every sequence on the warp-MMA kernel (the plan had use_tc off)
+  if (fast8) {
+    // fp8 pools: prefill-class sequences on the tcgen05 kernel (the codes widened to f16 in
+    // shared memory), then the decode tiles on the warp-MMA kernel, as for bf16 pools
     CUtensorMap tk, tv;
     if (!pool_map_fp8(&tk, k_blocks, num_blocks, block_size, num_kv_heads, head_dim) ||
         !pool_map_fp8(&tv, v_blocks, num_blocks, block_size, num_kv_heads, head_dim))
@@ -488,6 +508,30 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
     p.status = d->status;
     p.scale_log2 = scale * kLog2e;
     mma_waits(p);
+    if (L.use_tc) {
+      CUtensorMap tq, tv_half;
+      if (!query_map(&tq, q, num_tokens, num_heads, head_dim, m.group) ||
+          !pool_map_fp8_half(&tv_half, v_blocks, num_blocks, block_size, num_kv_heads, head_dim))
+        return PA_ECUDA;
+      TcParams tp;
+      std::memset(&tp, 0, sizeof tp);
+      tp.out = out;
+      tp.m = m;
+      tp.plan = plan;
+      tp.tc_off = L.tc_off;
+      tp.status = d->status;
+      tp.scale_log2 = scale * kLog2e;
+      stall_hook(tp.wait_limit_ns, tp.debug_stall);
+      tp.redo_flags = plan + L.redo_off;
+      tp.redo_list = plan + L.redo_list_off;
+      tp.redo_count = plan + 3;
+      tp.kv_fp8 = 1;
+      e = launch_tc_prefill(tq, tk, tv_half, tp, tc_grid, stream);
+      if (e != cudaSuccess) return PA_ECUDA;
+      p.after_tc = 1;
+      p.tc_off = L.tc_off;
+      p.redo_list_off = L.redo_list_off;
+    }
     return from_cuda(
         launch_mma16_varlen_fp8(tk, tv, p, (int)std::min<int64_t>(L.mma_cap, 65535), stream));
   }

@@ -388,6 +388,7 @@ struct TcParams {
   float scale_log2;
   uint64_t wait_limit_ns;
   uint32_t debug_stall;  // tests only: the softmax waits run out (PA_DEBUG_STALL_NS)
+  int32_t kv_fp8;        // e4m3 pools (tk: 128 x 1 x 16 byte boxes, tv: 64 x 1 x 16)
   // items whose V does not fit f16 (recomputed by the warp-MMA kernel afterwards): a flag per
   // 256-row item, the list of marked items and its length (all in the plan)
   int32_t* redo_flags;

@@ -148,7 +148,7 @@ CASES = {
     # decode tokens on the fp8 warp-MMA kernel, GQA 4
     "decode": dict(seq_lens=[1, 17, 300, 1000, 4096], q_lens=[1] * 5, num_heads=32,
                    num_kv_heads=8, head_dim=128),
-    # prefill chunks too: fp8 pools keep every sequence on the warp-MMA kernel
+    # prefill chunks too: the tcgen05 kernel widens the codes to f16 in shared memory
     "prefill": dict(seq_lens=[512, 700, 1300, 90, 2000], q_lens=[512, 200, 130, 1, 1],
                     num_heads=32, num_kv_heads=8, head_dim=128),
     # sliding window, GQA 2

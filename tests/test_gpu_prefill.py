@@ -165,3 +165,43 @@ def test_mixed_batch_equals_its_parts_bitwise(pa):
                              causal=w.causal, sliding_window=w.sliding_window)
         assert pa.pa_device_status() == pa.PA_OK
         assert torch.equal(out, mixed[rows]), f"{len(part)} sequences differ from the mixed call"
+
+
+@pytest.mark.parametrize("H,Hkv,window,causal", [(32, 8, 0, True), (8, 8, 0, True),
+                                                 (64, 8, 300, True), (32, 2, 0, False),
+                                                 (16, 8, 64, True)])
+def test_prefill_fp8_pools(pa, H, Hkv, window, causal):
+    """Prefill chunks over e4m3 pools on the tcgen05 kernel: the codes are staged by TMA and
+    widened to f16 in shared memory by the converter warps (K into the dim-half layout, V
+    into the MN-major one, rows past seq_len zeroed), q widened to f16 once per item; against
+    the oracle over the same codes and scales, with NaN codes in the never-written rows."""
+    import oracle
+    prior = [0, 5, 200, 1000, 40, 3000]
+    chunk = [150, 130, 256, 97, 1, 1]
+    w = workloads.build("pre8", seq_lens=[p + c for p, c in zip(prior, chunk)], q_lens=chunk,
+                        num_heads=H, num_kv_heads=Hkv, head_dim=128, seed=H + Hkv + window,
+                        sliding_window=window, causal=causal, device=DEV)
+    kb8, vb8 = workloads.fp8_pools(w)
+    tab = w.block_tables.cpu()
+    for s, n in enumerate(w.seq_lens_list):
+        if n % 16:
+            blk = int(tab[s, (n - 1) // 16])
+            kb8.view(torch.uint8)[blk, n % 16:] = 0x7F
+            vb8.view(torch.uint8)[blk, n % 16:] = 0xFF
+    ks, vs = 0.125, 0.0625
+    out = torch.full_like(w.q, float("nan"))
+    pa.pa_varlen_forward(w.q, kb8, vb8, out, w.query_start_loc, w.seq_lens, w.positions,
+                         w.block_tables, w.scale, causal=causal, sliding_window=window,
+                         k_scale=ks, v_scale=vs)
+    assert pa.pa_device_status() == pa.PA_OK
+    st, ref, _ = oracle.varlen_attention(w.q.cpu(), kb8.cpu(), vb8.cpu(), w.query_start_loc,
+                                         w.seq_lens, w.positions, w.block_tables, w.scale,
+                                         causal=causal, sliding_window=window, k_scale=ks,
+                                         v_scale=vs)
+    assert st == oracle.OK
+    assert_attn_close(out, ref, f"fp8 prefill H {H} Hkv {Hkv} window {window}")
+    again = torch.empty_like(out)
+    pa.pa_varlen_forward(w.q, kb8, vb8, again, w.query_start_loc, w.seq_lens, w.positions,
+                         w.block_tables, w.scale, causal=causal, sliding_window=window,
+                         k_scale=ks, v_scale=vs)
+    assert torch.equal(out, again), "not deterministic"
