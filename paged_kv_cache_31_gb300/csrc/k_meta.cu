@@ -520,7 +520,8 @@ __global__ void __launch_bounds__(1024)
   // the tcgen05 kernel's working pairs: every candidate K evaluated by its own thread
   if (L.use_tc && L.force_pairs <= 0) {
     const float tiles = (float)s_tc_tiles * m.num_kv_heads;
-    const float dec_bytes = (float)s_dec_units * m.num_kv_heads * 4.f * m.head_dim;
+    const float dec_bytes =
+        (float)s_dec_units * m.num_kv_heads * 2.f * L.kv_elem_bytes * m.head_dim;
     for (int k0 = warp * 32 + 1; k0 <= L.tc_pairs; k0 += blockDim.x) {
       const int k = k0 + lane;
       const unsigned long long key =

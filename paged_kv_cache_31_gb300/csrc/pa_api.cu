@@ -480,6 +480,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
   const int tc_grid = (int)std::max<int64_t>(2, std::min<int64_t>(tc_work, d->sms)) & ~1;
   L.tc_pairs = tc_grid / 2;
   L.num_sms = d->sms;
+  L.kv_elem_bytes = esize(kv_dtype);
   cudaError_t e = launch_plan_varlen(m, plan, L, d->status, stream);
   if (e != cudaSuccess) return PA_ECUDA;
   if (cache) {  // the new tokens' slots and rows, alongside the plan

@@ -278,6 +278,7 @@ struct PlanLayout {
   float tile_ns;           // one 128-key tile of a 256-row item on one pair
   float hbm_bytes_per_ns;  // decode tiles' K/V streaming rate on the whole GPU
   float margin;            // the prefill estimate is taken this much longer
+  int32_t kv_elem_bytes;   // bytes of one pool element (2 bf16, 1 e4m3), for the decode bytes
 };
 
 // Layout of the plan for a batch of num_tokens tokens over num_seqs sequences.
@@ -302,6 +303,7 @@ inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t grou
   L.tile_ns = 1300.f;
   L.hbm_bytes_per_ns = 6700.f;
   L.margin = 1.1f;
+  L.kv_elem_bytes = 2;
   return L;
 }
 
