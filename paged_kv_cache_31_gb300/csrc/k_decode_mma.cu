@@ -27,17 +27,26 @@
 // box of 2 KB with the 128-byte swizzle, so a stage is half the bf16 one and the ring is
 // twice as deep.  The codes stay in shared memory as they arrived; each lane loads the
 // bytes of its own MMA fragments with 16-byte loads and widens them in registers to f16
-// (exact for e4m3), and the products run on the f16 m16n8k16 MMA.  To make every lane's bytes
-// contiguous, both contractions are read in a permuted order, which leaves the sums alone:
-//   S = Q K^T: in k-step kk, fragment column 2c + j (c = lane % 4) is dimension 32c + 4kk + j
-//     and column 2c + 8 + j is dimension 32c + 4kk + 2 + j, so the lane reads bytes
-//     [32c, 32c + 32) of its key row and q is loaded in the same order;
-//   O = P V: output n-tile nt, fragment column n is dimension 16n + nt, so the lane reads
-//     bytes [16g, 16g + 16) (g = lane / 4) of its four key rows, pairs the bytes of rows 2c,
-//     2c + 1 (and 2c + 8, 2c + 9) with byte permutes and widens each pair; the accumulator
-//     columns are put back in order when the warps' states are merged.
-// k_scale is folded into the score scale and v_scale into the final normalisation.  P enters
-// the PV product as one f16 fragment (11 significant bits) instead of the bf16 hi/lo pair.
+// (exact for e4m3), and the products run on the f16 m16n8k16 MMA.  The operands are swapped
+// against the bf16 path: the block's 16 keys are the MMA's M and the tile's query rows its
+// N, in groups of 8 (S^T = K Q^T, O^T = V^T P^T).  For a GQA group of up to 8 heads a decode
+// token is one group: half the MMAs, exponentials and rescales of a 16-row tile.  Varlen
+// tiles over e4m3 pools are therefore 8 rows (the plan cuts them so), and a split-KV
+// partition of a larger group runs two groups with the same code per group, so a row's bits
+// do not depend on the tile it sits in.  Both contractions read their dimensions in a
+// permuted order, which leaves the sums alone and makes every lane's bytes contiguous:
+//   S^T = K Q^T: in k-step kk, fragment column 2c + j (c = lane % 4) is dimension
+//     32c + 4kk + j and column 2c + 8 + j is dimension 32c + 4kk + 2 + j, so the lane reads
+//     bytes [32c, 32c + 32) of key rows g and g + 8 (g = lane / 4), and q is loaded in the
+//     same order;
+//   O^T = V^T P^T: in M-tile t = 2i + h, fragment row g is dimension 16g + 4i + 2h and row
+//     g + 8 dimension 16g + 4i + 2h + 1, so the lane reads bytes [16g, 16g + 16) of its four
+//     key rows 2c, 2c + 1, 2c + 8, 2c + 9 and pairs them with byte permutes before widening;
+//     the accumulator rows are put back in order when the warps' states are merged.
+// P^T reaches the B operand by transposing the two 8 x 8 halves of its accumulator layout
+// across the warp (movmatrix).  k_scale is folded into the score scale and v_scale into the
+// final normalisation.  P enters the PV product as one f16 fragment (11 significant bits)
+// instead of the bf16 hi/lo pair.
 #include <algorithm>
 
 #include "pa_internal.cuh"
@@ -81,6 +90,19 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
   return pack_f16x2(f.x, f.y);
 }
 
+// Transpose of an 8 x 8 matrix of 16-bit elements held in the accumulator layout (lane l:
+// row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1), returned in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+template <int N>
+struct IntTag {
+  static constexpr int value = N;
+};
+
 // Byte offset of 16-byte chunk `chunk` (along D) of row `row` inside a tile written by TMA
 // with the 128-byte swizzle: halves of 64 dims are separate 2 KB boxes; inside a half the
 // chunk index is XORed with row mod 8.
@@ -94,6 +116,8 @@ __global__ void __launch_bounds__(NW * 32, 2)
     k_mma16(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
             const Mma16Params p) {
   using G_ = Geom<D, FP8>;
+  // query rows per tile: e4m3 varlen tiles are one group of 8 (one N of the swapped MMAs)
+  constexpr int TR = (FP8 && !SPLIT) ? 8 : 16;
   extern __shared__ uint8_t smem_raw[];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -170,7 +194,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
         __syncthreads();  // every thread has read the slot before it is written again
         pdl_wait();       // the tcgen05 kernel has finished: its marks are final
         phase = 1;
-        n_units = *reinterpret_cast<const volatile int32_t*>(p.plan + 3) * 16 * m.num_kv_heads;
+        n_units = *reinterpret_cast<const volatile int32_t*>(p.plan + 3) * (256 / TR) * m.num_kv_heads;
         continue;
       }
       item = unit / m.num_kv_heads;
@@ -188,13 +212,13 @@ __global__ void __launch_bounds__(NW * 32, 2)
       int2 it;
       if (phase == 0) {
         it = items[item];
-      } else {  // tile item % 16 of marked item item / 16: (sequence, 16-row tile index)
-        const int4 t4 =
-            reinterpret_cast<const int4*>(p.plan + p.tc_off)[p.plan[p.redo_list_off + item / 16]];
-        it = make_int2(t4.x, t4.y * 16 + item % 16);
+      } else {  // tile k of marked item j (item = j * 256 / TR + k): (sequence, tile index)
+        const int4 t4 = reinterpret_cast<const int4*>(
+            p.plan + p.tc_off)[p.plan[p.redo_list_off + item / (256 / TR)]];
+        it = make_int2(t4.x, t4.y * (256 / TR) + item % (256 / TR));
       }
       s = it.x;
-      row0 = it.y * 16;
+      row0 = it.y * TR;
       qs = m.query_start_loc[s];
       rows_total = (m.query_start_loc[s + 1] - qs) * G;
     }
@@ -208,7 +232,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int R = row0 + (lane >> 2) + 8 * i;
-      valid[i] = R < rows_total;
+      valid[i] = (i == 0 || TR == 16) && R < rows_total;
       const int tl = valid[i] ? R / G : 0;
       tok[i] = qs + tl;
       head[i] = kvh * G + (valid[i] ? R % G : 0);
@@ -275,8 +299,9 @@ __global__ void __launch_bounds__(NW * 32, 2)
     }
 
     // ---------------------------------------------------------------- streaming
-    float mrow[2] = {-INFINITY, -INFINITY};
-    float lrow[2] = {0.f, 0.f};
+    // bf16: this lane's rows g and g + 8 in [0], [1].  fp8: rows 8j + 2c + e in [2j + e].
+    float mrow[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    float lrow[4] = {0.f, 0.f, 0.f, 0.f};
     float o[G_::kNT][4];
 #pragma unroll
     for (int j = 0; j < G_::kNT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -306,6 +331,158 @@ __global__ void __launch_bounds__(NW * 32, 2)
       }
     };
 
+    // fp8: the tile's query rows are the MMA's N, in groups of 8, and the block's 16 keys its
+    // M.  A lane holds columns 2c, 2c + 1 of each group: their visible ranges come from the
+    // lanes that loaded those rows above (row 8j + r sits in lane 4r, index j).
+    const int nr = TR == 8 || rows_total - row0 <= 8 ? 1 : 2;  // row groups of this tile
+    int cst[2][2], cen[2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        cst[j][e] = __shfl_sync(kFull, st[j], (2 * (lane & 3) + e) * 4);
+        cen[j][e] = __shfl_sync(kFull, en[j], (2 * (lane & 3) + e) * 4);
+      }
+    // keys every valid row of the tile sees: blocks inside that range need no mask
+    int all_lo = 0, all_hi = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if (valid[i]) {
+        all_lo = max(all_lo, st[i]);
+        all_hi = min(all_hi, en[i]);
+      }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      all_lo = max(all_lo, __shfl_xor_sync(kFull, all_lo, o));
+      all_hi = min(all_hi, __shfl_xor_sync(kFull, all_hi, o));
+    }
+    auto fp8_step = [&](auto groups, const uint8_t* kt, const uint8_t* vt, int key_base) {
+      constexpr int NR = decltype(groups)::value;
+      const int c = lane & 3, g = lane >> 2;
+      // S^T = K Q^T: A = key rows g and g + 8, bytes [32c, 32c + 32) (chunks 2c, 2c + 1); B =
+      // the q fragments of group j, qa[kk][j] and qa[kk][j + 2]
+      const uint32_t kbase = smem_u32(kt);
+      uint4 kw[2][2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int key = g + mt * 8;
+        kw[mt][0] = lds128(kbase + key * 128 + (((2 * c) ^ (key & 7)) << 4));
+        kw[mt][1] = lds128(kbase + key * 128 + (((2 * c + 1) ^ (key & 7)) << 4));
+      }
+      // two accumulators per group (even / odd k-steps)
+      float sc[NR][4], sc2[NR][4];
+#pragma unroll
+      for (int j = 0; j < NR; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sc[j][i] = sc2[j][i] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < G_::kKS; ++kk) {
+        const uint4& k0 = kw[0][kk >> 2];
+        const uint4& k1 = kw[1][kk >> 2];
+        const int wsel = kk & 3;
+        const uint32_t w0 = wsel == 0 ? k0.x : wsel == 1 ? k0.y : wsel == 2 ? k0.z : k0.w;
+        const uint32_t w1 = wsel == 0 ? k1.x : wsel == 1 ? k1.y : wsel == 2 ? k1.z : k1.w;
+        uint32_t a[4];  // (key g, dims 32c + 4kk + {0, 1}), (key g + 8, same), then dims + 2
+        e4m3x4_to_f16(w0, a[0], a[2]);
+        e4m3x4_to_f16(w1, a[1], a[3]);
+#pragma unroll
+        for (int j = 0; j < NR; ++j) mma_f16_16816((kk & 1) ? sc2[j] : sc[j], a, qa[kk][j], qa[kk][j + 2]);
+      }
+      // sc[j][i]: key g + 8 (i >> 1), row 8j + 2c + (i & 1); mask and scale to log2 units
+      float alpha[NR][2];
+      bool grew = false;  // a row's running max rose: its O needs the rescale (else alpha = 1)
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        if (key_base >= all_lo && key_base + kBlk <= all_hi) {  // padding rows: unused values
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sc[j][i] = (sc[j][i] + sc2[j][i]) * sl2;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int key = key_base + g + 8 * (i >> 1);
+            const int e = i & 1;
+            const bool vis = key >= cst[j][e] && key < cen[j][e];
+            sc[j][i] = vis ? (sc[j][i] + sc2[j][i]) * sl2 : -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          // the column's max over 16 keys: the lane's two, then the eight lanes of the column
+          float mx = fmaxf(sc[j][e], sc[j][2 + e]);
+          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+          const float mo = mrow[2 * j + e];
+          const float mn = fmaxf(mo, mx);
+          const float base = mn == -INFINITY ? 0.f : mn;
+          alpha[j][e] = exp2f(mo - base);
+          grew |= mn > mo;
+          mrow[2 * j + e] = mn;
+          sc[j][e] = exp2f(sc[j][e] - base);
+          sc[j][2 + e] = exp2f(sc[j][2 + e] - base);
+          // l per lane over its two keys of each block; the column's lanes are summed at the end
+          lrow[2 * j + e] = lrow[2 * j + e] * alpha[j][e] + (sc[j][e] + sc[j][2 + e]);
+        }
+      }
+      if (__any_sync(kFull, grew)) {  // skipped, the factors are exactly 1
+#pragma unroll
+        for (int j = 0; j < NR; ++j)
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            o[8 * j + t][0] *= alpha[j][0];
+            o[8 * j + t][1] *= alpha[j][1];
+            o[8 * j + t][2] *= alpha[j][0];
+            o[8 * j + t][3] *= alpha[j][1];
+          }
+      }
+      // P^T as the B operand (k = keys, n = rows): each 8-key half of the f16 accumulator
+      // layout, transposed across the warp, is the fragment of that half
+      uint32_t pb[NR][2];
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        pb[j][0] = movmatrix_trans(pack_f16x2(sc[j][0], sc[j][1]));
+        pb[j][1] = movmatrix_trans(pack_f16x2(sc[j][2], sc[j][3]));
+      }
+      // O^T += V^T P^T.  A = V^T: M-tile t = 2i + h, row g is dimension 16g + 4i + 2h and row
+      // g + 8 dimension 16g + 4i + 2h + 1; its k columns are keys 2c, 2c + 1, 2c + 8, 2c + 9,
+      // so the lane reads bytes [16g, 16g + 16) of those four key rows
+      const uint32_t vbase = smem_u32(vt);
+      const int lim = n - key_base;  // rows at or past it were never written: zeros
+      uint4 vr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = 2 * c + (i & 1) + (i >> 1) * 8;
+        vr[i] = lds128(vbase + r * 128 + ((g ^ (r & 7)) << 4));
+        if (r >= lim) vr[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      const uint32_t ra[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w};
+      const uint32_t rb[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
+      const uint32_t rc[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w};
+      const uint32_t rd[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // byte j of word i is dimension 16g + 4i + j: pair keys (2c, 2c + 1) and (2c + 8,
+        // 2c + 9) byte by byte, lower key in the lower byte
+        const uint32_t lo01 = __byte_perm(ra[i], rb[i], 0x5140);
+        const uint32_t hi01 = __byte_perm(ra[i], rb[i], 0x7362);
+        const uint32_t lo89 = __byte_perm(rc[i], rd[i], 0x5140);
+        const uint32_t hi89 = __byte_perm(rc[i], rd[i], 0x7362);
+        const uint32_t a0[4] = {e4m3x2_to_f16x2((uint16_t)(lo01 & 0xffffu)),
+                                e4m3x2_to_f16x2((uint16_t)(lo01 >> 16)),
+                                e4m3x2_to_f16x2((uint16_t)(lo89 & 0xffffu)),
+                                e4m3x2_to_f16x2((uint16_t)(lo89 >> 16))};
+        const uint32_t a1[4] = {e4m3x2_to_f16x2((uint16_t)(hi01 & 0xffffu)),
+                                e4m3x2_to_f16x2((uint16_t)(hi01 >> 16)),
+                                e4m3x2_to_f16x2((uint16_t)(hi89 & 0xffffu)),
+                                e4m3x2_to_f16x2((uint16_t)(hi89 >> 16))};
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+          mma_f16_16816(o[8 * j + 2 * i], a0, pb[j][0], pb[j][1]);
+          mma_f16_16816(o[8 * j + 2 * i + 1], a1, pb[j][0], pb[j][1]);
+        }
+      }
+    };
+
     const int pro = my_count < NS ? my_count : NS;
     for (int x = 0; x < pro; ++x) issue(x);
     int issued = pro;
@@ -326,162 +503,108 @@ __global__ void __launch_bounds__(NW * 32, 2)
       const int lb = blk_lo + first + x * NW;
       const int key_base = lb * kBlk;
 
-      // rows of the sequence's last block past seq_len were never written: zero their V so
-      // that 0-weight * garbage cannot turn into NaN (fp8: in registers, below)
-      if (!FP8 && key_base + kBlk > n) {
-        const int first = n - key_base;  // 1..15
-        for (int i = lane; i < (kBlk - first) * G_::kHalves * 8; i += 32) {
-          const int r = first + i / (G_::kHalves * 8);
-          const int rest = i % (G_::kHalves * 8);
-          *reinterpret_cast<uint4*>(vt + (rest >> 3) * G_::kHalfBytes + r * 128 + (rest & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-
-      // S = Q K^T for 16 keys: two n-tiles of 8 keys
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      if constexpr (FP8) {
-        // key rows lane / 4 and lane / 4 + 8, bytes [32c, 32c + 32): chunks 2c and 2c + 1
-        const uint32_t kbase = smem_u32(kt);
-        const int c = lane & 3;
-        uint4 kw[2][2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int key = (lane >> 2) + nt * 8;
-          kw[nt][0] = lds128(kbase + key * 128 + (((2 * c) ^ (key & 7)) << 4));
-          kw[nt][1] = lds128(kbase + key * 128 + (((2 * c + 1) ^ (key & 7)) << 4));
-        }
-        // two accumulators per n-tile (even / odd k-steps): four dependent chains of four
-        float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int kk = 0; kk < G_::kKS; ++kk)
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const uint4& q4 = kw[nt][kk >> 2];
-            const uint32_t w = (kk & 3) == 0 ? q4.x : (kk & 3) == 1 ? q4.y : (kk & 3) == 2 ? q4.z : q4.w;
-            uint32_t b0, b1;
-            e4m3x4_to_f16(w, b0, b1);
-            mma_f16_16816((kk & 1) ? sc2[nt] : sc[nt], qa[kk], b0, b1);
+      if constexpr (FP8 && TR == 8) {
+        fp8_step(IntTag<1>{}, kt, vt, key_base);
+      } else if constexpr (FP8) {
+        if (nr == 1)
+          fp8_step(IntTag<1>{}, kt, vt, key_base);
+        else
+          fp8_step(IntTag<2>{}, kt, vt, key_base);
+      } else {
+        // rows of the sequence's last block past seq_len were never written: zero their V so
+        // that 0-weight * garbage cannot turn into NaN
+        if (key_base + kBlk > n) {
+          const int first = n - key_base;  // 1..15
+          for (int i = lane; i < (kBlk - first) * G_::kHalves * 8; i += 32) {
+            const int r = first + i / (G_::kHalves * 8);
+            const int rest = i % (G_::kHalves * 8);
+            *reinterpret_cast<uint4*>(vt + (rest >> 3) * G_::kHalfBytes + r * 128 + (rest & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+
+        // S = Q K^T for 16 keys: two n-tiles of 8 keys
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int key = rr + ((mi >> 1) << 3);
+          const uint32_t kbase = smem_u32(kt);
+#pragma unroll
+          for (int kk = 0; kk < G_::kKS; ++kk) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kbase + tile_off(key, kk * 2 + (mi & 1)), b0, b1, b2, b3);
+            mma_bf16_16816(sc[0], qa[kk], b0, b1);
+            mma_bf16_16816(sc[1], qa[kk], b2, b3);
+          }
+        }
+
+        // mask, scale to log2 units, online softmax update
+        const int kcol = key_base + (lane & 3) * 2;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int c2 = 0; c2 < 4; ++c2) sc[nt][c2] += sc2[nt][c2];
-      } else {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int key = rr + ((mi >> 1) << 3);
-        const uint32_t kbase = smem_u32(kt);
+          for (int c = 0; c < 4; ++c) {
+            const int key = kcol + nt * 8 + (c & 1);
+            const int r = c >> 1;
+            const bool vis = key >= st[r] && key < en[r];
+            sc[nt][c] = vis ? sc[nt][c] * sl2 : -INFINITY;
+          }
+        float alpha[2];
+        bool grew = false;  // a row's running max rose: its O needs the rescale (else alpha = 1)
 #pragma unroll
-        for (int kk = 0; kk < G_::kKS; ++kk) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kbase + tile_off(key, kk * 2 + (mi & 1)), b0, b1, b2, b3);
-          mma_bf16_16816(sc[0], qa[kk], b0, b1);
-          mma_bf16_16816(sc[1], qa[kk], b2, b3);
+        for (int r = 0; r < 2; ++r) {
+          float mx = fmaxf(fmaxf(sc[0][2 * r], sc[0][2 * r + 1]), fmaxf(sc[1][2 * r], sc[1][2 * r + 1]));
+          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+          const float mn = fmaxf(mrow[r], mx);
+          const float base = mn == -INFINITY ? 0.f : mn;
+          alpha[r] = exp2f(mrow[r] - base);
+          grew |= mn > mrow[r];
+          mrow[r] = mn;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            sc[nt][2 * r] = exp2f(sc[nt][2 * r] - base);
+            sc[nt][2 * r + 1] = exp2f(sc[nt][2 * r + 1] - base);
+          }
         }
-      }
-
-      // mask, scale to log2 units, online softmax update
-      const int kcol = key_base + (lane & 3) * 2;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int key = kcol + nt * 8 + (c & 1);
-          const int r = c >> 1;
-          const bool vis = key >= st[r] && key < en[r];
-          sc[nt][c] = vis ? sc[nt][c] * sl2 : -INFINITY;
-        }
-      float alpha[2];
-      bool grew = false;  // a row's running max rose: its O needs the rescale (else alpha = 1)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float mx = fmaxf(fmaxf(sc[0][2 * r], sc[0][2 * r + 1]), fmaxf(sc[1][2 * r], sc[1][2 * r + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-        const float mn = fmaxf(mrow[r], mx);
-        const float base = mn == -INFINITY ? 0.f : mn;
-        alpha[r] = exp2f(mrow[r] - base);
-        grew |= mn > mrow[r];
-        mrow[r] = mn;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          sc[nt][2 * r] = exp2f(sc[nt][2 * r] - base);
-          sc[nt][2 * r + 1] = exp2f(sc[nt][2 * r + 1] - base);
-        }
-      }
-      // P as two bf16 A fragments, hi = bf16(p) and lo = bf16(p - hi): the PV product of
-      // both keeps the weights to ~2^-17 relative, where bf16 P alone can be off by 2^-9 of
-      // |v| when a row sees few keys.  fp8 pools: one f16 fragment.
-      uint32_t ph[4], pl[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a = sc[i >> 1][(i & 1) * 2], b = sc[i >> 1][(i & 1) * 2 + 1];
-        if constexpr (FP8) {
-          ph[i] = pack_f16x2(a, b);
-          pl[i] = 0u;
-          continue;
-        }
-        ph[i] = pack_bf16x2(a, b);
-        const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ph[i]));
-        pl[i] = pack_bf16x2(a - hv.x, b - hv.y);
-      }
-      lrow[0] = lrow[0] * alpha[0] + ((sc[0][0] + sc[0][1]) + (sc[1][0] + sc[1][1]));
-      lrow[1] = lrow[1] * alpha[1] + ((sc[0][2] + sc[0][3]) + (sc[1][2] + sc[1][3]));
-      if (__any_sync(kFull, grew)) {  // skipped, the factors are exactly 1
-#pragma unroll
-        for (int j = 0; j < G_::kNT; ++j) {
-          o[j][0] *= alpha[0];
-          o[j][1] *= alpha[0];
-          o[j][2] *= alpha[1];
-          o[j][3] *= alpha[1];
-        }
-      }
-      // O += P V: V is the k-major B operand, read with transposing ldmatrix
-      if constexpr (FP8) {
-        // key rows 2c, 2c + 1, 2c + 8, 2c + 9, bytes [16g, 16g + 16) of each
-        const uint32_t vbase = smem_u32(vt);
-        const int c = lane & 3, g = lane >> 2;
-        const int lim = n - key_base;  // rows at or past it were never written
-        uint4 vr[4];
+        // P as two bf16 A fragments, hi = bf16(p) and lo = bf16(p - hi): the PV product of
+        // both keeps the weights to ~2^-17 relative, where bf16 P alone can be off by 2^-9 of
+        // |v| when a row sees few keys.
+        uint32_t ph[4], pl[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int r = 2 * c + (i & 1) + (i >> 1) * 8;
-          vr[i] = lds128(vbase + r * 128 + ((g ^ (r & 7)) << 4));
-          if (r >= lim) vr[i] = make_uint4(0u, 0u, 0u, 0u);
+          const float a = sc[i >> 1][(i & 1) * 2], b = sc[i >> 1][(i & 1) * 2 + 1];
+          ph[i] = pack_bf16x2(a, b);
+          const float2 hv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ph[i]));
+          pl[i] = pack_bf16x2(a - hv.x, b - hv.y);
         }
-        const uint32_t ra[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w};
-        const uint32_t rb[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
-        const uint32_t rc[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w};
-        const uint32_t rd[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
+        lrow[0] = lrow[0] * alpha[0] + ((sc[0][0] + sc[0][1]) + (sc[1][0] + sc[1][1]));
+        lrow[1] = lrow[1] * alpha[1] + ((sc[0][2] + sc[0][3]) + (sc[1][2] + sc[1][3]));
+        if (__any_sync(kFull, grew)) {  // skipped, the factors are exactly 1
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          // byte j of word i is dimension 16g + 4i + j: pair rows (2c, 2c + 1) and
-          // (2c + 8, 2c + 9) byte by byte, lower key in the lower byte
-          const uint32_t lo01 = __byte_perm(ra[i], rb[i], 0x5140);
-          const uint32_t hi01 = __byte_perm(ra[i], rb[i], 0x7362);
-          const uint32_t lo89 = __byte_perm(rc[i], rd[i], 0x5140);
-          const uint32_t hi89 = __byte_perm(rc[i], rd[i], 0x7362);
-          const uint32_t pr01[4] = {lo01 & 0xffffu, lo01 >> 16, hi01 & 0xffffu, hi01 >> 16};
-          const uint32_t pr89[4] = {lo89 & 0xffffu, lo89 >> 16, hi89 & 0xffffu, hi89 >> 16};
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_f16_16816(o[4 * i + j], ph, e4m3x2_to_f16x2((uint16_t)pr01[j]),
-                          e4m3x2_to_f16x2((uint16_t)pr89[j]));
+          for (int j = 0; j < G_::kNT; ++j) {
+            o[j][0] *= alpha[0];
+            o[j][1] *= alpha[0];
+            o[j][2] *= alpha[1];
+            o[j][3] *= alpha[1];
+          }
         }
-      } else {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int key = rr + ((mi & 1) << 3);
-        const uint32_t vbase = smem_u32(vt);
+        // O += P V: V is the k-major B operand, read with transposing ldmatrix
+        {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int key = rr + ((mi & 1) << 3);
+          const uint32_t vbase = smem_u32(vt);
 #pragma unroll
-        for (int dd = 0; dd < D / 16; ++dd) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(vbase + tile_off(key, dd * 2 + (mi >> 1)), b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * dd], ph, b0, b1);
-          mma_bf16_16816(o[2 * dd + 1], ph, b2, b3);
-          mma_bf16_16816(o[2 * dd], pl, b0, b1);
-          mma_bf16_16816(o[2 * dd + 1], pl, b2, b3);
+          for (int dd = 0; dd < D / 16; ++dd) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(vbase + tile_off(key, dd * 2 + (mi >> 1)), b0, b1, b2, b3);
+            mma_bf16_16816(o[2 * dd], ph, b0, b1);
+            mma_bf16_16816(o[2 * dd + 1], ph, b2, b3);
+            mma_bf16_16816(o[2 * dd], pl, b0, b1);
+            mma_bf16_16816(o[2 * dd + 1], pl, b2, b3);
+          }
         }
       }
       __syncwarp();
@@ -505,10 +628,19 @@ __global__ void __launch_bounds__(NW * 32, 2)
     ring_pos += issued;
 
     // ---------------------------------------------------------------- merge the warps
+    if constexpr (FP8) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      lrow[r] += __shfl_xor_sync(kFull, lrow[r], 1);
-      lrow[r] += __shfl_xor_sync(kFull, lrow[r], 2);
+      for (int r = 0; r < 4; ++r) {  // the column's eight lanes
+        lrow[r] += __shfl_xor_sync(kFull, lrow[r], 4);
+        lrow[r] += __shfl_xor_sync(kFull, lrow[r], 8);
+        lrow[r] += __shfl_xor_sync(kFull, lrow[r], 16);
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        lrow[r] += __shfl_xor_sync(kFull, lrow[r], 1);
+        lrow[r] += __shfl_xor_sync(kFull, lrow[r], 2);
+      }
     }
     __syncthreads();  // every warp is done with its ring: the O area may alias it now
     if (*reinterpret_cast<volatile int*>(fail)) {
@@ -516,28 +648,36 @@ __global__ void __launch_bounds__(NW * 32, 2)
       return;
     }
     {
-      const int r0 = lane >> 2;
-      if ((lane & 3) == 0) {
-        mrg_m[warp * 16 + r0] = mrow[0];
-        mrg_m[warp * 16 + r0 + 8] = mrow[1];
-        mrg_l[warp * 16 + r0] = lrow[0];
-        mrg_l[warp * 16 + r0 + 8] = lrow[1];
-      }
       float* ob = mrg_o + (size_t)warp * 16 * kOStride;
       if constexpr (FP8) {
-        // accumulator column n of n-tile nt is dimension 16n + nt (n = 2c + j)
-        const int c = lane & 3;
+        // group j, M-tile t = 2i + h: accumulator [e] is (dimension 16g + 4i + 2h, row
+        // 8j + 2c + e), [2 + e] the next dimension
+        const int c = lane & 3, g = lane >> 2;
 #pragma unroll
-        for (int j = 0; j < G_::kNT; j += 2) {
+        for (int j = 0; j < 2; ++j) {
+          if (j >= nr) break;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int col = 16 * (2 * c + e) + j;
-            *reinterpret_cast<float2*>(ob + r0 * kOStride + col) = make_float2(o[j][e], o[j + 1][e]);
-            *reinterpret_cast<float2*>(ob + (r0 + 8) * kOStride + col) =
-                make_float2(o[j][2 + e], o[j + 1][2 + e]);
+            const int row = 8 * j + 2 * c + e;
+            if (g == 0) {
+              mrg_m[warp * 16 + row] = mrow[2 * j + e];
+              mrg_l[warp * 16 + row] = lrow[2 * j + e];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<float4*>(ob + row * kOStride + 16 * g + 4 * i) =
+                  make_float4(o[8 * j + 2 * i][e], o[8 * j + 2 * i][2 + e],
+                              o[8 * j + 2 * i + 1][e], o[8 * j + 2 * i + 1][2 + e]);
           }
         }
       } else {
+        const int r0 = lane >> 2;
+        if ((lane & 3) == 0) {
+          mrg_m[warp * 16 + r0] = mrow[0];
+          mrg_m[warp * 16 + r0 + 8] = mrow[1];
+          mrg_l[warp * 16 + r0] = lrow[0];
+          mrg_l[warp * 16 + r0 + 8] = lrow[1];
+        }
 #pragma unroll
         for (int j = 0; j < G_::kNT; ++j) {
           const int col = j * 8 + (lane & 3) * 2;
@@ -554,7 +694,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
       static_assert(kSeg % 8 == 0, "epilogue writes 16-byte chunks");
       const int row = threadIdx.x / kSegs, seg = threadIdx.x % kSegs;
       const int R = row0 + row;
-      if (R < rows_total) {
+      if (row < TR && R < rows_total) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * 16 + row]);
@@ -622,24 +762,33 @@ __global__ void __launch_bounds__(NW * 32, 2)
   }
 }
 
-constexpr int kNW = 4;
-constexpr int kNS = 3;    // bf16: 8 KB stages (D = 128)
-constexpr int kNS8 = 6;   // fp8: 4 KB stages, twice as many: the same bytes in flight
+// Warps per CTA and ring stages per warp, two CTAs per SM in every case:
+//   bf16: 4 warps x 3 stages of 8 KB (D = 128);
+//   e4m3 split-KV partitions: 4 warps x 6 stages of 4 KB (the same bytes in flight);
+//   e4m3 varlen: 8 warps x 3 stages of 4 KB (the same bytes again).  Its 8-row tiles keep a
+//   thread within 128 registers, so 16 warps share an SM and each (sequence, kv head) is
+//   served by twice the warps: this path is bound by each warp's chain of dependent
+//   instructions (conversions, MMAs, the softmax), not by the bytes in flight.
+template <int D, bool SPLIT, bool FP8>
+struct Shape {
+  static constexpr int NW = (FP8 && !SPLIT) ? 8 : 4;
+  static constexpr int NS = FP8 ? (SPLIT ? 6 : 3) : 3;
+};
 
 template <int D, bool SPLIT, bool FP8 = false>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p, int grid_x,
                    cudaStream_t stream) {
-  constexpr int NS = FP8 ? kNS8 : kNS;
-  auto kern = k_mma16<D, kNW, NS, SPLIT, FP8>;
-  constexpr size_t smem = smem_bytes<D, kNW, NS, FP8>();
-  static_assert((size_t)kNW * 16 * (D + 4) * 4 <= (size_t)kNW * NS * Geom<D, FP8>::kStageBytes,
+  constexpr int NW = Shape<D, SPLIT, FP8>::NW, NS = Shape<D, SPLIT, FP8>::NS;
+  auto kern = k_mma16<D, NW, NS, SPLIT, FP8>;
+  constexpr size_t smem = smem_bytes<D, NW, NS, FP8>();
+  static_assert((size_t)NW * 16 * (D + 4) * 4 <= (size_t)NW * NS * Geom<D, FP8>::kStageBytes,
                 "merge area must fit in the ring");
   static_assert(2 * (smem + 1024) <= 228 * 1024, "two CTAs per SM");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_x, SPLIT ? p.m.num_kv_heads : 1);
-  cfg.blockDim = dim3(kNW * 32, 1, 1);
+  cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -206,9 +206,10 @@ __device__ __forceinline__ int cost_bucket(int c) {
 //     the pool, query positions inside [0, seq_len); the token -> sequence map and the keys the
 //     sequence's rows can see (its work estimate);
 //  B. the work lists: a sequence's q_len * G query rows (token major, head minor within the
-//     kv group) are cut into 16-row tiles for the warp-MMA kernel, or, for prefill-class
-//     sequences, into 256-row items for the tcgen05 kernel; both lists are ordered by the
-//     number of keys their rows see, longest first, so the kernels' last units are short.
+//     kv group) are cut into tiles of 16 rows (8 on e4m3 pools) for the warp-MMA kernel, or,
+//     for prefill-class sequences, into 256-row items for the tcgen05 kernel; both lists are
+//     ordered by the number of keys their rows see, longest first, so the kernels' last units
+//     are short.
 // The kernel is bound by the latency of its loads, not by bandwidth: every sequence's query
 // start and length come into shared memory in one coalesced pass, phase A then issues each
 // sequence's table and position loads together, and the work estimates stay in shared memory
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(1024)
     k_plan_varlen(VarlenMeta m, int32_t* plan, const PlanLayout L, int* status) {
   __shared__ int s_err;
   __shared__ int s_warp[32];
-  __shared__ int s_hist[kCostBuckets];    // 16-row tiles per cost bucket
+  __shared__ int s_hist[kCostBuckets];    // warp-MMA tiles per cost bucket
   __shared__ int s_hist_t[kCostBuckets];  // 256-row items per cost bucket
   __shared__ int s_tot;
   __shared__ unsigned long long s_dec_units;  // decode tiles x visible keys
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(1024)
   int4* tc_tmp = item_cap ? reinterpret_cast<int4*>(s_dyn) : reinterpret_cast<int4*>(plan + L.tc_tmp_off);
   const int tok_per_item = 256 / m.group;  // used only when use_tc (group divides 128)
   // B1: 256-row items of prefill-class sequences, in sequence order, the last one (most keys
-  // under a causal mask) first; the histogram of the 16-row tiles' costs
+  // under a causal mask) first; the histogram of the warp-MMA tiles' costs
   int carry_t = 0;
   if (L.use_tc) {
     unsigned long long dec_units = 0;
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(1024)
         if (rows > L.tc_min_rows)
           ct = (int)((rows + 255) / 256);
         else
-          cm = (int)((rows + 15) / 16);
+          cm = (int)((rows + L.mma_tile_rows - 1) / L.mma_tile_rows);
       }
       if (cm > 0) {
         atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(1024)
     if (lane == 0 && dec_units) atomicAdd(&s_dec_units, dec_units);
   } else {
     for (int s = tid; s < m.num_seqs; s += blockDim.x) {
-      const int cm = (int)(((int64_t)qlen_of(s) * m.group + 15) / 16);
+      const int cm = (int)(((int64_t)qlen_of(s) * m.group + L.mma_tile_rows - 1) / L.mma_tile_rows);
       if (cm > 0) atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
     }
   }
@@ -503,7 +504,7 @@ __global__ void __launch_bounds__(1024)
       tc_items[atomicAdd(&s_hist_t[cost_bucket(it.w - it.z)], 1)] = it;
     }
   }
-  // 16-row tiles, the sequences with the most visible keys first (a counting sort over
+  // warp-MMA tiles, the sequences with the most visible keys first (a counting sort over
   // logarithmic cost buckets), so the persistent kernel's last units are the short ones
   if (warp == 0) warp_scan_inplace<kCostBuckets>(s_hist, &s_tot);  // bucket starts
   __syncthreads();
@@ -511,7 +512,7 @@ __global__ void __launch_bounds__(1024)
   for (int s = tid; s < m.num_seqs; s += blockDim.x) {
     const int64_t rows = (int64_t)qlen_of(s) * m.group;
     if (rows == 0 || (L.use_tc && rows > L.tc_min_rows)) continue;
-    const int cm = (int)((rows + 15) / 16);
+    const int cm = (int)((rows + L.mma_tile_rows - 1) / L.mma_tile_rows);
     const int at = atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
     for (int i = 0; i < cm; ++i) mma_items[at + i] = make_int2(s, i);
   }

@@ -240,7 +240,7 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not lan
 
 // ------------------------------------------------------------------------------------------
 // per-call plan kept in the caller's workspace (int32 words)
-//   [0] number of 16-row tile items (decode-class sequences, warp-MMA kernel)
+//   [0] number of warp-MMA tile items (16 query rows, 8 on e4m3 pools; decode-class sequences)
 //   [1] number of 256-row items (prefill-class sequences, tcgen05 kernel)
 //   [2] work counter of the warp-MMA kernel (zeroed by the plan)
 //   [3] number of 256-row items the tcgen05 kernel marked for recomputing (zeroed by the plan)
@@ -251,7 +251,7 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not lan
 //   [tok_off, tok_off + T)        token -> sequence
 //   [cost_off, cost_off + S)      per sequence: keys its query rows can see (work estimate;
 //                                 written only for batches too large to keep it in smem)
-//   [mma_off, + 2 * mma_cap)      int2 items (seq, 16-row tile), longest first
+//   [mma_off, + 2 * mma_cap)      int2 items (seq, tile index), longest first
 //   [tc_off, + 4 * tc_cap)        int4 items (seq, 256-row item, kv lo, kv hi), longest first
 //   [tc_tmp_off, + 4 * tc_cap)    the same items in sequence order (planning scratch)
 //   [redo_off, + tc_cap)          per 256-row item: marked for recomputing (zeroed by the plan)
@@ -279,13 +279,14 @@ struct PlanLayout {
   float hbm_bytes_per_ns;  // decode tiles' K/V streaming rate on the whole GPU
   float margin;            // the prefill estimate is taken this much longer
   int32_t kv_elem_bytes;   // bytes of one pool element (2 bf16, 1 e4m3), for the decode bytes
+  int32_t mma_tile_rows;   // query rows per warp-MMA tile: 16, or 8 on e4m3 pools
 };
 
 // Layout of the plan for a batch of num_tokens tokens over num_seqs sequences.
 inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t group) {
   PlanLayout L;
   L.tok_off = kPlanHeaderWords;
-  L.mma_cap = (num_tokens * group + 15) / 16 + num_seqs + 1;
+  L.mma_cap = (num_tokens * group + 7) / 8 + num_seqs + 1;  // room for 8-row tiles
   L.tc_cap = (num_tokens * group + 255) / 256 + num_seqs + 1;
   L.cost_off = L.tok_off + num_tokens;
   L.mma_off = (L.cost_off + num_seqs + 3) & ~int64_t(3);
@@ -304,6 +305,7 @@ inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t grou
   L.hbm_bytes_per_ns = 6700.f;
   L.margin = 1.1f;
   L.kv_elem_bytes = 2;
+  L.mma_tile_rows = 16;
   return L;
 }
 
