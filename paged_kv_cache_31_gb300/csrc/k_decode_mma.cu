@@ -163,17 +163,15 @@ __global__ void __launch_bounds__(NW * 32, 2)
 
   // Split-KV: grid (partition x sequence, kv head), strided.  Varlen: a persistent 1-D grid
   // whose CTAs take (item, kv head) units from the plan's work counter, longest items first;
-  // then (behind the tcgen05 kernel) the 16-row tiles of the 256-row items that kernel marked
+  // then (behind the tcgen05 kernel) the tiles of the 256-row items that kernel marked
   // (V outside f16's range), from a second counter.
   int n_units;
-  const int2* items = nullptr;
   int* unit_slot = fail + 1;
   int phase = 0;
   if constexpr (SPLIT) {
     n_units = m.num_seqs * p.max_parts;
   } else {
     n_units = p.plan[0] * m.num_kv_heads;
-    items = reinterpret_cast<const int2*>(p.plan + p.items_off);
   }
 
   for (int it_no = 0;; ++it_no) {
@@ -202,32 +200,43 @@ __global__ void __launch_bounds__(NW * 32, 2)
     }
     // ---------------------------------------------------------------- item geometry
     int s, row0, rows_total, part = 0, qs, n;
+    int lo = INT_MAX, hi = 0;  // the union of the tile's rows' visible key ranges
+    bool have_range = false;   // the plan's tile record carries it
     if constexpr (SPLIT) {
       s = item / p.max_parts;
       part = item % p.max_parts;
       qs = s;
       row0 = 0;
       rows_total = G;
-    } else {
-      int2 it;
-      if (phase == 0) {
-        it = items[item];
-      } else {  // tile k of marked item j (item = j * 256 / TR + k): (sequence, tile index)
-        const int4 t4 = reinterpret_cast<const int4*>(
-            p.plan + p.tc_off)[p.plan[p.redo_list_off + item / (256 / TR)]];
-        it = make_int2(t4.x, t4.y * (256 / TR) + item % (256 / TR));
-      }
-      s = it.x;
-      row0 = it.y * TR;
+      n = m.seq_lens[s];
+    } else if (phase == 0) {
+      // the plan's record: (sequence, tile, query start, seq_len), (key range, rows): the
+      // first copies can be issued without waiting for the positions
+      const int4* rec = reinterpret_cast<const int4*>(p.plan + p.items_off) + 2 * item;
+      const int4 r0 = rec[0], r1 = rec[1];
+      s = r0.x;
+      row0 = r0.y * TR;
+      qs = r0.z;
+      n = r0.w;
+      lo = r1.x;
+      hi = r1.y;
+      rows_total = r1.z;
+      have_range = true;
+    } else {  // tile k of marked item j (item = j * 256 / TR + k): (sequence, tile index)
+      const int4 t4 = reinterpret_cast<const int4*>(
+          p.plan + p.tc_off)[p.plan[p.redo_list_off + item / (256 / TR)]];
+      s = t4.x;
+      row0 = (t4.y * (256 / TR) + item % (256 / TR)) * TR;
       qs = m.query_start_loc[s];
       rows_total = (m.query_start_loc[s + 1] - qs) * G;
+      n = m.seq_lens[s];
     }
-    n = m.seq_lens[s];
     // K = k_scales[kvh] * pool goes into the score scale (per kv head, when given)
     const float sl2 = head_scale(m.k_scales, kvh, p.scale_log2);
 
-    // this lane's two rows: r0 = lane / 4 and r1 = r0 + 8
-    int st[2], en[2], tok[2], head[2];
+    // this lane's two rows: r0 = lane / 4 and r1 = r0 + 8 (their positions are loaded now and
+    // used after the first copies are on their way)
+    int st[2], en[2], tok[2], head[2], pos[2];
     bool valid[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -236,32 +245,38 @@ __global__ void __launch_bounds__(NW * 32, 2)
       const int tl = valid[i] ? R / G : 0;
       tok[i] = qs + tl;
       head[i] = kvh * G + (valid[i] ? R % G : 0);
-      int e, b;
-      if constexpr (SPLIT) {
-        e = n;  // the decode query sits at n - 1: causal by construction
-        b = m.window > 0 ? max(0, e - m.window) : 0;
-        b = max(b, part * p.partition_size);
-        e = min(e, (part + 1) * p.partition_size);
-      } else {
-        const int pos = m.positions[tok[i]];
-        e = m.causal ? pos + 1 : n;
-        b = m.window > 0 ? max(0, e - m.window) : 0;
-      }
-      st[i] = valid[i] ? b : 0;
-      en[i] = valid[i] ? max(e, b) : 0;
+      pos[i] = (!SPLIT && valid[i]) ? m.positions[tok[i]] : 0;
     }
-    // union of the rows' visible ranges -> the blocks to stream
-    int lo = INT_MAX, hi = 0;
+    auto row_ranges = [&]() {
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-      if (valid[i] && en[i] > st[i]) {
-        lo = min(lo, st[i]);
-        hi = max(hi, en[i]);
+      for (int i = 0; i < 2; ++i) {
+        int e, b;
+        if constexpr (SPLIT) {
+          e = n;  // the decode query sits at n - 1: causal by construction
+          b = m.window > 0 ? max(0, e - m.window) : 0;
+          b = max(b, part * p.partition_size);
+          e = min(e, (part + 1) * p.partition_size);
+        } else {
+          e = m.causal ? pos[i] + 1 : n;
+          b = m.window > 0 ? max(0, e - m.window) : 0;
+        }
+        st[i] = valid[i] ? b : 0;
+        en[i] = valid[i] ? max(e, b) : 0;
       }
+    };
+    if (!have_range) {
+      row_ranges();
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      lo = min(lo, __shfl_xor_sync(kFull, lo, o));
-      hi = max(hi, __shfl_xor_sync(kFull, hi, o));
+      for (int i = 0; i < 2; ++i)
+        if (valid[i] && en[i] > st[i]) {
+          lo = min(lo, st[i]);
+          hi = max(hi, en[i]);
+        }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        lo = min(lo, __shfl_xor_sync(kFull, lo, o));
+        hi = max(hi, __shfl_xor_sync(kFull, hi, o));
+      }
     }
     const int blk_lo = lo < hi ? lo / kBlk : 0;
     const int nblk = lo < hi ? (hi + kBlk - 1) / kBlk - blk_lo : 0;
@@ -272,31 +287,6 @@ __global__ void __launch_bounds__(NW * 32, 2)
     const int first = ((warp - blk_lo) % NW + NW) % NW;  // this warp's first block, relative
     const int my_count = nblk > first ? (nblk - first + NW - 1) / NW : 0;
     const int32_t* table_row = m.block_tables + (int64_t)s * m.max_blocks;
-
-    // ---------------------------------------------------------------- q fragments
-    uint32_t qa[G_::kKS][4];
-    {
-      const uint32_t* q0 =
-          reinterpret_cast<const uint32_t*>(p.q + ((int64_t)tok[0] * H + head[0]) * D);
-      const uint32_t* q1 =
-          reinterpret_cast<const uint32_t*>(p.q + ((int64_t)tok[1] * H + head[1]) * D);
-      const int c = (lane & 3);
-#pragma unroll
-      for (int kk = 0; kk < G_::kKS; ++kk) {
-        if constexpr (FP8) {  // f16, dimensions in the permuted order (header comment)
-          const int w = 16 * c + 2 * kk;
-          qa[kk][0] = valid[0] ? bf2_to_h2(q0[w]) : 0u;
-          qa[kk][1] = valid[1] ? bf2_to_h2(q1[w]) : 0u;
-          qa[kk][2] = valid[0] ? bf2_to_h2(q0[w + 1]) : 0u;
-          qa[kk][3] = valid[1] ? bf2_to_h2(q1[w + 1]) : 0u;
-          continue;
-        }
-        qa[kk][0] = valid[0] ? q0[kk * 8 + c] : 0u;
-        qa[kk][1] = valid[1] ? q1[kk * 8 + c] : 0u;
-        qa[kk][2] = valid[0] ? q0[kk * 8 + 4 + c] : 0u;
-        qa[kk][3] = valid[1] ? q1[kk * 8 + 4 + c] : 0u;
-      }
-    }
 
     // ---------------------------------------------------------------- streaming
     // bf16: this lane's rows g and g + 8 in [0], [1].  fp8: rows 8j + 2c + e in [2j + e].
@@ -330,6 +320,37 @@ __global__ void __launch_bounds__(NW * 32, 2)
         }
       }
     };
+
+    const int pro = my_count < NS ? my_count : NS;
+    for (int x = 0; x < pro; ++x) issue(x);
+    int issued = pro;
+    bool timed_out = false;
+    if (have_range) row_ranges();
+
+    // ---------------------------------------------------------------- q fragments
+    uint32_t qa[G_::kKS][4];
+    {
+      const uint32_t* q0 =
+          reinterpret_cast<const uint32_t*>(p.q + ((int64_t)tok[0] * H + head[0]) * D);
+      const uint32_t* q1 =
+          reinterpret_cast<const uint32_t*>(p.q + ((int64_t)tok[1] * H + head[1]) * D);
+      const int c = (lane & 3);
+#pragma unroll
+      for (int kk = 0; kk < G_::kKS; ++kk) {
+        if constexpr (FP8) {  // f16, dimensions in the permuted order (header comment)
+          const int w = 16 * c + 2 * kk;
+          qa[kk][0] = valid[0] ? bf2_to_h2(q0[w]) : 0u;
+          qa[kk][1] = valid[1] ? bf2_to_h2(q1[w]) : 0u;
+          qa[kk][2] = valid[0] ? bf2_to_h2(q0[w + 1]) : 0u;
+          qa[kk][3] = valid[1] ? bf2_to_h2(q1[w + 1]) : 0u;
+          continue;
+        }
+        qa[kk][0] = valid[0] ? q0[kk * 8 + c] : 0u;
+        qa[kk][1] = valid[1] ? q1[kk * 8 + c] : 0u;
+        qa[kk][2] = valid[0] ? q0[kk * 8 + 4 + c] : 0u;
+        qa[kk][3] = valid[1] ? q1[kk * 8 + 4 + c] : 0u;
+      }
+    }
 
     // fp8: the tile's query rows are the MMA's N, in groups of 8, and the block's 16 keys its
     // M.  A lane holds columns 2c, 2c + 1 of each group: their visible ranges come from the
@@ -482,11 +503,6 @@ __global__ void __launch_bounds__(NW * 32, 2)
         }
       }
     };
-
-    const int pro = my_count < NS ? my_count : NS;
-    for (int x = 0; x < pro; ++x) issue(x);
-    int issued = pro;
-    bool timed_out = false;
 
     for (int x = 0; x < my_count; ++x) {
       const uint32_t cnt = ring_pos + x;

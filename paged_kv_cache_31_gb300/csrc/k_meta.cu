@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(1024)
     return cached ? s_qsl[s + 1] - s_qsl[s] : m.query_start_loc[s + 1] - m.query_start_loc[s];
   };
   auto cost_of = [&](int s) -> int { return cached ? s_cost[s] : plan[L.cost_off + s]; };
-  int2* mma_items = reinterpret_cast<int2*>(plan + L.mma_off);
+  int4* mma_recs = reinterpret_cast<int4*>(plan + L.mma_off);
   int4* tc_items = reinterpret_cast<int4*>(plan + L.tc_off);
   // the items in sequence order: in shared memory when they fit, else in the plan
   int4* tc_tmp = item_cap ? reinterpret_cast<int4*>(s_dyn) : reinterpret_cast<int4*>(plan + L.tc_tmp_off);
@@ -512,9 +512,35 @@ __global__ void __launch_bounds__(1024)
   for (int s = tid; s < m.num_seqs; s += blockDim.x) {
     const int64_t rows = (int64_t)qlen_of(s) * m.group;
     if (rows == 0 || (L.use_tc && rows > L.tc_min_rows)) continue;
-    const int cm = (int)((rows + L.mma_tile_rows - 1) / L.mma_tile_rows);
+    const int tr = L.mma_tile_rows;
+    const int cm = (int)((rows + tr - 1) / tr);
     const int at = atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
-    for (int i = 0; i < cm; ++i) mma_items[at + i] = make_int2(s, i);
+    const int qs = cached ? s_qsl[s] : m.query_start_loc[s];
+    const int n = cached ? s_n[s] : m.seq_lens[s];
+    for (int i = 0; i < cm; ++i) {
+      // the union of the visible key ranges of the tile's tokens, formed as the kernel would
+      // from the rows' positions (rows that see nothing do not count)
+      const int64_t ra = (int64_t)i * tr, rb = min(rows, ra + tr);
+      int lo = INT_MAX, hi = 0;
+      for (int64_t tl = ra / m.group; tl <= (rb - 1) / m.group; ++tl) {
+        const int64_t t = qs + tl;
+        int st, en;
+        if (tok_cached) {
+          st = s_ts[t];
+          en = s_te[t];
+        } else {
+          const int e = m.causal ? m.positions[t] + 1 : n;
+          st = m.window > 0 ? max(0, e - m.window) : 0;
+          en = max(e, st);
+        }
+        if (en > st) {
+          lo = min(lo, st);
+          hi = max(hi, en);
+        }
+      }
+      mma_recs[2 * (at + i)] = make_int4(s, i, qs, n);
+      mma_recs[2 * (at + i) + 1] = make_int4(lo, hi, (int)rows, 0);
+    }
   }
   // no 256-row item is marked for recomputing yet (the tcgen05 kernel marks them)
   for (int k = tid; k < carry_t; k += blockDim.x) plan[L.redo_off + k] = 0;

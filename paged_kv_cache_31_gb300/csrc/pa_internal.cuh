@@ -251,7 +251,9 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: a TMA that has not lan
 //   [tok_off, tok_off + T)        token -> sequence
 //   [cost_off, cost_off + S)      per sequence: keys its query rows can see (work estimate;
 //                                 written only for batches too large to keep it in smem)
-//   [mma_off, + 2 * mma_cap)      int2 items (seq, tile index), longest first
+//   [mma_off, + 8 * mma_cap)      warp-MMA tile records, longest first: two int4 each,
+//                                 (seq, tile index, query start, seq_len) and (union of the
+//                                 tile's rows' visible key ranges [lo, hi), q_len * G, 0)
 //   [tc_off, + 4 * tc_cap)        int4 items (seq, 256-row item, kv lo, kv hi), longest first
 //   [tc_tmp_off, + 4 * tc_cap)    the same items in sequence order (planning scratch)
 //   [redo_off, + tc_cap)          per 256-row item: marked for recomputing (zeroed by the plan)
@@ -290,7 +292,7 @@ inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t grou
   L.tc_cap = (num_tokens * group + 255) / 256 + num_seqs + 1;
   L.cost_off = L.tok_off + num_tokens;
   L.mma_off = (L.cost_off + num_seqs + 3) & ~int64_t(3);
-  L.tc_off = (L.mma_off + 2 * L.mma_cap + 3) & ~int64_t(3);
+  L.tc_off = (L.mma_off + 8 * L.mma_cap + 3) & ~int64_t(3);
   L.tc_tmp_off = L.tc_off + 4 * L.tc_cap;
   L.redo_off = L.tc_tmp_off + 4 * L.tc_cap;
   L.redo_list_off = L.redo_off + L.tc_cap;
@@ -345,7 +347,7 @@ struct Mma16Params {
   void* out;  // bf16 [T, H, D] (varlen) / [S, H, D]
   VarlenMeta m;
   const int32_t* plan;  // varlen: workspace plan; split: nullptr
-  int64_t items_off;    // varlen: word offset of the int2 item list in the plan
+  int64_t items_off;    // varlen: word offset of the tile records in the plan
   int* status;
   float scale_log2;  // scale * log2(e)
   // split-KV partial outputs (mode split)
