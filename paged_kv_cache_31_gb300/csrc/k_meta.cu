@@ -215,6 +215,10 @@ __device__ __forceinline__ int cost_bucket(int c) {
 // sequence's table and position loads together, and the work estimates stay in shared memory
 // (up to kPlanCacheSeqs sequences; larger batches read everything from global memory).  The
 // bucket scans run in one warp, and the prefill-item pass only when the tcgen05 kernel runs.
+// TOK: the batch's sequences and tokens fit the planner's shared memory; TC: the tcgen05
+// kernel runs (L.use_tc).  Each instance holds only the code its batches run: the kernel's
+// time is mostly latency, and instruction fetches from a cold L2 are part of it.
+template <bool TOK, bool TC>
 __global__ void __launch_bounds__(1024)
     k_plan_varlen(VarlenMeta m, int32_t* plan, const PlanLayout L, int* status) {
   __shared__ int s_err;
@@ -230,12 +234,14 @@ __global__ void __launch_bounds__(1024)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   pdl_wait();               // launched early: the batch's metadata may still be in flight
   pdl_launch_dependents();  // the attention kernels' prologues may overlap this kernel
-  if (blockIdx.x > 0) {     // blocks 1 .. V check the block tables
-    if (!status_set(status)) check_tables(m, status);
-    return;
+  if constexpr (TOK) {
+    if (blockIdx.x > 0) {  // blocks 1 .. V check the block tables
+      if (!status_set(status)) check_tables(m, status);
+      return;
+    }
   }
-  const bool cached = m.num_seqs <= kPlanCacheSeqs;
-  const bool tok_cached = cached && m.num_tokens <= kPlanCacheTokens;
+  const bool cached = TOK || m.num_seqs <= kPlanCacheSeqs;
+  constexpr bool tok_cached = TOK;
   const int item_cap = cached ? plan_items_cached(L) : 0;
   int* s_qsl = s_dyn + 4 * item_cap;
   int* s_n = s_qsl + (cached ? m.num_seqs + 1 : 0);
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(1024)
   const int tpt = (int)((m.num_tokens + blockDim.x - 1) / blockDim.x);  // <= kPlanTokPer
   const int t_first = tid * tpt;
   int32_t pos0[kPlanTokPer];
-  if (tok_cached) {
+  if constexpr (tok_cached) {
 #pragma unroll
     for (int u = 0; u < kPlanTokPer; ++u)
       pos0[u] = (u < tpt && t_first + u < m.num_tokens) ? m.positions[t_first + u] : 0;
@@ -280,7 +286,7 @@ __global__ void __launch_bounds__(1024)
         if (!(ks > 0.f && ks <= 3.402823466e38f) || !(vs > 0.f && vs <= 3.402823466e38f))
           atomicCAS(&s_err, 0, PA_EINVAL);
       }
-    if (tok_cached) {
+    if constexpr (tok_cached) {
       // A1: per sequence (a thread each): the query-start order, a table long enough for
       // seq_len, and an empty visible range to fill in (the entries themselves are checked
       // by the other blocks of this launch)
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(1024)
   // B1: 256-row items of prefill-class sequences, in sequence order, the last one (most keys
   // under a causal mask) first; the histogram of the warp-MMA tiles' costs
   int carry_t = 0;
-  if (L.use_tc) {
+  if constexpr (TC) {
     unsigned long long dec_units = 0;
     for (int base = 0; base < m.num_seqs; base += blockDim.x) {
       const int s = base + tid;
@@ -474,7 +480,7 @@ __global__ void __launch_bounds__(1024)
       int lo = INT_MAX, hi = 0;
       for (int t = ta + lane; t < tb; t += 32) {
         int e, st;
-        if (tok_cached) {
+        if constexpr (tok_cached) {
           e = s_te[t];
           st = s_ts[t];
         } else {
@@ -511,7 +517,7 @@ __global__ void __launch_bounds__(1024)
   const int carry_m = s_tot;
   for (int s = tid; s < m.num_seqs; s += blockDim.x) {
     const int64_t rows = (int64_t)qlen_of(s) * m.group;
-    if (rows == 0 || (L.use_tc && rows > L.tc_min_rows)) continue;
+    if (rows == 0 || (TC && rows > L.tc_min_rows)) continue;
     const int tr = L.mma_tile_rows;
     const int cm = (int)((rows + tr - 1) / tr);
     const int at = atomicAdd(&s_hist[cost_bucket(cost_of(s))], cm);
@@ -525,7 +531,7 @@ __global__ void __launch_bounds__(1024)
       for (int64_t tl = ra / m.group; tl <= (rb - 1) / m.group; ++tl) {
         const int64_t t = qs + tl;
         int st, en;
-        if (tok_cached) {
+        if constexpr (tok_cached) {
           st = s_ts[t];
           en = s_te[t];
         } else {
@@ -545,7 +551,7 @@ __global__ void __launch_bounds__(1024)
   // no 256-row item is marked for recomputing yet (the tcgen05 kernel marks them)
   for (int k = tid; k < carry_t; k += blockDim.x) plan[L.redo_off + k] = 0;
   // the tcgen05 kernel's working pairs: every candidate K evaluated by its own thread
-  if (L.use_tc && L.force_pairs <= 0) {
+  if (TC && L.force_pairs <= 0) {
     const float tiles = (float)s_tc_tiles * m.num_kv_heads;
     const float dec_bytes =
         (float)s_dec_units * m.num_kv_heads * 2.f * L.kv_elem_bytes * m.head_dim;
@@ -564,7 +570,7 @@ __global__ void __launch_bounds__(1024)
     plan[3] = 0;  // items marked by the tcgen05 kernel
     plan[4] = 0;  // work counter over their units
     int pairs = 0;
-    if (L.use_tc)
+    if (TC)
       pairs = L.force_pairs > 0 ? min(L.force_pairs, L.tc_pairs)
                                 : (int)(0xffffffffu - (unsigned)(s_split & 0xffffffffull));
     plan[5] = max(0, min(pairs, L.tc_pairs));
@@ -982,12 +988,13 @@ cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, const PlanLay
                          ? plan_smem_bytes(m.num_seqs, m.num_tokens, plan_items_cached(L))
                          : 0;
   const int validators = cached ? std::min(m.num_seqs, 32) : 0;
+  auto kern = cached ? (L.use_tc ? k_plan_varlen<true, true> : k_plan_varlen<true, false>)
+                     : (L.use_tc ? k_plan_varlen<false, true> : k_plan_varlen<false, false>);
   cudaError_t e = cudaFuncSetAttribute(
-      k_plan_varlen, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)plan_smem_bytes(kPlanCacheSeqs, kPlanCacheTokens, kPlanCacheItems));
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_plan_varlen, dim3(1 + validators), dim3(1024), dyn, stream, m, plan, L,
-                    status);
+  return launch_pdl(kern, dim3(1 + validators), dim3(1024), dyn, stream, m, plan, L, status);
 }
 
 cudaError_t launch_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
