@@ -508,6 +508,7 @@ __global__ void __launch_bounds__(1024)
     for (int k = tid; k < carry_t; k += blockDim.x) {
       const int4 it = tc_tmp[k];
       tc_items[atomicAdd(&s_hist_t[cost_bucket(it.w - it.z)], 1)] = it;
+      plan[L.redo_off + k] = 0;  // not marked for recomputing (the tcgen05 kernel marks items)
     }
   }
   // warp-MMA tiles, the sequences with the most visible keys first (a counting sort over
@@ -548,10 +549,9 @@ __global__ void __launch_bounds__(1024)
       mma_recs[2 * (at + i) + 1] = make_int4(lo, hi, (int)rows, 0);
     }
   }
-  // no 256-row item is marked for recomputing yet (the tcgen05 kernel marks them)
-  for (int k = tid; k < carry_t; k += blockDim.x) plan[L.redo_off + k] = 0;
-  // the tcgen05 kernel's working pairs: every candidate K evaluated by its own thread
-  if (TC && L.force_pairs <= 0) {
+  // the tcgen05 kernel's working pairs: every candidate K evaluated by its own thread (with no
+  // decode tiles the model picks all pairs, so it is not run)
+  if (TC && L.force_pairs <= 0 && s_dec_units > 0) {
     const float tiles = (float)s_tc_tiles * m.num_kv_heads;
     const float dec_bytes =
         (float)s_dec_units * m.num_kv_heads * 2.f * L.kv_elem_bytes * m.head_dim;
@@ -571,8 +571,9 @@ __global__ void __launch_bounds__(1024)
     plan[4] = 0;  // work counter over their units
     int pairs = 0;
     if (TC)
-      pairs = L.force_pairs > 0 ? min(L.force_pairs, L.tc_pairs)
-                                : (int)(0xffffffffu - (unsigned)(s_split & 0xffffffffull));
+      pairs = L.force_pairs > 0  ? min(L.force_pairs, L.tc_pairs)
+              : s_dec_units == 0 ? L.tc_pairs
+                                 : (int)(0xffffffffu - (unsigned)(s_split & 0xffffffffull));
     plan[5] = max(0, min(pairs, L.tc_pairs));
   }
 }
