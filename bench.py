@@ -35,7 +35,8 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode KV GB/s (% HBM peak); mixed-batch prefill TFLOP/s; tokens/s"
 KERNEL_SOURCES = {"k_mma16": "paged_kv_cache_31_gb300/csrc/k_decode_mma.cu",
                   "k_mma16_fp8": "paged_kv_cache_31_gb300/csrc/k_decode_mma.cu",
-                  "k_tc_prefill": "paged_kv_cache_31_gb300/csrc/k_prefill_tc.cu"}
+                  "k_tc_prefill": "paged_kv_cache_31_gb300/csrc/k_prefill_tc.cu",
+                  "k_tc_prefill_fp8": "paged_kv_cache_31_gb300/csrc/k_prefill_tc.cu"}
 
 
 def parse():
@@ -480,7 +481,8 @@ def fp8_prefill(pa, dev, args, peaks, stream, n):
     return {"workload": wp.name + "-fp8", "flops": fl, "ms": ms, "l2": "flushed between calls",
             "tflops": fl / (ms * 1e-3) / 1e12,
             "frac_of_bf16_peak": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-            "mma": "f16 x f16 (codes and q widened to f16), fp32 accumulation"}
+            "mma": "f16 x f16 (codes and q widened to f16), fp32 accumulation",
+            "traffic": ncu_traffic("k_tc_prefill_fp8", wp.name + "-fp8")}
 
 
 def secondary(pa, dev, args, peaks, stream):
