@@ -701,7 +701,8 @@ def main():
         houts = [torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory() for _ in range(2)]
         h2d = sum(nb for _, nb in layout.values())
         d2h = houts[0].numel() * houts[0].element_size()
-        e2e_steps = max(1, args.steps // 4)
+        e2e_steps = args.steps  # per repeat, as the device-timed loop
+        e2e_repeats = 5          # the same on every rank (each repeat ends at a barrier)
         cstream = torch.cuda.Stream(device=dev)
         copied = [torch.cuda.Event() for _ in range(2)]
         done = [torch.cuda.Event() for _ in range(2)]
@@ -727,15 +728,18 @@ def main():
         prefetch(0)
         for i in range(3):
             e2e_step(i)
-        torch.cuda.synchronize()
-        barrier()
-        t0 = time.perf_counter()
-        prefetch(0)
-        for i in range(e2e_steps):
-            e2e_step(i)
-        torch.cuda.synchronize()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-        barrier()
+        e2e_reps = []
+        for _ in range(e2e_repeats):
+            torch.cuda.synchronize()
+            barrier()
+            t0 = time.perf_counter()
+            prefetch(0)
+            for i in range(e2e_steps):
+                e2e_step(i)
+            torch.cuda.synchronize()
+            e2e_reps.append((time.perf_counter() - t0) * 1e3 / e2e_steps)
+            barrier()
+        e2e_ms = statistics.median(e2e_reps)
         assert torch.equal(houts[(e2e_steps - 1) & 1].to(dev), run.out), "e2e output differs"
     assert pa.pa_device_status() == pa.PA_OK, "device status set during the timed region"
     clocks = sampler.summary()
@@ -761,7 +765,7 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": T * world / (step_ms * 1e-3),
         "timing": {"step": spread(step_reps), "attention_call": spread(attn_reps),
-                   "steps_per_repeat": args.steps},
+                   "e2e_step": spread(e2e_reps), "steps_per_repeat": args.steps},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
