@@ -189,7 +189,10 @@ __device__ void check_tables(const VarlenMeta& m, int* status) {
     }
     __syncthreads();  // the next round reuses the arrays
   }
-  if (__any_sync(kFull, bad) && lane == 0) record_error(status, PA_EINVAL);
+  if (__any_sync(kFull, bad) && lane == 0) {
+    pdl_wait();  // the planner may run before the kernels ahead of it have finished
+    record_error(status, PA_EINVAL);
+  }
 }
 __device__ __forceinline__ int cost_bucket(int c) {
   if (c <= 0) return kCostBuckets - 1;
@@ -232,7 +235,16 @@ __global__ void __launch_bounds__(1024)
   // when cached: [num_seqs + 1] query starts, [num_seqs] seq_len, [num_seqs] visible keys
   extern __shared__ __align__(16) int s_dyn[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  pdl_wait();               // launched early: the batch's metadata may still be in flight
+  // early: everything the planner computes stays in shared memory until it writes the plan,
+  // so it reads the batch and plans before the kernels ahead of it in the stream have
+  // finished, and waits for them only before its first global write.  Its inputs are
+  // complete when it starts: the kernel ahead of it is this library's (an attention kernel,
+  // the planner or the scatter), which lets its dependents start only after its own wait for
+  // the kernels before it, and none of those writes the batch's metadata; anything else ahead
+  // of it (a copy, another kernel) has finished.  The grid still ends after the kernels ahead
+  // of it, so the kernels behind it see the stream's order.
+  const bool early = TOK && (!TC || L.tc_cap <= kPlanCacheItems);
+  if (!early) pdl_wait();
   pdl_launch_dependents();  // the attention kernels' prologues may overlap this kernel
   if constexpr (TOK) {
     if (blockIdx.x > 0) {  // blocks 1 .. V check the block tables
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(1024)
           }
           const int n = s_n[q];
           bad |= (pos0[u] < 0 || pos0[u] >= n);
-          plan[L.tok_off + t] = q;
+          if (!early) plan[L.tok_off + t] = q;
           const int e = m.causal ? pos0[u] + 1 : n;
           const int st = m.window > 0 ? max(0, e - m.window) : 0;
           s_ts[t] = st;
@@ -416,6 +428,7 @@ __global__ void __launch_bounds__(1024)
   }
   __syncthreads();
   if (s_err != 0) {
+    if (early) pdl_wait();
     if (tid == 0) {
       if (s_err > 0) record_error(status, s_err);
       plan[0] = 0;
@@ -505,6 +518,7 @@ __global__ void __launch_bounds__(1024)
     // B3: the items ordered by cost, longest first (a counting sort over the cost buckets)
     if (warp == 0) warp_scan_inplace<kCostBuckets>(s_hist_t, &s_tot);  // bucket starts
     __syncthreads();
+    if (early) pdl_wait();  // the first global write
     for (int k = tid; k < carry_t; k += blockDim.x) {
       const int4 it = tc_tmp[k];
       tc_items[atomicAdd(&s_hist_t[cost_bucket(it.w - it.z)], 1)] = it;
@@ -515,6 +529,19 @@ __global__ void __launch_bounds__(1024)
   // logarithmic cost buckets), so the persistent kernel's last units are the short ones
   if (warp == 0) warp_scan_inplace<kCostBuckets>(s_hist, &s_tot);  // bucket starts
   __syncthreads();
+  if (early) {
+    pdl_wait();  // (again, when there were items) the plan is written from here on
+    // the token -> sequence map, which only the scalar kernel reads
+    if (L.need_tok_map)
+      for (int t = tid; t < m.num_tokens; t += blockDim.x) {
+        int lo2 = 0, hi2 = m.num_seqs;  // s_qsl[lo2] <= t < s_qsl[hi2]
+        while (hi2 - lo2 > 1) {
+          const int mid = (lo2 + hi2) >> 1;
+          if (s_qsl[mid] <= t) lo2 = mid; else hi2 = mid;
+        }
+        plan[L.tok_off + t] = lo2;
+      }
+  }
   const int carry_m = s_tot;
   for (int s = tid; s < m.num_seqs; s += blockDim.x) {
     const int64_t rows = (int64_t)qlen_of(s) * m.group;
@@ -801,10 +828,12 @@ __global__ void k_validate_scales(const float* k_scales, const float* v_scales,
 // rows (one warp per token).  CTA 0 writes the slot mapping (-1 for an invalid token).  A token
 // that no sequence's range holds is invalid.
 //
-// AFTER_PLAN: launched right after the planning kernel of the same attention call (which has
-// already waited for the kernels before it), so it runs alongside the plan instead of before
-// it; it then waits for the plan before it ends, so the attention kernel behind it (which
-// waits for this grid) still finds both done.
+// AFTER_PLAN: launched right after the planning kernel of the same attention call, so it runs
+// alongside the plan instead of before it.  Its inputs are complete when it starts (the
+// planner's reasoning); its writes wait for the plan, which ends only after the kernels ahead
+// of it (an attention kernel of the previous call may still read a block this scatter writes,
+// when the caller reuses freed blocks).  The attention kernel behind it waits for this grid,
+// so it finds both done.
 constexpr int kFusedSeqs = 2047;
 template <typename VEC, bool AFTER_PLAN>
 __device__ __forceinline__ void map_and_scatter_body(
@@ -851,6 +880,7 @@ __device__ __forceinline__ void map_and_scatter_body(
     bad |= slot < 0;
   }
   bad = __syncthreads_or(bad);
+  if (AFTER_PLAN) pdl_wait();  // the first global write
   if (blockIdx.x == 0)
     for (int t = threadIdx.x; t < num_tokens; t += blockDim.x) slots[t] = s_slot[t];
   if (bad) {
@@ -880,7 +910,7 @@ __global__ void __launch_bounds__(256)
   map_and_scatter_body<VEC, AFTER_PLAN>(k, v, k_blocks, v_blocks, qsl, positions, tables,
                                         num_seqs, num_tokens, max_blocks, block_size,
                                         num_blocks, row_vecs, slots, status);
-  if (AFTER_PLAN) pdl_wait();  // this grid ends only after the plan has
+  if (AFTER_PLAN) pdl_wait();  // this grid ends only after the plan has (CTAs that skipped)
 }
 
 template <typename VEC, bool AFTER_PLAN = false>

@@ -482,6 +482,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
   L.num_sms = d->sms;
   L.kv_elem_bytes = esize(kv_dtype);
   if (fast8) L.mma_tile_rows = 8;  // the e4m3 warp-MMA kernel's tiles are one group of 8 rows
+  L.need_tok_map = !(fast || fast8);  // only the scalar kernel reads the token map
   cudaError_t e = launch_plan_varlen(m, plan, L, d->status, stream);
   if (e != cudaSuccess) return PA_ECUDA;
   if (cache) {  // the new tokens' slots and rows, alongside the plan

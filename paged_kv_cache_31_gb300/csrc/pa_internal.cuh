@@ -282,6 +282,7 @@ struct PlanLayout {
   float margin;            // the prefill estimate is taken this much longer
   int32_t kv_elem_bytes;   // bytes of one pool element (2 bf16, 1 e4m3), for the decode bytes
   int32_t mma_tile_rows;   // query rows per warp-MMA tile: 16, or 8 on e4m3 pools
+  int32_t need_tok_map;    // the scalar kernel runs: write the token -> sequence map
 };
 
 // Layout of the plan for a batch of num_tokens tokens over num_seqs sequences.
@@ -308,6 +309,7 @@ inline PlanLayout plan_layout(int32_t num_seqs, int64_t num_tokens, int32_t grou
   L.margin = 1.1f;
   L.kv_elem_bytes = 2;
   L.mma_tile_rows = 16;
+  L.need_tok_map = 1;
   return L;
 }
 
