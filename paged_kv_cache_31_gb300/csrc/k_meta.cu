@@ -880,6 +880,20 @@ __device__ __forceinline__ void map_and_scatter_body(
     bad |= slot < 0;
   }
   bad = __syncthreads_or(bad);
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t src = (int64_t)t * row_vecs;
+  // the start of this warp's token's rows is loaded before the wait (they are inputs), so
+  // only the stores follow it
+  constexpr int kPre = 4;
+  VEC ka[kPre], va[kPre];
+  if (!bad && t < num_tokens)
+#pragma unroll
+    for (int j = 0; j < kPre; ++j)
+      if (lane + 32 * j < row_vecs) {
+        ka[j] = k[src + lane + 32 * j];
+        va[j] = v[src + lane + 32 * j];
+      }
   if (AFTER_PLAN) pdl_wait();  // the first global write
   if (blockIdx.x == 0)
     for (int t = threadIdx.x; t < num_tokens; t += blockDim.x) slots[t] = s_slot[t];
@@ -887,11 +901,15 @@ __device__ __forceinline__ void map_and_scatter_body(
     if (blockIdx.x == 0 && threadIdx.x == 0) record_error(status, PA_EINVAL);
     return;
   }
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= num_tokens) return;
-  const int64_t dst = (int64_t)s_slot[t] * row_vecs, src = (int64_t)t * row_vecs;
-  for (int64_t i = lane; i < row_vecs; i += 32) {
+  const int64_t dst = (int64_t)s_slot[t] * row_vecs;
+#pragma unroll
+  for (int j = 0; j < kPre; ++j)
+    if (lane + 32 * j < row_vecs) {
+      k_blocks[dst + lane + 32 * j] = ka[j];
+      v_blocks[dst + lane + 32 * j] = va[j];
+    }
+  for (int64_t i = lane + 32 * kPre; i < row_vecs; i += 32) {
     const VEC a = k[src + i];
     const VEC b = v[src + i];
     k_blocks[dst + i] = a;
