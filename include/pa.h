@@ -6,6 +6,15 @@
  * the library allocates no device memory.  Every call is asynchronous on `stream`
  * (0 = the legacy default stream) and returns after enqueueing its kernels.
  *
+ * Stream order.  A call observes everything enqueued before it on `stream` and everything
+ * after it observes the call.  The varlen calls' planning kernel is launched with
+ * programmatic dependent launch and reads the metadata arrays (query_start_loc, seq_lens,
+ * positions, block_tables, per-head scales) before the kernel ahead of it on the stream
+ * has finished; it waits for that kernel before writing anything.  So the metadata must
+ * not be written by a kernel of the caller's that itself releases its programmatic
+ * dependents (griddepcontrol.launch_dependents) before those writes.  Copies, ordinary
+ * kernels and this library's own kernels ahead of the call are all safe.
+ *
  * Layouts (row-major, as the TensorSharp "ManagedPagedAttention.cs" class summary
  * states them):
  *   q, out               [num_tokens, num_heads, head_dim]
