@@ -81,6 +81,10 @@ def lib():
             L.oracle_splitkv_partials_per_head.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                                            i32, i32, i32, i32, i64, i32, i32, i32,
                                                            i32, i32, f32, i32, vp, vp]
+            # the per-block variants take the same arguments as the per-head ones
+            L.oracle_reshape_and_cache_per_block.argtypes = L.oracle_reshape_and_cache_per_head.argtypes
+            L.oracle_varlen_attention_per_block.argtypes = L.oracle_varlen_attention_per_head.argtypes
+            L.oracle_splitkv_partials_per_block.argtypes = L.oracle_splitkv_partials_per_head.argtypes
             L.oracle_splitkv_reduce.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
             L.oracle_merge_attn_states.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i64, i32]
             L.oracle_fp8_to_f32.argtypes = [ctypes.c_uint8]
@@ -176,6 +180,20 @@ def reshape_and_cache_per_head(k, v, k_blocks, v_blocks, slot_mapping_, block_si
                                                    _DT[k_blocks.dtype], _p(ksc), _p(vsc))
 
 
+def reshape_and_cache_per_block(k, v, k_blocks, v_blocks, slot_mapping_, block_size,
+                                k_block_scales, v_block_scales):
+    """Scatter with conversion and one scale per (pool block, kv head): head g of a row written
+    to slot s is stored as k / k_block_scales[s // block_size, g] (None: 1)."""
+    k, v, sm = _cpu(k), _cpu(v), _cpu(slot_mapping_)
+    ksc, vsc = _scales(k_block_scales), _scales(v_block_scales)
+    assert k_blocks.is_contiguous() and v_blocks.is_contiguous()
+    T, Hkv, D = k.shape
+    return lib().oracle_reshape_and_cache_per_block(_p(k), _p(v), _p(k_blocks), _p(v_blocks),
+                                                    _p(sm), T, Hkv, D, block_size,
+                                                    k_blocks.shape[0], _DT[k.dtype],
+                                                    _DT[k_blocks.dtype], _p(ksc), _p(vsc))
+
+
 def _scales(x):
     return None if x is None else _cpu(x).to(torch.float32).contiguous()
 
@@ -204,11 +222,13 @@ def gather_kv(k_blocks, v_blocks, cu_seq_lens, block_tables, seq_starts=None):
 def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions, block_tables,
                      scale, causal=True, sliding_window=0, out_dtype=torch.float32,
                      want_lse=False, num_kv_heads=None, out=None, sinks=None, k_scale=1.0,
-                     v_scale=1.0, k_scales=None, v_scales=None):
+                     v_scale=1.0, k_scales=None, v_scales=None, k_block_scales=None,
+                     v_block_scales=None):
     """Two-pass attention of every (token, head).  Returns (status, out [T,H,D], lse [H,T]).
     sinks: optional [H] fp32 sink logits (a virtual zero-valued position per head);
     k_scale / v_scale: dequantisation scales of the pool (K = k_scale * pool);
-    k_scales / v_scales: one scale per kv head instead (K = k_scales[g] * pool)."""
+    k_scales / v_scales: one scale per kv head instead (K = k_scales[g] * pool);
+    k_block_scales / v_block_scales: [NB, Hkv], one per (pool block, kv head) instead."""
     q, kb, vb = _cpu(q), _cpu(k_blocks), _cpu(v_blocks)
     qsl, sl, pos, bt = _cpu(query_start_loc), _cpu(seq_lens), _cpu(positions), _cpu(block_tables)
     T, H, D = q.shape
@@ -222,7 +242,10 @@ def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions
     args = (_p(q), _p(kb), _p(vb), _p(out), _p(lse), _p(qsl), _p(sl), _p(pos), _p(bt),
             qsl.numel() - 1, T, H, Hkv, D, bs, NB, bt.shape[1], _DT[q.dtype], _DT[kb.dtype],
             _DT[out.dtype], float(scale), int(bool(causal)), int(sliding_window), _p(sk))
-    if k_scales is not None or v_scales is not None:
+    if k_block_scales is not None or v_block_scales is not None:
+        ksc, vsc = _scales(k_block_scales), _scales(v_block_scales)
+        st = lib().oracle_varlen_attention_per_block(*args, _p(ksc), _p(vsc))
+    elif k_scales is not None or v_scales is not None:
         ksc, vsc = _scales(k_scales), _scales(v_scales)
         st = lib().oracle_varlen_attention_per_head(*args, _p(ksc), _p(vsc))
     else:
@@ -232,7 +255,7 @@ def varlen_attention(q, k_blocks, v_blocks, query_start_loc, seq_lens, positions
 
 def splitkv_partials(q, k_blocks, v_blocks, seq_lens, block_tables, scale, partition_size,
                      max_parts, sliding_window=0, k_scale=1.0, v_scale=1.0, k_scales=None,
-                     v_scales=None):
+                     v_scales=None, k_block_scales=None, v_block_scales=None):
     """Phase 1 of split-KV decode: (status, max_logits, exp_sums, tmp_out).  k_scale / v_scale:
     dequantisation scales of the pool (K = k_scale * pool); k_scales / v_scales: one per kv
     head instead."""
@@ -245,7 +268,10 @@ def splitkv_partials(q, k_blocks, v_blocks, seq_lens, block_tables, scale, parti
     args = (_p(q), _p(kb), _p(vb), _p(ml), _p(es), _p(to), _p(sl), _p(bt), S, H, Hkv, D, bs, NB,
             bt.shape[1], partition_size, max_parts, _DT[q.dtype], _DT[kb.dtype], float(scale),
             int(sliding_window))
-    if k_scales is not None or v_scales is not None:
+    if k_block_scales is not None or v_block_scales is not None:
+        ksc, vsc = _scales(k_block_scales), _scales(v_block_scales)
+        st = lib().oracle_splitkv_partials_per_block(*args, _p(ksc), _p(vsc))
+    elif k_scales is not None or v_scales is not None:
         ksc, vsc = _scales(k_scales), _scales(v_scales)  # kept alive across the call
         st = lib().oracle_splitkv_partials_per_head(*args, _p(ksc), _p(vsc))
     else:

@@ -43,7 +43,8 @@
 enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_ESHAPE = 2, ORC_EUNSUPPORTED = 3 };
 /* Element types the pages use for q / K / V / out ([MLA] LoadF/StoreF), and fp8 (e4m3) K/V
  * pools ([V2] kv_cache_dtype "fp8" with k_scale / v_scale; [TL] "Going further": fp8 KV, with
- * scales per head or per block -- the *_per_head functions take one scale per kv head). */
+ * scales per head or per block -- the *_per_head functions take one scale per kv head, the
+ * *_per_block ones one per (pool block, kv head)). */
 enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_FP8 = 2 };
 
 static int g_mutant = 0;
@@ -229,6 +230,29 @@ static float head_scale(const float* s, int32_t g, int32_t num_kv_heads, float s
   if (!s) return scalar;
   return MUTANT(75) ? s[0] : s[g % num_kv_heads];
 }
+/* Per-block scales ([num_blocks, num_kv_heads], NULL: none): every factor of every block a
+ * sequence reads -- the first ceil(seq_len / b) entries of its table row, of the sequences
+ * with query tokens when qsl is given -- must be finite and > 0.  Called after the tables
+ * themselves were checked. */
+static int block_scales_ok(const float* kbs, const float* vbs, const int32_t* qsl,
+                           const int32_t* seq_lens, const int32_t* block_tables,
+                           int32_t num_seqs, int32_t num_kv_heads, int32_t block_size,
+                           int32_t max_blocks) {
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    if (qsl && qsl[s + 1] <= qsl[s]) continue;
+    const int64_t need = ((int64_t)seq_lens[s] + block_size - 1) / block_size;
+    for (int64_t i = 0; i < need; ++i) {
+      const int64_t id = block_tables[(int64_t)s * max_blocks + i];
+      for (int32_t g = 0; g < num_kv_heads; ++g) {
+        if (kbs && !(kbs[id * num_kv_heads + g] > 0.f && kbs[id * num_kv_heads + g] <= FLT_MAX))
+          return 0;
+        if (vbs && !(vbs[id * num_kv_heads + g] > 0.f && vbs[id * num_kv_heads + g] <= FLT_MAX))
+          return 0;
+      }
+    }
+  }
+  return 1;
+}
 
 static int scatter_convert(const void* k, const void* v, void* k_blocks, void* v_blocks,
                            const int32_t* slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
@@ -266,6 +290,43 @@ int oracle_reshape_and_cache_ex(const void* k, const void* v, void* k_blocks, vo
   return scatter_convert(k, v, k_blocks, v_blocks, slot_mapping, num_tokens, num_kv_heads,
                          head_dim, block_size, num_blocks, src_dtype, kv_dtype, NULL, NULL,
                          k_scale, v_scale);
+}
+
+/* Scatter with one scale per (pool block, kv head): head g of a new row written to slot s is
+ * stored as x / k_bscales[(s / b) * Hkv + g] (x / v_bscales[...]); NULL arrays: 1.  A factor
+ * of a block written to that is not finite and positive is EINVAL, before any write. */
+int oracle_reshape_and_cache_per_block(const void* k, const void* v, void* k_blocks,
+                                       void* v_blocks, const int32_t* slot_mapping,
+                                       int64_t num_tokens, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                       int32_t src_dtype, int32_t kv_dtype,
+                                       const float* k_bscales, const float* v_bscales) {
+  if (!k || !v || !k_blocks || !v_blocks || !slot_mapping) return ORC_EINVAL;
+  if (!dtype_ok(src_dtype) || !pool_dtype_ok(kv_dtype)) return ORC_EUNSUPPORTED;
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return ORC_ESHAPE;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= num_blocks * block_size) return ORC_EINVAL;
+    const int64_t blk = slot / block_size;
+    for (int32_t g = 0; g < num_kv_heads; ++g) {
+      const float a = k_bscales ? k_bscales[blk * num_kv_heads + g] : 1.f;
+      const float b = v_bscales ? v_bscales[blk * num_kv_heads + g] : 1.f;
+      if (!(a > 0.f && a <= FLT_MAX) || !(b > 0.f && b <= FLT_MAX)) return ORC_EINVAL;
+    }
+  }
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    const int64_t blk = slot / block_size;
+    for (int64_t i = 0; i < row; ++i) {
+      const int32_t g = (int32_t)(i / head_dim);
+      const float ks = k_bscales ? k_bscales[blk * num_kv_heads + g] : 1.f;
+      const float vs = v_bscales ? v_bscales[blk * num_kv_heads + g] : 1.f;
+      store_elem(k_blocks, kv_dtype, slot * row + i, load_elem(k, src_dtype, t * row + i) / ks);
+      store_elem(v_blocks, kv_dtype, slot * row + i, load_elem(v, src_dtype, t * row + i) / vs);
+    }
+  }
+  return ORC_OK;
 }
 
 /* The same with one scale per kv head: head g of a new row is stored as x / k_scales[g]
@@ -334,8 +395,15 @@ static float attend_two_pass(const void* q, int64_t q_off, int q_dtype, const vo
                              int32_t num_kv_heads, int32_t head_dim, int32_t kv_head,
                              float scale, float* logits, float* acc, void* out,
                              int64_t out_off, int out_dtype, float* m_out, float* l_out,
-                             float sink, float k_scale, float v_scale) {
+                             float sink, float k_scale, float v_scale, const float* k_bscales,
+                             const float* v_bscales) {
   const int64_t n = end > start ? end - start : 0;
+  /* Per-block scales ([TL] "Going further": fp8 caches with scales per head or per block):
+   * position j is dequantised with the factor of (its block, this kv head) instead of the
+   * scalar; NULL arrays keep the scalar. */
+#define KV_FACTOR(arr, scalar, j) \
+  ((arr) ? (arr)[(int64_t)table_row[(j) / block_size] * num_kv_heads + (MUTANT(76) ? 0 : kv_head)] \
+         : (scalar))
   /* An attention sink ([MPA] ForwardWithSinks) is one more, virtual, position whose score is
    * the sink logit and whose value is zero: it enters the max and the exp-sum, never the
    * weighted sum.  sink = -inf means none (and then changes nothing). */
@@ -348,10 +416,11 @@ static float attend_two_pass(const void* q, int64_t q_off, int q_dtype, const vo
     int64_t j = start + i;
     int64_t k_off = pool_row_offset(table_row, j, block_size, num_kv_heads, head_dim, kv_head);
     float dot = 0.0f;
+    const float kf = KV_FACTOR(k_bscales, k_scale, j);
     for (int32_t d = 0; d < head_dim; ++d)
       dot += load_elem(q, q_dtype, q_off + d) *
              (MUTANT(72) ? load_elem(k_blocks, kv_dtype, k_off + d)
-                         : load_elem(k_blocks, kv_dtype, k_off + d) * k_scale);
+                         : load_elem(k_blocks, kv_dtype, k_off + d) * kf);
     float s = MUTANT(30) ? dot : dot * scale;
     logits[i] = s;
     if (s > m) m = s;
@@ -372,10 +441,12 @@ static float attend_two_pass(const void* q, int64_t q_off, int q_dtype, const vo
     int64_t v_off = pool_row_offset(table_row, j, block_size, num_kv_heads, head_dim, kv_head);
     const void* vsrc = MUTANT(8) ? k_blocks : v_blocks; /* s08: V read from the K pool */
     float p = logits[i];
+    const float vf = KV_FACTOR(v_bscales, v_scale, j);
     for (int32_t d = 0; d < head_dim; ++d)
       acc[d] += p * (MUTANT(73) ? load_elem(vsrc, kv_dtype, v_off + d)
-                                : load_elem(vsrc, kv_dtype, v_off + d) * v_scale);
+                                : load_elem(vsrc, kv_dtype, v_off + d) * vf);
   }
+#undef KV_FACTOR
 
   /* o = acc * (1/l); an empty range writes zeros ([MPA] "Empty context: write
    * zeros"; [MLA] inv = l > 0 ? 1/l : 0; [TL] 2.4 multiply by 1/l). */
@@ -444,7 +515,7 @@ static int varlen_core(const void* q, const void* k_blocks, const void* v_blocks
                        int32_t max_blocks, int32_t q_dtype, int32_t kv_dtype, int32_t out_dtype,
                        float scale, int32_t causal, int32_t sliding_window, const float* sinks,
                        const float* k_scales, const float* v_scales, float k_scale,
-                       float v_scale) {
+                       float v_scale, const float* k_bscales, const float* v_bscales) {
   if (num_kv_heads > 0 &&
       (!head_scales_ok(k_scales, num_kv_heads) || !head_scales_ok(v_scales, num_kv_heads)))
     return ORC_EINVAL;
@@ -453,6 +524,9 @@ static int varlen_core(const void* q, const void* k_blocks, const void* v_blocks
                            head_dim, block_size, num_blocks, max_blocks, q_dtype, kv_dtype);
   if (st != ORC_OK) return st;
   if (!dtype_ok(out_dtype)) return ORC_EUNSUPPORTED;
+  if (!block_scales_ok(k_bscales, v_bscales, query_start_loc, seq_lens, block_tables, num_seqs,
+                       num_kv_heads, block_size, max_blocks))
+    return ORC_EINVAL;
 
   /* token -> sequence, and the longest context (for the per-thread scratch). */
   int32_t* tok_seq = (int32_t*)malloc(sizeof(int32_t) * (size_t)(num_tokens > 0 ? num_tokens : 1));
@@ -487,7 +561,8 @@ static int varlen_core(const void* q, const void* k_blocks, const void* v_blocks
                                     (t * num_heads + h) * (int64_t)head_dim, out_dtype, NULL, NULL,
                                     sinks ? sinks[h] : -INFINITY,
                                     head_scale(k_scales, gs, num_kv_heads, k_scale),
-                                    head_scale(v_scales, gs, num_kv_heads, v_scale));
+                                    head_scale(v_scales, gs, num_kv_heads, v_scale), k_bscales,
+                                    v_bscales);
       if (lse) lse[(int64_t)h * num_tokens + t] = l_lse;
     }
     free(logits);
@@ -509,7 +584,7 @@ int oracle_varlen_attention_ex(const void* q, const void* k_blocks, const void* 
   return varlen_core(q, k_blocks, v_blocks, out, lse, query_start_loc, seq_lens, positions,
                      block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
                      block_size, num_blocks, max_blocks, q_dtype, kv_dtype, out_dtype, scale,
-                     causal, sliding_window, sinks, NULL, NULL, k_scale, v_scale);
+                     causal, sliding_window, sinks, NULL, NULL, k_scale, v_scale, NULL, NULL);
 }
 
 /* One dequantisation scale per kv head: query head h (kv head g = h / G) attends over
@@ -528,7 +603,27 @@ int oracle_varlen_attention_per_head(const void* q, const void* k_blocks, const 
   return varlen_core(q, k_blocks, v_blocks, out, lse, query_start_loc, seq_lens, positions,
                      block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
                      block_size, num_blocks, max_blocks, q_dtype, kv_dtype, out_dtype, scale,
-                     causal, sliding_window, sinks, k_scales, v_scales, 1.f, 1.f);
+                     causal, sliding_window, sinks, k_scales, v_scales, 1.f, 1.f, NULL, NULL);
+}
+
+/* One dequantisation scale per (pool block, kv head) ([TL] "Going further": scales per
+ * block): position j of a sequence attends over K = k_bscales[id * Hkv + g] * pool and
+ * V = v_bscales[id * Hkv + g] * pool, id = its block, g its kv head (NULL arrays: 1).  A
+ * factor of a block some sequence reads that is not finite and positive is EINVAL. */
+int oracle_varlen_attention_per_block(const void* q, const void* k_blocks, const void* v_blocks,
+                                      void* out, float* lse, const int32_t* query_start_loc,
+                                      const int32_t* seq_lens, const int32_t* positions,
+                                      const int32_t* block_tables, int32_t num_seqs,
+                                      int64_t num_tokens, int32_t num_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                      int64_t num_blocks, int32_t max_blocks, int32_t q_dtype,
+                                      int32_t kv_dtype, int32_t out_dtype, float scale,
+                                      int32_t causal, int32_t sliding_window, const float* sinks,
+                                      const float* k_bscales, const float* v_bscales) {
+  return varlen_core(q, k_blocks, v_blocks, out, lse, query_start_loc, seq_lens, positions,
+                     block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, max_blocks, q_dtype, kv_dtype, out_dtype, scale,
+                     causal, sliding_window, sinks, NULL, NULL, 1.f, 1.f, k_bscales, v_bscales);
 }
 
 int oracle_varlen_attention(const void* q, const void* k_blocks, const void* v_blocks,
@@ -565,7 +660,7 @@ static int splitkv_core(const void* q, const void* k_blocks, const void* v_block
                         int32_t partition_size, int32_t max_parts, int32_t q_dtype,
                         int32_t kv_dtype, float scale, int32_t sliding_window,
                         const float* k_scales, const float* v_scales, float k_scale,
-                        float v_scale) {
+                        float v_scale, const float* k_bscales, const float* v_bscales) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0 || partition_size <= 0 || max_parts <= 0)
     return ORC_ESHAPE;
@@ -588,6 +683,9 @@ static int splitkv_core(const void* q, const void* k_blocks, const void* v_block
     }
     if (n > max_ctx) max_ctx = n;
   }
+  if (!block_scales_ok(k_bscales, v_bscales, NULL, seq_lens, block_tables, num_seqs, num_kv_heads,
+                       block_size, max_blocks))
+    return ORC_EINVAL;
   const int32_t group = num_heads / num_kv_heads;
   const int64_t work = (int64_t)num_seqs * num_heads * max_parts;
 #pragma omp parallel
@@ -611,7 +709,8 @@ static int splitkv_core(const void* q, const void* k_blocks, const void* v_block
                       num_kv_heads, head_dim, h / group, scale, logits, acc, tmp_out,
                       idx * head_dim, ORC_F32, &m, &l, -INFINITY,
                       head_scale(k_scales, h / group, num_kv_heads, k_scale),
-                      head_scale(v_scales, h / group, num_kv_heads, v_scale));
+                      head_scale(v_scales, h / group, num_kv_heads, v_scale), k_bscales,
+                      v_bscales);
       max_logits[idx] = m;
       exp_sums[idx] = l;
     }
@@ -632,7 +731,7 @@ int oracle_splitkv_partials_ex(const void* q, const void* k_blocks, const void* 
   return splitkv_core(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
                       block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                       num_blocks, max_blocks, partition_size, max_parts, q_dtype, kv_dtype, scale,
-                      sliding_window, NULL, NULL, k_scale, v_scale);
+                      sliding_window, NULL, NULL, k_scale, v_scale, NULL, NULL);
 }
 
 /* Split-KV partials with one scale per kv head (NULL arrays: 1; not finite and positive:
@@ -649,7 +748,24 @@ int oracle_splitkv_partials_per_head(const void* q, const void* k_blocks, const 
   return splitkv_core(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
                       block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                       num_blocks, max_blocks, partition_size, max_parts, q_dtype, kv_dtype, scale,
-                      sliding_window, k_scales, v_scales, 1.f, 1.f);
+                      sliding_window, k_scales, v_scales, 1.f, 1.f, NULL, NULL);
+}
+
+/* Split-KV partials with one scale per (pool block, kv head), as
+ * oracle_varlen_attention_per_block (NULL arrays: 1). */
+int oracle_splitkv_partials_per_block(const void* q, const void* k_blocks, const void* v_blocks,
+                                      float* max_logits, float* exp_sums, float* tmp_out,
+                                      const int32_t* seq_lens, const int32_t* block_tables,
+                                      int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                      int32_t max_blocks, int32_t partition_size,
+                                      int32_t max_parts, int32_t q_dtype, int32_t kv_dtype,
+                                      float scale, int32_t sliding_window,
+                                      const float* k_bscales, const float* v_bscales) {
+  return splitkv_core(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
+                      block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, max_blocks, partition_size, max_parts, q_dtype, kv_dtype, scale,
+                      sliding_window, NULL, NULL, 1.f, 1.f, k_bscales, v_bscales);
 }
 
 int oracle_splitkv_partials(const void* q, const void* k_blocks, const void* v_blocks,

@@ -813,7 +813,97 @@ def pin_per_head_attention():
         assert st == oracle.EINVAL
 
 
+def _block_scales(NB, Hkv, seed, lo=0.2, hi=2.0):
+    g = torch.Generator().manual_seed(seed)
+    return lo + (hi - lo) * torch.rand((NB, Hkv), generator=g)
+
+
+def pin_per_block_scatter():
+    # head g of a new row written to slot s holds x / scales[s // b, g]: torch's e4m3 code of
+    # the IEEE quotient (clamped to +-448) in an fp8 pool, the quotient itself in an fp32 pool
+    g = torch.Generator().manual_seed(77)
+    T, Hkv, D, b, NB = 20, 3, 16, 16, 4
+    k = (torch.randn((T, Hkv, D), generator=g) * 3).to(torch.bfloat16)
+    v = (torch.randn((T, Hkv, D), generator=g) * 50).to(torch.bfloat16)
+    ks, vs = _block_scales(NB, Hkv, 78, 0.05, 2.0), _block_scales(NB, Hkv, 79, 0.1, 1.5)
+    slots = torch.randperm(NB * b, generator=g)[:T].to(torch.int32)
+    for dt in (torch.float8_e4m3fn, torch.float32):
+        kb = torch.zeros((NB, b, Hkv, D), dtype=dt)
+        vb = torch.zeros_like(kb)
+        assert oracle.reshape_and_cache_per_block(k, v, kb, vb, slots, b, ks, vs) == oracle.OK
+        for t in range(T):
+            sl = int(slots[t])
+            wk = k[t].float() / ks[sl // b][:, None]
+            wv = v[t].float() / vs[sl // b][:, None]
+            if dt == torch.float8_e4m3fn:
+                wk = torch.clamp(wk, -448, 448).to(dt).view(torch.uint8)
+                wv = torch.clamp(wv, -448, 448).to(dt).view(torch.uint8)
+                gk, gv = kb[sl // b, sl % b].view(torch.uint8), vb[sl // b, sl % b].view(torch.uint8)
+            else:
+                gk, gv = kb[sl // b, sl % b], vb[sl // b, sl % b]
+            assert torch.equal(gk, wk) and torch.equal(gv, wv)
+    # a bad factor of a block that is written to: EINVAL, nothing written; of a block no token
+    # writes to: ignored
+    written = {int(x) // b for x in slots}
+    unwritten = [i for i in range(NB) if i not in written]
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        ks2 = ks.clone()
+        ks2[int(slots[0]) // b, 1] = bad
+        kb = torch.zeros((NB, b, Hkv, D), dtype=torch.float32)
+        vb = torch.zeros_like(kb)
+        assert oracle.reshape_and_cache_per_block(k, v, kb, vb, slots, b, ks2, vs) == oracle.EINVAL
+        assert not kb.any() and not vb.any()
+        if unwritten:
+            ks3 = ks.clone()
+            ks3[unwritten[0], 0] = bad
+            assert oracle.reshape_and_cache_per_block(k, v, kb, vb, slots, b, ks3, vs) == oracle.OK
+
+
+def pin_per_block_attention():
+    # per (pool block, kv head) scales on an fp8 pool equal, bit for bit, the unscaled attention
+    # over the fp32 pool holding scales[block, g] * value(code) (one fp32 product), where block
+    # is the physical id the table names (the tables are permutations of the pool); GQA 3; the
+    # same for the split-KV partials
+    H, Hkv, D, lens, qsl, pos, q, kb8, vb8, table = _fp8_case(seed=80)
+    NB = kb8.shape[0]
+    ks, vs = _block_scales(NB, Hkv, 81), _block_scales(NB, Hkv, 82)
+    kbf = kb8.float() * ks.view(NB, 1, Hkv, 1)
+    vbf = vb8.float() * vs.view(NB, 1, Hkv, 1)
+    meta = dict(query_start_loc=_t(qsl), seq_lens=_t(lens), positions=_t(pos),
+                block_tables=table, scale=1.0 / math.sqrt(D), want_lse=True)
+    for window in (0, 20):
+        st, o1, l1 = oracle.varlen_attention(q, kb8, vb8, sliding_window=window,
+                                             k_block_scales=ks, v_block_scales=vs, **meta)
+        st2, o2, l2 = oracle.varlen_attention(q, kbf, vbf, sliding_window=window, **meta)
+        assert st == oracle.OK and st2 == oracle.OK
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    qd = torch.stack([q[qsl[s + 1] - 1] for s in range(len(lens))])
+    a = oracle.splitkv_partials(qd, kb8, vb8, _t(lens), table, 1.0 / math.sqrt(D), 16, 8,
+                                k_block_scales=ks, v_block_scales=vs)
+    b = oracle.splitkv_partials(qd, kbf, vbf, _t(lens), table, 1.0 / math.sqrt(D), 16, 8)
+    assert a[0] == oracle.OK and b[0] == oracle.OK
+    for x, y in zip(a[1:], b[1:]):
+        assert torch.equal(x, y)
+    # a bad factor of a block some sequence reads: EINVAL; of a block no table names: ignored
+    used = {int(table[s, j]) for s, n in enumerate(lens) for j in range((n + 15) // 16)}
+    unused = [i for i in range(NB) if i not in used]
+    for bad in (0.0, float("nan")):
+        vs2 = vs.clone()
+        vs2[int(table[1, 0]), 1] = bad
+        st, _, _ = oracle.varlen_attention(q, kb8, vb8, k_block_scales=ks, v_block_scales=vs2,
+                                           **meta)
+        assert st == oracle.EINVAL
+        if unused:
+            vs3 = vs.clone()
+            vs3[unused[0], 0] = bad
+            st, _, _ = oracle.varlen_attention(q, kb8, vb8, k_block_scales=ks,
+                                               v_block_scales=vs3, **meta)
+            assert st == oracle.OK
+
+
 ALL_PINS = {
+    "per_block_scatter": pin_per_block_scatter,
+    "per_block_attention": pin_per_block_attention,
     "per_head_scatter": pin_per_head_scatter,
     "per_head_attention": pin_per_head_attention,
     "fp8_codec": pin_fp8_codec,

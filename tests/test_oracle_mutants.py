@@ -8,8 +8,9 @@ block ids trusted) and further plausible slips in the scatter, gather, score,
 split-KV reduction and merge arithmetic, and in the attention-sink term (s60 the sink
 left out of the exp-sum, s61 its term taken as 1 instead of e^(sink - m)) and the fp8 pools
 (s70 a wrong exponent bias, s71 truncation instead of rounding, s72 / s73 a dequantisation
-scale ignored), and the per kv head scales (s74 the query head's index taken for the kv
-head's, s75 the first head's scale used for every head).
+scale ignored), the per kv head scales (s74 the query head's index taken for the kv
+head's, s75 the first head's scale used for every head) and the per-block scales (s76 the
+block's factor of kv head 0 used for every head).
 """
 import pytest
 
@@ -46,6 +47,7 @@ KILLERS = {
     73: ["fp8_attention_brute_force", "dequant_scales", "splitkv_fp8_scaled"],
     74: ["per_head_attention"],
     75: ["per_head_scatter", "per_head_attention"],
+    76: ["per_block_attention"],
 }
 
 
