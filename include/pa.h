@@ -9,11 +9,11 @@
  * Stream order.  A call observes everything enqueued before it on `stream` and everything
  * after it observes the call.  The varlen calls' planning kernel is launched with
  * programmatic dependent launch and reads the metadata arrays (query_start_loc, seq_lens,
- * positions, block_tables, per-head scales) before the kernel ahead of it on the stream
- * has finished; it waits for that kernel before writing anything.  So the metadata must
- * not be written by a kernel of the caller's that itself releases its programmatic
- * dependents (griddepcontrol.launch_dependents) before those writes.  Copies, ordinary
- * kernels and this library's own kernels ahead of the call are all safe.
+ * positions, block_tables, per-head scales, per-block factors) before the kernel ahead of it
+ * on the stream has finished; it waits for that kernel before writing anything.  So the
+ * metadata must not be written by a kernel of the caller's that itself releases its
+ * programmatic dependents (griddepcontrol.launch_dependents) before those writes.  Copies,
+ * ordinary kernels and this library's own kernels ahead of the call are all safe.
  *
  * Layouts (row-major, as the TensorSharp "ManagedPagedAttention.cs" class summary
  * states them):
@@ -162,6 +162,25 @@ pa_status pa_reshape_and_cache_per_head(const void* k, const void* v, void* k_bl
                                         cudaStream_t stream);
 
 /*
+ * pa_reshape_and_cache_per_block -- pa_reshape_and_cache_ex with one dequantisation factor per
+ * (pool block, kv head) (tinyllm "Going further": fp8 KV caches with scales per block): head g
+ * of a new row written to slot s is stored as x / k_block_scales[(s / block_size) *
+ * num_kv_heads + g] (x / v_block_scales[...]).  k_block_scales, v_block_scales: DEVICE arrays
+ * [num_blocks, num_kv_heads] of floats owned by the caller, both required (NULL: PA_EINVAL).
+ * A factor of a block some row is written to that is not finite and positive is recorded as
+ * PA_EINVAL in the device status and nothing is written; other errors as
+ * pa_reshape_and_cache_ex.  The caller chooses the factors (for example from a block's
+ * largest magnitude when it is allocated); the library does not change them.
+ */
+pa_status pa_reshape_and_cache_per_block(const void* k, const void* v, void* k_blocks,
+                                         void* v_blocks, const int32_t* slot_mapping,
+                                         int64_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t block_size,
+                                         int64_t num_blocks, pa_dtype src_dtype,
+                                         pa_dtype kv_dtype, const float* k_block_scales,
+                                         const float* v_block_scales, cudaStream_t stream);
+
+/*
  * pa_varlen_forward_workspace_size -- bytes of device workspace pa_varlen_forward needs
  * for these sizes (the per-call plan of work items and split-KV partial states).
  */
@@ -269,6 +288,36 @@ pa_status pa_varlen_forward_per_head(const void* q, const void* k_blocks, const 
                                      cudaStream_t stream);
 
 /*
+ * pa_varlen_forward_per_block -- pa_varlen_forward_ex over e4m3 pools with one dequantisation
+ * factor per (pool block, kv head) (tinyllm "Going further": scales per block): position j of
+ * a sequence, in pool block id = block_tables[s][j / block_size], is read by query head h (kv
+ * head g = h / (num_heads / num_kv_heads)) as K = k_block_scales[id * num_kv_heads + g] *
+ * k_blocks[...] and V = v_block_scales[...] * v_blocks[...].  k_block_scales, v_block_scales:
+ * DEVICE arrays [num_blocks, num_kv_heads] of floats owned by the caller, both required (NULL:
+ * PA_EINVAL).  The factors of every block a sequence with query tokens reads (the first
+ * ceil(seq_lens[s] / block_size) entries of its table row) must be finite and positive, else
+ * PA_EINVAL is recorded in the device status and out / lse are left untouched.  kv_dtype must
+ * be PA_FP8_E4M3 and the call must qualify for the warp-MMA path (q bf16, head_dim 128,
+ * block_size 16, 16-byte aligned tensors), else PA_EUNSUPPORTED before anything is enqueued.
+ * Every sequence, prefill chunks included, runs on the warp-MMA kernel.  The K factor
+ * multiplies each block's scores exactly; the V factor multiplies the block's softmax weights
+ * before they are rounded to f16 for P V.  Other arguments and errors as pa_varlen_forward_ex.
+ */
+pa_status pa_varlen_forward_per_block(const void* q, const void* k_blocks, const void* v_blocks,
+                                      void* out, const int32_t* query_start_loc,
+                                      const int32_t* seq_lens, const int32_t* positions,
+                                      const int32_t* block_tables, int32_t num_seqs,
+                                      int64_t num_tokens, int32_t num_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                      int64_t num_blocks, int32_t max_blocks_per_seq,
+                                      pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
+                                      int32_t causal, int32_t sliding_window, const float* sinks,
+                                      float* lse, const float* k_block_scales,
+                                      const float* v_block_scales, uint32_t flags,
+                                      void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream);
+
+/*
  * pa_cache_and_attend -- one decode / prefill step over the cache: pa_slot_mapping_and_cache
  * of the new tokens' rows (k_new, v_new [num_tokens, num_kv_heads, head_dim] of kv_dtype;
  * slot_mapping [num_tokens] written) followed by pa_varlen_forward of q over the updated pools,
@@ -371,6 +420,21 @@ pa_status pa_decode_splitkv_partials_per_head(
     int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int32_t partition_size,
     int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
     int32_t sliding_window, const float* k_scales, const float* v_scales, cudaStream_t stream);
+
+/*
+ * pa_decode_splitkv_partials_per_block -- pa_decode_splitkv_partials_ex with one factor per
+ * (pool block, kv head), as pa_varlen_forward_per_block (both arrays required; factors of the
+ * blocks the sequences read validated on the device: PA_EINVAL recorded, partials untouched;
+ * e4m3 pools on the warp-MMA path only, else PA_EUNSUPPORTED).
+ */
+pa_status pa_decode_splitkv_partials_per_block(
+    const void* q, const void* k_blocks, const void* v_blocks, float* max_logits,
+    float* exp_sums, float* tmp_out, const int32_t* seq_lens, const int32_t* block_tables,
+    int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int32_t partition_size,
+    int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
+    int32_t sliding_window, const float* k_block_scales, const float* v_block_scales,
+    cudaStream_t stream);
 
 /*
  * pa_decode_splitkv_reduce -- phase 2 ("Phase 2: Cross-partition reduction").  For each

@@ -42,6 +42,8 @@ _SIGS = {
                                  ctypes.c_int, ctypes.c_int, _f32, _f32, _vp], ctypes.c_int),
     "pa_reshape_and_cache_per_head": ([_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64,
                                        ctypes.c_int, ctypes.c_int, _vp, _vp, _vp], ctypes.c_int),
+    "pa_reshape_and_cache_per_block": ([_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64,
+                                        ctypes.c_int, ctypes.c_int, _vp, _vp, _vp], ctypes.c_int),
     "pa_varlen_forward_workspace_size": ([_i32, _i64, _i32, _i32, _i32, _i32, _i32], _sz),
     "pa_varlen_forward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
                            _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32, _i32, _i32, _vp,
@@ -54,6 +56,10 @@ _SIGS = {
                                     _i32, _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int,
                                     _f32, _i32, _i32, _vp, _vp, _vp, _vp, ctypes.c_uint32, _vp,
                                     _sz, _vp], ctypes.c_int),
+    "pa_varlen_forward_per_block": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32,
+                                     _i32, _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int,
+                                     _f32, _i32, _i32, _vp, _vp, _vp, _vp, ctypes.c_uint32, _vp,
+                                     _sz, _vp], ctypes.c_int),
     "pa_cache_and_attend": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32,
                              _i32, _i32, _i32, _i64, _i32, ctypes.c_int, ctypes.c_int, _f32,
                              _i32, _i32, _vp, _vp, _sz, _vp], ctypes.c_int),
@@ -70,6 +76,10 @@ _SIGS = {
                                              _i32, _i32, _i32, _i64, _i32, _i32, _i32,
                                              ctypes.c_int, ctypes.c_int, _f32, _i32, _vp, _vp,
                                              _vp], ctypes.c_int),
+    "pa_decode_splitkv_partials_per_block": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                              _i32, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
+                                              ctypes.c_int, ctypes.c_int, _f32, _i32, _vp, _vp,
+                                              _vp], ctypes.c_int),
     "pa_decode_splitkv_reduce": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                   ctypes.c_int, _vp], ctypes.c_int),
     "pa_decode_splitkv": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -175,12 +185,14 @@ def pa_slot_mapping_and_cache(k, v, k_blocks, v_blocks, query_start_loc, positio
 
 
 def pa_reshape_and_cache(k, v, k_blocks, v_blocks, slot_mapping, stream=None, k_scale=None,
-                         v_scale=None, k_scales=None, v_scales=None):
+                         v_scale=None, k_scales=None, v_scales=None, k_block_scales=None,
+                         v_block_scales=None):
     """pa_reshape_and_cache (rows and pools of one dtype, a copy), or pa_reshape_and_cache_ex
     when the pools' dtype differs from the rows' or a scale is given (pool = rows / scale,
     rounded to the pool's dtype, e.g. torch.float8_e4m3fn), or
     pa_reshape_and_cache_per_head when k_scales / v_scales (device fp32 [num_kv_heads]) are
-    given."""
+    given, or pa_reshape_and_cache_per_block with k_block_scales / v_block_scales (device fp32
+    [num_blocks, num_kv_heads], both)."""
     _dev(k, v, k_blocks, v_blocks, slot_mapping)
     _i32t(slot_mapping)
     if k.shape != v.shape or k.dim() != 3 or k_blocks.shape != v_blocks.shape:
@@ -191,6 +203,15 @@ def pa_reshape_and_cache(k, v, k_blocks, v_blocks, slot_mapping, stream=None, k_
     NB, bs, Hkv2, D2 = k_blocks.shape
     if (Hkv, D) != (Hkv2, D2):
         raise ValueError("kv heads / head size differ between rows and pool")
+    if k_block_scales is not None or v_block_scales is not None:
+        _block_scales(NB, Hkv, k_block_scales, v_block_scales)
+        _check(_lib.pa_reshape_and_cache_per_block(_p(k), _p(v), _p(k_blocks), _p(v_blocks),
+                                                   _p(slot_mapping), T, Hkv, D, bs, NB,
+                                                   _DT[k.dtype], _DT[k_blocks.dtype],
+                                                   _p(k_block_scales), _p(v_block_scales),
+                                                   _stream(stream)),
+               "pa_reshape_and_cache_per_block")
+        return
     if k_scales is not None or v_scales is not None:
         _head_scales(Hkv, k_scales, v_scales)
         _check(_lib.pa_reshape_and_cache_per_head(_p(k), _p(v), _p(k_blocks), _p(v_blocks),
@@ -221,6 +242,15 @@ def _head_scales(Hkv, *arrays):
             raise ValueError("per-head scales must be contiguous fp32 [num_kv_heads] tensors")
 
 
+def _block_scales(NB, Hkv, ks, vs):
+    if ks is None or vs is None:
+        raise ValueError("per-block scales need both k_block_scales and v_block_scales")
+    for a in (ks, vs):
+        _dev(a)
+        if a.dtype != torch.float32 or a.shape != (NB, Hkv) or not a.is_contiguous():
+            raise ValueError("per-block scales must be contiguous fp32 [num_blocks, num_kv_heads]")
+
+
 def pa_varlen_forward_workspace_size(num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
                                      max_blocks_per_seq, block_size) -> int:
     return int(_lib.pa_varlen_forward_workspace_size(num_seqs, num_tokens, num_heads, num_kv_heads,
@@ -238,11 +268,14 @@ def workspace_for(q, k_blocks, query_start_loc, block_tables):
 def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
                       block_tables, scale, causal=True, sliding_window=0, workspace=None,
                       stream=None, sinks=None, lse=None, k_scale=1.0, v_scale=1.0,
-                      bitwise=False, k_scales=None, v_scales=None):
+                      bitwise=False, k_scales=None, v_scales=None, k_block_scales=None,
+                      v_block_scales=None):
     """pa_varlen_forward, or pa_varlen_forward_ex when sinks ([H] fp32 sink logits), lse
     (a [H, T] fp32 output), a dequantisation scale other than 1 or bitwise=True
     (PA_FLAG_BITWISE: decode and prefill rows give the same bits) is given, or
-    pa_varlen_forward_per_head with k_scales / v_scales (device fp32 [num_kv_heads])."""
+    pa_varlen_forward_per_head with k_scales / v_scales (device fp32 [num_kv_heads]), or
+    pa_varlen_forward_per_block with k_block_scales / v_block_scales (device fp32
+    [num_blocks, num_kv_heads], both; e4m3 pools)."""
     _dev(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions, block_tables, workspace,
          sinks, lse)
     _i32t(query_start_loc, seq_lens, positions, block_tables)
@@ -257,10 +290,13 @@ def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, pos
     if workspace is None:
         workspace = workspace_for(q, k_blocks, query_start_loc, block_tables)
     per_head = k_scales is not None or v_scales is not None
-    if per_head and (k_scale != 1.0 or v_scale != 1.0):
-        raise ValueError("give either per-pool or per-head scales")
+    per_block = k_block_scales is not None or v_block_scales is not None
+    if (per_head or per_block) and (k_scale != 1.0 or v_scale != 1.0):
+        raise ValueError("give either per-pool, per-head or per-block scales")
+    if per_head and per_block:
+        raise ValueError("give either per-head or per-block scales")
     if (sinks is None and lse is None and k_scale == 1.0 and v_scale == 1.0 and not bitwise
-            and not per_head):
+            and not per_head and not per_block):
         _check(_lib.pa_varlen_forward(_p(q), _p(k_blocks), _p(v_blocks), _p(out),
                                       _p(query_start_loc), _p(seq_lens), _p(positions),
                                       _p(block_tables), query_start_loc.numel() - 1, T, H, Hkv, D,
@@ -285,6 +321,11 @@ def pa_varlen_forward(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, pos
         _head_scales(Hkv, k_scales, v_scales)
         _check(_lib.pa_varlen_forward_per_head(*head, _p(k_scales), _p(v_scales), *tail),
                "pa_varlen_forward_per_head")
+        return out
+    if per_block:
+        _block_scales(NB, Hkv, k_block_scales, v_block_scales)
+        _check(_lib.pa_varlen_forward_per_block(*head, _p(k_block_scales), _p(v_block_scales),
+                                                *tail), "pa_varlen_forward_per_block")
         return out
     _check(_lib.pa_varlen_forward_ex(*head, float(k_scale), float(v_scale), *tail),
            "pa_varlen_forward_ex")
@@ -361,13 +402,23 @@ def _split_shapes(q, k_blocks, max_logits, tmp_out):
 def pa_decode_splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
                                block_tables, scale, partition_size=512, sliding_window=0,
                                stream=None, k_scale=1.0, v_scale=1.0, k_scales=None,
-                               v_scales=None):
+                               v_scales=None, k_block_scales=None, v_block_scales=None):
     """pa_decode_splitkv_partials, or pa_decode_splitkv_partials_ex when a dequantisation scale
     other than 1 is given, or pa_decode_splitkv_partials_per_head with k_scales / v_scales
-    (device fp32 [num_kv_heads])."""
+    (device fp32 [num_kv_heads]), or pa_decode_splitkv_partials_per_block with k_block_scales /
+    v_block_scales (device fp32 [num_blocks, num_kv_heads], both; e4m3 pools)."""
     _dev(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens, block_tables)
     _i32t(seq_lens, block_tables)
     S, H, D, NB, bs, Hkv, P = _split_shapes(q, k_blocks, max_logits, tmp_out)
+    if k_block_scales is not None or v_block_scales is not None:
+        _block_scales(NB, Hkv, k_block_scales, v_block_scales)
+        _check(_lib.pa_decode_splitkv_partials_per_block(
+            _p(q), _p(k_blocks), _p(v_blocks), _p(max_logits), _p(exp_sums), _p(tmp_out),
+            _p(seq_lens), _p(block_tables), S, H, Hkv, D, bs, NB, block_tables.shape[1],
+            partition_size, P, _DT[q.dtype], _DT[k_blocks.dtype], float(scale),
+            int(sliding_window), _p(k_block_scales), _p(v_block_scales), _stream(stream)),
+            "pa_decode_splitkv_partials_per_block")
+        return
     if k_scales is not None or v_scales is not None:
         _head_scales(Hkv, k_scales, v_scales)
         _check(_lib.pa_decode_splitkv_partials_per_head(

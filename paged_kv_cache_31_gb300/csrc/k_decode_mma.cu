@@ -70,10 +70,21 @@ struct Geom {
 
 template <int D, int NW, int NS, bool FP8>
 constexpr size_t smem_bytes() {
-  // ring | full barriers, one that no copy signals | merge m, l | fail flag, work unit ; the O
-  // merge area aliases the ring
+  // ring | full barriers, one that no copy signals | merge m, l | fail flag, work unit | the
+  // per-block K and V factors of each ring stage ; the O merge area aliases the ring
   return 1024 + (size_t)NW * NS * Geom<D, FP8>::kStageBytes + (NW * NS + 1) * 8 +
-         NW * 16 * 4 * 2 + 16;
+         NW * 16 * 4 * 2 + 16 + (size_t)NW * NS * 8;
+}
+
+// 4 bytes global -> shared without registers; the mbarrier's pending arrival count (set for
+// it at initialisation) drops once every earlier cp.async of this thread has landed
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -111,10 +122,17 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
   return (uint32_t)(half * (kBlk * 128) + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
-template <int D, int NW, int NS, bool SPLIT, bool FP8>
+// PB (e4m3 pools only): one K and one V factor per (pool block, kv head), p.m.k_bscales /
+// v_bscales [num_blocks, num_kv_heads].  The K factor multiplies the block's scores with the
+// softmax scale; the V factor multiplies the block's fp32 weights where they are rounded to
+// f16 for P V (the row sum keeps the unscaled weights).  Lane 0 copies both factors into the
+// stage's slot with cp.async when it issues the block's TMA copies, and the stage's barrier
+// (two arrivals) completes only when they have landed too.
+template <int D, int NW, int NS, bool SPLIT, bool FP8, bool PB = false>
 __global__ void __launch_bounds__(NW * 32, 2)
     k_mma16(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
             const Mma16Params p) {
+  static_assert(!PB || FP8, "per-block factors are for e4m3 pools");
   using G_ = Geom<D, FP8>;
   // query rows per tile: e4m3 varlen tiles are one group of 8 (one N of the swapped MMAs)
   constexpr int TR = (FP8 && !SPLIT) ? 8 : 16;
@@ -128,11 +146,12 @@ __global__ void __launch_bounds__(NW * 32, 2)
   float* mrg_m = reinterpret_cast<float*>(full + NW * NS + 1);
   float* mrg_l = mrg_m + NW * 16;
   int* fail = reinterpret_cast<int*>(mrg_l + NW * 16);
+  float2* s_bs = reinterpret_cast<float2*>(fail + 2);  // [NW * NS] (K, V) factors (PB)
   float* mrg_o = reinterpret_cast<float*>(ring);  // [NW][16][D + 4], used after the ring drains
   constexpr int kOStride = D + 4;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x <= NW * NS) mbar_init(&full[threadIdx.x], 1);  // the ring's and `never`
+  if (threadIdx.x <= NW * NS) mbar_init(&full[threadIdx.x], PB ? 2 : 1);  // the ring's, `never`
   if (threadIdx.x == 0) {
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
@@ -312,6 +331,12 @@ __global__ void __launch_bounds__(NW * 32, 2)
         const uint32_t slot = (ring_pos + x) % NS;
         uint64_t* bar = &full[warp * NS + slot];
         uint8_t* dst = ring + (size_t)(warp * NS + slot) * G_::kStageBytes;
+        if constexpr (PB) {
+          const int64_t f = (int64_t)id * m.num_kv_heads + kvh;
+          cp_async4(&s_bs[warp * NS + slot].x, p.m.k_bscales + f);
+          cp_async4(&s_bs[warp * NS + slot].y, p.m.v_bscales + f);
+          cp_async_arrive(bar);
+        }
         mbar_arrive_expect_tx(bar, G_::kStageBytes);
 #pragma unroll
         for (int h = 0; h < G_::kHalves; ++h) {  // fp8: one 128-byte box per tile, x = 0
@@ -377,8 +402,11 @@ __global__ void __launch_bounds__(NW * 32, 2)
       all_lo = max(all_lo, __shfl_xor_sync(kFull, all_lo, o));
       all_hi = min(all_hi, __shfl_xor_sync(kFull, all_hi, o));
     }
-    auto fp8_step = [&](auto groups, const uint8_t* kt, const uint8_t* vt, int key_base) {
+    auto fp8_step = [&](auto groups, const uint8_t* kt, const uint8_t* vt, int key_base,
+                        float2 fac) {
       constexpr int NR = decltype(groups)::value;
+      float sk = sl2;  // the block's score scale
+      if constexpr (PB) sk = sl2 * fac.x;
       const int c = lane & 3, g = lane >> 2;
       // S^T = K Q^T: A = key rows g and g + 8, bytes [32c, 32c + 32) (chunks 2c, 2c + 1); B =
       // the q fragments of group j, qa[kk][j] and qa[kk][j + 2]
@@ -416,14 +444,14 @@ __global__ void __launch_bounds__(NW * 32, 2)
       for (int j = 0; j < NR; ++j) {
         if (key_base >= all_lo && key_base + kBlk <= all_hi) {  // padding rows: unused values
 #pragma unroll
-          for (int i = 0; i < 4; ++i) sc[j][i] = (sc[j][i] + sc2[j][i]) * sl2;
+          for (int i = 0; i < 4; ++i) sc[j][i] = (sc[j][i] + sc2[j][i]) * sk;
         } else {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int key = key_base + g + 8 * (i >> 1);
             const int e = i & 1;
             const bool vis = key >= cst[j][e] && key < cen[j][e];
-            sc[j][i] = vis ? (sc[j][i] + sc2[j][i]) * sl2 : -INFINITY;
+            sc[j][i] = vis ? (sc[j][i] + sc2[j][i]) * sk : -INFINITY;
           }
         }
 #pragma unroll
@@ -461,8 +489,12 @@ __global__ void __launch_bounds__(NW * 32, 2)
       uint32_t pb[NR][2];
 #pragma unroll
       for (int j = 0; j < NR; ++j) {
-        pb[j][0] = movmatrix_trans(pack_f16x2(sc[j][0], sc[j][1]));
-        pb[j][1] = movmatrix_trans(pack_f16x2(sc[j][2], sc[j][3]));
+        auto vw = [&](float x) {  // the block's V factor on the weight (PB)
+          if constexpr (PB) return x * fac.y;
+          else return x;
+        };
+        pb[j][0] = movmatrix_trans(pack_f16x2(vw(sc[j][0]), vw(sc[j][1])));
+        pb[j][1] = movmatrix_trans(pack_f16x2(vw(sc[j][2]), vw(sc[j][3])));
       }
       // O^T += V^T P^T.  A = V^T: M-tile t = 2i + h, row g is dimension 16g + 4i + 2h and row
       // g + 8 dimension 16g + 4i + 2h + 1; its k columns are keys 2c, 2c + 1, 2c + 8, 2c + 9,
@@ -516,16 +548,18 @@ __global__ void __launch_bounds__(NW * 32, 2)
       }
       uint8_t* kt = ring + (size_t)(warp * NS + slot) * G_::kStageBytes;
       uint8_t* vt = kt + G_::kTileBytes;
+      float2 fac = make_float2(1.f, 1.f);
+      if constexpr (PB) fac = s_bs[warp * NS + slot];
       const int lb = blk_lo + first + x * NW;
       const int key_base = lb * kBlk;
 
       if constexpr (FP8 && TR == 8) {
-        fp8_step(IntTag<1>{}, kt, vt, key_base);
+        fp8_step(IntTag<1>{}, kt, vt, key_base, fac);
       } else if constexpr (FP8) {
         if (nr == 1)
-          fp8_step(IntTag<1>{}, kt, vt, key_base);
+          fp8_step(IntTag<1>{}, kt, vt, key_base, fac);
         else
-          fp8_step(IntTag<2>{}, kt, vt, key_base);
+          fp8_step(IntTag<2>{}, kt, vt, key_base, fac);
       } else {
         // rows of the sequence's last block past seq_len were never written: zero their V so
         // that 0-weight * garbage cannot turn into NaN
@@ -791,11 +825,11 @@ struct Shape {
   static constexpr int NS = FP8 ? (SPLIT ? 6 : 3) : 3;
 };
 
-template <int D, bool SPLIT, bool FP8 = false>
+template <int D, bool SPLIT, bool FP8 = false, bool PB = false>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const Mma16Params& p, int grid_x,
                    cudaStream_t stream) {
   constexpr int NW = Shape<D, SPLIT, FP8>::NW, NS = Shape<D, SPLIT, FP8>::NS;
-  auto kern = k_mma16<D, NW, NS, SPLIT, FP8>;
+  auto kern = k_mma16<D, NW, NS, SPLIT, FP8, PB>;
   constexpr size_t smem = smem_bytes<D, NW, NS, FP8>();
   static_assert((size_t)NW * 16 * (D + 4) * 4 <= (size_t)NW * NS * Geom<D, FP8>::kStageBytes,
                 "merge area must fit in the ring");
@@ -833,6 +867,7 @@ cudaError_t launch_mma16_varlen_fp8(const CUtensorMap& tk, const CUtensorMap& tv
   const int64_t units = (int64_t)items_cap * p.m.num_kv_heads;
   const int64_t resident = 2 * (int64_t)num_sms();
   const int grid_x = (int)std::max<int64_t>(1, std::min(units, resident));
+  if (p.m.k_bscales) return launch<128, false, true, true>(tk, tv, p, grid_x, stream);
   return launch<128, false, true>(tk, tv, p, grid_x, stream);
 }
 
@@ -841,6 +876,7 @@ cudaError_t launch_mma16_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv,
   const int64_t items = (int64_t)p.m.num_seqs * p.max_parts;
   const int grid_x = items > 65535 ? 65535 : (int)items;
   if (grid_x <= 0) return cudaSuccess;
+  if (p.m.k_bscales) return launch<128, true, true, true>(tk, tv, p, grid_x, stream);
   return launch<128, true, true>(tk, tv, p, grid_x, stream);
 }
 

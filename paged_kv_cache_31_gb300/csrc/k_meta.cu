@@ -131,6 +131,17 @@ __host__ __device__ constexpr size_t plan_smem_bytes(int s, int64_t t, int items
 // word; the attention kernels wait for the whole launch, so this happens before anything is
 // written.  Table lengths beyond max_blocks and the other per-sequence checks are the
 // planner's; only existing entries are read here, whatever query_start_loc holds.
+// The per-block K and V factors of pool block id (every kv head) are finite and positive.
+__device__ __forceinline__ bool block_factors_bad(const float* kbs, const float* vbs, int32_t id,
+                                                  int32_t hkv) {
+  bool bad = false;
+  for (int g = 0; g < hkv; ++g) {
+    const float a = kbs[(int64_t)id * hkv + g], b = vbs[(int64_t)id * hkv + g];
+    bad |= !(a > 0.f && a <= 3.402823466e38f) || !(b > 0.f && b <= 3.402823466e38f);
+  }
+  return bad;
+}
+
 __device__ void check_tables(const VarlenMeta& m, int* status) {
   __shared__ int v_off[1025];  // chunk offsets of this round's sequences
   __shared__ int v_need[1024];
@@ -162,6 +173,7 @@ __device__ void check_tables(const VarlenMeta& m, int* status) {
     const int cnt = min((int)blockDim.x, K - k0);  // sequences of this round
     for (int j0 = warp; j0 < total; j0 += 2 * nwarps) {  // warp-uniform
       int32_t id[2][8];
+      uint32_t real = 0;  // bit 8h + u: a table entry (not padding)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int j = j0 + h * nwarps;
@@ -179,13 +191,21 @@ __device__ void check_tables(const VarlenMeta& m, int* status) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int i = base + lane + 32 * u;
-          id[h][u] = (j < total && i < v_need[t]) ? row[i] : 0;
+          const bool r = j < total && i < v_need[t];
+          id[h][u] = r ? row[i] : 0;
+          real |= (uint32_t)r << (8 * h + u);
         }
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) bad |= (id[h][u] < 0 || (int64_t)id[h][u] >= m.num_blocks);
+        for (int u = 0; u < 8; ++u) {
+          const bool out = id[h][u] < 0 || (int64_t)id[h][u] >= m.num_blocks;
+          bad |= out;
+          // per-block factors of the blocks the call reads (e4m3 pools)
+          if (m.k_bscales && !out && ((real >> (8 * h + u)) & 1u))
+            bad |= block_factors_bad(m.k_bscales, m.v_bscales, id[h][u], m.num_kv_heads);
+        }
     }
     __syncthreads();  // the next round reuses the arrays
   }
@@ -399,6 +419,8 @@ __global__ void __launch_bounds__(1024)
               for (int u = 0; u < 8; ++u) {
                 const int64_t i = base + lane + 32 * u;
                 bad |= (id[u] < 0 || (int64_t)id[u] >= m.num_blocks);
+                if (m.k_bscales && i < need && id[u] >= 0 && (int64_t)id[u] < m.num_blocks)
+                  bad |= block_factors_bad(m.k_bscales, m.v_bscales, id[u], m.num_kv_heads);
                 if (i < b - a) {
                   bad |= (pos[u] < 0 || pos[u] >= n);
                   plan[L.tok_off + a + i] = s;
@@ -609,7 +631,8 @@ __global__ void __launch_bounds__(1024)
 __global__ void k_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
                                   int32_t max_blocks, int32_t block_size, int64_t num_blocks,
                                   int32_t partition_size, int32_t max_parts, int check_tables,
-                                  int* status) {
+                                  const float* k_bscales, const float* v_bscales,
+                                  int32_t num_kv_heads, int* status) {
   const int s = blockIdx.x;
   const int n = seq_lens[s];
   if (n < 1) {
@@ -630,7 +653,9 @@ __global__ void k_validate_decode(const int32_t* seq_lens, const int32_t* block_
   bool bad = false;
   for (int64_t i = threadIdx.x; i < need; i += blockDim.x) {
     const int32_t id = row[i];
-    bad |= (id < 0 || (int64_t)id >= num_blocks);
+    const bool out = id < 0 || (int64_t)id >= num_blocks;
+    bad |= out;
+    if (k_bscales && !out) bad |= block_factors_bad(k_bscales, v_bscales, id, num_kv_heads);
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) record_error(status, PA_EINVAL);
 }
@@ -663,14 +688,18 @@ __global__ void k_slot_mapping(const int32_t* qsl, const int32_t* positions,
 }
 
 __global__ void k_validate_slots(const int32_t* slots, int64_t num_tokens, int64_t num_slots,
-                                 int* status) {
+                                 const float* kbs, const float* vbs, int32_t block_size,
+                                 int32_t num_kv_heads, int* status) {
   pdl_wait();
   pdl_launch_dependents();
   bool bad = false;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < num_tokens;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int32_t s = slots[t];
-    bad |= (s < 0 || (int64_t)s >= num_slots);
+    const bool out = s < 0 || (int64_t)s >= num_slots;
+    bad |= out;
+    // per-block factors of the block the row goes to
+    if (kbs && !out) bad |= block_factors_bad(kbs, vbs, s / block_size, num_kv_heads);
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) record_error(status, PA_EINVAL);
 }
@@ -747,7 +776,9 @@ __global__ void __launch_bounds__(256)
                       void* __restrict__ vb, const int32_t* __restrict__ slots, int64_t num_tokens,
                       int64_t num_slots, int64_t row_elems, float k_scale, float v_scale,
                       const float* __restrict__ k_scales, const float* __restrict__ v_scales,
-                      int32_t head_dim, int* status) {
+                      const float* __restrict__ kbs, const float* __restrict__ vbs,
+                      int32_t block_size, int32_t head_dim, int* status) {
+  const int32_t hkv = (int32_t)(row_elems / head_dim);
   __shared__ int s_skip;
   pdl_wait();
   pdl_launch_dependents();
@@ -758,7 +789,9 @@ __global__ void __launch_bounds__(256)
     bool bad = false;
     for (int64_t t = threadIdx.x; t < num_tokens; t += blockDim.x) {
       const int32_t sl = slots[t];
-      bad |= (sl < 0 || (int64_t)sl >= num_slots);
+      const bool out = sl < 0 || (int64_t)sl >= num_slots;
+      bad |= out;
+      if (kbs && !out) bad |= block_factors_bad(kbs, vbs, sl / block_size, hkv);
     }
     if (__syncthreads_or(bad)) {
       if (blockIdx.x == 0 && threadIdx.x == 0) record_error(status, PA_EINVAL);
@@ -768,12 +801,21 @@ __global__ void __launch_bounds__(256)
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= num_tokens) return;
-  const int64_t dst = (int64_t)slots[t] * row_elems, src = t * row_elems;
+  const int32_t slot = slots[t];
+  const int64_t dst = (int64_t)slot * row_elems, src = t * row_elems;
   for (int64_t i = lane; i < row_elems; i += 32) {
-    // one scale per kv head (head i / head_dim of the row) when the arrays are given
-    const int g = k_scales || v_scales ? (int)(i / head_dim) : 0;
-    const float a = __fdiv_rn(to_f32(k[src + i]), k_scales ? __ldg(k_scales + g) : k_scale);
-    const float b = __fdiv_rn(to_f32(v[src + i]), v_scales ? __ldg(v_scales + g) : v_scale);
+    // one scale per kv head (head i / head_dim of the row), or per (block, kv head), when the
+    // arrays are given
+    const int g = k_scales || v_scales || kbs ? (int)(i / head_dim) : 0;
+    float ks = k_scales ? __ldg(k_scales + g) : k_scale;
+    float vs = v_scales ? __ldg(v_scales + g) : v_scale;
+    if (kbs) {
+      const int64_t f = (int64_t)(slot / block_size) * hkv + g;
+      ks = __ldg(kbs + f);
+      vs = __ldg(vbs + f);
+    }
+    const float a = __fdiv_rn(to_f32(k[src + i]), ks);
+    const float b = __fdiv_rn(to_f32(v[src + i]), vs);
     if constexpr (DST == PA_FP8_E4M3) {
       static_cast<uint8_t*>(kb)[dst + i] = (uint8_t)(f32x2_to_e4m3x2(a, 0.f) & 0xffu);
       static_cast<uint8_t*>(vb)[dst + i] = (uint8_t)(f32x2_to_e4m3x2(b, 0.f) & 0xffu);
@@ -790,20 +832,22 @@ __global__ void __launch_bounds__(256)
 template <typename TS, int DST>
 cudaError_t convert_as(const void* k, const void* v, void* kb, void* vb, const int32_t* slots,
                        int64_t T, int64_t row_elems, int64_t num_slots, float k_scale,
-                       float v_scale, const float* ks, const float* vs, int32_t head_dim,
-                       int* status, cudaStream_t stream) {
+                       float v_scale, const float* ks, const float* vs, const float* kbs,
+                       const float* vbs, int32_t block_size, int32_t head_dim, int* status,
+                       cudaStream_t stream) {
   const dim3 grid((unsigned)((T + 7) / 8)), block(256);
   if (T <= kCheckedScatter)
     return launch_pdl(k_scatter_convert<TS, DST, true>, grid, block, 0, stream, (const TS*)k,
                       (const TS*)v, kb, vb, slots, T, num_slots, row_elems, k_scale, v_scale,
-                      ks, vs, head_dim, status);
+                      ks, vs, kbs, vbs, block_size, head_dim, status);
   const int64_t vgrid = std::min<int64_t>((T + 255) / 256, 1024);
   cudaError_t e = launch_pdl(k_validate_slots, dim3((unsigned)vgrid), dim3(256), 0, stream, slots,
-                             T, num_slots, status);
+                             T, num_slots, kbs, vbs, block_size,
+                             (int32_t)(row_elems / head_dim), status);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_scatter_convert<TS, DST, false>, grid, block, 0, stream, (const TS*)k,
                     (const TS*)v, kb, vb, slots, T, num_slots, row_elems, k_scale, v_scale, ks,
-                    vs, head_dim, status);
+                    vs, kbs, vbs, block_size, head_dim, status);
 }
 
 // Per kv head dequantisation scales must be finite and positive (tinyllm 2.6: reject before
@@ -1004,7 +1048,8 @@ cudaError_t scatter_as(const void* k, const void* v, void* kb, void* vb, const i
                       row_vecs, status);
   const int64_t vgrid = std::min<int64_t>((T + 255) / 256, 1024);
   cudaError_t e = launch_pdl(k_validate_slots, dim3((unsigned)vgrid), dim3(256), 0, stream, slots,
-                             T, num_slots, status);
+                             T, num_slots, (const float*)nullptr, (const float*)nullptr, 1, 0,
+                             status);
   if (e != cudaSuccess) return e;
   const int warps = 8;
   const int64_t grid = (T + warps - 1) / warps;
@@ -1049,11 +1094,14 @@ cudaError_t launch_plan_varlen(const VarlenMeta& m, int32_t* plan, const PlanLay
 cudaError_t launch_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
                                    int32_t num_seqs, int32_t max_blocks, int32_t block_size,
                                    int64_t num_blocks, int32_t partition_size, int32_t max_parts,
-                                   int check_tables, int* status, cudaStream_t stream) {
+                                   int check_tables, int* status, cudaStream_t stream,
+                                   const float* k_bscales, const float* v_bscales,
+                                   int32_t num_kv_heads) {
   if (num_seqs <= 0) return cudaSuccess;
   k_validate_decode<<<num_seqs, 256, 0, stream>>>(seq_lens, block_tables, max_blocks, block_size,
                                                   num_blocks, partition_size, max_parts,
-                                                  check_tables, status);
+                                                  check_tables, k_bscales, v_bscales,
+                                                  num_kv_heads, status);
   return cudaGetLastError();
 }
 
@@ -1168,12 +1216,14 @@ cudaError_t launch_reshape_and_cache_convert(const void* k, const void* v, void*
                                              int32_t block_size, int64_t num_blocks, int src_bf16,
                                              int dst, float k_scale, float v_scale,
                                              const float* k_scales, const float* v_scales,
-                                             int32_t head_dim, int* status, cudaStream_t stream) {
+                                             int32_t head_dim, int* status, cudaStream_t stream,
+                                             const float* k_bscales, const float* v_bscales) {
   if (num_tokens <= 0) return cudaSuccess;
   const int64_t ns = num_blocks * block_size;
 #define PA_CONVERT(TS, DST)                                                                  \
   convert_as<TS, DST>(k, v, k_blocks, v_blocks, slots, num_tokens, row_elems, ns, k_scale,   \
-                      v_scale, k_scales, v_scales, head_dim, status, stream)
+                      v_scale, k_scales, v_scales, k_bscales, v_bscales, block_size,        \
+                      head_dim, status, stream)
   cudaError_t e;
   if (src_bf16)
     e = dst == PA_FP8_E4M3 ? PA_CONVERT(__nv_bfloat16, PA_FP8_E4M3)

@@ -374,6 +374,29 @@ pa_status pa_reshape_and_cache_per_head(const void* k, const void* v, void* k_bl
       head_dim, d->status, stream));
 }
 
+pa_status pa_reshape_and_cache_per_block(const void* k, const void* v, void* k_blocks,
+                                         void* v_blocks, const int32_t* slot_mapping,
+                                         int64_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t block_size,
+                                         int64_t num_blocks, pa_dtype src_dtype,
+                                         pa_dtype kv_dtype, const float* k_block_scales,
+                                         const float* v_block_scales, cudaStream_t stream) {
+  if (num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return PA_ESHAPE;
+  if (!dtype_ok(src_dtype) || !pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
+  if (num_tokens < 0 || num_blocks < 0) return PA_EINVAL;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_blocks || !v_blocks || !slot_mapping || !k_block_scales ||
+      !v_block_scales)
+    return PA_EINVAL;
+  if (num_blocks * block_size > INT32_MAX) return PA_EUNSUPPORTED;  // slots are int32
+  const DeviceState* d = device_state();
+  if (!d) return PA_ECUDA;
+  return from_cuda(launch_reshape_and_cache_convert(
+      k, v, k_blocks, v_blocks, slot_mapping, num_tokens, (int64_t)num_kv_heads * head_dim,
+      block_size, num_blocks, src_dtype == PA_BF16, kv_dtype, 1.f, 1.f, nullptr, nullptr,
+      head_dim, d->status, stream, k_block_scales, v_block_scales));
+}
+
 size_t pa_varlen_forward_workspace_size(int32_t num_seqs, int64_t num_tokens, int32_t num_heads,
                                         int32_t num_kv_heads, int32_t head_dim,
                                         int32_t max_blocks_per_seq, int32_t block_size) {
@@ -423,7 +446,12 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
                              float k_scale, float v_scale, const float* k_scales,
                              const float* v_scales, uint32_t flags, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream,
-                             const CacheArgs* cache) {
+                             const CacheArgs* cache, const float* k_bscales = nullptr,
+                             const float* v_bscales = nullptr) {
+  // per-block factors: both arrays, e4m3 pools, not together with per-head scales
+  const bool per_block = k_bscales || v_bscales;
+  if (per_block && (!k_bscales || !v_bscales || k_scales || v_scales)) return PA_EINVAL;
+  if (per_block && kv_dtype != PA_FP8_E4M3) return PA_EUNSUPPORTED;
   bool empty = false;
   const pa_status chk = varlen_check(q, k_blocks, v_blocks, out, query_start_loc, seq_lens,
                                      positions, block_tables, num_seqs, num_tokens, num_heads,
@@ -460,12 +488,16 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
   m.v_scale = v_scale;
   m.k_scales = k_scales;
   m.v_scales = v_scales;
+  m.k_bscales = k_bscales;
+  m.v_bscales = v_bscales;
   scale *= k_scale;  // K = k_scale * pool: the scores take it with the softmax scale
   int32_t* plan = static_cast<int32_t*>(workspace);  // (the plan also checks per-head scales)
   PlanLayout L = plan_layout(num_seqs, num_tokens, m.group);
   const bool fast = mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
   const bool fast8 =
       mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
+  // per-block factors are applied by the e4m3 warp-MMA kernel only (every sequence runs there)
+  if (per_block && !fast8) return PA_EUNSUPPORTED;
   // prefill-class sequences (more than 64 query rows per kv head) go to the tcgen05 kernel:
   // head size 128 and a GQA group that divides the 128-row tile; bf16 or e4m3 pools
   // No sequence can have more than num_tokens - num_seqs + 1 query tokens: when even that
@@ -473,7 +505,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
   const int64_t max_rows = (num_tokens - (num_seqs > 0 ? num_seqs : 1) + 1) * m.group;
   L.use_tc = (fast || fast8) && head_dim == 128 && m.group <= 128 && (128 % m.group) == 0 &&
              aligned(q, 16) && max_rows > L.tc_min_rows && scale > 0.f && tc_enabled() &&
-             !(flags & PA_FLAG_BITWISE);
+             !(flags & PA_FLAG_BITWISE) && !per_block;
 
   // the tcgen05 kernel's launch: one CTA per SM, pairs, never more than there are items
   const int64_t tc_work = L.tc_cap * num_kv_heads;
@@ -634,6 +666,27 @@ pa_status pa_varlen_forward_per_head(const void* q, const void* k_blocks, const 
                      workspace_bytes, stream, nullptr);
 }
 
+pa_status pa_varlen_forward_per_block(const void* q, const void* k_blocks, const void* v_blocks,
+                                      void* out, const int32_t* query_start_loc,
+                                      const int32_t* seq_lens, const int32_t* positions,
+                                      const int32_t* block_tables, int32_t num_seqs,
+                                      int64_t num_tokens, int32_t num_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                      int64_t num_blocks, int32_t max_blocks_per_seq,
+                                      pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
+                                      int32_t causal, int32_t sliding_window, const float* sinks,
+                                      float* lse, const float* k_block_scales,
+                                      const float* v_block_scales, uint32_t flags,
+                                      void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream) {
+  if (!k_block_scales || !v_block_scales) return PA_EINVAL;
+  return varlen_impl(q, k_blocks, v_blocks, out, query_start_loc, seq_lens, positions,
+                     block_tables, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, max_blocks_per_seq, q_dtype, kv_dtype, scale, causal,
+                     sliding_window, sinks, lse, 1.f, 1.f, nullptr, nullptr, flags, workspace,
+                     workspace_bytes, stream, nullptr, k_block_scales, v_block_scales);
+}
+
 pa_status pa_cache_and_attend(const void* k_new, const void* v_new, const void* q,
                               void* k_blocks, void* v_blocks, void* out,
                               const int32_t* query_start_loc, const int32_t* seq_lens,
@@ -680,10 +733,14 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
                                   int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype,
                                   float scale, int32_t sliding_window, float k_scale,
                                   float v_scale, const float* k_scales, const float* v_scales,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, const float* k_bscales = nullptr,
+                                  const float* v_bscales = nullptr) {
   if (num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       num_heads % num_kv_heads != 0 || partition_size <= 0 || max_num_partitions <= 0)
     return PA_ESHAPE;
+  const bool per_block = k_bscales || v_bscales;
+  if (per_block && (!k_bscales || !v_bscales || k_scales || v_scales)) return PA_EINVAL;
+  if (per_block && kv_dtype != PA_FP8_E4M3) return PA_EUNSUPPORTED;
   if (!dtype_ok(q_dtype) || !pool_dtype_ok(kv_dtype)) return PA_EUNSUPPORTED;
   if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_EINVAL;
   scale *= k_scale;
@@ -695,11 +752,17 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
     return PA_EINVAL;
   const DeviceState* d = device_state();
   if (!d) return PA_ECUDA;
+  const bool fp8 =
+      mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, nullptr);
+  // per-block factors: the e4m3 warp-MMA kernel only
+  if (per_block && !(fp8 && num_heads / num_kv_heads <= 16 && aligned(tmp_out, 16)))
+    return PA_EUNSUPPORTED;
   if (launch_validate_scales(k_scales, v_scales, num_kv_heads, d->status, stream) != cudaSuccess)
     return PA_ECUDA;
   cudaError_t e = launch_validate_decode(seq_lens, block_tables, num_seqs, max_blocks_per_seq,
                                          block_size, num_blocks, partition_size,
-                                         max_num_partitions, 1, d->status, stream);
+                                         max_num_partitions, 1, d->status, stream, k_bscales,
+                                         v_bscales, num_kv_heads);
   if (e != cudaSuccess) return PA_ECUDA;
   VarlenMeta m{};
   std::memset(&m, 0, sizeof m);
@@ -719,8 +782,8 @@ static pa_status splitkv_partials(const void* q, const void* k_blocks, const voi
   m.v_scale = v_scale;
   m.k_scales = k_scales;
   m.v_scales = v_scales;
-  const bool fp8 =
-      mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, nullptr);
+  m.k_bscales = k_bscales;
+  m.v_bscales = v_bscales;
   if ((fp8 || mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, nullptr)) &&
       m.group <= 16 && aligned(tmp_out, 16)) {
     CUtensorMap tk, tv;
@@ -832,6 +895,22 @@ pa_status pa_decode_splitkv_partials_per_head(
                           num_blocks, max_blocks_per_seq, partition_size, max_num_partitions,
                           q_dtype, kv_dtype, scale, sliding_window, 1.f, 1.f, k_scales, v_scales,
                           stream);
+}
+
+pa_status pa_decode_splitkv_partials_per_block(
+    const void* q, const void* k_blocks, const void* v_blocks, float* max_logits,
+    float* exp_sums, float* tmp_out, const int32_t* seq_lens, const int32_t* block_tables,
+    int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, int32_t max_blocks_per_seq, int32_t partition_size,
+    int32_t max_num_partitions, pa_dtype q_dtype, pa_dtype kv_dtype, float scale,
+    int32_t sliding_window, const float* k_block_scales, const float* v_block_scales,
+    cudaStream_t stream) {
+  if (!k_block_scales || !v_block_scales) return PA_EINVAL;
+  return splitkv_partials(q, k_blocks, v_blocks, max_logits, exp_sums, tmp_out, seq_lens,
+                          block_tables, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, partition_size, max_num_partitions,
+                          q_dtype, kv_dtype, scale, sliding_window, 1.f, 1.f, nullptr, nullptr,
+                          stream, k_block_scales, v_block_scales);
 }
 
 pa_status pa_decode_splitkv_reduce(void* out, const float* max_logits, const float* exp_sums,

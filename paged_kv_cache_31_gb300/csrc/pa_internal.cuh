@@ -336,6 +336,11 @@ struct VarlenMeta {
   // k_scales[g] * pool (taken with the score scale), V is v_scales[g] * pool
   const float* k_scales;
   const float* v_scales;
+  // one factor per (pool block, kv head) (device, [num_blocks, num_kv_heads]), or null:
+  // position j of kv head g reads K = k_bscales[id * Hkv + g] * pool, id = its block (e4m3
+  // pools, the warp-MMA kernel); checked by the planner's table checks
+  const float* k_bscales;
+  const float* v_bscales;
 };
 
 // The scale of kv head g from a per-head array, times the per-pool scalar; the scalar alone
@@ -412,7 +417,9 @@ cudaError_t launch_tc_prefill(const CUtensorMap& tq, const CUtensorMap& tk, cons
 cudaError_t launch_validate_decode(const int32_t* seq_lens, const int32_t* block_tables,
                                    int32_t num_seqs, int32_t max_blocks, int32_t block_size,
                                    int64_t num_blocks, int32_t partition_size, int32_t max_parts,
-                                   int check_tables, int* status, cudaStream_t stream);
+                                   int check_tables, int* status, cudaStream_t stream,
+                                   const float* k_bscales = nullptr,
+                                   const float* v_bscales = nullptr, int32_t num_kv_heads = 0);
 cudaError_t launch_slot_mapping(const int32_t* qsl, const int32_t* positions,
                                 const int32_t* block_tables, int32_t num_seqs, int64_t num_tokens,
                                 int32_t max_blocks, int32_t block_size, int64_t num_blocks,
@@ -448,7 +455,9 @@ cudaError_t launch_reshape_and_cache_convert(const void* k, const void* v, void*
                                              int32_t block_size, int64_t num_blocks, int src_bf16,
                                              int dst, float k_scale, float v_scale,
                                              const float* k_scales, const float* v_scales,
-                                             int32_t head_dim, int* status, cudaStream_t stream);
+                                             int32_t head_dim, int* status, cudaStream_t stream,
+                                             const float* k_bscales = nullptr,
+                                             const float* v_bscales = nullptr);
 // Records PA_EINVAL when a per-head scale (either array may be null) is not finite and > 0.
 cudaError_t launch_validate_scales(const float* k_scales, const float* v_scales,
                                    int32_t num_kv_heads, int* status, cudaStream_t stream);
