@@ -431,19 +431,25 @@ def fp8_decode(pa, dev, args, peaks, stream, n):
     kb8, vb8 = workloads.fp8_pools(w2)
     out2 = torch.empty_like(w2.q)
     ws2 = pa.workspace_for(w2.q, kb8, w2.query_start_loc, w2.block_tables)
-    # the same pools with one dequantisation scale per kv head (device arrays)
+    # the same pools with one dequantisation scale per kv head, and one factor per (pool block,
+    # kv head) (device arrays)
     hs = torch.full((w2.num_kv_heads,), 0.125, device=dev)
+    bs = torch.full((kb8.shape[0], w2.num_kv_heads), 0.125, device=dev)
 
-    def call(per_head=False):
-        kw = dict(k_scales=hs, v_scales=hs) if per_head else dict(k_scale=0.125, v_scale=0.125)
+    def call(per_head=False, per_block=False):
+        kw = (dict(k_scales=hs, v_scales=hs) if per_head
+              else dict(k_block_scales=bs, v_block_scales=bs) if per_block
+              else dict(k_scale=0.125, v_scale=0.125))
         pa.pa_varlen_forward(w2.q, kb8, vb8, out2, w2.query_start_loc, w2.seq_lens,
                              w2.positions, w2.block_tables, w2.scale, workspace=ws2, **kw)
 
     for _ in range(max(3, args.warmup)):
         call()
         call(True)
+        call(False, True)
     ms = time_calls(call, n, stream)
     ms_h = time_calls(lambda: call(True), n, stream)
+    ms_b = time_calls(lambda: call(False, True), n, stream)
     assert pa.pa_device_status() == pa.PA_OK
     kv = kv_bytes(w2, elem_bytes=1)
     name = w2.name + "-fp8"
@@ -452,7 +458,9 @@ def fp8_decode(pa, dev, args, peaks, stream, n):
             "l2": "inputs (pools of ~300 MB) larger than L2",
             "traffic": ncu_traffic("k_mma16_fp8", name),
             "per_head_scales": {"ms": ms_h, "gbs": kv / (ms_h * 1e-3) / 1e9,
-                                "frac_of_hbm": kv / (ms_h * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+                                "frac_of_hbm": kv / (ms_h * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+            "per_block_scales": {"ms": ms_b, "gbs": kv / (ms_b * 1e-3) / 1e9,
+                                 "frac_of_hbm": kv / (ms_b * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
 
 
 def fp8_prefill(pa, dev, args, peaks, stream, n):
