@@ -199,12 +199,12 @@ __device__ void check_tables(const VarlenMeta& m, int* status) {
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const bool out = id[h][u] < 0 || (int64_t)id[h][u] >= m.num_blocks;
-          bad |= out;
-          // per-block factors of the blocks the call reads (e4m3 pools)
-          if (m.k_bscales && !out && ((real >> (8 * h + u)) & 1u))
-            bad |= block_factors_bad(m.k_bscales, m.v_bscales, id[h][u], m.num_kv_heads);
+        for (int u = 0; u < 8; ++u) bad |= (id[h][u] < 0 || (int64_t)id[h][u] >= m.num_blocks);
+      if (m.k_bscales)  // per-block factors of the blocks the call reads (e4m3 pools)
+        for (int e = 0; e < 16; ++e) {
+          const int32_t b = id[e >> 3][e & 7];
+          if (((real >> e) & 1u) && b >= 0 && (int64_t)b < m.num_blocks)
+            bad |= block_factors_bad(m.k_bscales, m.v_bscales, b, m.num_kv_heads);
         }
     }
     __syncthreads();  // the next round reuses the arrays
@@ -419,8 +419,6 @@ __global__ void __launch_bounds__(1024)
               for (int u = 0; u < 8; ++u) {
                 const int64_t i = base + lane + 32 * u;
                 bad |= (id[u] < 0 || (int64_t)id[u] >= m.num_blocks);
-                if (m.k_bscales && i < need && id[u] >= 0 && (int64_t)id[u] < m.num_blocks)
-                  bad |= block_factors_bad(m.k_bscales, m.v_bscales, id[u], m.num_kv_heads);
                 if (i < b - a) {
                   bad |= (pos[u] < 0 || pos[u] >= n);
                   plan[L.tok_off + a + i] = s;
@@ -429,6 +427,10 @@ __global__ void __launch_bounds__(1024)
                   hi = max(hi, e);
                 }
               }
+              if (m.k_bscales)  // per-block factors of the blocks the call reads
+                for (int u = 0; u < 8; ++u)
+                  if (base + lane + 32 * u < need && id[u] >= 0 && (int64_t)id[u] < m.num_blocks)
+                    bad |= block_factors_bad(m.k_bscales, m.v_bscales, id[u], m.num_kv_heads);
             }
           }
         }
@@ -653,10 +655,14 @@ __global__ void k_validate_decode(const int32_t* seq_lens, const int32_t* block_
   bool bad = false;
   for (int64_t i = threadIdx.x; i < need; i += blockDim.x) {
     const int32_t id = row[i];
-    const bool out = id < 0 || (int64_t)id >= num_blocks;
-    bad |= out;
-    if (k_bscales && !out) bad |= block_factors_bad(k_bscales, v_bscales, id, num_kv_heads);
+    bad |= (id < 0 || (int64_t)id >= num_blocks);
   }
+  if (k_bscales)  // per-block factors of the blocks the sequence reads (a pass of its own)
+    for (int64_t i = threadIdx.x; i < need; i += blockDim.x) {
+      const int32_t id = row[i];
+      if (id >= 0 && (int64_t)id < num_blocks)
+        bad |= block_factors_bad(k_bscales, v_bscales, id, num_kv_heads);
+    }
   if (__syncthreads_or(bad) && threadIdx.x == 0) record_error(status, PA_EINVAL);
 }
 
