@@ -167,8 +167,9 @@ pa_status pa_reshape_and_cache_per_head(const void* k, const void* v, void* k_bl
  * of a new row written to slot s is stored as x / k_block_scales[(s / block_size) *
  * num_kv_heads + g] (x / v_block_scales[...]).  k_block_scales, v_block_scales: DEVICE arrays
  * [num_blocks, num_kv_heads] of floats owned by the caller, both required (NULL: PA_EINVAL).
- * A factor of a block some row is written to that is not finite and positive is recorded as
- * PA_EINVAL in the device status and nothing is written; other errors as
+ * A factor of a block some row is written to that is not a finite positive normal float (at
+ * least 2^-126) is recorded as PA_EINVAL in the device status and nothing is written; other
+ * errors as
  * pa_reshape_and_cache_ex.  The caller chooses the factors (for example from a block's
  * largest magnitude when it is allocated); the library does not change them.
  */
@@ -295,13 +296,18 @@ pa_status pa_varlen_forward_per_head(const void* q, const void* k_blocks, const 
  * k_blocks[...] and V = v_block_scales[...] * v_blocks[...].  k_block_scales, v_block_scales:
  * DEVICE arrays [num_blocks, num_kv_heads] of floats owned by the caller, both required (NULL:
  * PA_EINVAL).  The factors of every block a sequence with query tokens reads (the first
- * ceil(seq_lens[s] / block_size) entries of its table row) must be finite and positive, else
- * PA_EINVAL is recorded in the device status and out / lse are left untouched.  kv_dtype must
+ * ceil(seq_lens[s] / block_size) entries of its table row) must be finite positive normal
+ * floats (at least 2^-126), else PA_EINVAL is recorded in the device status and out / lse are left untouched.  kv_dtype must
  * be PA_FP8_E4M3 and the call must qualify for the warp-MMA path (q bf16, head_dim 128,
  * block_size 16, 16-byte aligned tensors), else PA_EUNSUPPORTED before anything is enqueued.
- * Every sequence, prefill chunks included, runs on the warp-MMA kernel.  The K factor
- * multiplies each block's scores exactly; the V factor multiplies the block's softmax weights
- * before they are rounded to f16 for P V.  Other arguments and errors as pa_varlen_forward_ex.
+ * Both kernels multiply each block's scores by its K factor in fp32, exactly.  V: the
+ * warp-MMA kernel (decode tokens) multiplies the block's softmax weights by the factor over
+ * the largest factor the warp has met so far, before the weights are rounded to f16, and that
+ * reference multiplies the warp's fp32 output; the tcgen05 kernel (prefill chunks) multiplies
+ * the block's widened codes by the factor over its item's reference (the factor of the item's
+ * first block), rounded to f16, and the reference multiplies the output.  An item with a V
+ * ratio outside [2^-12, 146] is recomputed by the warp-MMA kernel.  So any finite positive
+ * factors keep the f16 values in range.  Other arguments and errors as pa_varlen_forward_ex.
  */
 pa_status pa_varlen_forward_per_block(const void* q, const void* k_blocks, const void* v_blocks,
                                       void* out, const int32_t* query_start_loc,

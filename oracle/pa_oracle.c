@@ -230,9 +230,13 @@ static float head_scale(const float* s, int32_t g, int32_t num_kv_heads, float s
   if (!s) return scalar;
   return MUTANT(75) ? s[0] : s[g % num_kv_heads];
 }
+/* A per-block factor is a finite, positive normal float: at least FLT_MIN (2^-126), so its
+ * reciprocal is finite as well (the library's reading of per-block scales; the pages give
+ * no range). */
+static int block_factor_ok(float a) { return a >= FLT_MIN && a <= FLT_MAX; }
 /* Per-block scales ([num_blocks, num_kv_heads], NULL: none): every factor of every block a
  * sequence reads -- the first ceil(seq_len / b) entries of its table row, of the sequences
- * with query tokens when qsl is given -- must be finite and > 0.  Called after the tables
+ * with query tokens when qsl is given -- must pass block_factor_ok.  Called after the tables
  * themselves were checked. */
 static int block_scales_ok(const float* kbs, const float* vbs, const int32_t* qsl,
                            const int32_t* seq_lens, const int32_t* block_tables,
@@ -244,10 +248,8 @@ static int block_scales_ok(const float* kbs, const float* vbs, const int32_t* qs
     for (int64_t i = 0; i < need; ++i) {
       const int64_t id = block_tables[(int64_t)s * max_blocks + i];
       for (int32_t g = 0; g < num_kv_heads; ++g) {
-        if (kbs && !(kbs[id * num_kv_heads + g] > 0.f && kbs[id * num_kv_heads + g] <= FLT_MAX))
-          return 0;
-        if (vbs && !(vbs[id * num_kv_heads + g] > 0.f && vbs[id * num_kv_heads + g] <= FLT_MAX))
-          return 0;
+        if (kbs && !block_factor_ok(kbs[id * num_kv_heads + g])) return 0;
+        if (vbs && !block_factor_ok(vbs[id * num_kv_heads + g])) return 0;
       }
     }
   }
@@ -311,7 +313,7 @@ int oracle_reshape_and_cache_per_block(const void* k, const void* v, void* k_blo
     for (int32_t g = 0; g < num_kv_heads; ++g) {
       const float a = k_bscales ? k_bscales[blk * num_kv_heads + g] : 1.f;
       const float b = v_bscales ? v_bscales[blk * num_kv_heads + g] : 1.f;
-      if (!(a > 0.f && a <= FLT_MAX) || !(b > 0.f && b <= FLT_MAX)) return ORC_EINVAL;
+      if (!block_factor_ok(a) || !block_factor_ok(b)) return ORC_EINVAL;
     }
   }
   const int64_t row = (int64_t)num_kv_heads * head_dim;

@@ -124,10 +124,13 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
 
 // PB (e4m3 pools only): one K and one V factor per (pool block, kv head), p.m.k_bscales /
 // v_bscales [num_blocks, num_kv_heads].  The K factor multiplies the block's scores with the
-// softmax scale; the V factor multiplies the block's fp32 weights where they are rounded to
-// f16 for P V (the row sum keeps the unscaled weights).  Lane 0 copies both factors into the
-// stage's slot with cp.async when it issues the block's TMA copies, and the stage's barrier
-// (two arrivals) completes only when they have landed too.
+// softmax scale.  The V factor, over the largest one the warp has met so far (its reference;
+// O is rescaled when it rises) and times 2^15, multiplies the block's fp32 weights where they
+// are rounded to f16 for P V, and the reference over 2^15 multiplies the warp's O where the
+// warps are merged: the f16 weights stay in [0, 2^15] whatever the factors' magnitude (the
+// row sum keeps the unscaled weights).  Lane 0 copies both factors into the stage's slot with cp.async when it issues
+// the block's TMA copies, and the stage's barrier (two arrivals) completes only when they
+// have landed too.
 template <int D, int NW, int NS, bool SPLIT, bool FP8, bool PB = false>
 __global__ void __launch_bounds__(NW * 32, 2)
     k_mma16(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -311,6 +314,10 @@ __global__ void __launch_bounds__(NW * 32, 2)
     // bf16: this lane's rows g and g + 8 in [0], [1].  fp8: rows 8j + 2c + e in [2j + e].
     float mrow[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     float lrow[4] = {0.f, 0.f, 0.f, 0.f};
+    // PB: the largest V factor of the blocks this warp has folded (0 until the first), and
+    // its reciprocal: the warp's O is kept in units of vref / 2^15, so the f16 weights, at
+    // most 2^15, keep 2^29 of range below their largest value before they turn subnormal
+    float vref = 0.f, vinv = 0.f;
     float o[G_::kNT][4];
 #pragma unroll
     for (int j = 0; j < G_::kNT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -406,7 +413,17 @@ __global__ void __launch_bounds__(NW * 32, 2)
                         float2 fac) {
       constexpr int NR = decltype(groups)::value;
       float sk = sl2;  // the block's score scale
-      if constexpr (PB) sk = sl2 * fac.x;
+      [[maybe_unused]] float fv = 1.f;  // PB: the weights' V factor, in vref / 2^15 units
+      [[maybe_unused]] float beta = 1.f;  // PB: O's rescale when vref rises
+      if constexpr (PB) {
+        sk = sl2 * fac.x;
+        if (fac.y > vref) {  // (the factors are the warp's own: uniform across it)
+          beta = vref * __frcp_rn(fac.y);
+          vref = fac.y;
+          vinv = __frcp_rn(fac.y);  // finite: the factors are normal floats
+        }
+        fv = fac.y * vinv * 32768.f;
+      }
       const int c = lane & 3, g = lane >> 2;
       // S^T = K Q^T: A = key rows g and g + 8, bytes [32c, 32c + 32) (chunks 2c, 2c + 1); B =
       // the q fragments of group j, qa[kk][j] and qa[kk][j + 2]
@@ -473,6 +490,16 @@ __global__ void __launch_bounds__(NW * 32, 2)
           lrow[2 * j + e] = lrow[2 * j + e] * alpha[j][e] + (sc[j][e] + sc[j][2 + e]);
         }
       }
+      if constexpr (PB) {
+        if (beta != 1.f) {  // O only: the row sums keep the unscaled weights
+#pragma unroll
+          for (int j = 0; j < NR; ++j) {
+            alpha[j][0] *= beta;
+            alpha[j][1] *= beta;
+          }
+          grew = true;
+        }
+      }
       if (__any_sync(kFull, grew)) {  // skipped, the factors are exactly 1
 #pragma unroll
         for (int j = 0; j < NR; ++j)
@@ -490,7 +517,7 @@ __global__ void __launch_bounds__(NW * 32, 2)
 #pragma unroll
       for (int j = 0; j < NR; ++j) {
         auto vw = [&](float x) {  // the block's V factor on the weight (PB)
-          if constexpr (PB) return x * fac.y;
+          if constexpr (PB) return x * fv;
           else return x;
         };
         pb[j][0] = movmatrix_trans(pack_f16x2(vw(sc[j][0]), vw(sc[j][1])));
@@ -703,6 +730,8 @@ __global__ void __launch_bounds__(NW * 32, 2)
         // group j, M-tile t = 2i + h: accumulator [e] is (dimension 16g + 4i + 2h, row
         // 8j + 2c + e), [2 + e] the next dimension
         const int c = lane & 3, g = lane >> 2;
+        // PB: O back from units of vref / 2^15 (vref first: a tiny vref stays normal)
+        auto u = [&](float x) { return PB ? x * vref * (1.f / 32768.f) : x; };
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           if (j >= nr) break;
@@ -716,8 +745,8 @@ __global__ void __launch_bounds__(NW * 32, 2)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               *reinterpret_cast<float4*>(ob + row * kOStride + 16 * g + 4 * i) =
-                  make_float4(o[8 * j + 2 * i][e], o[8 * j + 2 * i][2 + e],
-                              o[8 * j + 2 * i + 1][e], o[8 * j + 2 * i + 1][2 + e]);
+                  make_float4(u(o[8 * j + 2 * i][e]), u(o[8 * j + 2 * i][2 + e]),
+                              u(o[8 * j + 2 * i + 1][e]), u(o[8 * j + 2 * i + 1][2 + e]));
           }
         }
       } else {

@@ -131,13 +131,15 @@ __host__ __device__ constexpr size_t plan_smem_bytes(int s, int64_t t, int items
 // word; the attention kernels wait for the whole launch, so this happens before anything is
 // written.  Table lengths beyond max_blocks and the other per-sequence checks are the
 // planner's; only existing entries are read here, whatever query_start_loc holds.
-// The per-block K and V factors of pool block id (every kv head) are finite and positive.
+// The per-block K and V factors of pool block id (every kv head) are finite, positive
+// normal floats (at least 2^-126, so that their reciprocals are finite too).
 __device__ __forceinline__ bool block_factors_bad(const float* kbs, const float* vbs, int32_t id,
                                                   int32_t hkv) {
   bool bad = false;
   for (int g = 0; g < hkv; ++g) {
     const float a = kbs[(int64_t)id * hkv + g], b = vbs[(int64_t)id * hkv + g];
-    bad |= !(a > 0.f && a <= 3.402823466e38f) || !(b > 0.f && b <= 3.402823466e38f);
+    bad |= !(a >= 1.17549435e-38f && a <= 3.402823466e38f) ||
+           !(b >= 1.17549435e-38f && b <= 3.402823466e38f);
   }
   return bad;
 }

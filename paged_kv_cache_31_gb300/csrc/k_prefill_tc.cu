@@ -656,11 +656,95 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& a, uint32_t& b) {
 // before the stores and the four warps need no barrier between them.  Q (bf16 from TMA) is
 // widened to f16 in place once per item, a quarter per warp: exact in f16's normal range,
 // which is how the warp-MMA fp8 path takes q as well.
+// Per-block factors (p.m.k_bscales / v_bscales, [num_blocks, num_kv_heads]).  The softmax
+// applies each block's K factor to its scores in fp32, exactly as the warp-MMA kernel does.
+// V: the converter multiplies the widened codes of each block by the ratio of its factor to
+// the item's reference, the factor of its first block (f16 product; the softmax multiplies
+// the output by the reference), so the products stay in f16's normal range whatever the
+// factors' magnitude.  A ratio outside [kRatioMin, kRatioMax] could not (a product past f16's
+// range, or small values left with few bits): the item is then marked for the warp-MMA
+// kernel behind this one, which keeps its f16 weights in range for any finite factors.
+constexpr float kRatioMax = 146.0f;           // 65504 / 448, the largest e4m3 magnitude
+constexpr float kRatioMin = 1.0f / 4096.0f;   // products of the smallest codes stay near 2^-21
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ void hmul2x4(uint4& v, uint32_t f) {
+  v.x = hmul2(v.x, f);
+  v.y = hmul2(v.y, f);
+  v.z = hmul2(v.z, f);
+  v.w = hmul2(v.w, f);
+}
+__device__ __forceinline__ uint32_t half2_bits(float x) {
+  const __half2 h = __float2half2_rn(x);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// The factors of NB consecutive 16-key blocks a thread applies in each 128-key tile of an
+// item (logical blocks b0 + 8 j .. b0 + 8 j + NB - 1 in tile j), loaded ahead of their use:
+// the table entries two tiles ahead, the factors one tile ahead, so the tile loop never waits
+// for either.  Blocks past the last one with visible keys read nothing and take `dflt`.
+template <int NB>
+struct FactorPipe {
+  const int32_t* trow;
+  const float* f;
+  int64_t H;
+  int kvh, b0, lim;
+  float dflt;
+  int tb[NB];
+  float cur[NB], nxt[NB];
+  __device__ __forceinline__ void tables(int j) {
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      const int lb = b0 + 8 * j + q;
+      tb[q] = lb < lim ? trow[lb] : -1;
+    }
+  }
+  __device__ __forceinline__ void factors() {
+#pragma unroll
+    for (int q = 0; q < NB; ++q) nxt[q] = tb[q] >= 0 ? f[tb[q] * H + kvh] : dflt;
+  }
+  // item start: the factors of tile 0 and the table entries of tile 1
+  __device__ __forceinline__ void start() {
+    tables(0);
+    factors();
+    tables(1);
+  }
+  // top of tile j: cur = the factors of tile j
+  __device__ __forceinline__ void advance(int j) {
+#pragma unroll
+    for (int q = 0; q < NB; ++q) cur[q] = nxt[q];
+    factors();
+    tables(j + 2);
+  }
+};
+
+// The item's V reference: the factor of its first block (1 when it has no visible keys).
+__device__ __forceinline__ float v_reference(const VarlenMeta& m, const int32_t* trow,
+                                             const Item& I) {
+  const int b0 = I.kv0 / 16;
+  return b0 < I.nblk_vis ? m.v_bscales[(int64_t)trow[b0] * m.num_kv_heads + I.kvh] : 1.f;
+}
+
+template <bool PB>
 __device__ void fp8_converter(const Ctx& c, const TcParams& p, int n_items) {
   const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) - kFirstConvWarp;
   uint32_t kv = 0, it_cnt = 0;
   for (int idx; (idx = item_of(c, (int)it_cnt)) < n_items; ++it_cnt) {
     const Item I = load_item(p, idx, c.rank);
+    FactorPipe<2> vf;  // PB: the V factors of blocks 2w, 2w + 1 of each tile
+    float rref = 1.f;  // PB: 1 / the item's V reference
+    bool out_of_range = false;  // PB: a ratio outside [kRatioMin, kRatioMax]
+    if constexpr (PB) {
+      const int32_t* trow = p.m.block_tables + (int64_t)I.s * p.m.max_blocks;
+      const float vref = v_reference(p.m, trow, I);
+      rref = __frcp_rn(vref);
+      vf = FactorPipe<2>{trow, p.m.v_bscales, p.m.num_kv_heads, I.kvh, I.kv0 / 16 + 2 * w,
+                         I.nblk_vis, vref};
+      vf.start();
+    }
     {  // Q: this warp's quarter of the 128 x 128 bf16 tile, 16 chunks of 16 bytes per lane
       const uint32_t qb = it_cnt & 1u;
       if (!__all_sync(kFull, wait_bar(c, B_QFULL + qb, (it_cnt >> 1) & 1u))) return;
@@ -679,6 +763,15 @@ __device__ void fp8_converter(const Ctx& c, const TcParams& p, int n_items) {
       if (lane == 0) arrive_leader(c.bar + B_QCONV + qb);
     }
     for (int j = 0; j < I.ntiles; ++j, ++kv) {
+      uint32_t vr2a = 0, vr2b = 0;  // PB: the ratios of V blocks 2w, 2w + 1 (f16 pairs)
+      if constexpr (PB) {
+        vf.advance(j);
+        const float r0 = vf.cur[0] * rref, r1 = vf.cur[1] * rref;
+        out_of_range |= !(r0 >= kRatioMin && r0 <= kRatioMax && r1 >= kRatioMin &&
+                          r1 <= kRatioMax);
+        vr2a = half2_bits(r0);
+        vr2b = half2_bits(r1);
+      }
       {  // K block w
         const uint32_t st = kv % kStagesK;
         if (!__all_sync(kFull, wait_bar(c, B_KFULL + st, (kv / kStagesK) & 1u))) return;
@@ -726,6 +819,11 @@ __device__ void fp8_converter(const Ctx& c, const TcParams& p, int n_items) {
             widen4(src.y, lo.z, lo.w);
             widen4(src.z, hi.x, hi.y);
             widen4(src.w, hi.z, hi.w);
+            if constexpr (PB) {
+              const uint32_t r2 = (i >> 1) ? vr2b : vr2a;
+              hmul2x4(lo, r2);
+              hmul2x4(hi, r2);
+            }
           }
           uint8_t* row = slot + b * 2048 + r * 128;
           *reinterpret_cast<uint4*>(row + (((2 * L) ^ (r & 7)) << 4)) = lo;
@@ -735,6 +833,10 @@ __device__ void fp8_converter(const Ctx& c, const TcParams& p, int n_items) {
         __syncwarp();
         if (lane == 0) arrive_leader(c.bar + B_VCONV + st);
       }
+    }
+    if (out_of_range && lane == 0) {  // (uniform across the warp)
+      const int pi = idx / p.m.num_kv_heads;  // the plan's 256-row item (all its kv heads)
+      if (atomicCAS(p.redo_flags + pi, 0, 1) == 0) p.redo_list[atomicAdd(p.redo_count, 1)] = pi;
     }
   }
 }
@@ -747,6 +849,7 @@ __device__ __forceinline__ void pair_sync(int quad) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
 }
 
+template <bool PB>
 __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int n_items) {
   const VarlenMeta& m = p.m;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -778,7 +881,19 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     }
     float m_ref = -INFINITY, l = 0.f;
     const float sl = head_scale(m.k_scales, I.kvh, p.scale_log2);  // K = k_scales[g] * pool
+    // PB: the K factors of this thread's four blocks (64 columns) in each tile, and the V
+    // reference the converters divided the factors by
+    FactorPipe<4> kf;
+    float vref = 1.f;
+    if constexpr (PB) {
+      const int32_t* trow = m.block_tables + (int64_t)I.s * m.max_blocks;
+      kf = FactorPipe<4>{trow, m.k_bscales, m.num_kv_heads, I.kvh, I.kv0 / 16 + 4 * hf,
+                         I.nblk_vis, 1.f};
+      kf.start();
+      vref = v_reference(m, trow, I);
+    }
     for (int j = 0; j < I.ntiles; ++j) {
+      if constexpr (PB) kf.advance(j);
       const uint32_t s = kv + j, b = buf_of(s);
       const uint32_t sbase = tmem + lane_addr + col_s(b) + col0;  // this thread's S / P columns
       // debug_stall (tests only): the wait names a barrier nothing arrives on, so it runs out
@@ -812,17 +927,33 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
         for (int i = 0; i < 64; ++i) x[i] = (i >= a && i < bnd) ? x[i] : -INFINITY;
       }
       float mx[8];
+      float sq[4];  // PB: the score scale of each 16-column block, sl times its K factor
+      float mine;
+      if constexpr (PB) {
+        // the factors are positive, so a block's max commutes with its scale: the max of
+        // the scaled scores, exchanged as such
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = x[k];
+        for (int q = 0; q < 4; ++q) sq[q] = sl * kf.cur[q];
 #pragma unroll
-      for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-      const float mine = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int k = 0; k < 8; ++k) mx[k] = x[8 * k];
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i & 7) mx[i >> 3] = fmaxf(mx[i >> 3], x[i]);
+        mine = fmaxf(fmaxf(fmaxf(mx[0], mx[1]) * sq[0], fmaxf(mx[2], mx[3]) * sq[1]),
+                     fmaxf(fmaxf(mx[4], mx[5]) * sq[2], fmaxf(mx[6], mx[7]) * sq[3]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+        for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+        mine = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      }
       // the row max over both column halves; a failed wait travels as kBadMax
       xchg[hf * 128 + r] = bad ? __uint_as_float(kBadMax) : mine;
       pair_sync(quad);
       const float other = xchg[(hf ^ 1) * 128 + r];
-      const float mt = fmaxf(mine, other) * sl;
+      const float mt = PB ? fmaxf(mine, other) : fmaxf(mine, other) * sl;
       const bool leave = __any_sync(kFull, bad || __float_as_uint(other) == kBadMax);
       pair_sync(quad);  // both read before either writes again
       if (leave) return;
@@ -838,13 +969,18 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
       // weights, and p rounded to f16 for the P V MMAs
       const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
       const uint64_t sl2 = f2_pack(sl, sl), nb2 = f2_pack(nbase, nbase);
+      uint64_t sq2[4] = {sl2, sl2, sl2, sl2};
+      if constexpr (PB) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sq2[q] = f2_pack(sq[q], sq[q]);
+      }
       uint32_t ph[32];
       {
         uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           float a, bb;
-          f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sl2, nb2), a, bb);
+          f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), PB ? sq2[e >> 3] : sl2, nb2), a, bb);
           a = fast_exp2(a);
           bb = fast_exp2(bb);
           rs2[e & 3] = f2_add(rs2[e & 3], f2_pack(a, bb));
@@ -914,7 +1050,8 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
     }
     if (m.lse && hf == 0 && valid)
       m.lse[(int64_t)h * m.num_tokens + t] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-    const float inv = l > 0.f ? o_scale * head_scale(m.v_scales, I.kvh, m.v_scale) / l : 0.f;
+    const float inv =
+        l > 0.f ? o_scale * head_scale(m.v_scales, I.kvh, m.v_scale) * vref / l : 0.f;
     __nv_bfloat16* dst =
         reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)t * m.num_heads + h) * kD + col0;
     // rows start 256 bytes apart and halves at 0 / 128: 32-byte aligned when the output is
@@ -955,10 +1092,11 @@ __device__ void softmax_role(const Ctx& c, const TcParams& p, uint32_t tmem, int
   }
 }
 
-template <bool FP8>
+template <bool FP8, bool PB>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_prefill(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const TcParams p) {
+  static_assert(!PB || FP8, "per-block factors are for e4m3 pools");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -1031,7 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     if constexpr (FP8)
-      fp8_converter(c, p, n_items);
+      fp8_converter<PB>(c, p, n_items);
     else
       v_converter(c, p, n_items);
     tc_fence_before();
@@ -1076,7 +1214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
     else
       asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
-    softmax_role(c, p, tmem, n_items);
+    softmax_role<PB>(c, p, tmem, n_items);
     tc_fence_before();
     cluster_sync();
   }
@@ -1087,7 +1225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_tc_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const TcParams& p, int grid, cudaStream_t stream) {
   if (grid < 2) grid = 2;
-  auto kern = p.kv_fp8 ? k_tc_prefill<true> : k_tc_prefill<false>;
+  // per-block factors: e4m3 pools only (the caller checks)
+  auto kern = !p.kv_fp8 ? k_tc_prefill<false, false>
+              : p.m.k_bscales ? k_tc_prefill<true, true> : k_tc_prefill<true, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // pairs of CTAs (a cluster of two SMs) run the 2-SM MMAs

@@ -496,7 +496,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
   const bool fast = mma_path(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
   const bool fast8 =
       mma_path_fp8(q_dtype, kv_dtype, head_dim, block_size, q, k_blocks, v_blocks, out);
-  // per-block factors are applied by the e4m3 warp-MMA kernel only (every sequence runs there)
+  // per-block factors: the e4m3 kernels only (warp-MMA, and tcgen05 for prefill-class rows)
   if (per_block && !fast8) return PA_EUNSUPPORTED;
   // prefill-class sequences (more than 64 query rows per kv head) go to the tcgen05 kernel:
   // head size 128 and a GQA group that divides the 128-row tile; bf16 or e4m3 pools
@@ -505,7 +505,7 @@ static pa_status varlen_impl(const void* q, const void* k_blocks, const void* v_
   const int64_t max_rows = (num_tokens - (num_seqs > 0 ? num_seqs : 1) + 1) * m.group;
   L.use_tc = (fast || fast8) && head_dim == 128 && m.group <= 128 && (128 % m.group) == 0 &&
              aligned(q, 16) && max_rows > L.tc_min_rows && scale > 0.f && tc_enabled() &&
-             !(flags & PA_FLAG_BITWISE) && !per_block;
+             !(flags & PA_FLAG_BITWISE);
 
   // the tcgen05 kernel's launch: one CTA per SM, pairs, never more than there are items
   const int64_t tc_work = L.tc_cap * num_kv_heads;

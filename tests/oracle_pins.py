@@ -846,7 +846,7 @@ def pin_per_block_scatter():
     # writes to: ignored
     written = {int(x) // b for x in slots}
     unwritten = [i for i in range(NB) if i not in written]
-    for bad in (0.0, -1.0, float("inf"), float("nan")):
+    for bad in (0.0, -1.0, float("inf"), float("nan"), 1e-39):
         ks2 = ks.clone()
         ks2[int(slots[0]) // b, 1] = bad
         kb = torch.zeros((NB, b, Hkv, D), dtype=torch.float32)
@@ -887,7 +887,7 @@ def pin_per_block_attention():
     # a bad factor of a block some sequence reads: EINVAL; of a block no table names: ignored
     used = {int(table[s, j]) for s, n in enumerate(lens) for j in range((n + 15) // 16)}
     unused = [i for i in range(NB) if i not in used]
-    for bad in (0.0, float("nan")):
+    for bad in (0.0, float("nan"), 1e-39):
         vs2 = vs.clone()
         vs2[int(table[1, 0]), 1] = bad
         st, _, _ = oracle.varlen_attention(q, kb8, vb8, k_block_scales=ks, v_block_scales=vs2,
