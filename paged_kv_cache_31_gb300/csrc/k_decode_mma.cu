@@ -128,9 +128,9 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
 // O is rescaled when it rises) and times 2^15, multiplies the block's fp32 weights where they
 // are rounded to f16 for P V, and the reference over 2^15 multiplies the warp's O where the
 // warps are merged: the f16 weights stay in [0, 2^15] whatever the factors' magnitude (the
-// row sum keeps the unscaled weights).  Lane 0 copies both factors into the stage's slot with cp.async when it issues
-// the block's TMA copies, and the stage's barrier (two arrivals) completes only when they
-// have landed too.
+// row sum keeps the unscaled weights).  Lane 0 copies both factors into the stage's slot
+// with cp.async when it issues the block's TMA copies, and the stage's barrier (two
+// arrivals) completes only when they have landed too.
 template <int D, int NW, int NS, bool SPLIT, bool FP8, bool PB = false>
 __global__ void __launch_bounds__(NW * 32, 2)
     k_mma16(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
