@@ -420,6 +420,43 @@ def l2_flush_buffer(dev):
             torch.zeros(64 << 20, dtype=torch.float32, device=dev))
 
 
+def prefill_back_to_back(pa, dev, args, peaks, stream, n, copies=6):
+    """The prefill chunks as consecutive calls of a serving loop: `copies` copies of the
+    workload's inputs (q, pools, output; together several times L2) taken in turn, with no
+    flush between the calls.  No call finds its inputs in L2, and, as between the steps of a
+    serving loop, each call's planner overlaps the previous call's tail."""
+    import dataclasses
+
+    import torch
+
+    from paged_kv_cache_31_gb300 import workloads
+
+    base = workloads.prefill_chunks(seed=args.seed, device=dev)
+    runners = []
+    for _ in range(copies):
+        w = dataclasses.replace(base, q=base.q.clone(), k_blocks=base.k_blocks.clone(),
+                                v_blocks=base.v_blocks.clone())
+        runners.append(Runner(pa, w))
+    per_copy = sum(t.numel() * t.element_size()
+                   for t in (base.q, base.k_blocks, base.v_blocks, runners[0].out))
+    for r in runners:
+        r.attention()
+        r.attention()
+    nxt = [0]
+
+    def call():
+        runners[nxt[0]].attention()
+        nxt[0] = (nxt[0] + 1) % copies
+
+    ms = time_calls(call, n * copies, stream)
+    fl = attn_flops(base)
+    assert pa.pa_device_status() == pa.PA_OK
+    return {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+            "frac_of_bf16_peak": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "l2": f"{copies} copies of the inputs ({copies * per_copy / 1e6:.0f} MB, "
+                  "larger than L2) taken in turn, calls back to back"}
+
+
 def fp8_decode(pa, dev, args, peaks, stream, n):
     """The decode batch over fp8 (e4m3) pools with dequantisation scales: half the K/V bytes
     of the bf16 batch, 303 MB of codes (larger than L2, so no flush)."""
@@ -542,6 +579,9 @@ def secondary(pa, dev, args, peaks, stream):
     }
     assert pa.pa_device_status() == pa.PA_OK
     del w3, r3, wp, wd, rp, rd, rb
+    torch.cuda.empty_cache()
+    res["mixed"]["prefill"]["back_to_back"] = prefill_back_to_back(pa, dev, args, peaks,
+                                                                   stream, n)
     torch.cuda.empty_cache()
 
     res["fp8_decode"] = fp8_decode(pa, dev, args, peaks, stream, n)
