@@ -656,6 +656,30 @@ def secondary(pa, dev, args, peaks, stream):
     res["tiny_mixed"] = {"workload": w1.name, "tokens": w1.num_tokens, "us_per_call": ms1a * 1e3,
                          "us_per_step": ms1s * 1e3, "dtype": "f32"}
     del w1, r1
+
+    # the two-state merge of chunked-context prefill: 16384 query tokens x 32 heads x 128,
+    # bf16 states with fp32 lse (410 MB moved, larger than L2, so no flush)
+    T, H, D = 16384, 32, 128
+    g = torch.Generator(device=dev).manual_seed(args.seed + 11)
+    po = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    so = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    pl = torch.randn((H, T), generator=g, device=dev) * 4
+    sl = torch.randn((H, T), generator=g, device=dev) * 4
+    mo, ml = torch.empty_like(po), torch.empty_like(pl)
+
+    def merge():
+        pa.pa_merge_attn_states(mo, ml, po, pl, so, sl)
+
+    for _ in range(3):
+        merge()
+    msm = time_calls(merge, n, stream)
+    assert pa.pa_device_status() == pa.PA_OK
+    mb = 3 * T * H * D * 2 + 3 * H * T * 4
+    res["merge_attn_states"] = {"workload": f"merge-{T}x{H}x{D}-bf16", "bytes": mb, "ms": msm,
+                                "gbs": mb / (msm * 1e-3) / 1e9,
+                                "frac_of_hbm": mb / (msm * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                "l2": "states larger than L2, no flush"}
+    del po, so, pl, sl, mo, ml
     return res
 
 

@@ -238,8 +238,9 @@ pa_status pa_varlen_forward(const void* q, const void* k_blocks, const void* v_b
  *          the pool's codes widen exactly to f16; on the tensor-core path q (bf16) enters the
  *          products as f16, so q entries must lie within f16's range (|q| <= 65504; entries
  *          below 2^-14 keep f16's subnormal precision), and the softmax weights enter the PV
- *          product as f16 (2^-11 relative).  fp8 pools take the warp-MMA kernel for head size
- *          128 with 16-position blocks and the generic kernel otherwise.
+ *          product as f16 (2^-11 relative).  fp8 pools take the tensor-core kernels for head
+ *          size 128 with 16-position blocks (warp-MMA for decode tokens, tcgen05 for prefill
+ *          chunks, as bf16 pools do) and the generic kernel otherwise.
  *   flags  0, or PA_FLAG_BITWISE: every sequence runs on the 16-row warp-MMA kernel (bf16 or
  *          fp8 pools, head size 64 / 128, 16-position blocks), including prefill-class
  *          sequences that would otherwise take the tensor-core prefill kernel.  That kernel

@@ -142,6 +142,73 @@ __global__ void __launch_bounds__(256)
   if (out_lse && lane == 0) out_lse[li] = logf(ose) + mx;
 }
 
+// The same merge with 16-byte accesses: a (token, head) row of head_dim values is C chunks
+// of 16 bytes (C a power of two <= 256), and a thread takes CPT of them, chunks c and
+// c + C / CPT, ... (so a CTA of 256 threads holds 256 CPT / C whole rows, and each thread
+// has 2 CPT loads in flight).  Rows are taken head-major (row = h * num_tokens + t): the rows
+// of a CTA read and write consecutive lse entries of one head.  Per element it computes what
+// k_merge_attn_states does.
+template <typename T, int CPT>
+__global__ void __launch_bounds__(256)
+    k_merge_attn_states_v(T* __restrict__ out, float* __restrict__ out_lse,
+                          const T* __restrict__ prefix_out, const float* __restrict__ prefix_lse,
+                          const T* __restrict__ suffix_out, const float* __restrict__ suffix_lse,
+                          int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                          int64_t prefix_tokens, int log2_tpr, const int* status) {
+  if (status_set(status)) return;
+  constexpr int kE = 16 / (int)sizeof(T);  // values per chunk
+  const int tpr = 1 << log2_tpr;           // threads per row
+  const int c = threadIdx.x & (tpr - 1);
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> log2_tpr;
+  if (row >= num_tokens * num_heads) return;
+  const int h = (int)(row / num_tokens);
+  const int64_t t = row - (int64_t)h * num_tokens;
+  const int64_t base = (t * num_heads + h) * head_dim;
+  const int64_t li = row;  // h * num_tokens + t
+  if (t >= prefix_tokens) {
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+      const int64_t off = base + (int64_t)(c + k * tpr) * kE;
+      *reinterpret_cast<uint4*>(out + off) = *reinterpret_cast<const uint4*>(suffix_out + off);
+    }
+    if (out_lse && c == 0) out_lse[li] = suffix_lse[li];
+    return;
+  }
+  // all loads in flight together (the states do not wait for the lse values)
+  uint4 pv[CPT], sv[CPT];
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const int64_t off = base + (int64_t)(c + k * tpr) * kE;
+    pv[k] = *reinterpret_cast<const uint4*>(prefix_out + off);
+    sv[k] = *reinterpret_cast<const uint4*>(suffix_out + off);
+  }
+  float pl = prefix_lse[li], sl = suffix_lse[li];
+  if (isinf(pl)) pl = -INFINITY;
+  if (isinf(sl)) sl = -INFINITY;
+  const float mx = fmaxf(pl, sl);
+  if (isinf(mx)) {
+#pragma unroll
+    for (int k = 0; k < CPT; ++k)
+      *reinterpret_cast<uint4*>(out + base + (int64_t)(c + k * tpr) * kE) = pv[k];
+    if (out_lse && c == 0) out_lse[li] = mx;
+    return;
+  }
+  const float pse = expf(pl - mx), sse = expf(sl - mx);
+  const float ose = pse + sse;
+  const float ps = pse / ose, ss = sse / ose;
+#pragma unroll
+  for (int k = 0; k < CPT; ++k) {
+    const T* pe = reinterpret_cast<const T*>(&pv[k]);
+    const T* se = reinterpret_cast<const T*>(&sv[k]);
+    uint4 r;
+    T* re = reinterpret_cast<T*>(&r);
+#pragma unroll
+    for (int i = 0; i < kE; ++i) re[i] = from_f32<T>(to_f32(pe[i]) * ps + to_f32(se[i]) * ss);
+    *reinterpret_cast<uint4*>(out + base + (int64_t)(c + k * tpr) * kE) = r;
+  }
+  if (out_lse && c == 0) out_lse[li] = logf(ose) + mx;
+}
+
 }  // namespace
 
 cudaError_t launch_splitkv_reduce(void* out, int out_bf16, const float* max_logits,
@@ -182,6 +249,41 @@ cudaError_t launch_merge_attn_states(void* out, float* out_lse, const void* pref
                                      int bf16, int* status, cudaStream_t stream) {
   const int64_t warps = num_tokens * num_heads;
   if (warps <= 0) return cudaSuccess;
+  // whole 16-byte chunks per row, a power of two of them, and 16-byte aligned tensors: the
+  // vectorised kernel (2.5 -> 6+ TB/s on bf16 states of head size 128)
+  const int row_bytes = head_dim * (bf16 ? 2 : 4);
+  const int chunks = row_bytes / 16;
+  const bool vec = row_bytes % 16 == 0 && chunks >= 1 && chunks <= 256 &&
+                   (chunks & (chunks - 1)) == 0 &&
+                   ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(prefix_out) |
+                     reinterpret_cast<uintptr_t>(suffix_out)) & 15) == 0;
+  if (vec) {
+    // two chunks per thread when the row has two or more
+    const int cpt = chunks >= 2 ? 2 : 1;
+    const int tpr = chunks / cpt;
+    const int lg = 31 - __builtin_clz((unsigned)tpr);
+    const int64_t vgrid = (warps * tpr + 255) / 256;
+    auto go = [&](auto kern, auto* o, const auto* po, const auto* so) {
+      kern<<<(unsigned)vgrid, 256, 0, stream>>>(o, out_lse, po, prefix_lse, so, suffix_lse,
+                                                num_tokens, num_heads, head_dim, prefix_tokens,
+                                                lg, status);
+    };
+    using B = __nv_bfloat16;
+    if (bf16) {
+      if (cpt == 2)
+        go(k_merge_attn_states_v<B, 2>, (B*)out, (const B*)prefix_out, (const B*)suffix_out);
+      else
+        go(k_merge_attn_states_v<B, 1>, (B*)out, (const B*)prefix_out, (const B*)suffix_out);
+    } else {
+      if (cpt == 2)
+        go(k_merge_attn_states_v<float, 2>, (float*)out, (const float*)prefix_out,
+           (const float*)suffix_out);
+      else
+        go(k_merge_attn_states_v<float, 1>, (float*)out, (const float*)prefix_out,
+           (const float*)suffix_out);
+    }
+    return cudaGetLastError();
+  }
   const int64_t grid = (warps + 7) / 8;
   if (bf16)
     k_merge_attn_states<__nv_bfloat16><<<(unsigned)grid, 256, 0, stream>>>(

@@ -297,10 +297,14 @@ def test_splitkv_long_context_full_sampled(pa):
 # merge_attn_states
 
 
+# head sizes whose rows are a power of two of 16-byte chunks take the vectorised kernel (64,
+# 128, 256); 80 (and an output 2 bytes off a 16-byte boundary) the one with a warp per row
+@pytest.mark.parametrize("D,misaligned", [(128, False), (64, False), (256, False), (80, False),
+                                          (128, True)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_merge_attn_states(pa, dtype):
+def test_merge_attn_states(pa, dtype, D, misaligned):
     g = torch.Generator().manual_seed(77)
-    T, H, D = 300, 8, 128
+    T, H = 300, 8
     po = torch.randn((T, H, D), generator=g).to(dtype)
     so = torch.randn((T, H, D), generator=g).to(dtype)
     pl = torch.randn((H, T), generator=g) * 3
@@ -311,7 +315,10 @@ def test_merge_attn_states(pa, dtype):
     for i, (a, b) in enumerate(specials):
         pl[i % H, i], sl[i % H, i] = a, b
     for ptc in (-1, 250):
-        out = torch.empty_like(po, device=DEV)
+        if misaligned:  # a view one element into a larger buffer
+            out = torch.empty(T * H * D + 1, dtype=dtype, device=DEV)[1:].view(T, H, D)
+        else:
+            out = torch.empty_like(po, device=DEV)
         olse = torch.empty((H, T), device=DEV)
         pa.pa_merge_attn_states(out, olse, po.to(DEV), pl.to(DEV), so.to(DEV), sl.to(DEV), ptc)
         assert pa.pa_device_status() == pa.PA_OK
