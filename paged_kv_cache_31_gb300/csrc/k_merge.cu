@@ -80,19 +80,30 @@ __global__ void __launch_bounds__(kReduceWarps * 32)
   for (int i = 0; i < kReduceWarps; ++i) W += s_red[i];
   const float inv = 1.f / W;
 
-  // weighted sum: warp `warp` takes partitions warp, warp + 8, ...; lanes take 4 dims each
+  // weighted sum: warp `warp` takes partitions warp, warp + 8, ... in that order; lanes take
+  // 4 dims each.  Four partitions' loads are issued before their products (a grid of one
+  // CTA per (sequence, head) is too small to hide the latency of one load at a time); a
+  // partition without mass adds exactly nothing, whatever its tmp_out holds
+  auto add = [](float4& acc, float wp, float4 v) {
+    if (!(wp > 0.f)) v = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc.x += wp * v.x;
+    acc.y += wp * v.y;
+    acc.z += wp * v.z;
+    acc.w += wp * v.w;
+  };
   for (int d0 = lane * 4; d0 < D; d0 += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = warp; p < np; p += kReduceWarps) {
-      const float wp = w[p];
-      if (wp > 0.f) {
-        const float4 v = *reinterpret_cast<const float4*>(tmp_out + (base + p) * D + d0);
-        acc.x += wp * v.x;
-        acc.y += wp * v.y;
-        acc.z += wp * v.z;
-        acc.w += wp * v.w;
-      }
+    int p = warp;
+    for (; p + 3 * kReduceWarps < np; p += 4 * kReduceWarps) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[u] = *reinterpret_cast<const float4*>(tmp_out + (base + p + u * kReduceWarps) * D + d0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) add(acc, w[p + u * kReduceWarps], v[u]);
     }
+    for (; p < np; p += kReduceWarps)
+      add(acc, w[p], *reinterpret_cast<const float4*>(tmp_out + (base + p) * D + d0));
     *reinterpret_cast<float4*>(part + warp * D + d0) = acc;
   }
   __syncthreads();
