@@ -773,6 +773,65 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// One token's row in the quantising scatter, 8 consecutive values per lane (one kv head:
+// head_dim is a multiple of 8), 16-byte loads of bf16 rows; the same per-element arithmetic
+// as the one-value-per-lane loop of k_scatter_convert.
+template <typename TS, int DST>
+__device__ __forceinline__ void scatter_row_vec8(
+    const TS* __restrict__ k, const TS* __restrict__ v, void* __restrict__ kb,
+    void* __restrict__ vb, int64_t src, int64_t dst, int32_t slot, int64_t row_elems,
+    float k_scale, float v_scale, const float* __restrict__ k_scales,
+    const float* __restrict__ v_scales, const float* __restrict__ kbs,
+    const float* __restrict__ vbs, int32_t block_size, int32_t head_dim, int32_t hkv, int lane) {
+  for (int64_t i = (int64_t)lane * 8; i < row_elems; i += 256) {
+    const int g = (int)(i / head_dim);
+    float ks = k_scales ? __ldg(k_scales + g) : k_scale;
+    float vs = v_scales ? __ldg(v_scales + g) : v_scale;
+    if (kbs) {
+      const int64_t f = (int64_t)(slot / block_size) * hkv + g;
+      ks = __ldg(kbs + f);
+      vs = __ldg(vbs + f);
+    }
+    const uint4 kw = *reinterpret_cast<const uint4*>(k + src + i);
+    const uint4 vw = *reinterpret_cast<const uint4*>(v + src + i);
+    const TS* ke = reinterpret_cast<const TS*>(&kw);
+    const TS* ve = reinterpret_cast<const TS*>(&vw);
+    float a[8], b[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      a[e] = __fdiv_rn(to_f32(ke[e]), ks);
+      b[e] = __fdiv_rn(to_f32(ve[e]), vs);
+    }
+    if constexpr (DST == PA_FP8_E4M3) {
+      uint2 ko, vo;
+      ko.x = f32x2_to_e4m3x2(a[0], a[1]) | ((uint32_t)f32x2_to_e4m3x2(a[2], a[3]) << 16);
+      ko.y = f32x2_to_e4m3x2(a[4], a[5]) | ((uint32_t)f32x2_to_e4m3x2(a[6], a[7]) << 16);
+      vo.x = f32x2_to_e4m3x2(b[0], b[1]) | ((uint32_t)f32x2_to_e4m3x2(b[2], b[3]) << 16);
+      vo.y = f32x2_to_e4m3x2(b[4], b[5]) | ((uint32_t)f32x2_to_e4m3x2(b[6], b[7]) << 16);
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(kb) + dst + i) = ko;
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(vb) + dst + i) = vo;
+    } else if constexpr (DST == PA_BF16) {
+      uint4 ko, vo;
+      __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(&ko);
+      __nv_bfloat16* vr = reinterpret_cast<__nv_bfloat16*>(&vo);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        kr[e] = __float2bfloat16_rn(a[e]);
+        vr[e] = __float2bfloat16_rn(b[e]);
+      }
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(kb) + dst + i) = ko;
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(vb) + dst + i) = vo;
+    } else {
+      float* kf = static_cast<float*>(kb) + dst + i;
+      float* vf = static_cast<float*>(vb) + dst + i;
+      *reinterpret_cast<float4*>(kf) = make_float4(a[0], a[1], a[2], a[3]);
+      *reinterpret_cast<float4*>(kf + 4) = make_float4(a[4], a[5], a[6], a[7]);
+      *reinterpret_cast<float4*>(vf) = make_float4(b[0], b[1], b[2], b[3]);
+      *reinterpret_cast<float4*>(vf + 4) = make_float4(b[4], b[5], b[6], b[7]);
+    }
+  }
+}
+
 // Scatter with conversion ("paged_attention_v2_pytorch.py": the pool holds K / k_scale and
 // V / v_scale in kv_cache_dtype).  One warp per token; every element is divided by its scale
 // in fp32 (IEEE division, as written) and rounded to the pool's type to nearest even, fp8
@@ -812,58 +871,11 @@ __global__ void __launch_bounds__(256)
   const int32_t slot = slots[t];
   const int64_t dst = (int64_t)slot * row_elems, src = t * row_elems;
   if constexpr (sizeof(TS) == 2) {
-   if (vec8) {
-    // 8 consecutive values per lane (one kv head: head_dim is a multiple of 8), 16-byte
-    // loads of bf16 rows; the same per-element arithmetic as the loop below
-    for (int64_t i = (int64_t)lane * 8; i < row_elems; i += 256) {
-      const int g = (int)(i / head_dim);
-      float ks = k_scales ? __ldg(k_scales + g) : k_scale;
-      float vs = v_scales ? __ldg(v_scales + g) : v_scale;
-      if (kbs) {
-        const int64_t f = (int64_t)(slot / block_size) * hkv + g;
-        ks = __ldg(kbs + f);
-        vs = __ldg(vbs + f);
-      }
-      const uint4 kw = *reinterpret_cast<const uint4*>(k + src + i);
-      const uint4 vw = *reinterpret_cast<const uint4*>(v + src + i);
-      const TS* ke = reinterpret_cast<const TS*>(&kw);
-      const TS* ve = reinterpret_cast<const TS*>(&vw);
-      float a[8], b[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        a[e] = __fdiv_rn(to_f32(ke[e]), ks);
-        b[e] = __fdiv_rn(to_f32(ve[e]), vs);
-      }
-      if constexpr (DST == PA_FP8_E4M3) {
-        uint2 ko, vo;
-        ko.x = f32x2_to_e4m3x2(a[0], a[1]) | ((uint32_t)f32x2_to_e4m3x2(a[2], a[3]) << 16);
-        ko.y = f32x2_to_e4m3x2(a[4], a[5]) | ((uint32_t)f32x2_to_e4m3x2(a[6], a[7]) << 16);
-        vo.x = f32x2_to_e4m3x2(b[0], b[1]) | ((uint32_t)f32x2_to_e4m3x2(b[2], b[3]) << 16);
-        vo.y = f32x2_to_e4m3x2(b[4], b[5]) | ((uint32_t)f32x2_to_e4m3x2(b[6], b[7]) << 16);
-        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(kb) + dst + i) = ko;
-        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(vb) + dst + i) = vo;
-      } else if constexpr (DST == PA_BF16) {
-        uint4 ko, vo;
-        __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(&ko);
-        __nv_bfloat16* vr = reinterpret_cast<__nv_bfloat16*>(&vo);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          kr[e] = __float2bfloat16_rn(a[e]);
-          vr[e] = __float2bfloat16_rn(b[e]);
-        }
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(kb) + dst + i) = ko;
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(vb) + dst + i) = vo;
-      } else {
-        float* kf = static_cast<float*>(kb) + dst + i;
-        float* vf = static_cast<float*>(vb) + dst + i;
-        *reinterpret_cast<float4*>(kf) = make_float4(a[0], a[1], a[2], a[3]);
-        *reinterpret_cast<float4*>(kf + 4) = make_float4(a[4], a[5], a[6], a[7]);
-        *reinterpret_cast<float4*>(vf) = make_float4(b[0], b[1], b[2], b[3]);
-        *reinterpret_cast<float4*>(vf + 4) = make_float4(b[4], b[5], b[6], b[7]);
-      }
+    if (vec8) {
+      scatter_row_vec8<TS, DST>(k, v, kb, vb, src, dst, slot, row_elems, k_scale, v_scale,
+                                k_scales, v_scales, kbs, vbs, block_size, head_dim, hkv, lane);
+      return;
     }
-    return;
-   }
   }
   for (int64_t i = lane; i < row_elems; i += 32) {
     // one scale per kv head (head i / head_dim of the row), or per (block, kv head), when the
