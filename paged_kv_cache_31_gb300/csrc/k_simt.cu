@@ -64,31 +64,52 @@ __global__ void __launch_bounds__(128) k_simt(const SimtParams p) {
     acc[i] = 0.f;
   }
   float mx = -INFINITY, den = 0.f;
-  for (int j = start; j < end; ++j) {
-    const int64_t blk = row[j / m.block_size];
-    const int64_t base = ((blk * m.block_size + j % m.block_size) * m.num_kv_heads + g) * D;
-    float dot = 0.f;
+  // KC positions at a time: their K and V rows are all requested before the first is used,
+  // so a chunk waits for memory once instead of once per position; each position is then
+  // folded exactly as one at a time
+  constexpr int KC = DPL >= 8 ? 2 : 16 / DPL;
+  for (int j0 = start; j0 < end; j0 += KC) {
+    float kr[KC][DPL], vr[KC][DPL];
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) {
-      const int d = lane + 32 * i;
-      if (d < D) dot += qr[i] * to_f32(kb[base + d]);
+    for (int u = 0; u < KC; ++u) {
+      const int j = j0 + u;
+      if (j < end) {
+        const int64_t blk = row[j / m.block_size];
+        const int64_t base = ((blk * m.block_size + j % m.block_size) * m.num_kv_heads + g) * D;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) {
+          const int d = lane + 32 * i;
+          kr[u][i] = d < D ? to_f32(kb[base + d]) : 0.f;
+          vr[u][i] = d < D ? to_f32(vb[base + d]) : 0.f;
+        }
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
-    const float sc = dot * psc;
-    if (sc > mx) {
-      const float r = expf(mx - sc);
-      den *= r;
+    for (int u = 0; u < KC; ++u) {
+      if (j0 + u >= end) break;
+      float dot = 0.f;
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) acc[i] *= r;
-      mx = sc;
-    }
-    const float e = expf(sc - mx);
-    den += e;
+      for (int i = 0; i < DPL; ++i) {
+        const int d = lane + 32 * i;
+        if (d < D) dot += qr[i] * kr[u][i];
+      }
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) {
-      const int d = lane + 32 * i;
-      if (d < D) acc[i] += e * to_f32(vb[base + d]);
+      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
+      const float sc = dot * psc;
+      if (sc > mx) {
+        const float r = expf(mx - sc);
+        den *= r;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] *= r;
+        mx = sc;
+      }
+      const float e = expf(sc - mx);
+      den += e;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) {
+        const int d = lane + 32 * i;
+        if (d < D) acc[i] += e * vr[u][i];
+      }
     }
   }
   float inv = den > 0.f ? vsc / den : 0.f;
